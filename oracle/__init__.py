@@ -1,0 +1,244 @@
+"""CPU oracle for the f32 ``attention`` and ``cache_write`` ops.
+
+TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg are the only callers.  The product path (the
+``f32_gqa_attention_gb300`` package and its CUDA library) never imports this
+module, and this module never imports the product.
+
+The arithmetic lives in ``attention_oracle.c`` (plain C, every sum in double,
+OpenMP over query rows).  This wrapper only resolves the op's parameter
+defaults as the op catalog states them (vtmu.mpakt.dev/api/ops, op
+"attention"):
+
+* ``kvHeads`` defaults to ``heads``;
+* ``vHeadDim`` defaults to ``headDim`` ("value width per head when it
+  differs");
+* ``causal`` defaults to true, ``posOffset`` to 0;
+* ``scale`` replaces 1/sqrt(headDim);
+* ``softcap`` and ``window`` are off when absent (or 0);
+* ALiBi: ``alibiSlopes`` wins over ``alibiMax``, which wins over ``alibi``.
+
+``Oracle(path)`` wraps one compiled build; the module-level functions use the
+default build of ``attention_oracle.c``.  The tests also compile copies with a
+planted mistake and check that the pins catch each one.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+SOURCE = os.path.join(HERE, "attention_oracle.c")
+_LIB = os.path.join(HERE, "liboracle.so")
+
+BIAS_NONE, BIAS_TS, BIAS_HTS = 0, 1, 2
+ALIBI_BLOOM, ALIBI_MPT = 1, 2
+
+_lock = threading.Lock()
+_default = None
+
+
+class _Desc(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64),
+        ("S", ctypes.c_int64),
+        ("heads", ctypes.c_int),
+        ("kv_heads", ctypes.c_int),
+        ("head_dim", ctypes.c_int),
+        ("v_head_dim", ctypes.c_int),
+        ("causal", ctypes.c_int),
+        ("pos_offset", ctypes.c_int64),
+        ("scale", ctypes.c_double),
+        ("softcap", ctypes.c_double),
+        ("window", ctypes.c_int64),
+        ("slopes", ctypes.POINTER(ctypes.c_double)),
+        ("bias_kind", ctypes.c_int),
+    ]
+
+
+def compile_source(src: str, out: str) -> str:
+    """gcc -O2 -fopenmp a C file of the oracle into a shared library."""
+    tmp = out + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
+           "-o", tmp, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, out)
+    return out
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle (no CUDA involved).  Returns the .so path."""
+    with _lock:
+        if (not force and os.path.exists(_LIB)
+                and os.path.getmtime(_LIB) >= os.path.getmtime(SOURCE)):
+            return _LIB
+        return compile_source(SOURCE, _LIB)
+
+
+def _f32(a):
+    return np.ascontiguousarray(np.asarray(a, dtype=np.float32))
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+class Oracle:
+    """One compiled build of the oracle."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        p = ctypes.c_void_p
+        lib.oracle_attention.argtypes = [ctypes.POINTER(_Desc), p, p, p, p, p]
+        lib.oracle_attention_rows.argtypes = [ctypes.POINTER(_Desc), p, p, p,
+                                              p, p, p, ctypes.c_int64, p]
+        lib.oracle_alibi_slopes.argtypes = [ctypes.c_int, ctypes.c_int,
+                                            ctypes.c_double, p]
+        lib.oracle_cache_write.argtypes = [p, ctypes.c_int64, ctypes.c_int64,
+                                           p, ctypes.c_int64, ctypes.c_int64]
+        lib.oracle_num_threads.restype = ctypes.c_int
+        self.lib = lib
+        self.path = path
+
+    def num_threads(self) -> int:
+        return int(self.lib.oracle_num_threads())
+
+    def alibi_slopes(self, heads: int, alibi: bool = False, alibiMax=None,
+                     alibiSlopes=None):
+        """Per-head ALiBi slopes in double, or None when ALiBi is off."""
+        if alibiSlopes is not None:
+            s = np.ascontiguousarray(np.asarray(alibiSlopes, dtype=np.float64))
+            if s.shape != (heads,):
+                raise ValueError("alibiSlopes needs one slope per head")
+            return s
+        if alibiMax is not None:
+            kind, bmax = ALIBI_MPT, float(alibiMax)
+        elif alibi:
+            kind, bmax = ALIBI_BLOOM, 0.0
+        else:
+            return None
+        out = np.zeros(heads, dtype=np.float64)
+        if self.lib.oracle_alibi_slopes(int(heads), kind, bmax, _ptr(out)):
+            raise ValueError("oracle_alibi_slopes failed")
+        return out
+
+    def _prepare(self, q, k, v, bias, heads, headDim, kvHeads, vHeadDim,
+                 causal, posOffset, scale, softcap, window, alibi, alibiMax,
+                 alibiSlopes):
+        q, k, v = _f32(q), _f32(k), _f32(v)
+        kvHeads = heads if kvHeads is None else int(kvHeads)
+        vHeadDim = headDim if vHeadDim is None else int(vHeadDim)
+        if q.ndim != 2 or q.shape[1] != heads * headDim:
+            raise ValueError("q must be [T, heads*headDim]")
+        if k.ndim != 2 or k.shape[1] != kvHeads * headDim:
+            raise ValueError("k must be [S, kvHeads*headDim]")
+        if (v.ndim != 2 or v.shape[1] != kvHeads * vHeadDim
+                or v.shape[0] != k.shape[0]):
+            raise ValueError("v must be [S, kvHeads*vHeadDim]")
+        T, S = q.shape[0], k.shape[0]
+        bias_kind = BIAS_NONE
+        if bias is not None:
+            bias = _f32(bias)
+            if bias.shape == (T, S):
+                bias_kind = BIAS_TS
+            elif bias.shape == (heads, T, S):
+                bias_kind = BIAS_HTS
+            else:
+                raise ValueError("bias must be [T, S] or [heads, T, S]")
+        slopes = self.alibi_slopes(heads, alibi, alibiMax, alibiSlopes)
+        d = _Desc()
+        d.T, d.S = T, S
+        d.heads, d.kv_heads = heads, kvHeads
+        d.head_dim, d.v_head_dim = headDim, vHeadDim
+        d.causal = 1 if causal else 0
+        d.pos_offset = int(posOffset)
+        d.scale = (1.0 / math.sqrt(headDim)) if scale is None else float(scale)
+        d.softcap = 0.0 if softcap is None else float(softcap)
+        d.window = 0 if window is None else int(window)
+        d.slopes = (slopes.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+                    if slopes is not None else None)
+        d.bias_kind = bias_kind
+        return d, (q, k, v, bias, slopes)
+
+    def attention(self, q, k, v, bias=None, *, heads, headDim, kvHeads=None,
+                  vHeadDim=None, causal=True, posOffset=0, scale=None,
+                  softcap=None, window=None, alibi=False, alibiMax=None,
+                  alibiSlopes=None):
+        """The whole op: returns out [T, heads*vHeadDim] as float64."""
+        d, keep = self._prepare(q, k, v, bias, heads, headDim, kvHeads,
+                                vHeadDim, causal, posOffset, scale, softcap,
+                                window, alibi, alibiMax, alibiSlopes)
+        q, k, v, bias, _ = keep
+        out = np.zeros((d.T, d.heads * d.v_head_dim), dtype=np.float64)
+        rc = self.lib.oracle_attention(ctypes.byref(d), _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(bias), _ptr(out))
+        if rc:
+            raise ValueError(f"oracle_attention failed ({rc})")
+        return out
+
+    def attention_rows(self, q, k, v, bias=None, *, rows, heads, headDim,
+                       kvHeads=None, vHeadDim=None, causal=True, posOffset=0,
+                       scale=None, softcap=None, window=None, alibi=False,
+                       alibiMax=None, alibiSlopes=None):
+        """Selected (t, h) rows only: returns [len(rows), vHeadDim] float64."""
+        d, keep = self._prepare(q, k, v, bias, heads, headDim, kvHeads,
+                                vHeadDim, causal, posOffset, scale, softcap,
+                                window, alibi, alibiMax, alibiSlopes)
+        q, k, v, bias, _ = keep
+        rows = list(rows)
+        ts = np.ascontiguousarray([int(t) for t, _ in rows], dtype=np.int64)
+        hs = np.ascontiguousarray([int(h) for _, h in rows], dtype=np.int32)
+        out = np.zeros((len(rows), d.v_head_dim), dtype=np.float64)
+        rc = self.lib.oracle_attention_rows(ctypes.byref(d), _ptr(q), _ptr(k),
+                                            _ptr(v), _ptr(bias), _ptr(ts),
+                                            _ptr(hs), len(rows), _ptr(out))
+        if rc:
+            raise ValueError(f"oracle_attention_rows failed ({rc})")
+        return out
+
+    def cache_write(self, cache, values, offset):
+        """In place on the numpy array ``cache`` [maxRows, width]; returns it."""
+        if not (isinstance(cache, np.ndarray) and cache.dtype == np.float32
+                and cache.flags.c_contiguous and cache.ndim == 2):
+            raise ValueError("cache must be a C-contiguous float32 [maxRows, width]")
+        values = _f32(values)
+        if values.ndim != 2 or values.shape[1] != cache.shape[1]:
+            raise ValueError("values must be [rows, width]")
+        rc = self.lib.oracle_cache_write(_ptr(cache), cache.shape[0],
+                                         cache.shape[1], _ptr(values),
+                                         values.shape[0], int(offset))
+        if rc:
+            raise ValueError("cache_write: rows do not fit the cache at offset")
+        return cache
+
+
+def default() -> Oracle:
+    global _default
+    if _default is None:
+        _default = Oracle(build())
+    return _default
+
+
+def num_threads() -> int:
+    return default().num_threads()
+
+
+def alibi_slopes(heads, alibi=False, alibiMax=None, alibiSlopes=None):
+    return default().alibi_slopes(heads, alibi, alibiMax, alibiSlopes)
+
+
+def attention(q, k, v, bias=None, **params):
+    return default().attention(q, k, v, bias, **params)
+
+
+def attention_rows(q, k, v, bias=None, **params):
+    return default().attention_rows(q, k, v, bias, **params)
+
+
+def cache_write(cache, values, offset):
+    return default().cache_write(cache, values, offset)

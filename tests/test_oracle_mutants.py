@@ -1,0 +1,89 @@
+"""The oracle's pins are strong enough: a copy of the oracle with one plausible
+mistake planted (on the CPU, in a temporary copy of its C source) must fail
+at least one pin.  Each mutation names the statement of the op catalog
+(vtmu.mpakt.dev/api/ops) that it breaks."""
+import os
+import sys
+
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+
+import oracle  # noqa: E402
+import oracle_pins  # noqa: E402
+
+# (name, original text, planted text)
+MUTANTS = [
+    ("kv head by modulo instead of by group (grouped-query mapping)",
+     "const int kh = h / G;", "const int kh = h % a->kv_heads;"),
+    ("causal window boundary inclusive (pos - window < s)",
+     "if (!(p - window < s)) return 0;", "if (!(p - window <= s)) return 0;"),
+    ("non-causal window boundary exclusive (|pos - s| <= window)",
+     "if (dist > window) return 0;", "if (dist >= window) return 0;"),
+    ("causal mask hides the diagonal (s <= pos visible)",
+     "if (causal && s > p) return 0;", "if (causal && s >= p) return 0;"),
+    ("scale dropped (scale replaces 1/sqrt(headDim))",
+     "double xs = a->scale * dot;", "double xs = dot;"),
+    ("ALiBi sign flipped",
+     "xs += a->slopes[h] * (double)(s - p);", "xs += a->slopes[h] * (double)(p - s);"),
+    ("ALiBi dropped",
+     "xs += a->slopes[h] * (double)(s - p);", "xs += 0.0;"),
+    ("per-head bias indexed [T, heads, S]",
+     "bias[((int64_t)h * a->T + t) * a->S + s]", "bias[((int64_t)t * a->heads + h) * a->S + s]"),
+    ("bias dropped",
+     "xs += (double)bias[t * a->S + s];", "xs += 0.0;"),
+    ("softcap applied after the bias (softcap before the mask)", None, None),
+    ("softcap without the cap factor",
+     "xs = a->softcap * tanh(xs / a->softcap);", "xs = tanh(xs / a->softcap);"),
+    ("softmax not max-subtracted",
+     "double w = exp(x[s] - m);", "double w = exp(x[s]);"),
+    ("value rows strided by headDim",
+     "(int64_t)kh * Dv;", "(int64_t)kh * D;"),
+    ("posOffset ignored",
+     "const int64_t p = a->pos_offset + t;", "const int64_t p = t;"),
+    ("no-visible-key row not zeroed",
+     "if (m == -INFINITY) return; /* nothing visible: the row is zero */", ""),
+    ("BLOOM extra slopes on the wrong grid",
+     "out[c + j - 1] = pow(2.0, -4.0 * (2.0 * j - 1.0) / c);",
+     "out[c + j - 1] = pow(2.0, -4.0 * (2.0 * j) / c);"),
+    ("MPT odd slopes before the even ones",
+     "for (int i = 2; i <= n && w < heads; i += 2) out[w++] = a[i - 1];\n"
+     "            for (int i = 1; i <= n && w < heads; i += 2) out[w++] = a[i - 1];",
+     "for (int i = 1; i <= n && w < heads; i += 2) out[w++] = a[i - 1];\n"
+     "            for (int i = 2; i <= n && w < heads; i += 2) out[w++] = a[i - 1];"),
+    ("cache_write copies the first row everywhere",
+     "= values[r * width + c];", "= values[c];"),
+]
+
+
+def _plant_softcap_after_bias(src):
+    """Move the softcap line after the bias lines."""
+    line = "        if (a->softcap > 0.0) xs = a->softcap * tanh(xs / a->softcap);\n"
+    assert line in src
+    src = src.replace(line, "")
+    anchor = "        x[s] = xs;\n"
+    assert anchor in src
+    return src.replace(anchor, line + anchor)
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_planted_mistake(tmp_path, name, old, new):
+    with open(oracle.SOURCE) as f:
+        src = f.read()
+    if old is None:
+        mutated = _plant_softcap_after_bias(src)
+    else:
+        assert src.count(old) == 1, f"mutation anchor not unique: {old!r}"
+        mutated = src.replace(old, new)
+    assert mutated != src
+    c_path = tmp_path / "mutant.c"
+    c_path.write_text(mutated)
+    so = oracle.compile_source(str(c_path), str(tmp_path / "libmutant.so"))
+    orc = oracle.Oracle(so)
+    failed = []
+    for pin in oracle_pins.ALL_PINS:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, FloatingPointError) as e:
+            failed.append((pin.__name__, str(e)[:80]))
+    assert failed, f"no pin caught the planted mistake: {name}"
