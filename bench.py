@@ -1,0 +1,519 @@
+"""Benchmark of the f32 attention library on one GB300 (or N replicas).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vtmu|reference]
+                    [--workload gqa_decode|gqa_prefill|swa_softcap_prefill|
+                                latent_bias_prefill|alibi_prefill|tiny_prefill]
+
+Default workload: the GQA decode step (Llama-3-8B shape): cache_write of one
+new K row and one new V row at position 32767 into [32768, 8*128] f32 caches,
+then attention with T = 1 over S = 32768 keys, 32 query heads, 8 KV heads,
+headDim 128.  A step is that whole decode step.  Two independent caches
+(sessions) alternate between steps, so each step reads its 256 MiB of K/V
+from HBM (working set 512 MiB > the 126 MiB L2).
+
+One JSON line is printed by rank 0.  `value` is whole-job throughput in the
+workload's unit (decode: algorithmic GB/s; prefill: algorithmic TFLOP/s).
+`--impl reference` times the CPU oracle on the host cores instead, on a
+bounded sample of the same workload.
+
+N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
+op has no exchange step); ranks meet at a barrier around the timed region
+and the time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import seeded_inputs as si  # noqa: E402
+
+METRIC = "f32 attention: decode KV GB/s and prefill TFLOP/s on 1 GB300, % of roofline"
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+SMS = 152
+FP32_LANES_PER_SM = 128
+
+
+# ------------------------------------------------------------------ work model
+def decode_bytes(w):
+    """Algorithmic bytes of one decode step: every visible K and V row once,
+    q and out once, and the two one-row cache writes (read + write)."""
+    H, Hk, D = w["heads"], w["kvHeads"], w["headDim"]
+    S = w["offset"] + 1
+    kv = 2 * S * Hk * D * 4
+    qo = 2 * H * D * 4
+    cw = 2 * 2 * Hk * D * 4
+    return kv, kv + qo + cw
+
+
+def visible_pairs(w):
+    """Visible (query, key) pairs per head, from the op's masking rule."""
+    T, S = w["T"], w["S"]
+    p = w["params"]
+    causal = p.get("causal", True)
+    win = p.get("window") or 0
+    pos0 = p.get("posOffset", 0)
+    t = np.arange(T, dtype=np.int64) + pos0
+    if causal:
+        hi = np.minimum(t, S - 1)
+        lo = np.maximum(t - win + 1, 0) if win else np.zeros_like(t)
+    else:
+        lo = np.maximum(t - win, 0) if win else np.zeros_like(t)
+        hi = np.minimum(t + win, S - 1) if win else np.full_like(t, S - 1)
+    return int(np.maximum(hi - lo + 1, 0).sum())
+
+
+def prefill_flops(w):
+    D = w["headDim"]
+    Dv = w.get("vHeadDim") or D
+    return visible_pairs(w) * w["heads"] * (2 * D + 2 * Dv)
+
+
+def load_peaks():
+    try:
+        with open(PEAKS_FILE) as f:
+            pk = json.load(f)
+        return pk, "measured"
+    except (OSError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "sm_max_mhz": 2070.0}, "fallback"
+
+
+def profile_traffic(kernel_tag):
+    """DRAM bytes per launch from a committed ncu summary, when the kernel
+    source it was taken on is unchanged (sha256 recorded in the summary)."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    src = os.path.join(ROOT, "f32_gqa_attention_gb300", "csrc", f"{kernel_tag.split('__')[0]}.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    except OSError:
+        return None
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    if not m or not s or s.group(1) != sha:
+        return None
+    return int(m.group(1))
+
+
+# -------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu=timestamp,{self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for ln in out.splitlines():
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+            except ValueError:
+                continue
+        # samples inside the loaded window (second resolution timestamps)
+        lo, hi = (self.t0 or 0) - 1, (self.t1 or time.time()) + 1
+        sel = [r for r in rows if lo <= r[0] <= hi] or rows[-3:]
+        if not sel:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
+                "reasons": reasons, "samples": len(sel)}
+
+
+# ------------------------------------------------------------------ helpers
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def max_over_ranks(x, world):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- oracle timing
+def oracle_decode_step(x, w):
+    import oracle
+    H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
+    oracle.cache_write(x["kc"], x["k_new"], off)
+    oracle.cache_write(x["vc"], x["v_new"], off)
+    return oracle.attention(x["q"], x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
+
+
+class OracleSampler:
+    """Bounded samples of a workload computed by the oracle as it stands, on
+    all host cores.  decode: one whole decode step per sample; prefill: 16
+    query rows x all heads per sample (rows drawn at random), counted by their
+    visible pairs."""
+
+    ROWS = 16
+
+    def __init__(self, name, w, x=None):
+        import oracle
+        self.oracle = oracle
+        self.name, self.w = name, w
+        self.x = si.workload_inputs(name) if x is None else x
+        self.cores = oracle.num_threads()
+        self.order = np.random.default_rng(0).permutation(w.get("T", 1))
+        self.next_row = 0
+
+    def sample(self):
+        """Runs one sample; returns (work in the unit's numerator, seconds)."""
+        w, x = self.w, self.x
+        t0 = time.perf_counter()
+        if w["kind"] == "decode":
+            oracle_decode_step(x, w)
+            return decode_bytes(w)[1] / 1e9, time.perf_counter() - t0
+        H = w["heads"]
+        D = w["headDim"]
+        Dv = w.get("vHeadDim") or D
+        params = dict(heads=H, headDim=D, kvHeads=w["kvHeads"], vHeadDim=w.get("vHeadDim"), **w["params"])
+        lo_i = self.next_row % w["T"]
+        ts = self.order[lo_i:lo_i + self.ROWS]
+        self.next_row += len(ts)
+        rows = [(int(t), h) for t in ts for h in range(H)]
+        self.oracle.attention_rows(x["q"], x["k"], x["v"], x.get("bias"), rows=rows, **params)
+        dt = time.perf_counter() - t0
+        causal = w["params"].get("causal", True)
+        win = w["params"].get("window") or 0
+        pairs = 0
+        for t in ts:
+            p = int(t) + w["params"].get("posOffset", 0)
+            if causal:
+                lo, hi = (max(p - win + 1, 0) if win else 0), min(p, w["S"] - 1)
+            else:
+                lo, hi = (max(p - win, 0) if win else 0), (min(p + win, w["S"] - 1) if win else w["S"] - 1)
+            pairs += max(hi - lo + 1, 0)
+        return pairs * H * (2 * D + 2 * Dv) / 1e12, dt
+
+    def describe(self, n):
+        if self.w["kind"] == "decode":
+            return f"{n} whole decode steps (cache_write x2 + attention over {self.w['offset'] + 1} keys)"
+        return f"{n} samples of {self.ROWS} random query rows x all {self.w['heads']} heads"
+
+
+def time_oracle(name, w, budget_s=12.0, min_samples=2, x=None):
+    """cpu_baseline: oracle samples for about `budget_s` seconds."""
+    smp = OracleSampler(name, w, x)
+    work = secs = 0.0
+    n = 0
+    while n < min_samples or secs < budget_s:
+        a, b = smp.sample()
+        work += a
+        secs += b
+        n += 1
+    return work / secs, smp.describe(n), smp.cores
+
+
+# ------------------------------------------------------------- the GPU arm
+def run_vtmu(args, rank, world, local):
+    import torch
+    import f32_gqa_attention_gb300 as vtmu
+    vtmu.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    name = args.workload
+    w = si.WORKLOADS[name]
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+    launches_per_step = 0
+    x = si.workload_inputs(name)
+
+    if w["kind"] == "decode":
+        H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
+        kv_bytes, step_bytes = decode_bytes(w)
+        sessions = []
+        with torch.cuda.stream(stream):
+            for sidx in range(2):
+                sessions.append(dict(Kc=torch.from_numpy(x["kc"]).to(dev), Vc=torch.from_numpy(x["vc"]).to(dev)))
+            q = torch.from_numpy(x["q"]).to(dev)
+            kn = torch.from_numpy(x["k_new"]).to(dev)
+            vn = torch.from_numpy(x["v_new"]).to(dev)
+            out = torch.empty((1, H * D), dtype=torch.float32, device=dev)
+        p = vtmu.make_params(1, off + 1, heads=H, headDim=D, kvHeads=Hk, **w["params"])
+        ws_bytes = vtmu.vtmu_attention_workspace_size(p)
+        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+        width = Hk * D
+        launches_per_step = 3
+
+        def step(i, ev=None):
+            s = sessions[i % 2]
+            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kn, 1, off, st)
+            vtmu.vtmu_cache_write(s["Vc"], off + 1, width, vn, 1, off, st)
+            if ev is not None:
+                ev[0].record(stream)
+            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+            if ev is not None:
+                ev[1].record(stream)
+
+        work_per_step, unit = step_bytes / 1e9, "GB/s"
+        kernel_tag, kernel_work, kernel_unit = "decode", kv_bytes + 2 * H * D * 4, "GB/s"
+        bound, peak = "hbm", float(peaks["hbm_gbs"])
+        flush = None
+        l2_note = "inputs > L2: two 256 MiB K/V cache sets alternate between steps"
+    else:
+        H, Hk, D = w["heads"], w["kvHeads"], w["headDim"]
+        Dv = w.get("vHeadDim") or D
+        T, S = w["T"], w["S"]
+        with torch.cuda.stream(stream):
+            q = torch.from_numpy(x["q"]).to(dev)
+            k = torch.from_numpy(x["k"]).to(dev)
+            v = torch.from_numpy(x["v"]).to(dev)
+            b = torch.from_numpy(x["bias"]).to(dev) if "bias" in x else None
+            out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
+            flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        bias_kind = vtmu.VTMU_BIAS_NONE if b is None else (vtmu.VTMU_BIAS_TS if b.dim() == 2 else vtmu.VTMU_BIAS_HTS)
+        p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, vHeadDim=w.get("vHeadDim"),
+                             bias_kind=bias_kind, **w["params"])
+        launches_per_step = 1
+
+        def step(i, ev=None):
+            if ev is not None:
+                ev[0].record(stream)
+            vtmu.vtmu_attention(q, k, v, b, out, p, None, 0, st)
+            if ev is not None:
+                ev[1].record(stream)
+
+        flops = prefill_flops(w)
+        work_per_step, unit = flops / 1e12, "TFLOP/s"
+        kernel_tag, kernel_work, kernel_unit = "prefill_ffma", flops / 1e12, "TFLOP/s"
+        clk = float(peaks.get("sm_max_mhz", 2070.0))
+        bound, peak = "alu", SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+        l2_note = "L2 flushed between timed steps (256 MiB write, outside the timed events)"
+
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.6)
+    sampler.mark_start()
+    for i in range(args.warmup):
+        step(i)
+        if flush is not None:
+            flush.zero_()
+    torch.cuda.synchronize(dev)
+
+    # ---- timed region: device time per step and per dominant kernel ----------
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    for i in range(args.steps):
+        sev[i][0].record(stream)
+        step(i, kev[i])
+        sev[i][1].record(stream)
+        if flush is not None:
+            with torch.cuda.stream(stream):
+                flush.zero_()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    sampler.mark_end()
+    step_ms = sum(a.elapsed_time(b) for a, b in sev) / args.steps
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
+    step_ms = max_over_ranks(step_ms, world)
+
+    # ---- end to end through the public API with host buffers ----------------
+    e2e = None
+    if w["kind"] == "decode":
+        qh = torch.from_numpy(x["q"]).pin_memory()
+        knh = torch.from_numpy(x["k_new"]).pin_memory()
+        vnh = torch.from_numpy(x["v_new"]).pin_memory()
+        outh = torch.empty((1, H * D), dtype=torch.float32).pin_memory()
+
+        def e2e_step(i):
+            s = sessions[i % 2]
+            with torch.cuda.stream(stream):
+                q.copy_(qh, non_blocking=True)
+                kn.copy_(knh, non_blocking=True)
+                vn.copy_(vnh, non_blocking=True)
+            vtmu.vtmu_cache_write(s["Kc"], off + 1, Hk * D, kn, 1, off, st)
+            vtmu.vtmu_cache_write(s["Vc"], off + 1, Hk * D, vn, 1, off, st)
+            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+            with torch.cuda.stream(stream):
+                outh.copy_(out, non_blocking=True)
+            stream.synchronize()  # the step's output is on the host before the next step
+
+        h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
+        d2h = outh.numel() * 4
+    else:
+        qh = torch.from_numpy(x["q"]).pin_memory()
+        kh_ = torch.from_numpy(x["k"]).pin_memory()
+        vh = torch.from_numpy(x["v"]).pin_memory()
+        bh = torch.from_numpy(x["bias"]).pin_memory() if "bias" in x else None
+        outh = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+
+        def e2e_step(i):
+            with torch.cuda.stream(stream):
+                q.copy_(qh, non_blocking=True)
+                k.copy_(kh_, non_blocking=True)
+                v.copy_(vh, non_blocking=True)
+                if bh is not None:
+                    b.copy_(bh, non_blocking=True)
+            vtmu.vtmu_attention(q, k, v, b, out, p, None, 0, st)
+            with torch.cuda.stream(stream):
+                outh.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        h2d = (qh.numel() + kh_.numel() + vh.numel() + (bh.numel() if bh is not None else 0)) * 4
+        d2h = outh.numel() * 4
+    e2e_step(0)
+    n_e2e = max(3, min(args.steps, 200))
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
+    e2e = {"value": round(work_per_step * world / e2e_s, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "steps": n_e2e}
+
+    clocks = sampler.stop() if rank == 0 else None
+
+    achieved = kernel_work / (kern_ms / 1e3) / (1e9 if kernel_unit == "GB/s" else 1.0)
+    if kernel_unit == "GB/s":
+        achieved = kernel_work / (kern_ms / 1e3) / 1e9
+    else:
+        achieved = kernel_work / (kern_ms / 1e3)
+    traffic = profile_traffic(kernel_tag + "__" + name)
+    roofline = {"bound": bound, "kernel": kernel_tag, "achieved": round(achieved, 3), "peak": round(peak, 1),
+                "peak_source": peak_kind if bound != "alu" else "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                "unit": kernel_unit, "frac": round(achieved / peak, 4), "traffic": traffic,
+                "kernel_ms": round(kern_ms, 5)}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        val, sample, cores = time_oracle(name, w, budget_s=args.cpu_budget, x=x)
+        cpu = {"value": round(val, 4), "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
+
+    line = {
+        "metric": METRIC, "value": round(work_per_step * world / (step_ms / 1e3), 3), "unit": unit,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller, N(0,1) inputs of the workload's shapes)",
+        "config": {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
+                   "parallelism": f"replicas x{world}", "l2": l2_note},
+        "impl": "vtmu", "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank, world):
+    """The oracle on the host cores: W untimed samples, then K timed ones."""
+    if rank != 0:
+        return
+    name = args.workload
+    w = si.WORKLOADS[name]
+    unit = "GB/s" if w["kind"] == "decode" else "TFLOP/s"
+    smp = OracleSampler(name, w)
+    for _ in range(args.warmup):
+        smp.sample()
+    work = secs = 0.0
+    for _ in range(args.steps):
+        a, b = smp.sample()
+        work += a
+        secs += b
+    value = work / secs
+    line = {
+        "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded SplitMix64 / Box-Muller, N(0,1) inputs of the workload's shapes)",
+        "config": {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
+                   "parallelism": "host cores"},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 4), "unit": unit, "kind": "oracle", "cores": smp.cores,
+                         "sample": smp.describe(args.steps)},
+        "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["vtmu", "reference"], default="vtmu")
+    ap.add_argument("--workload", choices=sorted(si.WORKLOADS), default="gqa_decode")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_env()
+    if world != args.gpus and "RANK" in os.environ:
+        ap.error(f"--gpus {args.gpus} but WORLD_SIZE {world}")
+    if world > 1:
+        import torch.distributed as dist
+        backend = "gloo" if args.impl == "reference" else "nccl"
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_vtmu(args, rank, world, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,243 @@
+"""Python binding of the GB300 f32 attention library (``libvtmu.so``).
+
+Argument marshalling only: every step of the ops runs in the library's CUDA
+kernels.  The binding exposes the C ABI of ``include/vtmu_attention.h`` under
+the same names (``vtmu_attention``, ``vtmu_cache_write``, ...) plus two
+conveniences for PyTorch CUDA tensors, ``attention`` and ``cache_write``,
+whose keyword names follow the op catalog (vtmu.mpakt.dev/api/ops, ops
+"attention" and "cache_write").  PyTorch only provides device memory and
+streams.
+
+There is no fallback: if ``libvtmu.so`` is not built, loading raises.
+Build it with ``python -m f32_gqa_attention_gb300._build``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libvtmu.so")
+
+VTMU_OK = 0
+VTMU_ERR_INVALID = 1
+VTMU_ERR_UNSUPPORTED = 2
+VTMU_ERR_RANGE = 3
+VTMU_ERR_WORKSPACE = 4
+VTMU_ERR_CUDA = 5
+
+VTMU_ALIBI_NONE, VTMU_ALIBI_BLOOM, VTMU_ALIBI_MPT, VTMU_ALIBI_SLOPES = 0, 1, 2, 3
+VTMU_BIAS_NONE, VTMU_BIAS_TS, VTMU_BIAS_HTS = 0, 1, 2
+VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREFILL_TF32X3 = 0, 1, 2, 3
+
+EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
+            "vtmu_cache_write", "vtmu_features", "vtmu_last_error")
+
+
+class VtmuError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"vtmu status {status}: {message}")
+        self.status = status
+
+
+class vtmu_attention_params(ctypes.Structure):
+    """Mirror of ``vtmu_attention_params`` (include/vtmu_attention.h)."""
+    _fields_ = [
+        ("T", ctypes.c_int64),
+        ("S", ctypes.c_int64),
+        ("heads", ctypes.c_int32),
+        ("kv_heads", ctypes.c_int32),
+        ("head_dim", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("has_scale", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("softcap", ctypes.c_float),
+        ("pos_offset", ctypes.c_int64),
+        ("window", ctypes.c_int64),
+        ("alibi", ctypes.c_int32),
+        ("alibi_max", ctypes.c_float),
+        ("alibi_slopes", ctypes.POINTER(ctypes.c_float)),
+        ("bias_kind", ctypes.c_int32),
+        ("kernel", ctypes.c_int32),
+        ("decode_splits", ctypes.c_int32),
+    ]
+
+
+_lib = None
+_lib_lock = threading.Lock()
+
+
+def load_library():
+    """Load libvtmu.so (raises if it has not been built)."""
+    global _lib
+    with _lib_lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is not built; run `python -m f32_gqa_attention_gb300._build`")
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.POINTER(vtmu_attention_params)
+        vp = ctypes.c_void_p
+        lib.vtmu_attention_params_init.argtypes = [P]
+        lib.vtmu_attention_params_init.restype = None
+        lib.vtmu_attention_workspace_size.argtypes = [P, ctypes.POINTER(ctypes.c_size_t)]
+        lib.vtmu_attention_workspace_size.restype = ctypes.c_int
+        lib.vtmu_attention.argtypes = [vp, vp, vp, vp, vp, P, vp, ctypes.c_size_t, vp]
+        lib.vtmu_attention.restype = ctypes.c_int
+        lib.vtmu_cache_write.argtypes = [vp, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64,
+                                         ctypes.c_int64, vp]
+        lib.vtmu_cache_write.restype = ctypes.c_int
+        lib.vtmu_features.argtypes = []
+        lib.vtmu_features.restype = ctypes.c_char_p
+        lib.vtmu_last_error.argtypes = []
+        lib.vtmu_last_error.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(status: int):
+    if status != VTMU_OK:
+        raise VtmuError(status, load_library().vtmu_last_error().decode())
+
+
+def _addr(x):
+    """Device address of a torch tensor, or an int address, or None."""
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+# ---------------------------------------------------------------- C ABI names
+def vtmu_attention_params_init() -> vtmu_attention_params:
+    p = vtmu_attention_params()
+    load_library().vtmu_attention_params_init(ctypes.byref(p))
+    return p
+
+
+def vtmu_attention_workspace_size(p: vtmu_attention_params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().vtmu_attention_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
+def vtmu_attention(q, k, v, bias, out, p: vtmu_attention_params, workspace, workspace_bytes: int,
+                   stream: int = 0) -> None:
+    _check(load_library().vtmu_attention(_addr(q), _addr(k), _addr(v), _addr(bias), _addr(out),
+                                         ctypes.byref(p), _addr(workspace), int(workspace_bytes),
+                                         stream or None))
+
+
+def vtmu_cache_write(cache, max_rows: int, width: int, values, rows: int, offset: int, stream: int = 0) -> None:
+    _check(load_library().vtmu_cache_write(_addr(cache), int(max_rows), int(width), _addr(values),
+                                           int(rows), int(offset), stream or None))
+
+
+def vtmu_features() -> str:
+    return load_library().vtmu_features().decode()
+
+
+def vtmu_last_error() -> str:
+    return load_library().vtmu_last_error().decode()
+
+
+# ------------------------------------------------------------ torch helpers
+def make_params(T, S, *, heads, headDim, kvHeads=None, vHeadDim=None, causal=True, posOffset=0,
+                scale=None, softcap=None, window=None, alibi=False, alibiMax=None, alibiSlopes=None,
+                bias_kind=VTMU_BIAS_NONE, kernel=VTMU_KERNEL_AUTO, decode_splits=0):
+    """A params struct from the op catalog's parameter names.  ALiBi
+    precedence: alibiSlopes, then alibiMax, then alibi.  The returned struct
+    keeps any slope array alive as ``_slopes``."""
+    p = vtmu_attention_params_init()
+    p.T, p.S = int(T), int(S)
+    p.heads = int(heads)
+    p.kv_heads = 0 if kvHeads is None else int(kvHeads)
+    p.head_dim = int(headDim)
+    p.v_head_dim = 0 if vHeadDim is None else int(vHeadDim)
+    p.causal = 1 if causal else 0
+    p.pos_offset = int(posOffset)
+    if scale is not None:
+        p.has_scale, p.scale = 1, float(scale)
+    p.softcap = 0.0 if softcap is None else float(softcap)
+    p.window = 0 if window is None else int(window)
+    if alibiSlopes is not None:
+        arr = (ctypes.c_float * len(alibiSlopes))(*[float(s) for s in alibiSlopes])
+        p.alibi, p.alibi_slopes = VTMU_ALIBI_SLOPES, ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+        p._slopes = arr
+    elif alibiMax is not None:
+        p.alibi, p.alibi_max = VTMU_ALIBI_MPT, float(alibiMax)
+    elif alibi:
+        p.alibi = VTMU_ALIBI_BLOOM
+    p.bias_kind = int(bias_kind)
+    p.kernel = int(kernel)
+    p.decode_splits = int(decode_splits)
+    return p
+
+
+class Workspace:
+    """A zero-initialised device scratch buffer (torch-allocated) that grows
+    on demand.  One per concurrent stream."""
+
+    def __init__(self, device=None):
+        import torch
+        self.device = torch.device("cuda") if device is None else torch.device(device)
+        self.buf = None
+
+    def get(self, nbytes: int):
+        import torch
+        if nbytes == 0:
+            return None, 0
+        if self.buf is None or self.buf.numel() < nbytes:
+            self.buf = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+        return self.buf, self.buf.numel()
+
+
+_ws = {}
+
+
+def _default_workspace(device):
+    key = (device.type, device.index)
+    if key not in _ws:
+        _ws[key] = Workspace(device)
+    return _ws[key]
+
+
+def attention(q, k, v, bias=None, *, heads, headDim, out=None, workspace=None, stream=None, **params):
+    """op "attention" on CUDA tensors: q [T, heads*headDim], k [S, kvHeads*headDim],
+    v [S, kvHeads*vHeadDim], optional bias [T, S] or [heads, T, S]; returns
+    out [T, heads*vHeadDim] (float32).  Keyword names as in the op catalog."""
+    import torch
+    T, S = q.shape[0], k.shape[0]
+    vhd = params.get("vHeadDim") or headDim
+    bias_kind = VTMU_BIAS_NONE
+    if bias is not None:
+        bias_kind = VTMU_BIAS_TS if bias.dim() == 2 else VTMU_BIAS_HTS
+    p = make_params(T, S, heads=heads, headDim=headDim, bias_kind=bias_kind, **params)
+    for name, t in (("q", q), ("k", k), ("v", v), ("bias", bias)):
+        if t is not None and (not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty((T, heads * vhd), dtype=torch.float32, device=q.device)
+    nbytes = vtmu_attention_workspace_size(p)
+    ws = workspace if workspace is not None else _default_workspace(q.device)
+    buf, cap = ws.get(nbytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    vtmu_attention(q, k, v, bias, out, p, buf, cap, st)
+    return out
+
+
+def cache_write(cache, values, offset: int, stream=None):
+    """op "cache_write" on CUDA tensors: cache [maxRows, width] is updated in
+    place with values [rows, width] at row ``offset``; returns cache."""
+    import torch
+    for name, t in (("cache", cache), ("values", values)):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous() or t.dim() != 2:
+            raise ValueError(f"{name} must be a contiguous 2-D float32 CUDA tensor")
+    if values.shape[1] != cache.shape[1]:
+        raise ValueError("values must be as wide as the cache")
+    st = stream if stream is not None else torch.cuda.current_stream(cache.device).cuda_stream
+    vtmu_cache_write(cache, cache.shape[0], cache.shape[1], values, values.shape[0], offset, st)
+    return cache

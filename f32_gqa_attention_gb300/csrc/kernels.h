@@ -1,0 +1,38 @@
+// kernels.h -- host-side launch interface of the kernels (library-internal).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "attn_desc.h"
+
+namespace vtmu {
+
+// ---- split-KV decode (T == 1) ---------------------------------------------
+struct DecodePlan {
+    int64_t s_lo = 0;            // first visible key
+    int64_t s_end = 0;           // one past the last visible key
+    int64_t rows_per_split = 0;  // multiple of the kernel's stage rows
+    int32_t splits = 1;          // per KV head
+    size_t workspace_bytes = 0;
+};
+
+// True when the decode kernel's shape table covers this call (T == 1,
+// headDim == vHeadDim in {32, 64, 128}, group size in {2, 4, 8}, 16-byte
+// aligned rows).  Pointer alignment is checked separately at launch.
+bool decode_supported(const AttnDesc& a);
+// Fills `plan` for the call; `forced_splits` > 0 overrides the heuristic.
+void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan);
+cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
+                          void* workspace, cudaStream_t stream);
+
+// ---- tiled prefill on FP32 FMA ----------------------------------------------
+bool prefill_ffma_supported(const AttnDesc& a);
+cudaError_t launch_prefill_ffma(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream);
+
+// ---- cache_write --------------------------------------------------------------
+cudaError_t launch_cache_write(float* cache, int64_t width, const float* values, int64_t rows,
+                               int64_t offset, cudaStream_t stream);
+
+}  // namespace vtmu

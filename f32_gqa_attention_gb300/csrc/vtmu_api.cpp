@@ -1,0 +1,306 @@
+// vtmu_api.cpp -- the C ABI (include/vtmu_attention.h): parameter checks,
+// the op's defaults, ALiBi slope tables, kernel choice and launch.
+//
+// Defaults and parameter meanings follow op "attention" of the op catalog
+// (vtmu.mpakt.dev/api/ops): kvHeads defaults to heads, vHeadDim to headDim,
+// causal to true, scale to 1/sqrt(headDim); softcap and window are off when
+// absent.  A request the build cannot serve is refused with the parameter or
+// feature named, as the catalog refuses a graph "with the feature named".
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cuda_runtime.h>
+
+#include "kernels.h"
+#include "vtmu_attention.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+vtmu_status fail(vtmu_status st, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    std::vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+vtmu_status ok() {
+    g_last_error.clear();
+    return VTMU_OK;
+}
+
+vtmu_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(VTMU_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+// BLOOM slopes: c = largest power of two <= heads; the first c heads take
+// powers 1..c of 2^(-8/c), the rest take the odd powers 1, 3, 5, ... of
+// 2^(-4/c).
+void bloom_slopes(int heads, double* out) {
+    int c = 1;
+    while (2 * c <= heads) c *= 2;
+    const double base = std::exp2(-8.0 / c);
+    double acc = 1.0;
+    for (int i = 0; i < c; ++i) {
+        acc *= base;
+        out[i] = acc;
+    }
+    const double base2 = std::exp2(-4.0 / c);
+    for (int j = 0; j < heads - c; ++j) out[c + j] = std::pow(base2, 2 * j + 1);
+}
+
+// MPT slopes with alibi_bias_max b: n = smallest power of two >= heads,
+// s_i = 2^(-(i+1) b / n); when n != heads take s_1, s_3, ... (even
+// exponents first) then s_0, s_2, ..., cut to heads.
+void mpt_slopes(int heads, double bmax, double* out) {
+    int n = 1;
+    while (n < heads) n *= 2;
+    int w = 0;
+    if (n == heads) {
+        for (int i = 0; i < n; ++i) out[i] = std::exp2(-(i + 1) * bmax / n);
+        return;
+    }
+    for (int i = 1; i < n && w < heads; i += 2) out[w++] = std::exp2(-(i + 1) * bmax / n);
+    for (int i = 0; i < n && w < heads; i += 2) out[w++] = std::exp2(-(i + 1) * bmax / n);
+}
+
+int device_sm_count() {
+    static std::mutex mu;
+    static int cached[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+    std::lock_guard<std::mutex> lock(mu);
+    if (cached[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 152;
+        cached[dev] = n;
+    }
+    return cached[dev];
+}
+
+struct Resolved {
+    vtmu::AttnDesc a;
+    int kernel;  // resolved vtmu_kernel (never AUTO)
+};
+
+// Checks that need no pointer, resolves defaults.  Fills r.a except pointers.
+vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
+    if (!p) return fail(VTMU_ERR_INVALID, "params is NULL");
+    vtmu::AttnDesc& a = r->a;
+    std::memset(&a, 0, sizeof(a));
+    if (p->T < 0) return fail(VTMU_ERR_INVALID, "T must be >= 0 (got %lld)", (long long)p->T);
+    if (p->S < 0) return fail(VTMU_ERR_INVALID, "S must be >= 0 (got %lld)", (long long)p->S);
+    if (p->heads <= 0) return fail(VTMU_ERR_INVALID, "heads must be > 0 (got %d)", p->heads);
+    const int Hk = p->kv_heads == 0 ? p->heads : p->kv_heads;
+    if (Hk <= 0) return fail(VTMU_ERR_INVALID, "kvHeads must be > 0 (got %d)", p->kv_heads);
+    if (p->heads % Hk != 0)
+        return fail(VTMU_ERR_INVALID, "heads (%d) must be a multiple of kvHeads (%d)", p->heads, Hk);
+    if (p->head_dim <= 0) return fail(VTMU_ERR_INVALID, "headDim must be > 0 (got %d)", p->head_dim);
+    const int Dv = p->v_head_dim == 0 ? p->head_dim : p->v_head_dim;
+    if (Dv <= 0) return fail(VTMU_ERR_INVALID, "vHeadDim must be > 0 (got %d)", p->v_head_dim);
+    if (p->head_dim > 256) return fail(VTMU_ERR_UNSUPPORTED, "headDim %d > 256 is not supported", p->head_dim);
+    if (Dv > 256) return fail(VTMU_ERR_UNSUPPORTED, "vHeadDim %d > 256 is not supported", Dv);
+    if (p->pos_offset < 0) return fail(VTMU_ERR_RANGE, "posOffset must be >= 0 (got %lld)", (long long)p->pos_offset);
+    if (p->window < 0) return fail(VTMU_ERR_INVALID, "window must be >= 0 (got %lld)", (long long)p->window);
+    if (!(p->softcap >= 0.f) || !std::isfinite(p->softcap))
+        return fail(VTMU_ERR_INVALID, "softcap must be finite and >= 0");
+    if (p->has_scale && !std::isfinite(p->scale)) return fail(VTMU_ERR_INVALID, "scale must be finite");
+    if (p->bias_kind < VTMU_BIAS_NONE || p->bias_kind > VTMU_BIAS_HTS)
+        return fail(VTMU_ERR_INVALID, "bias_kind %d is not a vtmu_bias_kind", p->bias_kind);
+    if (p->alibi < VTMU_ALIBI_NONE || p->alibi > VTMU_ALIBI_SLOPES)
+        return fail(VTMU_ERR_INVALID, "alibi %d is not a vtmu_alibi_kind", p->alibi);
+    if (p->alibi == VTMU_ALIBI_SLOPES && !p->alibi_slopes)
+        return fail(VTMU_ERR_INVALID, "alibiSlopes: slopes pointer is NULL");
+    if (p->alibi == VTMU_ALIBI_MPT && !(p->alibi_max > 0.f && std::isfinite(p->alibi_max)))
+        return fail(VTMU_ERR_INVALID, "alibiMax must be finite and > 0");
+    if (p->alibi != VTMU_ALIBI_NONE && p->heads > vtmu::kMaxAlibiHeads)
+        return fail(VTMU_ERR_UNSUPPORTED, "attention.alibi with heads %d > %d is not supported", p->heads,
+                    vtmu::kMaxAlibiHeads);
+    if (p->kernel < VTMU_KERNEL_AUTO || p->kernel > VTMU_KERNEL_PREFILL_TF32X3)
+        return fail(VTMU_ERR_INVALID, "kernel %d is not a vtmu_kernel", p->kernel);
+    if (p->decode_splits < 0) return fail(VTMU_ERR_INVALID, "decode_splits must be >= 0");
+    if (p->heads > 65535 || Hk > 65535) return fail(VTMU_ERR_UNSUPPORTED, "more than 65535 heads");
+
+    a.T = p->T;
+    a.S = p->S;
+    a.H = p->heads;
+    a.Hk = Hk;
+    a.G = p->heads / Hk;
+    a.D = p->head_dim;
+    a.Dv = Dv;
+    a.causal = p->causal ? 1 : 0;
+    a.pos_offset = p->pos_offset;
+    a.window = p->window;
+    a.bias_kind = p->bias_kind;
+    const double scale = p->has_scale ? (double)p->scale : 1.0 / std::sqrt((double)p->head_dim);
+    if (p->softcap > 0.f) {
+        a.softcap_on = 1;
+        a.qk_mul = (float)(scale / (double)p->softcap);
+        a.cap_log2 = (float)((double)p->softcap * 1.4426950408889634);
+    } else {
+        a.softcap_on = 0;
+        a.qk_mul = (float)(scale * 1.4426950408889634);
+        a.cap_log2 = 0.f;
+    }
+    a.alibi_on = p->alibi != VTMU_ALIBI_NONE;
+
+    int kernel = p->kernel;
+    if (kernel == VTMU_KERNEL_AUTO) {
+        kernel = (a.T == 1 && vtmu::decode_supported(a)) ? VTMU_KERNEL_DECODE : VTMU_KERNEL_PREFILL_FFMA;
+    } else if (kernel == VTMU_KERNEL_DECODE) {
+        if (a.T != 1) return fail(VTMU_ERR_INVALID, "kernel DECODE needs T == 1 (got %lld)", (long long)a.T);
+        if (!vtmu::decode_supported(a))
+            return fail(VTMU_ERR_UNSUPPORTED,
+                        "kernel DECODE covers headDim == vHeadDim in {32,64,128} and group size "
+                        "heads/kvHeads in {2,4,8} (got headDim %d, vHeadDim %d, group %d)",
+                        a.D, a.Dv, a.G);
+    } else if (kernel == VTMU_KERNEL_PREFILL_TF32X3) {
+        return fail(VTMU_ERR_UNSUPPORTED, "kernel PREFILL_TF32X3 is not available in this build");
+    }
+    r->kernel = kernel;
+    return VTMU_OK;
+}
+
+void fill_alibi(const vtmu_attention_params* p, vtmu::AlibiTable* t) {
+    if (p->alibi == VTMU_ALIBI_NONE) return;
+    double s[vtmu::kMaxAlibiHeads];
+    if (p->alibi == VTMU_ALIBI_BLOOM)
+        bloom_slopes(p->heads, s);
+    else if (p->alibi == VTMU_ALIBI_MPT)
+        mpt_slopes(p->heads, (double)p->alibi_max, s);
+    else
+        for (int h = 0; h < p->heads; ++h) s[h] = (double)p->alibi_slopes[h];
+    for (int h = 0; h < p->heads; ++h) t->slope_log2[h] = (float)(s[h] * 1.4426950408889634);
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    if (!a || !b || na == 0 || nb == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+    return a0 < b0 + nb && b0 < a0 + na;
+}
+
+size_t decode_workspace(const vtmu::AttnDesc& a) {
+    vtmu::DecodePlan plan;
+    vtmu::decode_plan(a, 256, 1, &plan);  // upper bound: the most splits
+    return plan.workspace_bytes;
+}
+
+}  // namespace
+
+extern "C" {
+
+void vtmu_attention_params_init(vtmu_attention_params* p) {
+    if (!p) return;
+    std::memset(p, 0, sizeof(*p));
+    p->causal = 1;
+}
+
+vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t* bytes) {
+    if (!bytes) return fail(VTMU_ERR_INVALID, "bytes is NULL");
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    *bytes = (r.kernel == VTMU_KERNEL_DECODE) ? decode_workspace(r.a) : 0;
+    return ok();
+}
+
+vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const float* bias, float* out,
+                           const vtmu_attention_params* p, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    vtmu::AttnDesc& a = r.a;
+    if (a.T == 0) return ok();
+    if (!q) return fail(VTMU_ERR_INVALID, "q is NULL");
+    if (!out) return fail(VTMU_ERR_INVALID, "out is NULL");
+    if (a.S > 0 && (!k || !v)) return fail(VTMU_ERR_INVALID, "k or v is NULL");
+    if ((p->bias_kind != VTMU_BIAS_NONE) != (bias != nullptr))
+        return fail(VTMU_ERR_INVALID, "attention.bias: bias pointer and bias_kind disagree");
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+                          reinterpret_cast<uintptr_t>(bias);
+    if (mis & 3u) return fail(VTMU_ERR_INVALID, "tensor pointers must be 4-byte aligned");
+    const size_t out_b = (size_t)a.T * a.H * a.Dv * 4;
+    const size_t q_b = (size_t)a.T * a.H * a.D * 4, k_b = (size_t)a.S * a.Hk * a.D * 4,
+                 v_b = (size_t)a.S * a.Hk * a.Dv * 4;
+    const size_t b_b = p->bias_kind == VTMU_BIAS_TS    ? (size_t)a.T * a.S * 4
+                       : p->bias_kind == VTMU_BIAS_HTS ? (size_t)a.H * a.T * a.S * 4
+                                                       : 0;
+    if (overlaps(out, out_b, q, q_b) || overlaps(out, out_b, k, k_b) || overlaps(out, out_b, v, v_b) ||
+        overlaps(out, out_b, bias, b_b))
+        return fail(VTMU_ERR_INVALID, "out overlaps an input");
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.bias = bias;
+    a.out = out;
+
+    vtmu::AlibiTable alibi;
+    fill_alibi(p, &alibi);
+
+    cudaError_t e;
+    if (r.kernel == VTMU_KERNEL_DECODE) {
+        const uintptr_t m16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                              reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+        if (m16 & 15u) {
+            if (p->kernel == VTMU_KERNEL_DECODE)
+                return fail(VTMU_ERR_UNSUPPORTED, "kernel DECODE needs 16-byte aligned q, k, v, out");
+            r.kernel = VTMU_KERNEL_PREFILL_FFMA;
+        }
+    }
+    if (r.kernel == VTMU_KERNEL_DECODE) {
+        const size_t need = decode_workspace(a);
+        if (!workspace || workspace_bytes < need)
+            return fail(VTMU_ERR_WORKSPACE, "decode needs a zero-initialised workspace of %zu bytes (got %zu)",
+                        need, workspace ? workspace_bytes : (size_t)0);
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        vtmu::DecodePlan plan;
+        vtmu::decode_plan(a, p->decode_splits, device_sm_count(), &plan);
+        e = vtmu::launch_decode(a, alibi, plan, workspace, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+        return ok();
+    }
+    if (!vtmu::prefill_ffma_supported(a)) return fail(VTMU_ERR_UNSUPPORTED, "shape not covered by the prefill kernel");
+    e = vtmu::launch_prefill_ffma(a, alibi, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
+    return ok();
+}
+
+vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width, const float* values, int64_t rows,
+                             int64_t offset, cudaStream_t stream) {
+    if (max_rows < 0 || width < 0 || rows < 0)
+        return fail(VTMU_ERR_INVALID, "cache_write: negative size (max_rows %lld, width %lld, rows %lld)",
+                    (long long)max_rows, (long long)width, (long long)rows);
+    if (offset < 0 || offset > max_rows || rows > max_rows - offset)
+        return fail(VTMU_ERR_RANGE, "cache_write: offset %lld + rows %lld exceeds maxRows %lld", (long long)offset,
+                    (long long)rows, (long long)max_rows);
+    if (rows == 0 || width == 0) return ok();
+    if (!cache || !values) return fail(VTMU_ERR_INVALID, "cache_write: cache or values is NULL");
+    if ((reinterpret_cast<uintptr_t>(cache) | reinterpret_cast<uintptr_t>(values)) & 3u)
+        return fail(VTMU_ERR_INVALID, "cache_write: pointers must be 4-byte aligned");
+    if (overlaps(cache + offset * width, (size_t)(rows * width) * 4, values, (size_t)(rows * width) * 4))
+        return fail(VTMU_ERR_INVALID, "cache_write: values overlap the destination rows");
+    cudaError_t e = vtmu::launch_cache_write(cache, width, values, rows, offset, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cache_write launch");
+    return ok();
+}
+
+const char* vtmu_features(void) {
+    return "attention.alibi attention.bias attention.scale attention.softcap attention.window";
+}
+
+const char* vtmu_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

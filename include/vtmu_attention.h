@@ -1,0 +1,177 @@
+/*
+ * vtmu_attention.h -- C ABI of the GB300 (sm_103a) f32 attention library.
+ *
+ * Two ops of the volunteer-inference op catalog (vtmu.mpakt.dev/api/ops):
+ *
+ *   attention    op "attention": scaled dot-product attention with
+ *                grouped-query heads on flat row-major f32 tensors
+ *                  q    [T, heads*headDim]
+ *                  k    [S, kvHeads*headDim]
+ *                  v    [S, kvHeads*vHeadDim]
+ *                  bias [T, S] or [heads, T, S]   (optional, additive)
+ *                  out  [T, heads*vHeadDim]
+ *                Query head h reads KV head h / (heads/kvHeads).  Query row
+ *                t sits at absolute position p = posOffset + t and key row s
+ *                at position s.  For each visible key (see `window` and
+ *                `causal` below) the score is
+ *                  x = scale * q.k ; x = softcap*tanh(x/softcap) (if set) ;
+ *                  x += slope_h * (s - p) (ALiBi) ; x += bias ;
+ *                and the output row is the max-subtracted softmax of the
+ *                scores applied to the value rows.  A row with no visible key
+ *                (or only keys whose score is -inf) is written as zeros.
+ *                The score matrix never leaves the chip.
+ *   cache_write  op "cache_write": cache[offset + r, :] = values[r, :] for
+ *                r < rows, in place (the op mutates its first input).
+ *
+ * Conventions shared by every entry point
+ *  - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations)
+ *    owned by the caller; the library never allocates, frees or
+ *    synchronises.  Work is enqueued on `stream` and the call returns at
+ *    once.  Results are visible once the stream reaches that point.
+ *  - Host pointers are marked HOST and are read during the call only.
+ *  - Every check runs on the host before any launch.  A failed check
+ *    launches nothing and returns a status; vtmu_last_error() then names the
+ *    offending parameter or feature (the catalog refuses a graph "with the
+ *    feature named").
+ *  - A CUDA launch error returns VTMU_ERR_CUDA with the CUDA error string.
+ */
+#ifndef VTMU_ATTENTION_H
+#define VTMU_ATTENTION_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VTMU_API __attribute__((visibility("default")))
+#else
+#define VTMU_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* cudaStream_t;
+
+typedef enum vtmu_status {
+    VTMU_OK = 0,
+    VTMU_ERR_INVALID = 1,     /* null pointer, bad shape or parameter */
+    VTMU_ERR_UNSUPPORTED = 2, /* a valid request this build does not serve */
+    VTMU_ERR_RANGE = 3,       /* an offset or position outside its range */
+    VTMU_ERR_WORKSPACE = 4,   /* workspace missing or smaller than required */
+    VTMU_ERR_CUDA = 5         /* a CUDA runtime error at launch */
+} vtmu_status;
+
+/* ALiBi slope source (op "attention" params alibi / alibiMax / alibiSlopes). */
+typedef enum vtmu_alibi_kind {
+    VTMU_ALIBI_NONE = 0,
+    VTMU_ALIBI_BLOOM = 1,  /* alibi: true -> BLOOM geometric slopes */
+    VTMU_ALIBI_MPT = 2,    /* alibiMax: b -> MPT slopes with alibi_bias_max b */
+    VTMU_ALIBI_SLOPES = 3  /* alibiSlopes: explicit per-head slopes (HOST) */
+} vtmu_alibi_kind;
+
+/* Shape of the optional fourth input of op "attention". */
+typedef enum vtmu_bias_kind {
+    VTMU_BIAS_NONE = 0,
+    VTMU_BIAS_TS = 1,  /* bias [T, S], shared by every head */
+    VTMU_BIAS_HTS = 2  /* bias [heads, T, S] */
+} vtmu_bias_kind;
+
+/* Kernel choice.  AUTO takes the split-KV decode kernel for T == 1 (when its
+ * shape table covers headDim/vHeadDim/group size) and the prefill kernel
+ * otherwise.  The others force one kernel, for tests and measurement. */
+typedef enum vtmu_kernel {
+    VTMU_KERNEL_AUTO = 0,
+    VTMU_KERNEL_DECODE = 1,        /* T must be 1 */
+    VTMU_KERNEL_PREFILL_FFMA = 2,  /* tiled online-softmax kernel on FP32 FMA */
+    VTMU_KERNEL_PREFILL_TF32X3 = 3 /* tcgen05 3xTF32 tensor-core prefill */
+} vtmu_kernel;
+
+/*
+ * Parameters of one attention call.  Fill with vtmu_attention_params_init()
+ * (which writes the op's defaults), then set fields.  Names follow the op
+ * catalog: heads, headDim, kvHeads, vHeadDim, causal, posOffset, scale,
+ * softcap, window, alibi/alibiMax/alibiSlopes.
+ */
+typedef struct vtmu_attention_params {
+    int64_t T;            /* query rows (0 is a no-op) */
+    int64_t S;            /* key/value rows (0: every output row is zero) */
+    int32_t heads;        /* query heads, > 0 */
+    int32_t kv_heads;     /* KV heads; 0 means "= heads"; heads % kv_heads == 0 */
+    int32_t head_dim;     /* query/key width per head, 1..256 */
+    int32_t v_head_dim;   /* value width per head; 0 means "= head_dim"; 1..256 */
+    int32_t causal;       /* default 1 */
+    int32_t has_scale;    /* 0: scale = 1/sqrt(head_dim) */
+    float scale;          /* used when has_scale != 0; must be finite */
+    float softcap;        /* 0 = off; > 0: x = softcap * tanh(x / softcap) */
+    int64_t pos_offset;   /* absolute position of query row 0, >= 0 */
+    int64_t window;       /* 0 = off; causal: p - window < s <= p;
+                             non-causal: |p - s| <= window */
+    int32_t alibi;        /* vtmu_alibi_kind */
+    float alibi_max;      /* MPT alibi_bias_max (> 0) for VTMU_ALIBI_MPT */
+    const float* alibi_slopes; /* HOST [heads], for VTMU_ALIBI_SLOPES */
+    int32_t bias_kind;    /* vtmu_bias_kind; bias pointer must agree */
+    int32_t kernel;       /* vtmu_kernel */
+    int32_t decode_splits; /* decode kernel: KV splits per KV head, 0 = auto */
+} vtmu_attention_params;
+
+/* Writes the op's defaults: causal = 1, everything else 0 / off / AUTO. */
+VTMU_API void vtmu_attention_params_init(vtmu_attention_params* p);
+
+/*
+ * Scratch bytes that vtmu_attention needs for `p` (0 for the prefill
+ * kernels).  The decode kernel keeps per-split partial results (running max,
+ * sum and unnormalised output) and one arrival counter per KV head there.
+ * Returns VTMU_ERR_INVALID / VTMU_ERR_UNSUPPORTED for parameters that
+ * vtmu_attention would refuse.
+ */
+VTMU_API vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t* bytes);
+
+/*
+ * op "attention" (vtmu.mpakt.dev/api/ops).  q, k, v, out: DEVICE, layouts
+ * above, 4-byte aligned.  bias: DEVICE or NULL, must be non-NULL exactly when
+ * p->bias_kind != VTMU_BIAS_NONE.  out must not overlap an input.
+ * workspace: DEVICE, at least vtmu_attention_workspace_size() bytes (may be
+ * NULL when that is 0), 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE;
+ * each call leaves its arrival counters at zero again, so a workspace is
+ * reused without clearing.  Calls that share a workspace must not overlap on
+ * the GPU (use one workspace per concurrent stream).
+ *
+ * Errors: VTMU_ERR_INVALID (null pointer, T/S < 0, heads <= 0, heads not a
+ * multiple of kv_heads, window < 0, softcap < 0 or not finite, scale not
+ * finite, bias pointer and bias_kind disagree, alibi slopes missing, out
+ * aliasing an input, T != 1 with VTMU_KERNEL_DECODE), VTMU_ERR_RANGE
+ * (pos_offset < 0), VTMU_ERR_UNSUPPORTED (head_dim or v_head_dim outside
+ * 1..256, a forced kernel that does not cover the shape),
+ * VTMU_ERR_WORKSPACE, VTMU_ERR_CUDA.
+ */
+VTMU_API vtmu_status vtmu_attention(const float* q, const float* k, const float* v,
+                           const float* bias, float* out,
+                           const vtmu_attention_params* p, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * op "cache_write" (vtmu.mpakt.dev/api/ops): cache[offset + r, :] =
+ * values[r, :] for 0 <= r < rows, bit-exact, in place; rows outside
+ * [offset, offset + rows) are untouched.  cache [max_rows, width] and values
+ * [rows, width]: DEVICE, row-major f32, must not overlap.  rows == 0 is a
+ * no-op.  Errors: VTMU_ERR_INVALID (null pointer with rows > 0, negative
+ * sizes), VTMU_ERR_RANGE (offset < 0 or offset + rows > max_rows),
+ * VTMU_ERR_CUDA.
+ */
+VTMU_API vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width,
+                             const float* values, int64_t rows, int64_t offset,
+                             cudaStream_t stream);
+
+/* Space-separated optional features this build implements, named as the op
+ * catalog's feature table names them. */
+VTMU_API const char* vtmu_features(void);
+
+/* Message of the last failed call on this host thread ("" after success). */
+VTMU_API const char* vtmu_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* VTMU_ATTENTION_H */

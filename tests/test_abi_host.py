@@ -1,0 +1,141 @@
+"""The C-ABI library on the host (no GPU): it loads, exports every entry point
+that include/*.h declares, and refuses bad requests before any launch."""
+import glob
+import os
+import re
+
+import pytest
+
+import f32_gqa_attention_gb300 as vtmu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from f32_gqa_attention_gb300 import _build
+    _build.build()
+    return vtmu.load_library()
+
+
+def declared_symbols():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names.update(re.findall(r"VTMU_API\s+[\w\s\*]+?\b(vtmu_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_symbols()
+    for n in ("vtmu_attention", "vtmu_cache_write", "vtmu_attention_workspace_size",
+              "vtmu_attention_params_init", "vtmu_features", "vtmu_last_error"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for n in declared_symbols():
+        assert hasattr(lib, n), f"libvtmu.so does not export {n}"
+
+
+def test_exports_nothing_else(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", vtmu.LIB_PATH], capture_output=True,
+                         text=True).stdout
+    exported = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    assert exported == set(declared_symbols()), exported ^ set(declared_symbols())
+
+
+def test_features_name_the_catalog_features(lib):
+    assert set(vtmu.vtmu_features().split()) == {
+        "attention.alibi", "attention.bias", "attention.scale", "attention.softcap",
+        "attention.window"}
+
+
+def test_params_init_writes_defaults(lib):
+    p = vtmu.vtmu_attention_params_init()
+    assert p.causal == 1 and p.kv_heads == 0 and p.v_head_dim == 0 and p.has_scale == 0
+    assert p.softcap == 0 and p.window == 0 and p.alibi == 0 and p.kernel == 0
+
+
+def _err(fn):
+    with pytest.raises(vtmu.VtmuError) as e:
+        fn()
+    return e.value
+
+
+FAKE = 1 << 40  # never dereferenced: every case below fails before a launch
+
+
+@pytest.mark.parametrize("kw,status,word", [
+    (dict(heads=3, headDim=8, kvHeads=2), vtmu.VTMU_ERR_INVALID, "multiple of kvHeads"),
+    (dict(heads=0, headDim=8), vtmu.VTMU_ERR_INVALID, "heads"),
+    (dict(heads=2, headDim=0), vtmu.VTMU_ERR_INVALID, "headDim"),
+    (dict(heads=2, headDim=300), vtmu.VTMU_ERR_UNSUPPORTED, "headDim 300"),
+    (dict(heads=2, headDim=8, vHeadDim=512), vtmu.VTMU_ERR_UNSUPPORTED, "vHeadDim 512"),
+    (dict(heads=2, headDim=8, window=-1), vtmu.VTMU_ERR_INVALID, "window"),
+    (dict(heads=2, headDim=8, softcap=-1.0), vtmu.VTMU_ERR_INVALID, "softcap"),
+    (dict(heads=2, headDim=8, scale=float("inf")), vtmu.VTMU_ERR_INVALID, "scale"),
+    (dict(heads=2, headDim=8, posOffset=-3), vtmu.VTMU_ERR_RANGE, "posOffset"),
+    (dict(heads=2, headDim=8, alibiMax=-1.0), vtmu.VTMU_ERR_INVALID, "alibiMax"),
+    (dict(heads=1024, headDim=8, alibi=True), vtmu.VTMU_ERR_UNSUPPORTED, "attention.alibi"),
+    (dict(heads=4, headDim=8, kernel=vtmu.VTMU_KERNEL_DECODE), vtmu.VTMU_ERR_INVALID, "T == 1"),
+])
+def test_invalid_params_are_refused(lib, kw, status, word):
+    p = vtmu.make_params(4, 4, **kw)
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
+    assert e.status == status and word in str(e), str(e)
+    assert word in vtmu.vtmu_last_error()
+
+
+def test_decode_shape_outside_its_table_is_refused(lib):
+    p = vtmu.make_params(1, 64, heads=4, headDim=96, kvHeads=2, kernel=vtmu.VTMU_KERNEL_DECODE)
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED
+
+
+def test_null_and_aliasing_pointers_are_refused(lib):
+    p = vtmu.make_params(4, 4, heads=2, headDim=8)
+    assert _err(lambda: vtmu.vtmu_attention(None, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0)).status == \
+        vtmu.VTMU_ERR_INVALID
+    assert "overlaps" in str(_err(lambda: vtmu.vtmu_attention(FAKE, FAKE * 3, FAKE * 3, None, FAKE + 16, p,
+                                                              None, 0, 0)))
+    assert "4-byte" in str(_err(lambda: vtmu.vtmu_attention(FAKE + 2, FAKE * 3, FAKE * 3, None, FAKE * 2, p,
+                                                            None, 0, 0)))
+    pb = vtmu.make_params(4, 4, heads=2, headDim=8, bias_kind=vtmu.VTMU_BIAS_TS)
+    assert "attention.bias" in str(_err(lambda: vtmu.vtmu_attention(FAKE, FAKE * 3, FAKE * 3, None, FAKE * 2,
+                                                                    pb, None, 0, 0)))
+
+
+def test_decode_needs_its_workspace(lib):
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
+    need = vtmu.vtmu_attention_workspace_size(p)
+    assert need > 0
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 2, p, FAKE * 7, need - 1, 0))
+    assert e.status == vtmu.VTMU_ERR_WORKSPACE
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 2, p, FAKE * 7 + 16, need, 0))
+    assert e.status == vtmu.VTMU_ERR_WORKSPACE and "256-byte" in str(e)
+
+
+def test_prefill_needs_no_workspace(lib):
+    assert vtmu.vtmu_attention_workspace_size(vtmu.make_params(64, 64, heads=4, headDim=64)) == 0
+
+
+def test_zero_query_rows_is_a_no_op(lib):
+    vtmu.vtmu_attention(None, None, None, None, None, vtmu.make_params(0, 5, heads=2, headDim=8), None, 0, 0)
+
+
+@pytest.mark.parametrize("args,status", [
+    ((FAKE, 10, 4, FAKE * 2, 2, 9), vtmu.VTMU_ERR_RANGE),
+    ((FAKE, 10, 4, FAKE * 2, 2, -1), vtmu.VTMU_ERR_RANGE),
+    ((FAKE, 10, 4, FAKE * 2, -1, 0), vtmu.VTMU_ERR_INVALID),
+    ((None, 10, 4, FAKE * 2, 1, 0), vtmu.VTMU_ERR_INVALID),
+    ((FAKE, 10, 4, FAKE + 16, 2, 0), vtmu.VTMU_ERR_INVALID),  # values overlap the rows written
+])
+def test_cache_write_refusals(lib, args, status):
+    e = _err(lambda: vtmu.vtmu_cache_write(*args))
+    assert e.status == status
+
+
+def test_cache_write_empty_is_a_no_op(lib):
+    vtmu.vtmu_cache_write(None, 10, 4, None, 0, 10)

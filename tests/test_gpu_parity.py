@@ -1,0 +1,257 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle on
+the same seeded inputs.  Floating-point outputs must agree within 1e-4
+(absolute); cache_write must be bit-exact."""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+from gpu_util import TOL, gpu_attention, max_err, oracle_params, sample_rows, to_dev
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import f32_gqa_attention_gb300 as vtmu  # noqa: E402
+
+DECODE = vtmu.VTMU_KERNEL_DECODE
+FFMA = vtmu.VTMU_KERNEL_PREFILL_FFMA
+
+
+def check(inputs, params, tol=TOL):
+    out = gpu_attention(inputs["q"], inputs["k"], inputs["v"], inputs.get("bias"), **params)
+    ref = oracle.attention(inputs["q"], inputs["k"], inputs["v"], inputs.get("bias"), **oracle_params(params))
+    err = max_err(out, ref)
+    assert out.shape == ref.shape
+    assert np.all(np.isfinite(out))
+    assert err <= tol, f"max |err| {err:.3e} > {tol} for {params}"
+    return out, ref
+
+
+# ------------------------------------------------------------------ workloads
+def test_tiny_prefill_workload():
+    w = si.WORKLOADS["tiny_prefill"]
+    check(si.workload_inputs("tiny_prefill"),
+          dict(heads=w["heads"], headDim=w["headDim"], kvHeads=w["kvHeads"], **w["params"]))
+
+
+def test_gqa_decode_workload():
+    """cache_write one row at 32767 into [32768, 1024] K/V caches, then T=1
+    attention over all 32768 keys (32 heads, 8 KV heads, headDim 128)."""
+    w = si.WORKLOADS["gqa_decode"]
+    x = si.workload_inputs("gqa_decode")
+    H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
+    Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
+    vtmu.cache_write(Kc, to_dev(x["k_new"]), off)
+    vtmu.cache_write(Vc, to_dev(x["v_new"]), off)
+    out = vtmu.attention(to_dev(x["q"]), Kc, Vc, heads=H, headDim=D, kvHeads=Hk, **w["params"])
+    torch.cuda.synchronize()
+    oracle.cache_write(x["kc"], x["k_new"], off)
+    oracle.cache_write(x["vc"], x["v_new"], off)
+    assert torch.equal(Kc.cpu(), torch.from_numpy(x["kc"]))
+    assert torch.equal(Vc.cpu(), torch.from_numpy(x["vc"]))
+    ref = oracle.attention(x["q"], x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
+    err = max_err(out.cpu().numpy(), ref)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("name", ["gqa_prefill", "swa_softcap_prefill", "latent_bias_prefill",
+                                  "alibi_prefill"])
+def test_prefill_workload_sampled_rows(name):
+    """Full-size prefill on the GPU; the oracle recomputes sampled (t, h) rows."""
+    w = si.WORKLOADS[name]
+    x = si.workload_inputs(name)
+    params = dict(heads=w["heads"], headDim=w["headDim"], kvHeads=w["kvHeads"],
+                  vHeadDim=w.get("vHeadDim"), **w["params"])
+    out = gpu_attention(x["q"], x["k"], x["v"], x.get("bias"), **params)
+    assert np.all(np.isfinite(out))
+    H, Dv = w["heads"], w.get("vHeadDim") or w["headDim"]
+    rows = sample_rows(w["T"], H, H // w["kvHeads"], seed=1)
+    ref = oracle.attention_rows(x["q"], x["k"], x["v"], x.get("bias"), rows=rows, **params)
+    got = np.stack([out[t, h * Dv:(h + 1) * Dv] for t, h in rows])
+    err = max_err(got, ref)
+    assert err <= TOL, f"{name}: max |err| {err:.3e}"
+
+
+# --------------------------------------------------------------- random sweep
+def _case(seed):
+    g = np.random.default_rng(1000 + seed)
+    H, Hk = [(1, 1), (4, 1), (4, 2), (6, 3), (8, 8), (8, 2)][seed % 6]
+    D = int(g.choice([1, 4, 8, 32, 64, 96, 128, 192, 256]))
+    Dv = int(g.choice([D, D, 3, 16, 64, 128, 256]))
+    T = int(g.integers(1, 71))
+    S = int(g.integers(1, 200))
+    params = dict(heads=H, headDim=D, kvHeads=Hk, vHeadDim=Dv, causal=bool(g.integers(0, 4) > 0),
+                  posOffset=int(g.choice([0, 3, max(S - T, 0), S + 5])))
+    if g.random() < 0.4:
+        params["window"] = int(g.integers(1, 40))
+    if g.random() < 0.3:
+        params["softcap"] = float(g.choice([5.0, 30.0, 50.0]))
+    if g.random() < 0.3:
+        params["scale"] = float(g.uniform(0.02, 0.5))
+    r = g.random()
+    if r < 0.15:
+        params["alibi"] = True
+    elif r < 0.25:
+        params["alibiMax"] = float(g.choice([4.0, 8.0]))
+    elif r < 0.3:
+        params["alibiSlopes"] = [float(s) for s in g.uniform(0.0, 0.5, H)]
+    bias = None if g.random() < 0.6 else str(g.choice(["ts", "hts"]))
+    x = si.attention_inputs(T, S, H, Hk, D, Dv, seed, sigma=float(g.choice([1.0, 2.0])), bias=bias,
+                            bias_mask_p=0.1 if bias else 0.0)
+    if bias is not None:
+        # keep at least one unmasked visible key per row (rows whose only
+        # visible keys all carry -1e9 are implementation-defined)
+        b = x["bias"]
+        b[b == np.float32(-1e9)] = np.float32(-30.0)
+    return x, params
+
+
+@pytest.mark.parametrize("seed", range(48))
+def test_random_sweep(seed):
+    x, params = _case(seed)
+    check(x, params)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_sweep_forced_ffma(seed):
+    x, params = _case(seed)
+    check(x, dict(params, kernel=FFMA))
+
+
+# -------------------------------------------------------------------- decode
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("G", [2, 4, 8])
+@pytest.mark.parametrize("feat", ["plain", "window", "softcap_alibi", "bias_hts", "noncausal"])
+def test_decode_kernel(D, G, feat):
+    Hk = 2
+    H = G * Hk
+    S = 1000 + 37 * G + D  # ragged against the 64-row stages
+    pos = S - 120
+    x = si.attention_inputs(1, S, H, Hk, D, D, 10 * G + D, bias="hts" if feat == "bias_hts" else None)
+    params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=pos, kernel=DECODE)
+    if feat == "window":
+        params["window"] = 333
+    elif feat == "softcap_alibi":
+        params.update(softcap=20.0, alibi=True)
+    elif feat == "noncausal":
+        params.update(causal=False, window=150)
+    check(x, params)
+
+
+@pytest.mark.parametrize("splits", [1, 2, 7, 64, 256])
+def test_decode_forced_splits(splits):
+    x = si.attention_inputs(1, 5000, 16, 4, 128, 128, 77)
+    check(x, dict(heads=16, headDim=128, kvHeads=4, posOffset=4999, kernel=DECODE, decode_splits=splits))
+
+
+def test_decode_workspace_reused_across_shapes():
+    """Arrival counters return to zero: calls of different shapes in a row on
+    one workspace stay correct."""
+    ws = vtmu.Workspace()
+    for i, (S, H, Hk, D) in enumerate([(3000, 16, 4, 128), (700, 8, 4, 64), (3000, 16, 4, 128),
+                                        (64, 8, 1, 32)]):
+        x = si.attention_inputs(1, S, H, Hk, D, D, 300 + i)
+        params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=S - 1)
+        out = vtmu.attention(to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), workspace=ws, **params)
+        torch.cuda.synchronize()
+        ref = oracle.attention(x["q"], x["k"], x["v"], **params)
+        assert max_err(out.cpu().numpy(), ref) <= TOL
+    assert torch.count_nonzero(ws.buf[:64]).item() == 0  # counters back at zero
+
+
+def test_decode_equals_last_prefill_row():
+    S, H, Hk, D = 513, 8, 2, 128
+    x = si.attention_inputs(S, S, H, Hk, D, D, 55)
+    full = gpu_attention(x["q"], x["k"], x["v"], heads=H, headDim=D, kvHeads=Hk)
+    dec = gpu_attention(x["q"][-1:], x["k"], x["v"], heads=H, headDim=D, kvHeads=Hk, posOffset=S - 1,
+                        kernel=DECODE)
+    assert max_err(dec[0], full[-1]) <= 1e-5
+    ref = oracle.attention_rows(x["q"], x["k"], x["v"], rows=[(S - 1, h) for h in range(H)], heads=H,
+                                headDim=D, kvHeads=Hk)
+    assert max_err(dec[0].reshape(H, D), ref) <= TOL
+
+
+# --------------------------------------------------------------------- edges
+def test_no_keys_gives_zeros():
+    x = si.attention_inputs(5, 0, 4, 2, 32, 32, 1)
+    out = gpu_attention(x["q"], np.zeros((0, 64), np.float32), np.zeros((0, 64), np.float32),
+                        heads=4, headDim=32, kvHeads=2)
+    assert np.array_equal(out, np.zeros((5, 128), np.float32))
+
+
+@pytest.mark.parametrize("T", [1, 7])
+def test_nothing_visible_gives_zeros(T):
+    x = si.attention_inputs(T, 40, 4, 2, 64, 64, 2)
+    params = dict(heads=4, headDim=64, kvHeads=2, posOffset=500, window=10)
+    out, _ = check(x, params)
+    assert np.array_equal(out, np.zeros_like(out))
+
+
+def test_minus_inf_bias_masks_without_nan():
+    x = si.attention_inputs(9, 33, 2, 1, 32, 32, 3, bias="ts")
+    x["bias"][:, ::3] = -np.inf
+    x["bias"][4, :] = -np.inf  # a row with every key masked -> zeros
+    out, _ = check(x, dict(heads=2, headDim=32, kvHeads=1, causal=False))
+    assert np.array_equal(out[4], np.zeros_like(out[4]))
+
+
+def test_minus_1e9_bias_equals_explicit_mask():
+    x = si.attention_inputs(17, 17, 4, 4, 64, 64, 4, bias="ts")
+    mask = np.random.default_rng(0).random((17, 17)) < 0.3
+    np.fill_diagonal(mask, False)
+    b1 = np.where(mask, np.float32(-1e9), np.float32(0))
+    b2 = np.where(mask, np.float32(-np.inf), np.float32(0))
+    o1 = gpu_attention(x["q"], x["k"], x["v"], b1, heads=4, headDim=64, causal=False)
+    o2 = gpu_attention(x["q"], x["k"], x["v"], b2, heads=4, headDim=64, causal=False)
+    assert max_err(o1, o2) <= 1e-6
+
+
+def test_unaligned_views_take_the_scalar_path():
+    """Tensors that start 4 bytes past a 16-byte boundary."""
+    T, S, H, D = 20, 45, 4, 64
+    x = si.attention_inputs(T, S, H, H, D, D, 9)
+    def shifted(a):
+        buf = torch.zeros(a.size + 1, dtype=torch.float32, device="cuda")
+        buf[1:] = torch.from_numpy(a.ravel()).cuda()
+        return buf[1:].view(a.shape)
+    out_buf = torch.zeros(T * H * D + 1, dtype=torch.float32, device="cuda")
+    out = out_buf[1:].view(T, H * D)
+    vtmu.attention(shifted(x["q"]), shifted(x["k"]), shifted(x["v"]), heads=H, headDim=D, out=out)
+    torch.cuda.synchronize()
+    ref = oracle.attention(x["q"], x["k"], x["v"], heads=H, headDim=D)
+    assert max_err(out.cpu().numpy(), ref) <= TOL
+
+
+@pytest.mark.parametrize("T", [1, 300])
+def test_long_positions_with_alibi(T):
+    """Positions near 32767: the relative ALiBi form keeps scores small."""
+    S = 32768
+    x = si.attention_inputs(T, S, 4, 4, 32, 32, 12)
+    check(x, dict(heads=4, headDim=32, posOffset=S - T, alibi=True))
+
+
+# --------------------------------------------------------------- cache_write
+@pytest.mark.parametrize("width,rows,offset,max_rows", [
+    (1024, 1, 32767, 32768), (1024, 7, 0, 100), (33, 5, 10, 20), (3, 1, 0, 1), (256, 100, 155, 255)])
+def test_cache_write_bit_exact(width, rows, offset, max_rows):
+    g = si.Stream(width + rows)
+    cache = g.normal_f32(max_rows * width).reshape(max_rows, width)
+    vals = g.normal_f32(rows * width).reshape(rows, width)
+    vals.ravel()[::7] = np.float32(-0.0)
+    dc = to_dev(cache)
+    vtmu.cache_write(dc, to_dev(vals), offset)
+    torch.cuda.synchronize()
+    oracle.cache_write(cache, vals, offset)
+    got = dc.cpu().numpy()
+    assert got.tobytes() == cache.tobytes()
+
+
+def test_cache_write_out_of_range_launches_nothing():
+    dc = torch.zeros((8, 4), device="cuda")
+    with pytest.raises(vtmu.VtmuError):
+        vtmu.cache_write(dc, torch.ones((2, 4), device="cuda"), 7)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(dc).item() == 0
