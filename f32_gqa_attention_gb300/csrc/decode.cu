@@ -118,13 +118,14 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
     const int64_t n_rows = c_end > c_begin ? c_end - c_begin : 0;
     const int n_stages = (int)((n_rows + NR - 1) / NR);
 
-    // Query dims owned by this lane, for every head of the group, scaled.
+    // Query dims owned by this lane, for every head of the group (the
+    // score scale is applied in the epilogue).
     float qv[G][PL];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
         const float* qh = a.q + (int64_t)(kh * G + g) * D;
 #pragma unroll
-        for (int j = 0; j < PL; ++j) qv[g][j] = __ldg(qh + lane_dim<VEC>(lane, j)) * a.qk_mul;
+        for (int j = 0; j < PL; ++j) qv[g][j] = __ldg(qh + lane_dim<VEC>(lane, j));
     }
     // This lane's score slot: row rr of the warp's rows, head gg of the group.
     const int rr = lane / G;
