@@ -32,7 +32,8 @@ VTMU_BIAS_NONE, VTMU_BIAS_TS, VTMU_BIAS_HTS = 0, 1, 2
 VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREFILL_TF32X3 = 0, 1, 2, 3
 
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
-            "vtmu_cache_write", "vtmu_features", "vtmu_last_error")
+            "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc")
+NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 
 class VtmuError(RuntimeError):
@@ -93,6 +94,8 @@ def load_library():
         lib.vtmu_features.restype = ctypes.c_char_p
         lib.vtmu_last_error.argtypes = []
         lib.vtmu_last_error.restype = ctypes.c_char_p
+        lib.vtmu_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
+        lib.vtmu_attention_decode_noalloc.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -134,6 +137,15 @@ def vtmu_attention(q, k, v, bias, out, p: vtmu_attention_params, workspace, work
 def vtmu_cache_write(cache, max_rows: int, width: int, values, rows: int, offset: int, stream: int = 0) -> None:
     _check(load_library().vtmu_cache_write(_addr(cache), int(max_rows), int(width), _addr(values),
                                            int(rows), int(offset), stream or None))
+
+
+def vtmu_attention_decode_noalloc(q, k, v, bias, out, p: vtmu_attention_params, stream: int = 0) -> None:
+    """Decode (T == 1) with the library's static scratch: no workspace, no
+    allocation, for callers that cannot allocate device memory.  The first
+    call on a device looks up the scratch address (do it before any stream
+    capture); calls that overlap on the GPU race on the shared scratch."""
+    _check(load_library().vtmu_attention_decode_noalloc(_addr(q), _addr(k), _addr(v), _addr(bias), _addr(out),
+                                                        ctypes.byref(p), stream or None))
 
 
 def vtmu_features() -> str:

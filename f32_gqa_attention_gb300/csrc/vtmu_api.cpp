@@ -197,6 +197,11 @@ size_t decode_workspace(const vtmu::AttnDesc& a) {
 
 }  // namespace
 
+namespace vtmu {
+// Records `message` as this thread's vtmu_last_error() and returns `status`.
+vtmu_status report_error(vtmu_status status, const char* message) { return fail(status, "%s", message); }
+}  // namespace vtmu
+
 extern "C" {
 
 void vtmu_attention_params_init(vtmu_attention_params* p) {

@@ -11,6 +11,21 @@ import f32_gqa_attention_gb300 as vtmu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
+def _has_gpu():
+    try:
+        import torch
+        return torch.cuda.is_available()
+    except ImportError:
+        return False
+
+
+# The tests below hand the library fake device addresses and rely on its host
+# checks refusing each call before any launch.  They exist for the CPU-only
+# machine; where a GPU is present they are skipped, so that a wrong check can
+# never launch a kernel on those addresses.
+host_only = pytest.mark.skipif(_has_gpu(), reason="host-only checks with fake device addresses")
+
+
 @pytest.fixture(scope="module")
 def lib():
     from f32_gqa_attention_gb300 import _build
@@ -67,6 +82,7 @@ def _err(fn):
 FAKE = 1 << 40  # never dereferenced: every case below fails before a launch
 
 
+@host_only
 @pytest.mark.parametrize("kw,status,word", [
     (dict(heads=3, headDim=8, kvHeads=2), vtmu.VTMU_ERR_INVALID, "multiple of kvHeads"),
     (dict(heads=0, headDim=8), vtmu.VTMU_ERR_INVALID, "heads"),
@@ -88,12 +104,14 @@ def test_invalid_params_are_refused(lib, kw, status, word):
     assert word in vtmu.vtmu_last_error()
 
 
+@host_only
 def test_decode_shape_outside_its_table_is_refused(lib):
     p = vtmu.make_params(1, 64, heads=4, headDim=96, kvHeads=2, kernel=vtmu.VTMU_KERNEL_DECODE)
     e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
     assert e.status == vtmu.VTMU_ERR_UNSUPPORTED
 
 
+@host_only
 def test_null_and_aliasing_pointers_are_refused(lib):
     p = vtmu.make_params(4, 4, heads=2, headDim=8)
     assert _err(lambda: vtmu.vtmu_attention(None, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0)).status == \
@@ -107,6 +125,7 @@ def test_null_and_aliasing_pointers_are_refused(lib):
                                                                     pb, None, 0, 0)))
 
 
+@host_only
 def test_decode_needs_its_workspace(lib):
     p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
     need = vtmu.vtmu_attention_workspace_size(p)
@@ -121,10 +140,12 @@ def test_prefill_needs_no_workspace(lib):
     assert vtmu.vtmu_attention_workspace_size(vtmu.make_params(64, 64, heads=4, headDim=64)) == 0
 
 
+@host_only
 def test_zero_query_rows_is_a_no_op(lib):
     vtmu.vtmu_attention(None, None, None, None, None, vtmu.make_params(0, 5, heads=2, headDim=8), None, 0, 0)
 
 
+@host_only
 @pytest.mark.parametrize("args,status", [
     ((FAKE, 10, 4, FAKE * 2, 2, 9), vtmu.VTMU_ERR_RANGE),
     ((FAKE, 10, 4, FAKE * 2, 2, -1), vtmu.VTMU_ERR_RANGE),
@@ -137,5 +158,20 @@ def test_cache_write_refusals(lib, args, status):
     assert e.status == status
 
 
+@host_only
 def test_cache_write_empty_is_a_no_op(lib):
     vtmu.vtmu_cache_write(None, 10, 4, None, 0, 10)
+
+
+@host_only
+def test_noalloc_refuses_a_shape_beyond_its_scratch(lib):
+    p = vtmu.make_params(1, 32768, heads=64, headDim=128, kvHeads=8, posOffset=32767)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_WORKSPACE and "static scratch" in str(e)
+
+
+@host_only
+def test_noalloc_checks_parameters_first(lib):
+    p = vtmu.make_params(1, 64, heads=3, headDim=128, kvHeads=2)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID
