@@ -32,7 +32,8 @@ VTMU_BIAS_NONE, VTMU_BIAS_TS, VTMU_BIAS_HTS = 0, 1, 2
 VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREFILL_TF32X3 = 0, 1, 2, 3
 
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
-            "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc")
+            "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",
+            "vtmu_device_error")
 NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 
@@ -94,6 +95,8 @@ def load_library():
         lib.vtmu_features.restype = ctypes.c_char_p
         lib.vtmu_last_error.argtypes = []
         lib.vtmu_last_error.restype = ctypes.c_char_p
+        lib.vtmu_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
+        lib.vtmu_device_error.restype = ctypes.c_int
         lib.vtmu_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
         lib.vtmu_attention_decode_noalloc.restype = ctypes.c_int
         _lib = lib
@@ -146,6 +149,14 @@ def vtmu_attention_decode_noalloc(q, k, v, bias, out, p: vtmu_attention_params, 
     capture); calls that overlap on the GPU race on the shared scratch."""
     _check(load_library().vtmu_attention_decode_noalloc(_addr(q), _addr(k), _addr(v), _addr(bias), _addr(out),
                                                         ctypes.byref(p), stream or None))
+
+
+def vtmu_device_error() -> int:
+    """Synchronises the device; returns and clears the kernels' wait-timeout
+    flags (0 when no bounded wait gave up)."""
+    v = ctypes.c_uint(0)
+    _check(load_library().vtmu_device_error(ctypes.byref(v)))
+    return int(v.value)
 
 
 def vtmu_features() -> str:

@@ -8,29 +8,60 @@
 //  * grid (splits, kvHeads): one CTA streams a chunk of the range for one KV
 //    head and serves all G = heads/kvHeads query heads of its group, so each
 //    K/V byte is read once per group, not once per query head;
-//  * K/V rows go global -> shared through a multi-stage cp.async ring (no
-//    registers held by loads in flight; ~130-190 KB in flight per SM);
-//  * a warp takes R = 32/G rows of a stage: lane l holds the query dims
-//    {c*32*VEC + l*VEC + j}, computes R*G = 32 partial dot products, and a
+//  * a producer warp moves NR-row K and V tiles global -> shared with 2-D TMA
+//    (cp.async.bulk.tensor) into a ring of stages guarded by full/empty
+//    mbarriers; the consumer warps never issue a load;
+//  * a consumer warp takes R = 32/G rows of a stage.  Lane l holds the query
+//    dims {c*32*VEC + l*VEC + j}; it computes 32 partial dot products, and a
 //    5-step butterfly reduce-scatter over the warp leaves the full score of
-//    (row l/G, head l%G) in lane l;
-//  * fused epilogue (scale, softcap, ALiBi, bias) and online softmax in
-//    base 2; the probabilities go through 128 bytes of shared memory to the
-//    P.V step, where lane l owns value dims as it owns query dims;
+//    (row l/G, head l%G) in lane l.  Lane l stores its partials at slot
+//    index (logical slot XOR l) -- it reads the K row and the query head that
+//    the XOR names -- so every butterfly step is a plain shuffle-and-add with
+//    no selects;
+//  * fused epilogue (scale, softcap, ALiBi, bias) and online softmax in base
+//    2 (rescaling skipped when no running max moved); the probabilities go
+//    through 128 bytes of shared memory to the P.V step, where lane l owns
+//    value dims as it owns query dims;
 //  * warps merge in shared memory, each CTA writes its (m, l, o) partials,
 //    and the last CTA of a KV head (arrival counter, no waiting) merges the
 //    splits with the log-sum-exp rule  m* = max m_i, l* = sum l_i 2^(m_i-m*),
 //    o* = sum o_i 2^(m_i-m*) / l*  and writes the output row.
+//
+// Every mbarrier wait is bounded (see tma_sync.cuh); a wait that gives up
+// sets a bit of g_decode_device_error and the kernel unwinds.
 #include <cfloat>
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "tma_sync.cuh"
 
 namespace vtmu {
+
+__device__ unsigned int g_decode_device_error;
+
 namespace {
 
+// Stage geometry (compile-time; the defaults are the tuned configuration).
+#ifndef VTMU_DEC_NR
+#define VTMU_DEC_NR 64  // K/V rows per shared-memory stage
+#endif
+#ifndef VTMU_DEC_SMEM_KB
+#define VTMU_DEC_SMEM_KB 200  // shared-memory budget of one CTA's stage ring
+#endif
+#ifndef VTMU_DEC_MAX_STAGES
+#define VTMU_DEC_MAX_STAGES 4
+#endif
+#ifndef VTMU_DEC_CTAS_PER_SM
+#define VTMU_DEC_CTAS_PER_SM 1  // resident CTAs per SM the split count aims for
+#endif
+
 constexpr int kMaxSplits = 256;
-constexpr size_t kSmemBudget = 200 * 1024;
+constexpr size_t kSmemBudget = (size_t)VTMU_DEC_SMEM_KB * 1024;
 
 struct DecodeArgs {
     AttnDesc a;
@@ -47,18 +78,26 @@ struct DecodeArgs {
 template <int D, int G>
 struct DecCfg {
     static constexpr int R = 32 / G;                   // rows per warp step
-    static constexpr int NR = 64;                      // rows per stage
-    static constexpr int WARPS = NR / R;
-    static constexpr int THREADS = WARPS * 32;
+    // Rows per stage: VTMU_DEC_NR, but at most 8 consumer warps' worth (the
+    // split size is a multiple of VTMU_DEC_NR, hence of NR).
+    static constexpr int NR = VTMU_DEC_NR < 8 * R ? VTMU_DEC_NR : 8 * R;
+    static constexpr int WARPS = NR / R;               // consumer warps
+    static constexpr int THREADS = (WARPS + 1) * 32;   // + one producer warp
     static constexpr int VEC = (D % 128 == 0) ? 4 : ((D % 64 == 0) ? 2 : 1);
     static constexpr int NCH = D / (32 * VEC);         // chunks per row per lane
     static constexpr int PER_LANE = D / 32;            // dims per lane
-    static constexpr int STAGE_FLOATS = 2 * NR * D;    // K and V of one stage
-    static constexpr int STAGES_FIT = (int)(kSmemBudget / (STAGE_FLOATS * sizeof(float)));
-    static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
-    static constexpr size_t SMEM = (size_t)STAGES * STAGE_FLOATS * sizeof(float);
+    static constexpr int TILE_FLOATS = NR * D;         // one K (or V) tile
+    static constexpr int STAGE_FLOATS = 2 * TILE_FLOATS;
+    static constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * sizeof(float);
+    static constexpr int STAGES_FIT = (int)(kSmemBudget / STAGE_BYTES);
+    static constexpr int STAGES = STAGES_FIT > VTMU_DEC_MAX_STAGES ? VTMU_DEC_MAX_STAGES : STAGES_FIT;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES;
     static_assert(STAGES >= 2, "decode stage does not fit twice in shared memory");
-    static_assert(D % 32 == 0 && 32 % G == 0, "unsupported decode shape");
+    static_assert(NR % R == 0 && NR <= 256, "a stage must hold whole warp steps, <= 256 TMA rows");
+    static_assert(D % 32 == 0 && 32 % G == 0 && D <= 256, "unsupported decode shape");
+    // The warp merge and the split merge reuse the stage ring.
+    static_assert(WARPS * G * (2 + D) <= STAGES * STAGE_FLOATS, "merge area exceeds the stage ring");
+    static_assert(G * (kMaxSplits + 1) <= STAGES * STAGE_FLOATS, "split weights exceed the stage ring");
 };
 
 template <int VEC>
@@ -88,19 +127,22 @@ __device__ __forceinline__ void load_group(float* dst, const float* src) {
     }
 }
 
-// Lane-owned dim j (0 <= j < D/32) of chunked layout.
+// Lane-owned dim j (0 <= j < D/32) of the chunked layout.
 template <int VEC>
 __device__ __forceinline__ int lane_dim(int lane, int j) {
     return (j / VEC) * 32 * VEC + lane * VEC + (j % VEC);
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
-    decode_splitkv_kernel(const DecodeArgs args, const AlibiTable alibi) {
+__global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
+    decode_splitkv_kernel(const DecodeArgs args, const AlibiTable alibi, const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv) {
     using C = DecCfg<D, G>;
-    constexpr int R = C::R, NR = C::NR, VEC = C::VEC, PL = C::PER_LANE;
+    constexpr int R = C::R, NR = C::NR, VEC = C::VEC, PL = C::PER_LANE, STAGES = C::STAGES;
     constexpr unsigned FULL = 0xffffffffu;
-    extern __shared__ __align__(16) float smem[];
+    extern __shared__ __align__(1024) float smem[];
+    __shared__ __align__(8) uint64_t full_bar[STAGES];
+    __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(16) float pbuf[C::WARPS][32];
     __shared__ int s_is_last;
 
@@ -110,171 +152,185 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t p = a.pos_offset;  // position of the single query row
-    const int64_t ldk = (int64_t)a.Hk * D;
 
     const int64_t c_begin = args.s_lo + (int64_t)split * args.rows_per_split;
     int64_t c_end = c_begin + args.rows_per_split;
     if (c_end > args.s_end) c_end = args.s_end;
-    const int64_t n_rows = c_end > c_begin ? c_end - c_begin : 0;
-    const int n_stages = (int)((n_rows + NR - 1) / NR);
+    const int n_rows = c_end > c_begin ? (int)(c_end - c_begin) : 0;
+    const int n_stages = (n_rows + NR - 1) / NR;
 
-    // Query dims owned by this lane, for every head of the group (the
-    // score scale is applied in the epilogue).
-    float qv[G][PL];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        const float* qh = a.q + (int64_t)(kh * G + g) * D;
-#pragma unroll
-        for (int j = 0; j < PL; ++j) qv[g][j] = __ldg(qh + lane_dim<VEC>(lane, j));
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < STAGES; ++b) {
+            mbar_init(&full_bar[b], 1);
+            mbar_init(&empty_bar[b], C::WARPS);
+        }
+        fence_barrier_init();
     }
-    // This lane's score slot: row rr of the warp's rows, head gg of the group.
-    const int rr = lane / G;
-    const int gg = lane % G;
-    const int h_lane = kh * G + gg;
-    const float slope_lane = a.alibi_on ? alibi.slope_log2[h_lane] : 0.f;
+    __syncthreads();
 
-    float m_run = -INFINITY;  // per head gg (equal across lanes of the head)
-    float l_run = 0.f;        // this lane's share of the head's sum
+    float m_run = -INFINITY;  // running max of head lane%G (base 2)
+    float l_run = 0.f;        // this lane's share of that head's sum
     float o[G][PL];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
         for (int j = 0; j < PL; ++j) o[g][j] = 0.f;
 
-    // ---- stage loader: NR rows of K then NR rows of V, 16-byte cp.async ----
-    auto load_stage = [&](int st) {
-        float* sk = smem + (st % C::STAGES) * C::STAGE_FLOATS;
-        float* sv = sk + NR * D;
-        const int64_t r0 = c_begin + (int64_t)st * NR;
-        constexpr int CHUNKS = NR * D / 4;
-        for (int c = threadIdx.x; c < CHUNKS; c += C::THREADS) {
-            const int row = c / (D / 4);
-            const int col = (c % (D / 4)) * 4;
-            const int64_t s = r0 + row;
-            const bool ok = s < c_end;
-            const int64_t off = (ok ? s : c_begin) * ldk + (int64_t)kh * D + col;
-            cp_async16(sk + row * D + col, a.k + off, ok ? 16 : 0);
-            cp_async16(sv + row * D + col, a.v + off, ok ? 16 : 0);
+    if (warp == C::WARPS) {
+        // ---------------- producer: one thread issues every TMA ------------
+        if (lane == 0 && n_stages > 0) {
+            prefetch_tensormap(&tmk);
+            prefetch_tensormap(&tmv);
+            int issued = 0;
+            for (int st = 0; st < n_stages; ++st) {
+                const int b = st % STAGES;
+                if (st >= STAGES && !mbar_wait(&empty_bar[b], ((st / STAGES) - 1) & 1)) {
+                    raise_device_error(&g_decode_device_error, kErrDecodeEmptyWait);
+                    break;
+                }
+                float* sk = smem + b * C::STAGE_FLOATS;
+                mbar_arrive_expect_tx(&full_bar[b], C::STAGE_BYTES);
+                const int row = (int)(c_begin + (int64_t)st * NR);
+                tma_load_2d(sk, &tmk, kh * D, row, &full_bar[b]);
+                tma_load_2d(sk + C::TILE_FLOATS, &tmv, kh * D, row, &full_bar[b]);
+                ++issued;
+            }
+            // Drain: every copy issued has landed before the ring is reused.
+            for (int st = issued > STAGES ? issued - STAGES : 0; st < issued; ++st)
+                if (!mbar_wait(&full_bar[st % STAGES], (st / STAGES) & 1)) {
+                    raise_device_error(&g_decode_device_error, kErrDecodeDrainWait);
+                    break;
+                }
         }
-    };
-
+    } else {
+        // ---------------- consumers ----------------------------------------
+        // Query dims owned by this lane.  Slot gi holds head gi ^ (lane % G).
+        float qv[G][PL];
 #pragma unroll
-    for (int st = 0; st < C::STAGES - 1; ++st) {
-        if (st < n_stages) load_stage(st);
-        cp_async_commit();
+        for (int gi = 0; gi < G; ++gi) {
+            const float* qh = a.q + (int64_t)(kh * G + (gi ^ (lane % G))) * D;
+#pragma unroll
+            for (int j = 0; j < PL; ++j) qv[gi][j] = __ldg(qh + lane_dim<VEC>(lane, j));
+        }
+        const int rr = lane / G;  // logical slot after the butterfly: row rr, head gg
+        const int gg = lane % G;
+        const int h_lane = kh * G + gg;
+        const float slope_lane = a.alibi_on ? alibi.slope_log2[h_lane] : 0.f;
+        const float* bias_row = a.bias_kind == 0   ? nullptr
+                                : a.bias_kind == 1 ? a.bias + c_begin
+                                                   : a.bias + (int64_t)h_lane * a.S + c_begin;
+        const int64_t rel0 = c_begin - p;
+        const int rowx = lane / G;  // slot ri reads warp row ri ^ rowx
+
+        for (int st = 0; st < n_stages; ++st) {
+            const int b = st % STAGES;
+            if (!mbar_wait(&full_bar[b], (st / STAGES) & 1)) {
+                raise_device_error(&g_decode_device_error, kErrDecodeFullWait);
+                break;
+            }
+            const float* sk = smem + b * C::STAGE_FLOATS + warp * R * D;
+            const float* sv = sk + C::TILE_FLOATS;
+
+            // 32 partial dot products; slot ri*G + gi = (row ri^rowx, head gi^(lane%G)).
+            float part[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) part[i] = 0.f;
+#pragma unroll
+            for (int ri = 0; ri < R; ++ri) {
+                const float* krow = sk + (ri ^ rowx) * D + lane * VEC;
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c) {
+                    float kv[VEC];
+                    lds_vec<VEC>(kv, krow + c * 32 * VEC);
+#pragma unroll
+                    for (int gi = 0; gi < G; ++gi)
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            part[ri * G + gi] = fmaf(qv[gi][c * VEC + j], kv[j], part[ri * G + gi]);
+                }
+            }
+            // Reduce-scatter: lane L's slot i holds logical slot i ^ L, so each
+            // step keeps the low half and adds the partner's high half.
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1)
+#pragma unroll
+                for (int i = 0; i < off; ++i) part[i] += __shfl_xor_sync(FULL, part[i + off], off);
+
+            // Fused epilogue for (row rr, head gg).
+            const int row_l = st * NR + warp * R + rr;
+            float x = -INFINITY;
+            if (row_l < n_rows) {
+                const float bv = bias_row ? __ldg(bias_row + row_l) : 0.f;
+                x = score_log2(a, part[0], slope_lane, rel0 + row_l, bv);
+            }
+            // Online softmax per head: max over the R rows of the head.
+            float mt = x;
+#pragma unroll
+            for (int off = G; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, off));
+            const float m_new = fmaxf(m_run, mt);
+            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = fast_exp2(m_run - m_use);
+            const float pr = fast_exp2(x - m_use);
+            l_run = fmaf(l_run, alpha, pr);
+            m_run = m_new;
+            pbuf[warp][lane] = pr;
+            if (!__all_sync(FULL, alpha == 1.f)) {
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float ag = __shfl_sync(FULL, alpha, g);  // lane g serves head g
+#pragma unroll
+                    for (int j = 0; j < PL; ++j) o[g][j] *= ag;
+                }
+            }
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < R; ++r) {
+                float pw[G];
+                load_group<G>(pw, &pbuf[warp][r * G]);
+#pragma unroll
+                for (int c = 0; c < C::NCH; ++c) {
+                    float vv[VEC];
+                    lds_vec<VEC>(vv, sv + r * D + c * 32 * VEC + lane * VEC);
+#pragma unroll
+                    for (int g = 0; g < G; ++g)
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j)
+                            o[g][c * VEC + j] = fmaf(pw[g], vv[j], o[g][c * VEC + j]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty_bar[b]);  // this warp is done with stage b
+        }
+#pragma unroll
+        for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(FULL, l_run, off);
     }
-
-    for (int st = 0; st < n_stages; ++st) {
-        cp_async_wait<C::STAGES - 2>();
-        __syncthreads();  // stage st visible to all; stage st-1 fully consumed
-        if (st + C::STAGES - 1 < n_stages) load_stage(st + C::STAGES - 1);
-        cp_async_commit();
-
-        const float* sk = smem + (st % C::STAGES) * C::STAGE_FLOATS + warp * R * D;
-        const float* sv = sk + NR * D;
-
-        // 32 partial dot products: slot r*G + g.
-        float part[32];
-#pragma unroll
-        for (int i = 0; i < 32; ++i) part[i] = 0.f;
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-#pragma unroll
-            for (int c = 0; c < C::NCH; ++c) {
-                float kv[VEC];
-                lds_vec<VEC>(kv, sk + r * D + c * 32 * VEC + lane * VEC);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        part[r * G + g] = fmaf(qv[g][c * VEC + j], kv[j], part[r * G + g]);
-            }
-        }
-        // Butterfly reduce-scatter: after step `o` a lane keeps the half of
-        // its slots whose bit `o` matches its own lane bit.
-#pragma unroll
-        for (int step = 0; step < 5; ++step) {
-            const int off = 16 >> step;
-            const bool upper = (lane & off) != 0;
-#pragma unroll
-            for (int i = 0; i < off; ++i) {
-                const float send = upper ? part[i] : part[i + off];
-                const float keep = upper ? part[i + off] : part[i];
-                part[i] = keep + __shfl_xor_sync(FULL, send, off);
-            }
-        }
-
-        // Fused epilogue for (row rr, head gg).
-        const int64_t s = c_begin + (int64_t)st * NR + warp * R + rr;
-        float x = -INFINITY;
-        if (s < c_end) {
-            const float bv = a.bias_kind ? bias_at(a, h_lane, 0, s) : 0.f;
-            x = score_log2(a, part[0], slope_lane, s - p, bv);
-        }
-        // Online softmax per head: max over the R rows of the head.
-        float mt = x;
-#pragma unroll
-        for (int off = G; off < 32; off <<= 1) mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, off));
-        const float m_new = fmaxf(m_run, mt);
-        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = exp2f(m_run - m_use);
-        const float pr = exp2f(x - m_use);
-        l_run = fmaf(l_run, alpha, pr);
-        m_run = m_new;
-        pbuf[warp][lane] = pr;
-        __syncwarp();
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float ag = __shfl_sync(FULL, alpha, g);  // lane g serves head g
-#pragma unroll
-            for (int j = 0; j < PL; ++j) o[g][j] *= ag;
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            float pw[G];
-            load_group<G>(pw, &pbuf[warp][r * G]);
-#pragma unroll
-            for (int c = 0; c < C::NCH; ++c) {
-                float vv[VEC];
-                lds_vec<VEC>(vv, sv + r * D + c * 32 * VEC + lane * VEC);
-#pragma unroll
-                for (int g = 0; g < G; ++g)
-#pragma unroll
-                    for (int j = 0; j < VEC; ++j)
-                        o[g][c * VEC + j] = fmaf(pw[g], vv[j], o[g][c * VEC + j]);
-            }
-        }
-        __syncwarp();
-    }
-    cp_async_wait<0>();
 
     // ---- merge the warps of this CTA -------------------------------------
-#pragma unroll
-    for (int off = G; off < 32; off <<= 1) l_run += __shfl_xor_sync(FULL, l_run, off);
-    __syncthreads();  // every warp is done with the stage buffers
+    __syncthreads();  // all copies landed (producer drained) and all stages consumed
     float* wm = smem;                      // [WARPS][G]
     float* wl = wm + C::WARPS * G;         // [WARPS][G]
     float* wo = wl + C::WARPS * G;         // [WARPS][G][D]
-    if (lane < G) {
-        wm[warp * G + lane] = m_run;
-        wl[warp * G + lane] = l_run;
+    if (warp < C::WARPS) {
+        if (lane < G) {
+            wm[warp * G + lane] = m_run;
+            wl[warp * G + lane] = l_run;
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+            for (int j = 0; j < PL; ++j) wo[(warp * G + g) * D + lane_dim<VEC>(lane, j)] = o[g][j];
     }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-#pragma unroll
-        for (int j = 0; j < PL; ++j) wo[(warp * G + g) * D + lane_dim<VEC>(lane, j)] = o[g][j];
     __syncthreads();
 
     const int Hs = args.splits;
     for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
         const int g = idx / D, e = idx % D;
         float M = -INFINITY;
-#pragma unroll 4
         for (int w = 0; w < C::WARPS; ++w) M = fmaxf(M, wm[w * G + g]);
         const float mu = (M == -INFINITY) ? 0.f : M;
         float acc = 0.f, L = 0.f;
         for (int w = 0; w < C::WARPS; ++w) {
-            const float sc = exp2f(wm[w * G + g] - mu);
+            const float sc = fast_exp2(wm[w * G + g] - mu);
             acc = fmaf(wo[(w * G + g) * D + e], sc, acc);
             L = fmaf(wl[w * G + g], sc, L);
         }
@@ -297,9 +353,10 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
     if (!s_is_last) return;
     __threadfence();
 
-    float* sw = smem;            // [G][kMaxSplits] split weights
+    float* sw = smem;                   // [G][kMaxSplits] split weights
     float* sinv = sw + G * kMaxSplits;  // [G] 1 / l*
-    for (int g = warp; g < G; g += C::WARPS) {
+    constexpr int NW = C::THREADS / 32;
+    for (int g = warp; g < G; g += NW) {
         const int h = kh * G + g;
         float M = -INFINITY;
         for (int i = lane; i < Hs; i += 32) M = fmaxf(M, __ldcg(args.part_m + (int64_t)h * Hs + i));
@@ -308,7 +365,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
         const float mu = (M == -INFINITY) ? 0.f : M;
         float L = 0.f;
         for (int i = lane; i < Hs; i += 32) {
-            const float w = exp2f(__ldcg(args.part_m + (int64_t)h * Hs + i) - mu);
+            const float w = fast_exp2(__ldcg(args.part_m + (int64_t)h * Hs + i) - mu);
             sw[g * kMaxSplits + i] = w;
             L = fmaf(__ldcg(args.part_l + (int64_t)h * Hs + i), w, L);
         }
@@ -329,18 +386,55 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, 1)
     if (threadIdx.x == 0) args.counters[kh] = 0u;  // ready for the next call
 }
 
+// ---- host side ---------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Row-major [rows, cols] f32 matrix, tiles of box_rows x box_cols.
+bool encode_rows(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
+    auto fn = tensor_map_encoder();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D, int G>
 cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, cudaStream_t stream) {
     using C = DecCfg<D, G>;
+    const AttnDesc& a = args.a;
+    CUtensorMap tmk, tmv;
+    std::memset(&tmk, 0, sizeof(tmk));
+    std::memset(&tmv, 0, sizeof(tmv));
+    if (a.S > 0) {
+        if (!encode_rows(&tmk, a.k, a.S, (int64_t)a.Hk * D, D, C::NR) ||
+            !encode_rows(&tmv, a.v, a.S, (int64_t)a.Hk * D, D, C::NR))
+            return cudaErrorInvalidValue;
+    }
     auto kern = decode_splitkv_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(args.splits, args.a.Hk);
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(args, alibi);
+    dim3 grid(args.splits, a.Hk);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(args, alibi, tmk, tmv);
     return cudaGetLastError();
 }
 
-int stage_rows() { return 64; }
+int stage_rows() { return VTMU_DEC_NR; }
 
 }  // namespace
 
@@ -348,6 +442,7 @@ bool decode_supported(const AttnDesc& a) {
     if (a.T != 1 || a.D != a.Dv) return false;
     if (!(a.D == 32 || a.D == 64 || a.D == 128)) return false;
     if (!(a.G == 2 || a.G == 4 || a.G == 8)) return false;
+    if (a.S >= ((int64_t)1 << 31)) return false;
     return true;
 }
 
@@ -369,8 +464,9 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
     const int nr = stage_rows();
     int splits = forced_splits;
     if (splits <= 0) {
-        // One CTA per SM: split each KV head's range into ~num_sms/Hk chunks.
-        splits = (num_sms + a.Hk - 1) / a.Hk;
+        // Fill the SMs once: split each KV head's range into
+        // ~num_sms * ctas_per_sm / Hk chunks.
+        splits = (num_sms * VTMU_DEC_CTAS_PER_SM + a.Hk - 1) / a.Hk;
         if (splits < 1) splits = 1;
     }
     if (splits > kMaxSplits) splits = kMaxSplits;
@@ -413,6 +509,16 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
     VTMU_DEC(128, 2) VTMU_DEC(128, 4) VTMU_DEC(128, 8)
 #undef VTMU_DEC
     return cudaErrorInvalidValue;
+}
+
+unsigned int decode_take_device_error() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_device_error, sizeof(v)) != cudaSuccess) return 0;
+    if (v) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_decode_device_error, &zero, sizeof(zero));
+    }
+    return v;
 }
 
 }  // namespace vtmu

@@ -26,6 +26,8 @@ bool decode_supported(const AttnDesc& a);
 void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan);
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
                           void* workspace, cudaStream_t stream);
+// Reads and clears the decode kernel's device error flag (synchronous).
+unsigned int decode_take_device_error();
 
 // ---- tiled prefill on FP32 FMA ----------------------------------------------
 bool prefill_ffma_supported(const AttnDesc& a);

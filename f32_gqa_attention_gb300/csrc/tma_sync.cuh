@@ -1,0 +1,96 @@
+// tma_sync.cuh -- mbarrier and TMA (cp.async.bulk.tensor) helpers, written
+// from the PTX ISA, plus the library's device error flag.
+//
+// Every wait is bounded: a wait that has not seen its phase complete after
+// kWaitLimitNs of %globaltimer time returns false; the kernel records where it
+// gave up in its device error flag and unwinds instead of hanging the GPU.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "attn_common.cuh"
+
+namespace vtmu {
+
+// Wait limit for one mbarrier phase (1 s): far beyond any legitimate wait.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Device error codes, OR-ed into the flag (read by vtmu_device_error()).
+enum DeviceError : unsigned int {
+    kErrDecodeFullWait = 1u << 0,   // decode consumer gave up on a loaded stage
+    kErrDecodeEmptyWait = 1u << 1,  // decode producer gave up on a free stage
+    kErrDecodeDrainWait = 1u << 2,  // decode producer gave up draining its copies
+};
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of `bar` with the given parity; false after the limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// 2-D tiled TMA load of box (x = inner element coordinate, y = row) into
+// shared memory, completing on `bar` (complete_tx).  x * element size must be
+// a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];\n" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// 2^x on the MUFU unit (PTX ex2.approx.ftz.f32); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Each translation unit that waits keeps its own device flag (no relocatable
+// device code); the host ORs them together in vtmu_device_error().
+__device__ __forceinline__ void raise_device_error(unsigned int* flag, unsigned int code) { atomicOr(flag, code); }
+
+}  // namespace vtmu

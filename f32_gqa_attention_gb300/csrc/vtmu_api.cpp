@@ -308,4 +308,13 @@ const char* vtmu_features(void) {
 
 const char* vtmu_last_error(void) { return g_last_error.c_str(); }
 
+vtmu_status vtmu_device_error(unsigned int* flags) {
+    if (!flags) return fail(VTMU_ERR_INVALID, "flags is NULL");
+    *flags = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "device_error: synchronize");
+    *flags = vtmu::decode_take_device_error();
+    return ok();
+}
+
 }  // extern "C"

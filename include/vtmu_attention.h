@@ -192,6 +192,18 @@ VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, const float* 
                                                    const vtmu_attention_params* p,
                                                    cudaStream_t stream);
 
+/*
+ * Kernel-side failures.  Every wait inside a kernel (TMA stage arrival,
+ * stage release) gives up after one second instead of hanging the GPU; the
+ * kernel then sets a bit in a device flag, abandons its output and returns.
+ * This call synchronises the current device, stores the OR of the flags of
+ * every kernel in *flags (0: no wait gave up since the last call) and clears
+ * them.  Decode bits: 1 = a consumer gave up on a loaded stage, 2 = the
+ * producer gave up on a free stage, 4 = the producer gave up draining its
+ * copies.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
+ */
+VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
+
 /* Space-separated optional features this build implements, named as the op
  * catalog's feature table names them. */
 VTMU_API const char* vtmu_features(void);

@@ -175,3 +175,8 @@ def test_noalloc_checks_parameters_first(lib):
     p = vtmu.make_params(1, 64, heads=3, headDim=128, kvHeads=2)
     e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
     assert e.status == vtmu.VTMU_ERR_INVALID
+
+
+@host_only
+def test_device_error_needs_an_output(lib):
+    assert lib.vtmu_device_error(None) == vtmu.VTMU_ERR_INVALID

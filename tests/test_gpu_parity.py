@@ -255,3 +255,10 @@ def test_cache_write_out_of_range_launches_nothing():
         vtmu.cache_write(dc, torch.ones((2, 4), device="cuda"), 7)
     torch.cuda.synchronize()
     assert torch.count_nonzero(dc).item() == 0
+
+
+def test_no_bounded_wait_gave_up():
+    """After all the launches above, no kernel wait hit its time limit."""
+    x = si.attention_inputs(1, 4096, 16, 4, 128, 128, 91)
+    check(x, dict(heads=16, headDim=128, kvHeads=4, posOffset=4095, kernel=DECODE))
+    assert vtmu.vtmu_device_error() == 0
