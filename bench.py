@@ -7,7 +7,9 @@
 Default workload: the GQA decode step (Llama-3-8B shape): cache_write of one
 new K row and one new V row at position 32767 into [32768, 8*128] f32 caches,
 then attention with T = 1 over S = 32768 keys, 32 query heads, 8 KV heads,
-headDim 128.  A step is that whole decode step.  Two independent caches
+headDim 128.  A step is that whole decode step, run as one fused launch
+(vtmu_decode_step); the line also reports the same step as three separate
+launches (`unfused_ms_per_step`).  Two independent caches
 (sessions) alternate between steps, so each step reads its 256 MiB of K/V
 from HBM (working set 512 MiB > the 126 MiB L2).
 
@@ -291,20 +293,25 @@ def run_vtmu(args, rank, world, local):
         ws_bytes = vtmu.vtmu_attention_workspace_size(p)
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         width = Hk * D
-        launches_per_step = 3
+        launches_per_step = 1
 
         def step(i, ev=None):
+            # One fused launch: both cache_writes and the attention.
             s = sessions[i % 2]
-            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kn, 1, off, st)
-            vtmu.vtmu_cache_write(s["Vc"], off + 1, width, vn, 1, off, st)
             if ev is not None:
                 ev[0].record(stream)
-            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+            vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
             if ev is not None:
                 ev[1].record(stream)
 
+        def unfused_step(i):
+            s = sessions[i % 2]
+            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kn, 1, off, st)
+            vtmu.vtmu_cache_write(s["Vc"], off + 1, width, vn, 1, off, st)
+            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+
         work_per_step, unit = step_bytes / 1e9, "GB/s"
-        kernel_tag, kernel_work, kernel_unit = "decode", kv_bytes + 2 * H * D * 4, "GB/s"
+        kernel_tag, kernel_work, kernel_unit = "decode", step_bytes, "GB/s"
         bound, peak = "hbm", float(peaks["hbm_gbs"])
         flush = None
         l2_note = "inputs > L2: two 256 MiB K/V cache sets alternate between steps"
@@ -330,6 +337,8 @@ def run_vtmu(args, rank, world, local):
             vtmu.vtmu_attention(q, k, v, b, out, p, None, 0, st)
             if ev is not None:
                 ev[1].record(stream)
+
+        unfused_step = None
 
         flops = prefill_flops(w)
         work_per_step, unit = flops / 1e12, "TFLOP/s"
@@ -368,6 +377,19 @@ def run_vtmu(args, rank, world, local):
     kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
     step_ms = max_over_ranks(step_ms, world)
 
+    # The same decode step as three separate launches, for comparison.
+    unfused_ms = None
+    if unfused_step is not None:
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            unfused_step(i)
+        e0.record(stream)
+        for i in range(args.steps):
+            unfused_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        unfused_ms = e0.elapsed_time(e1) / args.steps
+
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
     if w["kind"] == "decode":
@@ -382,9 +404,7 @@ def run_vtmu(args, rank, world, local):
                 q.copy_(qh, non_blocking=True)
                 kn.copy_(knh, non_blocking=True)
                 vn.copy_(vnh, non_blocking=True)
-            vtmu.vtmu_cache_write(s["Kc"], off + 1, Hk * D, kn, 1, off, st)
-            vtmu.vtmu_cache_write(s["Vc"], off + 1, Hk * D, vn, 1, off, st)
-            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+            vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
             with torch.cuda.stream(stream):
                 outh.copy_(out, non_blocking=True)
             stream.synchronize()  # the step's output is on the host before the next step
@@ -450,6 +470,8 @@ def run_vtmu(args, rank, world, local):
         "impl": "vtmu", "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
         "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
     }
+    if unfused_ms is not None:
+        line["unfused_ms_per_step"] = round(unfused_ms, 5)
     if rank == 0:
         print(json.dumps(line), flush=True)
 

@@ -33,7 +33,7 @@ VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREF
 
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
             "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",
-            "vtmu_device_error")
+            "vtmu_device_error", "vtmu_decode_step")
 NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 
@@ -95,6 +95,9 @@ def load_library():
         lib.vtmu_features.restype = ctypes.c_char_p
         lib.vtmu_last_error.argtypes = []
         lib.vtmu_last_error.restype = ctypes.c_char_p
+        lib.vtmu_decode_step.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
+                                         vp, vp, vp, P, vp, ctypes.c_size_t, vp]
+        lib.vtmu_decode_step.restype = ctypes.c_int
         lib.vtmu_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint)]
         lib.vtmu_device_error.restype = ctypes.c_int
         lib.vtmu_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
@@ -135,6 +138,14 @@ def vtmu_attention(q, k, v, bias, out, p: vtmu_attention_params, workspace, work
     _check(load_library().vtmu_attention(_addr(q), _addr(k), _addr(v), _addr(bias), _addr(out),
                                          ctypes.byref(p), _addr(workspace), int(workspace_bytes),
                                          stream or None))
+
+
+def vtmu_decode_step(k_cache, v_cache, max_rows: int, k_new, v_new, new_rows: int, offset: int, q, bias, out,
+                     p: vtmu_attention_params, workspace, workspace_bytes: int, stream: int = 0) -> None:
+    _check(load_library().vtmu_decode_step(_addr(k_cache), _addr(v_cache), int(max_rows), _addr(k_new),
+                                           _addr(v_new), int(new_rows), int(offset), _addr(q), _addr(bias),
+                                           _addr(out), ctypes.byref(p), _addr(workspace), int(workspace_bytes),
+                                           stream or None))
 
 
 def vtmu_cache_write(cache, max_rows: int, width: int, values, rows: int, offset: int, stream: int = 0) -> None:
@@ -249,6 +260,30 @@ def attention(q, k, v, bias=None, *, heads, headDim, out=None, workspace=None, s
     buf, cap = ws.get(nbytes)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
     vtmu_attention(q, k, v, bias, out, p, buf, cap, st)
+    return out
+
+
+def decode_step(k_cache, v_cache, k_new, v_new, offset: int, q, bias=None, *, heads, headDim, out=None,
+                workspace=None, stream=None, **params):
+    """A decode step on CUDA tensors: cache_write of k_new / v_new into the
+    caches at row ``offset``, then attention of q over the updated caches
+    (all of their rows, posOffset defaulting to the last new row).  One launch
+    when the decode kernel covers the shape.  Returns out."""
+    import torch
+    T, S = q.shape[0], k_cache.shape[0]
+    vhd = params.get("vHeadDim") or headDim
+    params.setdefault("posOffset", offset + k_new.shape[0] - T)
+    bias_kind = VTMU_BIAS_NONE
+    if bias is not None:
+        bias_kind = VTMU_BIAS_TS if bias.dim() == 2 else VTMU_BIAS_HTS
+    p = make_params(T, S, heads=heads, headDim=headDim, bias_kind=bias_kind, **params)
+    if out is None:
+        out = torch.empty((T, heads * vhd), dtype=torch.float32, device=q.device)
+    nbytes = vtmu_attention_workspace_size(p)
+    ws = workspace if workspace is not None else _default_workspace(q.device)
+    buf, cap = ws.get(nbytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    vtmu_decode_step(k_cache, v_cache, S, k_new, v_new, k_new.shape[0], offset, q, bias, out, p, buf, cap, st)
     return out
 
 

@@ -73,6 +73,7 @@ struct DecodeArgs {
     float* part_l;           // [heads][splits]
     float* part_o;           // [heads][splits][Dv]
     unsigned int* counters;  // [kvHeads], zero between calls
+    DecodeCacheWrite cw;     // fused cache_write (cw.k_new == nullptr: none)
 };
 
 template <int D, int G>
@@ -166,6 +167,20 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
         }
         fence_barrier_init();
     }
+    // Fused cache_write, rows no split reads: written by split 0 of each KV
+    // head (its own columns).  Rows inside the visible range are written by
+    // the consumer warp that owns them, below.
+    const int64_t ld = (int64_t)a.Hk * D;
+    if (args.cw.k_new && split == 0 && warp == 0) {
+        for (int64_t r = args.cw.lo; r < args.cw.hi; ++r) {
+            if (r >= args.s_lo && r < args.s_end) continue;
+            const int64_t src = (r - args.cw.lo) * ld + (int64_t)kh * D, dst = r * ld + (int64_t)kh * D;
+            for (int d = lane; d < D; d += 32) {
+                args.cw.kc[dst + d] = __ldg(args.cw.k_new + src + d);
+                args.cw.vc[dst + d] = __ldg(args.cw.v_new + src + d);
+            }
+        }
+    }
     __syncthreads();
 
     float m_run = -INFINITY;  // running max of head lane%G (base 2)
@@ -228,7 +243,37 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
                 raise_device_error(&g_decode_device_error, kErrDecodeFullWait);
                 break;
             }
-            const float* sk = smem + b * C::STAGE_FLOATS + warp * R * D;
+            float* skw = smem + b * C::STAGE_FLOATS + warp * R * D;
+            if (args.cw.k_new) {
+                // Fused cache_write of rows this warp owns: the new values go
+                // to the cache and replace the staged (old) rows.
+                const int64_t row0 = c_begin + (int64_t)st * NR + warp * R;
+                int64_t lo = row0 > args.cw.lo ? row0 : args.cw.lo;
+                int64_t hi = row0 + R < args.cw.hi ? row0 + R : args.cw.hi;
+                if (hi > c_end) hi = c_end;
+                if (lo < hi) {
+                    for (int64_t r = lo; r < hi; ++r) {
+                        float* skr = skw + (int)(r - row0) * D;
+                        float* svr = skr + C::TILE_FLOATS;
+                        const int64_t src = (r - args.cw.lo) * ld + (int64_t)kh * D, dst = r * ld + (int64_t)kh * D;
+#pragma unroll
+                        for (int j = 0; j < PL; ++j) {
+                            const int d = lane_dim<VEC>(lane, j);
+                            const float kx = __ldg(args.cw.k_new + src + d);
+                            const float vx = __ldg(args.cw.v_new + src + d);
+                            skr[d] = kx;
+                            svr[d] = vx;
+                            args.cw.kc[dst + d] = kx;
+                            args.cw.vc[dst + d] = vx;
+                        }
+                    }
+                    // Order these generic-proxy writes before the TMA that
+                    // refills the stage later.
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    __syncwarp();
+                }
+            }
+            const float* sk = skw;
             const float* sv = sk + C::TILE_FLOATS;
 
             // 32 partial dot products; slot ri*G + gi = (row ri^rowx, head gi^(lane%G)).
@@ -487,8 +532,10 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
 }
 
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
-                          void* workspace, cudaStream_t stream) {
+                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw) {
     DecodeArgs args;
+    std::memset(&args.cw, 0, sizeof(args.cw));
+    if (cw) args.cw = *cw;
     args.a = a;
     args.s_lo = plan.s_lo;
     args.s_end = plan.s_end;

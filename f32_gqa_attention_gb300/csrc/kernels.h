@@ -18,6 +18,16 @@ struct DecodePlan {
     size_t workspace_bytes = 0;
 };
 
+// A cache_write fused into a decode launch: rows [lo, hi) of the K and V
+// caches (row-major [*, kvHeads*headDim]) take k_new / v_new rows 0..hi-lo-1.
+struct DecodeCacheWrite {
+    float* kc;
+    float* vc;
+    const float* k_new;
+    const float* v_new;
+    int64_t lo, hi;
+};
+
 // True when the decode kernel's shape table covers this call (T == 1,
 // headDim == vHeadDim in {32, 64, 128}, group size in {2, 4, 8}, 16-byte
 // aligned rows).  Pointer alignment is checked separately at launch.
@@ -25,7 +35,7 @@ bool decode_supported(const AttnDesc& a);
 // Fills `plan` for the call; `forced_splits` > 0 overrides the heuristic.
 void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan);
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
-                          void* workspace, cudaStream_t stream);
+                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw = nullptr);
 // Reads and clears the decode kernel's device error flag (synchronous).
 unsigned int decode_take_device_error();
 

@@ -219,14 +219,28 @@ vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t
     return ok();
 }
 
-vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const float* bias, float* out,
-                           const vtmu_attention_params* p, void* workspace, size_t workspace_bytes,
-                           cudaStream_t stream) {
-    Resolved r;
-    vtmu_status st = resolve(p, &r);
-    if (st != VTMU_OK) return st;
+}  // extern "C"
+
+namespace {
+
+// op "attention" after resolve(); with `cw`, the two cache writes of a
+// decode step come first (fused into the decode launch when it runs).
+vtmu_status run_attention(Resolved& r, const float* q, const float* k, const float* v, const float* bias,
+                          float* out, const vtmu_attention_params* p, void* workspace, size_t workspace_bytes,
+                          cudaStream_t stream, const vtmu::DecodeCacheWrite* cw) {
     vtmu::AttnDesc& a = r.a;
-    if (a.T == 0) return ok();
+    cudaError_t e;
+    auto write_caches = [&]() -> cudaError_t {
+        if (!cw) return cudaSuccess;
+        cudaError_t ce = vtmu::launch_cache_write(cw->kc, (int64_t)a.Hk * a.D, cw->k_new, cw->hi - cw->lo,
+                                                  cw->lo, stream);
+        if (ce != cudaSuccess) return ce;
+        return vtmu::launch_cache_write(cw->vc, (int64_t)a.Hk * a.Dv, cw->v_new, cw->hi - cw->lo, cw->lo, stream);
+    };
+    if (a.T == 0) {
+        e = write_caches();
+        return e == cudaSuccess ? ok() : cuda_fail(e, "cache_write launch");
+    }
     if (!q) return fail(VTMU_ERR_INVALID, "q is NULL");
     if (!out) return fail(VTMU_ERR_INVALID, "out is NULL");
     if (a.S > 0 && (!k || !v)) return fail(VTMU_ERR_INVALID, "k or v is NULL");
@@ -254,7 +268,6 @@ vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const
     vtmu::AlibiTable alibi;
     fill_alibi(p, &alibi);
 
-    cudaError_t e;
     if (r.kernel == VTMU_KERNEL_DECODE) {
         const uintptr_t m16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                               reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
@@ -273,14 +286,67 @@ vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const
             return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
         vtmu::DecodePlan plan;
         vtmu::decode_plan(a, p->decode_splits, device_sm_count(), &plan);
-        e = vtmu::launch_decode(a, alibi, plan, workspace, stream);
+        e = vtmu::launch_decode(a, alibi, plan, workspace, stream, cw);
         if (e != cudaSuccess) return cuda_fail(e, "decode launch");
         return ok();
     }
     if (!vtmu::prefill_ffma_supported(a)) return fail(VTMU_ERR_UNSUPPORTED, "shape not covered by the prefill kernel");
+    e = write_caches();
+    if (e != cudaSuccess) return cuda_fail(e, "cache_write launch");
     e = vtmu::launch_prefill_ffma(a, alibi, stream);
     if (e != cudaSuccess) return cuda_fail(e, "prefill launch");
     return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const float* bias, float* out,
+                           const vtmu_attention_params* p, void* workspace, size_t workspace_bytes,
+                           cudaStream_t stream) {
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    return run_attention(r, q, k, v, bias, out, p, workspace, workspace_bytes, stream, nullptr);
+}
+
+vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new,
+                             const float* v_new, int64_t new_rows, int64_t offset, const float* q,
+                             const float* bias, float* out, const vtmu_attention_params* p, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    const vtmu::AttnDesc& a = r.a;
+    if (max_rows < 0 || new_rows < 0)
+        return fail(VTMU_ERR_INVALID, "decode_step: negative size (max_rows %lld, new_rows %lld)",
+                    (long long)max_rows, (long long)new_rows);
+    if (offset < 0 || offset > max_rows || new_rows > max_rows - offset)
+        return fail(VTMU_ERR_RANGE, "decode_step: offset %lld + rows %lld exceeds maxRows %lld", (long long)offset,
+                    (long long)new_rows, (long long)max_rows);
+    if (a.S > max_rows)
+        return fail(VTMU_ERR_INVALID, "decode_step: S %lld exceeds the cache's %lld rows", (long long)a.S,
+                    (long long)max_rows);
+    if (new_rows == 0) return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes,
+                                            stream, nullptr);
+    if (!k_cache || !v_cache || !k_new || !v_new)
+        return fail(VTMU_ERR_INVALID, "decode_step: a cache or new-row pointer is NULL");
+    if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
+         reinterpret_cast<uintptr_t>(k_new) | reinterpret_cast<uintptr_t>(v_new)) & 3u)
+        return fail(VTMU_ERR_INVALID, "decode_step: pointers must be 4-byte aligned");
+    const int64_t wk = (int64_t)a.Hk * a.D, wv = (int64_t)a.Hk * a.Dv;
+    const size_t kc_b = (size_t)(max_rows * wk) * 4, vc_b = (size_t)(max_rows * wv) * 4;
+    const size_t kn_b = (size_t)(new_rows * wk) * 4, vn_b = (size_t)(new_rows * wv) * 4;
+    if (overlaps(k_cache, kc_b, v_cache, vc_b)) return fail(VTMU_ERR_INVALID, "decode_step: the caches overlap");
+    if (overlaps(k_new, kn_b, k_cache, kc_b) || overlaps(k_new, kn_b, v_cache, vc_b) ||
+        overlaps(v_new, vn_b, k_cache, kc_b) || overlaps(v_new, vn_b, v_cache, vc_b))
+        return fail(VTMU_ERR_INVALID, "decode_step: new rows overlap a cache");
+    if (out && (overlaps(out, (size_t)a.T * a.H * a.Dv * 4, k_cache, kc_b) ||
+                overlaps(out, (size_t)a.T * a.H * a.Dv * 4, v_cache, vc_b)))
+        return fail(VTMU_ERR_INVALID, "decode_step: out overlaps a cache");
+    vtmu::DecodeCacheWrite cw{k_cache, v_cache, k_new, v_new, offset, offset + new_rows};
+    return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes, stream, &cw);
 }
 
 vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width, const float* values, int64_t rows,

@@ -151,6 +151,32 @@ VTMU_API vtmu_status vtmu_attention(const float* q, const float* k, const float*
                            size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * A decode step of a KV-cached model: op "cache_write" of k_new into k_cache
+ * and of v_new into v_cache at row `offset`, then op "attention" of q over the
+ * updated caches (vtmu.mpakt.dev/api/ops: a whole decode step is meant to run
+ * without leaving the worker).  The result equals vtmu_cache_write(k_cache,
+ * ...), vtmu_cache_write(v_cache, ...), vtmu_attention(q, k_cache, v_cache,
+ * bias, out, p, ...) in that order; when the decode kernel covers the call
+ * (T == 1, same shape table as VTMU_KERNEL_DECODE) all three run as one
+ * launch: the CTA that reads a new row takes it from k_new / v_new and writes
+ * it to the cache itself.
+ *   k_cache [max_rows, kvHeads*headDim], v_cache [max_rows, kvHeads*vHeadDim]:
+ *     DEVICE, updated in place; the attention reads their first p->S rows
+ *     (p->S <= max_rows).
+ *   k_new [new_rows, kvHeads*headDim], v_new [new_rows, kvHeads*vHeadDim]:
+ *     DEVICE, must not overlap a cache; new_rows == 0 skips the writes.
+ *   q, bias, out, p, workspace: as for vtmu_attention.
+ * Errors: those of vtmu_attention, plus VTMU_ERR_RANGE (offset < 0 or
+ * offset + new_rows > max_rows), VTMU_ERR_INVALID (p->S > max_rows, NULL or
+ * overlapping cache / new-row buffers).
+ */
+VTMU_API vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows,
+                                      const float* k_new, const float* v_new, int64_t new_rows,
+                                      int64_t offset, const float* q, const float* bias, float* out,
+                                      const vtmu_attention_params* p, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * op "cache_write" (vtmu.mpakt.dev/api/ops): cache[offset + r, :] =
  * values[r, :] for 0 <= r < rows, bit-exact, in place; rows outside
  * [offset, offset + rows) are untouched.  cache [max_rows, width] and values

@@ -262,3 +262,66 @@ def test_no_bounded_wait_gave_up():
     x = si.attention_inputs(1, 4096, 16, 4, 128, 128, 91)
     check(x, dict(heads=16, headDim=128, kvHeads=4, posOffset=4095, kernel=DECODE))
     assert vtmu.vtmu_device_error() == 0
+
+
+# ----------------------------------------------------------- fused decode step
+def _decode_step_case(S, H, Hk, D, new_rows, offset, seed, T=1, **params):
+    g = si.Stream(seed)
+    x = {
+        "q": g.normal_f32(T * H * D).reshape(T, H * D),
+        "kc": g.normal_f32(S * Hk * D).reshape(S, Hk * D),
+        "vc": g.normal_f32(S * Hk * D).reshape(S, Hk * D),
+        "kn": g.normal_f32(new_rows * Hk * D).reshape(new_rows, Hk * D),
+        "vn": g.normal_f32(new_rows * Hk * D).reshape(new_rows, Hk * D),
+    }
+    Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
+    out = vtmu.decode_step(Kc, Vc, to_dev(x["kn"]), to_dev(x["vn"]), offset, to_dev(x["q"]), heads=H,
+                           headDim=D, kvHeads=Hk, **params)
+    torch.cuda.synchronize()
+    oracle.cache_write(x["kc"], x["kn"], offset)
+    oracle.cache_write(x["vc"], x["vn"], offset)
+    assert Kc.cpu().numpy().tobytes() == x["kc"].tobytes(), "K cache differs"
+    assert Vc.cpu().numpy().tobytes() == x["vc"].tobytes(), "V cache differs"
+    pos = params.get("posOffset", offset + new_rows - T)
+    ref = oracle.attention(x["q"], x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk,
+                           **dict(oracle_params(params), posOffset=pos))
+    err = max_err(out.cpu().numpy(), ref)
+    assert err <= TOL, err
+
+
+def test_decode_step_workload():
+    """The decode workload as one fused launch: cache_write of one row at 32767
+    into both [32768, 1024] caches, then attention over all 32768 keys."""
+    _decode_step_case(32768, 32, 8, 128, 1, 32767, 1)
+
+
+@pytest.mark.parametrize("case", [
+    dict(S=4000, H=16, Hk=4, D=128, new_rows=1, offset=2222),                  # mid-split row
+    dict(S=4000, H=16, Hk=4, D=128, new_rows=5, offset=1278, decode_splits=7),  # rows across a split edge
+    dict(S=3000, H=8, Hk=4, D=64, new_rows=3, offset=2990, posOffset=2500),     # new rows not visible
+    dict(S=3000, H=8, Hk=1, D=32, new_rows=2, offset=100, posOffset=2999, window=700),  # outside the window
+    dict(S=2048, H=16, Hk=8, D=64, new_rows=1, offset=1000, causal=False, window=300),
+    dict(S=1500, H=8, Hk=1, D=128, new_rows=1, offset=1499, softcap=30.0, alibi=True),
+])
+def test_decode_step_fused_cases(case):
+    case = dict(case)
+    _decode_step_case(case.pop("S"), case.pop("H"), case.pop("Hk"), case.pop("D"), case.pop("new_rows"),
+                      case.pop("offset"), 500, kernel=DECODE, **case)
+
+
+def test_decode_step_unfused_paths():
+    """Shapes outside the decode kernel: chunked prefill (T = 6) and a head
+    size the decode table does not cover run as three launches."""
+    _decode_step_case(700, 4, 2, 128, 6, 600, 501, T=6)
+    _decode_step_case(700, 4, 4, 96, 1, 650, 502)
+
+
+def test_decode_step_refuses_rows_past_the_cache():
+    Kc = torch.zeros((8, 4), device="cuda")
+    Vc = torch.zeros((8, 4), device="cuda")
+    with pytest.raises(vtmu.VtmuError) as e:
+        vtmu.decode_step(Kc, Vc, torch.ones((2, 4), device="cuda"), torch.ones((2, 4), device="cuda"), 7,
+                         torch.zeros((1, 8), device="cuda"), heads=2, headDim=4, kvHeads=1)
+    assert e.value.status == vtmu.VTMU_ERR_RANGE
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Kc).item() == 0 and torch.count_nonzero(Vc).item() == 0
