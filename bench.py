@@ -364,16 +364,23 @@ def run_vtmu(args, rank, world, local):
     barrier(world)
     torch.cuda.synchronize(dev)
     for i in range(args.steps):
-        sev[i][0].record(stream)
+        if flush is not None or i == 0:
+            sev[i][0].record(stream)
         step(i, kev[i])
-        sev[i][1].record(stream)
+        if flush is not None or i == args.steps - 1:
+            sev[i][1].record(stream)
         if flush is not None:
             with torch.cuda.stream(stream):
                 flush.zero_()
     torch.cuda.synchronize(dev)
     barrier(world)
     sampler.mark_end()
-    step_ms = sum(a.elapsed_time(b) for a, b in sev) / args.steps
+    if flush is None:
+        # No flush between steps: the whole run, gaps between launches included.
+        step_ms = sev[0][0].elapsed_time(sev[-1][1]) / args.steps
+    else:
+        # L2 flushed between steps: sum of the steps, flushes excluded.
+        step_ms = sum(a.elapsed_time(b) for a, b in sev) / args.steps
     kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
     step_ms = max_over_ranks(step_ms, world)
 

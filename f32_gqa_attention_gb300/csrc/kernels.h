@@ -43,6 +43,14 @@ unsigned int decode_take_device_error();
 bool prefill_ffma_supported(const AttnDesc& a);
 cudaError_t launch_prefill_ffma(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream);
 
+// ---- tcgen05 3xTF32 prefill ---------------------------------------------------
+// headDim == vHeadDim in {32, 64, 96, 128}, q and out 16-byte aligned.
+bool prefill_tc_supported(const AttnDesc& a);
+// Scratch for the tf32 hi/lo copies of K and of V transposed.
+size_t prefill_tc_workspace(const AttnDesc& a);
+cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* workspace, cudaStream_t stream);
+unsigned int tc_take_device_error();
+
 // ---- cache_write --------------------------------------------------------------
 cudaError_t launch_cache_write(float* cache, int64_t width, const float* values, int64_t rows,
                                int64_t offset, cudaStream_t stream);

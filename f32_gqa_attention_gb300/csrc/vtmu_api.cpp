@@ -88,6 +88,10 @@ int device_sm_count() {
     return cached[dev];
 }
 
+// Query rows from which AUTO prefers the tensor-core prefill (one 128-row
+// MMA tile is then at least half full).
+constexpr int64_t kTcMinRows = 64;
+
 struct Resolved {
     vtmu::AttnDesc a;
     int kernel;  // resolved vtmu_kernel (never AUTO)
@@ -156,7 +160,12 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
 
     int kernel = p->kernel;
     if (kernel == VTMU_KERNEL_AUTO) {
-        kernel = (a.T == 1 && vtmu::decode_supported(a)) ? VTMU_KERNEL_DECODE : VTMU_KERNEL_PREFILL_FFMA;
+        if (a.T == 1 && vtmu::decode_supported(a))
+            kernel = VTMU_KERNEL_DECODE;
+        else if (a.T >= kTcMinRows && vtmu::prefill_tc_supported(a))
+            kernel = VTMU_KERNEL_PREFILL_TF32X3;
+        else
+            kernel = VTMU_KERNEL_PREFILL_FFMA;
     } else if (kernel == VTMU_KERNEL_DECODE) {
         if (a.T != 1) return fail(VTMU_ERR_INVALID, "kernel DECODE needs T == 1 (got %lld)", (long long)a.T);
         if (!vtmu::decode_supported(a))
@@ -165,7 +174,11 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
                         "heads/kvHeads in {2,4,8} (got headDim %d, vHeadDim %d, group %d)",
                         a.D, a.Dv, a.G);
     } else if (kernel == VTMU_KERNEL_PREFILL_TF32X3) {
-        return fail(VTMU_ERR_UNSUPPORTED, "kernel PREFILL_TF32X3 is not available in this build");
+        if (!vtmu::prefill_tc_supported(a))
+            return fail(VTMU_ERR_UNSUPPORTED,
+                        "kernel PREFILL_TF32X3 covers headDim == vHeadDim in {32,64,96,128} with S >= 1 "
+                        "(got headDim %d, vHeadDim %d, S %lld)",
+                        a.D, a.Dv, (long long)a.S);
     }
     r->kernel = kernel;
     return VTMU_OK;
@@ -215,7 +228,9 @@ vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t
     Resolved r;
     vtmu_status st = resolve(p, &r);
     if (st != VTMU_OK) return st;
-    *bytes = (r.kernel == VTMU_KERNEL_DECODE) ? decode_workspace(r.a) : 0;
+    *bytes = r.kernel == VTMU_KERNEL_DECODE         ? decode_workspace(r.a)
+             : r.kernel == VTMU_KERNEL_PREFILL_TF32X3 ? vtmu::prefill_tc_workspace(r.a)
+                                                      : 0;
     return ok();
 }
 
@@ -288,6 +303,24 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
         vtmu::decode_plan(a, p->decode_splits, device_sm_count(), &plan);
         e = vtmu::launch_decode(a, alibi, plan, workspace, stream, cw);
         if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+        return ok();
+    }
+    if (r.kernel == VTMU_KERNEL_PREFILL_TF32X3 && !vtmu::prefill_tc_supported(a)) {
+        if (p->kernel == VTMU_KERNEL_PREFILL_TF32X3)
+            return fail(VTMU_ERR_UNSUPPORTED, "kernel PREFILL_TF32X3 needs 16-byte aligned q and out");
+        r.kernel = VTMU_KERNEL_PREFILL_FFMA;
+    }
+    if (r.kernel == VTMU_KERNEL_PREFILL_TF32X3) {
+        const size_t need = vtmu::prefill_tc_workspace(a);
+        if (!workspace || workspace_bytes < need)
+            return fail(VTMU_ERR_WORKSPACE, "tensor-core prefill needs a workspace of %zu bytes (got %zu)", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        e = write_caches();
+        if (e != cudaSuccess) return cuda_fail(e, "cache_write launch");
+        e = vtmu::launch_prefill_tc(a, alibi, workspace, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core prefill launch");
         return ok();
     }
     if (!vtmu::prefill_ffma_supported(a)) return fail(VTMU_ERR_UNSUPPORTED, "shape not covered by the prefill kernel");
@@ -379,7 +412,7 @@ vtmu_status vtmu_device_error(unsigned int* flags) {
     *flags = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device_error: synchronize");
-    *flags = vtmu::decode_take_device_error();
+    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error();
     return ok();
 }
 

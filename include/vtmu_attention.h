@@ -78,7 +78,9 @@ typedef enum vtmu_bias_kind {
 } vtmu_bias_kind;
 
 /* Kernel choice.  AUTO takes the split-KV decode kernel for T == 1 (when its
- * shape table covers headDim/vHeadDim/group size) and the prefill kernel
+ * shape table covers headDim/vHeadDim/group size), the tcgen05 3xTF32
+ * prefill for T >= 64 when it covers the shape (headDim == vHeadDim in
+ * {32, 64, 96, 128}, 16-byte aligned q and out), and the FFMA prefill
  * otherwise.  The others force one kernel, for tests and measurement. */
 typedef enum vtmu_kernel {
     VTMU_KERNEL_AUTO = 0,
@@ -119,9 +121,11 @@ typedef struct vtmu_attention_params {
 VTMU_API void vtmu_attention_params_init(vtmu_attention_params* p);
 
 /*
- * Scratch bytes that vtmu_attention needs for `p` (0 for the prefill
- * kernels).  The decode kernel keeps per-split partial results (running max,
- * sum and unnormalised output) and one arrival counter per KV head there.
+ * Scratch bytes that vtmu_attention needs for `p` (0 for the FFMA prefill).
+ * The decode kernel keeps per-split partial results (running max, sum and
+ * unnormalised output) and one arrival counter per KV head there; the
+ * tensor-core prefill keeps the tf32 hi/lo halves of K and of V transposed
+ * (4 * S * kvHeads * headDim floats).
  * Returns VTMU_ERR_INVALID / VTMU_ERR_UNSUPPORTED for parameters that
  * vtmu_attention would refuse.
  */
@@ -226,7 +230,9 @@ VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, const float* 
  * every kernel in *flags (0: no wait gave up since the last call) and clears
  * them.  Decode bits: 1 = a consumer gave up on a loaded stage, 2 = the
  * producer gave up on a free stage, 4 = the producer gave up draining its
- * copies.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
+ * copies; tensor-core prefill bits: 0x100 stage load, 0x200 free stage,
+ * 0x400 drain, 0x800 query load, 0x1000 score tile, 0x2000 probabilities,
+ * 0x4000 P.V product.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
  */
 VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
 

@@ -136,8 +136,23 @@ def test_decode_needs_its_workspace(lib):
     assert e.status == vtmu.VTMU_ERR_WORKSPACE and "256-byte" in str(e)
 
 
-def test_prefill_needs_no_workspace(lib):
-    assert vtmu.vtmu_attention_workspace_size(vtmu.make_params(64, 64, heads=4, headDim=64)) == 0
+def test_ffma_prefill_needs_no_workspace(lib):
+    p = vtmu.make_params(64, 64, heads=4, headDim=64, kernel=vtmu.VTMU_KERNEL_PREFILL_FFMA)
+    assert vtmu.vtmu_attention_workspace_size(p) == 0
+    assert vtmu.vtmu_attention_workspace_size(vtmu.make_params(16, 16, heads=4, headDim=32)) == 0
+
+
+def test_tensor_core_prefill_workspace_holds_the_split_operands(lib):
+    S, Hk, D = 1000, 2, 128
+    p = vtmu.make_params(256, S, heads=4, headDim=D, kvHeads=Hk)  # AUTO picks the tcgen05 prefill
+    assert vtmu.vtmu_attention_workspace_size(p) >= 4 * S * Hk * D * 4
+
+
+@host_only
+def test_tensor_core_prefill_shape_table(lib):
+    p = vtmu.make_params(256, 256, heads=4, headDim=256, kernel=vtmu.VTMU_KERNEL_PREFILL_TF32X3)
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "PREFILL_TF32X3" in str(e)
 
 
 @host_only

@@ -325,3 +325,65 @@ def test_decode_step_refuses_rows_past_the_cache():
     assert e.value.status == vtmu.VTMU_ERR_RANGE
     torch.cuda.synchronize()
     assert torch.count_nonzero(Kc).item() == 0 and torch.count_nonzero(Vc).item() == 0
+
+
+# ------------------------------------------------------ tcgen05 3xTF32 prefill
+TC = vtmu.VTMU_KERNEL_PREFILL_TF32X3
+
+
+def _tc_case(seed):
+    g = np.random.default_rng(7000 + seed)
+    H, Hk = [(1, 1), (4, 1), (4, 2), (6, 3), (8, 8), (8, 2)][seed % 6]
+    D = int(g.choice([32, 64, 96, 128]))
+    T = int(g.integers(1, 300))
+    S = int(g.integers(1, 500))
+    params = dict(heads=H, headDim=D, kvHeads=Hk, causal=bool(g.integers(0, 4) > 0),
+                  posOffset=int(g.choice([0, 5, max(S - T, 0), S + 7])))
+    if g.random() < 0.4:
+        params["window"] = int(g.integers(1, 120))
+    if g.random() < 0.3:
+        params["softcap"] = float(g.choice([5.0, 30.0, 50.0]))
+    if g.random() < 0.3:
+        params["scale"] = float(g.uniform(0.02, 0.5))
+    r = g.random()
+    if r < 0.2:
+        params["alibi"] = True
+    elif r < 0.3:
+        params["alibiMax"] = 8.0
+    bias = None if g.random() < 0.6 else str(g.choice(["ts", "hts"]))
+    x = si.attention_inputs(T, S, H, Hk, D, D, 50 + seed, sigma=float(g.choice([1.0, 2.0])), bias=bias,
+                            bias_mask_p=0.1 if bias else 0.0)
+    if bias is not None:
+        b = x["bias"]
+        b[b == np.float32(-1e9)] = np.float32(-30.0)
+    return x, params
+
+
+@pytest.mark.parametrize("seed", range(36))
+def test_tensor_core_prefill_random_sweep(seed):
+    x, params = _tc_case(seed)
+    check(x, dict(params, kernel=TC))
+
+
+@pytest.mark.parametrize("T,S,pos", [(128, 128, 0), (129, 64, 0), (1, 40, 39), (300, 1, 0), (257, 1000, 743)])
+def test_tensor_core_prefill_tile_edges(T, S, pos):
+    x = si.attention_inputs(T, S, 4, 2, 128, 128, 61)
+    check(x, dict(heads=4, headDim=128, kvHeads=2, posOffset=pos, kernel=TC))
+
+
+def test_tensor_core_prefill_masked_rows_give_zeros():
+    x = si.attention_inputs(140, 50, 2, 1, 64, 64, 62, bias="ts")
+    x["bias"][:, ::3] = -np.inf
+    x["bias"][7, :] = -np.inf
+    x["bias"][139, :] = -np.inf
+    out, _ = check(x, dict(heads=2, headDim=64, kvHeads=1, causal=False, kernel=TC))
+    assert np.array_equal(out[7], np.zeros_like(out[7])) and np.array_equal(out[139], np.zeros_like(out[139]))
+
+
+def test_tensor_core_prefill_agrees_with_ffma():
+    x = si.attention_inputs(512, 512, 8, 2, 128, 128, 63)
+    params = dict(heads=8, headDim=128, kvHeads=2, window=200, softcap=30.0)
+    a = gpu_attention(x["q"], x["k"], x["v"], kernel=TC, **params)
+    b = gpu_attention(x["q"], x["k"], x["v"], kernel=FFMA, **params)
+    assert max_err(a, b) <= 5e-5
+    assert vtmu.vtmu_device_error() == 0
