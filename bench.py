@@ -313,6 +313,7 @@ def run_vtmu(args, rank, world, local):
         work_per_step, unit = step_bytes / 1e9, "GB/s"
         kernel_tag, kernel_work, kernel_unit = "decode", step_bytes, "GB/s"
         bound, peak = "hbm", float(peaks["hbm_gbs"])
+        peak_note = peak_kind
         flush = None
         l2_note = "inputs > L2: two 256 MiB K/V cache sets alternate between steps"
     else:
@@ -327,14 +328,20 @@ def run_vtmu(args, rank, world, local):
             out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
             flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         bias_kind = vtmu.VTMU_BIAS_NONE if b is None else (vtmu.VTMU_BIAS_TS if b.dim() == 2 else vtmu.VTMU_BIAS_HTS)
+        tc_ok = D == Dv and D in (32, 64, 96, 128) and T >= 64
+        use_tc = tc_ok if args.kernel == "auto" else args.kernel == "tc"
+        kernel = vtmu.VTMU_KERNEL_PREFILL_TF32X3 if use_tc else vtmu.VTMU_KERNEL_PREFILL_FFMA
         p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, vHeadDim=w.get("vHeadDim"),
-                             bias_kind=bias_kind, **w["params"])
-        launches_per_step = 1
+                             bias_kind=bias_kind, kernel=kernel, **w["params"])
+        ws_bytes = vtmu.vtmu_attention_workspace_size(p)
+        ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+        # one launch per step (+2 split passes of K and V for the tensor-core kernel)
+        launches_per_step = 3 if use_tc else 1
 
         def step(i, ev=None):
             if ev is not None:
                 ev[0].record(stream)
-            vtmu.vtmu_attention(q, k, v, b, out, p, None, 0, st)
+            vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
             if ev is not None:
                 ev[1].record(stream)
 
@@ -342,9 +349,17 @@ def run_vtmu(args, rank, world, local):
 
         flops = prefill_flops(w)
         work_per_step, unit = flops / 1e12, "TFLOP/s"
-        kernel_tag, kernel_work, kernel_unit = "prefill_ffma", flops / 1e12, "TFLOP/s"
-        clk = float(peaks.get("sm_max_mhz", 2070.0))
-        bound, peak = "alu", SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+        kernel_work, kernel_unit = flops / 1e12, "TFLOP/s"
+        if use_tc:
+            # 3xTF32: three tf32 products per f32 product on the tensor pipe.
+            kernel_tag, bound = "prefill_tc", "tensor"
+            peak = float(peaks["bf16_tflops"]) * (1.1 / 2.25) / 3.0
+            peak_note = "measured bf16 burst x 1.1/2.25 (tf32/bf16 nominal) / 3 (3xTF32 products)"
+        else:
+            clk = float(peaks.get("sm_max_mhz", 2070.0))
+            kernel_tag, bound = "prefill_ffma", "alu"
+            peak = SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
+            peak_note = "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
         l2_note = "L2 flushed between timed steps (256 MiB write, outside the timed events)"
 
     sampler = ClockSampler(local)
@@ -432,7 +447,7 @@ def run_vtmu(args, rank, world, local):
                 v.copy_(vh, non_blocking=True)
                 if bh is not None:
                     b.copy_(bh, non_blocking=True)
-            vtmu.vtmu_attention(q, k, v, b, out, p, None, 0, st)
+            vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
             with torch.cuda.stream(stream):
                 outh.copy_(out, non_blocking=True)
             stream.synchronize()
@@ -458,7 +473,7 @@ def run_vtmu(args, rank, world, local):
         achieved = kernel_work / (kern_ms / 1e3)
     traffic = profile_traffic(kernel_tag + "__" + name)
     roofline = {"bound": bound, "kernel": kernel_tag, "achieved": round(achieved, 3), "peak": round(peak, 1),
-                "peak_source": peak_kind if bound != "alu" else "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock",
+                "peak_source": peak_note,
                 "unit": kernel_unit, "frac": round(achieved / peak, 4), "traffic": traffic,
                 "kernel_ms": round(kern_ms, 5)}
 
@@ -523,6 +538,8 @@ def main():
     ap.add_argument("--workload", choices=sorted(si.WORKLOADS), default="gqa_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--kernel", choices=["auto", "tc", "ffma"], default="auto",
+                    help="prefill kernel: tcgen05 3xTF32 or FFMA (auto: tcgen05 where it covers the shape)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -488,6 +488,7 @@ bool decode_supported(const AttnDesc& a) {
     if (!(a.D == 32 || a.D == 64 || a.D == 128)) return false;
     if (!(a.G == 2 || a.G == 4 || a.G == 8)) return false;
     if (a.S >= ((int64_t)1 << 31)) return false;
+    if (a.Hk > kMaxDecodeKvHeads) return false;
     return true;
 }
 
@@ -526,9 +527,9 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
     plan->splits = (int32_t)n;
     const size_t H = (size_t)a.H, Sp = (size_t)n;
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
-    // Arrival counters first (fixed place, so they stay zero between calls
-    // of any shape), then m, l and o partials.
-    plan->workspace_bytes = up((size_t)a.Hk * 4) + up(H * Sp * 4) * 2 + up(H * Sp * (size_t)a.Dv * 4);
+    // Arrival counters in the workspace header (fixed place, so they stay
+    // zero between calls of any shape), then m, l and o partials.
+    plan->workspace_bytes = kWorkspaceHeader + up(H * Sp * 4) * 2 + up(H * Sp * (size_t)a.Dv * 4);
 }
 
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
@@ -545,7 +546,7 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
     const size_t H = (size_t)a.H, Sp = (size_t)plan.splits;
     char* w = static_cast<char*>(workspace);
     args.counters = reinterpret_cast<unsigned int*>(w);
-    w += up((size_t)a.Hk * 4);
+    w += kWorkspaceHeader;
     args.part_m = reinterpret_cast<float*>(w);
     args.part_l = reinterpret_cast<float*>(w + up(H * Sp * 4));
     args.part_o = reinterpret_cast<float*>(w + 2 * up(H * Sp * 4));

@@ -9,6 +9,13 @@
 
 namespace vtmu {
 
+// Every workspace starts with this header, which only the decode kernel's
+// arrival counters use (one per KV head, zero between calls).  Other
+// kernels keep their scratch after it, so the counters survive any mix of
+// calls on one workspace.
+constexpr size_t kWorkspaceHeader = 64 * 1024;
+constexpr int kMaxDecodeKvHeads = (int)(kWorkspaceHeader / 4);
+
 // ---- split-KV decode (T == 1) ---------------------------------------------
 struct DecodePlan {
     int64_t s_lo = 0;            // first visible key

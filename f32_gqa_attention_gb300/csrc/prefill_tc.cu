@@ -439,7 +439,7 @@ TcLayout tc_layout(const AttnDesc& a) {
     L.s_pad = (a.S + 3) / 4 * 4;
     L.k_bytes = up256((size_t)a.S * a.Hk * a.D * sizeof(float));
     L.vt_bytes = up256((size_t)a.Hk * a.Dv * L.s_pad * sizeof(float));
-    L.total = 2 * L.k_bytes + 2 * L.vt_bytes;
+    L.total = kWorkspaceHeader + 2 * L.k_bytes + 2 * L.vt_bytes;
     return L;
 }
 
@@ -475,7 +475,7 @@ size_t prefill_tc_workspace(const AttnDesc& a) { return tc_layout(a).total; }
 
 cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* workspace, cudaStream_t stream) {
     const TcLayout L = tc_layout(a);
-    char* w = static_cast<char*>(workspace);
+    char* w = static_cast<char*>(workspace) + kWorkspaceHeader;  // the header is the decode kernel's
     float* khi = reinterpret_cast<float*>(w);
     float* klo = reinterpret_cast<float*>(w + L.k_bytes);
     float* vthi = reinterpret_cast<float*>(w + 2 * L.k_bytes);

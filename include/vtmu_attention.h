@@ -136,10 +136,12 @@ VTMU_API vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* 
  * above, 4-byte aligned.  bias: DEVICE or NULL, must be non-NULL exactly when
  * p->bias_kind != VTMU_BIAS_NONE.  out must not overlap an input.
  * workspace: DEVICE, at least vtmu_attention_workspace_size() bytes (may be
- * NULL when that is 0), 256-byte aligned, ZERO-FILLED BEFORE ITS FIRST USE;
- * each call leaves its arrival counters at zero again, so a workspace is
- * reused without clearing.  Calls that share a workspace must not overlap on
- * the GPU (use one workspace per concurrent stream).
+ * NULL when that is 0), 256-byte aligned.  Its first 64 KiB hold the decode
+ * kernel's arrival counters and must be ZERO before the first decode call;
+ * every call leaves them zero again and no kernel writes scratch there, so a
+ * workspace is reused across calls of any kind and shape without clearing.
+ * Calls that share a workspace must not overlap on the GPU (use one
+ * workspace per concurrent stream).
  *
  * Errors: VTMU_ERR_INVALID (null pointer, T/S < 0, heads <= 0, heads not a
  * multiple of kv_heads, window < 0, softcap < 0 or not finite, scale not
@@ -208,7 +210,7 @@ VTMU_API vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t wi
  *  - Limit: a call whose decode scratch (vtmu_attention_workspace_size with
  *    kernel = VTMU_KERNEL_DECODE) exceeds VTMU_NOALLOC_SCRATCH_BYTES is
  *    refused with VTMU_ERR_WORKSPACE (over 16384 visible keys at vHeadDim
- *    128 that leaves room for up to 63 query heads).
+ *    128 that leaves room for up to 62 query heads).
  *  - The first call on each device looks up the array's device address
  *    (cudaGetSymbolAddress, with that device current) and caches it; make
  *    that first call before any stream capture.

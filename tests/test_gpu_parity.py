@@ -151,15 +151,17 @@ def test_decode_workspace_reused_across_shapes():
     """Arrival counters return to zero: calls of different shapes in a row on
     one workspace stay correct."""
     ws = vtmu.Workspace()
-    for i, (S, H, Hk, D) in enumerate([(3000, 16, 4, 128), (700, 8, 4, 64), (3000, 16, 4, 128),
-                                        (64, 8, 1, 32)]):
-        x = si.attention_inputs(1, S, H, Hk, D, D, 300 + i)
-        params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=S - 1)
+    # (T, S, H, Hk, D): decode calls interleaved with tensor-core prefills,
+    # whose scratch shares the workspace.
+    for i, (T, S, H, Hk, D) in enumerate([(1, 3000, 16, 4, 128), (256, 700, 8, 4, 64), (1, 700, 8, 4, 64),
+                                           (1, 3000, 16, 4, 128), (128, 3000, 16, 4, 128), (1, 64, 8, 1, 32)]):
+        x = si.attention_inputs(T, S, H, Hk, D, D, 300 + i)
+        params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=S - T)
         out = vtmu.attention(to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"]), workspace=ws, **params)
         torch.cuda.synchronize()
         ref = oracle.attention(x["q"], x["k"], x["v"], **params)
-        assert max_err(out.cpu().numpy(), ref) <= TOL
-    assert torch.count_nonzero(ws.buf[:64]).item() == 0  # counters back at zero
+        assert max_err(out.cpu().numpy(), ref) <= TOL, (T, S, H, Hk, D)
+    assert torch.count_nonzero(ws.buf[:65536]).item() == 0  # counters back at zero
 
 
 def test_decode_equals_last_prefill_row():
