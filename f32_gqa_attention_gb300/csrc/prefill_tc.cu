@@ -78,6 +78,33 @@ struct TcCfg {
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
+// The fused score epilogue over one 32-key tile of one query row, in base 2:
+// scale (or softcap), ALiBi, bias, then the mask -- slots outside
+// [lo_i, hi_i] become -inf.  `full` tiles skip the mask.  Features are
+// template flags so that each combination compiles to straight-line code.
+template <bool SOFTCAP, bool ALIBI, bool BIAS>
+__device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[32], float slope, int rel0,
+                                              const float* bias, int lo_i, int hi_i, bool full) {
+    if (full) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
+            if (BIAS) v = fmaf(__ldg(bias + i), kLog2e, v);
+            x[i] = v;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const bool vis = i >= lo_i && i <= hi_i;
+            float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
+            if (BIAS) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
+            x[i] = vis ? v : -INFINITY;
+        }
+    }
+}
+
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_khi,
@@ -251,7 +278,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&q_ready);
         }
-        // Keys this row can see.
+        // Keys this row can see: one contiguous range [lo_t, hi_t] (empty for
+        // padding rows past T).
         const int64_t p = a.pos_offset + t;
         int64_t lo_t = 0, hi_t = a.S - 1;
         if (a.causal) {
@@ -261,9 +289,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             lo_t = p - a.window;
             if (p + a.window < hi_t) hi_t = p + a.window;
         }
+        if (!row_ok) {
+            lo_t = 1;
+            hi_t = 0;
+        }
         const float* brow = a.bias_kind == 0 ? nullptr
                             : a.bias_kind == 1 ? a.bias + t * a.S
                                                : a.bias + ((int64_t)h * a.T + t) * a.S;
+        const int feat = (a.softcap_on ? 1 : 0) | (a.alibi_on ? 2 : 0) | (a.bias_kind ? 4 : 0);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
@@ -277,17 +310,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(trow + C::S0 + (uint32_t)(j & 1) * kBN, x);
             tmem_wait_ld();
             const int64_t n0 = (jt_begin + j) * kBN;
-            const bool full = row_ok && n0 >= lo_t && n0 + kBN - 1 <= hi_t;
+            // Visible slots of this tile, clamped to [-1, 32].
+            int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
+            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > 32 ? 32 : lo64));
+            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > 32 ? 32 : hi64));
+            const bool full = lo_i <= 0 && hi_i >= kBN - 1;
+            const int rel0 = (int)(n0 - p);  // s - p of slot 0
+            const float* bt = brow ? brow + n0 : nullptr;
+            switch (feat) {
+                case 0: tile_epilogue<false, false, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 1: tile_epilogue<true, false, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 2: tile_epilogue<false, true, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 3: tile_epilogue<true, true, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 4: tile_epilogue<false, false, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 5: tile_epilogue<true, false, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                case 6: tile_epilogue<false, true, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+                default: tile_epilogue<true, true, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
+            }
             float mt = -INFINITY;
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int64_t s = n0 + i;
-                float v = -INFINITY;
-                if (full || (row_ok && key_visible(a, p, s)))
-                    v = score_log2(a, x[i], slope, s - p, brow ? __ldg(brow + s) : 0.f);
-                x[i] = v;
-                mt = fmaxf(mt, v);
-            }
+            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
             // Lazy rescale: keep the reference max unless this tile beats it by > 2^8.
             float alpha = 1.f;
             if (mt > m_ref + kRescaleLog2) {
@@ -467,7 +509,8 @@ bool prefill_tc_supported(const AttnDesc& a) {
     const bool dims = (a.D == 32 || a.D == 64 || a.D == 96 || a.D == 128) && a.Dv == a.D;
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
     const bool q_aligned = (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
-    return dims && a.T >= 1 && a.S >= 1 && a.S < ((int64_t)1 << 31) && (a.T + kBM - 1) / kBM < (1 << 30) &&
+    return dims && a.T >= 1 && a.S >= 1 && a.S < ((int64_t)1 << 31) && a.pos_offset + a.T < ((int64_t)1 << 31) &&
+           (a.T + kBM - 1) / kBM < (1 << 30) &&
            (a.out == nullptr || out_aligned) && (a.q == nullptr || q_aligned);
 }
 
