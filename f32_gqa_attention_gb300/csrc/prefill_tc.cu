@@ -14,18 +14,25 @@
 //    own layout and V^T_hi / V^T_lo transposed to [kvHeads*vHeadDim, S],
 //    so every tile the MMAs read is K-major;
 //  * one CTA owns 128 query rows of one head (the MMA M); per key tile of
-//    BN = 32 keys:
-//      S_j  = Q K_j^T          (TMEM accumulator, double buffered)
+//    BN = 64 keys:
+//      S_j  = Q K_j^T          (TMEM accumulator, M=128 x N=64)
 //      P_j  = softmax part     (4 warps; thread = query row = TMEM lane)
-//      O   += P_j V_j          (TMEM accumulator)
-//  * warp 0 issues TMA loads of the K/V hi/lo tiles into a 3-stage ring;
+//      O   += P_j V_j          (TMEM accumulator, M=128 x N=vHeadDim)
+//    A kind::tf32 MMA takes at least ~46 cycles to issue whatever its N, so
+//    the score MMAs use N = 64 (70 % of the tensor rate; N = 32 reaches 35 %);
+//  * warp 0 issues TMA loads: a 2-deep ring of K hi/lo tiles and one V^T
+//    hi/lo tile (V_j is needed only after the softmax of tile j, so one
+//    buffer, refilled as soon as P.V_j completes, keeps it ahead);
 //    warp 1 owns TMEM and one of its threads issues every MMA; warps 2-5
 //    load Q (split into TMEM), run the fused epilogue and online softmax
 //    (base 2, rescaling O only when a row max grows by more than 2^8),
 //    write P hi/lo into TMEM and finally normalise and store O;
 //  * Q hi/lo and P hi/lo live in TMEM (the MMA's A operand), K and V^T in
 //    shared memory (B operand, 128-byte swizzled).  TMEM columns:
-//    Q_hi | Q_lo | O | S0 | S1 | P_hi | P_lo = 2D + Dv + 4*32 <= 512.
+//    Q_hi | Q_lo | O | S (= P_hi) | P_lo = 2D + Dv + 2*64 <= 512.
+//    P_hi of tile j overwrites S_j once the scores are in registers; the
+//    MMAs of one thread execute in issue order, so S_{j+1} (issued after
+//    P.V_j) overwrites it only after P.V_j has read it.
 //
 // Every wait is bounded (tma_sync.cuh); a wait that gives up sets a bit of
 // g_tc_device_error and the kernel unwinds.
@@ -47,8 +54,7 @@ __device__ unsigned int g_tc_device_error;
 namespace {
 
 constexpr int kBM = 128;      // query rows per CTA = MMA M = TMEM lanes
-constexpr int kBN = 32;       // keys per tile
-constexpr int kStages = 3;    // K/V ring depth
+constexpr int kBN = 64;       // keys per tile = score MMA N
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
 
@@ -65,29 +71,55 @@ enum TcError : unsigned int {
 template <int D, int DV>
 struct TcCfg {
     static constexpr int KB = D / 32;                    // 32-float K sub-tiles
-    static constexpr int K_FLOATS = kBN * D;             // one K tile (hi or lo)
-    static constexpr int V_FLOATS = DV * kBN;            // one V^T tile (hi or lo)
-    static constexpr int STAGE_FLOATS = 2 * K_FLOATS + 2 * V_FLOATS;
-    static constexpr uint32_t STAGE_BYTES = STAGE_FLOATS * sizeof(float);
-    static constexpr size_t SMEM = (size_t)kStages * STAGE_BYTES + 1024;  // + alignment slack
+    static constexpr int K_FLOATS = kBN * D;             // one K tile (hi or lo): KB x [64 x 32]
+    static constexpr int V_FLOATS = DV * kBN;            // one V^T tile (hi or lo): 2 x [DV x 32]
+    static constexpr int KSTAGE_FLOATS = 2 * K_FLOATS;   // K hi + lo
+    static constexpr uint32_t KSTAGE_BYTES = KSTAGE_FLOATS * sizeof(float);
+    static constexpr uint32_t V_BYTES = 2 * V_FLOATS * sizeof(float);
+    static constexpr int V_OFF = 2 * KSTAGE_FLOATS;      // after the two K stages
+    static constexpr size_t SMEM = (size_t)(2 * KSTAGE_FLOATS + 2 * V_FLOATS) * sizeof(float) + 1024;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, Q_LO = D, O = 2 * D, S0 = 2 * D + DV, P_HI = S0 + 2 * kBN,
-                              P_LO = P_HI + kBN, COLS = P_LO + kBN;
+    static constexpr uint32_t Q_HI = 0, Q_LO = D, O = 2 * D, S = 2 * D + DV, P_LO = S + kBN, COLS = P_LO + kBN;
     static_assert(D % 32 == 0 && DV % 32 == 0 && D <= 128 && DV <= 128, "tcgen05 prefill shape");
     static_assert(COLS <= 512, "TMEM budget");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
 };
 
-// The fused score epilogue over one 32-key tile of one query row, in base 2:
+// Pairwise (tree) max and sum: short dependency chains.
+template <int N>
+__device__ __forceinline__ float tree_max(const float (&v)[N]) {
+    float m[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) m[i] = fmaxf(v[i], v[i + N / 2]);
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = fmaxf(m[i], m[i + w]);
+    return m[0];
+}
+
+template <int N>
+__device__ __forceinline__ float tree_sum(const float (&v)[N]) {
+    float m[N / 2];
+#pragma unroll
+    for (int i = 0; i < N / 2; ++i) m[i] = v[i] + v[i + N / 2];
+#pragma unroll
+    for (int w = N / 4; w >= 1; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) m[i] = m[i] + m[i + w];
+    return m[0];
+}
+
+// The fused score epilogue over one key tile of one query row, in base 2:
 // scale (or softcap), ALiBi, bias, then the mask -- slots outside
 // [lo_i, hi_i] become -inf.  `full` tiles skip the mask.  Features are
 // template flags so that each combination compiles to straight-line code.
-template <bool SOFTCAP, bool ALIBI, bool BIAS>
-__device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[32], float slope, int rel0,
+template <bool SOFTCAP, bool ALIBI, bool BIAS, int N>
+__device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], float slope, int rel0,
                                               const float* bias, int lo_i, int hi_i, bool full) {
     if (full) {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < N; ++i) {
             float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
             if (BIAS) v = fmaf(__ldg(bias + i), kLog2e, v);
@@ -95,7 +127,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[32],
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
+        for (int i = 0; i < N; ++i) {
             const bool vis = i >= lo_i && i <= hi_i;
             float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
@@ -105,15 +137,31 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[32],
     }
 }
 
+template <int N>
+__device__ __forceinline__ void run_epilogue(int feat, const AttnDesc& a, float (&x)[N], float slope, int rel0,
+                                             const float* bias, int lo_i, int hi_i, bool full) {
+    switch (feat) {
+        case 0: tile_epilogue<false, false, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 1: tile_epilogue<true, false, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 2: tile_epilogue<false, true, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 3: tile_epilogue<true, true, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 4: tile_epilogue<false, false, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 5: tile_epilogue<true, false, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 6: tile_epilogue<false, true, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        default: tile_epilogue<true, true, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+    }
+}
+
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_khi,
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
     using C = TcCfg<D, DV>;
+    constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
-    float* ring = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
-    __shared__ __align__(8) uint64_t full_bar[kStages], empty_bar[kStages], s_full[2], p_full, pv_done, q_ready;
+    float* smem = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full, v_empty, s_full, p_full, pv_done, q_ready;
     __shared__ uint32_t tmem_base_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -138,12 +186,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = (s_hi >= s_lo) ? (int)(s_hi / kBN + 1 - jt_begin) : 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full_bar[s], 1);
-            mbar_init(&empty_bar[s], 1);
+        // Every barrier below completes once per tile (k_* once per two
+        // tiles), and no wait ever targets a phase two behind the current.
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&k_full[b], 1);
+            mbar_init(&k_empty[b], 1);
         }
-        mbar_init(&s_full[0], 1);
-        mbar_init(&s_full[1], 1);
+        mbar_init(&v_full, 1);
+        mbar_init(&v_empty, 1);
+        mbar_init(&s_full, 1);
         mbar_init(&p_full, 4);
         mbar_init(&pv_done, 1);
         mbar_init(&q_ready, 4);
@@ -162,30 +213,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             prefetch_tensormap(&tm_klo);
             prefetch_tensormap(&tm_vhi);
             prefetch_tensormap(&tm_vlo);
-            int issued = 0;
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n_tiles; ++j) {
-                const int s = j % kStages;
-                if (j >= kStages && !mbar_wait(&empty_bar[s], ((j / kStages) - 1) & 1)) {
+                const int n0 = (int)((jt_begin + j) * kBN);
+                const int b = j & 1;
+                if (j >= 2 && !mbar_wait(&k_empty[b], ((j >> 1) - 1) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcEmpty);
                     break;
                 }
-                float* st = ring + s * C::STAGE_FLOATS;
-                mbar_arrive_expect_tx(&full_bar[s], C::STAGE_BYTES);
-                const int n0 = (int)((jt_begin + j) * kBN);
+                float* ks = smem + b * C::KSTAGE_FLOATS;
+                mbar_arrive_expect_tx(&k_full[b], C::KSTAGE_BYTES);
 #pragma unroll
                 for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_2d(st + kb * kBN * 32, &tm_khi, kh * D + kb * 32, n0, &full_bar[s]);
-                    tma_load_2d(st + C::K_FLOATS + kb * kBN * 32, &tm_klo, kh * D + kb * 32, n0, &full_bar[s]);
+                    tma_load_2d(ks + kb * kBN * 32, &tm_khi, kh * D + kb * 32, n0, &k_full[b]);
+                    tma_load_2d(ks + C::K_FLOATS + kb * kBN * 32, &tm_klo, kh * D + kb * 32, n0, &k_full[b]);
                 }
-                tma_load_2d(st + 2 * C::K_FLOATS, &tm_vhi, n0, kh * DV, &full_bar[s]);
-                tma_load_2d(st + 2 * C::K_FLOATS + C::V_FLOATS, &tm_vlo, n0, kh * DV, &full_bar[s]);
-                ++issued;
-            }
-            for (int j = issued > kStages ? issued - kStages : 0; j < issued; ++j)
-                if (!mbar_wait(&full_bar[j % kStages], (j / kStages) & 1)) {
-                    raise_device_error(&g_tc_device_error, kErrTcDrain);
+                ++k_issued;
+                if (j >= 1 && !mbar_wait(&v_empty, (j - 1) & 1)) {
+                    raise_device_error(&g_tc_device_error, kErrTcEmpty);
                     break;
                 }
+                float* vs = smem + C::V_OFF;
+                mbar_arrive_expect_tx(&v_full, C::V_BYTES);
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c) {
+                    tma_load_2d(vs + c * DV * 32, &tm_vhi, n0 + c * 32, kh * DV, &v_full);
+                    tma_load_2d(vs + C::V_FLOATS + c * DV * 32, &tm_vlo, n0 + c * 32, kh * DV, &v_full);
+                }
+                ++v_issued;
+            }
+            // Drain: every copy issued has landed before the CTA moves on.
+            bool drained = true;
+            for (int j = k_issued > 2 ? k_issued - 2 : 0; j < k_issued; ++j)
+                drained &= mbar_wait(&k_full[j & 1], (j >> 1) & 1);
+            if (v_issued > 0) drained &= mbar_wait(&v_full, (v_issued - 1) & 1);
+            if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
@@ -194,56 +256,60 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(&q_ready, 0);
             if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
             tc_fence_after();
-            // S_j = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi into S buffer j & 1.
-            auto issue_s = [&](int j) -> bool {
-                const int s = j % kStages;
-                if (!mbar_wait(&full_bar[s], (j / kStages) & 1)) {
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                // S_j = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi.  Issued after P.V_{j-1},
+                // which read P_hi_{j-1} from the same columns.
+                const int b = j & 1;
+                if (!mbar_wait(&k_full[b], (j >> 1) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcFull);
-                    return false;
+                    break;
                 }
                 tc_fence_after();
-                const float* st = ring + s * C::STAGE_FLOATS;
-                const uint32_t d = tmem + C::S0 + (uint32_t)(j & 1) * kBN;
+                const float* ks = smem + b * C::KSTAGE_FLOATS;
                 uint32_t acc = 0;
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
                     const uint32_t a_col = pass == 2 ? C::Q_LO : C::Q_HI;
-                    const float* b = st + (pass == 1 ? C::K_FLOATS : 0);
+                    const float* kt = ks + (pass == 1 ? C::K_FLOATS : 0);
 #pragma unroll
                     for (int kb = 0; kb < C::KB; ++kb) {
-                        const uint64_t bd = smem_desc_sw128(b + kb * kBN * 32);
+                        const uint64_t bd = smem_desc_sw128(kt + kb * kBN * 32);
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            mma_tf32_ts(d, tmem + a_col + kb * 32 + k * 8, bd + (uint64_t)((k * 32) >> 4), id_s, acc);
+                            mma_tf32_ts(tmem + C::S, tmem + a_col + kb * 32 + k * 8, bd + (uint64_t)((k * 32) >> 4),
+                                        id_s, acc);
                             acc = 1;
                         }
                     }
                 }
-                mma_commit(&s_full[j & 1]);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+                mma_commit(&s_full);
+                mma_commit(&k_empty[b]);
+                // O += P_hi V_hi + P_hi V_lo + P_lo V_hi.
                 if (!mbar_wait(&p_full, j & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     break;
                 }
+                if (!mbar_wait(&v_full, j & 1)) {
+                    raise_device_error(&g_tc_device_error, kErrTcFull);
+                    break;
+                }
                 tc_fence_after();
-                const int s = j % kStages;
-                const float* vhi = ring + s * C::STAGE_FLOATS + 2 * C::K_FLOATS;
-                const float* vlo = vhi + C::V_FLOATS;
+                const float* vs = smem + C::V_OFF;
 #pragma unroll
                 for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a_col = pass == 2 ? C::P_LO : C::P_HI;
-                    const uint64_t bd = smem_desc_sw128(pass == 1 ? vlo : vhi);
+                    const uint32_t a_col = pass == 2 ? C::P_LO : C::S;
+                    const float* vt = vs + (pass == 1 ? C::V_FLOATS : 0);
 #pragma unroll
-                    for (int k = 0; k < kBN / 8; ++k)
-                        mma_tf32_ts(tmem + C::O, tmem + a_col + k * 8, bd + (uint64_t)((k * 32) >> 4), id_o,
-                                    (j > 0 || pass > 0 || k > 0) ? 1u : 0u);
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        const uint64_t bd = smem_desc_sw128(vt + c * DV * 32);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            mma_tf32_ts(tmem + C::O, tmem + a_col + c * 32 + k * 8, bd + (uint64_t)((k * 32) >> 4),
+                                        id_o, (j > 0 || pass > 0 || c > 0 || k > 0) ? 1u : 0u);
+                    }
                 }
                 mma_commit(&pv_done);
-                mma_commit(&empty_bar[s]);
+                mma_commit(&v_empty);
             }
         }
     } else {
@@ -300,36 +366,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&s_full[j & 1], (j >> 1) & 1))) {
+            if (!__all_sync(FULL, mbar_wait(&s_full, j & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcS);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            float x[32];
-            tmem_ld32(trow + C::S0 + (uint32_t)(j & 1) * kBN, x);
+            float x[kBN];
+            tmem_ld32(trow + C::S, x);
+            tmem_ld32(trow + C::S + 32, x + 32);
             tmem_wait_ld();
             const int64_t n0 = (jt_begin + j) * kBN;
-            // Visible slots of this tile, clamped to [-1, 32].
-            int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
-            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > 32 ? 32 : lo64));
-            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > 32 ? 32 : hi64));
+            // Visible slots of this tile, clamped to [-1, kBN].
+            const int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
+            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > kBN ? kBN : lo64));
+            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > kBN ? kBN : hi64));
             const bool full = lo_i <= 0 && hi_i >= kBN - 1;
-            const int rel0 = (int)(n0 - p);  // s - p of slot 0
-            const float* bt = brow ? brow + n0 : nullptr;
-            switch (feat) {
-                case 0: tile_epilogue<false, false, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 1: tile_epilogue<true, false, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 2: tile_epilogue<false, true, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 3: tile_epilogue<true, true, false>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 4: tile_epilogue<false, false, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 5: tile_epilogue<true, false, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                case 6: tile_epilogue<false, true, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-                default: tile_epilogue<true, true, true>(a, x, slope, rel0, bt, lo_i, hi_i, full); break;
-            }
-            float mt = -INFINITY;
-#pragma unroll
-            for (int i = 0; i < 32; ++i) mt = fmaxf(mt, x[i]);
+            run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
+            const float mt = tree_max<kBN>(x);
             // Lazy rescale: keep the reference max unless this tile beats it by > 2^8.
             float alpha = 1.f;
             if (mt > m_ref + kRescaleLog2) {
@@ -337,24 +391,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mt;
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
-            float phi[32], plo[32], rs = 0.f;
+            float plo[kBN];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
+            for (int i = 0; i < kBN; ++i) {
                 const float pi = fast_exp2(x[i] - m_use);
-                rs += pi;
-                phi[i] = tf32_hi(pi);
-                plo[i] = pi - phi[i];
+                x[i] = tf32_hi(pi);  // P_hi replaces the score in registers
+                plo[i] = pi - x[i];
             }
-            l = fmaf(l, alpha, rs);
-            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(&pv_done, (j - 1) & 1))) {  // P and O free again
+            l = fmaf(l, alpha, tree_sum<kBN>(x) + tree_sum<kBN>(plo));
+            // P.V_{j-1} has completed: it ran before S_j in issue order.  The
+            // wait costs nothing and makes the O rescale below safe.
+            if (j > 0 && !__all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcPv);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_st32(trow + C::P_HI, phi);
+            tmem_st32(trow + C::S, x);
+            tmem_st32(trow + C::S + 32, x + 32);
             tmem_st32(trow + C::P_LO, plo);
-            if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            tmem_st32(trow + C::P_LO + 32, plo + 32);
+            if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     float o[32];
@@ -371,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&p_full);
         }
         // Epilogue: O / l -> out.
-        if (ok && n_tiles > 0 && !__all_sync(0xffffffffu, mbar_wait(&pv_done, (n_tiles - 1) & 1))) {
+        if (ok && n_tiles > 0 && !__all_sync(FULL, mbar_wait(&pv_done, (n_tiles - 1) & 1))) {
             raise_device_error(&g_tc_device_error, kErrTcPv);
             ok = false;
         }
