@@ -20,19 +20,24 @@
 //      O   += P_j V_j          (TMEM accumulator, M=128 x N=vHeadDim)
 //    A kind::tf32 MMA takes at least ~46 cycles to issue whatever its N, so
 //    the score MMAs use N = 64 (70 % of the tensor rate; N = 32 reaches 35 %);
-//  * warp 0 issues TMA loads: a 2-deep ring of K hi/lo tiles and one V^T
-//    hi/lo tile (V_j is needed only after the softmax of tile j, so one
-//    buffer, refilled as soon as P.V_j completes, keeps it ahead);
-//    warp 1 owns TMEM and one of its threads issues every MMA; warps 2-5
-//    load Q (split into TMEM), run the fused epilogue and online softmax
-//    (base 2, rescaling O only when a row max grows by more than 2^8),
-//    write P hi/lo into TMEM and finally normalise and store O;
-//  * Q hi/lo and P hi/lo live in TMEM (the MMA's A operand), K and V^T in
-//    shared memory (B operand, 128-byte swizzled).  TMEM columns:
-//    Q_hi | Q_lo | O | S (= P_hi) | P_lo = 2D + Dv + 2*64 <= 512.
-//    P_hi of tile j overwrites S_j once the scores are in registers; the
-//    MMAs of one thread execute in issue order, so S_{j+1} (issued after
-//    P.V_j) overwrites it only after P.V_j has read it.
+//  * operands: Q_hi and P_hi / P_lo in TMEM (A operand of the TS-form MMA),
+//    Q_lo in shared memory (A operand of the SS-form MMA of the third
+//    product), K and V^T hi/lo in shared memory (B operand); every shared
+//    tile is K-major with the 128-byte swizzle;
+//  * TMEM columns: Q_hi | O | S_0 (= P_hi) | S_1 | P_lo_0 | P_lo_1, i.e.
+//    headDim + vHeadDim + 128 * NSB <= 512.  With two S/P buffers (headDim
+//    <= 128) the softmax of tile j runs while the tensor core computes the
+//    scores of tile j+1; headDim 192 has room for one;
+//  * warp 0: lane 0 streams K through a ring of 32-dim sub-tiles (hi + lo,
+//    16 KB each) by TMA, lane 1 loads the V^T hi/lo tile of each key tile
+//    into one buffer; warp 1 owns TMEM and one thread issues every MMA;
+//    warps 2-5 load Q (hi into TMEM, lo into shared memory), run the
+//    tile-specialised epilogue and online softmax (base 2, O rescaled only
+//    when a row max grows by more than 2^8), write P hi/lo into TMEM and
+//    finally normalise and store O.
+//  * P_hi of tile j overwrites its own S buffer once the scores are in
+//    registers.  The MMAs of one thread execute in issue order, so the next
+//    score MMA into that buffer (issued after P.V_j) runs after P.V_j read it.
 //
 // Every wait is bounded (tma_sync.cuh); a wait that gives up sets a bit of
 // g_tc_device_error and the kernel unwinds.
@@ -57,6 +62,7 @@ constexpr int kBM = 128;      // query rows per CTA = MMA M = TMEM lanes
 constexpr int kBN = 64;       // keys per tile = score MMA N
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
+constexpr size_t kSmemLimit = 227 * 1024;
 
 enum TcError : unsigned int {
     kErrTcFull = 1u << 8,
@@ -70,19 +76,23 @@ enum TcError : unsigned int {
 
 template <int D, int DV>
 struct TcCfg {
-    static constexpr int KB = D / 32;                    // 32-float K sub-tiles
-    static constexpr int K_FLOATS = kBN * D;             // one K tile (hi or lo): KB x [64 x 32]
-    static constexpr int V_FLOATS = DV * kBN;            // one V^T tile (hi or lo): 2 x [DV x 32]
-    static constexpr int KSTAGE_FLOATS = 2 * K_FLOATS;   // K hi + lo
-    static constexpr uint32_t KSTAGE_BYTES = KSTAGE_FLOATS * sizeof(float);
+    static constexpr int KB = D / 32;                          // 32-dim K sub-tiles per key tile
+    static constexpr int NSB = (D + DV + 256 <= 512) ? 2 : 1;  // S/P buffers that fit in TMEM
+    static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
+    static constexpr int KSLOT_FLOATS = 2 * kBN * 32;          // one sub-tile, hi + lo
+    static constexpr uint32_t KSLOT_BYTES = KSLOT_FLOATS * sizeof(float);
+    static constexpr int V_FLOATS = DV * kBN;                  // V^T tile (hi or lo): 2 x [DV x 32]
     static constexpr uint32_t V_BYTES = 2 * V_FLOATS * sizeof(float);
-    static constexpr int V_OFF = 2 * KSTAGE_FLOATS;      // after the two K stages
-    static constexpr size_t SMEM = (size_t)(2 * KSTAGE_FLOATS + 2 * V_FLOATS) * sizeof(float) + 1024;
+    static constexpr size_t FIXED = (size_t)(QLO_FLOATS + 2 * V_FLOATS) * sizeof(float) + 1024;
+    static constexpr int NKS_FIT = (int)((kSmemLimit - FIXED) / KSLOT_BYTES);
+    static constexpr int NKS = NKS_FIT > 8 ? 8 : NKS_FIT;      // K ring slots
+    static constexpr int QLO_OFF = 0, V_OFF = QLO_FLOATS, K_OFF = QLO_FLOATS + 2 * V_FLOATS;
+    static constexpr size_t SMEM = FIXED + (size_t)NKS * KSLOT_BYTES;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, Q_LO = D, O = 2 * D, S = 2 * D + DV, P_LO = S + kBN, COLS = P_LO + kBN;
-    static_assert(D % 32 == 0 && DV % 32 == 0 && D <= 128 && DV <= 128, "tcgen05 prefill shape");
+    static constexpr uint32_t Q_HI = 0, O = D, S = D + DV, P_LO = S + NSB * kBN, COLS = P_LO + NSB * kBN;
+    static_assert(D % 32 == 0 && DV % 32 == 0 && D <= 256 && DV <= 256, "tcgen05 prefill shape");
     static_assert(COLS <= 512, "TMEM budget");
-    static_assert(SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(NKS >= 2 && SMEM <= kSmemLimit, "shared memory budget");
 };
 
 // Pairwise (tree) max and sum: short dependency chains.
@@ -152,16 +162,25 @@ __device__ __forceinline__ void run_epilogue(int feat, const AttnDesc& a, float 
     }
 }
 
+// Element (row r, k) of a [rows x 32] f32 tile stored K-major with the
+// 128-byte swizzle: rows of 128 B, 16-byte chunk c of row r at chunk c ^ (r % 8).
+__device__ __forceinline__ int sw128_offset(int r, int chunk) { return r * 32 + ((chunk ^ (r & 7)) << 2); }
+
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_khi,
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
     using C = TcCfg<D, DV>;
+    constexpr int NSB = C::NSB, NKS = C::NKS, KB = C::KB;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
-    __shared__ __align__(8) uint64_t k_full[2], k_empty[2], v_full, v_empty, s_full, p_full, pv_done, q_ready;
+    float* qlo = smem + C::QLO_OFF;
+    float* vsm = smem + C::V_OFF;
+    float* ksm = smem + C::K_OFF;
+    __shared__ __align__(8) uint64_t k_full[NKS], k_empty[NKS], v_full, v_empty, s_full[NSB], p_full[NSB],
+        pv_done[NSB], q_ready;
     __shared__ uint32_t tmem_base_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -186,17 +205,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = (s_hi >= s_lo) ? (int)(s_hi / kBN + 1 - jt_begin) : 0;
 
     if (threadIdx.x == 0) {
-        // Every barrier below completes once per tile (k_* once per two
-        // tiles), and no wait ever targets a phase two behind the current.
-        for (int b = 0; b < 2; ++b) {
+        // One barrier per buffer: no wait ever targets a phase two behind.
+        for (int b = 0; b < NKS; ++b) {
             mbar_init(&k_full[b], 1);
             mbar_init(&k_empty[b], 1);
         }
+        for (int b = 0; b < NSB; ++b) {
+            mbar_init(&s_full[b], 1);
+            mbar_init(&p_full[b], 4);
+            mbar_init(&pv_done[b], 1);
+        }
         mbar_init(&v_full, 1);
         mbar_init(&v_empty, 1);
-        mbar_init(&s_full, 1);
-        mbar_init(&p_full, 4);
-        mbar_init(&pv_done, 1);
         mbar_init(&q_ready, 4);
         fence_barrier_init();
     }
@@ -207,47 +227,52 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
 
     if (warp == 0) {
-        // ------------------------------ TMA producer ------------------------------
+        // ------------------------------ TMA producers -----------------------------
         if (lane == 0 && n_tiles > 0) {
+            // K: sub-tile c = j * KB + kb goes to slot c % NKS.
             prefetch_tensormap(&tm_khi);
             prefetch_tensormap(&tm_klo);
-            prefetch_tensormap(&tm_vhi);
-            prefetch_tensormap(&tm_vlo);
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int n0 = (int)((jt_begin + j) * kBN);
-                const int b = j & 1;
-                if (j >= 2 && !mbar_wait(&k_empty[b], ((j >> 1) - 1) & 1)) {
+            const int total = n_tiles * KB;
+            int issued = 0;
+            for (int c = 0; c < total; ++c) {
+                const int slot = c % NKS;
+                if (c >= NKS && !mbar_wait(&k_empty[slot], ((c / NKS) - 1) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcEmpty);
                     break;
                 }
-                float* ks = smem + b * C::KSTAGE_FLOATS;
-                mbar_arrive_expect_tx(&k_full[b], C::KSTAGE_BYTES);
-#pragma unroll
-                for (int kb = 0; kb < C::KB; ++kb) {
-                    tma_load_2d(ks + kb * kBN * 32, &tm_khi, kh * D + kb * 32, n0, &k_full[b]);
-                    tma_load_2d(ks + C::K_FLOATS + kb * kBN * 32, &tm_klo, kh * D + kb * 32, n0, &k_full[b]);
-                }
-                ++k_issued;
+                const int j = c / KB, kb = c % KB;
+                const int n0 = (int)((jt_begin + j) * kBN);
+                float* ks = ksm + slot * C::KSLOT_FLOATS;
+                mbar_arrive_expect_tx(&k_full[slot], C::KSLOT_BYTES);
+                tma_load_2d(ks, &tm_khi, kh * D + kb * 32, n0, &k_full[slot]);
+                tma_load_2d(ks + kBN * 32, &tm_klo, kh * D + kb * 32, n0, &k_full[slot]);
+                ++issued;
+            }
+            bool drained = true;
+            for (int c = issued > NKS ? issued - NKS : 0; c < issued; ++c)
+                drained &= mbar_wait(&k_full[c % NKS], (c / NKS) & 1);
+            if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
+        } else if (lane == 1 && n_tiles > 0) {
+            // V^T hi/lo of key tile j, one buffer, refilled once P.V_{j-1} is done.
+            prefetch_tensormap(&tm_vhi);
+            prefetch_tensormap(&tm_vlo);
+            int issued = 0;
+            for (int j = 0; j < n_tiles; ++j) {
                 if (j >= 1 && !mbar_wait(&v_empty, (j - 1) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcEmpty);
                     break;
                 }
-                float* vs = smem + C::V_OFF;
+                const int n0 = (int)((jt_begin + j) * kBN);
                 mbar_arrive_expect_tx(&v_full, C::V_BYTES);
 #pragma unroll
                 for (int c = 0; c < kBN / 32; ++c) {
-                    tma_load_2d(vs + c * DV * 32, &tm_vhi, n0 + c * 32, kh * DV, &v_full);
-                    tma_load_2d(vs + C::V_FLOATS + c * DV * 32, &tm_vlo, n0 + c * 32, kh * DV, &v_full);
+                    tma_load_2d(vsm + c * DV * 32, &tm_vhi, n0 + c * 32, kh * DV, &v_full);
+                    tma_load_2d(vsm + C::V_FLOATS + c * DV * 32, &tm_vlo, n0 + c * 32, kh * DV, &v_full);
                 }
-                ++v_issued;
+                ++issued;
             }
-            // Drain: every copy issued has landed before the CTA moves on.
-            bool drained = true;
-            for (int j = k_issued > 2 ? k_issued - 2 : 0; j < k_issued; ++j)
-                drained &= mbar_wait(&k_full[j & 1], (j >> 1) & 1);
-            if (v_issued > 0) drained &= mbar_wait(&v_full, (v_issued - 1) & 1);
-            if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
+            if (issued > 0 && !mbar_wait(&v_full, (issued - 1) & 1))
+                raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
@@ -256,60 +281,76 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(&q_ready, 0);
             if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
             tc_fence_after();
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                // S_j = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi.  Issued after P.V_{j-1},
-                // which read P_hi_{j-1} from the same columns.
-                const int b = j & 1;
-                if (!mbar_wait(&k_full[b], (j >> 1) & 1)) {
-                    raise_device_error(&g_tc_device_error, kErrTcFull);
-                    break;
-                }
-                tc_fence_after();
-                const float* ks = smem + b * C::KSTAGE_FLOATS;
+            // S_j = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi into S buffer j % NSB.
+            auto issue_s = [&](int j) -> bool {
+                const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * kBN;
                 uint32_t acc = 0;
-#pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a_col = pass == 2 ? C::Q_LO : C::Q_HI;
-                    const float* kt = ks + (pass == 1 ? C::K_FLOATS : 0);
-#pragma unroll
-                    for (int kb = 0; kb < C::KB; ++kb) {
-                        const uint64_t bd = smem_desc_sw128(kt + kb * kBN * 32);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            mma_tf32_ts(tmem + C::S, tmem + a_col + kb * 32 + k * 8, bd + (uint64_t)((k * 32) >> 4),
-                                        id_s, acc);
-                            acc = 1;
-                        }
+                for (int kb = 0; kb < KB; ++kb) {
+                    const int c = j * KB + kb, slot = c % NKS;
+                    if (!mbar_wait(&k_full[slot], (c / NKS) & 1)) {
+                        raise_device_error(&g_tc_device_error, kErrTcFull);
+                        return false;
                     }
+                    tc_fence_after();
+                    const float* ks = ksm + slot * C::KSLOT_FLOATS;
+                    const uint64_t b_hi = smem_desc_sw128(ks), b_lo = smem_desc_sw128(ks + kBN * 32);
+                    const uint64_t a_lo = smem_desc_sw128(qlo + kb * kBM * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ko = (uint64_t)((k * 32) >> 4);
+                        const uint32_t a_hi = tmem + C::Q_HI + kb * 32 + k * 8;
+                        mma_tf32_ts(d, a_hi, b_hi + ko, id_s, acc);
+                        mma_tf32_ts(d, a_hi, b_lo + ko, id_s, 1u);
+                        mma_tf32_ss(d, a_lo + ko, b_hi + ko, id_s, 1u);
+                        acc = 1;
+                    }
+                    mma_commit(&k_empty[slot]);
                 }
-                mma_commit(&s_full);
-                mma_commit(&k_empty[b]);
-                // O += P_hi V_hi + P_hi V_lo + P_lo V_hi.
-                if (!mbar_wait(&p_full, j & 1)) {
+                mma_commit(&s_full[j % NSB]);
+                return true;
+            };
+            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi for tile j.
+            auto issue_pv = [&](int j) -> bool {
+                if (!mbar_wait(&p_full[j % NSB], (j / NSB) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcP);
-                    break;
+                    return false;
                 }
                 if (!mbar_wait(&v_full, j & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcFull);
-                    break;
+                    return false;
                 }
                 tc_fence_after();
-                const float* vs = smem + C::V_OFF;
+                const uint32_t p_hi = C::S + (uint32_t)(j % NSB) * kBN, p_lo = C::P_LO + (uint32_t)(j % NSB) * kBN;
 #pragma unroll
-                for (int pass = 0; pass < 3; ++pass) {
-                    const uint32_t a_col = pass == 2 ? C::P_LO : C::S;
-                    const float* vt = vs + (pass == 1 ? C::V_FLOATS : 0);
+                for (int c = 0; c < kBN / 32; ++c) {
+                    const uint64_t v_hi = smem_desc_sw128(vsm + c * DV * 32);
+                    const uint64_t v_lo = smem_desc_sw128(vsm + C::V_FLOATS + c * DV * 32);
 #pragma unroll
-                    for (int c = 0; c < kBN / 32; ++c) {
-                        const uint64_t bd = smem_desc_sw128(vt + c * DV * 32);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            mma_tf32_ts(tmem + C::O, tmem + a_col + c * 32 + k * 8, bd + (uint64_t)((k * 32) >> 4),
-                                        id_o, (j > 0 || pass > 0 || c > 0 || k > 0) ? 1u : 0u);
+                    for (int k = 0; k < 4; ++k) {
+                        const uint64_t ko = (uint64_t)((k * 32) >> 4);
+                        const uint32_t col = c * 32 + k * 8;
+                        mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_hi + ko, id_o,
+                                    (j > 0 || c > 0 || k > 0) ? 1u : 0u);
+                        mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_lo + ko, id_o, 1u);
+                        mma_tf32_ts(tmem + C::O, tmem + p_lo + col, v_hi + ko, id_o, 1u);
                     }
                 }
-                mma_commit(&pv_done);
+                mma_commit(&pv_done[j % NSB]);
                 mma_commit(&v_empty);
+                return true;
+            };
+            if constexpr (NSB == 2) {
+                // S_{j+1} goes in before P.V_j so the tensor core computes the
+                // next scores while the softmax warps work on tile j.
+                if (ok) ok = issue_s(0);
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    if (j + 1 < n_tiles && !issue_s(j + 1)) break;
+                    if (!issue_pv(j)) break;
+                }
+            } else {
+                for (int j = 0; ok && j < n_tiles; ++j) {
+                    if (!issue_s(j) || !issue_pv(j)) break;
+                }
             }
         }
     } else {
@@ -320,15 +361,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = t < a.T;
         const uint32_t trow = tmem + (lrow << 16);
         const float slope = a.alibi_on ? alibi.slope_log2[h] : 0.f;
-        // Q row -> hi / lo -> TMEM.
+        // Q row -> hi (TMEM) / lo (shared memory, 128-byte swizzled).
         {
             const float* qrow = a.q + t * (int64_t)a.H * D + (int64_t)h * D;
 #pragma unroll 1
-            for (int c0 = 0; c0 < D; c0 += 32) {
+            for (int kb = 0; kb < KB; ++kb) {
                 float hi[32], lo[32];
 #pragma unroll
                 for (int i = 0; i < 32; i += 4) {
-                    float4 v4 = row_ok ? __ldg(reinterpret_cast<const float4*>(qrow + c0 + i)) : make_float4(0, 0, 0, 0);
+                    float4 v4 = row_ok ? __ldg(reinterpret_cast<const float4*>(qrow + kb * 32 + i))
+                                       : make_float4(0, 0, 0, 0);
                     const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -336,9 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         lo[i + e] = vv[e] - hi[i + e];
                     }
                 }
-                tmem_st32(trow + C::Q_HI + c0, hi);
-                tmem_st32(trow + C::Q_LO + c0, lo);
+                tmem_st32(trow + C::Q_HI + kb * 32, hi);
+                float* sub = qlo + kb * kBM * 32;
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4*>(sub + sw128_offset(r, c)) =
+                        make_float4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
             }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // Q_lo -> MMA (async proxy)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -366,15 +413,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(FULL, mbar_wait(&s_full, j & 1))) {
+            const int b = j % NSB;
+            if (!__all_sync(FULL, mbar_wait(&s_full[b], (j / NSB) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcS);
                 ok = false;
                 break;
             }
             tc_fence_after();
+            const uint32_t s_col = C::S + (uint32_t)b * kBN, plo_col = C::P_LO + (uint32_t)b * kBN;
             float x[kBN];
-            tmem_ld32(trow + C::S, x);
-            tmem_ld32(trow + C::S + 32, x + 32);
+            tmem_ld32(trow + s_col, x);
+            tmem_ld32(trow + s_col + 32, x + 32);
             tmem_wait_ld();
             const int64_t n0 = (jt_begin + j) * kBN;
             // Visible slots of this tile, clamped to [-1, kBN].
@@ -399,19 +448,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 plo[i] = pi - x[i];
             }
             l = fmaf(l, alpha, tree_sum<kBN>(x) + tree_sum<kBN>(plo));
-            // P.V_{j-1} has completed: it ran before S_j in issue order.  The
-            // wait costs nothing and makes the O rescale below safe.
-            if (j > 0 && !__all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1))) {
+            // This buffer's P was last read by P.V_{j-NSB}, which ran before
+            // S_j in issue order; the wait costs nothing.
+            if (j >= NSB && !__all_sync(FULL, mbar_wait(&pv_done[b], ((j / NSB) - 1) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcPv);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_st32(trow + C::S, x);
-            tmem_st32(trow + C::S + 32, x + 32);
-            tmem_st32(trow + C::P_LO, plo);
-            tmem_st32(trow + C::P_LO + 32, plo + 32);
+            tmem_st32(trow + s_col, x);
+            tmem_st32(trow + s_col + 32, x + 32);
+            tmem_st32(trow + plo_col, plo);
+            tmem_st32(trow + plo_col + 32, plo + 32);
             if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
+                // O must hold P.V_{j-1} before it is rescaled.
+                const int bp = (j - 1) % NSB;
+                if (!__all_sync(FULL, mbar_wait(&pv_done[bp], ((j - 1) / NSB) & 1))) {
+                    raise_device_error(&g_tc_device_error, kErrTcPv);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < DV; c0 += 32) {
                     float o[32];
@@ -425,12 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full);
+            if (lane == 0) mbar_arrive(&p_full[b]);
         }
         // Epilogue: O / l -> out.
-        if (ok && n_tiles > 0 && !__all_sync(FULL, mbar_wait(&pv_done, (n_tiles - 1) & 1))) {
-            raise_device_error(&g_tc_device_error, kErrTcPv);
-            ok = false;
+        if (ok && n_tiles > 0) {
+            const int last = n_tiles - 1;
+            if (!__all_sync(FULL, mbar_wait(&pv_done[last % NSB], (last / NSB) & 1))) {
+                raise_device_error(&g_tc_device_error, kErrTcPv);
+                ok = false;
+            }
         }
         tc_fence_after();
         const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
@@ -563,7 +623,8 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
 }  // namespace
 
 bool prefill_tc_supported(const AttnDesc& a) {
-    const bool dims = (a.D == 32 || a.D == 64 || a.D == 96 || a.D == 128) && a.Dv == a.D;
+    const bool dims = ((a.D == 32 || a.D == 64 || a.D == 96 || a.D == 128) && a.Dv == a.D) ||
+                      (a.D == 192 && a.Dv == 128);
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
     const bool q_aligned = (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
     return dims && a.T >= 1 && a.S >= 1 && a.S < ((int64_t)1 << 31) && a.pos_offset + a.T < ((int64_t)1 << 31) &&
@@ -591,9 +652,9 @@ cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* 
     split_vt_kernel<<<g2, dim3(32, 8), 0, stream>>>(a.v, vthi, vtlo, a.S, L.s_pad, cols);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-#define VTMU_TC(D_) \
-    if (a.D == D_) return launch_cfg<D_, D_>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream);
-    VTMU_TC(32) VTMU_TC(64) VTMU_TC(96) VTMU_TC(128)
+#define VTMU_TC(D_, DV_) \
+    if (a.D == D_ && a.Dv == DV_) return launch_cfg<D_, DV_>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream);
+    VTMU_TC(32, 32) VTMU_TC(64, 64) VTMU_TC(96, 96) VTMU_TC(128, 128) VTMU_TC(192, 128)
 #undef VTMU_TC
     return cudaErrorInvalidValue;
 }

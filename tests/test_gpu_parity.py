@@ -336,10 +336,10 @@ TC = vtmu.VTMU_KERNEL_PREFILL_TF32X3
 def _tc_case(seed):
     g = np.random.default_rng(7000 + seed)
     H, Hk = [(1, 1), (4, 1), (4, 2), (6, 3), (8, 8), (8, 2)][seed % 6]
-    D = int(g.choice([32, 64, 96, 128]))
+    D, Dv = [(32, 32), (64, 64), (96, 96), (128, 128), (192, 128)][int(g.integers(0, 5))]
     T = int(g.integers(1, 300))
     S = int(g.integers(1, 500))
-    params = dict(heads=H, headDim=D, kvHeads=Hk, causal=bool(g.integers(0, 4) > 0),
+    params = dict(heads=H, headDim=D, kvHeads=Hk, vHeadDim=Dv, causal=bool(g.integers(0, 4) > 0),
                   posOffset=int(g.choice([0, 5, max(S - T, 0), S + 7])))
     if g.random() < 0.4:
         params["window"] = int(g.integers(1, 120))
@@ -353,7 +353,7 @@ def _tc_case(seed):
     elif r < 0.3:
         params["alibiMax"] = 8.0
     bias = None if g.random() < 0.6 else str(g.choice(["ts", "hts"]))
-    x = si.attention_inputs(T, S, H, Hk, D, D, 50 + seed, sigma=float(g.choice([1.0, 2.0])), bias=bias,
+    x = si.attention_inputs(T, S, H, Hk, D, Dv, 50 + seed, sigma=float(g.choice([1.0, 2.0])), bias=bias,
                             bias_mask_p=0.1 if bias else 0.0)
     if bias is not None:
         b = x["bias"]
@@ -361,7 +361,7 @@ def _tc_case(seed):
     return x, params
 
 
-@pytest.mark.parametrize("seed", range(36))
+@pytest.mark.parametrize("seed", range(40))
 def test_tensor_core_prefill_random_sweep(seed):
     x, params = _tc_case(seed)
     check(x, dict(params, kernel=TC))
@@ -371,6 +371,13 @@ def test_tensor_core_prefill_random_sweep(seed):
 def test_tensor_core_prefill_tile_edges(T, S, pos):
     x = si.attention_inputs(T, S, 4, 2, 128, 128, 61)
     check(x, dict(heads=4, headDim=128, kvHeads=2, posOffset=pos, kernel=TC))
+
+
+@pytest.mark.parametrize("T,S,pos", [(128, 128, 0), (200, 333, 133), (1, 64, 63)])
+def test_tensor_core_prefill_latent_shape(T, S, pos):
+    """headDim 192 with vHeadDim 128 (one S buffer in TMEM)."""
+    x = si.attention_inputs(T, S, 4, 4, 192, 128, 64, bias="ts")
+    check(x, dict(heads=4, headDim=192, vHeadDim=128, posOffset=pos, causal=False, kernel=TC))
 
 
 def test_tensor_core_prefill_masked_rows_give_zeros():
