@@ -24,10 +24,16 @@
 //    Q_lo in shared memory (A operand of the SS-form MMA of the third
 //    product), K and V^T hi/lo in shared memory (B operand); every shared
 //    tile is K-major with the 128-byte swizzle;
-//  * TMEM columns: Q_hi | O | S_0 (= P_hi) | S_1 | P_lo_0 | P_lo_1, i.e.
-//    headDim + vHeadDim + 128 * NSB <= 512.  With two S/P buffers (headDim
-//    <= 128) the softmax of tile j runs while the tensor core computes the
-//    scores of tile j+1; headDim 192 has room for one;
+//  * the two products with Q_hi come from ONE MMA: each K ring slot holds
+//    the 64 K_hi rows followed by the 64 K_lo rows, i.e. a 128-row B operand,
+//    so Q_hi.[K_hi; K_lo]^T lands as [S_hihi | S_hilo] in 128 TMEM columns at
+//    the full N = 128 tensor rate; the third product Q_lo.K_hi (N = 64)
+//    accumulates into the first half and the softmax adds the two halves;
+//  * TMEM columns: Q_hi | O | S_0 | S_1 with 128-column S buffers, i.e.
+//    headDim + vHeadDim + 128 * NSB <= 512; P_hi and P_lo of a tile are
+//    written over the two halves of its S buffer.  With two buffers
+//    (headDim <= 128) the softmax of tile j runs while the tensor core
+//    computes the scores of tile j+1; headDim 192 has room for one;
 //  * warp 0: lane 0 streams K through a ring of 32-dim sub-tiles (hi + lo,
 //    16 KB each) by TMA, lane 1 loads the V^T hi/lo tile of each key tile
 //    into one buffer; warp 1 owns TMEM and one thread issues every MMA;
@@ -35,7 +41,7 @@
 //    tile-specialised epilogue and online softmax (base 2, O rescaled only
 //    when a row max grows by more than 2^8), write P hi/lo into TMEM and
 //    finally normalise and store O.
-//  * P_hi of tile j overwrites its own S buffer once the scores are in
+//  * P of tile j overwrites its own S buffer once the scores are in
 //    registers.  The MMAs of one thread execute in issue order, so the next
 //    score MMA into that buffer (issued after P.V_j) runs after P.V_j read it.
 //
@@ -77,7 +83,7 @@ enum TcError : unsigned int {
 template <int D, int DV>
 struct TcCfg {
     static constexpr int KB = D / 32;                          // 32-dim K sub-tiles per key tile
-    static constexpr int NSB = (D + DV + 256 <= 512) ? 2 : 1;  // S/P buffers that fit in TMEM
+    static constexpr int NSB = (D + DV + 256 <= 512) ? 2 : 1;  // 128-column S/P buffers that fit in TMEM
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
     static constexpr int KSLOT_FLOATS = 2 * kBN * 32;          // one sub-tile, hi + lo
     static constexpr uint32_t KSLOT_BYTES = KSLOT_FLOATS * sizeof(float);
@@ -89,7 +95,7 @@ struct TcCfg {
     static constexpr int QLO_OFF = 0, V_OFF = QLO_FLOATS, K_OFF = QLO_FLOATS + 2 * V_FLOATS;
     static constexpr size_t SMEM = FIXED + (size_t)NKS * KSLOT_BYTES;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, O = D, S = D + DV, P_LO = S + NSB * kBN, COLS = P_LO + NSB * kBN;
+    static constexpr uint32_t Q_HI = 0, O = D, S = D + DV, SB = 2 * kBN, COLS = S + NSB * SB;
     static_assert(D % 32 == 0 && DV % 32 == 0 && D <= 256 && DV <= 256, "tcgen05 prefill shape");
     static_assert(COLS <= 512, "TMEM budget");
     static_assert(NKS >= 2 && SMEM <= kSmemLimit, "shared memory budget");
@@ -277,13 +283,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0 && n_tiles > 0) {
-            constexpr uint32_t id_s = idesc_tf32(kBM, kBN), id_o = idesc_tf32(kBM, DV);
+            constexpr uint32_t id_s2 = idesc_tf32(kBM, 2 * kBN), id_s = idesc_tf32(kBM, kBN),
+                               id_o = idesc_tf32(kBM, DV);
             bool ok = mbar_wait(&q_ready, 0);
             if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
             tc_fence_after();
-            // S_j = Q_hi K_hi + Q_hi K_lo + Q_lo K_hi into S buffer j % NSB.
+            // S buffer j % NSB: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
-                const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * kBN;
+                const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * C::SB;
                 uint32_t acc = 0;
                 for (int kb = 0; kb < KB; ++kb) {
                     const int c = j * KB + kb, slot = c % NKS;
@@ -292,16 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                         return false;
                     }
                     tc_fence_after();
-                    const float* ks = ksm + slot * C::KSLOT_FLOATS;
-                    const uint64_t b_hi = smem_desc_sw128(ks), b_lo = smem_desc_sw128(ks + kBN * 32);
+                    const uint64_t b_k = smem_desc_sw128(ksm + slot * C::KSLOT_FLOATS);  // [K_hi; K_lo]
                     const uint64_t a_lo = smem_desc_sw128(qlo + kb * kBM * 32);
+                    const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
 #pragma unroll
                     for (int k = 0; k < 4; ++k) {
                         const uint64_t ko = (uint64_t)((k * 32) >> 4);
-                        const uint32_t a_hi = tmem + C::Q_HI + kb * 32 + k * 8;
-                        mma_tf32_ts(d, a_hi, b_hi + ko, id_s, acc);
-                        mma_tf32_ts(d, a_hi, b_lo + ko, id_s, 1u);
-                        mma_tf32_ss(d, a_lo + ko, b_hi + ko, id_s, 1u);
+                        mma_tf32_ts(d, a_hi + k * 8, b_k + ko, id_s2, acc);
+                        mma_tf32_ss(d, a_lo + ko, b_k + ko, id_s, 1u);
                         acc = 1;
                     }
                     mma_commit(&k_empty[slot]);
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     return false;
                 }
                 tc_fence_after();
-                const uint32_t p_hi = C::S + (uint32_t)(j % NSB) * kBN, p_lo = C::P_LO + (uint32_t)(j % NSB) * kBN;
+                const uint32_t p_hi = C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
 #pragma unroll
                 for (int c = 0; c < kBN / 32; ++c) {
                     const uint64_t v_hi = smem_desc_sw128(vsm + c * DV * 32);
@@ -420,11 +425,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t s_col = C::S + (uint32_t)b * kBN, plo_col = C::P_LO + (uint32_t)b * kBN;
+            const uint32_t s_col = C::S + (uint32_t)b * C::SB, plo_col = s_col + kBN;
             float x[kBN];
-            tmem_ld32(trow + s_col, x);
-            tmem_ld32(trow + s_col + 32, x + 32);
-            tmem_wait_ld();
+#pragma unroll
+            for (int h2 = 0; h2 < kBN; h2 += 32) {  // S = first half + second half
+                float y[32];
+                tmem_ld32(trow + s_col + h2, x + h2);
+                tmem_ld32(trow + s_col + kBN + h2, y);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[h2 + i] += y[i];
+            }
             const int64_t n0 = (jt_begin + j) * kBN;
             // Visible slots of this tile, clamped to [-1, kBN].
             const int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
