@@ -5,7 +5,7 @@
 // range [s_lo, s_end) of cache rows.  The work is HBM-bound: every K and V
 // byte of that range is read once.  Layout of the work:
 //
-//  * grid (splits, kvHeads): one CTA streams a chunk of the range for one KV
+//  * grid (kvHeads, splits): one CTA streams a chunk of the range for one KV
 //    head and serves all G = heads/kvHeads query heads of its group, so each
 //    K/V byte is read once per group, not once per query head;
 //  * a producer warp moves NR-row K and V tiles global -> shared with 2-D TMA
@@ -58,6 +58,9 @@ namespace {
 #endif
 #ifndef VTMU_DEC_CTAS_PER_SM
 #define VTMU_DEC_CTAS_PER_SM 1  // resident CTAs per SM the split count aims for
+#endif
+#ifndef VTMU_DEC_KH_FAST
+#define VTMU_DEC_KH_FAST 1  // 1: the KV heads of one split are adjacent CTAs
 #endif
 
 constexpr int kMaxSplits = 256;
@@ -148,8 +151,8 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     __shared__ int s_is_last;
 
     const AttnDesc& a = args.a;
-    const int split = blockIdx.x;
-    const int kh = blockIdx.y;
+    const int split = VTMU_DEC_KH_FAST ? blockIdx.y : blockIdx.x;
+    const int kh = VTMU_DEC_KH_FAST ? blockIdx.x : blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t p = a.pos_offset;  // position of the single query row
@@ -388,45 +391,90 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     }
 
     // ---- last CTA of this KV head merges the splits ----------------------
-    __threadfence();
+    // Release: the barrier orders every thread's partial stores before
+    // thread 0's gpu-scope fence, which publishes them before the ticket.
     __syncthreads();
     if (threadIdx.x == 0) {
+        __threadfence();
         const unsigned ticket = atomicAdd(&args.counters[kh], 1u);
-        s_is_last = (ticket == (unsigned)(Hs - 1));
+        const bool last = (ticket == (unsigned)(Hs - 1));
+        if (last) __threadfence();  // acquire: the other splits' partials
+        s_is_last = last;
     }
     __syncthreads();
     if (!s_is_last) return;
-    __threadfence();
+
+    // Thread t owns outputs t + k*THREADS (k < NOUT).  It issues the loads of
+    // its first CH split partials before warp g (g < G) turns head g's split
+    // maxima into weights, so both L2 round trips overlap.
+    constexpr int NOUT = (G * D + C::THREADS - 1) / C::THREADS;
+    constexpr int CH = 64 / NOUT > 32 ? 32 : (64 / NOUT < 8 ? 8 : 64 / NOUT);
+    float ov[NOUT][CH];
+    auto load_chunk = [&](int i0) {
+#pragma unroll
+        for (int k = 0; k < NOUT; ++k) {
+            const int idx = threadIdx.x + k * C::THREADS;
+            const int64_t base = idx < G * D ? ((int64_t)(kh * G + idx / D) * Hs) * D + idx % D : 0;
+#pragma unroll
+            for (int c = 0; c < CH; ++c) {
+                const int i = i0 + c;
+                ov[k][c] = (idx < G * D && i < Hs) ? __ldcg(args.part_o + base + (int64_t)i * D) : 0.f;
+            }
+        }
+    };
+    load_chunk(0);
 
     float* sw = smem;                   // [G][kMaxSplits] split weights
     float* sinv = sw + G * kMaxSplits;  // [G] 1 / l*
-    constexpr int NW = C::THREADS / 32;
-    for (int g = warp; g < G; g += NW) {
-        const int h = kh * G + g;
+    if (warp < G) {
+        const int h = kh * G + warp;
+        constexpr int PER = kMaxSplits / 32;
+        float mv[PER], lv[PER];
+#pragma unroll
+        for (int t = 0; t < PER; ++t) {
+            const int i = lane + 32 * t;
+            mv[t] = i < Hs ? __ldcg(args.part_m + (int64_t)h * Hs + i) : -INFINITY;
+            lv[t] = i < Hs ? __ldcg(args.part_l + (int64_t)h * Hs + i) : 0.f;
+        }
         float M = -INFINITY;
-        for (int i = lane; i < Hs; i += 32) M = fmaxf(M, __ldcg(args.part_m + (int64_t)h * Hs + i));
+#pragma unroll
+        for (int t = 0; t < PER; ++t) M = fmaxf(M, mv[t]);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, off));
         const float mu = (M == -INFINITY) ? 0.f : M;
         float L = 0.f;
-        for (int i = lane; i < Hs; i += 32) {
-            const float w = fast_exp2(__ldcg(args.part_m + (int64_t)h * Hs + i) - mu);
-            sw[g * kMaxSplits + i] = w;
-            L = fmaf(__ldcg(args.part_l + (int64_t)h * Hs + i), w, L);
+#pragma unroll
+        for (int t = 0; t < PER; ++t) {
+            const float w = fast_exp2(mv[t] - mu);
+            if (lane + 32 * t < Hs) sw[warp * kMaxSplits + lane + 32 * t] = w;
+            L = fmaf(lv[t], w, L);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
-        if (lane == 0) sinv[g] = (L > 0.f) ? 1.f / L : 0.f;
+        if (lane == 0) sinv[warp] = (L > 0.f) ? 1.f / L : 0.f;
     }
     __syncthreads();
-    for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
-        const int g = idx / D, e = idx % D;
-        const int h = kh * G + g;
-        const float* po = args.part_o + (int64_t)h * Hs * D + e;
-        float acc = 0.f;
-#pragma unroll 8
-        for (int i = 0; i < Hs; ++i) acc = fmaf(__ldcg(po + (int64_t)i * D), sw[g * kMaxSplits + i], acc);
-        a.out[(int64_t)h * D + e] = acc * sinv[g];
+
+    float acc[NOUT];
+#pragma unroll
+    for (int k = 0; k < NOUT; ++k) acc[k] = 0.f;
+    for (int i0 = 0;;) {
+#pragma unroll
+        for (int k = 0; k < NOUT; ++k) {
+            const int idx = threadIdx.x + k * C::THREADS;
+            const float* wg = sw + (idx < G * D ? idx / D : 0) * kMaxSplits + i0;
+#pragma unroll
+            for (int c = 0; c < CH; ++c)
+                if (i0 + c < Hs) acc[k] = fmaf(ov[k][c], wg[c], acc[k]);
+        }
+        i0 += CH;
+        if (i0 >= Hs) break;
+        load_chunk(i0);
+    }
+#pragma unroll
+    for (int k = 0; k < NOUT; ++k) {
+        const int idx = threadIdx.x + k * C::THREADS;
+        if (idx < G * D) a.out[(int64_t)(kh * G + idx / D) * D + idx % D] = acc[k] * sinv[idx / D];
     }
     if (threadIdx.x == 0) args.counters[kh] = 0u;  // ready for the next call
 }
@@ -474,7 +522,7 @@ cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, cudaStre
     auto kern = decode_splitkv_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid(args.splits, a.Hk);
+    dim3 grid = VTMU_DEC_KH_FAST ? dim3(a.Hk, args.splits) : dim3(args.splits, a.Hk);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(args, alibi, tmk, tmv);
     return cudaGetLastError();
 }
