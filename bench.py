@@ -328,7 +328,7 @@ def run_vtmu(args, rank, world, local):
             out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
             flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
         bias_kind = vtmu.VTMU_BIAS_NONE if b is None else (vtmu.VTMU_BIAS_TS if b.dim() == 2 else vtmu.VTMU_BIAS_HTS)
-        tc_ok = ((D == Dv and D in (32, 64, 96, 128)) or (D, Dv) == (192, 128)) and T >= 64
+        tc_ok = ((D == Dv and D in (32, 64, 96, 128, 256)) or (D, Dv) == (192, 128)) and T >= 64
         use_tc = tc_ok if args.kernel == "auto" else args.kernel == "tc"
         kernel = vtmu.VTMU_KERNEL_PREFILL_TF32X3 if use_tc else vtmu.VTMU_KERNEL_PREFILL_FFMA
         p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, vHeadDim=w.get("vHeadDim"),

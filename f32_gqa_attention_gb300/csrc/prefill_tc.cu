@@ -69,6 +69,9 @@ constexpr int kBN = 64;       // keys per tile = score MMA N
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
 constexpr size_t kSmemLimit = 227 * 1024;
+#ifndef VTMU_TC_MAX_SLOTS
+#define VTMU_TC_MAX_SLOTS 6  // shared-memory ring slots (32 KB each) at most
+#endif
 
 enum TcError : unsigned int {
     kErrTcFull = 1u << 8,
@@ -82,23 +85,31 @@ enum TcError : unsigned int {
 
 template <int D, int DV>
 struct TcCfg {
+    static constexpr int DVC = DV <= 128 ? DV : DV / 2;       // V columns per CTA (grid.z = DV / DVC)
     static constexpr int KB = D / 32;                          // 32-dim K sub-tiles per key tile
-    static constexpr int NSB = (D + DV + 256 <= 512) ? 2 : 1;  // 128-column S/P buffers that fit in TMEM
+    static constexpr int NSB = (D + DVC + 256 <= 512) ? 2 : 1; // 128-column S/P buffers that fit in TMEM
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
-    static constexpr int KSLOT_FLOATS = 2 * kBN * 32;          // one sub-tile, hi + lo
-    static constexpr uint32_t KSLOT_BYTES = KSLOT_FLOATS * sizeof(float);
-    static constexpr int V_FLOATS = DV * kBN;                  // V^T tile (hi or lo): 2 x [DV x 32]
-    static constexpr uint32_t V_BYTES = 2 * V_FLOATS * sizeof(float);
-    static constexpr size_t FIXED = (size_t)(QLO_FLOATS + 2 * V_FLOATS) * sizeof(float) + 1024;
-    static constexpr int NKS_FIT = (int)((kSmemLimit - FIXED) / KSLOT_BYTES);
-    static constexpr int NKS = NKS_FIT > 8 ? 8 : NKS_FIT;      // K ring slots
-    static constexpr int QLO_OFF = 0, V_OFF = QLO_FLOATS, K_OFF = QLO_FLOATS + 2 * V_FLOATS;
-    static constexpr size_t SMEM = FIXED + (size_t)NKS * KSLOT_BYTES;
+    // Ring slots of 32 KB.  A K item holds two 32-dim sub-tiles, each K_hi
+    // (64 rows) then K_lo (64 rows); a V item holds V^T_hi then V^T_lo of
+    // VCH 32-key chunks.
+    static constexpr int KSUB_FLOATS = 2 * kBN * 32;
+    static constexpr int SLOT_FLOATS = 2 * KSUB_FLOATS;
+    static constexpr int KITEMS = (KB + 1) / 2;
+    static constexpr int VCHUNK_FLOATS = 2 * DVC * 32;
+    static constexpr int VCH = 2 * VCHUNK_FLOATS <= SLOT_FLOATS ? 2 : 1;
+    static constexpr int VITEMS = (kBN / 32) / VCH;
+    static constexpr uint32_t SLOT_BYTES = SLOT_FLOATS * sizeof(float);
+    static constexpr size_t FIXED = (size_t)QLO_FLOATS * sizeof(float) + 1024;
+    static constexpr int NS_FIT = (int)((kSmemLimit - FIXED) / SLOT_BYTES);
+    static constexpr int NS = NS_FIT > VTMU_TC_MAX_SLOTS ? VTMU_TC_MAX_SLOTS : NS_FIT;  // ring slots
+    static constexpr int QLO_OFF = 0, RING_OFF = QLO_FLOATS;
+    static constexpr size_t SMEM = FIXED + (size_t)NS * SLOT_BYTES;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, O = D, S = D + DV, SB = 2 * kBN, COLS = S + NSB * SB;
-    static_assert(D % 32 == 0 && DV % 32 == 0 && D <= 256 && DV <= 256, "tcgen05 prefill shape");
+    static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, SB = 2 * kBN, COLS = S + NSB * SB;
+    static_assert(D % 32 == 0 && DVC % 32 == 0 && D <= 256 && DVC <= 128 && DV % DVC == 0, "tcgen05 prefill shape");
+    static_assert(VCHUNK_FLOATS <= SLOT_FLOATS && (DVC * 32 * 4) % 1024 == 0, "V^T chunk layout");
     static_assert(COLS <= 512, "TMEM budget");
-    static_assert(NKS >= 2 && SMEM <= kSmemLimit, "shared memory budget");
+    static_assert(NS >= 3 && SMEM <= kSmemLimit, "shared memory budget");
 };
 
 // Pairwise (tree) max and sum: short dependency chains.
@@ -178,21 +189,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
     using C = TcCfg<D, DV>;
-    constexpr int NSB = C::NSB, NKS = C::NKS, KB = C::KB;
+    constexpr int NSB = C::NSB, NS = C::NS, KB = C::KB, DVC = C::DVC;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     float* qlo = smem + C::QLO_OFF;
-    float* vsm = smem + C::V_OFF;
-    float* ksm = smem + C::K_OFF;
-    __shared__ __align__(8) uint64_t k_full[NKS], k_empty[NKS], v_full, v_empty, s_full[NSB], p_full[NSB],
-        pv_done[NSB], q_ready;
+    float* ring = smem + C::RING_OFF;
+    __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full[NSB], p_full[NSB], pv_done[NSB], q_ready;
     __shared__ uint32_t tmem_base_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (int)((a.T + kBM - 1) / kBM);
     const int qt = n_qt - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
     const int h = blockIdx.y, kh = h / a.G;
+    const int dv0 = (int)blockIdx.z * DVC;      // this CTA's V columns [dv0, dv0 + DVC)
     const int64_t t0 = (int64_t)qt * kBM;
     const int64_t t_last = (t0 + kBM < a.T ? t0 + kBM : a.T) - 1;
 
@@ -212,17 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         // One barrier per buffer: no wait ever targets a phase two behind.
-        for (int b = 0; b < NKS; ++b) {
-            mbar_init(&k_full[b], 1);
-            mbar_init(&k_empty[b], 1);
+        for (int b = 0; b < NS; ++b) {
+            mbar_init(&r_full[b], 1);
+            mbar_init(&r_empty[b], 1);
         }
         for (int b = 0; b < NSB; ++b) {
             mbar_init(&s_full[b], 1);
             mbar_init(&p_full[b], 4);
             mbar_init(&pv_done[b], 1);
         }
-        mbar_init(&v_full, 1);
-        mbar_init(&v_empty, 1);
         mbar_init(&q_ready, 4);
         fence_barrier_init();
     }
@@ -232,84 +240,111 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
+    // Both the TMA thread and the MMA thread walk the same sequence of ring
+    // items: the score step of tile j takes KB items (K_hi + K_lo of 32 dims),
+    // the P.V step takes 2 * kBN/32 (V^T_hi then V^T_lo of 32 keys).  With two
+    // S buffers the steps run S_0, then S_{j+1}, PV_j for every j.
     if (warp == 0) {
-        // ------------------------------ TMA producers -----------------------------
+        // ------------------------------ TMA producer -----------------------------
         if (lane == 0 && n_tiles > 0) {
-            // K: sub-tile c = j * KB + kb goes to slot c % NKS.
             prefetch_tensormap(&tm_khi);
             prefetch_tensormap(&tm_klo);
-            const int total = n_tiles * KB;
-            int issued = 0;
-            for (int c = 0; c < total; ++c) {
-                const int slot = c % NKS;
-                if (c >= NKS && !mbar_wait(&k_empty[slot], ((c / NKS) - 1) & 1)) {
-                    raise_device_error(&g_tc_device_error, kErrTcEmpty);
-                    break;
-                }
-                const int j = c / KB, kb = c % KB;
-                const int n0 = (int)((jt_begin + j) * kBN);
-                float* ks = ksm + slot * C::KSLOT_FLOATS;
-                mbar_arrive_expect_tx(&k_full[slot], C::KSLOT_BYTES);
-                tma_load_2d(ks, &tm_khi, kh * D + kb * 32, n0, &k_full[slot]);
-                tma_load_2d(ks + kBN * 32, &tm_klo, kh * D + kb * 32, n0, &k_full[slot]);
-                ++issued;
-            }
-            bool drained = true;
-            for (int c = issued > NKS ? issued - NKS : 0; c < issued; ++c)
-                drained &= mbar_wait(&k_full[c % NKS], (c / NKS) & 1);
-            if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
-        } else if (lane == 1 && n_tiles > 0) {
-            // V^T hi/lo of key tile j, one buffer, refilled once P.V_{j-1} is done.
             prefetch_tensormap(&tm_vhi);
             prefetch_tensormap(&tm_vlo);
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                if (j >= 1 && !mbar_wait(&v_empty, (j - 1) & 1)) {
+            int it = 0;
+            auto acquire = [&](uint32_t bytes) -> float* {
+                const int slot = it % NS;
+                if (it >= NS && !mbar_wait(&r_empty[slot], ((it / NS) - 1) & 1)) {
                     raise_device_error(&g_tc_device_error, kErrTcEmpty);
-                    break;
+                    return nullptr;
                 }
+                mbar_arrive_expect_tx(&r_full[slot], bytes);
+                return ring + slot * C::SLOT_FLOATS;
+            };
+            auto load_s = [&](int j) -> bool {
                 const int n0 = (int)((jt_begin + j) * kBN);
-                mbar_arrive_expect_tx(&v_full, C::V_BYTES);
-#pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    tma_load_2d(vsm + c * DV * 32, &tm_vhi, n0 + c * 32, kh * DV, &v_full);
-                    tma_load_2d(vsm + C::V_FLOATS + c * DV * 32, &tm_vlo, n0 + c * 32, kh * DV, &v_full);
+                for (int ki = 0; ki < C::KITEMS; ++ki) {
+                    const int nsub = KB - 2 * ki < 2 ? KB - 2 * ki : 2;
+                    float* dst = acquire((uint32_t)nsub * C::KSUB_FLOATS * sizeof(float));
+                    if (!dst) return false;
+                    for (int u = 0; u < nsub; ++u) {
+                        const int x = kh * D + (2 * ki + u) * 32;
+                        float* sub = dst + u * C::KSUB_FLOATS;
+                        tma_load_2d(sub, &tm_khi, x, n0, &r_full[it % NS]);
+                        tma_load_2d(sub + kBN * 32, &tm_klo, x, n0, &r_full[it % NS]);
+                    }
+                    ++it;
                 }
-                ++issued;
+                return true;
+            };
+            auto load_pv = [&](int j) -> bool {
+                const int n0 = (int)((jt_begin + j) * kBN);
+                for (int vi = 0; vi < C::VITEMS; ++vi) {
+                    float* dst = acquire(C::VCH * C::VCHUNK_FLOATS * sizeof(float));
+                    if (!dst) return false;
+                    for (int u = 0; u < C::VCH; ++u) {
+                        const int key = n0 + (vi * C::VCH + u) * 32;
+                        float* chunk = dst + u * C::VCHUNK_FLOATS;
+                        tma_load_2d(chunk, &tm_vhi, key, kh * DV + dv0, &r_full[it % NS]);
+                        tma_load_2d(chunk + DVC * 32, &tm_vlo, key, kh * DV + dv0, &r_full[it % NS]);
+                    }
+                    ++it;
+                }
+                return true;
+            };
+            bool ok = true;
+            if constexpr (NSB == 2) {
+                ok = load_s(0);
+                for (int j = 0; ok && j < n_tiles; ++j) ok = (j + 1 >= n_tiles || load_s(j + 1)) && load_pv(j);
+            } else {
+                for (int j = 0; ok && j < n_tiles; ++j) ok = load_s(j) && load_pv(j);
             }
-            if (issued > 0 && !mbar_wait(&v_full, (issued - 1) & 1))
-                raise_device_error(&g_tc_device_error, kErrTcDrain);
+            // Drain: every copy issued has landed before the CTA exits.
+            bool drained = true;
+            for (int c = it > NS ? it - NS : 0; c < it; ++c) drained &= mbar_wait(&r_full[c % NS], (c / NS) & 1);
+            if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
     } else if (warp == 1) {
         // ------------------------------ MMA issuer --------------------------------
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t id_s2 = idesc_tf32(kBM, 2 * kBN), id_s = idesc_tf32(kBM, kBN),
-                               id_o = idesc_tf32(kBM, DV);
+                               id_o = idesc_tf32(kBM, DVC);
             bool ok = mbar_wait(&q_ready, 0);
             if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
             tc_fence_after();
+            int it = 0;
+            auto take = [&](int item) -> float* {
+                const int slot = item % NS;
+                if (!mbar_wait(&r_full[slot], (item / NS) & 1)) {
+                    raise_device_error(&g_tc_device_error, kErrTcFull);
+                    return nullptr;
+                }
+                return ring + slot * C::SLOT_FLOATS;
+            };
             // S buffer j % NSB: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
                 const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * C::SB;
                 uint32_t acc = 0;
-                for (int kb = 0; kb < KB; ++kb) {
-                    const int c = j * KB + kb, slot = c % NKS;
-                    if (!mbar_wait(&k_full[slot], (c / NKS) & 1)) {
-                        raise_device_error(&g_tc_device_error, kErrTcFull);
-                        return false;
-                    }
+                for (int ki = 0; ki < C::KITEMS; ++ki) {
+                    const float* ks = take(it);
+                    if (!ks) return false;
                     tc_fence_after();
-                    const uint64_t b_k = smem_desc_sw128(ksm + slot * C::KSLOT_FLOATS);  // [K_hi; K_lo]
-                    const uint64_t a_lo = smem_desc_sw128(qlo + kb * kBM * 32);
-                    const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
+                    const int nsub = KB - 2 * ki < 2 ? KB - 2 * ki : 2;
+                    for (int u = 0; u < nsub; ++u) {
+                        const int kb = 2 * ki + u;
+                        const uint64_t b_k = smem_desc_sw128(ks + u * C::KSUB_FLOATS);  // [K_hi; K_lo]
+                        const uint64_t a_lo = smem_desc_sw128(qlo + kb * kBM * 32);
+                        const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ko = (uint64_t)((k * 32) >> 4);
-                        mma_tf32_ts(d, a_hi + k * 8, b_k + ko, id_s2, acc);
-                        mma_tf32_ss(d, a_lo + ko, b_k + ko, id_s, 1u);
-                        acc = 1;
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ko = (uint64_t)((k * 32) >> 4);
+                            mma_tf32_ts(d, a_hi + k * 8, b_k + ko, id_s2, acc);
+                            mma_tf32_ss(d, a_lo + ko, b_k + ko, id_s, 1u);
+                            acc = 1;
+                        }
                     }
-                    mma_commit(&k_empty[slot]);
+                    mma_commit(&r_empty[it % NS]);
+                    ++it;
                 }
                 mma_commit(&s_full[j % NSB]);
                 return true;
@@ -320,42 +355,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     return false;
                 }
-                if (!mbar_wait(&v_full, j & 1)) {
-                    raise_device_error(&g_tc_device_error, kErrTcFull);
-                    return false;
-                }
-                tc_fence_after();
                 const uint32_t p_hi = C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
+                for (int vi = 0; vi < C::VITEMS; ++vi) {
+                    const float* vs = take(it);
+                    if (!vs) return false;
+                    tc_fence_after();
 #pragma unroll
-                for (int c = 0; c < kBN / 32; ++c) {
-                    const uint64_t v_hi = smem_desc_sw128(vsm + c * DV * 32);
-                    const uint64_t v_lo = smem_desc_sw128(vsm + C::V_FLOATS + c * DV * 32);
+                    for (int u = 0; u < C::VCH; ++u) {
+                        const int c = vi * C::VCH + u;
+                        const uint64_t v_hi = smem_desc_sw128(vs + u * C::VCHUNK_FLOATS);
+                        const uint64_t v_lo = smem_desc_sw128(vs + u * C::VCHUNK_FLOATS + DVC * 32);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const uint64_t ko = (uint64_t)((k * 32) >> 4);
-                        const uint32_t col = c * 32 + k * 8;
-                        mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_hi + ko, id_o,
-                                    (j > 0 || c > 0 || k > 0) ? 1u : 0u);
-                        mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_lo + ko, id_o, 1u);
-                        mma_tf32_ts(tmem + C::O, tmem + p_lo + col, v_hi + ko, id_o, 1u);
+                        for (int k = 0; k < 4; ++k) {
+                            const uint64_t ko = (uint64_t)((k * 32) >> 4);
+                            const uint32_t col = c * 32 + k * 8;
+                            mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_hi + ko, id_o,
+                                        (j > 0 || c > 0 || k > 0) ? 1u : 0u);
+                            mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_lo + ko, id_o, 1u);
+                            mma_tf32_ts(tmem + C::O, tmem + p_lo + col, v_hi + ko, id_o, 1u);
+                        }
                     }
+                    mma_commit(&r_empty[it % NS]);
+                    ++it;
                 }
                 mma_commit(&pv_done[j % NSB]);
-                mma_commit(&v_empty);
                 return true;
             };
             if constexpr (NSB == 2) {
                 // S_{j+1} goes in before P.V_j so the tensor core computes the
                 // next scores while the softmax warps work on tile j.
                 if (ok) ok = issue_s(0);
-                for (int j = 0; ok && j < n_tiles; ++j) {
-                    if (j + 1 < n_tiles && !issue_s(j + 1)) break;
-                    if (!issue_pv(j)) break;
-                }
+                for (int j = 0; ok && j < n_tiles; ++j) ok = (j + 1 >= n_tiles || issue_s(j + 1)) && issue_pv(j);
             } else {
-                for (int j = 0; ok && j < n_tiles; ++j) {
-                    if (!issue_s(j) || !issue_pv(j)) break;
-                }
+                for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j) && issue_pv(j);
             }
         }
     } else {
@@ -481,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
 #pragma unroll 1
-                for (int c0 = 0; c0 < DV; c0 += 32) {
+                for (int c0 = 0; c0 < DVC; c0 += 32) {
                     float o[32];
                     tmem_ld32(trow + C::O + c0, o);
                     tmem_wait_ld();
@@ -505,9 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
-        float* orow = a.out + t * (int64_t)a.H * DV + (int64_t)h * DV;
+        float* orow = a.out + t * (int64_t)a.H * DV + (int64_t)h * DV + dv0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < DV; c0 += 32) {
+        for (int c0 = 0; c0 < DVC; c0 += 32) {
             float o[32];
             if (n_tiles > 0) {
                 tmem_ld32(trow + C::O + c0, o);
@@ -620,13 +652,13 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     CUtensorMap m_khi, m_klo, m_vhi, m_vlo;
     if (!encode_sw128(&m_khi, khi, a.S, (int64_t)a.Hk * D, kBN) ||
         !encode_sw128(&m_klo, klo, a.S, (int64_t)a.Hk * D, kBN) ||
-        !encode_sw128(&m_vhi, vthi, (int64_t)a.Hk * DV, s_pad, DV) ||
-        !encode_sw128(&m_vlo, vtlo, (int64_t)a.Hk * DV, s_pad, DV))
+        !encode_sw128(&m_vhi, vthi, (int64_t)a.Hk * DV, s_pad, C::DVC) ||
+        !encode_sw128(&m_vlo, vtlo, (int64_t)a.Hk * DV, s_pad, C::DVC))
         return cudaErrorInvalidValue;
     auto kern = prefill_tc_kernel<D, DV>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H);
+    dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
     kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, m_khi, m_klo, m_vhi, m_vlo);
     return cudaGetLastError();
 }
@@ -634,7 +666,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
 }  // namespace
 
 bool prefill_tc_supported(const AttnDesc& a) {
-    const bool dims = ((a.D == 32 || a.D == 64 || a.D == 96 || a.D == 128) && a.Dv == a.D) ||
+    const bool dims = ((a.D == 32 || a.D == 64 || a.D == 96 || a.D == 128 || a.D == 256) && a.Dv == a.D) ||
                       (a.D == 192 && a.Dv == 128);
     const bool out_aligned = (reinterpret_cast<uintptr_t>(a.out) & 15u) == 0;
     const bool q_aligned = (reinterpret_cast<uintptr_t>(a.q) & 15u) == 0;
@@ -665,7 +697,7 @@ cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* 
     if (e != cudaSuccess) return e;
 #define VTMU_TC(D_, DV_) \
     if (a.D == D_ && a.Dv == DV_) return launch_cfg<D_, DV_>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream);
-    VTMU_TC(32, 32) VTMU_TC(64, 64) VTMU_TC(96, 96) VTMU_TC(128, 128) VTMU_TC(192, 128)
+    VTMU_TC(32, 32) VTMU_TC(64, 64) VTMU_TC(96, 96) VTMU_TC(128, 128) VTMU_TC(192, 128) VTMU_TC(256, 256)
 #undef VTMU_TC
     return cudaErrorInvalidValue;
 }

@@ -176,7 +176,7 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
     } else if (kernel == VTMU_KERNEL_PREFILL_TF32X3) {
         if (!vtmu::prefill_tc_supported(a))
             return fail(VTMU_ERR_UNSUPPORTED,
-                        "kernel PREFILL_TF32X3 covers headDim == vHeadDim in {32,64,96,128} and headDim 192 "
+                        "kernel PREFILL_TF32X3 covers headDim == vHeadDim in {32,64,96,128,256} and headDim 192 "
                         "with vHeadDim 128, with S >= 1 "
                         "(got headDim %d, vHeadDim %d, S %lld)",
                         a.D, a.Dv, (long long)a.S);

@@ -80,7 +80,7 @@ typedef enum vtmu_bias_kind {
 /* Kernel choice.  AUTO takes the split-KV decode kernel for T == 1 (when its
  * shape table covers headDim/vHeadDim/group size), the tcgen05 3xTF32
  * prefill for T >= 64 when it covers the shape (headDim == vHeadDim in
- * {32, 64, 96, 128}, or headDim 192 with vHeadDim 128; 16-byte aligned q
+ * {32, 64, 96, 128, 256}, or headDim 192 with vHeadDim 128; 16-byte aligned q
  * and out), and the FFMA prefill otherwise.  The others force one kernel,
  * for tests and measurement. */
 typedef enum vtmu_kernel {

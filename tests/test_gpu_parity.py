@@ -336,7 +336,7 @@ TC = vtmu.VTMU_KERNEL_PREFILL_TF32X3
 def _tc_case(seed):
     g = np.random.default_rng(7000 + seed)
     H, Hk = [(1, 1), (4, 1), (4, 2), (6, 3), (8, 8), (8, 2)][seed % 6]
-    D, Dv = [(32, 32), (64, 64), (96, 96), (128, 128), (192, 128)][int(g.integers(0, 5))]
+    D, Dv = [(32, 32), (64, 64), (96, 96), (128, 128), (192, 128), (256, 256)][int(g.integers(0, 6))]
     T = int(g.integers(1, 300))
     S = int(g.integers(1, 500))
     params = dict(heads=H, headDim=D, kvHeads=Hk, vHeadDim=Dv, causal=bool(g.integers(0, 4) > 0),
@@ -378,6 +378,15 @@ def test_tensor_core_prefill_latent_shape(T, S, pos):
     """headDim 192 with vHeadDim 128 (one S buffer in TMEM)."""
     x = si.attention_inputs(T, S, 4, 4, 192, 128, 64, bias="ts")
     check(x, dict(heads=4, headDim=192, vHeadDim=128, posOffset=pos, causal=False, kernel=TC))
+
+
+@pytest.mark.parametrize("T,S,pos,window", [(128, 128, 0, 0), (200, 333, 133, 0), (1, 64, 63, 0),
+                                            (300, 300, 0, 100), (257, 1000, 743, 64)])
+def test_tensor_core_prefill_head_dim_256(T, S, pos, window):
+    """headDim = vHeadDim = 256: the V columns split over two CTAs per tile."""
+    x = si.attention_inputs(T, S, 4, 2, 256, 256, 65, sigma=2.0)
+    check(x, dict(heads=4, headDim=256, kvHeads=2, posOffset=pos, window=window, scale=1 / 16, softcap=50.0,
+                  kernel=TC))
 
 
 def test_tensor_core_prefill_masked_rows_give_zeros():
