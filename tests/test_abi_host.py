@@ -150,7 +150,7 @@ def test_tensor_core_prefill_workspace_holds_the_split_operands(lib):
 
 @host_only
 def test_tensor_core_prefill_shape_table(lib):
-    p = vtmu.make_params(256, 256, heads=4, headDim=256, kernel=vtmu.VTMU_KERNEL_PREFILL_TF32X3)
+    p = vtmu.make_params(256, 256, heads=4, headDim=160, kernel=vtmu.VTMU_KERNEL_PREFILL_TF32X3)
     e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
     assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "PREFILL_TF32X3" in str(e)
 
