@@ -30,13 +30,32 @@ __device__ __forceinline__ bool key_visible(const AttnDesc& a, int64_t p, int64_
     return true;
 }
 
+// tanh(y) for the softcap, from two identities of the hyperbolic tangent:
+// its odd Taylor series y - y^3/3 + 2y^5/15 - 17y^7/315 + 62y^9/2835 for
+// |y| < 1/4 (the first dropped term, 1382 y^11 / 155925, is below 3e-9 there)
+// and tanh|y| = (1 - e) / (1 + e) with e = exp(-2|y|) = 2^(-2|y| log2 e) on the
+// MUFU unit elsewhere.  Absolute error a few 1e-7, the order of tanhf's; both
+// tails are exact (e -> 0 gives 1).
+__device__ __forceinline__ float softcap_tanh(float y) {
+    const float ay = fabsf(y);
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(e) : "f"(ay * -2.8853900817779268f));
+    const float big = __fdividef(1.f - e, 1.f + e);
+    const float y2 = y * y;
+    float p = fmaf(y2, 62.f / 2835.f, -17.f / 315.f);
+    p = fmaf(y2, p, 2.f / 15.f);
+    p = fmaf(y2, p, -1.f / 3.f);
+    p = fmaf(y2, p, 1.f);
+    return ay < 0.25f ? y * p : copysignf(big, y);
+}
+
 // The fused epilogue, in base-2 units: scale -> softcap -> ALiBi -> bias.
 // `dot` is the raw q.k sum; `rel` = s - p; `bias_val` the bias entry (or 0).
 __device__ __forceinline__ float score_log2(const AttnDesc& a, float dot, float slope_log2,
                                             int64_t rel, float bias_val) {
     float x;
     if (a.softcap_on)
-        x = a.cap_log2 * tanhf(dot * a.qk_mul);
+        x = a.cap_log2 * softcap_tanh(dot * a.qk_mul);
     else
         x = dot * a.qk_mul;
     if (a.alibi_on) x = fmaf(slope_log2, (float)rel, x);

@@ -147,7 +147,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
     if (full) {
 #pragma unroll
         for (int i = 0; i < N; ++i) {
-            float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
             if (BIAS) v = fmaf(__ldg(bias + i), kLog2e, v);
             x[i] = v;
@@ -156,7 +156,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             const bool vis = i >= lo_i && i <= hi_i;
-            float v = SOFTCAP ? a.cap_log2 * tanhf(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
             if (BIAS) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
             x[i] = vis ? v : -INFINITY;
@@ -185,7 +185,8 @@ __device__ __forceinline__ int sw128_offset(int r, int chunk) { return r * 32 + 
 
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_khi,
+    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_q,
+                      const __grid_constant__ CUtensorMap tm_khi,
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
     using C = TcCfg<D, DV>;
@@ -195,7 +196,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* smem = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     float* qlo = smem + C::QLO_OFF;
     float* ring = smem + C::RING_OFF;
-    __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full[NSB], p_full[NSB], pv_done[NSB], q_ready;
+    __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full[NSB], p_full[NSB], pv_done[NSB], q_full,
+        q_ready;
     __shared__ uint32_t tmem_base_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -231,6 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_full[b], 4);
             mbar_init(&pv_done[b], 1);
         }
+        mbar_init(&q_full, 1);
         mbar_init(&q_ready, 4);
         fence_barrier_init();
     }
@@ -246,6 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     // S buffers the steps run S_0, then S_{j+1}, PV_j for every j.
     if (warp == 0) {
         // ------------------------------ TMA producer -----------------------------
+        if (lane == 0) {
+            // The Q tile lands in the Q_lo area (128-byte swizzled, rows past T
+            // read as zero); the softmax warps split it in place.
+            mbar_arrive_expect_tx(&q_full, (uint32_t)(kBM * D * sizeof(float)));
+            for (int kb = 0; kb < KB; ++kb) tma_load_2d(qlo + kb * kBM * 32, &tm_q, h * D + kb * 32, (int)t0, &q_full);
+        }
         if (lane == 0 && n_tiles > 0) {
             prefetch_tensormap(&tm_khi);
             prefetch_tensormap(&tm_klo);
@@ -312,39 +321,54 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = mbar_wait(&q_ready, 0);
             if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
             tc_fence_after();
-            int it = 0;
-            auto take = [&](int item) -> float* {
-                const int slot = item % NS;
-                if (!mbar_wait(&r_full[slot], (item / NS) & 1)) {
+            // Ring position (slot, phase) of the next item; descriptors are
+            // base + byte offset / 16, computed once.
+            int slot = 0;
+            uint32_t phase = 0;
+            auto take = [&]() -> bool {
+                if (!mbar_wait(&r_full[slot], phase)) {
                     raise_device_error(&g_tc_device_error, kErrTcFull);
-                    return nullptr;
+                    return false;
                 }
-                return ring + slot * C::SLOT_FLOATS;
+                tc_fence_after();
+                return true;
             };
+            auto release = [&]() {
+                mma_commit(&r_empty[slot]);
+                if (++slot == NS) {
+                    slot = 0;
+                    phase ^= 1u;
+                }
+            };
+            const uint64_t ring_d = smem_desc_sw128(ring), qlo_d = smem_desc_sw128(qlo);
+            constexpr uint64_t SLOT_D = C::SLOT_FLOATS * 4 / 16, KSUB_D = C::KSUB_FLOATS * 4 / 16,
+                               QSUB_D = kBM * 32 * 4 / 16, VCH_D = C::VCHUNK_FLOATS * 4 / 16,
+                               VLO_D = DVC * 32 * 4 / 16, KSTEP_D = 32 / 16;
             // S buffer j % NSB: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
                 const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * C::SB;
-                uint32_t acc = 0;
-                for (int ki = 0; ki < C::KITEMS; ++ki) {
-                    const float* ks = take(it);
-                    if (!ks) return false;
-                    tc_fence_after();
-                    const int nsub = KB - 2 * ki < 2 ? KB - 2 * ki : 2;
-                    for (int u = 0; u < nsub; ++u) {
-                        const int kb = 2 * ki + u;
-                        const uint64_t b_k = smem_desc_sw128(ks + u * C::KSUB_FLOATS);  // [K_hi; K_lo]
-                        const uint64_t a_lo = smem_desc_sw128(qlo + kb * kBM * 32);
-                        const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint64_t ko = (uint64_t)((k * 32) >> 4);
-                            mma_tf32_ts(d, a_hi + k * 8, b_k + ko, id_s2, acc);
-                            mma_tf32_ss(d, a_lo + ko, b_k + ko, id_s, 1u);
-                            acc = 1;
+                for (int ki = 0; ki < C::KITEMS; ++ki) {
+                    if (!take()) return false;
+                    const uint64_t b_slot = ring_d + (uint64_t)slot * SLOT_D;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const int kb = 2 * ki + u;
+                        if (kb < KB) {
+                            const uint64_t b_k = b_slot + u * KSUB_D;  // [K_hi; K_lo]
+                            const uint64_t a_lo = qlo_d + kb * QSUB_D;
+                            const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
+#pragma unroll
+                            for (int k = 0; k < 4; ++k) {
+                                if (kb == 0 && k == 0)
+                                    mma_tf32_ts(d, a_hi, b_k, id_s2, 0u);
+                                else
+                                    mma_tf32_ts_acc(d, a_hi + k * 8, b_k + k * KSTEP_D, id_s2);
+                                mma_tf32_ss_acc(d, a_lo + k * KSTEP_D, b_k + k * KSTEP_D, id_s);
+                            }
                         }
                     }
-                    mma_commit(&r_empty[it % NS]);
-                    ++it;
+                    release();
                 }
                 mma_commit(&s_full[j % NSB]);
                 return true;
@@ -355,28 +379,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     return false;
                 }
-                const uint32_t p_hi = C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
+                const uint32_t p_hi = tmem + C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
+                const uint32_t o = tmem + C::O;
+#pragma unroll
                 for (int vi = 0; vi < C::VITEMS; ++vi) {
-                    const float* vs = take(it);
-                    if (!vs) return false;
-                    tc_fence_after();
+                    if (!take()) return false;
+                    const uint64_t v_slot = ring_d + (uint64_t)slot * SLOT_D;
 #pragma unroll
                     for (int u = 0; u < C::VCH; ++u) {
                         const int c = vi * C::VCH + u;
-                        const uint64_t v_hi = smem_desc_sw128(vs + u * C::VCHUNK_FLOATS);
-                        const uint64_t v_lo = smem_desc_sw128(vs + u * C::VCHUNK_FLOATS + DVC * 32);
+                        const uint64_t v_hi = v_slot + u * VCH_D, v_lo = v_hi + VLO_D;
 #pragma unroll
                         for (int k = 0; k < 4; ++k) {
-                            const uint64_t ko = (uint64_t)((k * 32) >> 4);
                             const uint32_t col = c * 32 + k * 8;
-                            mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_hi + ko, id_o,
-                                        (j > 0 || c > 0 || k > 0) ? 1u : 0u);
-                            mma_tf32_ts(tmem + C::O, tmem + p_hi + col, v_lo + ko, id_o, 1u);
-                            mma_tf32_ts(tmem + C::O, tmem + p_lo + col, v_hi + ko, id_o, 1u);
+                            if (c == 0 && k == 0)
+                                mma_tf32_ts(o, p_hi + col, v_hi + k * KSTEP_D, id_o, j > 0 ? 1u : 0u);
+                            else
+                                mma_tf32_ts_acc(o, p_hi + col, v_hi + k * KSTEP_D, id_o);
+                            mma_tf32_ts_acc(o, p_hi + col, v_lo + k * KSTEP_D, id_o);
+                            mma_tf32_ts_acc(o, p_lo + col, v_hi + k * KSTEP_D, id_o);
                         }
                     }
-                    mma_commit(&r_empty[it % NS]);
-                    ++it;
+                    release();
                 }
                 mma_commit(&pv_done[j % NSB]);
                 return true;
@@ -398,25 +422,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool row_ok = t < a.T;
         const uint32_t trow = tmem + (lrow << 16);
         const float slope = a.alibi_on ? alibi.slope_log2[h] : 0.f;
-        // Q row -> hi (TMEM) / lo (shared memory, 128-byte swizzled).
+        // Q row (staged by TMA) -> hi (TMEM) / lo (in place, shared memory).
         {
-            const float* qrow = a.q + t * (int64_t)a.H * D + (int64_t)h * D;
+            if (!__all_sync(FULL, mbar_wait(&q_full, 0))) raise_device_error(&g_tc_device_error, kErrTcQ);
 #pragma unroll 1
             for (int kb = 0; kb < KB; ++kb) {
+                float* sub = qlo + kb * kBM * 32;
                 float hi[32], lo[32];
 #pragma unroll
-                for (int i = 0; i < 32; i += 4) {
-                    float4 v4 = row_ok ? __ldg(reinterpret_cast<const float4*>(qrow + kb * 32 + i))
-                                       : make_float4(0, 0, 0, 0);
+                for (int c = 0; c < 8; ++c) {
+                    const float4 v4 = *reinterpret_cast<const float4*>(sub + sw128_offset(r, c));
                     const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        hi[i + e] = tf32_hi(vv[e]);
-                        lo[i + e] = vv[e] - hi[i + e];
+                        hi[4 * c + e] = tf32_hi(vv[e]);
+                        lo[4 * c + e] = vv[e] - hi[4 * c + e];
                     }
                 }
                 tmem_st32(trow + C::Q_HI + kb * 32, hi);
-                float* sub = qlo + kb * kBM * 32;
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
                     *reinterpret_cast<float4*>(sub + sw128_offset(r, c)) =
@@ -474,8 +497,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > kBN ? kBN : lo64));
             const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > kBN ? kBN : hi64));
             const bool full = lo_i <= 0 && hi_i >= kBN - 1;
-            run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
-            const float mt = tree_max<kBN>(x);
+            // Plain scaled scores (no softcap, ALiBi or bias) with a positive
+            // scale: the mask alone here, and the scale goes into the exp2's FFMA.
+            const bool fold = feat == 0 && a.qk_mul > 0.f;
+            if (!fold) {
+                run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
+            } else if (!full) {
+#pragma unroll
+                for (int i = 0; i < kBN; ++i) x[i] = (i >= lo_i && i <= hi_i) ? x[i] : -INFINITY;
+            }
+            const float cx = fold ? a.qk_mul : 1.f;
+            const float mt = tree_max<kBN>(x) * cx;
             // Lazy rescale: keep the reference max unless this tile beats it by > 2^8.
             float alpha = 1.f;
             if (mt > m_ref + kRescaleLog2) {
@@ -483,14 +515,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m_ref = mt;
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
+#pragma unroll
+            for (int i = 0; i < kBN; ++i) x[i] = fast_exp2(fmaf(x[i], cx, -m_use));
+            l = fmaf(l, alpha, tree_sum<kBN>(x));
             float plo[kBN];
 #pragma unroll
             for (int i = 0; i < kBN; ++i) {
-                const float pi = fast_exp2(x[i] - m_use);
-                x[i] = tf32_hi(pi);  // P_hi replaces the score in registers
+                const float pi = x[i];
+                x[i] = tf32_hi(pi);  // P_hi replaces P in registers
                 plo[i] = pi - x[i];
             }
-            l = fmaf(l, alpha, tree_sum<kBN>(x) + tree_sum<kBN>(plo));
             // This buffer's P was last read by P.V_{j-NSB}, which ran before
             // S_j in issue order; the wait costs nothing.
             if (j >= NSB && !__all_sync(FULL, mbar_wait(&pv_done[b], ((j / NSB) - 1) & 1))) {
@@ -649,8 +683,9 @@ template <int D, int DV>
 cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, float* klo, float* vthi,
                        float* vtlo, int64_t s_pad, cudaStream_t stream) {
     using C = TcCfg<D, DV>;
-    CUtensorMap m_khi, m_klo, m_vhi, m_vlo;
-    if (!encode_sw128(&m_khi, khi, a.S, (int64_t)a.Hk * D, kBN) ||
+    CUtensorMap m_q, m_khi, m_klo, m_vhi, m_vlo;
+    if (!encode_sw128(&m_q, a.q, a.T, (int64_t)a.H * D, kBM) ||
+        !encode_sw128(&m_khi, khi, a.S, (int64_t)a.Hk * D, kBN) ||
         !encode_sw128(&m_klo, klo, a.S, (int64_t)a.Hk * D, kBN) ||
         !encode_sw128(&m_vhi, vthi, (int64_t)a.Hk * DV, s_pad, C::DVC) ||
         !encode_sw128(&m_vlo, vtlo, (int64_t)a.Hk * DV, s_pad, C::DVC))
@@ -659,7 +694,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
-    kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, m_khi, m_klo, m_vhi, m_vlo);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, m_q, m_khi, m_klo, m_vhi, m_vlo);
     return cudaGetLastError();
 }
 
