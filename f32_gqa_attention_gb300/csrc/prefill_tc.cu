@@ -69,6 +69,9 @@ constexpr int kBN = 64;       // keys per tile = score MMA N
 constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
 constexpr size_t kSmemLimit = 227 * 1024;
+#ifndef VTMU_TC_BSTAGE_MAX_D
+#define VTMU_TC_BSTAGE_MAX_D 192  // widest headDim that stages bias blocks in shared memory
+#endif
 #ifndef VTMU_TC_MAX_SLOTS
 #define VTMU_TC_MAX_SLOTS 6  // shared-memory ring slots (32 KB each) at most
 #endif
@@ -99,10 +102,16 @@ struct TcCfg {
     static constexpr int VCH = 2 * VCHUNK_FLOATS <= SLOT_FLOATS ? 2 : 1;
     static constexpr int VITEMS = (kBN / 32) / VCH;
     static constexpr uint32_t SLOT_BYTES = SLOT_FLOATS * sizeof(float);
-    static constexpr size_t FIXED = (size_t)QLO_FLOATS * sizeof(float) + 1024;
+    // Bias blocks staged by TMA: per softmax warp 32 rows x 64 keys as two
+    // 128-byte-swizzled [32 x 32] boxes (headDim <= 192; wider heads leave no
+    // room next to Q_lo and three ring slots, and read the bias from global).
+    static constexpr bool BSTAGE = D <= VTMU_TC_BSTAGE_MAX_D;
+    static constexpr int BWARP_FLOATS = 32 * kBN;
+    static constexpr int BIAS_FLOATS = BSTAGE ? 4 * BWARP_FLOATS : 0;
+    static constexpr size_t FIXED = (size_t)(QLO_FLOATS + BIAS_FLOATS) * sizeof(float) + 1024;
     static constexpr int NS_FIT = (int)((kSmemLimit - FIXED) / SLOT_BYTES);
     static constexpr int NS = NS_FIT > VTMU_TC_MAX_SLOTS ? VTMU_TC_MAX_SLOTS : NS_FIT;  // ring slots
-    static constexpr int QLO_OFF = 0, RING_OFF = QLO_FLOATS;
+    static constexpr int QLO_OFF = 0, BIAS_OFF = QLO_FLOATS, RING_OFF = QLO_FLOATS + BIAS_FLOATS;
     static constexpr size_t SMEM = FIXED + (size_t)NS * SLOT_BYTES;
     // TMEM columns
     static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, SB = 2 * kBN, COLS = S + NSB * SB;
@@ -137,19 +146,37 @@ __device__ __forceinline__ float tree_sum(const float (&v)[N]) {
     return m[0];
 }
 
+// Element (row r, k) of a [rows x 32] f32 tile stored K-major with the
+// 128-byte swizzle: rows of 128 B, 16-byte chunk c of row r at chunk c ^ (r % 8).
+__device__ __forceinline__ int sw128_offset(int r, int chunk) { return r * 32 + ((chunk ^ (r & 7)) << 2); }
+
 // The fused score epilogue over one key tile of one query row, in base 2:
 // scale (or softcap), ALiBi, bias, then the mask -- slots outside
 // [lo_i, hi_i] become -inf.  `full` tiles skip the mask.  Features are
 // template flags so that each combination compiles to straight-line code.
-template <bool SOFTCAP, bool ALIBI, bool BIAS, int N>
+// BIAS: 0 none; 1 `bias` is this row's bias at the tile's first key (global);
+// 2 `bias` is the warp's staged block, row = lane, read as swizzled float4s.
+template <int BIAS>
+__device__ __forceinline__ float bias_slot(const float* bias, int i, float (&b4)[4]) {
+    if constexpr (BIAS == 1) return __ldg(bias + i);
+    if ((i & 3) == 0) {
+        const float4 t = *reinterpret_cast<const float4*>(bias + (i >> 5) * 1024 +
+                                                          sw128_offset(threadIdx.x & 31, (i & 31) >> 2));
+        b4[0] = t.x; b4[1] = t.y; b4[2] = t.z; b4[3] = t.w;
+    }
+    return b4[i & 3];
+}
+
+template <bool SOFTCAP, bool ALIBI, int BIAS, int N>
 __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], float slope, int rel0,
                                               const float* bias, int lo_i, int hi_i, bool full) {
+    float b4[4] = {0.f, 0.f, 0.f, 0.f};
     if (full) {
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
-            if (BIAS) v = fmaf(__ldg(bias + i), kLog2e, v);
+            if (BIAS) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
             x[i] = v;
         }
     } else {
@@ -158,7 +185,8 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
             const bool vis = i >= lo_i && i <= hi_i;
             float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
-            if (BIAS) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
+            if (BIAS == 1) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
+            if (BIAS == 2) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
             x[i] = vis ? v : -INFINITY;
         }
     }
@@ -168,24 +196,33 @@ template <int N>
 __device__ __forceinline__ void run_epilogue(int feat, const AttnDesc& a, float (&x)[N], float slope, int rel0,
                                              const float* bias, int lo_i, int hi_i, bool full) {
     switch (feat) {
-        case 0: tile_epilogue<false, false, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 1: tile_epilogue<true, false, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 2: tile_epilogue<false, true, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 3: tile_epilogue<true, true, false>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 4: tile_epilogue<false, false, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 5: tile_epilogue<true, false, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        case 6: tile_epilogue<false, true, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
-        default: tile_epilogue<true, true, true>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 0: tile_epilogue<false, false, 0>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 1: tile_epilogue<true, false, 0>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 2: tile_epilogue<false, true, 0>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 3: tile_epilogue<true, true, 0>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 4: tile_epilogue<false, false, 1>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 5: tile_epilogue<true, false, 1>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        case 6: tile_epilogue<false, true, 1>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
+        default: tile_epilogue<true, true, 1>(a, x, slope, rel0, bias, lo_i, hi_i, full); break;
     }
 }
 
-// Element (row r, k) of a [rows x 32] f32 tile stored K-major with the
-// 128-byte swizzle: rows of 128 B, 16-byte chunk c of row r at chunk c ^ (r % 8).
-__device__ __forceinline__ int sw128_offset(int r, int chunk) { return r * 32 + ((chunk ^ (r & 7)) << 2); }
+// The same with the bias read from the warp's staged block.
+template <int N>
+__device__ __forceinline__ void run_epilogue_staged(int feat, const AttnDesc& a, float (&x)[N], float slope,
+                                                    int rel0, const float* block, int lo_i, int hi_i, bool full) {
+    switch (feat & 3) {
+        case 0: tile_epilogue<false, false, 2>(a, x, slope, rel0, block, lo_i, hi_i, full); break;
+        case 1: tile_epilogue<true, false, 2>(a, x, slope, rel0, block, lo_i, hi_i, full); break;
+        case 2: tile_epilogue<false, true, 2>(a, x, slope, rel0, block, lo_i, hi_i, full); break;
+        default: tile_epilogue<true, true, 2>(a, x, slope, rel0, block, lo_i, hi_i, full); break;
+    }
+}
 
 template <int D, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const __grid_constant__ CUtensorMap tm_q,
+    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const int bias_staged,
+                      const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_bias,
                       const __grid_constant__ CUtensorMap tm_khi,
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
@@ -197,7 +234,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* qlo = smem + C::QLO_OFF;
     float* ring = smem + C::RING_OFF;
     __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full[NSB], p_full[NSB], pv_done[NSB], q_full,
-        q_ready;
+        q_ready, b_full[4];
     __shared__ uint32_t tmem_base_s;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -235,6 +272,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(&q_full, 1);
         mbar_init(&q_ready, 4);
+        for (int b = 0; b < 4; ++b) mbar_init(&b_full[b], 1);
         fence_barrier_init();
     }
     if (warp == 1) tmem_alloc(&tmem_base_s, 512);
@@ -469,6 +507,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float* brow = a.bias_kind == 0 ? nullptr
                             : a.bias_kind == 1 ? a.bias + t * a.S
                                                : a.bias + ((int64_t)h * a.T + t) * a.S;
+        // Staged bias: lane 0 of each softmax warp loads the warp's 32 rows x 64
+        // keys of tile j + 1 as soon as the epilogue of tile j has read tile j's.
+        const bool bstage = C::BSTAGE && bias_staged && a.bias_kind != 0;
+        const int wq = warp & 3;
+        float* bbuf = smem + C::BIAS_OFF + wq * C::BWARP_FLOATS;
+        const int brow0 = (int)((a.bias_kind == 2 ? (int64_t)h * a.T : 0) + t0) + 32 * wq;
+        int b_issued = 0;  // bias blocks requested (tiles 0 .. b_issued - 1)
+        auto issue_bias = [&](int j) {
+            if (lane == 0) {
+                const int n0 = (int)((jt_begin + j) * kBN);
+                mbar_arrive_expect_tx(&b_full[wq], (uint32_t)(C::BWARP_FLOATS * sizeof(float)));
+                tma_load_2d(bbuf, &tm_bias, n0, brow0, &b_full[wq]);
+                tma_load_2d(bbuf + 32 * 32, &tm_bias, n0 + 32, brow0, &b_full[wq]);
+            }
+            ++b_issued;
+        };
+        if (bstage && n_tiles > 0) issue_bias(0);
         const int feat = (a.softcap_on ? 1 : 0) | (a.alibi_on ? 2 : 0) | (a.bias_kind ? 4 : 0);
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
@@ -476,6 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int b = j % NSB;
             if (!__all_sync(FULL, mbar_wait(&s_full[b], (j / NSB) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcS);
+                ok = false;
+                break;
+            }
+            if (bstage && !__all_sync(FULL, mbar_wait(&b_full[wq], j & 1))) {
+                raise_device_error(&g_tc_device_error, kErrTcFull);
                 ok = false;
                 break;
             }
@@ -501,7 +561,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             // scale: the mask alone here, and the scale goes into the exp2's FFMA.
             const bool fold = feat == 0 && a.qk_mul > 0.f;
             if (!fold) {
-                run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
+                if (!bstage) {
+                    run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
+                } else {
+                    run_epilogue_staged<kBN>(feat, a, x, slope, (int)(n0 - p), bbuf, lo_i, hi_i, full);
+                }
+                if (bstage && j + 1 < n_tiles) {
+                    // The block has been read (generic proxy) before TMA refills it.
+                    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+                    __syncwarp();
+                    issue_bias(j + 1);
+                }
             } else if (!full) {
 #pragma unroll
                 for (int i = 0; i < kBN; ++i) x[i] = (i >= lo_i && i <= hi_i) ? x[i] : -INFINITY;
@@ -561,6 +631,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[b]);
         }
+        // No bias block may still be in flight when the CTA exits (a loop
+        // that stopped early can leave one).
+        if (bstage && b_issued > 0 && !__all_sync(FULL, mbar_wait(&b_full[wq], (b_issued - 1) & 1)))
+            raise_device_error(&g_tc_device_error, kErrTcDrain);
         // Epilogue: O / l -> out.
         if (ok && n_tiles > 0) {
             const int last = n_tiles - 1;
@@ -683,7 +757,15 @@ template <int D, int DV>
 cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, float* klo, float* vthi,
                        float* vtlo, int64_t s_pad, cudaStream_t stream) {
     using C = TcCfg<D, DV>;
-    CUtensorMap m_q, m_khi, m_klo, m_vhi, m_vlo;
+    CUtensorMap m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo;
+    // The bias goes through TMA when a row of it starts on a 16-byte boundary.
+    std::memset(&m_bias, 0, sizeof(m_bias));
+    int bias_staged = 0;
+    if (C::BSTAGE && a.bias_kind != 0 && (reinterpret_cast<uintptr_t>(a.bias) & 15u) == 0 && a.S % 4 == 0) {
+        const int64_t rows = a.bias_kind == 2 ? (int64_t)a.H * a.T : a.T;
+        if (!encode_sw128(&m_bias, a.bias, rows, a.S, 32)) return cudaErrorInvalidValue;
+        bias_staged = 1;
+    }
     if (!encode_sw128(&m_q, a.q, a.T, (int64_t)a.H * D, kBM) ||
         !encode_sw128(&m_khi, khi, a.S, (int64_t)a.Hk * D, kBN) ||
         !encode_sw128(&m_klo, klo, a.S, (int64_t)a.Hk * D, kBN) ||
@@ -694,7 +776,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
-    kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, m_q, m_khi, m_klo, m_vhi, m_vlo);
+    kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, bias_staged, m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo);
     return cudaGetLastError();
 }
 
