@@ -171,11 +171,15 @@ template <bool SOFTCAP, bool ALIBI, int BIAS, int N>
 __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], float slope, int rel0,
                                               const float* bias, int lo_i, int hi_i, bool full) {
     float b4[4] = {0.f, 0.f, 0.f, 0.f};
+    // ALiBi distance of slot i as (float)rel0 + i: the same value as
+    // (float)(rel0 + i) while distances stay below 2^24, without an int ->
+    // float conversion per slot.
+    const float frel0 = (float)rel0;
     if (full) {
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
-            if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
+            if (ALIBI) v = fmaf(slope, frel0 + (float)i, v);
             if (BIAS) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
             x[i] = v;
         }
@@ -184,7 +188,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
         for (int i = 0; i < N; ++i) {
             const bool vis = i >= lo_i && i <= hi_i;
             float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
-            if (ALIBI) v = fmaf(slope, (float)(rel0 + i), v);
+            if (ALIBI) v = fmaf(slope, frel0 + (float)i, v);
             if (BIAS == 1) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
             if (BIAS == 2) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
             x[i] = vis ? v : -INFINITY;
@@ -258,6 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (s_lo < 0) s_lo = 0;
     const int64_t jt_begin = s_lo / kBN;
     const int n_tiles = (s_hi >= s_lo) ? (int)(s_hi / kBN + 1 - jt_begin) : 0;
+    // Key tiles run from the last (nearest the diagonal) down: with ALiBi the
+    // largest scores come first and the running max rarely moves, so O is
+    // seldom rescaled.  The producer, the MMA thread and the softmax share it.
+    auto tile_key0 = [&](int j) -> int64_t { return (jt_begin + (n_tiles - 1 - j)) * kBN; };
 
     if (threadIdx.x == 0) {
         // One barrier per buffer: no wait ever targets a phase two behind.
@@ -309,7 +317,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return ring + slot * C::SLOT_FLOATS;
             };
             auto load_s = [&](int j) -> bool {
-                const int n0 = (int)((jt_begin + j) * kBN);
+                const int n0 = (int)tile_key0(j);
                 for (int ki = 0; ki < C::KITEMS; ++ki) {
                     const int nsub = KB - 2 * ki < 2 ? KB - 2 * ki : 2;
                     float* dst = acquire((uint32_t)nsub * C::KSUB_FLOATS * sizeof(float));
@@ -325,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             auto load_pv = [&](int j) -> bool {
-                const int n0 = (int)((jt_begin + j) * kBN);
+                const int n0 = (int)tile_key0(j);
                 for (int vi = 0; vi < C::VITEMS; ++vi) {
                     float* dst = acquire(C::VCH * C::VCHUNK_FLOATS * sizeof(float));
                     if (!dst) return false;
@@ -516,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b_issued = 0;  // bias blocks requested (tiles 0 .. b_issued - 1)
         auto issue_bias = [&](int j) {
             if (lane == 0) {
-                const int n0 = (int)((jt_begin + j) * kBN);
+                const int n0 = (int)tile_key0(j);
                 mbar_arrive_expect_tx(&b_full[wq], (uint32_t)(C::BWARP_FLOATS * sizeof(float)));
                 tma_load_2d(bbuf, &tm_bias, n0, brow0, &b_full[wq]);
                 tma_load_2d(bbuf + 32 * 32, &tm_bias, n0 + 32, brow0, &b_full[wq]);
@@ -551,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[h2 + i] += y[i];
             }
-            const int64_t n0 = (jt_begin + j) * kBN;
+            const int64_t n0 = tile_key0(j);
             // Visible slots of this tile, clamped to [-1, kBN].
             const int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
             const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > kBN ? kBN : lo64));
