@@ -14,36 +14,35 @@
 //    own layout and V^T_hi / V^T_lo transposed to [kvHeads*vHeadDim, S],
 //    so every tile the MMAs read is K-major;
 //  * one CTA owns 128 query rows of one head (the MMA M); per key tile of
-//    BN = 64 keys:
-//      S_j  = Q K_j^T          (TMEM accumulator, M=128 x N=64)
+//    BN = 64 keys, visited from the diagonal down:
+//      S_j  = Q K_j^T          (TMEM accumulator, M=128)
 //      P_j  = softmax part     (4 warps; thread = query row = TMEM lane)
-//      O   += P_j V_j          (TMEM accumulator, M=128 x N=vHeadDim)
-//    A kind::tf32 MMA takes at least ~46 cycles to issue whatever its N, so
-//    the score MMAs use N = 64 (70 % of the tensor rate; N = 32 reaches 35 %);
+//      O   += P_j V_j          (TMEM accumulator, M=128 x N=vHeadDim share)
 //  * operands: Q_hi and P_hi / P_lo in TMEM (A operand of the TS-form MMA),
 //    Q_lo in shared memory (A operand of the SS-form MMA of the third
 //    product), K and V^T hi/lo in shared memory (B operand); every shared
-//    tile is K-major with the 128-byte swizzle;
-//  * the two products with Q_hi come from ONE MMA: each K ring slot holds
+//    tile is K-major with the 128-byte swizzle.  The Q tile itself arrives
+//    by TMA and is split in place;
+//  * the two products with Q_hi come from ONE MMA: each K sub-tile holds
 //    the 64 K_hi rows followed by the 64 K_lo rows, i.e. a 128-row B operand,
 //    so Q_hi.[K_hi; K_lo]^T lands as [S_hihi | S_hilo] in 128 TMEM columns at
 //    the full N = 128 tensor rate; the third product Q_lo.K_hi (N = 64)
 //    accumulates into the first half and the softmax adds the two halves;
 //  * TMEM columns: Q_hi | O | S_0 | S_1 with 128-column S buffers, i.e.
-//    headDim + vHeadDim + 128 * NSB <= 512; P_hi and P_lo of a tile are
-//    written over the two halves of its S buffer.  With two buffers
+//    headDim + vHeadDim share + 128 * NSB <= 512; P_hi and P_lo of a tile
+//    are written over the two halves of its S buffer.  With two buffers
 //    (headDim <= 128) the softmax of tile j runs while the tensor core
-//    computes the scores of tile j+1; headDim 192 has room for one;
-//  * warp 0: lane 0 streams K through a ring of 32-dim sub-tiles (hi + lo,
-//    16 KB each) by TMA, lane 1 loads the V^T hi/lo tile of each key tile
-//    into one buffer; warp 1 owns TMEM and one thread issues every MMA;
-//    warps 2-5 load Q (hi into TMEM, lo into shared memory), run the
+//    computes the scores of tile j+1; headDim 192 and 256 have room for one
+//    (at 256 vHeadDim is split over grid.z: two CTAs, each half of P.V);
+//  * warp 0 lane 0 streams every K and V^T tile by TMA through one ring of
+//    32 KB items, in the order the MMAs consume them; warp 1 owns TMEM and
+//    one of its threads issues the score MMAs, one thread of warp 6 the P.V
+//    MMAs (with one S buffer warp 1 issues both); warps 2-5 split Q, run the
 //    tile-specialised epilogue and online softmax (base 2, O rescaled only
 //    when a row max grows by more than 2^8), write P hi/lo into TMEM and
-//    finally normalise and store O.
+//    finally normalise and store O;
 //  * P of tile j overwrites its own S buffer once the scores are in
-//    registers.  The MMAs of one thread execute in issue order, so the next
-//    score MMA into that buffer (issued after P.V_j) runs after P.V_j read it.
+//    registers; the score MMAs of tile j + 2 wait until P.V_j has read it.
 //
 // Every wait is bounded (tma_sync.cuh); a wait that gives up sets a bit of
 // g_tc_device_error and the kernel unwinds.
@@ -66,7 +65,7 @@ namespace {
 
 constexpr int kBM = 128;      // query rows per CTA = MMA M = TMEM lanes
 constexpr int kBN = 64;       // keys per tile = score MMA N
-constexpr int kThreads = 192; // warp 0 TMA, warp 1 MMA, warps 2-5 softmax
+constexpr int kThreads = 224; // warp 0 TMA, warp 1 score MMAs, warps 2-5 softmax, warp 6 P.V MMAs
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
 constexpr size_t kSmemLimit = 227 * 1024;
 #ifndef VTMU_TC_BSTAGE_MAX_D
@@ -264,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = (s_hi >= s_lo) ? (int)(s_hi / kBN + 1 - jt_begin) : 0;
     // Key tiles run from the last (nearest the diagonal) down: with ALiBi the
     // largest scores come first and the running max rarely moves, so O is
-    // seldom rescaled.  The producer, the MMA thread and the softmax share it.
+    // seldom rescaled.  The producer, the MMA threads and the softmax share it.
     auto tile_key0 = [&](int j) -> int64_t { return (jt_begin + (n_tiles - 1 - j)) * kBN; };
 
     if (threadIdx.x == 0) {
@@ -289,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = tmem_base_s;
 
-    // Both the TMA thread and the MMA thread walk the same sequence of ring
+    // The TMA thread and the MMA threads walk the same sequence of ring
     // items: the score step of tile j takes KB items (K_hi + K_lo of 32 dims),
     // the P.V step takes 2 * kBN/32 (V^T_hi then V^T_lo of 32 keys).  With two
     // S buffers the steps run S_0, then S_{j+1}, PV_j for every j.
@@ -359,33 +358,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = it > NS ? it - NS : 0; c < it; ++c) drained &= mbar_wait(&r_full[c % NS], (c / NS) & 1);
             if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
-    } else if (warp == 1) {
-        // ------------------------------ MMA issuer --------------------------------
+    } else if (warp == 1 || warp == 6) {
+        // ------------- MMA issuers: warp 1 the scores, warp 6 P.V (two S buffers) -------------
+        // One kind::tf32 MMA issues at most every ~53 cycles from one thread, so
+        // with two S buffers the score and P.V streams come from two threads
+        // (two warps) and meet in the tensor pipe.  Both index the ring sequence
+        // of the TMA thread: item numbers follow from the step order above.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t id_s2 = idesc_tf32(kBM, 2 * kBN), id_s = idesc_tf32(kBM, kBN),
                                id_o = idesc_tf32(kBM, DVC);
-            bool ok = mbar_wait(&q_ready, 0);
-            if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
-            tc_fence_after();
-            // Ring position (slot, phase) of the next item; descriptors are
-            // base + byte offset / 16, computed once.
-            int slot = 0;
-            uint32_t phase = 0;
-            auto take = [&]() -> bool {
-                if (!mbar_wait(&r_full[slot], phase)) {
+            constexpr int KI = C::KITEMS, VI = C::VITEMS;
+            auto s_first = [&](int j) -> int {
+                return NSB == 2 ? (j == 0 ? 0 : KI + (j - 1) * (KI + VI)) : j * (KI + VI);
+            };
+            auto pv_first = [&](int j) -> int {
+                return NSB == 2 ? KI + j * (KI + VI) + (j + 1 < n_tiles ? KI : 0) : j * (KI + VI) + KI;
+            };
+            auto take = [&](int item) -> bool {
+                if (!mbar_wait(&r_full[item % NS], (uint32_t)(item / NS) & 1u)) {
                     raise_device_error(&g_tc_device_error, kErrTcFull);
                     return false;
                 }
                 tc_fence_after();
                 return true;
             };
-            auto release = [&]() {
-                mma_commit(&r_empty[slot]);
-                if (++slot == NS) {
-                    slot = 0;
-                    phase ^= 1u;
-                }
-            };
+            // Descriptors are base + byte offset / 16, computed once.
             const uint64_t ring_d = smem_desc_sw128(ring), qlo_d = smem_desc_sw128(qlo);
             constexpr uint64_t SLOT_D = C::SLOT_FLOATS * 4 / 16, KSUB_D = C::KSUB_FLOATS * 4 / 16,
                                QSUB_D = kBM * 32 * 4 / 16, VCH_D = C::VCHUNK_FLOATS * 4 / 16,
@@ -393,10 +390,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             // S buffer j % NSB: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
                 const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * C::SB;
+                const int it0 = s_first(j);
 #pragma unroll
-                for (int ki = 0; ki < C::KITEMS; ++ki) {
-                    if (!take()) return false;
-                    const uint64_t b_slot = ring_d + (uint64_t)slot * SLOT_D;
+                for (int ki = 0; ki < KI; ++ki) {
+                    const int item = it0 + ki;
+                    if (!take(item)) return false;
+                    const uint64_t b_slot = ring_d + (uint64_t)(item % NS) * SLOT_D;
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const int kb = 2 * ki + u;
@@ -414,23 +413,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                     }
-                    release();
+                    mma_commit(&r_empty[item % NS]);
                 }
                 mma_commit(&s_full[j % NSB]);
                 return true;
             };
             // O += P_hi V_hi + P_hi V_lo + P_lo V_hi for tile j.
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait(&p_full[j % NSB], (j / NSB) & 1)) {
+                if (!mbar_wait(&p_full[j % NSB], (uint32_t)(j / NSB) & 1u)) {
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     return false;
                 }
-                const uint32_t p_hi = tmem + C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
                 const uint32_t o = tmem + C::O;
+                const uint32_t p_hi = tmem + C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
+                const int it0 = pv_first(j);
 #pragma unroll
-                for (int vi = 0; vi < C::VITEMS; ++vi) {
-                    if (!take()) return false;
-                    const uint64_t v_slot = ring_d + (uint64_t)slot * SLOT_D;
+                for (int vi = 0; vi < VI; ++vi) {
+                    const int item = it0 + vi;
+                    if (!take(item)) return false;
+                    const uint64_t v_slot = ring_d + (uint64_t)(item % NS) * SLOT_D;
 #pragma unroll
                     for (int u = 0; u < C::VCH; ++u) {
                         const int c = vi * C::VCH + u;
@@ -446,18 +447,37 @@ __global__ void __launch_bounds__(kThreads, 1)
                             mma_tf32_ts_acc(o, p_lo + col, v_hi + k * KSTEP_D, id_o);
                         }
                     }
-                    release();
+                    mma_commit(&r_empty[item % NS]);
                 }
                 mma_commit(&pv_done[j % NSB]);
                 return true;
             };
-            if constexpr (NSB == 2) {
-                // S_{j+1} goes in before P.V_j so the tensor core computes the
-                // next scores while the softmax warps work on tile j.
-                if (ok) ok = issue_s(0);
-                for (int j = 0; ok && j < n_tiles; ++j) ok = (j + 1 >= n_tiles || issue_s(j + 1)) && issue_pv(j);
-            } else {
-                for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j) && issue_pv(j);
+            if (warp == 1) {
+                bool ok = mbar_wait(&q_ready, 0);
+                if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
+                tc_fence_after();
+                if constexpr (NSB == 2) {
+                    // Scores only.  S_j reuses the buffer of P_{j-2}: it waits until
+                    // P.V_{j-2} (the other thread's) has read it.
+                    for (int j = 0; ok && j < n_tiles; ++j) {
+                        if (j >= 2) {
+                            ok = mbar_wait(&pv_done[j % 2], (uint32_t)((j - 2) / 2) & 1u);
+                            if (!ok) {
+                                raise_device_error(&g_tc_device_error, kErrTcPv);
+                                break;
+                            }
+                            tc_fence_after();
+                        }
+                        ok = issue_s(j);
+                    }
+                } else {
+                    // One S buffer: the two steps alternate anyway, so one thread
+                    // issues both; in issue order P.V_j reads P_j before S_{j+1}.
+                    for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j) && issue_pv(j);
+                }
+            } else if (NSB == 2) {
+                bool ok = true;
+                for (int j = 0; ok && j < n_tiles; ++j) ok = issue_pv(j);
             }
         }
     } else {
