@@ -28,21 +28,20 @@
 //    so Q_hi.[K_hi; K_lo]^T lands as [S_hihi | S_hilo] in 128 TMEM columns at
 //    the full N = 128 tensor rate; the third product Q_lo.K_hi (N = 64)
 //    accumulates into the first half and the softmax adds the two halves;
-//  * TMEM columns: Q_hi | O | S_0 | S_1 with 128-column S buffers, i.e.
-//    headDim + vHeadDim share + 128 * NSB <= 512; P_hi and P_lo of a tile
-//    are written over the two halves of its S buffer.  With two buffers
-//    (headDim <= 128) the softmax of tile j runs while the tensor core
-//    computes the scores of tile j+1; headDim 192 and 256 have room for one
-//    (at 256 vHeadDim is split over grid.z: two CTAs, each half of P.V);
+//  * TMEM columns: Q_hi | O | S | P with 128-column S and P buffers when they
+//    fit (headDim + vHeadDim share <= 256): the score MMAs of tile j+1 start
+//    as soon as the softmax has read S_j, and run while it works on tile j;
+//    P_j (hi | lo) waits only for P.V_{j-1}.  At headDim 192 and 256 there is
+//    room for one 128-column buffer, P is written over S and the steps
+//    alternate (at 256 vHeadDim is split over grid.z: two CTAs, each half of
+//    P.V);
 //  * warp 0 lane 0 streams every K and V^T tile by TMA through one ring of
 //    32 KB items, in the order the MMAs consume them; warp 1 owns TMEM and
 //    one of its threads issues the score MMAs, one thread of warp 6 the P.V
-//    MMAs (with one S buffer warp 1 issues both); warps 2-5 split Q, run the
+//    MMAs (with P over S warp 1 issues both); warps 2-5 split Q, run the
 //    tile-specialised epilogue and online softmax (base 2, O rescaled only
 //    when a row max grows by more than 2^8), write P hi/lo into TMEM and
-//    finally normalise and store O;
-//  * P of tile j overwrites its own S buffer once the scores are in
-//    registers; the score MMAs of tile j + 2 wait until P.V_j has read it.
+//    finally normalise and store O.
 //
 // Every wait is bounded (tma_sync.cuh); a wait that gives up sets a bit of
 // g_tc_device_error and the kernel unwinds.
@@ -89,7 +88,9 @@ template <int D, int DV>
 struct TcCfg {
     static constexpr int DVC = DV <= 128 ? DV : DV / 2;       // V columns per CTA (grid.z = DV / DVC)
     static constexpr int KB = D / 32;                          // 32-dim K sub-tiles per key tile
-    static constexpr int NSB = (D + DVC + 256 <= 512) ? 2 : 1; // 128-column S/P buffers that fit in TMEM
+    // Separate 128-column S and P buffers when TMEM has room (headDim <= 128):
+    // the next score MMAs may then start once the softmax has read S.
+    static constexpr bool SPLIT = D + DVC + 4 * kBN <= 512;
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
     // Ring slots of 32 KB.  A K item holds two 32-dim sub-tiles, each K_hi
     // (64 rows) then K_lo (64 rows); a V item holds V^T_hi then V^T_lo of
@@ -113,7 +114,8 @@ struct TcCfg {
     static constexpr int QLO_OFF = 0, BIAS_OFF = QLO_FLOATS, RING_OFF = QLO_FLOATS + BIAS_FLOATS;
     static constexpr size_t SMEM = FIXED + (size_t)NS * SLOT_BYTES;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, SB = 2 * kBN, COLS = S + NSB * SB;
+    static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, P = SPLIT ? S + 2 * kBN : S,
+                              COLS = S + (SPLIT ? 4 : 2) * kBN;
     static_assert(D % 32 == 0 && DVC % 32 == 0 && D <= 256 && DVC <= 128 && DV % DVC == 0, "tcgen05 prefill shape");
     static_assert(VCHUNK_FLOATS <= SLOT_FLOATS && (DVC * 32 * 4) % 1024 == 0, "V^T chunk layout");
     static_assert(COLS <= 512, "TMEM budget");
@@ -230,13 +232,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
                       const __grid_constant__ CUtensorMap tm_vlo) {
     using C = TcCfg<D, DV>;
-    constexpr int NSB = C::NSB, NS = C::NS, KB = C::KB, DVC = C::DVC;
+    constexpr int NS = C::NS, KB = C::KB, DVC = C::DVC;
     constexpr unsigned FULL = 0xffffffffu;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     float* smem = reinterpret_cast<float*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
     float* qlo = smem + C::QLO_OFF;
     float* ring = smem + C::RING_OFF;
-    __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full[NSB], p_full[NSB], pv_done[NSB], q_full,
+    __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full, s_free, p_full, pv_done, q_full,
         q_ready, b_full[4];
     __shared__ uint32_t tmem_base_s;
 
@@ -272,11 +274,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&r_full[b], 1);
             mbar_init(&r_empty[b], 1);
         }
-        for (int b = 0; b < NSB; ++b) {
-            mbar_init(&s_full[b], 1);
-            mbar_init(&p_full[b], 4);
-            mbar_init(&pv_done[b], 1);
-        }
+        // Each completes once per key tile: tile j waits on phase j & 1.
+        mbar_init(&s_full, 1);
+        mbar_init(&s_free, 4);
+        mbar_init(&p_full, 4);
+        mbar_init(&pv_done, 1);
         mbar_init(&q_full, 1);
         mbar_init(&q_ready, 4);
         for (int b = 0; b < 4; ++b) mbar_init(&b_full[b], 1);
@@ -289,9 +291,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
 
     // The TMA thread and the MMA threads walk the same sequence of ring
-    // items: the score step of tile j takes KB items (K_hi + K_lo of 32 dims),
-    // the P.V step takes 2 * kBN/32 (V^T_hi then V^T_lo of 32 keys).  With two
-    // S buffers the steps run S_0, then S_{j+1}, PV_j for every j.
+    // items: the score step of tile j takes KITEMS items (K_hi + K_lo of two
+    // 32-dim sub-tiles each), the P.V step VITEMS (V^T_hi and V^T_lo of VCH
+    // 32-key chunks each).  With two S buffers the steps run S_0, then
+    // S_{j+1}, PV_j for every j; with one, S_j, PV_j.
     if (warp == 0) {
         // ------------------------------ TMA producer -----------------------------
         if (lane == 0) {
@@ -347,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 return true;
             };
             bool ok = true;
-            if constexpr (NSB == 2) {
+            if constexpr (C::SPLIT) {
                 ok = load_s(0);
                 for (int j = 0; ok && j < n_tiles; ++j) ok = (j + 1 >= n_tiles || load_s(j + 1)) && load_pv(j);
             } else {
@@ -369,10 +372,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                                id_o = idesc_tf32(kBM, DVC);
             constexpr int KI = C::KITEMS, VI = C::VITEMS;
             auto s_first = [&](int j) -> int {
-                return NSB == 2 ? (j == 0 ? 0 : KI + (j - 1) * (KI + VI)) : j * (KI + VI);
+                return C::SPLIT ? (j == 0 ? 0 : KI + (j - 1) * (KI + VI)) : j * (KI + VI);
             };
             auto pv_first = [&](int j) -> int {
-                return NSB == 2 ? KI + j * (KI + VI) + (j + 1 < n_tiles ? KI : 0) : j * (KI + VI) + KI;
+                return C::SPLIT ? KI + j * (KI + VI) + (j + 1 < n_tiles ? KI : 0) : j * (KI + VI) + KI;
             };
             auto take = [&](int item) -> bool {
                 if (!mbar_wait(&r_full[item % NS], (uint32_t)(item / NS) & 1u)) {
@@ -387,9 +390,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint64_t SLOT_D = C::SLOT_FLOATS * 4 / 16, KSUB_D = C::KSUB_FLOATS * 4 / 16,
                                QSUB_D = kBM * 32 * 4 / 16, VCH_D = C::VCHUNK_FLOATS * 4 / 16,
                                VLO_D = DVC * 32 * 4 / 16, KSTEP_D = 32 / 16;
-            // S buffer j % NSB: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
+            // S buffer: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
-                const uint32_t d = tmem + C::S + (uint32_t)(j % NSB) * C::SB;
+                const uint32_t d = tmem + C::S;
                 const int it0 = s_first(j);
 #pragma unroll
                 for (int ki = 0; ki < KI; ++ki) {
@@ -415,17 +418,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(&r_empty[item % NS]);
                 }
-                mma_commit(&s_full[j % NSB]);
+                mma_commit(&s_full);
                 return true;
             };
             // O += P_hi V_hi + P_hi V_lo + P_lo V_hi for tile j.
             auto issue_pv = [&](int j) -> bool {
-                if (!mbar_wait(&p_full[j % NSB], (uint32_t)(j / NSB) & 1u)) {
+                if (!mbar_wait(&p_full, (uint32_t)j & 1u)) {
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     return false;
                 }
                 const uint32_t o = tmem + C::O;
-                const uint32_t p_hi = tmem + C::S + (uint32_t)(j % NSB) * C::SB, p_lo = p_hi + kBN;
+                const uint32_t p_hi = tmem + C::P, p_lo = p_hi + kBN;
                 const int it0 = pv_first(j);
 #pragma unroll
                 for (int vi = 0; vi < VI; ++vi) {
@@ -449,21 +452,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(&r_empty[item % NS]);
                 }
-                mma_commit(&pv_done[j % NSB]);
+                mma_commit(&pv_done);
                 return true;
             };
             if (warp == 1) {
                 bool ok = mbar_wait(&q_ready, 0);
                 if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
                 tc_fence_after();
-                if constexpr (NSB == 2) {
-                    // Scores only.  S_j reuses the buffer of P_{j-2}: it waits until
-                    // P.V_{j-2} (the other thread's) has read it.
+                if constexpr (C::SPLIT) {
+                    // Scores only: S_j overwrites S_{j-1} once the softmax has read it.
                     for (int j = 0; ok && j < n_tiles; ++j) {
-                        if (j >= 2) {
-                            ok = mbar_wait(&pv_done[j % 2], (uint32_t)((j - 2) / 2) & 1u);
+                        if (j >= 1) {
+                            ok = mbar_wait(&s_free, (uint32_t)(j - 1) & 1u);
                             if (!ok) {
-                                raise_device_error(&g_tc_device_error, kErrTcPv);
+                                raise_device_error(&g_tc_device_error, kErrTcS);
                                 break;
                             }
                             tc_fence_after();
@@ -471,11 +473,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = issue_s(j);
                     }
                 } else {
-                    // One S buffer: the two steps alternate anyway, so one thread
-                    // issues both; in issue order P.V_j reads P_j before S_{j+1}.
+                    // P over S: the two steps alternate anyway, so one thread issues
+                    // both; in issue order P.V_j reads P_j before S_{j+1} lands.
                     for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j) && issue_pv(j);
                 }
-            } else if (NSB == 2) {
+            } else if (C::SPLIT) {
                 bool ok = true;
                 for (int j = 0; ok && j < n_tiles; ++j) ok = issue_pv(j);
             }
@@ -556,8 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            const int b = j % NSB;
-            if (!__all_sync(FULL, mbar_wait(&s_full[b], (j / NSB) & 1))) {
+            if (!__all_sync(FULL, mbar_wait(&s_full, j & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcS);
                 ok = false;
                 break;
@@ -568,16 +569,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            const uint32_t s_col = C::S + (uint32_t)b * C::SB, plo_col = s_col + kBN;
             float x[kBN];
 #pragma unroll
             for (int h2 = 0; h2 < kBN; h2 += 32) {  // S = first half + second half
                 float y[32];
-                tmem_ld32(trow + s_col + h2, x + h2);
-                tmem_ld32(trow + s_col + kBN + h2, y);
+                tmem_ld32(trow + C::S + h2, x + h2);
+                tmem_ld32(trow + C::S + kBN + h2, y);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; ++i) x[h2 + i] += y[i];
+            }
+            if constexpr (C::SPLIT) {
+                // The scores are in registers: the next score MMAs may overwrite S.
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free);
             }
             const int64_t n0 = tile_key0(j);
             // Visible slots of this tile, clamped to [-1, kBN].
@@ -623,27 +629,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 x[i] = tf32_hi(pi);  // P_hi replaces P in registers
                 plo[i] = pi - x[i];
             }
-            // This buffer's P was last read by P.V_{j-NSB}, which ran before
-            // S_j in issue order; the wait costs nothing.
-            if (j >= NSB && !__all_sync(FULL, mbar_wait(&pv_done[b], ((j / NSB) - 1) & 1))) {
+            // P_{j-1} has been read and O holds P.V_{j-1} (with P over S the
+            // landing of S_j already implies it, and the wait costs nothing).
+            if (j >= 1 && !__all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcPv);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_st32(trow + s_col, x);
-            tmem_st32(trow + s_col + 32, x + 32);
-            tmem_st32(trow + plo_col, plo);
-            tmem_st32(trow + plo_col + 32, plo + 32);
+            tmem_st32(trow + C::P, x);
+            tmem_st32(trow + C::P + 32, x + 32);
+            tmem_st32(trow + C::P + kBN, plo);
+            tmem_st32(trow + C::P + kBN + 32, plo + 32);
             if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
-                // O must hold P.V_{j-1} before it is rescaled.
-                const int bp = (j - 1) % NSB;
-                if (!__all_sync(FULL, mbar_wait(&pv_done[bp], ((j - 1) / NSB) & 1))) {
-                    raise_device_error(&g_tc_device_error, kErrTcPv);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
 #pragma unroll 1
                 for (int c0 = 0; c0 < DVC; c0 += 32) {
                     float o[32];
@@ -657,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&p_full[b]);
+            if (lane == 0) mbar_arrive(&p_full);
         }
         // No bias block may still be in flight when the CTA exits (a loop
         // that stopped early can leave one).
@@ -666,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Epilogue: O / l -> out.
         if (ok && n_tiles > 0) {
             const int last = n_tiles - 1;
-            if (!__all_sync(FULL, mbar_wait(&pv_done[last % NSB], (last / NSB) & 1))) {
+            if (!__all_sync(FULL, mbar_wait(&pv_done, last & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcPv);
                 ok = false;
             }
