@@ -120,6 +120,12 @@ struct TcCfg {
     static_assert(VCHUNK_FLOATS <= SLOT_FLOATS && (DVC * 32 * 4) % 1024 == 0, "V^T chunk layout");
     static_assert(COLS <= 512, "TMEM budget");
     static_assert(NS >= 3 && SMEM <= kSmemLimit, "shared memory budget");
+    // With two issuing threads each skips the other's ring items, and an
+    // mbarrier wait only checks the parity of a slot's phase: a wait for item
+    // i is sound only if the slot's previous item, i - NS, has landed.  Each
+    // issuer's own earlier items cover that when the score and P.V items of
+    // one tile fit in the ring together.
+    static_assert(!SPLIT || KITEMS + VITEMS <= NS, "two-issuer ring: a tile's items must fit in the ring");
 };
 
 // Pairwise (tree) max and sum: short dependency chains.
