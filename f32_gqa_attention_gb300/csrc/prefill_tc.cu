@@ -153,6 +153,36 @@ __device__ __forceinline__ float tree_sum(const float (&v)[N]) {
     return m[0];
 }
 
+// Softcap of a tile's raw scores, in place, by a converged warp: x <- cap *
+// tanh(x * qk_mul) (cap and qk_mul in base-2 units).  The odd Taylor series of
+// tanh through y^13 (coefficients 1, -1/3, 2/15, -17/315, 62/2835,
+// -1382/155925, 21844/6081075) covers |y| < 1/2, where the first dropped term,
+// 929569 y^15 / 638512875, is below 5e-8; it needs no MUFU operation.  Typical
+// softcap arguments (score / cap) stay below 1/2; if any lane of the warp
+// sees a larger one, the whole tile takes softcap_tanh instead.
+template <int N>
+__device__ __forceinline__ void softcap_tile(float (&x)[N], float qk_mul, float cap) {
+    float am = 0.f;
+#pragma unroll
+    for (int i = 0; i < N; ++i) am = fmaxf(am, fabsf(x[i]));
+    if (__any_sync(0xffffffffu, am * fabsf(qk_mul) >= 0.5f)) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) x[i] = cap * softcap_tanh(x[i] * qk_mul);
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float y = x[i] * qk_mul, y2 = y * y;
+            float p = fmaf(y2, 21844.f / 6081075.f, -1382.f / 155925.f);
+            p = fmaf(y2, p, 62.f / 2835.f);
+            p = fmaf(y2, p, -17.f / 315.f);
+            p = fmaf(y2, p, 2.f / 15.f);
+            p = fmaf(y2, p, -1.f / 3.f);
+            p = fmaf(y2, p, 1.f);
+            x[i] = cap * (y * p);
+        }
+    }
+}
+
 // Element (row r, k) of a [rows x 32] f32 tile stored K-major with the
 // 128-byte swizzle: rows of 128 B, 16-byte chunk c of row r at chunk c ^ (r % 8).
 __device__ __forceinline__ int sw128_offset(int r, int chunk) { return r * 32 + ((chunk ^ (r & 7)) << 2); }
@@ -178,6 +208,7 @@ template <bool SOFTCAP, bool ALIBI, int BIAS, int N>
 __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], float slope, int rel0,
                                               const float* bias, int lo_i, int hi_i, bool full) {
     float b4[4] = {0.f, 0.f, 0.f, 0.f};
+    if (SOFTCAP) softcap_tile<N>(x, a.qk_mul, a.cap_log2);
     // ALiBi distance of slot i as (float)rel0 + i: the same value as
     // (float)(rel0 + i) while distances stay below 2^24, without an int ->
     // float conversion per slot.
@@ -185,7 +216,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
     if (full) {
 #pragma unroll
         for (int i = 0; i < N; ++i) {
-            float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            float v = SOFTCAP ? x[i] : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, frel0 + (float)i, v);
             if (BIAS) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
             x[i] = v;
@@ -194,7 +225,7 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             const bool vis = i >= lo_i && i <= hi_i;
-            float v = SOFTCAP ? a.cap_log2 * softcap_tanh(x[i] * a.qk_mul) : x[i] * a.qk_mul;
+            float v = SOFTCAP ? x[i] : x[i] * a.qk_mul;
             if (ALIBI) v = fmaf(slope, frel0 + (float)i, v);
             if (BIAS == 1) v = fmaf(vis ? __ldg(bias + i) : 0.f, kLog2e, v);
             if (BIAS == 2) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
