@@ -128,7 +128,7 @@ struct TcCfg {
     static_assert(!SPLIT || KITEMS + VITEMS <= NS, "two-issuer ring: a tile's items must fit in the ring");
 };
 
-// Pairwise (tree) max and sum: short dependency chains.
+// Pairwise (tree) max: short dependency chains.
 template <int N>
 __device__ __forceinline__ float tree_max(const float (&v)[N]) {
     float m[N / 2];
@@ -141,16 +141,47 @@ __device__ __forceinline__ float tree_max(const float (&v)[N]) {
     return m[0];
 }
 
+// Packed pairs of f32 (Blackwell's f32x2 add / mul / fma): two lanes of
+// arithmetic per instruction for the softmax's elementwise work.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Pairwise (tree) sum on packed pairs: pair k holds elements (2k, 2k+1) and
+// (2k + N/2, 2k+1 + N/2) first, then halves until one pair is left.
 template <int N>
 __device__ __forceinline__ float tree_sum(const float (&v)[N]) {
-    float m[N / 2];
+    uint64_t m[N / 4];
 #pragma unroll
-    for (int i = 0; i < N / 2; ++i) m[i] = v[i] + v[i + N / 2];
+    for (int k = 0; k < N / 4; ++k)
+        m[k] = f2_add(f2_pack(v[2 * k], v[2 * k + 1]), f2_pack(v[2 * k + N / 2], v[2 * k + 1 + N / 2]));
 #pragma unroll
-    for (int w = N / 4; w >= 1; w >>= 1)
+    for (int w = N / 8; w >= 1; w >>= 1)
 #pragma unroll
-        for (int i = 0; i < w; ++i) m[i] = m[i] + m[i + w];
-    return m[0];
+        for (int k = 0; k < w; ++k) m[k] = f2_add(m[k], m[k + w]);
+    float a, b;
+    f2_unpack(m[0], a, b);
+    return a + b;
 }
 
 // Softcap of a tile's raw scores, in place, by a converged warp: x <- cap *
@@ -169,16 +200,22 @@ __device__ __forceinline__ void softcap_tile(float (&x)[N], float qk_mul, float 
 #pragma unroll
         for (int i = 0; i < N; ++i) x[i] = cap * softcap_tanh(x[i] * qk_mul);
     } else {
+        const uint64_t q2 = f2_pack(qk_mul, qk_mul), cap2 = f2_pack(cap, cap);
+        const uint64_t c13 = f2_pack(21844.f / 6081075.f, 21844.f / 6081075.f),
+                       c11 = f2_pack(-1382.f / 155925.f, -1382.f / 155925.f),
+                       c9 = f2_pack(62.f / 2835.f, 62.f / 2835.f), c7 = f2_pack(-17.f / 315.f, -17.f / 315.f),
+                       c5 = f2_pack(2.f / 15.f, 2.f / 15.f), c3 = f2_pack(-1.f / 3.f, -1.f / 3.f),
+                       c1 = f2_pack(1.f, 1.f);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            const float y = x[i] * qk_mul, y2 = y * y;
-            float p = fmaf(y2, 21844.f / 6081075.f, -1382.f / 155925.f);
-            p = fmaf(y2, p, 62.f / 2835.f);
-            p = fmaf(y2, p, -17.f / 315.f);
-            p = fmaf(y2, p, 2.f / 15.f);
-            p = fmaf(y2, p, -1.f / 3.f);
-            p = fmaf(y2, p, 1.f);
-            x[i] = cap * (y * p);
+        for (int i = 0; i < N; i += 2) {
+            const uint64_t y = f2_mul(f2_pack(x[i], x[i + 1]), q2), y2 = f2_mul(y, y);
+            uint64_t p = f2_fma(y2, c13, c11);
+            p = f2_fma(y2, p, c9);
+            p = f2_fma(y2, p, c7);
+            p = f2_fma(y2, p, c5);
+            p = f2_fma(y2, p, c3);
+            p = f2_fma(y2, p, c1);
+            f2_unpack(f2_mul(cap2, f2_mul(y, p)), x[i], x[i + 1]);
         }
     }
 }
@@ -214,12 +251,18 @@ __device__ __forceinline__ void tile_epilogue(const AttnDesc& a, float (&x)[N], 
     // float conversion per slot.
     const float frel0 = (float)rel0;
     if (full) {
+        const uint64_t qk2 = f2_pack(a.qk_mul, a.qk_mul), sl2 = f2_pack(slope, slope),
+                       fr2 = f2_pack(frel0, frel0), l2e = f2_pack(kLog2e, kLog2e);
 #pragma unroll
-        for (int i = 0; i < N; ++i) {
-            float v = SOFTCAP ? x[i] : x[i] * a.qk_mul;
-            if (ALIBI) v = fmaf(slope, frel0 + (float)i, v);
-            if (BIAS) v = fmaf(bias_slot<BIAS>(bias, i, b4), kLog2e, v);
-            x[i] = v;
+        for (int i = 0; i < N; i += 2) {
+            uint64_t v = f2_pack(x[i], x[i + 1]);
+            if (!SOFTCAP) v = f2_mul(v, qk2);
+            if (ALIBI) v = f2_fma(sl2, f2_add(fr2, f2_pack((float)i, (float)(i + 1))), v);
+            if (BIAS) {
+                const float b0 = bias_slot<BIAS>(bias, i, b4);
+                v = f2_fma(f2_pack(b0, bias_slot<BIAS>(bias, i + 1, b4)), l2e, v);
+            }
+            f2_unpack(v, x[i], x[i + 1]);
         }
     } else {
 #pragma unroll
@@ -614,7 +657,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(trow + C::S + kBN + h2, y);
                 tmem_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) x[h2 + i] += y[i];
+                for (int i = 0; i < 32; i += 2)
+                    f2_unpack(f2_add(f2_pack(x[h2 + i], x[h2 + i + 1]), f2_pack(y[i], y[i + 1])), x[h2 + i],
+                              x[h2 + i + 1]);
             }
             if constexpr (C::SPLIT) {
                 // The scores are in registers: the next score MMAs may overwrite S.
@@ -657,14 +702,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) x[i] = fast_exp2(fmaf(x[i], cx, -m_use));
+            for (int i = 0; i < kBN; i += 2) {
+                float e0, e1;
+                f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), f2_pack(cx, cx), f2_pack(-m_use, -m_use)), e0, e1);
+                x[i] = fast_exp2(e0);
+                x[i + 1] = fast_exp2(e1);
+            }
             l = fmaf(l, alpha, tree_sum<kBN>(x));
             float plo[kBN];
+            const uint64_t m1 = f2_pack(-1.f, -1.f);
 #pragma unroll
-            for (int i = 0; i < kBN; ++i) {
-                const float pi = x[i];
-                x[i] = tf32_hi(pi);  // P_hi replaces P in registers
-                plo[i] = pi - x[i];
+            for (int i = 0; i < kBN; i += 2) {  // P_hi replaces P in registers; P_lo = P - P_hi (exact)
+                const float h0 = tf32_hi(x[i]), h1 = tf32_hi(x[i + 1]);
+                f2_unpack(f2_fma(f2_pack(h0, h1), m1, f2_pack(x[i], x[i + 1])), plo[i], plo[i + 1]);
+                x[i] = h0;
+                x[i + 1] = h1;
             }
             // P_{j-1} has been read and O holds P.V_{j-1} (with P over S the
             // landing of S_j already implies it, and the wait costs nothing).
