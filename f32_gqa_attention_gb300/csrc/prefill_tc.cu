@@ -28,17 +28,19 @@
 //    so Q_hi.[K_hi; K_lo]^T lands as [S_hihi | S_hilo] in 128 TMEM columns at
 //    the full N = 128 tensor rate; the third product Q_lo.K_hi (N = 64)
 //    accumulates into the first half and the softmax adds the two halves;
-//  * TMEM columns: Q_hi | O | S | P with 128-column S and P buffers when they
-//    fit (headDim + vHeadDim share <= 256): the score MMAs of tile j+1 start
-//    as soon as the softmax has read S_j, and run while it works on tile j;
-//    P_j (hi | lo) waits only for P.V_{j-1}.  At headDim 192 and 256 there is
-//    room for one 128-column buffer, P is written over S and the steps
-//    alternate (at 256 vHeadDim is split over grid.z: two CTAs, each half of
-//    P.V);
+//  * TMEM columns: Q_hi | O | S | P.  At headDim <= 128 S and P are separate
+//    128-column buffers: the score MMAs of tile j+1 start as soon as the
+//    softmax has read S_j and run while it works on tile j; P_j (hi | lo)
+//    waits only for P.V_{j-1}.  At headDim 192 P_hi takes the last 64 TMEM
+//    columns and P_lo goes to shared memory (the third P.V product is then
+//    SS-form), with the same overlap.  At headDim 256 P is written over S
+//    and the steps alternate (vHeadDim is split over grid.z there: two CTAs,
+//    each half of P.V);
 //  * warp 0 lane 0 streams every K and V^T tile by TMA through one ring of
-//    32 KB items, in the order the MMAs consume them; warp 1 owns TMEM and
-//    one of its threads issues the score MMAs, one thread of warp 6 the P.V
-//    MMAs (with P over S warp 1 issues both); warps 2-5 split Q, run the
+//    32 KB items (16 KB at headDim 192), in the order the MMAs consume them;
+//    warp 1 owns TMEM and one of its threads issues the score MMAs, one
+//    thread of warp 6 the P.V MMAs (at headDim 192 and 256 warp 1 issues
+//    both, consuming the ring in order); warps 2-5 split Q, run the
 //    tile-specialised epilogue and online softmax (base 2, O rescaled only
 //    when a row max grows by more than 2^8), write P hi/lo into TMEM and
 //    finally normalise and store O.
@@ -88,19 +90,31 @@ template <int D, int DV>
 struct TcCfg {
     static constexpr int DVC = DV <= 128 ? DV : DV / 2;       // V columns per CTA (grid.z = DV / DVC)
     static constexpr int KB = D / 32;                          // 32-dim K sub-tiles per key tile
-    // Separate 128-column S and P buffers when TMEM has room (headDim <= 128):
-    // the next score MMAs may then start once the softmax has read S.
-    static constexpr bool SPLIT = D + DVC + 4 * kBN <= 512;
+    // Where S and P live.  PMODE 2 (headDim <= 128): 128-column S and P
+    // buffers in TMEM, score and P.V MMAs from two threads.  PMODE 1 (headDim
+    // 192): S and a 64-column P_hi in TMEM, P_lo in shared memory, one issuing
+    // thread.  With either, the next score MMAs may start as soon as the
+    // softmax has read S.  PMODE 0 (headDim 256): one 128-column buffer, P
+    // written over S, the steps alternate from one thread.  S is stacked:
+    // [S_hihi | S_hilo] in 128 columns.
+    static constexpr int PMODE = D + DVC + 4 * kBN <= 512 ? 2 : (D + DVC + 3 * kBN <= 512 ? 1 : 0);
+    static constexpr bool TWO_ISSUERS = PMODE == 2;
+    static constexpr bool SPLIT = PMODE != 0;  // S and P apart
+    static constexpr int SCOLS = 2 * kBN;
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
-    // Ring slots of 32 KB.  A K item holds two 32-dim sub-tiles, each K_hi
-    // (64 rows) then K_lo (64 rows); a V item holds V^T_hi then V^T_lo of
-    // VCH 32-key chunks.
+    static constexpr int PLO_FLOATS = PMODE == 1 ? kBM * kBN : 0;  // P_lo: 2 x [128 x 32]
+    // Ring slots of 32 KB (16 KB with PMODE 1, where P_lo takes shared
+    // memory).  A K item holds KPI 32-dim sub-tiles, each K_hi (64 rows) then
+    // K_lo (64 rows); a V item holds V^T_hi then V^T_lo of VCH 32-key chunks,
+    // or, when a chunk's hi + lo exceed a slot (VHALF), one of the two.
     static constexpr int KSUB_FLOATS = 2 * kBN * 32;
-    static constexpr int SLOT_FLOATS = 2 * KSUB_FLOATS;
-    static constexpr int KITEMS = (KB + 1) / 2;
+    static constexpr int KPI = PMODE == 1 ? 1 : 2;
+    static constexpr int SLOT_FLOATS = KPI * KSUB_FLOATS;
+    static constexpr int KITEMS = (KB + KPI - 1) / KPI;
     static constexpr int VCHUNK_FLOATS = 2 * DVC * 32;
-    static constexpr int VCH = 2 * VCHUNK_FLOATS <= SLOT_FLOATS ? 2 : 1;
-    static constexpr int VITEMS = (kBN / 32) / VCH;
+    static constexpr bool VHALF = VCHUNK_FLOATS > SLOT_FLOATS;
+    static constexpr int VCH = VHALF ? 1 : (2 * VCHUNK_FLOATS <= SLOT_FLOATS ? 2 : 1);
+    static constexpr int VITEMS = VHALF ? 2 * (kBN / 32) : (kBN / 32) / VCH;
     static constexpr uint32_t SLOT_BYTES = SLOT_FLOATS * sizeof(float);
     // Bias blocks staged by TMA: per softmax warp 32 rows x 64 keys as two
     // 128-byte-swizzled [32 x 32] boxes (headDim <= 192; wider heads leave no
@@ -108,16 +122,19 @@ struct TcCfg {
     static constexpr bool BSTAGE = D <= VTMU_TC_BSTAGE_MAX_D;
     static constexpr int BWARP_FLOATS = 32 * kBN;
     static constexpr int BIAS_FLOATS = BSTAGE ? 4 * BWARP_FLOATS : 0;
-    static constexpr size_t FIXED = (size_t)(QLO_FLOATS + BIAS_FLOATS) * sizeof(float) + 1024;
+    static constexpr size_t FIXED = (size_t)(QLO_FLOATS + BIAS_FLOATS + PLO_FLOATS) * sizeof(float) + 1024;
     static constexpr int NS_FIT = (int)((kSmemLimit - FIXED) / SLOT_BYTES);
     static constexpr int NS = NS_FIT > VTMU_TC_MAX_SLOTS ? VTMU_TC_MAX_SLOTS : NS_FIT;  // ring slots
-    static constexpr int QLO_OFF = 0, BIAS_OFF = QLO_FLOATS, RING_OFF = QLO_FLOATS + BIAS_FLOATS;
+    static constexpr int QLO_OFF = 0, BIAS_OFF = QLO_FLOATS, PLO_OFF = QLO_FLOATS + BIAS_FLOATS,
+                         RING_OFF = QLO_FLOATS + BIAS_FLOATS + PLO_FLOATS;
     static constexpr size_t SMEM = FIXED + (size_t)NS * SLOT_BYTES;
     // TMEM columns
-    static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, P = SPLIT ? S + 2 * kBN : S,
-                              COLS = S + (SPLIT ? 4 : 2) * kBN;
+    static constexpr uint32_t Q_HI = 0, O = D, S = D + DVC, P = SPLIT ? S + SCOLS : S,
+                              COLS = PMODE == 2 ? P + 2 * kBN : (PMODE == 1 ? P + kBN : S + SCOLS);
     static_assert(D % 32 == 0 && DVC % 32 == 0 && D <= 256 && DVC <= 128 && DV % DVC == 0, "tcgen05 prefill shape");
-    static_assert(VCHUNK_FLOATS <= SLOT_FLOATS && (DVC * 32 * 4) % 1024 == 0, "V^T chunk layout");
+    static_assert((VHALF ? VCHUNK_FLOATS / 2 : VCH * VCHUNK_FLOATS) <= SLOT_FLOATS && (DVC * 32 * 4) % 1024 == 0,
+                  "V^T chunk layout");
+    static_assert(PLO_OFF + PLO_FLOATS == RING_OFF, "shared-memory layout");
     static_assert(COLS <= 512, "TMEM budget");
     static_assert(NS >= 3 && SMEM <= kSmemLimit, "shared memory budget");
     // With two issuing threads each skips the other's ring items, and an
@@ -125,7 +142,7 @@ struct TcCfg {
     // i is sound only if the slot's previous item, i - NS, has landed.  Each
     // issuer's own earlier items cover that when the score and P.V items of
     // one tile fit in the ring together.
-    static_assert(!SPLIT || KITEMS + VITEMS <= NS, "two-issuer ring: a tile's items must fit in the ring");
+    static_assert(!TWO_ISSUERS || KITEMS + VITEMS <= NS, "two-issuer ring: a tile's items must fit in the ring");
 };
 
 // Pairwise (tree) max: short dependency chains.
@@ -401,11 +418,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_s = [&](int j) -> bool {
                 const int n0 = (int)tile_key0(j);
                 for (int ki = 0; ki < C::KITEMS; ++ki) {
-                    const int nsub = KB - 2 * ki < 2 ? KB - 2 * ki : 2;
+                    const int nsub = KB - C::KPI * ki < C::KPI ? KB - C::KPI * ki : C::KPI;
                     float* dst = acquire((uint32_t)nsub * C::KSUB_FLOATS * sizeof(float));
                     if (!dst) return false;
                     for (int u = 0; u < nsub; ++u) {
-                        const int x = kh * D + (2 * ki + u) * 32;
+                        const int x = kh * D + (C::KPI * ki + u) * 32;
                         float* sub = dst + u * C::KSUB_FLOATS;
                         tma_load_2d(sub, &tm_khi, x, n0, &r_full[it % NS]);
                         tma_load_2d(sub + kBN * 32, &tm_klo, x, n0, &r_full[it % NS]);
@@ -417,13 +434,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             auto load_pv = [&](int j) -> bool {
                 const int n0 = (int)tile_key0(j);
                 for (int vi = 0; vi < C::VITEMS; ++vi) {
-                    float* dst = acquire(C::VCH * C::VCHUNK_FLOATS * sizeof(float));
-                    if (!dst) return false;
-                    for (int u = 0; u < C::VCH; ++u) {
-                        const int key = n0 + (vi * C::VCH + u) * 32;
-                        float* chunk = dst + u * C::VCHUNK_FLOATS;
-                        tma_load_2d(chunk, &tm_vhi, key, kh * DV + dv0, &r_full[it % NS]);
-                        tma_load_2d(chunk + DVC * 32, &tm_vlo, key, kh * DV + dv0, &r_full[it % NS]);
+                    if constexpr (C::VHALF) {
+                        // item 2c: V^T_hi of chunk c; item 2c + 1: V^T_lo.
+                        float* dst = acquire(DVC * 32 * sizeof(float));
+                        if (!dst) return false;
+                        tma_load_2d(dst, (vi & 1) ? &tm_vlo : &tm_vhi, n0 + (vi >> 1) * 32, kh * DV + dv0,
+                                    &r_full[it % NS]);
+                    } else {
+                        float* dst = acquire(C::VCH * C::VCHUNK_FLOATS * sizeof(float));
+                        if (!dst) return false;
+                        for (int u = 0; u < C::VCH; ++u) {
+                            const int key = n0 + (vi * C::VCH + u) * 32;
+                            float* chunk = dst + u * C::VCHUNK_FLOATS;
+                            tma_load_2d(chunk, &tm_vhi, key, kh * DV + dv0, &r_full[it % NS]);
+                            tma_load_2d(chunk + DVC * 32, &tm_vlo, key, kh * DV + dv0, &r_full[it % NS]);
+                        }
                     }
                     ++it;
                 }
@@ -442,11 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
     } else if (warp == 1 || warp == 6) {
-        // ------------- MMA issuers: warp 1 the scores, warp 6 P.V (two S buffers) -------------
+        // ---------- MMA issuers: warp 1 the scores, warp 6 P.V (PMODE 2); warp 1 both (PMODE 1) ----------
         // One kind::tf32 MMA issues at most every ~53 cycles from one thread, so
-        // with two S buffers the score and P.V streams come from two threads
-        // (two warps) and meet in the tensor pipe.  Both index the ring sequence
-        // of the TMA thread: item numbers follow from the step order above.
+        // with PMODE 2 the score and P.V streams come from two threads (two
+        // warps) and meet in the tensor pipe.  Both index the ring sequence of
+        // the TMA thread: item numbers follow from the step order S_0, then
+        // S_{j+1}, PV_j for every j.  With PMODE 1 one thread issues both in
+        // that order and consumes the ring in order.
         if (lane == 0 && n_tiles > 0) {
             constexpr uint32_t id_s2 = idesc_tf32(kBM, 2 * kBN), id_s = idesc_tf32(kBM, kBN),
                                id_o = idesc_tf32(kBM, DVC);
@@ -467,10 +494,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             // Descriptors are base + byte offset / 16, computed once.
             const uint64_t ring_d = smem_desc_sw128(ring), qlo_d = smem_desc_sw128(qlo);
+            const uint64_t plo_d = smem_desc_sw128(smem + C::PLO_OFF);
             constexpr uint64_t SLOT_D = C::SLOT_FLOATS * 4 / 16, KSUB_D = C::KSUB_FLOATS * 4 / 16,
-                               QSUB_D = kBM * 32 * 4 / 16, VCH_D = C::VCHUNK_FLOATS * 4 / 16,
-                               VLO_D = DVC * 32 * 4 / 16, KSTEP_D = 32 / 16;
-            // S buffer: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
+                               QSUB_D = kBM * 32 * 4 / 16,
+                               VCH_D = C::VCHUNK_FLOATS * 4 / 16, VLO_D = DVC * 32 * 4 / 16, KSTEP_D = 32 / 16,
+                               PLO_CHUNK_D = kBM * 32 * 4 / 16;
+            // S: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
             auto issue_s = [&](int j) -> bool {
                 const uint32_t d = tmem + C::S;
                 const int it0 = s_first(j);
@@ -480,19 +509,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!take(item)) return false;
                     const uint64_t b_slot = ring_d + (uint64_t)(item % NS) * SLOT_D;
 #pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const int kb = 2 * ki + u;
+                    for (int u = 0; u < C::KPI; ++u) {
+                        const int kb = C::KPI * ki + u;
                         if (kb < KB) {
                             const uint64_t b_k = b_slot + u * KSUB_D;  // [K_hi; K_lo]
                             const uint64_t a_lo = qlo_d + kb * QSUB_D;
                             const uint32_t a_hi = tmem + C::Q_HI + kb * 32;
 #pragma unroll
                             for (int k = 0; k < 4; ++k) {
+                                const uint64_t bk = b_k + k * KSTEP_D;
                                 if (kb == 0 && k == 0)
-                                    mma_tf32_ts(d, a_hi, b_k, id_s2, 0u);
+                                    mma_tf32_ts(d, a_hi, bk, id_s2, 0u);
                                 else
-                                    mma_tf32_ts_acc(d, a_hi + k * 8, b_k + k * KSTEP_D, id_s2);
-                                mma_tf32_ss_acc(d, a_lo + k * KSTEP_D, b_k + k * KSTEP_D, id_s);
+                                    mma_tf32_ts_acc(d, a_hi + k * 8, bk, id_s2);
+                                mma_tf32_ss_acc(d, a_lo + k * KSTEP_D, bk, id_s);
                             }
                         }
                     }
@@ -501,63 +531,83 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&s_full);
                 return true;
             };
-            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi for tile j.
+            // O += P_hi V_hi + P_hi V_lo + P_lo V_hi for one 32-key chunk c of
+            // tile j; P_lo from TMEM (PMODE 2) or shared memory (PMODE 1).
+            auto pv_chunk = [&](int j, int c, uint64_t v_hi, uint64_t v_lo) {
+                const uint32_t o = tmem + C::O;
+                const uint32_t p_hi = tmem + C::P, p_lo = p_hi + kBN;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const uint32_t col = c * 32 + k * 8;
+                    if (c == 0 && k == 0)
+                        mma_tf32_ts(o, p_hi + col, v_hi + k * KSTEP_D, id_o, j > 0 ? 1u : 0u);
+                    else
+                        mma_tf32_ts_acc(o, p_hi + col, v_hi + k * KSTEP_D, id_o);
+                    mma_tf32_ts_acc(o, p_hi + col, v_lo + k * KSTEP_D, id_o);
+                    if constexpr (C::PMODE == 1)
+                        mma_tf32_ss_acc(o, plo_d + c * PLO_CHUNK_D + k * KSTEP_D, v_hi + k * KSTEP_D, id_o);
+                    else
+                        mma_tf32_ts_acc(o, p_lo + col, v_hi + k * KSTEP_D, id_o);
+                }
+            };
             auto issue_pv = [&](int j) -> bool {
                 if (!mbar_wait(&p_full, (uint32_t)j & 1u)) {
                     raise_device_error(&g_tc_device_error, kErrTcP);
                     return false;
                 }
-                const uint32_t o = tmem + C::O;
-                const uint32_t p_hi = tmem + C::P, p_lo = p_hi + kBN;
                 const int it0 = pv_first(j);
+                if constexpr (C::VHALF) {
 #pragma unroll
-                for (int vi = 0; vi < VI; ++vi) {
-                    const int item = it0 + vi;
-                    if (!take(item)) return false;
-                    const uint64_t v_slot = ring_d + (uint64_t)(item % NS) * SLOT_D;
-#pragma unroll
-                    for (int u = 0; u < C::VCH; ++u) {
-                        const int c = vi * C::VCH + u;
-                        const uint64_t v_hi = v_slot + u * VCH_D, v_lo = v_hi + VLO_D;
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            const uint32_t col = c * 32 + k * 8;
-                            if (c == 0 && k == 0)
-                                mma_tf32_ts(o, p_hi + col, v_hi + k * KSTEP_D, id_o, j > 0 ? 1u : 0u);
-                            else
-                                mma_tf32_ts_acc(o, p_hi + col, v_hi + k * KSTEP_D, id_o);
-                            mma_tf32_ts_acc(o, p_hi + col, v_lo + k * KSTEP_D, id_o);
-                            mma_tf32_ts_acc(o, p_lo + col, v_hi + k * KSTEP_D, id_o);
-                        }
+                    for (int c = 0; c < kBN / 32; ++c) {
+                        const int ih = it0 + 2 * c, il = ih + 1;  // V^T_hi item, V^T_lo item
+                        if (!take(ih) || !take(il)) return false;
+                        pv_chunk(j, c, ring_d + (uint64_t)(ih % NS) * SLOT_D, ring_d + (uint64_t)(il % NS) * SLOT_D);
+                        mma_commit(&r_empty[ih % NS]);
+                        mma_commit(&r_empty[il % NS]);
                     }
-                    mma_commit(&r_empty[item % NS]);
+                } else {
+#pragma unroll
+                    for (int vi = 0; vi < VI; ++vi) {
+                        const int item = it0 + vi;
+                        if (!take(item)) return false;
+                        const uint64_t v_slot = ring_d + (uint64_t)(item % NS) * SLOT_D;
+#pragma unroll
+                        for (int u = 0; u < C::VCH; ++u) {
+                            const uint64_t v_hi = v_slot + u * VCH_D;
+                            pv_chunk(j, vi * C::VCH + u, v_hi, v_hi + VLO_D);
+                        }
+                        mma_commit(&r_empty[item % NS]);
+                    }
                 }
                 mma_commit(&pv_done);
+                return true;
+            };
+            // S_j overwrites S_{j-1} once the softmax has read it.
+            auto wait_s_free = [&](int j) -> bool {
+                if (j >= 1) {
+                    if (!mbar_wait(&s_free, (uint32_t)(j - 1) & 1u)) {
+                        raise_device_error(&g_tc_device_error, kErrTcS);
+                        return false;
+                    }
+                    tc_fence_after();
+                }
                 return true;
             };
             if (warp == 1) {
                 bool ok = mbar_wait(&q_ready, 0);
                 if (!ok) raise_device_error(&g_tc_device_error, kErrTcQ);
                 tc_fence_after();
-                if constexpr (C::SPLIT) {
-                    // Scores only: S_j overwrites S_{j-1} once the softmax has read it.
-                    for (int j = 0; ok && j < n_tiles; ++j) {
-                        if (j >= 1) {
-                            ok = mbar_wait(&s_free, (uint32_t)(j - 1) & 1u);
-                            if (!ok) {
-                                raise_device_error(&g_tc_device_error, kErrTcS);
-                                break;
-                            }
-                            tc_fence_after();
-                        }
-                        ok = issue_s(j);
-                    }
+                if constexpr (C::TWO_ISSUERS) {
+                    for (int j = 0; ok && j < n_tiles; ++j) ok = wait_s_free(j) && issue_s(j);
+                } else if constexpr (C::SPLIT) {
+                    ok = ok && issue_s(0);
+                    for (int j = 0; ok && j < n_tiles; ++j)
+                        ok = (j + 1 >= n_tiles || (wait_s_free(j + 1) && issue_s(j + 1))) && issue_pv(j);
                 } else {
-                    // P over S: the two steps alternate anyway, so one thread issues
-                    // both; in issue order P.V_j reads P_j before S_{j+1} lands.
+                    // P over S: in issue order P.V_j reads P_j before S_{j+1} lands.
                     for (int j = 0; ok && j < n_tiles; ++j) ok = issue_s(j) && issue_pv(j);
                 }
-            } else if (C::SPLIT) {
+            } else if (C::TWO_ISSUERS) {
                 bool ok = true;
                 for (int j = 0; ok && j < n_tiles; ++j) ok = issue_pv(j);
             }
@@ -728,8 +778,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             tmem_st32(trow + C::P, x);
             tmem_st32(trow + C::P + 32, x + 32);
-            tmem_st32(trow + C::P + kBN, plo);
-            tmem_st32(trow + C::P + kBN + 32, plo + 32);
+            if constexpr (C::PMODE == 1) {
+                // P_lo row r -> shared memory, K-major 128-byte-swizzled [128 x 32]
+                // chunks (the A operand of the SS-form product).
+                float* pl = smem + C::PLO_OFF;
+#pragma unroll
+                for (int c = 0; c < kBN / 32; ++c)
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        *reinterpret_cast<float4*>(pl + c * kBM * 32 + sw128_offset(r, q)) =
+                            make_float4(plo[32 * c + 4 * q], plo[32 * c + 4 * q + 1], plo[32 * c + 4 * q + 2],
+                                        plo[32 * c + 4 * q + 3]);
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // P_lo -> MMA (async proxy)
+            } else {
+                tmem_st32(trow + C::P + kBN, plo);
+                tmem_st32(trow + C::P + kBN + 32, plo + 32);
+            }
             if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c0 = 0; c0 < DVC; c0 += 32) {
