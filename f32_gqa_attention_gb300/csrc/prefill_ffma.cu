@@ -83,8 +83,14 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     float* sP = smem + C::P_OFF;
 
     const int n_qt = (int)((a.T + BM - 1) / BM);
-    const int qt = n_qt - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const int h = blockIdx.y;
+    // Linear block order: when the query tiles' work differs (causal or
+    // windowed), query tile outermost, latest (heaviest) first, so the longest
+    // CTAs of every head start first; otherwise heads outermost, so the CTAs
+    // running together share one head's K/V in L2.
+    const int64_t lin = blockIdx.x + (int64_t)gridDim.x * blockIdx.y;
+    const bool uniform = !a.causal && a.window <= 0;
+    const int h = (int)(uniform ? lin / n_qt : lin % a.H);
+    const int qt = n_qt - 1 - (int)(uniform ? lin % n_qt : lin / a.H);
     const int kh = h / a.G;
     const int tx = threadIdx.x % TX;
     const int ty = threadIdx.x / TX;

@@ -341,9 +341,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (int)((a.T + kBM - 1) / kBM);
-    const int qt = n_qt - 1 - (int)blockIdx.x;  // heaviest (latest) query tiles first
-    const int h = blockIdx.y, kh = h / a.G;
-    const int dv0 = (int)blockIdx.z * DVC;      // this CTA's V columns [dv0, dv0 + DVC)
+    // CTAs start in linear block order (V half innermost).  When the query
+    // tiles' work differs (causal or windowed), the query tile is outermost,
+    // latest (heaviest) first, so the longest CTAs of every head start first
+    // and short ones fill the tail; when every tile sees the same keys, heads
+    // are outermost so that the CTAs running together share one head's K/V
+    // in L2.
+    const int nz = (int)gridDim.z;
+    const int64_t lin = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
+    const int zz = (int)(lin % nz);
+    const bool uniform = !a.causal && a.window <= 0;
+    const int h = (int)(uniform ? lin / ((int64_t)nz * n_qt) : (lin / nz) % a.H), kh = h / a.G;
+    const int qt = n_qt - 1 - (int)(uniform ? (lin / nz) % n_qt : lin / ((int64_t)nz * a.H));
+    const int dv0 = zz * DVC;  // this CTA's V columns [dv0, dv0 + DVC)
     const int64_t t0 = (int64_t)qt * kBM;
     const int64_t t_last = (t0 + kBM < a.T ? t0 + kBM : a.T) - 1;
 
