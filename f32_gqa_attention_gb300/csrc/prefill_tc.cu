@@ -66,7 +66,6 @@ namespace {
 
 constexpr int kBM = 128;      // query rows per CTA = MMA M = TMEM lanes
 constexpr int kBN = 64;       // keys per tile = score MMA N
-constexpr int kThreads = 224; // warp 0 TMA, warp 1 score MMAs, warps 2-5 softmax, warp 6 P.V MMAs
 constexpr float kRescaleLog2 = 8.f;  // rescale O when a row max grows by more
 constexpr size_t kSmemLimit = 227 * 1024;
 #ifndef VTMU_TC_BSTAGE_MAX_D
@@ -99,6 +98,14 @@ struct TcCfg {
     // [S_hihi | S_hilo] in 128 columns.
     static constexpr int PMODE = D + DVC + 4 * kBN <= 512 ? 2 : (D + DVC + 3 * kBN <= 512 ? 1 : 0);
     static constexpr bool TWO_ISSUERS = PMODE == 2;
+    // Softmax warps.  Four (one per TMEM lane quarter, 64 keys each), or with
+    // PMODE 0, where the softmax is not overlapped with the score MMAs, eight:
+    // two per lane quarter, 32 keys each, exchanging row maxima per tile.
+    // Warp 0 is the TMA thread, warp 1 issues MMAs, warps 2 .. 1 + SMW run the
+    // softmax; with 224 threads warp 6 issues the P.V MMAs (PMODE 2).
+    static constexpr int SMW = PMODE == 0 ? 8 : 4;
+    static constexpr int NCOL = kBN * 4 / SMW;  // keys per softmax thread and tile
+    static constexpr int THREADS = PMODE == 0 ? 32 * (2 + SMW) : 224;
     static constexpr bool SPLIT = PMODE != 0;  // S and P apart
     static constexpr int SCOLS = 2 * kBN;
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
@@ -143,7 +150,22 @@ struct TcCfg {
     // issuer's own earlier items cover that when the score and P.V items of
     // one tile fit in the ring together.
     static_assert(!TWO_ISSUERS || KITEMS + VITEMS <= NS, "two-issuer ring: a tile's items must fit in the ring");
+    // Paired softmax warps rely on P over S (the landing of S_j implies P.V_{j-1}
+    // is done) and read the bias from global memory.
+    static_assert(SMW == 4 || (!SPLIT && !BSTAGE && DVC % 64 == 0 && KB % 2 == 0), "paired softmax warps");
 };
+
+// Barrier over the two softmax warps of one TMEM lane quarter (named barrier
+// `id`, 64 threads); returns the AND of `v` over them.
+__device__ __forceinline__ bool pair_sync_and(uint32_t id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 64, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
 
 // Pairwise (tree) max: short dependency chains.
 template <int N>
@@ -322,7 +344,7 @@ __device__ __forceinline__ void run_epilogue_staged(int feat, const AttnDesc& a,
 }
 
 template <int D, int DV>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
     prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const int bias_staged,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_bias,
                       const __grid_constant__ CUtensorMap tm_khi,
@@ -338,6 +360,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(8) uint64_t r_full[NS], r_empty[NS], s_full, s_free, p_full, pv_done, q_full,
         q_ready, b_full[4];
     __shared__ uint32_t tmem_base_s;
+    // Paired softmax warps: a partial value per key half and row (at headDim
+    // 256 static shared memory has room for one such array, 1 KB).
+    __shared__ float pair_x[C::SMW == 8 ? 2 * kBM : 1];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (int)((a.T + kBM - 1) / kBM);
@@ -384,10 +409,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Each completes once per key tile: tile j waits on phase j & 1.
         mbar_init(&s_full, 1);
         mbar_init(&s_free, 4);
-        mbar_init(&p_full, 4);
+        mbar_init(&p_full, C::SMW);
         mbar_init(&pv_done, 1);
         mbar_init(&q_full, 1);
-        mbar_init(&q_ready, 4);
+        mbar_init(&q_ready, C::SMW);
         for (int b = 0; b < 4; ++b) mbar_init(&b_full[b], 1);
         fence_barrier_init();
     }
@@ -476,7 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int c = it > NS ? it - NS : 0; c < it; ++c) drained &= mbar_wait(&r_full[c % NS], (c / NS) & 1);
             if (!drained) raise_device_error(&g_tc_device_error, kErrTcDrain);
         }
-    } else if (warp == 1 || warp == 6) {
+    } else if (warp == 1 || (C::SMW == 4 && warp == 6)) {
         // ---------- MMA issuers: warp 1 the scores, warp 6 P.V (PMODE 2); warp 1 both (PMODE 1) ----------
         // One kind::tf32 MMA issues at most every ~53 cycles from one thread, so
         // with PMODE 2 the score and P.V streams come from two threads (two
@@ -624,8 +649,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // --------------------- softmax warps: thread = query row ---------------------
+        constexpr bool PAIR = C::SMW == 8;
+        constexpr int NCOL = C::NCOL;
         const uint32_t lrow = 32u * (uint32_t)(warp & 3);  // TMEM lane quarter of this warp
         const int r = (int)lrow + lane;
+        // Paired warps: half 0 (warps 2-5) takes keys [0, 32) of each tile, the
+        // first half of the Q sub-tiles and of O; half 1 (warps 6-9) the rest.
+        const int half = PAIR ? (warp - 2) >> 2 : 0;
+        const int c0 = half * NCOL;                      // this warp's first key of a tile
+        const int oc0 = half * (DVC / (PAIR ? 2 : 1));   // and its first O column
+        constexpr int OCOLS = DVC / (PAIR ? 2 : 1);
+        const uint32_t pair_id = 1u + (uint32_t)(warp & 3);
         const int64_t t = t0 + r;
         const bool row_ok = t < a.T;
         const uint32_t trow = tmem + (lrow << 16);
@@ -634,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         {
             if (!__all_sync(FULL, mbar_wait(&q_full, 0))) raise_device_error(&g_tc_device_error, kErrTcQ);
 #pragma unroll 1
-            for (int kb = 0; kb < KB; ++kb) {
+            for (int kb = half * (KB / (PAIR ? 2 : 1)); kb < (half + 1) * (KB / (PAIR ? 2 : 1)); ++kb) {
                 float* sub = qlo + kb * kBM * 32;
                 float hi[32], lo[32];
 #pragma unroll
@@ -698,8 +732,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
-            if (!__all_sync(FULL, mbar_wait(&s_full, j & 1))) {
-                raise_device_error(&g_tc_device_error, kErrTcS);
+            bool got = __all_sync(FULL, mbar_wait(&s_full, j & 1));
+            if (!got) raise_device_error(&g_tc_device_error, kErrTcS);
+            if constexpr (PAIR) {
+                // P over S: S_j has landed, so P.V_{j-1} is done and this wait
+                // returns at once.  Both warps of the pair leave the loop
+                // together, at the barrier below.
+                if (got && j >= 1) {
+                    got = __all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1));
+                    if (!got) raise_device_error(&g_tc_device_error, kErrTcPv);
+                }
+            } else if (!got) {
                 ok = false;
                 break;
             }
@@ -709,12 +752,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             tc_fence_after();
-            float x[kBN];
+            float x[NCOL];
 #pragma unroll
-            for (int h2 = 0; h2 < kBN; h2 += 32) {  // S = first half + second half
+            for (int h2 = 0; h2 < NCOL; h2 += 32) {  // S = first half + second half
                 float y[32];
-                tmem_ld32(trow + C::S + h2, x + h2);
-                tmem_ld32(trow + C::S + kBN + h2, y);
+                tmem_ld32(trow + C::S + c0 + h2, x + h2);
+                tmem_ld32(trow + C::S + kBN + c0 + h2, y);
                 tmem_wait_ld();
 #pragma unroll
                 for (int i = 0; i < 32; i += 2)
@@ -727,20 +770,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&s_free);
             }
-            const int64_t n0 = tile_key0(j);
-            // Visible slots of this tile, clamped to [-1, kBN].
+            const int64_t n0 = tile_key0(j) + c0;
+            // Visible slots of this warp's keys, clamped to [-1, NCOL].
             const int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
-            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > kBN ? kBN : lo64));
-            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > kBN ? kBN : hi64));
-            const bool full = lo_i <= 0 && hi_i >= kBN - 1;
+            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > NCOL ? NCOL : lo64));
+            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > NCOL ? NCOL : hi64));
+            const bool full = lo_i <= 0 && hi_i >= NCOL - 1;
             // Plain scaled scores (no softcap, ALiBi or bias) with a positive
             // scale: the mask alone here, and the scale goes into the exp2's FFMA.
             const bool fold = feat == 0 && a.qk_mul > 0.f;
             if (!fold) {
                 if (!bstage) {
-                    run_epilogue<kBN>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i, full);
+                    run_epilogue<NCOL>(feat, a, x, slope, (int)(n0 - p), brow ? brow + n0 : nullptr, lo_i, hi_i,
+                                       full);
                 } else {
-                    run_epilogue_staged<kBN>(feat, a, x, slope, (int)(n0 - p), bbuf, lo_i, hi_i, full);
+                    run_epilogue_staged<NCOL>(feat, a, x, slope, (int)(n0 - p), bbuf, lo_i, hi_i, full);
                 }
                 if (bstage && j + 1 < n_tiles) {
                     // The block has been read (generic proxy) before TMA refills it.
@@ -750,10 +794,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             } else if (!full) {
 #pragma unroll
-                for (int i = 0; i < kBN; ++i) x[i] = (i >= lo_i && i <= hi_i) ? x[i] : -INFINITY;
+                for (int i = 0; i < NCOL; ++i) x[i] = (i >= lo_i && i <= hi_i) ? x[i] : -INFINITY;
             }
             const float cx = fold ? a.qk_mul : 1.f;
-            const float mt = tree_max<kBN>(x) * cx;
+            float mt = tree_max<NCOL>(x) * cx;
+            if constexpr (PAIR) {
+                // The partner reads this slot after the barrier and before its
+                // p_full arrival (its P depends on the value), and tile j + 1's
+                // write waits for S_{j+1}, which waits for that arrival: one
+                // array serves every tile.
+                pair_x[half * kBM + r] = mt;
+                if (!pair_sync_and(pair_id, got)) {
+                    ok = false;
+                    break;
+                }
+                mt = fmaxf(mt, pair_x[(half ^ 1) * kBM + r]);
+            }
             // Lazy rescale: keep the reference max unless this tile beats it by > 2^8.
             float alpha = 1.f;
             if (mt > m_ref + kRescaleLog2) {
@@ -762,17 +818,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float m_use = m_ref == -INFINITY ? 0.f : m_ref;
 #pragma unroll
-            for (int i = 0; i < kBN; i += 2) {
+            for (int i = 0; i < NCOL; i += 2) {
                 float e0, e1;
                 f2_unpack(f2_fma(f2_pack(x[i], x[i + 1]), f2_pack(cx, cx), f2_pack(-m_use, -m_use)), e0, e1);
                 x[i] = fast_exp2(e0);
                 x[i + 1] = fast_exp2(e1);
             }
-            l = fmaf(l, alpha, tree_sum<kBN>(x));
-            float plo[kBN];
+            l = fmaf(l, alpha, tree_sum<NCOL>(x));
+            float plo[NCOL];
             const uint64_t m1 = f2_pack(-1.f, -1.f);
 #pragma unroll
-            for (int i = 0; i < kBN; i += 2) {  // P_hi replaces P in registers; P_lo = P - P_hi (exact)
+            for (int i = 0; i < NCOL; i += 2) {  // P_hi replaces P in registers; P_lo = P - P_hi (exact)
                 const float h0 = tf32_hi(x[i]), h1 = tf32_hi(x[i + 1]);
                 f2_unpack(f2_fma(f2_pack(h0, h1), m1, f2_pack(x[i], x[i + 1])), plo[i], plo[i + 1]);
                 x[i] = h0;
@@ -780,14 +836,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // P_{j-1} has been read and O holds P.V_{j-1} (with P over S the
             // landing of S_j already implies it, and the wait costs nothing).
-            if (j >= 1 && !__all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1))) {
+            if (!PAIR && j >= 1 && !__all_sync(FULL, mbar_wait(&pv_done, (j - 1) & 1))) {
                 raise_device_error(&g_tc_device_error, kErrTcPv);
                 ok = false;
                 break;
             }
             tc_fence_after();
-            tmem_st32(trow + C::P, x);
-            tmem_st32(trow + C::P + 32, x + 32);
+#pragma unroll
+            for (int c = 0; c < NCOL; c += 32) tmem_st32(trow + C::P + c0 + c, x + c);
             if constexpr (C::PMODE == 1) {
                 // P_lo row r -> shared memory, K-major 128-byte-swizzled [128 x 32]
                 // chunks (the A operand of the SS-form product).
@@ -801,18 +857,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                                         plo[32 * c + 4 * q + 3]);
                 asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // P_lo -> MMA (async proxy)
             } else {
-                tmem_st32(trow + C::P + kBN, plo);
-                tmem_st32(trow + C::P + kBN + 32, plo + 32);
+#pragma unroll
+                for (int c = 0; c < NCOL; c += 32) tmem_st32(trow + C::P + kBN + c0 + c, plo + c);
             }
             if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
-                for (int c0 = 0; c0 < DVC; c0 += 32) {
+                for (int c = oc0; c < oc0 + OCOLS; c += 32) {
                     float o[32];
-                    tmem_ld32(trow + C::O + c0, o);
+                    tmem_ld32(trow + C::O + c, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tmem_st32(trow + C::O + c0, o);
+                    tmem_st32(trow + C::O + c, o);
                 }
             }
             tmem_wait_st();
@@ -832,14 +888,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
             }
         }
+        if constexpr (PAIR) {
+            // Row sum over both key halves (each warp of the pair reaches this
+            // barrier once: both left the loop together).
+            ok = pair_sync_and(pair_id, ok);  // both have read the last maxima
+            pair_x[half * kBM + r] = l;
+            pair_sync_and(pair_id, true);
+            l += pair_x[(half ^ 1) * kBM + r];
+        }
         tc_fence_after();
         const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
         float* orow = a.out + t * (int64_t)a.H * DV + (int64_t)h * DV + dv0;
 #pragma unroll 1
-        for (int c0 = 0; c0 < DVC; c0 += 32) {
+        for (int c = oc0; c < oc0 + OCOLS; c += 32) {
             float o[32];
             if (n_tiles > 0) {
-                tmem_ld32(trow + C::O + c0, o);
+                tmem_ld32(trow + C::O + c, o);
                 tmem_wait_ld();
             } else {
 #pragma unroll
@@ -848,7 +912,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (row_ok) {
 #pragma unroll
                 for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(orow + c0 + i) =
+                    *reinterpret_cast<float4*>(orow + c + i) =
                         make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
             }
         }
@@ -965,7 +1029,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
-    kern<<<grid, kThreads, C::SMEM, stream>>>(a, alibi, bias_staged, m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi, bias_staged, m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo);
     return cudaGetLastError();
 }
 
