@@ -420,16 +420,15 @@ def run_vtmu(args, rank, world, local):
         vnh = torch.from_numpy(x["v_new"]).pin_memory()
         outh = torch.empty((1, H * D), dtype=torch.float32).pin_memory()
 
+        # The host-buffer decode step of the C ABI: it copies q and the new
+        # rows in, runs the fused step, copies the output row back and waits.
+        hws_bytes = vtmu.vtmu_decode_step_host_workspace_size(p, 1)
+        hws = torch.zeros(hws_bytes, dtype=torch.uint8, device=dev)
+
         def e2e_step(i):
             s = sessions[i % 2]
-            with torch.cuda.stream(stream):
-                q.copy_(qh, non_blocking=True)
-                kn.copy_(knh, non_blocking=True)
-                vn.copy_(vnh, non_blocking=True)
-            vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
-            with torch.cuda.stream(stream):
-                outh.copy_(out, non_blocking=True)
-            stream.synchronize()  # the step's output is on the host before the next step
+            vtmu.vtmu_decode_step_host(s["Kc"], s["Vc"], off + 1, knh, vnh, 1, off, qh, None, outh, p, hws,
+                                       hws_bytes, st)
 
         h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
         d2h = outh.numel() * 4

@@ -102,6 +102,11 @@ def load_library():
         lib.vtmu_device_error.restype = ctypes.c_int
         lib.vtmu_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
         lib.vtmu_attention_decode_noalloc.restype = ctypes.c_int
+        lib.vtmu_decode_step_host_workspace_size.argtypes = [P, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.vtmu_decode_step_host_workspace_size.restype = ctypes.c_int
+        lib.vtmu_decode_step_host.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
+                                              vp, vp, vp, P, vp, ctypes.c_size_t, vp]
+        lib.vtmu_decode_step_host.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -118,6 +123,19 @@ def _addr(x):
     if isinstance(x, int):
         return x
     return x.data_ptr()
+
+
+def _haddr(x):
+    """Host address of a contiguous f32 numpy array or CPU tensor, an int, or None."""
+    if x is None or isinstance(x, int):
+        return x
+    if hasattr(x, "data_ptr"):
+        if x.device.type != "cpu" or not x.is_contiguous() or x.element_size() != 4:
+            raise ValueError("host buffer: expected a contiguous f32 CPU tensor")
+        return x.data_ptr()
+    if x.dtype.itemsize != 4 or x.dtype.kind != "f" or not x.flags["C_CONTIGUOUS"]:
+        raise ValueError("host buffer: expected a C-contiguous float32 array")
+    return x.ctypes.data
 
 
 # ---------------------------------------------------------------- C ABI names
@@ -146,6 +164,24 @@ def vtmu_decode_step(k_cache, v_cache, max_rows: int, k_new, v_new, new_rows: in
                                            _addr(v_new), int(new_rows), int(offset), _addr(q), _addr(bias),
                                            _addr(out), ctypes.byref(p), _addr(workspace), int(workspace_bytes),
                                            stream or None))
+
+
+def vtmu_decode_step_host_workspace_size(p: vtmu_attention_params, new_rows: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().vtmu_decode_step_host_workspace_size(ctypes.byref(p), int(new_rows), ctypes.byref(n)))
+    return int(n.value)
+
+
+def vtmu_decode_step_host(k_cache, v_cache, max_rows: int, k_new_host, v_new_host, new_rows: int, offset: int,
+                          q_host, bias_host, out_host, p: vtmu_attention_params, workspace, workspace_bytes: int,
+                          stream: int = 0) -> None:
+    """vtmu_decode_step with q / new rows / bias / out in host memory (numpy
+    arrays or CPU tensors, f32, contiguous; pinned memory copies
+    asynchronously).  Returns once out_host holds the result."""
+    _check(load_library().vtmu_decode_step_host(_addr(k_cache), _addr(v_cache), int(max_rows), _haddr(k_new_host),
+                                                _haddr(v_new_host), int(new_rows), int(offset), _haddr(q_host),
+                                                _haddr(bias_host), _haddr(out_host), ctypes.byref(p),
+                                                _addr(workspace), int(workspace_bytes), stream or None))
 
 
 def vtmu_cache_write(cache, max_rows: int, width: int, values, rows: int, offset: int, stream: int = 0) -> None:

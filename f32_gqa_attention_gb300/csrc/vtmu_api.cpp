@@ -209,6 +209,39 @@ size_t decode_workspace(const vtmu::AttnDesc& a) {
     return plan.workspace_bytes;
 }
 
+size_t attention_workspace(const Resolved& r) {
+    return r.kernel == VTMU_KERNEL_DECODE         ? decode_workspace(r.a)
+           : r.kernel == VTMU_KERNEL_PREFILL_TF32X3 ? vtmu::prefill_tc_workspace(r.a)
+                                                    : 0;
+}
+
+// Workspace of vtmu_decode_step_host: the attention workspace, then the
+// staging areas of q, k_new, v_new, bias and out (byte offsets, 256-aligned).
+struct HostStaging {
+    size_t q, k_new, v_new, bias, out, total;
+    size_t q_b, k_new_b, v_new_b, bias_b, out_b;
+};
+
+HostStaging host_staging(const Resolved& r, int64_t new_rows) {
+    const vtmu::AttnDesc& a = r.a;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    HostStaging h;
+    h.q_b = (size_t)a.T * a.H * a.D * 4;
+    h.k_new_b = (size_t)new_rows * a.Hk * a.D * 4;
+    h.v_new_b = (size_t)new_rows * a.Hk * a.Dv * 4;
+    h.bias_b = a.bias_kind == VTMU_BIAS_TS    ? (size_t)a.T * a.S * 4
+               : a.bias_kind == VTMU_BIAS_HTS ? (size_t)a.H * a.T * a.S * 4
+                                              : 0;
+    h.out_b = (size_t)a.T * a.H * a.Dv * 4;
+    h.q = up(attention_workspace(r));
+    h.k_new = h.q + up(h.q_b);
+    h.v_new = h.k_new + up(h.k_new_b);
+    h.bias = h.v_new + up(h.v_new_b);
+    h.out = h.bias + up(h.bias_b);
+    h.total = h.out + up(h.out_b);
+    return h;
+}
+
 }  // namespace
 
 namespace vtmu {
@@ -229,9 +262,7 @@ vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t
     Resolved r;
     vtmu_status st = resolve(p, &r);
     if (st != VTMU_OK) return st;
-    *bytes = r.kernel == VTMU_KERNEL_DECODE         ? decode_workspace(r.a)
-             : r.kernel == VTMU_KERNEL_PREFILL_TF32X3 ? vtmu::prefill_tc_workspace(r.a)
-                                                      : 0;
+    *bytes = attention_workspace(r);
     return ok();
 }
 
@@ -381,6 +412,69 @@ vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, c
         return fail(VTMU_ERR_INVALID, "decode_step: out overlaps a cache");
     vtmu::DecodeCacheWrite cw{k_cache, v_cache, k_new, v_new, offset, offset + new_rows};
     return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes, stream, &cw);
+}
+
+vtmu_status vtmu_decode_step_host_workspace_size(const vtmu_attention_params* p, int64_t new_rows, size_t* bytes) {
+    if (!bytes) return fail(VTMU_ERR_INVALID, "bytes is NULL");
+    if (new_rows < 0) return fail(VTMU_ERR_INVALID, "decode_step_host: negative new_rows %lld", (long long)new_rows);
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    *bytes = host_staging(r, new_rows).total;
+    return ok();
+}
+
+vtmu_status vtmu_decode_step_host(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new_host,
+                                  const float* v_new_host, int64_t new_rows, int64_t offset, const float* q_host,
+                                  const float* bias_host, float* out_host, const vtmu_attention_params* p,
+                                  void* workspace, size_t workspace_bytes, cudaStream_t stream) {
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    const vtmu::AttnDesc& a = r.a;
+    if (max_rows < 0 || new_rows < 0)
+        return fail(VTMU_ERR_INVALID, "decode_step_host: negative size (max_rows %lld, new_rows %lld)",
+                    (long long)max_rows, (long long)new_rows);
+    if (offset < 0 || offset > max_rows || new_rows > max_rows - offset)
+        return fail(VTMU_ERR_RANGE, "decode_step_host: offset %lld + rows %lld exceeds maxRows %lld",
+                    (long long)offset, (long long)new_rows, (long long)max_rows);
+    const HostStaging h = host_staging(r, new_rows);
+    if (!workspace || workspace_bytes < h.total)
+        return fail(VTMU_ERR_WORKSPACE, "decode_step_host: workspace of %zu bytes, %zu needed", workspace_bytes,
+                    h.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(VTMU_ERR_INVALID, "decode_step_host: workspace must be 256-byte aligned");
+    if ((h.q_b && !q_host) || (h.out_b && !out_host) || (h.k_new_b && !k_new_host) ||
+        (h.v_new_b && !v_new_host))
+        return fail(VTMU_ERR_INVALID, "decode_step_host: a host buffer is NULL");
+    if ((p->bias_kind != VTMU_BIAS_NONE) != (bias_host != nullptr))
+        return fail(VTMU_ERR_INVALID, "attention.bias: bias pointer and bias_kind disagree");
+    if (new_rows > 0 && (!k_cache || !v_cache))
+        return fail(VTMU_ERR_INVALID, "decode_step_host: a cache pointer is NULL");
+    if (a.S > max_rows)
+        return fail(VTMU_ERR_INVALID, "decode_step_host: S %lld exceeds the cache's %lld rows", (long long)a.S,
+                    (long long)max_rows);
+    char* w = static_cast<char*>(workspace);
+    auto stage = [&](size_t off, const float* src, size_t n) -> cudaError_t {
+        return n ? cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, stream) : cudaSuccess;
+    };
+    cudaError_t e = stage(h.q, q_host, h.q_b);
+    if (e == cudaSuccess) e = stage(h.k_new, k_new_host, h.k_new_b);
+    if (e == cudaSuccess) e = stage(h.v_new, v_new_host, h.v_new_b);
+    if (e == cudaSuccess) e = stage(h.bias, bias_host, h.bias_b);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: host to device copy");
+    auto dev = [&](size_t off, size_t n) -> float* { return n ? reinterpret_cast<float*>(w + off) : nullptr; };
+    st = vtmu_decode_step(k_cache, v_cache, max_rows, dev(h.k_new, h.k_new_b), dev(h.v_new, h.v_new_b), new_rows,
+                          offset, dev(h.q, h.q_b), dev(h.bias, h.bias_b), dev(h.out, h.out_b), p, workspace, h.q,
+                          stream);
+    if (st != VTMU_OK) return st;
+    if (h.out_b) {
+        e = cudaMemcpyAsync(out_host, w + h.out, h.out_b, cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: device to host copy");
+    }
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: stream synchronisation");
+    return ok();
 }
 
 vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width, const float* values, int64_t rows,

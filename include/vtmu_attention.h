@@ -25,9 +25,11 @@
  *
  * Conventions shared by every entry point
  *  - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations)
- *    owned by the caller; the library never allocates, frees or
- *    synchronises.  Work is enqueued on `stream` and the call returns at
- *    once.  Results are visible once the stream reaches that point.
+ *    owned by the caller; the library never allocates or frees, and never
+ *    synchronises except in vtmu_decode_step_host (host buffers), which
+ *    waits for its stream.  Work is enqueued on `stream` and the call
+ *    returns at once.  Results are visible once the stream reaches that
+ *    point.
  *  - Host pointers are marked HOST and are read during the call only.
  *  - Every check runs on the host before any launch.  A failed check
  *    launches nothing and returns a status; vtmu_last_error() then names the
@@ -182,6 +184,44 @@ VTMU_API vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t ma
                                       int64_t offset, const float* q, const float* bias, float* out,
                                       const vtmu_attention_params* p, void* workspace,
                                       size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * Workspace bytes of vtmu_decode_step_host for these params and new_rows:
+ * the workspace vtmu_attention needs for `p`, then device staging areas for
+ * q, k_new, v_new, the bias and out, each starting on a 256-byte boundary.
+ * Errors: those of vtmu_attention_workspace_size, VTMU_ERR_INVALID
+ * (new_rows < 0).
+ */
+VTMU_API vtmu_status vtmu_decode_step_host_workspace_size(const vtmu_attention_params* p,
+                                                          int64_t new_rows, size_t* bytes);
+
+/*
+ * A decode step whose inputs and output live in HOST memory: the call a
+ * worker makes when a step's q and new K/V rows arrive over the network and
+ * its output row goes back (vtmu.mpakt.dev/api/ops: the worker runs the
+ * step and returns the result).  On `stream` it copies q_host, k_new_host,
+ * v_new_host and bias_host into the staging areas of `workspace`, runs
+ * vtmu_decode_step on those copies, copies out back to out_host and WAITS for
+ * the stream: unlike every other entry point it returns only when out_host
+ * holds the result (or an error occurred).
+ *   k_cache, v_cache, max_rows, new_rows, offset, p: as for vtmu_decode_step
+ *     (the caches are DEVICE memory, updated in place).
+ *   q_host [T, heads*headDim], k_new_host / v_new_host [new_rows, kvHeads*
+ *     headDim / vHeadDim], bias_host (as bias_kind says, or NULL), out_host
+ *     [T, heads*vHeadDim]: HOST, row-major f32.  Page-locked memory lets the
+ *     copies run asynchronously; pageable memory works with staged copies.
+ *   workspace: DEVICE, at least vtmu_decode_step_host_workspace_size bytes,
+ *     256-byte aligned; its first 64 KiB follow vtmu_attention's rule.
+ * Errors: those of vtmu_decode_step, VTMU_ERR_WORKSPACE (workspace too
+ * small), VTMU_ERR_INVALID (a host pointer NULL where data is needed),
+ * VTMU_ERR_CUDA (a copy or the wait failed).  Checks run before any copy.
+ */
+VTMU_API vtmu_status vtmu_decode_step_host(float* k_cache, float* v_cache, int64_t max_rows,
+                                           const float* k_new_host, const float* v_new_host,
+                                           int64_t new_rows, int64_t offset, const float* q_host,
+                                           const float* bias_host, float* out_host,
+                                           const vtmu_attention_params* p, void* workspace,
+                                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
  * op "cache_write" (vtmu.mpakt.dev/api/ops): cache[offset + r, :] =

@@ -195,3 +195,40 @@ def test_noalloc_checks_parameters_first(lib):
 @host_only
 def test_device_error_needs_an_output(lib):
     assert lib.vtmu_device_error(None) == vtmu.VTMU_ERR_INVALID
+
+
+def test_host_decode_step_workspace_adds_the_staging_areas(lib):
+    """vtmu_decode_step_host's workspace: the attention workspace, then q, the
+    new rows, the bias and out, each on a 256-byte boundary."""
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
+    base = vtmu.vtmu_attention_workspace_size(p)
+    up = lambda n: (n + 255) // 256 * 256
+    want = up(base) + up(32 * 128 * 4) + 2 * up(3 * 8 * 128 * 4) + up(32 * 128 * 4)
+    assert vtmu.vtmu_decode_step_host_workspace_size(p, 3) == want
+    pb = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095, bias_kind=vtmu.VTMU_BIAS_HTS)
+    assert vtmu.vtmu_decode_step_host_workspace_size(pb, 3) == want + up(32 * 4096 * 4)
+    assert _err(lambda: vtmu.vtmu_decode_step_host_workspace_size(p, -1)).status == vtmu.VTMU_ERR_INVALID
+
+
+@host_only
+def test_host_decode_step_checks_before_any_copy(lib):
+    import numpy as np
+
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
+    need = vtmu.vtmu_decode_step_host_workspace_size(p, 1)
+    q = np.zeros((1, 32 * 128), np.float32)
+    kn = np.zeros((1, 8 * 128), np.float32)
+    out = np.zeros((1, 32 * 128), np.float32)
+    call = lambda **o: _err(lambda: vtmu.vtmu_decode_step_host(
+        o.get("kc", FAKE * 3), FAKE * 5, o.get("rows", 4096), kn, kn, 1, o.get("off", 4095), o.get("q", q),
+        o.get("b"), out, o.get("p", p), o.get("ws", FAKE * 7), o.get("wsb", need), 0))
+    assert call(wsb=need - 1).status == vtmu.VTMU_ERR_WORKSPACE
+    assert "256-byte" in str(call(ws=FAKE * 7 + 16))
+    assert call(q=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(off=4096).status == vtmu.VTMU_ERR_RANGE
+    assert "attention.bias" in str(call(b=q))
+    assert call(kc=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(rows=4000, off=3000).status == vtmu.VTMU_ERR_INVALID  # S > max_rows
+    with pytest.raises(ValueError):
+        vtmu.vtmu_decode_step_host(FAKE * 3, FAKE * 5, 4096, kn, kn, 1, 4095, q.astype(np.float64), None, out, p,
+                                   FAKE * 7, need, 0)

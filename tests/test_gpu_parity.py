@@ -318,6 +318,46 @@ def test_decode_step_unfused_paths():
     _decode_step_case(700, 4, 4, 96, 1, 650, 502)
 
 
+@pytest.mark.parametrize("case", [
+    dict(S=32768, H=32, Hk=8, D=128, T=1, new_rows=1, offset=32767, pinned=True),   # the decode workload
+    dict(S=3000, H=8, Hk=4, D=64, T=1, new_rows=3, offset=2990, pinned=False, bias=True),
+    dict(S=700, H=4, Hk=2, D=128, T=6, new_rows=6, offset=600, pinned=True),       # unfused (T = 6)
+])
+def test_decode_step_host_buffers(case):
+    """vtmu_decode_step_host: the step's inputs and output in host memory
+    (pinned or pageable).  Caches bit-exact against the oracle's cache_write,
+    the output bit-identical to the device-buffer step on the same data and
+    within tolerance of the oracle."""
+    S, H, Hk, D, T, n, off = (case[k] for k in ("S", "H", "Hk", "D", "T", "new_rows", "offset"))
+    g = si.Stream(510)
+    x = {"q": g.normal_f32(T * H * D).reshape(T, H * D), "kc": g.normal_f32(S * Hk * D).reshape(S, Hk * D),
+         "vc": g.normal_f32(S * Hk * D).reshape(S, Hk * D), "kn": g.normal_f32(n * Hk * D).reshape(n, Hk * D),
+         "vn": g.normal_f32(n * Hk * D).reshape(n, Hk * D)}
+    bias = g.normal_f32(T * S).reshape(T, S) if case.get("bias") else None
+    pos = off + n - T
+    p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, posOffset=pos,
+                         bias_kind=vtmu.VTMU_BIAS_TS if bias is not None else vtmu.VTMU_BIAS_NONE)
+    host = lambda a: torch.from_numpy(a).pin_memory() if case["pinned"] else a
+    nb = vtmu.vtmu_decode_step_host_workspace_size(p, n)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
+    out_h = host(np.zeros((T, H * D), np.float32))
+    st = torch.cuda.current_stream().cuda_stream
+    vtmu.vtmu_decode_step_host(Kc, Vc, S, host(x["kn"]), host(x["vn"]), n, off, host(x["q"]),
+                               None if bias is None else host(bias), out_h, p, ws, nb, st)
+    out_host = np.asarray(out_h).copy()
+    Kd, Vd = to_dev(x["kc"]), to_dev(x["vc"])
+    out_dev = vtmu.decode_step(Kd, Vd, to_dev(x["kn"]), to_dev(x["vn"]), off, to_dev(x["q"]),
+                               None if bias is None else to_dev(bias), heads=H, headDim=D, kvHeads=Hk, posOffset=pos)
+    torch.cuda.synchronize()
+    assert out_host.tobytes() == out_dev.cpu().numpy().tobytes(), "host-buffer step differs from the device step"
+    oracle.cache_write(x["kc"], x["kn"], off)
+    oracle.cache_write(x["vc"], x["vn"], off)
+    assert Kc.cpu().numpy().tobytes() == x["kc"].tobytes() and Vc.cpu().numpy().tobytes() == x["vc"].tobytes()
+    ref = oracle.attention(x["q"], x["kc"], x["vc"], bias, heads=H, headDim=D, kvHeads=Hk, posOffset=pos)
+    assert max_err(out_host, ref) <= TOL
+
+
 def test_decode_step_refuses_rows_past_the_cache():
     Kc = torch.zeros((8, 4), device="cuda")
     Vc = torch.zeros((8, 4), device="cuda")
