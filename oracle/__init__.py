@@ -1,4 +1,4 @@
-"""CPU oracle for the f32 ``attention`` and ``cache_write`` ops.
+"""CPU oracle for the f32 ``attention``, ``cache_write`` and ``rope`` ops.
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg are the only callers.  The product path (the
@@ -102,6 +102,10 @@ class Oracle:
         lib.oracle_cache_write.argtypes = [p, ctypes.c_int64, ctypes.c_int64,
                                            p, ctypes.c_int64, ctypes.c_int64]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_rope_inv_freq.argtypes = [ctypes.c_int, ctypes.c_double, p]
+        lib.oracle_rope.argtypes = [p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
+                                    ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                    ctypes.c_double, p, ctypes.c_double, p]
         self.lib = lib
         self.path = path
 
@@ -216,6 +220,51 @@ class Oracle:
             raise ValueError("cache_write: rows do not fit the cache at offset")
         return cache
 
+    def rope_inv_freq(self, rotaryDim, base=None):
+        """base^(-2j / rotaryDim) for j < rotaryDim / 2, in double."""
+        out = np.zeros(int(rotaryDim) // 2, dtype=np.float64)
+        if self.lib.oracle_rope_inv_freq(int(rotaryDim), 10000.0 if base is None else float(base), _ptr(out)):
+            raise ValueError("rope: rotaryDim must be positive and even, base positive")
+        return out
+
+    def rope(self, x, *, headDim, offset=0, base=None, rotaryDim=None,
+             interleaved=False, scaling=None, invFreq=None,
+             attentionFactor=None):
+        """op "rope" (vtmu.mpakt.dev/api/ops): x [T, heads*headDim] -> the
+        same shape, float64.  Defaults as the catalog states them: base
+        (rope_theta) 10000, offset 0, rotaryDim = headDim, half-split pairs.
+        ``scaling`` is config.json's rope_scaling object; the linear scheme
+        (positions divided by ``factor``) is the one implemented here.
+        ``invFreq`` replaces the base-derived frequencies; ``attentionFactor``
+        multiplies cos and sin (default 1)."""
+        x = _f32(x)
+        headDim = int(headDim)
+        if x.ndim != 2 or headDim <= 0 or x.shape[1] % headDim:
+            raise ValueError("x must be [T, heads*headDim]")
+        heads = x.shape[1] // headDim
+        rd = headDim if rotaryDim is None else int(rotaryDim)
+        if rd <= 0 or rd % 2 or rd > headDim:
+            raise ValueError("rotaryDim must be even and at most headDim")
+        if invFreq is not None:
+            inv = np.ascontiguousarray(np.asarray(invFreq, dtype=np.float64))
+            if inv.shape != (rd // 2,):
+                raise ValueError("invFreq needs rotaryDim / 2 values")
+        else:
+            inv = self.rope_inv_freq(rd, base)
+        divisor = 1.0
+        if scaling is not None:
+            kind = scaling.get("rope_type", scaling.get("type"))
+            if kind != "linear":
+                raise ValueError(f"rope.scaling: {kind!r} is not implemented")
+            divisor = float(scaling["factor"])
+        af = 1.0 if attentionFactor is None else float(attentionFactor)
+        out = np.zeros(x.shape, dtype=np.float64)
+        if x.shape[0] and self.lib.oracle_rope(_ptr(x), x.shape[0], heads, headDim, rd,
+                                               1 if interleaved else 0, int(offset), divisor,
+                                               _ptr(inv), af, _ptr(out)):
+            raise ValueError("oracle_rope failed")
+        return out
+
 
 def default() -> Oracle:
     global _default
@@ -242,3 +291,11 @@ def attention_rows(q, k, v, bias=None, **params):
 
 def cache_write(cache, values, offset):
     return default().cache_write(cache, values, offset)
+
+
+def rope(x, **params):
+    return default().rope(x, **params)
+
+
+def rope_inv_freq(rotaryDim, base=None):
+    return default().rope_inv_freq(rotaryDim, base)

@@ -1,7 +1,7 @@
 /*
- * attention_oracle.c -- plain, slow CPU oracle for the f32 `attention` and
- * `cache_write` ops of the volunteer-inference op catalog
- * (vtmu.mpakt.dev/api/ops, ops "attention" and "cache_write").
+ * attention_oracle.c -- plain, slow CPU oracle for the f32 `attention`,
+ * `cache_write` and `rope` ops of the volunteer-inference op catalog
+ * (vtmu.mpakt.dev/api/ops, ops "attention", "cache_write" and "rope").
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the tests, the package smoke check and the benchmark's
@@ -235,6 +235,54 @@ int oracle_cache_write(float* cache, int64_t max_rows, int64_t width,
     for (int64_t r = 0; r < rows; ++r)
         for (int64_t c = 0; c < width; ++c)
             cache[(offset + r) * width + c] = values[r * width + c];
+    return 0;
+}
+
+/* Inverse frequencies of op "rope" (same page, param base = rope_theta,
+ * default 10000): inv_freq[j] = base^(-2j / rotary_dim) for j < rotary_dim/2,
+ * the geometric sequence of rotary position embeddings (Su et al.,
+ * "RoFormer", 2021).  Returns 1 on a bad argument. */
+int oracle_rope_inv_freq(int rotary_dim, double base, double* out)
+{
+    if (rotary_dim <= 0 || rotary_dim % 2 != 0 || !(base > 0.0)) return 1;
+    for (int j = 0; j < rotary_dim / 2; ++j)
+        out[j] = pow(base, -2.0 * (double)j / (double)rotary_dim);
+    return 0;
+}
+
+/* op "rope": rotary position embedding of x [T, heads*head_dim].  Row t sits
+ * at position (offset + t) / pos_divisor (pos_divisor is 1, or the factor of
+ * a linear frequency scaling).  Pair j < rotary_dim/2 of every head turns by
+ * theta = position * inv_freq[j]: channels (j, j + rotary_dim/2), or
+ * (2j, 2j + 1) when interleaved, go
+ *     (a, b) -> (a cos(theta) - b sin(theta), b cos(theta) + a sin(theta)),
+ * with cos and sin multiplied by attention_factor; channels at or past
+ * rotary_dim pass through.  Output in double.  Returns 1 on a bad argument. */
+int oracle_rope(const float* x, int64_t T, int heads, int head_dim, int rotary_dim,
+                int interleaved, int64_t offset, double pos_divisor,
+                const double* inv_freq, double attention_factor, double* out)
+{
+    if (T < 0 || heads <= 0 || head_dim <= 0 || rotary_dim < 0 || rotary_dim > head_dim ||
+        rotary_dim % 2 != 0 || offset < 0 || !(pos_divisor > 0.0))
+        return 1;
+    const int half = rotary_dim / 2;
+    for (int64_t t = 0; t < T; ++t) {
+        const double position = (double)(offset + t) / pos_divisor;
+        for (int h = 0; h < heads; ++h) {
+            const float* xr = x + (t * heads + h) * (int64_t)head_dim;
+            double* orow = out + (t * heads + h) * (int64_t)head_dim;
+            for (int d = rotary_dim; d < head_dim; ++d) orow[d] = xr[d];
+            for (int j = 0; j < half; ++j) {
+                const int ia = interleaved ? 2 * j : j;
+                const int ib = interleaved ? 2 * j + 1 : j + half;
+                const double theta = position * inv_freq[j];
+                const double c = cos(theta) * attention_factor;
+                const double s = sin(theta) * attention_factor;
+                orow[ia] = (double)xr[ia] * c - (double)xr[ib] * s;
+                orow[ib] = (double)xr[ib] * c + (double)xr[ia] * s;
+            }
+        }
+    }
     return 0;
 }
 

@@ -2,7 +2,7 @@
 
 Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
 oracle disagrees with something the op catalog (vtmu.mpakt.dev/api/ops, ops
-"attention", "softcap", "softmax", "cache_write") or plain mathematics fixes:
+"attention", "softcap", "softmax", "cache_write", "rope") or plain mathematics fixes:
 hand-worked examples, closed forms, limits, invariants, a library routine
 (PyTorch's float64 ``scaled_dot_product_attention``) on the cases it can
 express, and exact rational brute force.  ``test_oracle_pins.py`` runs them on
@@ -356,6 +356,90 @@ def pin_cache_write(orc):
             raise AssertionError(f"offset {bad} must be refused")
     orc.cache_write(cache, np.zeros((0, 3), np.float32), 6)  # empty write at the end
     assert np.array_equal(cache, want)
+
+
+# ------------------------------------------------------------------------ rope
+# op "rope" of the same page: rotary position embedding over [T, heads*headDim].
+def pin_rope_hand_examples(orc):
+    with open(os.path.join(GOLDEN, "rope_hand_examples.json")) as f:
+        doc = json.load(f)
+    for c in doc["cases"]:
+        out = orc.rope(np.asarray(c["x"], np.float32), **c["params"])
+        want = np.asarray(c["expected"], np.float64)
+        err = np.max(np.abs(out - want))
+        assert err <= doc["tol"], f"{c['name']}: err {err} ({out} vs {want})"
+
+
+def _pairs(headDim, rd, interleaved):
+    half = rd // 2
+    return [((2 * j, 2 * j + 1) if interleaved else (j, j + half)) for j in range(half)]
+
+
+def pin_rope_relative_position(orc):
+    """The defining property of rotary embeddings: the dot product of a query
+    at position m with a key at position n depends on m - n only (per head, on
+    the rotated channels; the pass-through channels add a constant)."""
+    g = _rng(41)
+    D, H = 10, 2
+    for interleaved in (False, True):
+        q = g.standard_normal((1, H * D)).astype(np.float32)
+        k = g.standard_normal((1, H * D)).astype(np.float32)
+        kw = dict(headDim=D, rotaryDim=8, interleaved=interleaved, base=500.0)
+        dots = []
+        for m, n in ((7, 3), (40, 36), (1004, 1000)):
+            a = orc.rope(q, offset=m, **kw).reshape(H, D)
+            b = orc.rope(k, offset=n, **kw).reshape(H, D)
+            dots.append(np.sum(a * b, axis=1))
+        assert np.allclose(dots[0], dots[1], rtol=0, atol=1e-9), dots
+        assert np.allclose(dots[0], dots[2], rtol=0, atol=1e-9), dots
+        # and a different offset changes it
+        c = orc.rope(q, offset=8, **kw).reshape(H, D)
+        assert not np.allclose(np.sum(c * orc.rope(k, offset=3, **kw).reshape(H, D), axis=1), dots[0])
+
+
+def pin_rope_norm_and_pass_through(orc):
+    """Each pair is rotated (its norm times attentionFactor); channels past
+    rotaryDim come out unchanged."""
+    g = _rng(42)
+    D, H, rd, af = 12, 3, 8, 1.5
+    x = g.standard_normal((5, H * D)).astype(np.float32)
+    for interleaved in (False, True):
+        out = orc.rope(x, headDim=D, rotaryDim=rd, interleaved=interleaved, offset=17,
+                       attentionFactor=af).reshape(5, H, D)
+        xr = x.astype(np.float64).reshape(5, H, D)
+        assert np.array_equal(out[:, :, rd:], xr[:, :, rd:])
+        for a, b in _pairs(D, rd, interleaved):
+            n_in = np.hypot(xr[:, :, a], xr[:, :, b])
+            n_out = np.hypot(out[:, :, a], out[:, :, b])
+            assert np.allclose(n_out, af * n_in, rtol=1e-12, atol=1e-12)
+        assert not np.allclose(out[:, :, :rd], af * xr[:, :, :rd])  # it does turn
+
+
+def pin_rope_interleaved_is_permuted_half_split(orc):
+    """Interleaved pairing is half-split pairing on permuted channels: the
+    permutation sending channel 2j -> j and 2j+1 -> j + rd/2 conjugates one
+    into the other."""
+    g = _rng(43)
+    D, H, rd = 8, 2, 8
+    perm = np.array([2 * j for j in range(rd // 2)] + [2 * j + 1 for j in range(rd // 2)])
+    x = g.standard_normal((3, H * D)).astype(np.float32)
+    xi = x.reshape(3, H, D)
+    xh = xi[:, :, perm].reshape(3, H * D)  # half-split order
+    a = orc.rope(x, headDim=D, interleaved=True, offset=9).reshape(3, H, D)
+    b = orc.rope(xh, headDim=D, interleaved=False, offset=9).reshape(3, H, D)
+    assert np.allclose(a[:, :, perm], b, rtol=0, atol=1e-12)
+
+
+def pin_rope_linear_scaling_and_inv_freq(orc):
+    """Linear scaling by f at position f*p equals no scaling at p; explicit
+    inverse frequencies equal to the base-derived ones change nothing."""
+    g = _rng(44)
+    x = g.standard_normal((3, 2 * 16)).astype(np.float32)
+    plain = orc.rope(x, headDim=16, offset=6)
+    lin = orc.rope(x, headDim=16, offset=18, scaling={"rope_type": "linear", "factor": 3.0})
+    assert np.allclose(plain[0], lin[0], rtol=0, atol=1e-12)  # row 0: 18 / 3 = 6
+    inv = [10000.0 ** (-2.0 * j / 16) for j in range(8)]
+    assert np.allclose(orc.rope(x, headDim=16, offset=6, invFreq=inv), plain, rtol=0, atol=1e-12)
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -53,6 +53,22 @@ MUTANTS = [
      "            for (int i = 2; i <= n && w < heads; i += 2) out[w++] = a[i - 1];"),
     ("cache_write copies the first row everywhere",
      "= values[r * width + c];", "= values[c];"),
+    ("rope turns the wrong way (op rope: rotary embedding)",
+     "orow[ia] = (double)xr[ia] * c - (double)xr[ib] * s;", "orow[ia] = (double)xr[ia] * c + (double)xr[ib] * s;"),
+    ("rope half-split partner i + 1 instead of i + rotaryDim/2",
+     "const int ib = interleaved ? 2 * j + 1 : j + half;", "const int ib = interleaved ? 2 * j + 1 : j + 1;"),
+    ("rope interleaved flag ignored for the partner",
+     "const int ib = interleaved ? 2 * j + 1 : j + half;", "const int ib = interleaved ? j + half : j + half;"),
+    ("rope frequencies base^(-j/rotaryDim)",
+     "pow(base, -2.0 * (double)j / (double)rotary_dim)", "pow(base, -1.0 * (double)j / (double)rotary_dim)"),
+    ("rope attentionFactor on cos only (it multiplies cos and sin)",
+     "const double s = sin(theta) * attention_factor;", "const double s = sin(theta);"),
+    ("rope pass-through channels dropped (rotaryDim: the rest pass through)",
+     "for (int d = rotary_dim; d < head_dim; ++d) orow[d] = xr[d];", ""),
+    ("rope offset ignored (offset: position of the first row)",
+     "const double position = (double)(offset + t) / pos_divisor;", "const double position = (double)t / pos_divisor;"),
+    ("rope linear scaling ignored",
+     "const double position = (double)(offset + t) / pos_divisor;", "const double position = (double)(offset + t);"),
 ]
 
 
