@@ -67,6 +67,23 @@ class vtmu_attention_params(ctypes.Structure):
     ]
 
 
+VTMU_ROPE_SCALING_NONE, VTMU_ROPE_SCALING_LINEAR = 0, 1
+
+
+class vtmu_rope_params(ctypes.Structure):
+    """Mirror of ``vtmu_rope_params`` (include/vtmu_attention.h)."""
+    _fields_ = [
+        ("head_dim", ctypes.c_int32),
+        ("rotary_dim", ctypes.c_int32),
+        ("interleaved", ctypes.c_int32),
+        ("scaling", ctypes.c_int32),
+        ("base", ctypes.c_float),
+        ("scaling_factor", ctypes.c_float),
+        ("attention_factor", ctypes.c_float),
+        ("inv_freq", ctypes.POINTER(ctypes.c_float)),
+    ]
+
+
 _lib = None
 _lib_lock = threading.Lock()
 
@@ -102,6 +119,14 @@ def load_library():
         lib.vtmu_device_error.restype = ctypes.c_int
         lib.vtmu_attention_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, P, vp]
         lib.vtmu_attention_decode_noalloc.restype = ctypes.c_int
+        R = ctypes.POINTER(vtmu_rope_params)
+        lib.vtmu_rope_params_init.argtypes = [R]
+        lib.vtmu_rope_params_init.restype = None
+        lib.vtmu_rope.argtypes = [vp, vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int64, R, vp]
+        lib.vtmu_rope.restype = ctypes.c_int
+        lib.vtmu_decode_step_rope.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
+                                              vp, vp, vp, P, R, vp, ctypes.c_size_t, vp]
+        lib.vtmu_decode_step_rope.restype = ctypes.c_int
         lib.vtmu_decode_step_host_workspace_size.argtypes = [P, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
         lib.vtmu_decode_step_host_workspace_size.restype = ctypes.c_int
         lib.vtmu_decode_step_host.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
@@ -184,6 +209,26 @@ def vtmu_decode_step_host(k_cache, v_cache, max_rows: int, k_new_host, v_new_hos
                                                 _addr(workspace), int(workspace_bytes), stream or None))
 
 
+def vtmu_rope_params_init() -> vtmu_rope_params:
+    r = vtmu_rope_params()
+    load_library().vtmu_rope_params_init(ctypes.byref(r))
+    return r
+
+
+def vtmu_rope(x, out, T: int, heads: int, offset: int, r: vtmu_rope_params, stream: int = 0) -> None:
+    _check(load_library().vtmu_rope(_addr(x), _addr(out), int(T), int(heads), int(offset), ctypes.byref(r),
+                                    stream or None))
+
+
+def vtmu_decode_step_rope(k_cache, v_cache, max_rows: int, k_new, v_new, new_rows: int, offset: int, q, bias, out,
+                          p: vtmu_attention_params, r: vtmu_rope_params, workspace, workspace_bytes: int,
+                          stream: int = 0) -> None:
+    _check(load_library().vtmu_decode_step_rope(_addr(k_cache), _addr(v_cache), int(max_rows), _addr(k_new),
+                                                _addr(v_new), int(new_rows), int(offset), _addr(q), _addr(bias),
+                                                _addr(out), ctypes.byref(p), ctypes.byref(r), _addr(workspace),
+                                                int(workspace_bytes), stream or None))
+
+
 def vtmu_cache_write(cache, max_rows: int, width: int, values, rows: int, offset: int, stream: int = 0) -> None:
     _check(load_library().vtmu_cache_write(_addr(cache), int(max_rows), int(width), _addr(values),
                                            int(rows), int(offset), stream or None))
@@ -245,6 +290,29 @@ def make_params(T, S, *, heads, headDim, kvHeads=None, vHeadDim=None, causal=Tru
     p.kernel = int(kernel)
     p.decode_splits = int(decode_splits)
     return p
+
+
+def make_rope_params(*, headDim, base=None, rotaryDim=None, interleaved=False, scaling=None, invFreq=None,
+                     attentionFactor=None):
+    """A rope params struct from op "rope"'s parameter names.  ``scaling`` is
+    config.json's rope_scaling object; "linear" maps to the library's linear
+    scaling and any other kind is passed on so that the library refuses it
+    with "rope.scaling" named.  Keeps an invFreq array alive as ``_inv``."""
+    r = vtmu_rope_params_init()
+    r.head_dim = int(headDim)
+    r.rotary_dim = 0 if rotaryDim is None else int(rotaryDim)
+    r.interleaved = 1 if interleaved else 0
+    r.base = 0.0 if base is None else float(base)
+    if scaling is not None:
+        kind = scaling.get("rope_type", scaling.get("type"))
+        r.scaling = VTMU_ROPE_SCALING_LINEAR if kind == "linear" else 100
+        r.scaling_factor = float(scaling.get("factor", 0.0))
+    r.attention_factor = 0.0 if attentionFactor is None else float(attentionFactor)
+    if invFreq is not None:
+        arr = (ctypes.c_float * len(invFreq))(*[float(f) for f in invFreq])
+        r.inv_freq = ctypes.cast(arr, ctypes.POINTER(ctypes.c_float))
+        r._inv = arr
+    return r
 
 
 class Workspace:
@@ -320,6 +388,44 @@ def decode_step(k_cache, v_cache, k_new, v_new, offset: int, q, bias=None, *, he
     buf, cap = ws.get(nbytes)
     st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
     vtmu_decode_step(k_cache, v_cache, S, k_new, v_new, k_new.shape[0], offset, q, bias, out, p, buf, cap, st)
+    return out
+
+
+def rope(x, *, headDim, offset=0, out=None, stream=None, **params):
+    """op "rope" on a CUDA tensor x [T, heads*headDim]; ``out=x`` turns it in
+    place.  Params as make_rope_params.  Returns out."""
+    import torch
+    T, width = x.shape
+    if out is None:
+        out = torch.empty_like(x)
+    r = make_rope_params(headDim=headDim, **params)
+    st = stream if stream is not None else torch.cuda.current_stream(x.device).cuda_stream
+    vtmu_rope(x, out, T, width // headDim, offset, r, st)
+    return out
+
+
+def decode_step_rope(k_cache, v_cache, k_new, v_new, offset: int, q, bias=None, *, heads, headDim, rope: dict,
+                     out=None, workspace=None, stream=None, **params):
+    """decode_step with the rotary embedding ``rope`` (make_rope_params
+    names, headDim taken from the call) fused in: q and the new keys are
+    turned inside the one decode launch, the caches receive turned keys."""
+    import torch
+    T, S = q.shape[0], k_cache.shape[0]
+    vhd = params.get("vHeadDim") or headDim
+    params.setdefault("posOffset", offset + k_new.shape[0] - T)
+    bias_kind = VTMU_BIAS_NONE
+    if bias is not None:
+        bias_kind = VTMU_BIAS_TS if bias.dim() == 2 else VTMU_BIAS_HTS
+    p = make_params(T, S, heads=heads, headDim=headDim, bias_kind=bias_kind, **params)
+    r = make_rope_params(headDim=headDim, **rope)
+    if out is None:
+        out = torch.empty((T, heads * vhd), dtype=torch.float32, device=q.device)
+    nbytes = vtmu_attention_workspace_size(p)
+    ws = workspace if workspace is not None else _default_workspace(q.device)
+    buf, cap = ws.get(nbytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    vtmu_decode_step_rope(k_cache, v_cache, S, k_new, v_new, k_new.shape[0], offset, q, bias, out, p, r, buf, cap,
+                          st)
     return out
 
 

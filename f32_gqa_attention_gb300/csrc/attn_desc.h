@@ -35,4 +35,16 @@ struct AlibiTable {
     float slope_log2[kMaxAlibiHeads];
 };
 
+// Rotary position embedding (op "rope"), resolved on the host (passed by
+// value).  Pair j < half turns by pos * inv_freq[j]: channels (j, j + half),
+// or (2j, 2j + 1) when interleaved; channels at or past 2 * half pass through.
+constexpr int kRopeMaxPairs = 128;  // rotaryDim <= 256
+struct RopeDev {
+    int32_t half;         // rotaryDim / 2 (0: nothing turns)
+    int32_t interleaved;
+    float attn;           // attentionFactor, multiplies cos and sin
+    int32_t pad;
+    double inv_freq[kRopeMaxPairs];  // with a linear scaling's factor divided out
+};
+
 }  // namespace vtmu

@@ -38,6 +38,7 @@
 
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "rope.cuh"
 #include "tma_sync.cuh"
 
 namespace vtmu {
@@ -77,7 +78,19 @@ struct DecodeArgs {
     float* part_o;           // [heads][splits][Dv]
     unsigned int* counters;  // [kvHeads], zero between calls
     DecodeCacheWrite cw;     // fused cache_write (cw.k_new == nullptr: none)
+    RopeDev rope;            // rotary embedding of q and the new keys (rope.half == 0: none)
 };
+
+// Element d of new key row `pos` (k_new row base `src`), turned by the rotary
+// embedding when it is on: the cache stores turned keys.
+__device__ __forceinline__ float new_key(const DecodeArgs& args, int64_t src, int d, int64_t pos) {
+    const float own = __ldg(args.cw.k_new + src + d);
+    if (d >= 2 * args.rope.half) return own;
+    int j, partner;
+    bool first;
+    rope_pair_of(args.rope, d, j, partner, first);
+    return rope_channel(own, __ldg(args.cw.k_new + src + partner), first, rope_cos_sin(args.rope, pos, j));
+}
 
 template <int D, int G>
 struct DecCfg {
@@ -149,6 +162,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     __shared__ __align__(8) uint64_t empty_bar[STAGES];
     __shared__ __align__(16) float pbuf[C::WARPS][32];
     __shared__ int s_is_last;
+    __shared__ float2 q_cs[D / 2];  // rotary (cos, sin) of the query row, per pair
 
     const AttnDesc& a = args.a;
     const int split = VTMU_DEC_KH_FAST ? blockIdx.y : blockIdx.x;
@@ -179,11 +193,12 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
             if (r >= args.s_lo && r < args.s_end) continue;
             const int64_t src = (r - args.cw.lo) * ld + (int64_t)kh * D, dst = r * ld + (int64_t)kh * D;
             for (int d = lane; d < D; d += 32) {
-                args.cw.kc[dst + d] = __ldg(args.cw.k_new + src + d);
+                args.cw.kc[dst + d] = new_key(args, src, d, r);
                 args.cw.vc[dst + d] = __ldg(args.cw.v_new + src + d);
             }
         }
     }
+    for (int j = threadIdx.x; j < args.rope.half; j += blockDim.x) q_cs[j] = rope_cos_sin(args.rope, p, j);
     __syncthreads();
 
     float m_run = -INFINITY;  // running max of head lane%G (base 2)
@@ -228,7 +243,17 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
         for (int gi = 0; gi < G; ++gi) {
             const float* qh = a.q + (int64_t)(kh * G + (gi ^ (lane % G))) * D;
 #pragma unroll
-            for (int j = 0; j < PL; ++j) qv[gi][j] = __ldg(qh + lane_dim<VEC>(lane, j));
+            for (int j = 0; j < PL; ++j) {
+                const int d = lane_dim<VEC>(lane, j);
+                float x = __ldg(qh + d);
+                if (d < 2 * args.rope.half) {
+                    int pj, partner;
+                    bool first;
+                    rope_pair_of(args.rope, d, pj, partner, first);
+                    x = rope_channel(x, __ldg(qh + partner), first, q_cs[pj]);
+                }
+                qv[gi][j] = x;
+            }
         }
         const int rr = lane / G;  // logical slot after the butterfly: row rr, head gg
         const int gg = lane % G;
@@ -262,7 +287,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 #pragma unroll
                         for (int j = 0; j < PL; ++j) {
                             const int d = lane_dim<VEC>(lane, j);
-                            const float kx = __ldg(args.cw.k_new + src + d);
+                            const float kx = new_key(args, src, d, r);
                             const float vx = __ldg(args.cw.v_new + src + d);
                             skr[d] = kx;
                             svr[d] = vx;
@@ -581,10 +606,12 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
 }
 
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
-                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw) {
+                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw, const RopeDev* rope) {
     DecodeArgs args;
     std::memset(&args.cw, 0, sizeof(args.cw));
     if (cw) args.cw = *cw;
+    std::memset(&args.rope, 0, sizeof(args.rope));
+    if (rope) args.rope = *rope;
     args.a = a;
     args.s_lo = plan.s_lo;
     args.s_end = plan.s_end;

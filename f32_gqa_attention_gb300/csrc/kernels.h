@@ -41,8 +41,11 @@ struct DecodeCacheWrite {
 bool decode_supported(const AttnDesc& a);
 // Fills `plan` for the call; `forced_splits` > 0 overrides the heuristic.
 void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan);
+// With `rope`, the query row and the new key rows are turned by the rotary
+// embedding first (the cache receives turned keys).
 cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const DecodePlan& plan,
-                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw = nullptr);
+                          void* workspace, cudaStream_t stream, const DecodeCacheWrite* cw = nullptr,
+                          const RopeDev* rope = nullptr);
 // Reads and clears the decode kernel's device error flag (synchronous).
 unsigned int decode_take_device_error();
 
@@ -57,6 +60,11 @@ bool prefill_tc_supported(const AttnDesc& a);
 size_t prefill_tc_workspace(const AttnDesc& a);
 cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* workspace, cudaStream_t stream);
 unsigned int tc_take_device_error();
+
+// ---- rope -----------------------------------------------------------------------
+// out = rope(x) for x [T, H*D], row t at position offset + t; out may equal x.
+cudaError_t launch_rope(const float* x, float* out, int64_t T, int H, int D, int64_t offset, const RopeDev& r,
+                        cudaStream_t stream);
 
 // ---- cache_write --------------------------------------------------------------
 cudaError_t launch_cache_write(float* cache, int64_t width, const float* values, int64_t rows,

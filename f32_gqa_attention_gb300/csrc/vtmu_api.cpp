@@ -215,6 +215,45 @@ size_t attention_workspace(const Resolved& r) {
                                                     : 0;
 }
 
+// Checks op "rope"'s parameters and resolves them for the kernels: the
+// inverse frequencies base^(-2j / rotary_dim) (or the given ones) in double,
+// with a linear scaling factor divided out.
+vtmu_status resolve_rope(const vtmu_rope_params* r, vtmu::RopeDev* out) {
+    if (!r) return fail(VTMU_ERR_INVALID, "rope params is NULL");
+    if (r->head_dim <= 0 || r->head_dim > 4096)
+        return fail(VTMU_ERR_INVALID, "rope: head_dim %d outside 1..4096", r->head_dim);
+    const int rd = r->rotary_dim ? r->rotary_dim : r->head_dim;
+    if (rd < 0 || rd % 2 != 0 || rd > r->head_dim)
+        return fail(VTMU_ERR_INVALID, "rope.rotaryDim: %d must be even and at most head_dim %d", rd, r->head_dim);
+    if (rd > 2 * vtmu::kRopeMaxPairs)
+        return fail(VTMU_ERR_UNSUPPORTED, "rope.rotaryDim: %d above the %d this build turns", rd,
+                    2 * vtmu::kRopeMaxPairs);
+    const double base = r->base == 0.f ? 10000.0 : (double)r->base;
+    if (!(base > 0.0) || !std::isfinite(base)) return fail(VTMU_ERR_INVALID, "rope: base must be finite and > 0");
+    double divisor = 1.0;
+    if (r->scaling == VTMU_ROPE_SCALING_LINEAR) {
+        divisor = r->scaling_factor;
+        if (!(divisor > 0.0) || !std::isfinite(divisor))
+            return fail(VTMU_ERR_INVALID, "rope.scaling: linear factor must be finite and > 0");
+    } else if (r->scaling != VTMU_ROPE_SCALING_NONE) {
+        return fail(VTMU_ERR_UNSUPPORTED,
+                    "rope.scaling: kind %d is not served (linear, or explicit inv_freq and attention_factor)",
+                    r->scaling);
+    }
+    const float af = r->attention_factor == 0.f ? 1.f : r->attention_factor;
+    if (!std::isfinite(af)) return fail(VTMU_ERR_INVALID, "rope.scaling: attention_factor must be finite");
+    std::memset(out, 0, sizeof(*out));
+    out->half = rd / 2;
+    out->interleaved = r->interleaved ? 1 : 0;
+    out->attn = af;
+    for (int j = 0; j < rd / 2; ++j) {
+        double f = r->inv_freq ? (double)r->inv_freq[j] : std::pow(base, -2.0 * j / rd);
+        if (!std::isfinite(f)) return fail(VTMU_ERR_INVALID, "rope.scaling: inv_freq[%d] is not finite", j);
+        out->inv_freq[j] = f / divisor;
+    }
+    return ok();
+}
+
 // Workspace of vtmu_decode_step_host: the attention workspace, then the
 // staging areas of q, k_new, v_new, bias and out (byte offsets, 256-aligned).
 struct HostStaging {
@@ -274,7 +313,8 @@ namespace {
 // decode step come first (fused into the decode launch when it runs).
 vtmu_status run_attention(Resolved& r, const float* q, const float* k, const float* v, const float* bias,
                           float* out, const vtmu_attention_params* p, void* workspace, size_t workspace_bytes,
-                          cudaStream_t stream, const vtmu::DecodeCacheWrite* cw) {
+                          cudaStream_t stream, const vtmu::DecodeCacheWrite* cw,
+                          const vtmu::RopeDev* rope = nullptr) {
     vtmu::AttnDesc& a = r.a;
     cudaError_t e;
     auto write_caches = [&]() -> cudaError_t {
@@ -324,6 +364,10 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
             r.kernel = VTMU_KERNEL_PREFILL_FFMA;
         }
     }
+    if (rope && r.kernel != VTMU_KERNEL_DECODE)
+        return fail(VTMU_ERR_UNSUPPORTED,
+                    "decode_step_rope: the fused step needs T == 1, a decode-kernel shape and 16-byte aligned "
+                    "q, caches, out; compose vtmu_rope and vtmu_decode_step otherwise");
     if (r.kernel == VTMU_KERNEL_DECODE) {
         const size_t need = decode_workspace(a);
         if (!workspace || workspace_bytes < need)
@@ -333,7 +377,7 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
             return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
         vtmu::DecodePlan plan;
         vtmu::decode_plan(a, p->decode_splits, device_sm_count(), &plan);
-        e = vtmu::launch_decode(a, alibi, plan, workspace, stream, cw);
+        e = vtmu::launch_decode(a, alibi, plan, workspace, stream, cw, rope);
         if (e != cudaSuccess) return cuda_fail(e, "decode launch");
         return ok();
     }
@@ -376,14 +420,19 @@ vtmu_status vtmu_attention(const float* q, const float* k, const float* v, const
     return run_attention(r, q, k, v, bias, out, p, workspace, workspace_bytes, stream, nullptr);
 }
 
-vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new,
-                             const float* v_new, int64_t new_rows, int64_t offset, const float* q,
-                             const float* bias, float* out, const vtmu_attention_params* p, void* workspace,
-                             size_t workspace_bytes, cudaStream_t stream) {
+// vtmu_decode_step, with the rotary embedding fused in when `rope` is set.
+static vtmu_status decode_step_impl(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new,
+                                    const float* v_new, int64_t new_rows, int64_t offset, const float* q,
+                                    const float* bias, float* out, const vtmu_attention_params* p,
+                                    void* workspace, size_t workspace_bytes, cudaStream_t stream,
+                                    const vtmu::RopeDev* rope) {
     Resolved r;
     vtmu_status st = resolve(p, &r);
     if (st != VTMU_OK) return st;
     const vtmu::AttnDesc& a = r.a;
+    if (rope && a.T != 1)
+        return fail(VTMU_ERR_UNSUPPORTED, "decode_step_rope: the fused step takes one query row (T = %lld)",
+                    (long long)a.T);
     if (max_rows < 0 || new_rows < 0)
         return fail(VTMU_ERR_INVALID, "decode_step: negative size (max_rows %lld, new_rows %lld)",
                     (long long)max_rows, (long long)new_rows);
@@ -394,7 +443,7 @@ vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, c
         return fail(VTMU_ERR_INVALID, "decode_step: S %lld exceeds the cache's %lld rows", (long long)a.S,
                     (long long)max_rows);
     if (new_rows == 0) return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes,
-                                            stream, nullptr);
+                                            stream, nullptr, rope);
     if (!k_cache || !v_cache || !k_new || !v_new)
         return fail(VTMU_ERR_INVALID, "decode_step: a cache or new-row pointer is NULL");
     if ((reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache) |
@@ -411,7 +460,55 @@ vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, c
                 overlaps(out, (size_t)a.T * a.H * a.Dv * 4, v_cache, vc_b)))
         return fail(VTMU_ERR_INVALID, "decode_step: out overlaps a cache");
     vtmu::DecodeCacheWrite cw{k_cache, v_cache, k_new, v_new, offset, offset + new_rows};
-    return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes, stream, &cw);
+    return run_attention(r, q, k_cache, v_cache, bias, out, p, workspace, workspace_bytes, stream, &cw, rope);
+}
+
+vtmu_status vtmu_decode_step(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new,
+                             const float* v_new, int64_t new_rows, int64_t offset, const float* q,
+                             const float* bias, float* out, const vtmu_attention_params* p, void* workspace,
+                             size_t workspace_bytes, cudaStream_t stream) {
+    return decode_step_impl(k_cache, v_cache, max_rows, k_new, v_new, new_rows, offset, q, bias, out, p, workspace,
+                            workspace_bytes, stream, nullptr);
+}
+
+void vtmu_rope_params_init(vtmu_rope_params* r) {
+    if (r) std::memset(r, 0, sizeof(*r));
+}
+
+vtmu_status vtmu_rope(const float* x, float* out, int64_t T, int32_t heads, int64_t offset,
+                      const vtmu_rope_params* rp, cudaStream_t stream) {
+    vtmu::RopeDev rd;
+    vtmu_status st = resolve_rope(rp, &rd);
+    if (st != VTMU_OK) return st;
+    if (T < 0 || heads <= 0)
+        return fail(VTMU_ERR_INVALID, "rope: T %lld and heads %d must be >= 0 and > 0", (long long)T, heads);
+    if (offset < 0) return fail(VTMU_ERR_RANGE, "rope: offset %lld is negative", (long long)offset);
+    if (T == 0) return ok();
+    if (!x || !out) return fail(VTMU_ERR_INVALID, "rope: x or out is NULL");
+    if ((reinterpret_cast<uintptr_t>(x) | reinterpret_cast<uintptr_t>(out)) & 3u)
+        return fail(VTMU_ERR_INVALID, "rope: pointers must be 4-byte aligned");
+    const size_t nb = (size_t)T * heads * rp->head_dim * 4;
+    if (x != out && overlaps(x, nb, out, nb))
+        return fail(VTMU_ERR_INVALID, "rope: out overlaps x without being x");
+    cudaError_t e = vtmu::launch_rope(x, out, T, heads, rp->head_dim, offset, rd, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "rope launch");
+    return ok();
+}
+
+vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64_t max_rows, const float* k_new,
+                                  const float* v_new, int64_t new_rows, int64_t offset, const float* q,
+                                  const float* bias, float* out, const vtmu_attention_params* p,
+                                  const vtmu_rope_params* rope, void* workspace, size_t workspace_bytes,
+                                  cudaStream_t stream) {
+    vtmu::RopeDev rd;
+    vtmu_status st = resolve_rope(rope, &rd);
+    if (st != VTMU_OK) return st;
+    if (!p) return fail(VTMU_ERR_INVALID, "params is NULL");
+    if (rope->head_dim != p->head_dim)
+        return fail(VTMU_ERR_INVALID, "decode_step_rope: rope head_dim %d differs from head_dim %d", rope->head_dim,
+                    p->head_dim);
+    return decode_step_impl(k_cache, v_cache, max_rows, k_new, v_new, new_rows, offset, q, bias, out, p, workspace,
+                            workspace_bytes, stream, &rd);
 }
 
 vtmu_status vtmu_decode_step_host_workspace_size(const vtmu_attention_params* p, int64_t new_rows, size_t* bytes) {
@@ -497,7 +594,8 @@ vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width, cons
 }
 
 const char* vtmu_features(void) {
-    return "attention.alibi attention.bias attention.scale attention.softcap attention.window";
+    return "attention.alibi attention.bias attention.scale attention.softcap attention.window rope.interleaved "
+           "rope.rotaryDim";
 }
 
 const char* vtmu_last_error(void) { return g_last_error.c_str(); }

@@ -1,7 +1,7 @@
 /*
  * vtmu_attention.h -- C ABI of the GB300 (sm_103a) f32 attention library.
  *
- * Two ops of the volunteer-inference op catalog (vtmu.mpakt.dev/api/ops):
+ * Three ops of the volunteer-inference op catalog (vtmu.mpakt.dev/api/ops):
  *
  *   attention    op "attention": scaled dot-product attention with
  *                grouped-query heads on flat row-major f32 tensors
@@ -22,6 +22,9 @@
  *                The score matrix never leaves the chip.
  *   cache_write  op "cache_write": cache[offset + r, :] = values[r, :] for
  *                r < rows, in place (the op mutates its first input).
+ *   rope         op "rope": rotary position embedding of [T, heads*headDim]
+ *                (vtmu_rope), also fused into a decode step
+ *                (vtmu_decode_step_rope).
  *
  * Conventions shared by every entry point
  *  - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations)
@@ -265,6 +268,75 @@ VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, const float* 
                                                    const vtmu_attention_params* p,
                                                    cudaStream_t stream);
 
+/* Frequency scaling of op "rope" (param scaling, config.json's rope_scaling).
+ * Linear divides every position by the factor.  Other schemes (llama3, yarn,
+ * longrope, dynamic) are served through explicit inverse frequencies and an
+ * attention factor computed by the caller; requesting them by kind is
+ * refused with "rope.scaling" named. */
+typedef enum vtmu_rope_scaling {
+    VTMU_ROPE_SCALING_NONE = 0,
+    VTMU_ROPE_SCALING_LINEAR = 1
+} vtmu_rope_scaling;
+
+/*
+ * Parameters of op "rope" (vtmu.mpakt.dev/api/ops): rotary position
+ * embedding over x [T, heads*headDim].  Row t sits at position offset + t
+ * (divided by scaling_factor with linear scaling).  Pair j < rotary_dim/2
+ * of every head turns by theta = position * inv_freq[j]: channels
+ * (j, j + rotary_dim/2) (Llama, Qwen, Mistral, NeoX) or, interleaved,
+ * (2j, 2j + 1) (GPT-J), as (a, b) -> (a cos - b sin, b cos + a sin), with
+ * cos and sin multiplied by attention_factor; channels at or past rotary_dim
+ * pass through.  inv_freq[j] = base^(-2j / rotary_dim) unless given.
+ * Fill with vtmu_rope_params_init(), then set fields.
+ */
+typedef struct vtmu_rope_params {
+    int32_t head_dim;        /* per-head width, 1..4096 */
+    int32_t rotary_dim;      /* 0 means head_dim; even, <= head_dim, <= 256 */
+    int32_t interleaved;     /* 0: half-split pairs; 1: (2j, 2j + 1) */
+    int32_t scaling;         /* vtmu_rope_scaling */
+    float base;              /* rope_theta; 0 means 10000; > 0 */
+    float scaling_factor;    /* VTMU_ROPE_SCALING_LINEAR: > 0 */
+    float attention_factor;  /* 0 means 1; multiplies cos and sin */
+    const float* inv_freq;   /* HOST [rotary_dim/2] explicit inverse frequencies, or NULL */
+} vtmu_rope_params;
+
+/* Writes the op's defaults: base 10000, rotary_dim = head_dim, half-split
+ * pairs, no scaling, attention factor 1 (head_dim is left 0: set it). */
+VTMU_API void vtmu_rope_params_init(vtmu_rope_params* r);
+
+/*
+ * op "rope": out = rope(x) for x, out [T, heads*head_dim], DEVICE, row-major
+ * f32, 4-byte aligned; out == x turns x in place, otherwise they must not
+ * overlap.  offset (param offset, >= 0): position of row 0.
+ * Errors: VTMU_ERR_INVALID (NULL pointer with T > 0, T < 0, heads <= 0,
+ * head_dim outside 1..4096, rotary_dim odd or above head_dim, base, factor
+ * or attention factor not finite / not positive where required, inv_freq
+ * not finite, partial overlap of x and out), VTMU_ERR_UNSUPPORTED
+ * (rotary_dim above 256, a scaling kind other than none / linear:
+ * "rope.scaling"), VTMU_ERR_RANGE (offset < 0), VTMU_ERR_CUDA.
+ */
+VTMU_API vtmu_status vtmu_rope(const float* x, float* out, int64_t T, int32_t heads, int64_t offset,
+                               const vtmu_rope_params* r, cudaStream_t stream);
+
+/*
+ * A decode step with the rotary embedding fused in: what op "rope" on q
+ * (position p->pos_offset) and on k_new (row i at position offset + i),
+ * then vtmu_decode_step with the turned q and k_new compute -- the caches
+ * receive turned keys, q is left as given -- in ONE launch of the decode
+ * kernel (vtmu.mpakt.dev/api/ops: a whole decode step is meant to stay on
+ * the worker).  Arguments as for vtmu_decode_step, plus `rope` with
+ * rope->head_dim == p->head_dim.  Only the fused form is offered: the call
+ * needs T == 1 and a shape the decode kernel covers (same table and 16-byte
+ * alignment as VTMU_KERNEL_DECODE); anything else is refused with
+ * VTMU_ERR_UNSUPPORTED -- compose vtmu_rope and vtmu_decode_step there.
+ * Errors: those of vtmu_decode_step and vtmu_rope, VTMU_ERR_UNSUPPORTED.
+ */
+VTMU_API vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64_t max_rows,
+                                           const float* k_new, const float* v_new, int64_t new_rows,
+                                           int64_t offset, const float* q, const float* bias, float* out,
+                                           const vtmu_attention_params* p, const vtmu_rope_params* rope,
+                                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
 /*
  * Kernel-side failures.  Every wait inside a kernel (TMA stage arrival,
  * stage release) gives up after one second instead of hanging the GPU; the
@@ -280,7 +352,9 @@ VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, const float* 
 VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
 
 /* Space-separated optional features this build implements, named as the op
- * catalog's feature table names them. */
+ * catalog's feature table names them.  rope.scaling is not listed: of the
+ * schemes it covers only linear scaling, explicit inverse frequencies and
+ * the attention factor are served. */
 VTMU_API const char* vtmu_features(void);
 
 /* Message of the last failed call on this host thread ("" after success). */

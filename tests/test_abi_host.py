@@ -64,7 +64,7 @@ def test_exports_nothing_else(lib):
 def test_features_name_the_catalog_features(lib):
     assert set(vtmu.vtmu_features().split()) == {
         "attention.alibi", "attention.bias", "attention.scale", "attention.softcap",
-        "attention.window"}
+        "attention.window", "rope.interleaved", "rope.rotaryDim"}
 
 
 def test_params_init_writes_defaults(lib):
@@ -232,3 +232,40 @@ def test_host_decode_step_checks_before_any_copy(lib):
     with pytest.raises(ValueError):
         vtmu.vtmu_decode_step_host(FAKE * 3, FAKE * 5, 4096, kn, kn, 1, 4095, q.astype(np.float64), None, out, p,
                                    FAKE * 7, need, 0)
+
+
+@host_only
+def test_rope_refusals(lib):
+    ok = dict(headDim=64)
+    call = lambda T=4, heads=2, off=0, x=FAKE, out=FAKE * 2, **kw: _err(
+        lambda: vtmu.vtmu_rope(x, out, T, heads, off, vtmu.make_rope_params(**dict(ok, **kw)), 0))
+    assert "rope.rotaryDim" in str(call(rotaryDim=33))
+    assert "rope.rotaryDim" in str(call(rotaryDim=66))
+    assert call(headDim=4096 + 2).status == vtmu.VTMU_ERR_INVALID
+    assert call(headDim=512, rotaryDim=512).status == vtmu.VTMU_ERR_UNSUPPORTED
+    e = call(scaling={"rope_type": "yarn", "factor": 4.0})
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "rope.scaling" in str(e)
+    assert "rope.scaling" in str(call(scaling={"rope_type": "linear", "factor": 0.0}))
+    assert call(base=-1.0).status == vtmu.VTMU_ERR_INVALID
+    assert call(invFreq=[float("nan")] * 32).status == vtmu.VTMU_ERR_INVALID
+    assert call(off=-1).status == vtmu.VTMU_ERR_RANGE
+    assert call(x=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(heads=0).status == vtmu.VTMU_ERR_INVALID
+    assert "overlaps" in str(call(out=FAKE + 4))
+    vtmu.vtmu_rope(None, None, 0, 2, 0, vtmu.make_rope_params(headDim=64), 0)  # T == 0: nothing to do
+
+
+@host_only
+def test_decode_step_rope_refusals(lib):
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
+    need = vtmu.vtmu_attention_workspace_size(p)
+    r = vtmu.make_rope_params(headDim=128)
+    call = lambda p=p, r=r: _err(lambda: vtmu.vtmu_decode_step_rope(
+        FAKE * 3, FAKE * 5, 4096, FAKE * 7, FAKE * 9, 1, 4095, FAKE, None, FAKE * 2, p, r, FAKE * 11, need, 0))
+    assert "head_dim" in str(call(r=vtmu.make_rope_params(headDim=64)))
+    e = call(p=vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095,
+                                kernel=vtmu.VTMU_KERNEL_PREFILL_FFMA))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "compose" in str(e)
+    e = call(p=vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED
+    assert call(r=vtmu.make_rope_params(headDim=128, rotaryDim=130)).status == vtmu.VTMU_ERR_INVALID
