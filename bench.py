@@ -193,9 +193,13 @@ def barrier(world):
 def oracle_decode_step(x, w):
     import oracle
     H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
-    oracle.cache_write(x["kc"], x["k_new"], off)
+    q, kn = x["q"], x["k_new"]
+    if w.get("rope"):  # op rope on q (at posOffset) and on the new key row (at its cache row)
+        q = oracle.rope(q, headDim=D, offset=w["params"]["posOffset"], **w["rope"]).astype(np.float32)
+        kn = oracle.rope(kn, headDim=D, offset=off, **w["rope"]).astype(np.float32)
+    oracle.cache_write(x["kc"], kn, off)
     oracle.cache_write(x["vc"], x["v_new"], off)
-    return oracle.attention(x["q"], x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
+    return oracle.attention(q, x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
 
 
 class OracleSampler:
@@ -277,6 +281,7 @@ def run_vtmu(args, rank, world, local):
     st = stream.cuda_stream
     launches_per_step = 0
     x = si.workload_inputs(name)
+    rope = None
 
     if w["kind"] == "decode":
         H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
@@ -294,21 +299,35 @@ def run_vtmu(args, rank, world, local):
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         width = Hk * D
         launches_per_step = 1
+        rope = vtmu.make_rope_params(headDim=D, **w["rope"]) if w.get("rope") else None
+        if rope is not None:
+            with torch.cuda.stream(stream):
+                q_rot, kn_rot = torch.empty_like(q), torch.empty_like(kn)
 
         def step(i, ev=None):
-            # One fused launch: both cache_writes and the attention.
+            # One fused launch: both cache_writes and the attention (and the
+            # rotary embedding of q and the new key row).
             s = sessions[i % 2]
             if ev is not None:
                 ev[0].record(stream)
-            vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
+            if rope is None:
+                vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
+            else:
+                vtmu.vtmu_decode_step_rope(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, rope, ws,
+                                           ws_bytes, st)
             if ev is not None:
                 ev[1].record(stream)
 
         def unfused_step(i):
             s = sessions[i % 2]
-            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kn, 1, off, st)
+            qq, kk = q, kn
+            if rope is not None:
+                vtmu.vtmu_rope(q, q_rot, 1, H, w["params"]["posOffset"], rope, st)
+                vtmu.vtmu_rope(kn, kn_rot, 1, Hk, off, rope, st)
+                qq, kk = q_rot, kn_rot
+            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kk, 1, off, st)
             vtmu.vtmu_cache_write(s["Vc"], off + 1, width, vn, 1, off, st)
-            vtmu.vtmu_attention(q, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+            vtmu.vtmu_attention(qq, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
 
         work_per_step, unit = step_bytes / 1e9, "GB/s"
         kernel_tag, kernel_work, kernel_unit = "decode", step_bytes, "GB/s"
@@ -414,7 +433,27 @@ def run_vtmu(args, rank, world, local):
 
     # ---- end to end through the public API with host buffers ----------------
     e2e = None
-    if w["kind"] == "decode":
+    if rope is not None:
+        # The rotary decode step has no host-buffer entry point: pinned copies
+        # in, the fused step, the output back, a host sync.
+        qh = torch.from_numpy(x["q"]).pin_memory()
+        knh = torch.from_numpy(x["k_new"]).pin_memory()
+        vnh = torch.from_numpy(x["v_new"]).pin_memory()
+        outh = torch.empty((1, H * D), dtype=torch.float32).pin_memory()
+
+        def e2e_step(i):
+            with torch.cuda.stream(stream):
+                q.copy_(qh, non_blocking=True)
+                kn.copy_(knh, non_blocking=True)
+                vn.copy_(vnh, non_blocking=True)
+            step(i)
+            with torch.cuda.stream(stream):
+                outh.copy_(out, non_blocking=True)
+            stream.synchronize()
+
+        h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
+        d2h = outh.numel() * 4
+    elif w["kind"] == "decode":
         qh = torch.from_numpy(x["q"]).pin_memory()
         knh = torch.from_numpy(x["k_new"]).pin_memory()
         vnh = torch.from_numpy(x["v_new"]).pin_memory()

@@ -116,6 +116,10 @@ WORKLOADS = {
     "gqa_decode": dict(
         kind="decode", max_rows=32768, offset=32767, heads=32, kvHeads=8,
         headDim=128, seed=1, params=dict(causal=True, posOffset=32767)),
+    "gqa_decode_rope": dict(
+        kind="decode", max_rows=32768, offset=32767, heads=32, kvHeads=8,
+        headDim=128, seed=1, params=dict(causal=True, posOffset=32767),
+        rope=dict(base=500000.0)),
     "gqa_prefill": dict(
         kind="prefill", T=4096, S=4096, heads=32, kvHeads=8, headDim=128,
         seed=2, params=dict(causal=True, posOffset=0)),
