@@ -52,12 +52,13 @@ FP32_LANES_PER_SM = 128
 # ------------------------------------------------------------------ work model
 def decode_bytes(w):
     """Algorithmic bytes of one decode step: every visible K and V row once,
-    q and out once, and the two one-row cache writes (read + write)."""
-    H, Hk, D = w["heads"], w["kvHeads"], w["headDim"]
-    S = w["offset"] + 1
+    the query and output rows once, and the two cache writes of the new rows
+    (read + write)."""
+    H, Hk, D, R = w["heads"], w["kvHeads"], w["headDim"], w.get("rows", 1)
+    S = w["offset"] + R
     kv = 2 * S * Hk * D * 4
-    qo = 2 * H * D * 4
-    cw = 2 * 2 * Hk * D * 4
+    qo = 2 * R * H * D * 4
+    cw = 2 * 2 * R * Hk * D * 4
     return kv, kv + qo + cw
 
 
@@ -285,6 +286,7 @@ def run_vtmu(args, rank, world, local):
 
     if w["kind"] == "decode":
         H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
+        R = w.get("rows", 1)  # query rows = new cache rows of the step
         kv_bytes, step_bytes = decode_bytes(w)
         sessions = []
         with torch.cuda.stream(stream):
@@ -293,8 +295,11 @@ def run_vtmu(args, rank, world, local):
             q = torch.from_numpy(x["q"]).to(dev)
             kn = torch.from_numpy(x["k_new"]).to(dev)
             vn = torch.from_numpy(x["v_new"]).to(dev)
-            out = torch.empty((1, H * D), dtype=torch.float32, device=dev)
-        p = vtmu.make_params(1, off + 1, heads=H, headDim=D, kvHeads=Hk, **w["params"])
+            out = torch.empty((R, H * D), dtype=torch.float32, device=dev)
+        # --kernel ffma: the same step through the FFMA prefill (cache_writes
+        # and attention as three launches), for comparison.
+        forced = vtmu.VTMU_KERNEL_PREFILL_FFMA if args.kernel == "ffma" else vtmu.VTMU_KERNEL_AUTO
+        p = vtmu.make_params(R, off + R, heads=H, headDim=D, kvHeads=Hk, kernel=forced, **w["params"])
         ws_bytes = vtmu.vtmu_attention_workspace_size(p)
         ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
         width = Hk * D
@@ -311,9 +316,9 @@ def run_vtmu(args, rank, world, local):
             if ev is not None:
                 ev[0].record(stream)
             if rope is None:
-                vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, ws, ws_bytes, st)
+                vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, ws, ws_bytes, st)
             else:
-                vtmu.vtmu_decode_step_rope(s["Kc"], s["Vc"], off + 1, kn, vn, 1, off, q, None, out, p, rope, ws,
+                vtmu.vtmu_decode_step_rope(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, rope, ws,
                                            ws_bytes, st)
             if ev is not None:
                 ev[1].record(stream)
@@ -325,12 +330,14 @@ def run_vtmu(args, rank, world, local):
                 vtmu.vtmu_rope(q, q_rot, 1, H, w["params"]["posOffset"], rope, st)
                 vtmu.vtmu_rope(kn, kn_rot, 1, Hk, off, rope, st)
                 qq, kk = q_rot, kn_rot
-            vtmu.vtmu_cache_write(s["Kc"], off + 1, width, kk, 1, off, st)
-            vtmu.vtmu_cache_write(s["Vc"], off + 1, width, vn, 1, off, st)
+            vtmu.vtmu_cache_write(s["Kc"], off + R, width, kk, R, off, st)
+            vtmu.vtmu_cache_write(s["Vc"], off + R, width, vn, R, off, st)
             vtmu.vtmu_attention(qq, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
 
         work_per_step, unit = step_bytes / 1e9, "GB/s"
         kernel_tag, kernel_work, kernel_unit = "decode", step_bytes, "GB/s"
+        if args.kernel == "ffma":
+            kernel_tag, launches_per_step = "prefill_ffma", 3
         bound, peak = "hbm", float(peaks["hbm_gbs"])
         peak_note = peak_kind
         flush = None
@@ -439,7 +446,7 @@ def run_vtmu(args, rank, world, local):
         qh = torch.from_numpy(x["q"]).pin_memory()
         knh = torch.from_numpy(x["k_new"]).pin_memory()
         vnh = torch.from_numpy(x["v_new"]).pin_memory()
-        outh = torch.empty((1, H * D), dtype=torch.float32).pin_memory()
+        outh = torch.empty((R, H * D), dtype=torch.float32).pin_memory()
 
         def e2e_step(i):
             with torch.cuda.stream(stream):
@@ -457,16 +464,16 @@ def run_vtmu(args, rank, world, local):
         qh = torch.from_numpy(x["q"]).pin_memory()
         knh = torch.from_numpy(x["k_new"]).pin_memory()
         vnh = torch.from_numpy(x["v_new"]).pin_memory()
-        outh = torch.empty((1, H * D), dtype=torch.float32).pin_memory()
+        outh = torch.empty((R, H * D), dtype=torch.float32).pin_memory()
 
         # The host-buffer decode step of the C ABI: it copies q and the new
         # rows in, runs the fused step, copies the output row back and waits.
-        hws_bytes = vtmu.vtmu_decode_step_host_workspace_size(p, 1)
+        hws_bytes = vtmu.vtmu_decode_step_host_workspace_size(p, R)
         hws = torch.zeros(hws_bytes, dtype=torch.uint8, device=dev)
 
         def e2e_step(i):
             s = sessions[i % 2]
-            vtmu.vtmu_decode_step_host(s["Kc"], s["Vc"], off + 1, knh, vnh, 1, off, qh, None, outh, p, hws,
+            vtmu.vtmu_decode_step_host(s["Kc"], s["Vc"], off + R, knh, vnh, R, off, qh, None, outh, p, hws,
                                        hws_bytes, st)
 
         h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4

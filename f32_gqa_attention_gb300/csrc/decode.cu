@@ -1,13 +1,18 @@
-// decode.cu -- split-KV flash-decode kernel for one query row (T == 1).
+// decode.cu -- split-KV flash-decode kernel for a few query rows (1 <= T <= 16).
 //
-// Op "attention" (vtmu.mpakt.dev/api/ops) with a KV cache: the single query
-// row sits at position posOffset and the visible keys form one contiguous
+// Op "attention" (vtmu.mpakt.dev/api/ops) with a KV cache: query row t sits
+// at position posOffset + t and the keys any row sees form one contiguous
 // range [s_lo, s_end) of cache rows.  The work is HBM-bound: every K and V
-// byte of that range is read once.  Layout of the work:
+// byte of that range is read once per row group.  Layout of the work:
 //
-//  * grid (kvHeads, splits): one CTA streams a chunk of the range for one KV
-//    head and serves all G = heads/kvHeads query heads of its group, so each
-//    K/V byte is read once per group, not once per query head;
+//  * the kernel's G "heads" are virtual heads: the group's query heads times
+//    the query rows of a row group (tc rows, G = group size x tc <= 8, padded
+//    to 2), so one K/V tile serves every query row and head of its group;
+//    each row masks the keys of the range it cannot see.  T = 1 is the
+//    common decode step; 1 < T is a speculative or chunked step;
+//  * grid (kvHeads, splits, row groups): one CTA streams a chunk of the range
+//    for one KV head and serves all virtual heads of its group, so each K/V
+//    byte is read once per row group, not once per query head;
 //  * a producer warp moves NR-row K and V tiles global -> shared with 2-D TMA
 //    (cp.async.bulk.tensor) into a ring of stages guarded by full/empty
 //    mbarriers; the consumer warps never issue a load;
@@ -23,7 +28,7 @@
 //    through 128 bytes of shared memory to the P.V step, where lane l owns
 //    value dims as it owns query dims;
 //  * warps merge in shared memory, each CTA writes its (m, l, o) partials,
-//    and the last CTA of a KV head (arrival counter, no waiting) merges the
+//    and the last CTA of a (KV head, row group) (arrival counter, no waiting) merges the
 //    splits with the log-sum-exp rule  m* = max m_i, l* = sum l_i 2^(m_i-m*),
 //    o* = sum o_i 2^(m_i-m*) / l*  and writes the output row.
 //
@@ -79,7 +84,28 @@ struct DecodeArgs {
     unsigned int* counters;  // [kvHeads], zero between calls
     DecodeCacheWrite cw;     // fused cache_write (cw.k_new == nullptr: none)
     RopeDev rope;            // rotary embedding of q and the new keys (rope.half == 0: none)
+    // Query rows: the kernel's G "heads" are virtual heads vh = t_local * gr + g
+    // (row t_local of this CTA's row group, query head kh * gr + g), tc query
+    // rows per row group, one row group per blockIdx.z.
+    int32_t gr;              // heads per KV head (group size)
+    int32_t tc;              // query rows per row group
 };
+
+// Query row and head of virtual head vh of KV head kh in this CTA's row group;
+// `ok` is false for padding (past T, or past the row group).
+struct VHead {
+    int64_t t;
+    int h;
+    bool ok;
+};
+__device__ __forceinline__ VHead vhead(const DecodeArgs& args, int kh, int vh) {
+    const int tl = vh / args.gr;
+    VHead r;
+    r.t = (int64_t)blockIdx.z * args.tc + tl;
+    r.h = kh * args.gr + vh % args.gr;
+    r.ok = tl < args.tc && r.t < args.a.T;
+    return r;
+}
 
 // Element d of new key row `pos` (k_new row base `src`), turned by the rotary
 // embedding when it is on: the cache stores turned keys.
@@ -169,7 +195,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     const int kh = VTMU_DEC_KH_FAST ? blockIdx.x : blockIdx.y;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t p = a.pos_offset;  // position of the single query row
+    const int64_t p = a.pos_offset;  // position of query row 0 (row t sits at p + t)
 
     const int64_t c_begin = args.s_lo + (int64_t)split * args.rows_per_split;
     int64_t c_end = c_begin + args.rows_per_split;
@@ -188,7 +214,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     // head (its own columns).  Rows inside the visible range are written by
     // the consumer warp that owns them, below.
     const int64_t ld = (int64_t)a.Hk * D;
-    if (args.cw.k_new && split == 0 && warp == 0) {
+    if (args.cw.k_new && split == 0 && blockIdx.z == 0 && warp == 0) {
         for (int64_t r = args.cw.lo; r < args.cw.hi; ++r) {
             if (r >= args.s_lo && r < args.s_end) continue;
             const int64_t src = (r - args.cw.lo) * ld + (int64_t)kh * D, dst = r * ld + (int64_t)kh * D;
@@ -241,12 +267,13 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
         float qv[G][PL];
 #pragma unroll
         for (int gi = 0; gi < G; ++gi) {
-            const float* qh = a.q + (int64_t)(kh * G + (gi ^ (lane % G))) * D;
+            const VHead vq = vhead(args, kh, gi ^ (lane % G));
+            const float* qh = a.q + (vq.t * a.H + vq.h) * D;  // read only when vq.ok
 #pragma unroll
             for (int j = 0; j < PL; ++j) {
                 const int d = lane_dim<VEC>(lane, j);
-                float x = __ldg(qh + d);
-                if (d < 2 * args.rope.half) {
+                float x = vq.ok ? __ldg(qh + d) : 0.f;
+                if (vq.ok && d < 2 * args.rope.half) {
                     int pj, partner;
                     bool first;
                     rope_pair_of(args.rope, d, pj, partner, first);
@@ -255,14 +282,18 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
                 qv[gi][j] = x;
             }
         }
-        const int rr = lane / G;  // logical slot after the butterfly: row rr, head gg
+        const int rr = lane / G;  // logical slot after the butterfly: row rr, virtual head gg
         const int gg = lane % G;
-        const int h_lane = kh * G + gg;
-        const float slope_lane = a.alibi_on ? alibi.slope_log2[h_lane] : 0.f;
-        const float* bias_row = a.bias_kind == 0   ? nullptr
-                                : a.bias_kind == 1 ? a.bias + c_begin
-                                                   : a.bias + (int64_t)h_lane * a.S + c_begin;
-        const int64_t rel0 = c_begin - p;
+        const VHead vl = vhead(args, kh, gg);
+        const float slope_lane = a.alibi_on ? alibi.slope_log2[vl.h] : 0.f;
+        const float* bias_row = (a.bias_kind == 0 || !vl.ok) ? nullptr
+                                : a.bias_kind == 1          ? a.bias + vl.t * a.S + c_begin
+                                                            : a.bias + ((int64_t)vl.h * a.T + vl.t) * a.S + c_begin;
+        const int64_t p_lane = p + vl.t;  // position of this lane's query row
+        const int64_t rel0 = c_begin - p_lane;
+        // With several query rows the key range is their union: each row
+        // masks the keys it cannot see.
+        const bool multi = a.T > 1;
         const int rowx = lane / G;  // slot ri reads warp row ri ^ rowx
 
         for (int st = 0; st < n_stages; ++st) {
@@ -291,8 +322,10 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
                             const float vx = __ldg(args.cw.v_new + src + d);
                             skr[d] = kx;
                             svr[d] = vx;
-                            args.cw.kc[dst + d] = kx;
-                            args.cw.vc[dst + d] = vx;
+                            if (blockIdx.z == 0) {  // one row group writes the cache
+                                args.cw.kc[dst + d] = kx;
+                                args.cw.vc[dst + d] = vx;
+                            }
                         }
                     }
                     // Order these generic-proxy writes before the TMA that
@@ -332,7 +365,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
             // Fused epilogue for (row rr, head gg).
             const int row_l = st * NR + warp * R + rr;
             float x = -INFINITY;
-            if (row_l < n_rows) {
+            if (row_l < n_rows && vl.ok && (!multi || key_visible(a, p_lane, c_begin + row_l))) {
                 const float bv = bias_row ? __ldg(bias_row + row_l) : 0.f;
                 x = score_log2(a, part[0], slope_lane, rel0 + row_l, bv);
             }
@@ -396,6 +429,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     __syncthreads();
 
     const int Hs = args.splits;
+    const int64_t vbase = ((int64_t)blockIdx.z * a.Hk + kh) * G;  // this CTA's virtual heads in the partials
     for (int idx = threadIdx.x; idx < G * D; idx += C::THREADS) {
         const int g = idx / D, e = idx % D;
         float M = -INFINITY;
@@ -407,7 +441,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
             acc = fmaf(wo[(w * G + g) * D + e], sc, acc);
             L = fmaf(wl[w * G + g], sc, L);
         }
-        const int h = kh * G + g;
+        const int64_t h = vbase + g;
         args.part_o[((int64_t)h * Hs + split) * D + e] = acc;
         if (e == 0) {
             args.part_m[(int64_t)h * Hs + split] = M;
@@ -421,7 +455,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     __syncthreads();
     if (threadIdx.x == 0) {
         __threadfence();
-        const unsigned ticket = atomicAdd(&args.counters[kh], 1u);
+        const unsigned ticket = atomicAdd(&args.counters[blockIdx.z * a.Hk + kh], 1u);
         const bool last = (ticket == (unsigned)(Hs - 1));
         if (last) __threadfence();  // acquire: the other splits' partials
         s_is_last = last;
@@ -430,8 +464,8 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     if (!s_is_last) return;
 
     // Thread t owns outputs t + k*THREADS (k < NOUT).  It issues the loads of
-    // its first CH split partials before warp g (g < G) turns head g's split
-    // maxima into weights, so both L2 round trips overlap.
+    // its first CH split partials before the warps turn the virtual heads'
+    // split maxima into weights, so both L2 round trips overlap.
     constexpr int NOUT = (G * D + C::THREADS - 1) / C::THREADS;
     constexpr int CH = 64 / NOUT > 32 ? 32 : (64 / NOUT < 8 ? 8 : 64 / NOUT);
     float ov[NOUT][CH];
@@ -439,7 +473,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 #pragma unroll
         for (int k = 0; k < NOUT; ++k) {
             const int idx = threadIdx.x + k * C::THREADS;
-            const int64_t base = idx < G * D ? ((int64_t)(kh * G + idx / D) * Hs) * D + idx % D : 0;
+            const int64_t base = idx < G * D ? ((vbase + idx / D) * Hs) * D + idx % D : 0;
 #pragma unroll
             for (int c = 0; c < CH; ++c) {
                 const int i = i0 + c;
@@ -451,8 +485,9 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 
     float* sw = smem;                   // [G][kMaxSplits] split weights
     float* sinv = sw + G * kMaxSplits;  // [G] 1 / l*
-    if (warp < G) {
-        const int h = kh * G + warp;
+    // Warp w serves virtual heads w, w + warps, ... (one each when G <= warps).
+    for (int gw = warp; gw < G; gw += C::THREADS / 32) {
+        const int64_t h = vbase + gw;
         constexpr int PER = kMaxSplits / 32;
         float mv[PER], lv[PER];
 #pragma unroll
@@ -471,12 +506,12 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 #pragma unroll
         for (int t = 0; t < PER; ++t) {
             const float w = fast_exp2(mv[t] - mu);
-            if (lane + 32 * t < Hs) sw[warp * kMaxSplits + lane + 32 * t] = w;
+            if (lane + 32 * t < Hs) sw[gw * kMaxSplits + lane + 32 * t] = w;
             L = fmaf(lv[t], w, L);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
-        if (lane == 0) sinv[warp] = (L > 0.f) ? 1.f / L : 0.f;
+        if (lane == 0) sinv[gw] = (L > 0.f) ? 1.f / L : 0.f;
     }
     __syncthreads();
 
@@ -499,9 +534,12 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 #pragma unroll
     for (int k = 0; k < NOUT; ++k) {
         const int idx = threadIdx.x + k * C::THREADS;
-        if (idx < G * D) a.out[(int64_t)(kh * G + idx / D) * D + idx % D] = acc[k] * sinv[idx / D];
+        if (idx < G * D) {
+            const VHead vo = vhead(args, kh, idx / D);
+            if (vo.ok) a.out[(vo.t * a.H + vo.h) * D + idx % D] = acc[k] * sinv[idx / D];
+        }
     }
-    if (threadIdx.x == 0) args.counters[kh] = 0u;  // ready for the next call
+    if (threadIdx.x == 0) args.counters[blockIdx.z * a.Hk + kh] = 0u;  // ready for the next call
 }
 
 // ---- host side ---------------------------------------------------------------
@@ -533,7 +571,7 @@ bool encode_rows(CUtensorMap* map, const float* base, int64_t rows, int64_t cols
 }
 
 template <int D, int G>
-cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, cudaStream_t stream) {
+cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, int n_rg, cudaStream_t stream) {
     using C = DecCfg<D, G>;
     const AttnDesc& a = args.a;
     CUtensorMap tmk, tmv;
@@ -547,7 +585,7 @@ cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, cudaStre
     auto kern = decode_splitkv_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
-    dim3 grid = VTMU_DEC_KH_FAST ? dim3(a.Hk, args.splits) : dim3(args.splits, a.Hk);
+    dim3 grid = VTMU_DEC_KH_FAST ? dim3(a.Hk, args.splits, n_rg) : dim3(args.splits, a.Hk, n_rg);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(args, alibi, tmk, tmv);
     return cudaGetLastError();
 }
@@ -556,36 +594,62 @@ int stage_rows() { return VTMU_DEC_NR; }
 
 }  // namespace
 
+// Rows per row group: as many of the T query rows as fit 8 virtual heads
+// (group size x rows), a power of two; padded to 2 virtual heads at least.
+// (16 virtual heads, R = 2 rows per warp step, measured slower than two row
+// groups of 8 that read the keys twice: the butterfly reduction then serves
+// 2 rows instead of 4 to 16.)
+void decode_rows(const AttnDesc& a, int* gv, int* tc, int* n_rg) {
+    int t2 = 1;
+    while (t2 < a.T) t2 *= 2;
+    int c = 8 / a.G;
+    if (c > t2) c = t2;
+    if (c < 1) c = 1;
+    *tc = c;
+    *gv = a.G * c < 2 ? 2 : a.G * c;
+    *n_rg = (int)((a.T + c - 1) / c);
+}
+
 bool decode_supported(const AttnDesc& a) {
-    if (a.T != 1 || a.D != a.Dv) return false;
+    if (a.T < 1 || a.T > kDecodeMaxRows || a.D != a.Dv) return false;
     if (!(a.D == 32 || a.D == 64 || a.D == 128)) return false;
-    if (!(a.G == 2 || a.G == 4 || a.G == 8)) return false;
+    if (!(a.G == 1 || a.G == 2 || a.G == 4 || a.G == 8)) return false;
     if (a.S >= ((int64_t)1 << 31)) return false;
-    if (a.Hk > kMaxDecodeKvHeads) return false;
+    int gv, tc, n_rg;
+    decode_rows(a, &gv, &tc, &n_rg);
+    if ((int64_t)a.Hk * n_rg > kMaxDecodeKvHeads) return false;
     return true;
 }
 
 void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan) {
-    // Visible keys of the single row form one range (causal: s <= p; causal
-    // window: s > p - w; non-causal window: |p - s| <= w).
-    const int64_t p = a.pos_offset;
+    // The keys any query row sees form one range (causal: s <= p; causal
+    // window: s > p - w; non-causal window: |p - s| <= w), for rows at
+    // positions p0 .. p1; each row masks the rest of it in the kernel.
+    const int64_t p0 = a.pos_offset, p1 = a.pos_offset + (a.T > 0 ? a.T - 1 : 0);
     int64_t lo = 0, hi = a.S;  // [lo, hi)
     if (a.causal) {
-        hi = p + 1 < hi ? p + 1 : hi;
-        if (a.window > 0) lo = p - a.window + 1;
+        hi = p1 + 1 < hi ? p1 + 1 : hi;
+        if (a.window > 0) lo = p0 - a.window + 1;
     } else if (a.window > 0) {
-        lo = p - a.window;
-        hi = p + a.window + 1 < hi ? p + a.window + 1 : hi;
+        lo = p0 - a.window;
+        hi = p1 + a.window + 1 < hi ? p1 + a.window + 1 : hi;
     }
+    int gv, tc, n_rg;
+    decode_rows(a, &gv, &tc, &n_rg);
+    plan->gv = gv;
+    plan->tc = tc;
+    plan->n_rg = n_rg;
     if (lo < 0) lo = 0;
     if (hi < lo) hi = lo;
     const int64_t rows = hi - lo;
     const int nr = stage_rows();
     int splits = forced_splits;
     if (splits <= 0) {
-        // Fill the SMs once: split each KV head's range into
-        // ~num_sms * ctas_per_sm / Hk chunks.
-        splits = (num_sms * VTMU_DEC_CTAS_PER_SM + a.Hk - 1) / a.Hk;
+        // Fill the SMs once, in one wave: split each (KV head, row group)'s
+        // range into floor(num_sms * ctas_per_sm / (Hk * n_rg)) chunks (rounding
+        // up would start a few CTAs in a second wave and double the time).
+        const int units = a.Hk * n_rg;
+        splits = (num_sms * VTMU_DEC_CTAS_PER_SM) / units;
         if (splits < 1) splits = 1;
     }
     if (splits > kMaxSplits) splits = kMaxSplits;
@@ -598,7 +662,7 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
     plan->s_end = hi;
     plan->rows_per_split = per;
     plan->splits = (int32_t)n;
-    const size_t H = (size_t)a.H, Sp = (size_t)n;
+    const size_t H = (size_t)n_rg * a.Hk * gv, Sp = (size_t)n;  // virtual heads
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
     // Arrival counters in the workspace header (fixed place, so they stay
     // zero between calls of any shape), then m, l and o partials.
@@ -617,8 +681,10 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
     args.s_end = plan.s_end;
     args.rows_per_split = plan.rows_per_split;
     args.splits = plan.splits;
+    args.gr = a.G;
+    args.tc = plan.tc;
     auto up = [](size_t b) { return (b + 255) / 256 * 256; };
-    const size_t H = (size_t)a.H, Sp = (size_t)plan.splits;
+    const size_t H = (size_t)plan.n_rg * a.Hk * plan.gv, Sp = (size_t)plan.splits;
     char* w = static_cast<char*>(workspace);
     args.counters = reinterpret_cast<unsigned int*>(w);
     w += kWorkspaceHeader;
@@ -626,7 +692,7 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
     args.part_l = reinterpret_cast<float*>(w + up(H * Sp * 4));
     args.part_o = reinterpret_cast<float*>(w + 2 * up(H * Sp * 4));
 #define VTMU_DEC(D_, G_) \
-    if (a.D == D_ && a.G == G_) return launch_cfg<D_, G_>(args, alibi, stream);
+    if (a.D == D_ && plan.gv == G_) return launch_cfg<D_, G_>(args, alibi, plan.n_rg, stream);
     VTMU_DEC(32, 2) VTMU_DEC(32, 4) VTMU_DEC(32, 8)
     VTMU_DEC(64, 2) VTMU_DEC(64, 4) VTMU_DEC(64, 8)
     VTMU_DEC(128, 2) VTMU_DEC(128, 4) VTMU_DEC(128, 8)

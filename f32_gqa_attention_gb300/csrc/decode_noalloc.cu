@@ -76,6 +76,7 @@ extern "C" VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, co
                                                               const vtmu_attention_params* p,
                                                               cudaStream_t stream) {
     if (!p) return vtmu::report_error(VTMU_ERR_INVALID, "params is NULL");
+    if (p->T != 1) return vtmu::report_error(VTMU_ERR_INVALID, "decode_noalloc: T must be 1");
     vtmu_attention_params dp = *p;
     dp.kernel = VTMU_KERNEL_DECODE;
     size_t need = 0;

@@ -21,7 +21,12 @@ struct DecodePlan {
     int64_t s_lo = 0;            // first visible key
     int64_t s_end = 0;           // one past the last visible key
     int64_t rows_per_split = 0;  // multiple of the kernel's stage rows
-    int32_t splits = 1;          // per KV head
+    int32_t splits = 1;          // per KV head and row group
+    // Query rows: gv virtual heads (tc rows x the group's heads, padded to a
+    // power of two >= 2) per KV head and row group; n_rg row groups.
+    int32_t gv = 2;
+    int32_t tc = 1;
+    int32_t n_rg = 1;
     size_t workspace_bytes = 0;
 };
 
@@ -35,9 +40,10 @@ struct DecodeCacheWrite {
     int64_t lo, hi;
 };
 
-// True when the decode kernel's shape table covers this call (T == 1,
-// headDim == vHeadDim in {32, 64, 128}, group size in {2, 4, 8}, 16-byte
-// aligned rows).  Pointer alignment is checked separately at launch.
+// True when the decode kernel's shape table covers this call (1 <= T <=
+// kDecodeMaxRows, headDim == vHeadDim in {32, 64, 128}, group size in
+// {1, 2, 4, 8}).  Pointer alignment is checked separately at launch.
+constexpr int kDecodeMaxRows = 16;
 bool decode_supported(const AttnDesc& a);
 // Fills `plan` for the call; `forced_splits` > 0 overrides the heuristic.
 void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* plan);

@@ -91,6 +91,10 @@ int device_sm_count() {
 // Query rows from which AUTO prefers the tensor-core prefill (one 128-row
 // MMA tile is then at least half full).
 constexpr int64_t kTcMinRows = 64;
+// AUTO takes the decode kernel up to this many query rows: it reads K/V once
+// per row group (8 virtual heads), where the prefill kernels would read them
+// once per query head and fill 64- or 128-row tiles with a few rows.
+constexpr int64_t kDecodeAutoRows = 8;
 
 struct Resolved {
     vtmu::AttnDesc a;
@@ -160,18 +164,20 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
 
     int kernel = p->kernel;
     if (kernel == VTMU_KERNEL_AUTO) {
-        if (a.T == 1 && vtmu::decode_supported(a))
+        if (a.T <= kDecodeAutoRows && vtmu::decode_supported(a))
             kernel = VTMU_KERNEL_DECODE;
         else if (a.T >= kTcMinRows && vtmu::prefill_tc_supported(a))
             kernel = VTMU_KERNEL_PREFILL_TF32X3;
         else
             kernel = VTMU_KERNEL_PREFILL_FFMA;
     } else if (kernel == VTMU_KERNEL_DECODE) {
-        if (a.T != 1) return fail(VTMU_ERR_INVALID, "kernel DECODE needs T == 1 (got %lld)", (long long)a.T);
+        if (a.T < 1 || a.T > vtmu::kDecodeMaxRows)
+            return fail(VTMU_ERR_INVALID, "kernel DECODE needs 1 <= T <= %d (got %lld)", vtmu::kDecodeMaxRows,
+                        (long long)a.T);
         if (!vtmu::decode_supported(a))
             return fail(VTMU_ERR_UNSUPPORTED,
                         "kernel DECODE covers headDim == vHeadDim in {32,64,128} and group size "
-                        "heads/kvHeads in {2,4,8} (got headDim %d, vHeadDim %d, group %d)",
+                        "heads/kvHeads in {1,2,4,8} (got headDim %d, vHeadDim %d, group %d)",
                         a.D, a.Dv, a.G);
     } else if (kernel == VTMU_KERNEL_PREFILL_TF32X3) {
         if (!vtmu::prefill_tc_supported(a))

@@ -82,15 +82,15 @@ typedef enum vtmu_bias_kind {
     VTMU_BIAS_HTS = 2  /* bias [heads, T, S] */
 } vtmu_bias_kind;
 
-/* Kernel choice.  AUTO takes the split-KV decode kernel for T == 1 (when its
- * shape table covers headDim/vHeadDim/group size), the tcgen05 3xTF32
+/* Kernel choice.  AUTO takes the split-KV decode kernel for 1 <= T <= 8
+ * (when its shape table covers headDim/vHeadDim/group size), the tcgen05 3xTF32
  * prefill for T >= 64 when it covers the shape (headDim == vHeadDim in
  * {32, 64, 96, 128, 256}, or headDim 192 with vHeadDim 128; 16-byte aligned q
  * and out), and the FFMA prefill otherwise.  The others force one kernel,
  * for tests and measurement. */
 typedef enum vtmu_kernel {
     VTMU_KERNEL_AUTO = 0,
-    VTMU_KERNEL_DECODE = 1,        /* T must be 1 */
+    VTMU_KERNEL_DECODE = 1,        /* 1 <= T <= 16: T query rows against a cache */
     VTMU_KERNEL_PREFILL_FFMA = 2,  /* tiled online-softmax kernel on FP32 FMA */
     VTMU_KERNEL_PREFILL_TF32X3 = 3 /* tcgen05 3xTF32 tensor-core prefill */
 } vtmu_kernel;
@@ -152,7 +152,7 @@ VTMU_API vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* 
  * Errors: VTMU_ERR_INVALID (null pointer, T/S < 0, heads <= 0, heads not a
  * multiple of kv_heads, window < 0, softcap < 0 or not finite, scale not
  * finite, bias pointer and bias_kind disagree, alibi slopes missing, out
- * aliasing an input, T != 1 with VTMU_KERNEL_DECODE), VTMU_ERR_RANGE
+ * aliasing an input, T outside 1..16 with VTMU_KERNEL_DECODE), VTMU_ERR_RANGE
  * (pos_offset < 0), VTMU_ERR_UNSUPPORTED (head_dim or v_head_dim outside
  * 1..256, a forced kernel that does not cover the shape),
  * VTMU_ERR_WORKSPACE, VTMU_ERR_CUDA.
@@ -169,7 +169,7 @@ VTMU_API vtmu_status vtmu_attention(const float* q, const float* k, const float*
  * without leaving the worker).  The result equals vtmu_cache_write(k_cache,
  * ...), vtmu_cache_write(v_cache, ...), vtmu_attention(q, k_cache, v_cache,
  * bias, out, p, ...) in that order; when the decode kernel covers the call
- * (T == 1, same shape table as VTMU_KERNEL_DECODE) all three run as one
+ * (1 <= T <= 8 under AUTO, same shape table as VTMU_KERNEL_DECODE) all three run as one
  * launch: the CTA that reads a new row takes it from k_new / v_new and writes
  * it to the cache itself.
  *   k_cache [max_rows, kvHeads*headDim], v_cache [max_rows, kvHeads*vHeadDim]:

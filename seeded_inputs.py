@@ -93,17 +93,17 @@ def attention_inputs(T, S, heads, kvHeads, headDim, vHeadDim, seed, *,
     return out
 
 
-def decode_inputs(max_rows, heads, kvHeads, headDim, vHeadDim, seed, *, sigma=1.0):
+def decode_inputs(max_rows, heads, kvHeads, headDim, vHeadDim, seed, *, sigma=1.0, rows=1):
     """A decode step: caches kc [max_rows, kvHeads*headDim] and
-    vc [max_rows, kvHeads*vHeadDim] already filled, the step's query
-    q [1, heads*headDim] and the new rows k_new / v_new [1, ...]."""
+    vc [max_rows, kvHeads*vHeadDim] already filled, the step's query rows
+    q [rows, heads*headDim] and the new rows k_new / v_new [rows, ...]."""
     st = Stream(seed)
     return {
-        "q": st.normal_f32(heads * headDim, sigma).reshape(1, heads * headDim),
+        "q": st.normal_f32(rows * heads * headDim, sigma).reshape(rows, heads * headDim),
         "kc": st.normal_f32(max_rows * kvHeads * headDim, sigma).reshape(max_rows, kvHeads * headDim),
         "vc": st.normal_f32(max_rows * kvHeads * vHeadDim, sigma).reshape(max_rows, kvHeads * vHeadDim),
-        "k_new": st.normal_f32(kvHeads * headDim, sigma).reshape(1, kvHeads * headDim),
-        "v_new": st.normal_f32(kvHeads * vHeadDim, sigma).reshape(1, kvHeads * vHeadDim),
+        "k_new": st.normal_f32(rows * kvHeads * headDim, sigma).reshape(rows, kvHeads * headDim),
+        "v_new": st.normal_f32(rows * kvHeads * vHeadDim, sigma).reshape(rows, kvHeads * vHeadDim),
     }
 
 
@@ -120,6 +120,9 @@ WORKLOADS = {
         kind="decode", max_rows=32768, offset=32767, heads=32, kvHeads=8,
         headDim=128, seed=1, params=dict(causal=True, posOffset=32767),
         rope=dict(base=500000.0)),
+    "gqa_spec_decode": dict(
+        kind="decode", rows=4, max_rows=32768, offset=32764, heads=32, kvHeads=8,
+        headDim=128, seed=6, params=dict(causal=True, posOffset=32764)),
     "gqa_prefill": dict(
         kind="prefill", T=4096, S=4096, heads=32, kvHeads=8, headDim=128,
         seed=2, params=dict(causal=True, posOffset=0)),
@@ -143,7 +146,8 @@ def workload_inputs(name):
     vhd = w.get("vHeadDim", w["headDim"])
     if w["kind"] == "decode":
         return decode_inputs(w["max_rows"], w["heads"], w["kvHeads"],
-                             w["headDim"], vhd, w["seed"], sigma=w.get("sigma", 1.0))
+                             w["headDim"], vhd, w["seed"], sigma=w.get("sigma", 1.0),
+                             rows=w.get("rows", 1))
     return attention_inputs(w["T"], w["S"], w["heads"], w["kvHeads"],
                             w["headDim"], vhd, w["seed"],
                             sigma=w.get("sigma", 1.0), bias=w.get("bias"),

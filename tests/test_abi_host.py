@@ -95,13 +95,19 @@ FAKE = 1 << 40  # never dereferenced: every case below fails before a launch
     (dict(heads=2, headDim=8, posOffset=-3), vtmu.VTMU_ERR_RANGE, "posOffset"),
     (dict(heads=2, headDim=8, alibiMax=-1.0), vtmu.VTMU_ERR_INVALID, "alibiMax"),
     (dict(heads=1024, headDim=8, alibi=True), vtmu.VTMU_ERR_UNSUPPORTED, "attention.alibi"),
-    (dict(heads=4, headDim=8, kernel=vtmu.VTMU_KERNEL_DECODE), vtmu.VTMU_ERR_INVALID, "T == 1"),
 ])
 def test_invalid_params_are_refused(lib, kw, status, word):
     p = vtmu.make_params(4, 4, **kw)
     e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
     assert e.status == status and word in str(e), str(e)
     assert word in vtmu.vtmu_last_error()
+
+
+@host_only
+def test_decode_kernel_row_limit(lib):
+    p = vtmu.make_params(17, 64, heads=4, headDim=64, kernel=vtmu.VTMU_KERNEL_DECODE)
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "1 <= T <= 16" in str(e)
 
 
 @host_only

@@ -141,6 +141,41 @@ def test_decode_kernel(D, G, feat):
     check(x, params)
 
 
+@pytest.mark.parametrize("G,T", [(1, 1), (1, 3), (1, 9), (2, 2), (2, 5), (4, 2), (4, 4), (4, 7), (8, 3),
+                                 (4, 16), (8, 16)])
+@pytest.mark.parametrize("feat", ["plain", "window", "bias_ts", "softcap_alibi", "noncausal", "bias_hts"])
+def test_decode_kernel_query_rows(G, T, feat):
+    """Several query rows against a cache (speculative or chunked decode): the
+    kernel's virtual heads are query rows x group heads, in row groups of at
+    most 8; each row masks the keys of the shared range it cannot see."""
+    Hk = 2
+    H = G * Hk
+    D = (32, 64, 128)[(G + T) % 3]
+    S = 900 + 13 * T + D
+    pos = S - T - 40 + (17 if feat == "noncausal" else 0)
+    bias = {"bias_ts": "ts", "bias_hts": "hts"}.get(feat)
+    x = si.attention_inputs(T, S, H, Hk, D, D, 1000 + 10 * G + T, bias=bias)
+    params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=pos, kernel=DECODE)
+    if feat == "window":
+        params["window"] = 1 + 3 * T + 41  # rows see different key ranges
+    elif feat == "softcap_alibi":
+        params.update(softcap=20.0, alibi=True)
+    elif feat == "noncausal":
+        params.update(causal=False, window=150)
+    check(x, params)
+
+
+def test_decode_query_rows_forced_splits_and_auto():
+    """Forced splits over row groups, and AUTO choosing the decode kernel for
+    T <= 8 (a row past S - 1 sees every key)."""
+    x = si.attention_inputs(6, 5000, 32, 8, 128, 128, 78)
+    for splits in (1, 5, 64):
+        check(x, dict(heads=32, headDim=128, kvHeads=8, posOffset=4996, kernel=DECODE, decode_splits=splits))
+    check(x, dict(heads=32, headDim=128, kvHeads=8, posOffset=4996))
+    x = si.attention_inputs(8, 3000, 8, 8, 64, 64, 79)
+    check(x, dict(heads=8, headDim=64, posOffset=2995))  # MHA, rows at 2995..3002
+
+
 @pytest.mark.parametrize("splits", [1, 2, 7, 64, 256])
 def test_decode_forced_splits(splits):
     x = si.attention_inputs(1, 5000, 16, 4, 128, 128, 77)
@@ -311,10 +346,17 @@ def test_decode_step_fused_cases(case):
                       case.pop("offset"), 500, kernel=DECODE, **case)
 
 
-def test_decode_step_unfused_paths():
-    """Shapes outside the decode kernel: chunked prefill (T = 6) and a head
-    size the decode table does not cover run as three launches."""
+def test_decode_step_query_rows_fused():
+    """A chunked step of T = 6 new rows runs as one decode launch."""
     _decode_step_case(700, 4, 2, 128, 6, 600, 501, T=6)
+    _decode_step_case(3000, 32, 8, 128, 4, 2996, 503, T=4)
+
+
+def test_decode_step_unfused_paths():
+    """Shapes outside the decode kernel: a chunk of T = 12 rows (AUTO takes
+    the prefill kernel past 8) and a head size the decode table does not
+    cover run as three launches."""
+    _decode_step_case(700, 4, 2, 128, 12, 600, 501, T=12)
     _decode_step_case(700, 4, 4, 96, 1, 650, 502)
 
 
