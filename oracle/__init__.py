@@ -16,7 +16,9 @@ defaults as the op catalog states them (vtmu.mpakt.dev/api/ops, op
 * ``causal`` defaults to true, ``posOffset`` to 0;
 * ``scale`` replaces 1/sqrt(headDim);
 * ``softcap`` and ``window`` are off when absent (or 0);
-* ALiBi: ``alibiSlopes`` wins over ``alibiMax``, which wins over ``alibi``.
+* ALiBi: ``alibiSlopes`` wins over ``alibiMax``, which wins over ``alibi``;
+* ``sinks`` (the IR page's attention sinks, not a param of the op page):
+  with a window, keys before ``sinks`` stay visible; 0 or absent = none.
 
 ``Oracle(path)`` wraps one compiled build; the module-level functions use the
 default build of ``attention_oracle.c``.  The tests also compile copies with a
@@ -58,6 +60,7 @@ class _Desc(ctypes.Structure):
         ("window", ctypes.c_int64),
         ("slopes", ctypes.POINTER(ctypes.c_double)),
         ("bias_kind", ctypes.c_int),
+        ("sinks", ctypes.c_int64),
     ]
 
 
@@ -133,7 +136,7 @@ class Oracle:
 
     def _prepare(self, q, k, v, bias, heads, headDim, kvHeads, vHeadDim,
                  causal, posOffset, scale, softcap, window, alibi, alibiMax,
-                 alibiSlopes):
+                 alibiSlopes, sinks=None):
         q, k, v = _f32(q), _f32(k), _f32(v)
         kvHeads = heads if kvHeads is None else int(kvHeads)
         vHeadDim = headDim if vHeadDim is None else int(vHeadDim)
@@ -167,16 +170,19 @@ class Oracle:
         d.slopes = (slopes.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
                     if slopes is not None else None)
         d.bias_kind = bias_kind
+        d.sinks = 0 if sinks is None else int(sinks)
+        if d.sinks < 0:
+            raise ValueError("sinks must be >= 0")
         return d, (q, k, v, bias, slopes)
 
     def attention(self, q, k, v, bias=None, *, heads, headDim, kvHeads=None,
                   vHeadDim=None, causal=True, posOffset=0, scale=None,
                   softcap=None, window=None, alibi=False, alibiMax=None,
-                  alibiSlopes=None):
+                  alibiSlopes=None, sinks=None):
         """The whole op: returns out [T, heads*vHeadDim] as float64."""
         d, keep = self._prepare(q, k, v, bias, heads, headDim, kvHeads,
                                 vHeadDim, causal, posOffset, scale, softcap,
-                                window, alibi, alibiMax, alibiSlopes)
+                                window, alibi, alibiMax, alibiSlopes, sinks)
         q, k, v, bias, _ = keep
         out = np.zeros((d.T, d.heads * d.v_head_dim), dtype=np.float64)
         rc = self.lib.oracle_attention(ctypes.byref(d), _ptr(q), _ptr(k),
@@ -188,11 +194,11 @@ class Oracle:
     def attention_rows(self, q, k, v, bias=None, *, rows, heads, headDim,
                        kvHeads=None, vHeadDim=None, causal=True, posOffset=0,
                        scale=None, softcap=None, window=None, alibi=False,
-                       alibiMax=None, alibiSlopes=None):
+                       alibiMax=None, alibiSlopes=None, sinks=None):
         """Selected (t, h) rows only: returns [len(rows), vHeadDim] float64."""
         d, keep = self._prepare(q, k, v, bias, heads, headDim, kvHeads,
                                 vHeadDim, causal, posOffset, scale, softcap,
-                                window, alibi, alibiMax, alibiSlopes)
+                                window, alibi, alibiMax, alibiSlopes, sinks)
         q, k, v, bias, _ = keep
         rows = list(rows)
         ts = np.ascontiguousarray([int(t) for t, _ in rows], dtype=np.int64)

@@ -57,14 +57,19 @@ typedef struct {
     int64_t window; /* 0 = off */
     const double* slopes; /* [heads] or NULL */
     int bias_kind;
+    int64_t sinks;  /* 0 = none */
 } oracle_attn_desc;
 
 /* op "attention", param "window": causal keys are visible when
- * pos - window < s <= pos, non-causal ones when |pos - s| <= window. */
-static int key_visible(int causal, int64_t window, int64_t p, int64_t s)
+ * pos - window < s <= pos, non-causal ones when |pos - s| <= window.
+ * Attention sinks (the IR page's integer `sinks` beside `window`, read as
+ * the sink tokens of streaming attention): with a window, keys s < sinks
+ * stay visible wherever the window has moved (still subject to causality). */
+static int key_visible(int causal, int64_t window, int64_t sinks, int64_t p, int64_t s)
 {
     if (causal && s > p) return 0;
     if (window > 0) {
+        if (s < sinks) return 1;
         if (causal) {
             if (!(p - window < s)) return 0;
         } else {
@@ -88,7 +93,7 @@ static void attend_row(const oracle_attn_desc* a, const float* q, const float* k
     double m = -INFINITY;
 
     for (int64_t s = 0; s < a->S; ++s) {
-        vis[s] = (char)key_visible(a->causal, a->window, p, s);
+        vis[s] = (char)key_visible(a->causal, a->window, a->sinks, p, s);
         if (!vis[s]) continue;
         const float* krow = k + s * (int64_t)a->kv_heads * D + (int64_t)kh * D;
         double dot = 0.0;

@@ -30,11 +30,14 @@ def _sym(x):
     return x
 
 
-def visible(causal, window, p, s):
-    """The op catalog's visibility rule, written from its `window` text."""
+def visible(causal, window, p, s, sinks=0):
+    """The op catalog's visibility rule, written from its `window` text, with
+    the IR page's attention sinks (keys before `sinks` escape the window)."""
     if causal and s > p:
         return False
     if window:
+        if s < sinks:
+            return True
         if causal:
             return p - window < s
         return abs(p - s) <= window
@@ -184,7 +187,7 @@ def pin_softcap_limits(orc):
 
 # --------------------------------------------------------------- torch library
 def _sdpa(q, k, v, bias, *, heads, headDim, kvHeads, vHeadDim, causal, posOffset,
-          scale, window, slopes):
+          scale, window, slopes, sinks=0):
     """PyTorch float64 scaled_dot_product_attention with the masks, the ALiBi
     term (absolute form slope * s) and the bias folded into an additive mask."""
     import torch
@@ -195,7 +198,7 @@ def _sdpa(q, k, v, bias, *, heads, headDim, kvHeads, vHeadDim, causal, posOffset
     mask = np.zeros((heads, T, S), np.float64)
     for t in range(T):
         for s in range(S):
-            if not visible(causal, window or 0, posOffset + t, s):
+            if not visible(causal, window or 0, posOffset + t, s, sinks or 0):
                 mask[:, t, s] = -np.inf
     if slopes is not None:
         mask += np.asarray(slopes, np.float64)[:, None, None] * np.arange(S)[None, None, :]
@@ -222,6 +225,12 @@ def pin_torch_sdpa(orc):
              bias="hts", slopes=True),
         dict(T=9, S=9, heads=8, kvHeads=8, headDim=4, vHeadDim=4, causal=True, posOffset=0,
              slopes=True),
+        dict(T=6, S=20, heads=4, kvHeads=2, headDim=8, vHeadDim=8, causal=True, posOffset=12,
+             window=3, sinks=4),
+        dict(T=5, S=16, heads=2, kvHeads=1, headDim=4, vHeadDim=6, causal=False, posOffset=9,
+             window=2, sinks=3, bias="ts"),
+        dict(T=8, S=8, heads=2, kvHeads=2, headDim=4, vHeadDim=4, causal=True, posOffset=0,
+             window=2, sinks=5),
     ]
     for c in cases:
         T, S, H, Hk = c["T"], c["S"], c["heads"], c["kvHeads"]
@@ -238,11 +247,11 @@ def pin_torch_sdpa(orc):
         scale = c.get("scale")
         out = orc.attention(q, k, v, bias, heads=H, headDim=D, kvHeads=Hk, vHeadDim=Dv,
                             causal=c["causal"], posOffset=c["posOffset"], scale=scale,
-                            window=c.get("window"), alibiSlopes=slopes)
+                            window=c.get("window"), alibiSlopes=slopes, sinks=c.get("sinks"))
         want = _sdpa(q, k, v, bias, heads=H, headDim=D, kvHeads=Hk, vHeadDim=Dv,
                      causal=c["causal"], posOffset=c["posOffset"],
                      scale=(1.0 / math.sqrt(D)) if scale is None else scale,
-                     window=c.get("window"), slopes=slopes)
+                     window=c.get("window"), slopes=slopes, sinks=c.get("sinks"))
         err = np.max(np.abs(out - want))
         assert err < 1e-10, (c, err)
 

@@ -53,6 +53,11 @@ MUTANTS = [
      "            for (int i = 2; i <= n && w < heads; i += 2) out[w++] = a[i - 1];"),
     ("cache_write copies the first row everywhere",
      "= values[r * width + c];", "= values[c];"),
+    ("sinks escape causality (sinks keep keys the window drops, not future keys)",
+     "    if (causal && s > p) return 0;\n    if (window > 0) {\n        if (s < sinks) return 1;",
+     "    if (s < sinks) return 1;\n    if (causal && s > p) return 0;\n    if (window > 0) {"),
+    ("sinks ignored",
+     "        if (s < sinks) return 1;\n", ""),
     ("rope turns the wrong way (op rope: rotary embedding)",
      "orow[ia] = (double)xr[ia] * c - (double)xr[ib] * s;", "orow[ia] = (double)xr[ia] * c + (double)xr[ib] * s;"),
     ("rope half-split partner i + 1 instead of i + rotaryDim/2",
