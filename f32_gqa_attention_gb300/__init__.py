@@ -64,6 +64,7 @@ class vtmu_attention_params(ctypes.Structure):
         ("bias_kind", ctypes.c_int32),
         ("kernel", ctypes.c_int32),
         ("decode_splits", ctypes.c_int32),
+        ("sinks", ctypes.c_int64),
     ]
 
 
@@ -262,7 +263,7 @@ def vtmu_last_error() -> str:
 # ------------------------------------------------------------ torch helpers
 def make_params(T, S, *, heads, headDim, kvHeads=None, vHeadDim=None, causal=True, posOffset=0,
                 scale=None, softcap=None, window=None, alibi=False, alibiMax=None, alibiSlopes=None,
-                bias_kind=VTMU_BIAS_NONE, kernel=VTMU_KERNEL_AUTO, decode_splits=0):
+                bias_kind=VTMU_BIAS_NONE, kernel=VTMU_KERNEL_AUTO, decode_splits=0, sinks=None):
     """A params struct from the op catalog's parameter names.  ALiBi
     precedence: alibiSlopes, then alibiMax, then alibi.  The returned struct
     keeps any slope array alive as ``_slopes``."""
@@ -289,6 +290,7 @@ def make_params(T, S, *, heads, headDim, kvHeads=None, vHeadDim=None, causal=Tru
     p.bias_kind = int(bias_kind)
     p.kernel = int(kernel)
     p.decode_splits = int(decode_splits)
+    p.sinks = 0 if sinks is None else int(sinks)
     return p
 
 

@@ -23,6 +23,7 @@ __device__ __forceinline__ bool key_visible(const AttnDesc& a, int64_t p, int64_
     if (s < 0 || s >= a.S) return false;
     if (a.causal && s > p) return false;
     if (a.window > 0) {
+        if (s < a.sinks) return true;  // attention sinks escape the window
         if (a.causal) return s > p - a.window;
         int64_t d = p > s ? p - s : s - p;
         return d <= a.window;

@@ -21,6 +21,7 @@ struct AttnDesc {
     int32_t causal;
     int64_t pos_offset;
     int64_t window;      // 0 = off
+    int64_t sinks;       // with a window: keys s < sinks stay visible (0 = none)
     int32_t bias_kind;   // 0 none, 1 [T,S], 2 [H,T,S]
     int32_t softcap_on;
     int32_t alibi_on;

@@ -77,6 +77,8 @@ struct DecodeArgs {
     int64_t s_lo;
     int64_t s_end;
     int64_t rows_per_split;
+    int64_t sink_end;        // attention sinks: rows [0, sink_end) are a range of their own
+    int32_t sink_splits;     // splits [0, sink_splits) stream the sink range
     int32_t splits;
     float* part_m;           // [heads][splits]
     float* part_l;           // [heads][splits]
@@ -197,9 +199,12 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     const int lane = threadIdx.x & 31;
     const int64_t p = a.pos_offset;  // position of query row 0 (row t sits at p + t)
 
-    const int64_t c_begin = args.s_lo + (int64_t)split * args.rows_per_split;
+    const bool sink_split = split < args.sink_splits;
+    const int64_t c_begin = sink_split ? (int64_t)split * args.rows_per_split
+                                       : args.s_lo + (int64_t)(split - args.sink_splits) * args.rows_per_split;
     int64_t c_end = c_begin + args.rows_per_split;
-    if (c_end > args.s_end) c_end = args.s_end;
+    const int64_t c_cap = sink_split ? args.sink_end : args.s_end;
+    if (c_end > c_cap) c_end = c_cap;
     const int n_rows = c_end > c_begin ? (int)(c_end - c_begin) : 0;
     const int n_stages = (n_rows + NR - 1) / NR;
 
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
     const int64_t ld = (int64_t)a.Hk * D;
     if (args.cw.k_new && split == 0 && blockIdx.z == 0 && warp == 0) {
         for (int64_t r = args.cw.lo; r < args.cw.hi; ++r) {
-            if (r >= args.s_lo && r < args.s_end) continue;
+            if ((r >= args.s_lo && r < args.s_end) || r < args.sink_end) continue;
             const int64_t src = (r - args.cw.lo) * ld + (int64_t)kh * D, dst = r * ld + (int64_t)kh * D;
             for (int d = lane; d < D; d += 32) {
                 args.cw.kc[dst + d] = new_key(args, src, d, r);
@@ -641,7 +646,18 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
     plan->n_rg = n_rg;
     if (lo < 0) lo = 0;
     if (hi < lo) hi = lo;
-    const int64_t rows = hi - lo;
+    // Attention sinks: keys [0, sink_end) stay visible (within the causal
+    // limit); a range of their own before the window's, or one range with it
+    // when the two touch.
+    const int64_t sink_cap = a.causal ? hi : a.S;
+    int64_t sink_end = a.sinks < sink_cap ? a.sinks : sink_cap;
+    if (sink_end > 0 && sink_end >= lo) {
+        if (sink_end > hi) hi = sink_end;
+        lo = 0;
+        sink_end = 0;
+    }
+    if (sink_end < 0) sink_end = 0;
+    const int64_t rows = hi - lo + sink_end;
     const int nr = stage_rows();
     int splits = forced_splits;
     if (splits <= 0) {
@@ -652,14 +668,20 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
         splits = (num_sms * VTMU_DEC_CTAS_PER_SM) / units;
         if (splits < 1) splits = 1;
     }
-    if (splits > kMaxSplits) splits = kMaxSplits;
+    // With a separate sink range the two ranges can take one split more.
+    const int max_splits = sink_end > 0 ? kMaxSplits - 1 : kMaxSplits;
+    if (splits > max_splits) splits = max_splits;
     const int64_t min_rows = nr;
     int64_t per = (rows + splits - 1) / splits;
     if (per < min_rows) per = min_rows;
     per = (per + nr - 1) / nr * nr;
-    int64_t n = rows > 0 ? (rows + per - 1) / per : 1;
+    const int64_t n_sink = (sink_end + per - 1) / per;
+    int64_t n = n_sink + (hi - lo + per - 1) / per;
+    if (n < 1) n = 1;
     plan->s_lo = lo;
     plan->s_end = hi;
+    plan->sink_end = sink_end;
+    plan->sink_splits = (int32_t)n_sink;
     plan->rows_per_split = per;
     plan->splits = (int32_t)n;
     const size_t H = (size_t)n_rg * a.Hk * gv, Sp = (size_t)n;  // virtual heads
@@ -680,6 +702,8 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
     args.s_lo = plan.s_lo;
     args.s_end = plan.s_end;
     args.rows_per_split = plan.rows_per_split;
+    args.sink_end = plan.sink_end;
+    args.sink_splits = plan.sink_splits;
     args.splits = plan.splits;
     args.gr = a.G;
     args.tc = plan.tc;

@@ -21,6 +21,8 @@ struct DecodePlan {
     int64_t s_lo = 0;            // first visible key
     int64_t s_end = 0;           // one past the last visible key
     int64_t rows_per_split = 0;  // multiple of the kernel's stage rows
+    int64_t sink_end = 0;        // attention sinks: rows [0, sink_end) stream first
+    int32_t sink_splits = 0;     // splits given to them
     int32_t splits = 1;          // per KV head and row group
     // Query rows: gv virtual heads (tc rows x the group's heads, padded to a
     // power of two >= 2) per KV head and row group; n_rg row groups.

@@ -110,20 +110,35 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         if (p_last + a.window < s_hi) s_hi = p_last + a.window;
     }
     if (s_lo < 0) s_lo = 0;
-    const int64_t jt_begin = s_lo / BN;
-    const int64_t jt_end = (s_hi >= s_lo) ? s_hi / BN + 1 : jt_begin;
+    int64_t jt_begin = s_lo / BN;
+    int64_t jt_end = (s_hi >= s_lo) ? s_hi / BN + 1 : jt_begin;
+    // Attention sinks: keys s < sink_end stay visible (within the causal
+    // limit).  Their tiles come first, or join the window's into one range
+    // when the two touch.
+    const int64_t sink_cap = a.causal ? s_hi + 1 : a.S;
+    const int64_t sink_end = a.sinks < sink_cap ? a.sinks : sink_cap;
+    const int64_t n_st = sink_end > 0 ? (sink_end + BN - 1) / BN : 0;
+    int64_t n_sink = 0;
+    if (n_st > 0 && n_st >= jt_begin) {
+        if (n_st > jt_end) jt_end = n_st;
+        jt_begin = 0;
+    } else {
+        n_sink = n_st;
+    }
+    const int64_t n_tiles = n_sink + (jt_end - jt_begin);
+    auto tile_of = [&](int64_t it) -> int64_t { return it < n_sink ? it : jt_begin + (it - n_sink); };
 
     const int64_t ldq = (int64_t)a.H * a.D, ldk = (int64_t)a.Hk * a.D, ldv = (int64_t)a.Hk * a.Dv;
     const float slope = a.alibi_on ? alibi.slope_log2[h] : 0.f;
 
     // Prologue: Q and K_0 in one group, V_0 in the next.
     stage_rows<VEC16, C::THREADS>(sQ, C::QLD, a.q, ldq, (int64_t)h * a.D, t0, BM, a.T, a.D, Dp);
-    if (jt_begin < jt_end)
-        stage_rows<VEC16, C::THREADS>(sK, C::KLD, a.k, ldk, (int64_t)kh * a.D, jt_begin * BN, BN,
+    if (n_tiles > 0)
+        stage_rows<VEC16, C::THREADS>(sK, C::KLD, a.k, ldk, (int64_t)kh * a.D, tile_of(0) * BN, BN,
                                       a.S, a.D, Dp);
     cp_async_commit();
-    if (jt_begin < jt_end)
-        stage_rows<VEC16, C::THREADS>(sV, C::VLD, a.v, ldv, (int64_t)kh * a.Dv, jt_begin * BN, BN,
+    if (n_tiles > 0)
+        stage_rows<VEC16, C::THREADS>(sV, C::VLD, a.v, ldv, (int64_t)kh * a.Dv, tile_of(0) * BN, BN,
                                       a.S, a.Dv, Dvp);
     cp_async_commit();
 
@@ -139,8 +154,9 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int e = 0; e < 4; ++e) o[i][c][e] = 0.f;
     }
 
-    for (int64_t jt = jt_begin; jt < jt_end; ++jt) {
-        const int64_t n0 = jt * BN;
+    for (int64_t it = 0; it < n_tiles; ++it) {
+        const int64_t n0 = tile_of(it) * BN;
+        const int64_t n_next = it + 1 < n_tiles ? tile_of(it + 1) * BN : 0;
         cp_async_wait<1>();
         __syncthreads();  // K_jt (and Q) landed
 
@@ -210,8 +226,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
         }
         __syncthreads();  // P written, K_jt consumed
 
-        if (jt + 1 < jt_end)
-            stage_rows<VEC16, C::THREADS>(sK, C::KLD, a.k, ldk, (int64_t)kh * a.D, n0 + BN, BN, a.S,
+        if (it + 1 < n_tiles)
+            stage_rows<VEC16, C::THREADS>(sK, C::KLD, a.k, ldk, (int64_t)kh * a.D, n_next, BN, a.S,
                                           a.D, Dp);
         cp_async_commit();
         cp_async_wait<1>();
@@ -242,8 +258,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             }
         }
         __syncthreads();  // V_jt and P consumed
-        if (jt + 1 < jt_end)
-            stage_rows<VEC16, C::THREADS>(sV, C::VLD, a.v, ldv, (int64_t)kh * a.Dv, n0 + BN, BN, a.S,
+        if (it + 1 < n_tiles)
+            stage_rows<VEC16, C::THREADS>(sV, C::VLD, a.v, ldv, (int64_t)kh * a.Dv, n_next, BN, a.S,
                                           a.Dv, Dvp);
         cp_async_commit();
     }

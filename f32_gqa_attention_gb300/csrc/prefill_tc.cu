@@ -343,7 +343,9 @@ __device__ __forceinline__ void run_epilogue_staged(int feat, const AttnDesc& a,
     }
 }
 
-template <int D, int DV>
+// SINKS: attention sinks are on (a separate instantiation, so that the
+// common path carries none of their bookkeeping).
+template <int D, int DV, bool SINKS>
 __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
     prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const int bias_staged,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_bias,
@@ -393,12 +395,31 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
         if (p_last + a.window < s_hi) s_hi = p_last + a.window;
     }
     if (s_lo < 0) s_lo = 0;
-    const int64_t jt_begin = s_lo / kBN;
-    const int n_tiles = (s_hi >= s_lo) ? (int)(s_hi / kBN + 1 - jt_begin) : 0;
-    // Key tiles run from the last (nearest the diagonal) down: with ALiBi the
-    // largest scores come first and the running max rarely moves, so O is
+    int64_t jt_begin = s_lo / kBN;
+    int64_t jt_end = (s_hi >= s_lo) ? s_hi / kBN + 1 : jt_begin;
+    // Attention sinks: keys s < sink_end stay visible (within the causal
+    // limit).  Their tiles come after the window's, or join them into one
+    // range when the two touch.
+    const int64_t sinks = SINKS ? a.sinks : 0;
+    const int64_t sink_cap = a.causal ? s_hi + 1 : a.S;
+    const int64_t sink_end = sinks < sink_cap ? sinks : sink_cap;
+    const int64_t n_st = sink_end > 0 ? (sink_end + kBN - 1) / kBN : 0;
+    int n_sink = 0;
+    if (n_st > 0 && n_st >= jt_begin) {
+        if (n_st > jt_end) jt_end = n_st;
+        jt_begin = 0;
+    } else {
+        n_sink = (int)n_st;
+    }
+    const int n_win = (int)(jt_end - jt_begin);
+    const int n_tiles = n_win + n_sink;
+    // Window tiles run from the last (nearest the diagonal) down: with ALiBi
+    // the largest scores come first and the running max rarely moves, so O is
     // seldom rescaled.  The producer, the MMA threads and the softmax share it.
-    auto tile_key0 = [&](int j) -> int64_t { return (jt_begin + (n_tiles - 1 - j)) * kBN; };
+    auto tile_key0 = [&](int j) -> int64_t {
+        if constexpr (SINKS) return (j < n_win ? jt_begin + (n_win - 1 - j) : (int64_t)(j - n_win)) * kBN;
+        return (jt_begin + (n_win - 1 - j)) * kBN;
+    };
 
     if (threadIdx.x == 0) {
         // One barrier per buffer: no wait ever targets a phase two behind.
@@ -708,6 +729,14 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
             lo_t = 1;
             hi_t = 0;
         }
+        // Attention sinks: keys below sink_t are visible too (0 when none;
+        // key indices fit 31 bits, as the TMA coordinates do).
+        const bool has_sinks = SINKS && a.sinks > 0;  // the same for every thread
+        int sink_t = 0;
+        if (has_sinks && row_ok) {
+            const int64_t cap = a.causal ? hi_t + 1 : a.S;
+            sink_t = (int)(a.sinks < cap ? a.sinks : cap);
+        }
         const float* brow = a.bias_kind == 0 ? nullptr
                             : a.bias_kind == 1 ? a.bias + t * a.S
                                                : a.bias + ((int64_t)h * a.T + t) * a.S;
@@ -773,9 +802,27 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
             const int64_t n0 = tile_key0(j) + c0;
             // Visible slots of this warp's keys, clamped to [-1, NCOL].
             const int64_t lo64 = lo_t - n0, hi64 = hi_t - n0;
-            const int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > NCOL ? NCOL : lo64));
-            const int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > NCOL ? NCOL : hi64));
-            const bool full = lo_i <= 0 && hi_i >= NCOL - 1;
+            int lo_i = (int)(lo64 < -1 ? -1 : (lo64 > NCOL ? NCOL : lo64));
+            int hi_i = (int)(hi64 < -1 ? -1 : (hi64 > NCOL ? NCOL : hi64));
+            // Attention sinks in this tile (rare): slots below sk_i are visible
+            // too.  The epilogue then covers [0, max(hi_i, sk_i - 1)] and the
+            // gap [sk_i, lo_i) between the sinks and the window is masked after
+            // it (its keys lie inside the key range, so the bias reads stay in
+            // bounds).
+            int gap_lo = NCOL, gap_hi = NCOL;
+            if (has_sinks) {
+                const int sk_r = sink_t - (int)n0;
+                const int sk_i = sk_r < 0 ? 0 : (sk_r > NCOL ? NCOL : sk_r);
+                if (sk_i > 0) {
+                    if (sk_i < lo_i) {
+                        gap_lo = sk_i;
+                        gap_hi = lo_i < NCOL ? lo_i : NCOL;
+                    }
+                    lo_i = 0;
+                    if (hi_i < sk_i - 1) hi_i = sk_i - 1;
+                }
+            }
+            const bool full = lo_i <= 0 && hi_i >= NCOL - 1 && gap_lo >= gap_hi;
             // Plain scaled scores (no softcap, ALiBi or bias) with a positive
             // scale: the mask alone here, and the scale goes into the exp2's FFMA.
             const bool fold = feat == 0 && a.qk_mul > 0.f;
@@ -795,6 +842,11 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
             } else if (!full) {
 #pragma unroll
                 for (int i = 0; i < NCOL; ++i) x[i] = (i >= lo_i && i <= hi_i) ? x[i] : -INFINITY;
+            }
+            if (has_sinks && gap_lo < gap_hi) {  // sinks and window apart in this tile: hide the keys between
+#pragma unroll
+                for (int i = 0; i < NCOL; ++i)
+                    if (i >= gap_lo && i < gap_hi) x[i] = -INFINITY;
             }
             const float cx = fold ? a.qk_mul : 1.f;
             float mt = tree_max<NCOL>(x) * cx;
@@ -1006,7 +1058,7 @@ TcLayout tc_layout(const AttnDesc& a) {
     return L;
 }
 
-template <int D, int DV>
+template <int D, int DV, bool SINKS>
 cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, float* klo, float* vthi,
                        float* vtlo, int64_t s_pad, cudaStream_t stream) {
     using C = TcCfg<D, DV>;
@@ -1025,7 +1077,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
         !encode_sw128(&m_vhi, vthi, (int64_t)a.Hk * DV, s_pad, C::DVC) ||
         !encode_sw128(&m_vlo, vtlo, (int64_t)a.Hk * DV, s_pad, C::DVC))
         return cudaErrorInvalidValue;
-    auto kern = prefill_tc_kernel<D, DV>;
+    auto kern = prefill_tc_kernel<D, DV, SINKS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
@@ -1065,8 +1117,10 @@ cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* 
     split_vt_kernel<<<g2, dim3(32, 8), 0, stream>>>(a.v, vthi, vtlo, a.S, L.s_pad, cols);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-#define VTMU_TC(D_, DV_) \
-    if (a.D == D_ && a.Dv == DV_) return launch_cfg<D_, DV_>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream);
+#define VTMU_TC(D_, DV_)                                                                                     \
+    if (a.D == D_ && a.Dv == DV_)                                                                            \
+        return a.sinks > 0 ? launch_cfg<D_, DV_, true>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream)      \
+                           : launch_cfg<D_, DV_, false>(a, alibi, khi, klo, vthi, vtlo, L.s_pad, stream);
     VTMU_TC(32, 32) VTMU_TC(64, 64) VTMU_TC(96, 96) VTMU_TC(128, 128) VTMU_TC(192, 128) VTMU_TC(256, 256)
 #undef VTMU_TC
     return cudaErrorInvalidValue;

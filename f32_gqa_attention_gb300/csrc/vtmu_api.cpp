@@ -120,6 +120,7 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
     if (Dv > 256) return fail(VTMU_ERR_UNSUPPORTED, "vHeadDim %d > 256 is not supported", Dv);
     if (p->pos_offset < 0) return fail(VTMU_ERR_RANGE, "posOffset must be >= 0 (got %lld)", (long long)p->pos_offset);
     if (p->window < 0) return fail(VTMU_ERR_INVALID, "window must be >= 0 (got %lld)", (long long)p->window);
+    if (p->sinks < 0) return fail(VTMU_ERR_INVALID, "sinks must be >= 0 (got %lld)", (long long)p->sinks);
     if (!(p->softcap >= 0.f) || !std::isfinite(p->softcap))
         return fail(VTMU_ERR_INVALID, "softcap must be finite and >= 0");
     if (p->has_scale && !std::isfinite(p->scale)) return fail(VTMU_ERR_INVALID, "scale must be finite");
@@ -149,6 +150,7 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
     a.causal = p->causal ? 1 : 0;
     a.pos_offset = p->pos_offset;
     a.window = p->window;
+    a.sinks = p->window > 0 ? p->sinks : 0;  // without a window no key is dropped
     a.bias_kind = p->bias_kind;
     const double scale = p->has_scale ? (double)p->scale : 1.0 / std::sqrt((double)p->head_dim);
     if (p->softcap > 0.f) {

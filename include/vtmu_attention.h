@@ -121,6 +121,9 @@ typedef struct vtmu_attention_params {
     int32_t bias_kind;    /* vtmu_bias_kind; bias pointer must agree */
     int32_t kernel;       /* vtmu_kernel */
     int32_t decode_splits; /* decode kernel: KV splits per KV head, 0 = auto */
+    int64_t sinks;        /* attention sinks (the IR page's op_attention.sinks, not a
+                             param of the op page): with a window, keys s < sinks
+                             stay visible (causality still applies); 0 = none */
 } vtmu_attention_params;
 
 /* Writes the op's defaults: causal = 1, everything else 0 / off / AUTO. */

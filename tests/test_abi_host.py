@@ -275,3 +275,10 @@ def test_decode_step_rope_refusals(lib):
     e = call(p=vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094))
     assert e.status == vtmu.VTMU_ERR_UNSUPPORTED
     assert call(r=vtmu.make_rope_params(headDim=128, rotaryDim=130)).status == vtmu.VTMU_ERR_INVALID
+
+
+@host_only
+def test_negative_sinks_are_refused(lib):
+    p = vtmu.make_params(4, 4, heads=2, headDim=8, window=2, sinks=-1)
+    e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "sinks" in str(e)

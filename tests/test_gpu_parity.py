@@ -176,6 +176,53 @@ def test_decode_query_rows_forced_splits_and_auto():
     check(x, dict(heads=8, headDim=64, posOffset=2995))  # MHA, rows at 2995..3002
 
 
+# ------------------------------------------------------------ attention sinks
+SINK_CASES = [
+    # (T, S, posOffset, window, sinks, causal)
+    (200, 900, 700, 150, 4, True),      # sinks far below the window (a tile of their own)
+    (130, 700, 0, 100, 37, True),       # sinks inside the first window tiles of early rows
+    (64, 3000, 2900, 64, 130, True),    # sink range of several tiles
+    (96, 500, 100, 20, 300, False),     # non-causal: sinks past the window's far end
+    (1, 5000, 4999, 1000, 4, True),     # decode step with sinks
+    (4, 5000, 4990, 700, 64, True),     # speculative step with sinks
+    (3, 300, 296, 50, 500, True),       # sinks beyond every key: only causality limits them
+]
+
+
+@pytest.mark.parametrize("kernel", ["auto", "ffma", "tc", "decode"])
+@pytest.mark.parametrize("case", SINK_CASES, ids=[str(i) for i in range(len(SINK_CASES))])
+def test_attention_sinks(case, kernel):
+    """The IR page's attention sinks (keys before `sinks` escape the window)
+    on every kernel that covers the shape."""
+    T, S, pos, window, sinks, causal = case
+    H, Hk, D = 8, 2, 64
+    if kernel == "decode" and T > 16:
+        pytest.skip("decode kernel: T <= 16")
+    if kernel == "tc" and T < 64:
+        pytest.skip("tensor-core prefill case list uses T >= 64")
+    x = si.attention_inputs(T, S, H, Hk, D, D, 700 + T + sinks)
+    params = dict(heads=H, headDim=D, kvHeads=Hk, posOffset=pos, window=window, sinks=sinks, causal=causal)
+    if kernel != "auto":
+        params["kernel"] = {"ffma": FFMA, "tc": vtmu.VTMU_KERNEL_PREFILL_TF32X3, "decode": DECODE}[kernel]
+    check(x, params)
+
+
+def test_attention_sinks_decode_splits():
+    x = si.attention_inputs(1, 6000, 16, 4, 128, 128, 777)
+    for splits in (1, 3, 255, 256):
+        check(x, dict(heads=16, headDim=128, kvHeads=4, posOffset=5999, window=2048, sinks=100, kernel=DECODE,
+                      decode_splits=splits))
+
+
+def test_attention_sinks_softcap_alibi_bias_tc():
+    x = si.attention_inputs(256, 1200, 4, 2, 128, 128, 778, bias="hts")
+    check(x, dict(heads=4, headDim=128, kvHeads=2, posOffset=900, window=300, sinks=70, softcap=20.0, alibi=True,
+                  kernel=vtmu.VTMU_KERNEL_PREFILL_TF32X3))
+    x = si.attention_inputs(256, 1200, 4, 4, 256, 256, 779)
+    check(x, dict(heads=4, headDim=256, posOffset=900, window=300, sinks=9, scale=1 / 16, softcap=50.0,
+                  kernel=vtmu.VTMU_KERNEL_PREFILL_TF32X3))
+
+
 @pytest.mark.parametrize("splits", [1, 2, 7, 64, 256])
 def test_decode_forced_splits(splits):
     x = si.attention_inputs(1, 5000, 16, 4, 128, 128, 77)
