@@ -51,32 +51,54 @@ FP32_LANES_PER_SM = 128
 
 # ------------------------------------------------------------------ work model
 def decode_bytes(w):
-    """Algorithmic bytes of one decode step: every visible K and V row once,
-    the query and output rows once, and the two cache writes of the new rows
-    (read + write)."""
+    """Algorithmic bytes of one decode step: every K and V row some query row
+    sees once, the query and output rows once, and the two cache writes of
+    the new rows (read + write)."""
     H, Hk, D, R = w["heads"], w["kvHeads"], w["headDim"], w.get("rows", 1)
     S = w["offset"] + R
-    kv = 2 * S * Hk * D * 4
+    p = w["params"]
+    seen = np.zeros(S, dtype=bool)
+    for t in range(R):
+        pos = p.get("posOffset", 0) + t
+        s = np.arange(S)
+        vis = np.ones(S, dtype=bool)
+        if p.get("causal", True):
+            vis &= s <= pos
+        win = p.get("window") or 0
+        if win:
+            inw = (s > pos - win) if p.get("causal", True) else (np.abs(pos - s) <= win)
+            vis &= inw | (s < (p.get("sinks") or 0))
+        seen |= vis
+    kv = 2 * int(seen.sum()) * Hk * D * 4
     qo = 2 * R * H * D * 4
     cw = 2 * 2 * R * Hk * D * 4
     return kv, kv + qo + cw
 
 
+def visible_counts(pos, S, params):
+    """Visible keys of query rows at positions `pos` (numpy int64), from the
+    op's masking rule: the causal limit, the window, and attention sinks
+    (keys before `sinks` escape the window)."""
+    causal = params.get("causal", True)
+    win = params.get("window") or 0
+    sinks = params.get("sinks") or 0
+    if causal:
+        hi = np.minimum(pos, S - 1)
+        lo = np.maximum(pos - win + 1, 0) if win else np.zeros_like(pos)
+    else:
+        lo = np.maximum(pos - win, 0) if win else np.zeros_like(pos)
+        hi = np.minimum(pos + win, S - 1) if win else np.full_like(pos, S - 1)
+    n = np.maximum(hi - lo + 1, 0)
+    if win and sinks:
+        cap = np.minimum(sinks, hi + 1) if causal else np.full_like(pos, min(sinks, S))
+        n = n + np.maximum(np.minimum(cap, lo), 0) + np.maximum(cap - (hi + 1), 0)
+    return n
+
+
 def visible_pairs(w):
     """Visible (query, key) pairs per head, from the op's masking rule."""
-    T, S = w["T"], w["S"]
-    p = w["params"]
-    causal = p.get("causal", True)
-    win = p.get("window") or 0
-    pos0 = p.get("posOffset", 0)
-    t = np.arange(T, dtype=np.int64) + pos0
-    if causal:
-        hi = np.minimum(t, S - 1)
-        lo = np.maximum(t - win + 1, 0) if win else np.zeros_like(t)
-    else:
-        lo = np.maximum(t - win, 0) if win else np.zeros_like(t)
-        hi = np.minimum(t + win, S - 1) if win else np.full_like(t, S - 1)
-    return int(np.maximum(hi - lo + 1, 0).sum())
+    pos = np.arange(w["T"], dtype=np.int64) + w["params"].get("posOffset", 0)
+    return int(visible_counts(pos, w["S"], w["params"]).sum())
 
 
 def prefill_flops(w):
@@ -237,16 +259,8 @@ class OracleSampler:
         rows = [(int(t), h) for t in ts for h in range(H)]
         self.oracle.attention_rows(x["q"], x["k"], x["v"], x.get("bias"), rows=rows, **params)
         dt = time.perf_counter() - t0
-        causal = w["params"].get("causal", True)
-        win = w["params"].get("window") or 0
-        pairs = 0
-        for t in ts:
-            p = int(t) + w["params"].get("posOffset", 0)
-            if causal:
-                lo, hi = (max(p - win + 1, 0) if win else 0), min(p, w["S"] - 1)
-            else:
-                lo, hi = (max(p - win, 0) if win else 0), (min(p + win, w["S"] - 1) if win else w["S"] - 1)
-            pairs += max(hi - lo + 1, 0)
+        pairs = int(visible_counts(np.asarray(ts, dtype=np.int64) + w["params"].get("posOffset", 0), w["S"],
+                                   w["params"]).sum())
         return pairs * H * (2 * D + 2 * Dv) / 1e12, dt
 
     def describe(self, n):

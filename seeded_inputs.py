@@ -123,6 +123,9 @@ WORKLOADS = {
     "gqa_spec_decode": dict(
         kind="decode", rows=4, max_rows=32768, offset=32764, heads=32, kvHeads=8,
         headDim=128, seed=6, params=dict(causal=True, posOffset=32764)),
+    "gqa_decode_sinks": dict(
+        kind="decode", max_rows=32768, offset=32767, heads=32, kvHeads=8,
+        headDim=128, seed=1, params=dict(causal=True, posOffset=32767, window=8188, sinks=4)),
     "gqa_prefill": dict(
         kind="prefill", T=4096, S=4096, heads=32, kvHeads=8, headDim=128,
         seed=2, params=dict(causal=True, posOffset=0)),
@@ -130,6 +133,10 @@ WORKLOADS = {
         kind="prefill", T=8192, S=8192, heads=16, kvHeads=8, headDim=256,
         seed=3, sigma=2.0,
         params=dict(causal=True, scale=1.0 / 16, softcap=50.0, window=4096)),
+    "swa_sinks_prefill": dict(
+        kind="prefill", T=8192, S=8192, heads=16, kvHeads=8, headDim=256,
+        seed=3, sigma=2.0,
+        params=dict(causal=True, scale=1.0 / 16, softcap=50.0, window=4096, sinks=4)),
     "latent_bias_prefill": dict(
         kind="prefill", T=2048, S=2048, heads=128, kvHeads=128, headDim=192,
         vHeadDim=128, seed=4, bias="ts", bias_mask_p=0.1,
