@@ -18,12 +18,14 @@
 namespace vtmu {
 
 // op "attention", param window: causal keys visible when p - w < s <= p,
-// non-causal ones when |p - s| <= w (w == 0: no window).
+// non-causal ones when |p - s| <= w (w == 0: no window).  SINKS: attention
+// sinks may be on (keys s < a.sinks escape the window).
+template <bool SINKS = true>
 __device__ __forceinline__ bool key_visible(const AttnDesc& a, int64_t p, int64_t s) {
     if (s < 0 || s >= a.S) return false;
     if (a.causal && s > p) return false;
     if (a.window > 0) {
-        if (s < a.sinks) return true;  // attention sinks escape the window
+        if (SINKS && s < a.sinks) return true;  // attention sinks escape the window
         if (a.causal) return s > p - a.window;
         int64_t d = p > s ? p - s : s - p;
         return d <= a.window;

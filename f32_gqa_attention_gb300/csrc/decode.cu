@@ -456,13 +456,18 @@ __global__ void __launch_bounds__(DecCfg<D, G>::THREADS, VTMU_DEC_CTAS_PER_SM)
 
     // ---- last CTA of this KV head merges the splits ----------------------
     // Release: the barrier orders every thread's partial stores before
-    // thread 0's gpu-scope fence, which publishes them before the ticket.
+    // thread 0's ticket, whose gpu-scope release publishes them.
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        const unsigned ticket = atomicAdd(&args.counters[blockIdx.z * a.Hk + kh], 1u);
+        // One acquire-release atomic: releases this CTA's partials (ordered
+        // before it by the barrier) and, for the last CTA, acquires the other
+        // splits' (measured ~0.9 us faster per step than two full fences).
+        unsigned ticket;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;"
+                     : "=r"(ticket)
+                     : "l"(&args.counters[blockIdx.z * a.Hk + kh])
+                     : "memory");
         const bool last = (ticket == (unsigned)(Hs - 1));
-        if (last) __threadfence();  // acquire: the other splits' partials
         s_is_last = last;
     }
     __syncthreads();
@@ -668,15 +673,20 @@ void decode_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodePlan* 
         splits = (num_sms * VTMU_DEC_CTAS_PER_SM) / units;
         if (splits < 1) splits = 1;
     }
-    // With a separate sink range the two ranges can take one split more.
-    const int max_splits = sink_end > 0 ? kMaxSplits - 1 : kMaxSplits;
-    if (splits > max_splits) splits = max_splits;
+    if (splits > kMaxSplits) splits = kMaxSplits;
     const int64_t min_rows = nr;
     int64_t per = (rows + splits - 1) / splits;
     if (per < min_rows) per = min_rows;
     per = (per + nr - 1) / nr * nr;
-    const int64_t n_sink = (sink_end + per - 1) / per;
+    // Each range takes whole splits: grow the split size until both fit the
+    // split count (a sink range of its own needs one split of its own).
+    int64_t n_sink = (sink_end + per - 1) / per;
     int64_t n = n_sink + (hi - lo + per - 1) / per;
+    while (n > splits && per < rows) {
+        per += nr;
+        n_sink = (sink_end + per - 1) / per;
+        n = n_sink + (hi - lo + per - 1) / per;
+    }
     if (n < 1) n = 1;
     plan->s_lo = lo;
     plan->s_end = hi;

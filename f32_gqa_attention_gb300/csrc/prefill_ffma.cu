@@ -71,7 +71,9 @@ __device__ __forceinline__ void stage_rows(float* sdst, int sld, const float* g,
     }
 }
 
-template <class C, bool VEC16>
+// SINKS: attention sinks are on (a separate instantiation keeps their tile
+// bookkeeping and mask test out of the common path).
+template <class C, bool VEC16, bool SINKS>
 __global__ void __launch_bounds__(C::THREADS, 1)
     prefill_ffma_kernel(const AttnDesc a, const AlibiTable alibi) {
     constexpr int BM = C::BM, BN = C::BN, TX = C::TX, TY = C::TY, RPT = C::RPT;
@@ -116,7 +118,8 @@ __global__ void __launch_bounds__(C::THREADS, 1)
     // limit).  Their tiles come first, or join the window's into one range
     // when the two touch.
     const int64_t sink_cap = a.causal ? s_hi + 1 : a.S;
-    const int64_t sink_end = a.sinks < sink_cap ? a.sinks : sink_cap;
+    const int64_t sinks = SINKS ? a.sinks : 0;
+    const int64_t sink_end = sinks < sink_cap ? sinks : sink_cap;
     const int64_t n_st = sink_end > 0 ? (sink_end + BN - 1) / BN : 0;
     int64_t n_sink = 0;
     if (n_st > 0 && n_st >= jt_begin) {
@@ -198,7 +201,7 @@ __global__ void __launch_bounds__(C::THREADS, 1)
             for (int j = 0; j < KPT; ++j) {
                 const int64_t s = n0 + tx + TX * j;
                 float x = -INFINITY;
-                if (t < a.T && key_visible(a, p, s)) {
+                if (t < a.T && key_visible<SINKS>(a, p, s)) {
                     const float bv = a.bias_kind ? bias_at(a, h, t, s) : 0.f;
                     x = score_log2(a, sacc[i][j], slope, s - p, bv);
                 }
@@ -297,9 +300,9 @@ using CfgA = PfCfg<128, 16, 128, 128>;  // headDim, vHeadDim <= 128
 using CfgB = PfCfg<128, 16, 192, 128>;  // headDim <= 192, vHeadDim <= 128
 using CfgC = PfCfg<64, 32, 256, 256>;   // anything up to 256
 
-template <class C, bool VEC16>
+template <class C, bool VEC16, bool SINKS>
 cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream) {
-    auto kern = prefill_ffma_kernel<C, VEC16>;
+    auto kern = prefill_ffma_kernel<C, VEC16, SINKS>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + C::BM - 1) / C::BM), (unsigned)a.H);
@@ -318,11 +321,16 @@ bool prefill_ffma_supported(const AttnDesc& a) {
 cudaError_t launch_prefill_ffma(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream) {
     const bool vec16 = (a.D % 4 == 0) && (a.Dv % 4 == 0) && aligned16(a.q) && aligned16(a.k) &&
                        aligned16(a.v) && aligned16(a.out);
-    if (a.D <= 128 && a.Dv <= 128)
-        return vec16 ? launch_cfg<CfgA, true>(a, alibi, stream) : launch_cfg<CfgA, false>(a, alibi, stream);
-    if (a.D <= 192 && a.Dv <= 128)
-        return vec16 ? launch_cfg<CfgB, true>(a, alibi, stream) : launch_cfg<CfgB, false>(a, alibi, stream);
-    return vec16 ? launch_cfg<CfgC, true>(a, alibi, stream) : launch_cfg<CfgC, false>(a, alibi, stream);
+    const bool sinks = a.sinks > 0;
+    auto pick = [&](auto cfg) -> cudaError_t {
+        using C = decltype(cfg);
+        if (sinks)
+            return vec16 ? launch_cfg<C, true, true>(a, alibi, stream) : launch_cfg<C, false, true>(a, alibi, stream);
+        return vec16 ? launch_cfg<C, true, false>(a, alibi, stream) : launch_cfg<C, false, false>(a, alibi, stream);
+    };
+    if (a.D <= 128 && a.Dv <= 128) return pick(CfgA{});
+    if (a.D <= 192 && a.Dv <= 128) return pick(CfgB{});
+    return pick(CfgC{});
 }
 
 }  // namespace vtmu
