@@ -5,7 +5,7 @@
 // query row t of head h as
 //     x = scale * q.k ; x = softcap * tanh(x / softcap) ; x += slope_h * (s - p)
 //     x += bias ; masked when s is not visible from p = posOffset + t
-// (softcap "before the mask", bias "added to the scores").  The kernels keep
+// (the cap ahead of masking, the bias an additive term).  The kernels keep
 // x in base-2 units (x * log2 e) so that the softmax uses exp2; the factor is
 // folded into the constants below, never applied as a separate pass.
 #pragma once

@@ -5,7 +5,7 @@
 // (vtmu.mpakt.dev/api/ops): kvHeads defaults to heads, vHeadDim to headDim,
 // causal to true, scale to 1/sqrt(headDim); softcap and window are off when
 // absent.  A request the build cannot serve is refused with the parameter or
-// feature named, as the catalog refuses a graph "with the feature named".
+// feature named, as the catalog refuses a graph by naming the missing feature.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>

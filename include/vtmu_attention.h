@@ -36,8 +36,8 @@
  *  - Host pointers are marked HOST and are read during the call only.
  *  - Every check runs on the host before any launch.  A failed check
  *    launches nothing and returns a status; vtmu_last_error() then names the
- *    offending parameter or feature (the catalog refuses a graph "with the
- *    feature named").
+ *    offending parameter or feature (the catalog, likewise, names the missing
+ *    feature when it refuses a graph).
  *  - A CUDA launch error returns VTMU_ERR_CUDA with the CUDA error string.
  */
 #ifndef VTMU_ATTENTION_H

@@ -11,8 +11,8 @@ defaults as the op catalog states them (vtmu.mpakt.dev/api/ops, op
 "attention"):
 
 * ``kvHeads`` defaults to ``heads``;
-* ``vHeadDim`` defaults to ``headDim`` ("value width per head when it
-  differs");
+* ``vHeadDim`` defaults to ``headDim`` (the page gives it only for a value
+  width that is not headDim);
 * ``causal`` defaults to true, ``posOffset`` to 0;
 * ``scale`` replaces 1/sqrt(headDim);
 * ``softcap`` and ``window`` are off when absent (or 0);

@@ -26,7 +26,7 @@
  * the caller's f32 arrays, outputs are double.
  *
  * The order scale -> softcap -> ALiBi -> bias -> mask follows the catalog's
- * feature table ("score softcapping before the mask") and its bias text
+ * feature table (the cap comes ahead of masking) and its bias text
  * (-1e9 masks, which only works if the bias is added after the cap).
  *
  * ALiBi slopes follow the geometric sequences BLOOM and MPT use
@@ -112,7 +112,7 @@ static void attend_row(const oracle_attn_desc* a, const float* q, const float* k
     for (int e = 0; e < Dv; ++e) o[e] = 0.0;
     if (m == -INFINITY) return; /* nothing visible: the row is zero */
 
-    /* op "softmax": max-subtracted so large logits do not overflow. */
+    /* op "softmax": the row maximum is subtracted first, which keeps exp finite. */
     double l = 0.0;
     for (int64_t s = 0; s < a->S; ++s) {
         if (!vis[s]) continue;
