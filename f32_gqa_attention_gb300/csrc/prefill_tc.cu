@@ -16,7 +16,8 @@
 //  * one CTA owns 128 query rows of one head (the MMA M); per key tile of
 //    BN = 64 keys, visited from the diagonal down:
 //      S_j  = Q K_j^T          (TMEM accumulator, M=128)
-//      P_j  = softmax part     (4 warps; thread = query row = TMEM lane)
+//      P_j  = softmax part     (4 warps; thread = query row = TMEM lane;
+//                               8 at headDim 256, two per lane quarter)
 //      O   += P_j V_j          (TMEM accumulator, M=128 x N=vHeadDim share)
 //  * operands: Q_hi and P_hi / P_lo in TMEM (A operand of the TS-form MMA),
 //    Q_lo in shared memory (A operand of the SS-form MMA of the third
@@ -40,10 +41,12 @@
 //    32 KB items (16 KB at headDim 192), in the order the MMAs consume them;
 //    warp 1 owns TMEM and one of its threads issues the score MMAs, one
 //    thread of warp 6 the P.V MMAs (at headDim 192 and 256 warp 1 issues
-//    both, consuming the ring in order); warps 2-5 split Q, run the
-//    tile-specialised epilogue and online softmax (base 2, O rescaled only
-//    when a row max grows by more than 2^8), write P hi/lo into TMEM and
-//    finally normalise and store O.
+//    both, consuming the ring in order); warps 2-5 (2-9 at headDim 256)
+//    split Q, run the tile-specialised epilogue and online softmax (base 2,
+//    O rescaled only when a row max grows by more than 2^8), write P hi/lo
+//    into TMEM and finally normalise and store O;
+//  * attention sinks are a template flag: with them, the key tiles holding
+//    keys before `sinks` follow the window's tiles (or join them).
 //
 // Every wait is bounded (tma_sync.cuh); a wait that gives up sets a bit of
 // g_tc_device_error and the kernel unwinds.
