@@ -43,6 +43,7 @@
 
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "launch_cache.h"
 #include "rope.cuh"
 #include "tma_sync.cuh"
 
@@ -569,15 +570,17 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // Row-major [rows, cols] f32 matrix, tiles of box_rows x box_cols.
 bool encode_rows(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int box_cols, int box_rows) {
-    auto fn = tensor_map_encoder();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return cached_tensor_map(map, base, rows, cols, box_cols, box_rows, 0, [&](CUtensorMap* m) {
+        auto fn = tensor_map_encoder();
+        if (!fn) return false;
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+        const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+        const cuuint32_t estr[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
 }
 
 template <int D, int G>
@@ -593,7 +596,7 @@ cudaError_t launch_cfg(const DecodeArgs& args, const AlibiTable& alibi, int n_rg
             return cudaErrorInvalidValue;
     }
     auto kern = decode_splitkv_kernel<D, G>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid = VTMU_DEC_KH_FAST ? dim3(a.Hk, args.splits, n_rg) : dim3(args.splits, a.Hk, n_rg);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(args, alibi, tmk, tmv);

@@ -20,6 +20,7 @@
 // distinct banks.
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "launch_cache.h"
 
 namespace vtmu {
 namespace {
@@ -303,7 +304,7 @@ using CfgC = PfCfg<64, 32, 256, 256>;   // anything up to 256
 template <class C, bool VEC16, bool SINKS>
 cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream) {
     auto kern = prefill_ffma_kernel<C, VEC16, SINKS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + C::BM - 1) / C::BM), (unsigned)a.H);
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi);

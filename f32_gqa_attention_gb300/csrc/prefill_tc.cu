@@ -58,6 +58,7 @@
 
 #include "attn_common.cuh"
 #include "kernels.h"
+#include "launch_cache.h"
 #include "tcgen05_ops.cuh"
 #include "tma_sync.cuh"
 
@@ -1034,15 +1035,17 @@ PFN_cuTensorMapEncodeTiled_v12000 encoder() {
 
 // [rows, cols] f32 row-major, 128-byte swizzled boxes of 32 columns x box_rows.
 bool encode_sw128(CUtensorMap* map, const float* base, int64_t rows, int64_t cols, int box_rows) {
-    auto fn = encoder();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
-    const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    return cached_tensor_map(map, base, rows, cols, 32, box_rows, 128, [&](CUtensorMap* m) {
+        auto fn = encoder();
+        if (!fn) return false;
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+        const cuuint32_t box[2] = {32, (cuuint32_t)box_rows};
+        const cuuint32_t estr[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
 }
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
@@ -1081,7 +1084,7 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
         !encode_sw128(&m_vlo, vtlo, (int64_t)a.Hk * DV, s_pad, C::DVC))
         return cudaErrorInvalidValue;
     auto kern = prefill_tc_kernel<D, DV, SINKS>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), (int)C::SMEM);
     if (e != cudaSuccess) return e;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi, bias_staged, m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo);
