@@ -33,7 +33,8 @@ VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREF
 
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
             "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",
-            "vtmu_device_error", "vtmu_decode_step")
+            "vtmu_device_error", "vtmu_decode_step", "vtmu_decode_step_host_workspace_size",
+            "vtmu_decode_step_host", "vtmu_rope_params_init", "vtmu_rope", "vtmu_decode_step_rope")
 NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 

@@ -282,3 +282,10 @@ def test_negative_sinks_are_refused(lib):
     p = vtmu.make_params(4, 4, heads=2, headDim=8, window=2, sinks=-1)
     e = _err(lambda: vtmu.vtmu_attention(FAKE, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0))
     assert e.status == vtmu.VTMU_ERR_INVALID and "sinks" in str(e)
+
+
+def test_binding_lists_every_entry_point(lib):
+    """The binding's EXPORTED names are exactly the entry points the header declares."""
+    hdr = open(os.path.join(ROOT, "include", "vtmu_attention.h")).read()
+    declared = set(re.findall(r"VTMU_API\s+[\w\s\*]+?\b(vtmu_\w+)\s*\(", hdr))
+    assert set(vtmu.EXPORTED) == declared
