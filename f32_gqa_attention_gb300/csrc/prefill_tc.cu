@@ -984,9 +984,26 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
 }
 
 // ---- pre-pass: tf32 hi/lo split of K, and of V transposed -------------------------
+// Elementwise and HBM-bound: 16-byte accesses when K is 16-byte aligned
+// (the workspace halves always are), so that each thread keeps 16 bytes in
+// flight per load instead of 4.
 __global__ void split_k_kernel(const float* __restrict__ k, float* __restrict__ khi, float* __restrict__ klo,
                                int64_t n) {
-    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    const int64_t i0 = blockIdx.x * (int64_t)blockDim.x + threadIdx.x;
+    if ((reinterpret_cast<uintptr_t>(k) & 15u) == 0 && (n & 3) == 0) {
+        const float4* k4 = reinterpret_cast<const float4*>(k);
+        float4* hi4 = reinterpret_cast<float4*>(khi);
+        float4* lo4 = reinterpret_cast<float4*>(klo);
+        for (int64_t i = i0; i < n / 4; i += stride) {
+            const float4 x = __ldg(k4 + i);
+            const float4 h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+            hi4[i] = h;
+            lo4[i] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+        }
+        return;
+    }
+    for (int64_t i = i0; i < n; i += stride) {
         const float x = __ldg(k + i);
         const float hi = tf32_hi(x);
         khi[i] = hi;
@@ -995,18 +1012,25 @@ __global__ void split_k_kernel(const float* __restrict__ k, float* __restrict__ 
 }
 
 // v [S, cols] -> vt_hi / vt_lo [cols, s_pad]; columns s >= S are zero.
+// Blocks of 32 x 8 threads; the four loads (and stores) of a thread are
+// independent, so they are all in flight at once.
+constexpr int kSplitVtRows = 8;
 __global__ void split_vt_kernel(const float* __restrict__ v, float* __restrict__ vthi, float* __restrict__ vtlo,
                                 int64_t S, int64_t s_pad, int cols) {
     __shared__ float tile[32][33];
     const int64_t s0 = (int64_t)blockIdx.x * 32;
     const int c0 = blockIdx.y * 32;
-    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+#pragma unroll
+    for (int rr = 0; rr < 32 / kSplitVtRows; ++rr) {
+        const int r = threadIdx.y + rr * kSplitVtRows;
         const int64_t s = s0 + r;
         const int c = c0 + threadIdx.x;
         tile[r][threadIdx.x] = (s < S && c < cols) ? __ldg(v + s * cols + c) : 0.f;
     }
     __syncthreads();
-    for (int r = threadIdx.y; r < 32; r += blockDim.y) {
+#pragma unroll
+    for (int rr = 0; rr < 32 / kSplitVtRows; ++rr) {
+        const int r = threadIdx.y + rr * kSplitVtRows;
         const int c = c0 + r;
         const int64_t s = s0 + threadIdx.x;
         if (c < cols && s < s_pad) {
@@ -1120,7 +1144,7 @@ cudaError_t launch_prefill_tc(const AttnDesc& a, const AlibiTable& alibi, void* 
     if (e != cudaSuccess) return e;
     const int cols = a.Hk * a.Dv;
     dim3 g2((unsigned)((L.s_pad + 31) / 32), (unsigned)((cols + 31) / 32));
-    split_vt_kernel<<<g2, dim3(32, 8), 0, stream>>>(a.v, vthi, vtlo, a.S, L.s_pad, cols);
+    split_vt_kernel<<<g2, dim3(32, kSplitVtRows), 0, stream>>>(a.v, vthi, vtlo, a.S, L.s_pad, cols);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
 #define VTMU_TC(D_, DV_)                                                                                     \
