@@ -1,8 +1,14 @@
 """Benchmark of the f32 attention library on one GB300 (or N replicas).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vtmu|reference]
-                    [--workload gqa_decode|gqa_prefill|swa_softcap_prefill|
-                                latent_bias_prefill|alibi_prefill|tiny_prefill]
+                    [--workload NAME] [--kernel auto|tc|ffma] [--no-cpu-baseline]
+
+Workloads (seeded_inputs.WORKLOADS): gqa_decode (default), gqa_decode_rope
+(the same step with the rotary embedding fused in), gqa_spec_decode (4 query
+rows), gqa_decode_sinks (a window with attention sinks), gqa_prefill,
+swa_softcap_prefill, swa_sinks_prefill, latent_bias_prefill, alibi_prefill,
+tiny_prefill.  `--kernel ffma` forces the FFMA prefill (for a decode workload:
+the step as cache_writes + the FFMA prefill), `--kernel tc` the tensor cores.
 
 Default workload: the GQA decode step (Llama-3-8B shape): cache_write of one
 new K row and one new V row at position 32767 into [32768, 8*128] f32 caches,
