@@ -289,3 +289,10 @@ def test_binding_lists_every_entry_point(lib):
     hdr = open(os.path.join(ROOT, "include", "vtmu_attention.h")).read()
     declared = set(re.findall(r"VTMU_API\s+[\w\s\*]+?\b(vtmu_\w+)\s*\(", hdr))
     assert set(vtmu.EXPORTED) == declared
+
+
+@host_only
+def test_noalloc_needs_one_query_row(lib):
+    p = vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "T must be 1" in str(e)
