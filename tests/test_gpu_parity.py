@@ -57,8 +57,30 @@ def test_gqa_decode_workload():
     assert err <= TOL, err
 
 
+@pytest.mark.parametrize("name", ["gqa_spec_decode", "gqa_decode_sinks"])
+def test_decode_step_workloads(name):
+    """The 4-row speculative step and the windowed step with sinks at full size, as the
+    bench runs them: one fused vtmu_decode_step (cache_write of the new rows + attention)."""
+    w = si.WORKLOADS[name]
+    x = si.workload_inputs(name)
+    H, Hk, D, off, R = w["heads"], w["kvHeads"], w["headDim"], w["offset"], w.get("rows", 1)
+    Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
+    out = vtmu.decode_step(Kc, Vc, to_dev(x["k_new"]), to_dev(x["v_new"]), off, to_dev(x["q"]), heads=H,
+                           headDim=D, kvHeads=Hk, **w["params"])
+    torch.cuda.synchronize()
+    oracle.cache_write(x["kc"], x["k_new"], off)
+    oracle.cache_write(x["vc"], x["v_new"], off)
+    assert torch.equal(Kc.cpu(), torch.from_numpy(x["kc"]))
+    assert torch.equal(Vc.cpu(), torch.from_numpy(x["vc"]))
+    assert out.shape == (R, H * D)
+    ref = oracle.attention(x["q"], x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
+    err = max_err(out.cpu().numpy(), ref)
+    assert err <= TOL, err
+    assert vtmu.vtmu_device_error() == 0
+
+
 @pytest.mark.parametrize("name", ["gqa_prefill", "swa_softcap_prefill", "latent_bias_prefill",
-                                  "alibi_prefill"])
+                                  "alibi_prefill", "swa_sinks_prefill"])
 def test_prefill_workload_sampled_rows(name):
     """Full-size prefill on the GPU; the oracle recomputes sampled (t, h) rows."""
     w = si.WORKLOADS[name]
