@@ -2,6 +2,7 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vtmu|reference]
                     [--workload NAME] [--kernel auto|tc|ffma] [--no-cpu-baseline]
+                    [--no-prefill] [--cpu-budget SEC] [--prefill-cpu-budget SEC]
 
 Workloads (seeded_inputs.WORKLOADS): gqa_decode (default), gqa_decode_rope
 (the same step with the rotary embedding fused in), gqa_spec_decode (4 query
@@ -21,8 +22,14 @@ from HBM (working set 512 MiB > the 126 MiB L2).
 
 One JSON line is printed by rank 0.  `value` is whole-job throughput in the
 workload's unit (decode: algorithmic GB/s; prefill: algorithmic TFLOP/s).
-`--impl reference` times the CPU oracle on the host cores instead, on a
-bounded sample of the same workload.
+After a decode workload the line also carries `prefill`: one entry per
+prefill workload (gqa_prefill, swa_softcap_prefill, latent_bias_prefill,
+alibi_prefill) with its step and kernel time, TFLOP/s, its tensor-pipe
+roofline against two ceilings (the measured bf16 rate scaled to 3xTF32, and
+the measured kind::tf32 rate per SM at the sampled SM clock), end-to-end
+TFLOP/s from host buffers and a bounded oracle sample; `--no-prefill` leaves
+them out.  `--impl reference` times the CPU oracle on the host cores instead,
+on a bounded sample of the same workload.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
 op has no exchange step); ranks meet at a barrier around the timed region
@@ -123,34 +130,90 @@ def load_peaks():
                 "sm_max_mhz": 2070.0}, "fallback"
 
 
-def profile_traffic(kernel_tag):
-    """DRAM bytes per launch from a committed ncu summary, when the kernel
-    source it was taken on is unchanged (sha256 recorded in the summary)."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
-    src = os.path.join(ROOT, "f32_gqa_attention_gb300", "csrc", f"{kernel_tag.split('__')[0]}.cu")
+PREFILL_SET = ("gqa_prefill", "swa_softcap_prefill", "latent_bias_prefill", "alibi_prefill")
+# kind::tf32 MMA throughput per SM measured on this GPU (one CTA, M = 128,
+# N = 128, K = 8 every 64 cycles): the tensor pipe's clock-scaled ceiling.
+TF32_FLOP_PER_CYCLE_SM = 4096
+
+
+def kernel_source_hash(kernel_tag):
+    """sha256 over a kernel's .cu file and every library header it includes
+    (transitively), in a fixed order: a committed ncu summary is trusted only
+    while this matches the hash it records."""
+    csrc = os.path.join(ROOT, "f32_gqa_attention_gb300", "csrc")
+    seen, order = set(), []
+
+    def visit(fname):
+        if fname in seen:
+            return
+        seen.add(fname)
+        path = os.path.join(csrc, fname)
+        data = open(path, "rb").read()
+        order.append((fname, data))
+        for inc in re.findall(rb'#include\s+"([^"]+)"', data):
+            inc = inc.decode()
+            if os.path.exists(os.path.join(csrc, inc)):
+                visit(inc)
+
     try:
-        text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        visit(kernel_tag + ".cu")
     except OSError:
         return None
-    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    h = hashlib.sha256()
+    first, rest = order[0], sorted(order[1:])
+    for fname, data in [first] + rest:
+        h.update(fname.encode() + b"\0" + data + b"\0")
+    return h.hexdigest()
+
+
+def profile_info(profile_name):
+    """Figures from a committed ncu summary `profiles/<kernel>__<workload>.md`
+    (traffic per launch, tensor-pipe busy %), when the kernel source it was
+    taken on is unchanged; {} otherwise."""
+    path = os.path.join(ROOT, "profiles", f"{profile_name}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return {}
     s = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
-    if not m or not s or s.group(1) != sha:
-        return None
-    return int(m.group(1))
+    if not s or s.group(1) != kernel_source_hash(profile_name.split("__")[0]):
+        return {}
+    info = {}
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9]+)", text)
+    if m:
+        info["traffic"] = int(m.group(1))
+    m = re.search(r"tensor_pipe_active_pct:\s*([0-9.]+)", text)
+    if m:
+        info["tensor_pipe_active_pct"] = float(m.group(1))
+    return info
+
+
+def profile_traffic(profile_name):
+    return profile_info(profile_name).get("traffic")
+
+
+def tensor_ceilings(peaks, sm_mhz):
+    """The 3xTF32 ceilings of the tensor pipe, in TFLOP/s: (measured bf16
+    burst x 1.1/2.25 (tf32/bf16 nominal) / 3, measured kind::tf32 rate per SM
+    x SMs x SM clock / 3).  Three tf32 products make one f32 product."""
+    bf16_scaled = float(peaks["bf16_tflops"]) * (1.1 / 2.25) / 3.0
+    clk = SMS * TF32_FLOP_PER_CYCLE_SM * float(sm_mhz) * 1e6 / 3.0 / 1e12
+    return bf16_scaled, clk
 
 
 # -------------------------------------------------------------------- clocks
 class ClockSampler:
-    """nvidia-smi clock/throttle samples every 200 ms while running."""
+    """nvidia-smi clock/throttle samples every 200 ms while running; summaries
+    for any wall-clock window of the run."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
     def __init__(self, gpu_index):
         self.gpu = gpu_index
         self.proc = None
-        self.t0 = self.t1 = None
+        self.rows = []
 
     def start(self):
         try:
@@ -161,35 +224,30 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
-    def mark_start(self):
-        self.t0 = time.time()
-
-    def mark_end(self):
-        self.t1 = time.time()
-
     def stop(self):
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+            return
         time.sleep(0.25)
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
-        rows = []
+        self.proc = None
         for ln in out.splitlines():
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 10:
                 continue
             try:
                 ts = time.mktime(time.strptime(parts[0].split(".")[0], "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
+                self.rows.append((ts, float(parts[2]), float(parts[3]), parts[6:10]))
             except ValueError:
                 continue
-        # samples inside the loaded window (second resolution timestamps)
-        lo, hi = (self.t0 or 0) - 1, (self.t1 or time.time()) + 1
-        sel = [r for r in rows if lo <= r[0] <= hi] or rows[-3:]
-        if not sel:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
+
+    def summary(self, t0, t1):
+        """Median SM clock, max clock and active throttle reasons of the
+        samples inside [t0, t1] (timestamps have one-second resolution)."""
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        sel = [r for r in self.rows if t0 - 1 <= r[0] <= t1 + 1] or self.rows[-3:]
+        reasons = sorted({self.REASONS[i] for r in sel for i, v in enumerate(r[3]) if v.lower() == "active"})
         return {"sm_mhz": statistics.median(r[1] for r in sel), "sm_max_mhz": max(r[2] for r in sel),
                 "reasons": reasons, "samples": len(sel)}
 
@@ -216,6 +274,20 @@ def barrier(world):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
+
+
+def workload_config(name, world):
+    """The `config` object of a JSON line: the workload's shape and params,
+    the replica count and how L2 is kept out of the timing (the same for both
+    arms)."""
+    w = si.WORKLOADS[name]
+    l2 = ("inputs > L2: two 256 MiB K/V cache sets alternate between steps" if w["kind"] == "decode"
+          else "L2 flushed between timed steps (256 MiB write, outside the timed events)")
+    return {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
+            "parallelism": f"replicas x{world}", "l2": l2}
+
+
+DATA = "synthetic (seeded SplitMix64 / Box-Muller, N(0,1) inputs of the workload's shapes)"
 
 
 # ------------------------------------------------------------- oracle timing
@@ -289,185 +361,248 @@ def time_oracle(name, w, budget_s=12.0, min_samples=2, x=None):
 
 
 # ------------------------------------------------------------- the GPU arm
-def run_vtmu(args, rank, world, local):
-    import torch
-    import f32_gqa_attention_gb300 as vtmu
-    vtmu.load_library()
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    name = args.workload
-    w = si.WORKLOADS[name]
-    peaks, peak_kind = load_peaks()
-    stream = torch.cuda.Stream(device=dev)
-    st = stream.cuda_stream
-    launches_per_step = 0
-    x = si.workload_inputs(name)
-    rope = None
+class Ctx:
+    """What every measurement of one run shares: torch, the library, the
+    device and stream, the peaks, the clock sampler, rank and world."""
 
-    if w["kind"] == "decode":
-        H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
-        R = w.get("rows", 1)  # query rows = new cache rows of the step
-        kv_bytes, step_bytes = decode_bytes(w)
-        sessions = []
-        with torch.cuda.stream(stream):
-            for sidx in range(2):
-                sessions.append(dict(Kc=torch.from_numpy(x["kc"]).to(dev), Vc=torch.from_numpy(x["vc"]).to(dev)))
-            q = torch.from_numpy(x["q"]).to(dev)
-            kn = torch.from_numpy(x["k_new"]).to(dev)
-            vn = torch.from_numpy(x["v_new"]).to(dev)
-            out = torch.empty((R, H * D), dtype=torch.float32, device=dev)
-        # --kernel ffma: the same step through the FFMA prefill (cache_writes
-        # and attention as three launches), for comparison.
-        forced = vtmu.VTMU_KERNEL_PREFILL_FFMA if args.kernel == "ffma" else vtmu.VTMU_KERNEL_AUTO
-        p = vtmu.make_params(R, off + R, heads=H, headDim=D, kvHeads=Hk, kernel=forced, **w["params"])
-        ws_bytes = vtmu.vtmu_attention_workspace_size(p)
-        ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
-        width = Hk * D
-        launches_per_step = 1
-        rope = vtmu.make_rope_params(headDim=D, **w["rope"]) if w.get("rope") else None
-        if rope is not None:
-            with torch.cuda.stream(stream):
-                q_rot, kn_rot = torch.empty_like(q), torch.empty_like(kn)
+    def __init__(self, torch, vtmu, dev, stream, peaks, peak_kind, sampler, rank, world, args):
+        self.torch, self.vtmu, self.dev, self.stream = torch, vtmu, dev, stream
+        self.st = stream.cuda_stream
+        self.peaks, self.peak_kind, self.sampler = peaks, peak_kind, sampler
+        self.rank, self.world, self.args = rank, world, args
 
-        def step(i, ev=None):
-            # One fused launch: both cache_writes and the attention (and the
-            # rotary embedding of q and the new key row).
-            s = sessions[i % 2]
-            if ev is not None:
-                ev[0].record(stream)
-            if rope is None:
-                vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, ws, ws_bytes, st)
-            else:
-                vtmu.vtmu_decode_step_rope(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, rope, ws,
-                                           ws_bytes, st)
-            if ev is not None:
-                ev[1].record(stream)
 
-        def unfused_step(i):
-            s = sessions[i % 2]
-            qq, kk = q, kn
-            if rope is not None:
-                vtmu.vtmu_rope(q, q_rot, 1, H, w["params"]["posOffset"], rope, st)
-                vtmu.vtmu_rope(kn, kn_rot, 1, Hk, off, rope, st)
-                qq, kk = q_rot, kn_rot
-            vtmu.vtmu_cache_write(s["Kc"], off + R, width, kk, R, off, st)
-            vtmu.vtmu_cache_write(s["Vc"], off + R, width, vn, R, off, st)
-            vtmu.vtmu_attention(qq, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
-
-        work_per_step, unit = step_bytes / 1e9, "GB/s"
-        kernel_tag, kernel_work, kernel_unit = "decode", step_bytes, "GB/s"
-        if args.kernel == "ffma":
-            kernel_tag, launches_per_step = "prefill_ffma", 3
-        bound, peak = "hbm", float(peaks["hbm_gbs"])
-        peak_note = peak_kind
-        flush = None
-        l2_note = "inputs > L2: two 256 MiB K/V cache sets alternate between steps"
-    else:
-        H, Hk, D = w["heads"], w["kvHeads"], w["headDim"]
-        Dv = w.get("vHeadDim") or D
-        T, S = w["T"], w["S"]
-        with torch.cuda.stream(stream):
-            q = torch.from_numpy(x["q"]).to(dev)
-            k = torch.from_numpy(x["k"]).to(dev)
-            v = torch.from_numpy(x["v"]).to(dev)
-            b = torch.from_numpy(x["bias"]).to(dev) if "bias" in x else None
-            out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
-            flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-        bias_kind = vtmu.VTMU_BIAS_NONE if b is None else (vtmu.VTMU_BIAS_TS if b.dim() == 2 else vtmu.VTMU_BIAS_HTS)
-        tc_ok = ((D == Dv and D in (32, 64, 96, 128, 256)) or (D, Dv) == (192, 128)) and T >= 64
-        use_tc = tc_ok if args.kernel == "auto" else args.kernel == "tc"
-        kernel = vtmu.VTMU_KERNEL_PREFILL_TF32X3 if use_tc else vtmu.VTMU_KERNEL_PREFILL_FFMA
-        p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, vHeadDim=w.get("vHeadDim"),
-                             bias_kind=bias_kind, kernel=kernel, **w["params"])
-        ws_bytes = vtmu.vtmu_attention_workspace_size(p)
-        ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-        # one launch per step (+2 split passes of K and V for the tensor-core kernel)
-        launches_per_step = 3 if use_tc else 1
-
-        def step(i, ev=None):
-            if ev is not None:
-                ev[0].record(stream)
-            vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
-            if ev is not None:
-                ev[1].record(stream)
-
-        unfused_step = None
-
-        flops = prefill_flops(w)
-        work_per_step, unit = flops / 1e12, "TFLOP/s"
-        kernel_work, kernel_unit = flops / 1e12, "TFLOP/s"
-        if use_tc:
-            # 3xTF32: three tf32 products per f32 product on the tensor pipe.
-            kernel_tag, bound = "prefill_tc", "tensor"
-            peak = float(peaks["bf16_tflops"]) * (1.1 / 2.25) / 3.0
-            peak_note = "measured bf16 burst x 1.1/2.25 (tf32/bf16 nominal) / 3 (3xTF32 products)"
-        else:
-            clk = float(peaks.get("sm_max_mhz", 2070.0))
-            kernel_tag, bound = "prefill_ffma", "alu"
-            peak = SMS * FP32_LANES_PER_SM * 2 * clk * 1e6 / 1e12
-            peak_note = "derived: 152 SMs x 128 FP32 lanes x 2 x max SM clock"
-        l2_note = "L2 flushed between timed steps (256 MiB write, outside the timed events)"
-
-    sampler = ClockSampler(local)
-    if rank == 0:
-        sampler.start()
-        time.sleep(0.6)
-    sampler.mark_start()
-    for i in range(args.warmup):
+def timed_loop(ctx, step, steps, warmup, flush=None):
+    """W untimed steps, then K timed steps between a barrier and a device
+    synchronisation on both sides.  Returns (ms per step, ms per step of the
+    events `step` records around its dominant launch, wall-clock window).
+    With `flush`, L2 is overwritten after every step outside the events and
+    the step time is the sum of the steps; without, it is the span of the
+    whole run, gaps between launches included."""
+    torch, dev, stream = ctx.torch, ctx.dev, ctx.stream
+    for i in range(warmup):
         step(i)
         if flush is not None:
-            flush.zero_()
+            with torch.cuda.stream(stream):
+                flush.zero_()
     torch.cuda.synchronize(dev)
-
-    # ---- timed region: device time per step and per dominant kernel ----------
-    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    barrier(world)
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    sev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(ctx.world)
     torch.cuda.synchronize(dev)
-    for i in range(args.steps):
+    t0 = time.time()
+    for i in range(steps):
         if flush is not None or i == 0:
             sev[i][0].record(stream)
         step(i, kev[i])
-        if flush is not None or i == args.steps - 1:
+        if flush is not None or i == steps - 1:
             sev[i][1].record(stream)
         if flush is not None:
             with torch.cuda.stream(stream):
                 flush.zero_()
     torch.cuda.synchronize(dev)
-    barrier(world)
-    sampler.mark_end()
+    barrier(ctx.world)
+    t1 = time.time()
     if flush is None:
-        # No flush between steps: the whole run, gaps between launches included.
-        step_ms = sev[0][0].elapsed_time(sev[-1][1]) / args.steps
+        step_ms = sev[0][0].elapsed_time(sev[-1][1]) / steps
     else:
-        # L2 flushed between steps: sum of the steps, flushes excluded.
-        step_ms = sum(a.elapsed_time(b) for a, b in sev) / args.steps
-    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / args.steps
-    step_ms = max_over_ranks(step_ms, world)
+        step_ms = sum(a.elapsed_time(b) for a, b in sev) / steps
+    kern_ms = sum(a.elapsed_time(b) for a, b in kev) / steps
+    return max_over_ranks(step_ms, ctx.world), max_over_ranks(kern_ms, ctx.world), (t0, t1)
 
-    # The same decode step as three separate launches, for comparison.
-    unfused_ms = None
-    if unfused_step is not None:
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        for i in range(3):
-            unfused_step(i)
-        e0.record(stream)
-        for i in range(args.steps):
-            unfused_step(i)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        unfused_ms = e0.elapsed_time(e1) / args.steps
+
+def measure_prefill(ctx, name, steps, warmup, kernel_arg="auto", cpu_budget=0.0, e2e_steps=None):
+    """One prefill workload: W + K steps of vtmu_attention with L2 flushed
+    between steps, the same call end to end from pinned host buffers, and a
+    bounded oracle sample on the host cores (rank 0, cpu_budget > 0).
+    Returns the measurements; finish_prefill() adds clocks and rooflines."""
+    torch, vtmu, dev, stream, st = ctx.torch, ctx.vtmu, ctx.dev, ctx.stream, ctx.st
+    w = si.WORKLOADS[name]
+    x = si.workload_inputs(name)
+    H, Hk, D = w["heads"], w["kvHeads"], w["headDim"]
+    Dv = w.get("vHeadDim") or D
+    T, S = w["T"], w["S"]
+    with torch.cuda.stream(stream):
+        q = torch.from_numpy(x["q"]).to(dev)
+        k = torch.from_numpy(x["k"]).to(dev)
+        v = torch.from_numpy(x["v"]).to(dev)
+        b = torch.from_numpy(x["bias"]).to(dev) if "bias" in x else None
+        out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    bias_kind = vtmu.VTMU_BIAS_NONE if b is None else (vtmu.VTMU_BIAS_TS if b.dim() == 2 else vtmu.VTMU_BIAS_HTS)
+    tc_ok = ((D == Dv and D in (32, 64, 96, 128, 256)) or (D, Dv) == (192, 128)) and T >= 64
+    use_tc = tc_ok if kernel_arg == "auto" else kernel_arg == "tc"
+    kernel = vtmu.VTMU_KERNEL_PREFILL_TF32X3 if use_tc else vtmu.VTMU_KERNEL_PREFILL_FFMA
+    p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, vHeadDim=w.get("vHeadDim"),
+                         bias_kind=bias_kind, kernel=kernel, **w["params"])
+    ws_bytes = vtmu.vtmu_attention_workspace_size(p)
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
+        if ev is not None:
+            ev[1].record(stream)
+
+    step_ms, kern_ms, window = timed_loop(ctx, step, steps, warmup, flush)
+
+    # End to end through the public API: inputs copied in from pinned host
+    # memory, the call, the output copied back, a host sync.
+    qh = torch.from_numpy(x["q"]).pin_memory()
+    kh = torch.from_numpy(x["k"]).pin_memory()
+    vh = torch.from_numpy(x["v"]).pin_memory()
+    bh = torch.from_numpy(x["bias"]).pin_memory() if "bias" in x else None
+    outh = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q.copy_(qh, non_blocking=True)
+            k.copy_(kh, non_blocking=True)
+            v.copy_(vh, non_blocking=True)
+            if bh is not None:
+                b.copy_(bh, non_blocking=True)
+        vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
+        with torch.cuda.stream(stream):
+            outh.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    flops = prefill_flops(w)
+    e2e_step()
+    n_e2e = e2e_steps or max(3, min(steps, 200))
+    barrier(ctx.world)
+    t0 = time.perf_counter()
+    for _ in range(n_e2e):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
+    h2d = (qh.numel() + kh.numel() + vh.numel() + (bh.numel() if bh is not None else 0)) * 4
+    e2e = {"value": round(flops / 1e12 * ctx.world / e2e_s, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": outh.numel() * 4, "steps": n_e2e}
+    del q, k, v, b, out, flush, ws, qh, kh, vh, bh, outh
+    torch.cuda.empty_cache()
+
+    cpu = None
+    if ctx.rank == 0 and cpu_budget > 0:
+        val, sample, cores = time_oracle(name, w, budget_s=cpu_budget, min_samples=1, x=x)
+        cpu = {"value": round(val, 5), "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": sample}
+    return {"workload": name, "kernel": "prefill_tc" if use_tc else "prefill_ffma", "flops": flops,
+            "steps": steps, "warmup": warmup, "ms_per_step": step_ms, "kernel_ms": kern_ms,
+            "gpu_launches": (3 if use_tc else 1) * steps, "e2e": e2e, "cpu_baseline": cpu, "_window": window}
+
+
+def prefill_roofline(ctx, res, clocks):
+    """The dominant kernel's roofline: algorithmic FLOPs / kernel time against
+    the 3xTF32 tensor ceilings (both ways) or the FP32 FMA peak."""
+    peaks = ctx.peaks
+    name, kern_ms = res["workload"], res["kernel_ms"]
+    achieved = res["flops"] / 1e12 / (kern_ms / 1e3)
+    sm = clocks.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    prof = profile_info(f"{res['kernel']}__{name}")
+    if res["kernel"] == "prefill_tc":
+        bf16_scaled, clk = tensor_ceilings(peaks, sm)
+        return {"bound": "tensor", "kernel": "prefill_tc", "achieved": round(achieved, 3),
+                "peak": round(bf16_scaled, 1), "unit": "TFLOP/s", "frac": round(achieved / bf16_scaled, 4),
+                "peak_source": (f"{ctx.peak_kind} bf16 burst x 1.1/2.25 (tf32/bf16 nominal) / 3 (3xTF32 products)"),
+                "peak_clock_scaled": round(clk, 1), "frac_clock_scaled": round(achieved / clk, 4),
+                "peak_clock_scaled_source": (f"kind::tf32 {TF32_FLOP_PER_CYCLE_SM} FLOP/cycle/SM (measured) x "
+                                             f"{SMS} SMs x {sm:.0f} MHz (sampled) / 3"),
+                "tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct"),
+                "traffic": prof.get("traffic"), "kernel_ms": round(kern_ms, 5)}
+    peak = SMS * FP32_LANES_PER_SM * 2 * sm * 1e6 / 1e12
+    return {"bound": "alu", "kernel": "prefill_ffma", "achieved": round(achieved, 3), "peak": round(peak, 1),
+            "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+            "peak_source": f"derived: {SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm:.0f} MHz (sampled)",
+            "traffic": prof.get("traffic"), "kernel_ms": round(kern_ms, 5)}
+
+
+def finish_prefill(ctx, res):
+    """A prefill entry of the JSON line, once the clock samples are in."""
+    clocks = ctx.sampler.summary(*res.pop("_window"))
+    flops = res["flops"]
+    return {"workload": res["workload"], "config": workload_config(res["workload"], ctx.world),
+            "value": round(flops * ctx.world / 1e12 / (res["ms_per_step"] / 1e3), 3), "unit": "TFLOP/s",
+            "ms_per_step": round(res["ms_per_step"], 5), "kernel_ms": round(res["kernel_ms"], 5),
+            "algorithmic_flop": flops, "steps": res["steps"], "warmup": res["warmup"],
+            "roofline": prefill_roofline(ctx, res, clocks), "e2e": res["e2e"], "cpu_baseline": res["cpu_baseline"],
+            "gpu_launches": res["gpu_launches"], "clocks": clocks}
+
+
+def measure_decode(ctx, name):
+    """The decode step of a decode workload: W + K fused steps alternating two
+    cache sets (each step's K/V come from HBM), the same step as separate
+    launches, and end to end from host buffers."""
+    torch, vtmu, dev, stream, st, args = ctx.torch, ctx.vtmu, ctx.dev, ctx.stream, ctx.st, ctx.args
+    w = si.WORKLOADS[name]
+    x = si.workload_inputs(name)
+    H, Hk, D, off = w["heads"], w["kvHeads"], w["headDim"], w["offset"]
+    R = w.get("rows", 1)  # query rows = new cache rows of the step
+    kv_bytes, step_bytes = decode_bytes(w)
+    sessions = []
+    with torch.cuda.stream(stream):
+        for _ in range(2):
+            sessions.append(dict(Kc=torch.from_numpy(x["kc"]).to(dev), Vc=torch.from_numpy(x["vc"]).to(dev)))
+        q = torch.from_numpy(x["q"]).to(dev)
+        kn = torch.from_numpy(x["k_new"]).to(dev)
+        vn = torch.from_numpy(x["v_new"]).to(dev)
+        out = torch.empty((R, H * D), dtype=torch.float32, device=dev)
+    # --kernel ffma: the same step through the FFMA prefill (cache_writes
+    # and attention as three launches), for comparison.
+    forced = vtmu.VTMU_KERNEL_PREFILL_FFMA if args.kernel == "ffma" else vtmu.VTMU_KERNEL_AUTO
+    p = vtmu.make_params(R, off + R, heads=H, headDim=D, kvHeads=Hk, kernel=forced, **w["params"])
+    ws_bytes = vtmu.vtmu_attention_workspace_size(p)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    width = Hk * D
+    rope = vtmu.make_rope_params(headDim=D, **w["rope"]) if w.get("rope") else None
+    if rope is not None:
+        with torch.cuda.stream(stream):
+            q_rot, kn_rot = torch.empty_like(q), torch.empty_like(kn)
+
+    def step(i, ev=None):
+        # One fused launch: both cache_writes and the attention (and the
+        # rotary embedding of q and the new key row).
+        s = sessions[i % 2]
+        if ev is not None:
+            ev[0].record(stream)
+        if rope is None:
+            vtmu.vtmu_decode_step(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, ws, ws_bytes, st)
+        else:
+            vtmu.vtmu_decode_step_rope(s["Kc"], s["Vc"], off + R, kn, vn, R, off, q, None, out, p, rope, ws,
+                                       ws_bytes, st)
+        if ev is not None:
+            ev[1].record(stream)
+
+    def unfused_step(i):
+        s = sessions[i % 2]
+        qq, kk = q, kn
+        if rope is not None:
+            vtmu.vtmu_rope(q, q_rot, 1, H, w["params"]["posOffset"], rope, st)
+            vtmu.vtmu_rope(kn, kn_rot, 1, Hk, off, rope, st)
+            qq, kk = q_rot, kn_rot
+        vtmu.vtmu_cache_write(s["Kc"], off + R, width, kk, R, off, st)
+        vtmu.vtmu_cache_write(s["Vc"], off + R, width, vn, R, off, st)
+        vtmu.vtmu_attention(qq, s["Kc"], s["Vc"], None, out, p, ws, ws_bytes, st)
+
+    step_ms, kern_ms, window = timed_loop(ctx, step, args.steps, args.warmup)
+
+    # The same decode step as separate launches, for comparison.
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    for i in range(3):
+        unfused_step(i)
+    e0.record(stream)
+    for i in range(args.steps):
+        unfused_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    unfused_ms = e0.elapsed_time(e1) / args.steps
 
     # ---- end to end through the public API with host buffers ----------------
-    e2e = None
+    qh = torch.from_numpy(x["q"]).pin_memory()
+    knh = torch.from_numpy(x["k_new"]).pin_memory()
+    vnh = torch.from_numpy(x["v_new"]).pin_memory()
+    outh = torch.empty((R, H * D), dtype=torch.float32).pin_memory()
     if rope is not None:
         # The rotary decode step has no host-buffer entry point: pinned copies
         # in, the fused step, the output back, a host sync.
-        qh = torch.from_numpy(x["q"]).pin_memory()
-        knh = torch.from_numpy(x["k_new"]).pin_memory()
-        vnh = torch.from_numpy(x["v_new"]).pin_memory()
-        outh = torch.empty((R, H * D), dtype=torch.float32).pin_memory()
-
         def e2e_step(i):
             with torch.cuda.stream(stream):
                 q.copy_(qh, non_blocking=True)
@@ -477,15 +612,7 @@ def run_vtmu(args, rank, world, local):
             with torch.cuda.stream(stream):
                 outh.copy_(out, non_blocking=True)
             stream.synchronize()
-
-        h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
-        d2h = outh.numel() * 4
-    elif w["kind"] == "decode":
-        qh = torch.from_numpy(x["q"]).pin_memory()
-        knh = torch.from_numpy(x["k_new"]).pin_memory()
-        vnh = torch.from_numpy(x["v_new"]).pin_memory()
-        outh = torch.empty((R, H * D), dtype=torch.float32).pin_memory()
-
+    else:
         # The host-buffer decode step of the C ABI: it copies q and the new
         # rows in, runs the fused step, copies the output row back and waits.
         hws_bytes = vtmu.vtmu_decode_step_host_workspace_size(p, R)
@@ -496,69 +623,83 @@ def run_vtmu(args, rank, world, local):
             vtmu.vtmu_decode_step_host(s["Kc"], s["Vc"], off + R, knh, vnh, R, off, qh, None, outh, p, hws,
                                        hws_bytes, st)
 
-        h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
-        d2h = outh.numel() * 4
-    else:
-        qh = torch.from_numpy(x["q"]).pin_memory()
-        kh_ = torch.from_numpy(x["k"]).pin_memory()
-        vh = torch.from_numpy(x["v"]).pin_memory()
-        bh = torch.from_numpy(x["bias"]).pin_memory() if "bias" in x else None
-        outh = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
-
-        def e2e_step(i):
-            with torch.cuda.stream(stream):
-                q.copy_(qh, non_blocking=True)
-                k.copy_(kh_, non_blocking=True)
-                v.copy_(vh, non_blocking=True)
-                if bh is not None:
-                    b.copy_(bh, non_blocking=True)
-            vtmu.vtmu_attention(q, k, v, b, out, p, ws, ws_bytes, st)
-            with torch.cuda.stream(stream):
-                outh.copy_(out, non_blocking=True)
-            stream.synchronize()
-
-        h2d = (qh.numel() + kh_.numel() + vh.numel() + (bh.numel() if bh is not None else 0)) * 4
-        d2h = outh.numel() * 4
+    h2d = (qh.numel() + knh.numel() + vnh.numel()) * 4
+    d2h = outh.numel() * 4
     e2e_step(0)
     n_e2e = max(3, min(args.steps, 200))
-    barrier(world)
+    barrier(ctx.world)
     t0 = time.perf_counter()
     for i in range(n_e2e):
         e2e_step(i)
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, world)
-    e2e = {"value": round(work_per_step * world / e2e_s, 3), "unit": unit, "h2d_bytes_per_step": h2d,
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
+    e2e = {"value": round(step_bytes / 1e9 * ctx.world / e2e_s, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": n_e2e}
+    del sessions, q, kn, vn, out, ws
+    torch.cuda.empty_cache()
+    kernel_tag = "prefill_ffma" if args.kernel == "ffma" else "decode"
+    return {"workload": name, "x": x, "w": w, "step_bytes": step_bytes, "step_ms": step_ms, "kernel_ms": kern_ms,
+            "unfused_ms": unfused_ms, "e2e": e2e, "kernel_tag": kernel_tag,
+            "launches_per_step": 3 if args.kernel == "ffma" else 1, "_window": window}
 
-    clocks = sampler.stop() if rank == 0 else None
 
-    achieved = kernel_work / (kern_ms / 1e3) / (1e9 if kernel_unit == "GB/s" else 1.0)
-    if kernel_unit == "GB/s":
-        achieved = kernel_work / (kern_ms / 1e3) / 1e9
+def run_vtmu(args, rank, world, local):
+    import torch
+    import f32_gqa_attention_gb300 as vtmu
+    vtmu.load_library()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    peaks, peak_kind = load_peaks()
+    stream = torch.cuda.Stream(device=dev)
+    sampler = ClockSampler(local)
+    if rank == 0:
+        sampler.start()
+        time.sleep(0.6)
+    ctx = Ctx(torch, vtmu, dev, stream, peaks, peak_kind, sampler, rank, world, args)
+    name = args.workload
+    w = si.WORKLOADS[name]
+
+    if w["kind"] == "decode":
+        d = measure_decode(ctx, name)
+        block = []
+        if not args.no_prefill:
+            for pname in PREFILL_SET:
+                block.append(measure_prefill(ctx, pname, args.steps, args.warmup,
+                                             cpu_budget=0.0 if args.no_cpu_baseline else args.prefill_cpu_budget,
+                                             e2e_steps=3))
+        sampler.stop()
+        clocks = sampler.summary(*d["_window"])
+        achieved = d["step_bytes"] / (d["kernel_ms"] / 1e3) / 1e9
+        peak = float(peaks["hbm_gbs"])
+        roofline = {"bound": "hbm", "kernel": d["kernel_tag"], "achieved": round(achieved, 3), "peak": round(peak, 1),
+                    "peak_source": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                    "traffic": profile_traffic(d["kernel_tag"] + "__" + name), "kernel_ms": round(d["kernel_ms"], 5)}
+        cpu = None
+        if rank == 0 and not args.no_cpu_baseline:
+            val, sample, cores = time_oracle(name, w, budget_s=args.cpu_budget, x=d["x"])
+            cpu = {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": METRIC, "value": round(d["step_bytes"] / 1e9 * world / (d["step_ms"] / 1e3), 3),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(d["step_ms"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": DATA, "config": workload_config(name, world),
+            "impl": "vtmu", "roofline": roofline, "cpu_baseline": cpu, "e2e": d["e2e"],
+            "gpu_launches": d["launches_per_step"] * args.steps, "clocks": clocks,
+            "unfused_ms_per_step": round(d["unfused_ms"], 5),
+        }
+        if block:
+            line["prefill"] = [finish_prefill(ctx, r) for r in block]
     else:
-        achieved = kernel_work / (kern_ms / 1e3)
-    traffic = profile_traffic(kernel_tag + "__" + name)
-    roofline = {"bound": bound, "kernel": kernel_tag, "achieved": round(achieved, 3), "peak": round(peak, 1),
-                "peak_source": peak_note,
-                "unit": kernel_unit, "frac": round(achieved / peak, 4), "traffic": traffic,
-                "kernel_ms": round(kern_ms, 5)}
-
-    cpu = None
-    if rank == 0 and not args.no_cpu_baseline:
-        val, sample, cores = time_oracle(name, w, budget_s=args.cpu_budget, x=x)
-        cpu = {"value": round(val, 4), "unit": unit, "cores": cores, "kind": "oracle", "sample": sample}
-
-    line = {
-        "metric": METRIC, "value": round(work_per_step * world / (step_ms / 1e3), 3), "unit": unit,
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_ms, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic (seeded SplitMix64 / Box-Muller, N(0,1) inputs of the workload's shapes)",
-        "config": {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
-                   "parallelism": f"replicas x{world}", "l2": l2_note},
-        "impl": "vtmu", "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
-        "gpu_launches": launches_per_step * args.steps, "clocks": clocks,
-    }
-    if unfused_ms is not None:
-        line["unfused_ms_per_step"] = round(unfused_ms, 5)
+        r = measure_prefill(ctx, name, args.steps, args.warmup, kernel_arg=args.kernel,
+                            cpu_budget=0.0 if args.no_cpu_baseline else args.cpu_budget)
+        sampler.stop()
+        e = finish_prefill(ctx, r)
+        line = {
+            "metric": METRIC, "value": e["value"], "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": e["ms_per_step"], "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": DATA, "config": workload_config(name, world),
+            "impl": "vtmu", "roofline": e["roofline"], "cpu_baseline": e["cpu_baseline"], "e2e": e["e2e"],
+            "gpu_launches": e["gpu_launches"], "clocks": e["clocks"], "kernel_ms": e["kernel_ms"],
+        }
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -582,11 +723,8 @@ def run_reference(args, rank, world):
     line = {
         "metric": METRIC, "value": round(value, 4), "unit": unit, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 3), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic (seeded SplitMix64 / Box-Muller, N(0,1) inputs of the workload's shapes)",
-        "config": {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
-                   "parallelism": "host cores"},
-        "impl": "reference",
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": DATA,
+        "config": workload_config(name, world), "impl": "reference",
         "cpu_baseline": {"value": round(value, 4), "unit": unit, "kind": "oracle", "cores": smp.cores,
                          "sample": smp.describe(args.steps)},
         "e2e": {"value": round(value, 4), "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -603,6 +741,10 @@ def main():
     ap.add_argument("--workload", choices=sorted(si.WORKLOADS), default="gqa_decode")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle timing")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="decode workloads: leave out the four prefill workloads that follow the decode line")
+    ap.add_argument("--prefill-cpu-budget", type=float, default=3.0,
+                    help="seconds of oracle timing per prefill workload after a decode line")
     ap.add_argument("--kernel", choices=["auto", "tc", "ffma"], default="auto",
                     help="prefill kernel: tcgen05 3xTF32 or FFMA (auto: tcgen05 where it covers the shape)")
     args = ap.parse_args()

@@ -317,6 +317,56 @@ vtmu_status vtmu_attention_workspace_size(const vtmu_attention_params* p, size_t
 
 namespace {
 
+// The pointer checks of op "attention" (nulls, alignment, bias against
+// bias_kind, out overlapping an input); launches nothing.
+vtmu_status check_pointers(const vtmu::AttnDesc& a, const float* q, const float* k, const float* v,
+                           const float* bias, const float* out, const vtmu_attention_params* p) {
+    if (!q) return fail(VTMU_ERR_INVALID, "q is NULL");
+    if (!out) return fail(VTMU_ERR_INVALID, "out is NULL");
+    if (a.S > 0 && (!k || !v)) return fail(VTMU_ERR_INVALID, "k or v is NULL");
+    if ((p->bias_kind != VTMU_BIAS_NONE) != (bias != nullptr))
+        return fail(VTMU_ERR_INVALID, "attention.bias: bias pointer and bias_kind disagree");
+    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
+                          reinterpret_cast<uintptr_t>(bias);
+    if (mis & 3u) return fail(VTMU_ERR_INVALID, "tensor pointers must be 4-byte aligned");
+    const size_t out_b = (size_t)a.T * a.H * a.Dv * 4;
+    const size_t q_b = (size_t)a.T * a.H * a.D * 4, k_b = (size_t)a.S * a.Hk * a.D * 4,
+                 v_b = (size_t)a.S * a.Hk * a.Dv * 4;
+    const size_t b_b = p->bias_kind == VTMU_BIAS_TS    ? (size_t)a.T * a.S * 4
+                       : p->bias_kind == VTMU_BIAS_HTS ? (size_t)a.H * a.T * a.S * 4
+                                                       : 0;
+    if (overlaps(out, out_b, q, q_b) || overlaps(out, out_b, k, k_b) || overlaps(out, out_b, v, v_b) ||
+        overlaps(out, out_b, bias, b_b))
+        return fail(VTMU_ERR_INVALID, "out overlaps an input");
+    return VTMU_OK;
+}
+
+}  // namespace
+
+namespace vtmu {
+// Every check that vtmu_attention makes before it launches the decode kernel
+// with params `p` (p->kernel must be VTMU_KERNEL_DECODE), and the scratch
+// bytes that launch needs; launches nothing and touches no device memory.
+vtmu_status check_decode_call(const vtmu_attention_params* p, const float* q, const float* k, const float* v,
+                              const float* bias, const float* out, size_t* scratch_bytes) {
+    Resolved r;
+    vtmu_status st = resolve(p, &r);
+    if (st != VTMU_OK) return st;
+    if (r.kernel != VTMU_KERNEL_DECODE) return fail(VTMU_ERR_INVALID, "check_decode_call: kernel is not DECODE");
+    if (r.a.T == 0) return fail(VTMU_ERR_INVALID, "decode needs T >= 1");
+    st = check_pointers(r.a, q, k, v, bias, out, p);
+    if (st != VTMU_OK) return st;
+    const uintptr_t m16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+    if (m16 & 15u) return fail(VTMU_ERR_UNSUPPORTED, "kernel DECODE needs 16-byte aligned q, k, v, out");
+    *scratch_bytes = decode_workspace(r.a);
+    return VTMU_OK;
+}
+}  // namespace vtmu
+
+namespace {
+
 // op "attention" after resolve(); with `cw`, the two cache writes of a
 // decode step come first (fused into the decode launch when it runs).
 vtmu_status run_attention(Resolved& r, const float* q, const float* k, const float* v, const float* bias,
@@ -336,24 +386,8 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
         e = write_caches();
         return e == cudaSuccess ? ok() : cuda_fail(e, "cache_write launch");
     }
-    if (!q) return fail(VTMU_ERR_INVALID, "q is NULL");
-    if (!out) return fail(VTMU_ERR_INVALID, "out is NULL");
-    if (a.S > 0 && (!k || !v)) return fail(VTMU_ERR_INVALID, "k or v is NULL");
-    if ((p->bias_kind != VTMU_BIAS_NONE) != (bias != nullptr))
-        return fail(VTMU_ERR_INVALID, "attention.bias: bias pointer and bias_kind disagree");
-    const uintptr_t mis = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
-                          reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out) |
-                          reinterpret_cast<uintptr_t>(bias);
-    if (mis & 3u) return fail(VTMU_ERR_INVALID, "tensor pointers must be 4-byte aligned");
-    const size_t out_b = (size_t)a.T * a.H * a.Dv * 4;
-    const size_t q_b = (size_t)a.T * a.H * a.D * 4, k_b = (size_t)a.S * a.Hk * a.D * 4,
-                 v_b = (size_t)a.S * a.Hk * a.Dv * 4;
-    const size_t b_b = p->bias_kind == VTMU_BIAS_TS    ? (size_t)a.T * a.S * 4
-                       : p->bias_kind == VTMU_BIAS_HTS ? (size_t)a.H * a.T * a.S * 4
-                                                       : 0;
-    if (overlaps(out, out_b, q, q_b) || overlaps(out, out_b, k, k_b) || overlaps(out, out_b, v, v_b) ||
-        overlaps(out, out_b, bias, b_b))
-        return fail(VTMU_ERR_INVALID, "out overlaps an input");
+    vtmu_status pst = check_pointers(a, q, k, v, bias, out, p);
+    if (pst != VTMU_OK) return pst;
     a.q = q;
     a.k = k;
     a.v = v;

@@ -248,22 +248,27 @@ VTMU_API vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t wi
  * a plug-in whose host process owns all device memory through its own pool,
  * or a latency-critical decode loop that must not call cudaMalloc (it can
  * synchronise the device).  It computes exactly what vtmu_attention does
- * with VTMU_KERNEL_DECODE (same arguments, same checks, T must be 1 and the
- * decode kernel's shape table must cover the call) but takes no workspace:
- * the kernel's scratch (split partials and arrival counters) lives in a
- * static device array of VTMU_NOALLOC_SCRATCH_BYTES that every GPU loading
- * this library holds until the process exits.  The call itself allocates
- * nothing.
+ * with VTMU_KERNEL_DECODE (same arguments, same checks, T must be 1, the
+ * decode kernel's shape table must cover the call and p->kernel must be
+ * VTMU_KERNEL_AUTO or VTMU_KERNEL_DECODE) but takes no workspace: the
+ * kernel's scratch (split partials and arrival counters) lives in a static
+ * device array of VTMU_NOALLOC_SCRATCH_BYTES that every GPU loading this
+ * library holds until the process exits.  The call itself allocates nothing.
  *  - Limit: a call whose decode scratch (vtmu_attention_workspace_size with
  *    kernel = VTMU_KERNEL_DECODE) exceeds VTMU_NOALLOC_SCRATCH_BYTES is
- *    refused with VTMU_ERR_WORKSPACE (over 16384 visible keys at vHeadDim
- *    128 that leaves room for up to 62 query heads).
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current) and caches it; make
- *    that first call before any stream capture.
- *  - All calls share the one array.  Its arrival counters are cleared on
- *    `stream` before each launch; calls whose GPU work overlaps (several
- *    streams or host threads at once) race on the array: serialise them.
+ *    refused with VTMU_ERR_WORKSPACE.  With 16384 or more visible keys at
+ *    vHeadDim 128 the array holds 62 virtual heads: up to 62 query heads
+ *    when heads/kvHeads >= 2, up to 31 when heads == kvHeads (the kernel
+ *    pads each KV head to two virtual heads there).
+ *  - Every call looks up the array's device address (cudaGetSymbolAddress,
+ *    with the caller's device current), so the address stays right after
+ *    cudaDeviceReset or under another context of the same device.  The first
+ *    call in a context may load the library's device code: make it before
+ *    any stream capture.
+ *  - All calls share the one array.  Every host-side check runs before the
+ *    array is touched; then its arrival counters are cleared on `stream`
+ *    and the kernel launched.  Calls whose GPU work overlaps (several streams
+ *    or host threads at once) race on the array: serialise them.
  */
 #define VTMU_NOALLOC_SCRATCH_BYTES (8u << 20)
 VTMU_API vtmu_status vtmu_attention_decode_noalloc(const float* q, const float* k, const float* v,

@@ -43,3 +43,18 @@ def sample_rows(T, H, G, bm=(64, 128), extra=24, seed=0):
     rows = [(t, h) for t in ts for h in hs]
     rows += [(int(g.integers(0, T)), int(g.integers(0, H))) for _ in range(extra)]
     return rows
+
+
+def sample_tile_rows(T, H, G, bm=128, seed=0):
+    """One random row of every bm-row query tile for each of the heads 0,
+    G - 1, H // 2 and H - 1 (the first and last group and the last head), so
+    every (query tile, head group) work item of a full-size launch has a row
+    checked."""
+    g = np.random.default_rng(seed)
+    hs = sorted({0, G - 1, H // 2, H - 1} & set(range(H)))
+    rows = []
+    for t0 in range(0, T, bm):
+        t1 = min(T, t0 + bm)
+        for h in hs:
+            rows.append((int(g.integers(t0, t1)), h))
+    return rows

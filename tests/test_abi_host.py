@@ -296,3 +296,38 @@ def test_noalloc_needs_one_query_row(lib):
     p = vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094)
     e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
     assert e.status == vtmu.VTMU_ERR_INVALID and "T must be 1" in str(e)
+
+
+@host_only
+def test_noalloc_takes_only_the_decode_kernel(lib):
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095,
+                         kernel=vtmu.VTMU_KERNEL_PREFILL_FFMA)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "VTMU_KERNEL_DECODE" in str(e)
+
+
+@host_only
+def test_noalloc_checks_pointers_before_touching_its_scratch(lib):
+    """Null, misaligned and overlapping pointers are refused before the call
+    clears the shared array's counters (no CUDA call is made on this host)."""
+    p = vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, None, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "out is NULL" in str(e)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE + 4, FAKE * 3, FAKE * 5, None, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "16-byte" in str(e)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, None, FAKE * 3, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "overlaps" in str(e)
+    e = _err(lambda: vtmu.vtmu_attention_decode_noalloc(FAKE, FAKE * 3, FAKE * 5, FAKE * 9, FAKE * 7, p, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "bias" in str(e)
+
+
+def test_noalloc_scratch_limit_in_virtual_heads(lib):
+    """Over 32768 keys at vHeadDim 128 the static scratch holds 62 virtual
+    heads: 62 query heads with groups of two or more, 31 when every query
+    head has its own KV head (each KV head is padded to two virtual heads)."""
+    def need(H, Hk):
+        return vtmu.vtmu_attention_workspace_size(vtmu.make_params(
+            1, 32768, heads=H, headDim=128, kvHeads=Hk, posOffset=32767, kernel=vtmu.VTMU_KERNEL_DECODE))
+    cap = vtmu.NOALLOC_SCRATCH_BYTES
+    assert need(62, 31) <= cap < need(64, 32)
+    assert need(31, 31) <= cap < need(32, 32)

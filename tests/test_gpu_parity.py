@@ -6,7 +6,7 @@ import pytest
 
 import oracle
 import seeded_inputs as si
-from gpu_util import TOL, gpu_attention, max_err, oracle_params, sample_rows, to_dev
+from gpu_util import TOL, gpu_attention, max_err, oracle_params, sample_rows, sample_tile_rows, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -82,7 +82,10 @@ def test_decode_step_workloads(name):
 @pytest.mark.parametrize("name", ["gqa_prefill", "swa_softcap_prefill", "latent_bias_prefill",
                                   "alibi_prefill", "swa_sinks_prefill"])
 def test_prefill_workload_sampled_rows(name):
-    """Full-size prefill on the GPU; the oracle recomputes sampled (t, h) rows."""
+    """Full-size prefill on the GPU; the oracle recomputes sampled (t, h) rows:
+    the first and last rows, tile edges and random rows, plus one row of
+    every 128-row query tile for four heads (every output column of a row is
+    compared, so both vHeadDim halves of a headDim-256 launch are covered)."""
     w = si.WORKLOADS[name]
     x = si.workload_inputs(name)
     params = dict(heads=w["heads"], headDim=w["headDim"], kvHeads=w["kvHeads"],
@@ -90,7 +93,8 @@ def test_prefill_workload_sampled_rows(name):
     out = gpu_attention(x["q"], x["k"], x["v"], x.get("bias"), **params)
     assert np.all(np.isfinite(out))
     H, Dv = w["heads"], w.get("vHeadDim") or w["headDim"]
-    rows = sample_rows(w["T"], H, H // w["kvHeads"], seed=1)
+    G = H // w["kvHeads"]
+    rows = sample_rows(w["T"], H, G, seed=1) + sample_tile_rows(w["T"], H, G, seed=2)
     ref = oracle.attention_rows(x["q"], x["k"], x["v"], x.get("bias"), rows=rows, **params)
     got = np.stack([out[t, h * Dv:(h + 1) * Dv] for t, h in rows])
     err = max_err(got, ref)

@@ -19,9 +19,6 @@ if not torch.cuda.is_available():
 
 import f32_gqa_attention_gb300 as vtmu  # noqa: E402
 
-TOL = 1e-4
-
-
 def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a)).cuda()
 
@@ -42,17 +39,33 @@ def _both(x, **params):
     out = torch.full_like(ref, float("nan"))
     vtmu.vtmu_attention_decode_noalloc(q, k, v, b, out, p, st)
     torch.cuda.synchronize()
+    assert vtmu.vtmu_device_error() == 0, "a kernel wait gave up"
     return ref.cpu().numpy(), out.cpu().numpy()
+
+
+def _same(ref, out):
+    """Both calls run the same kernel with the same plan, so the outputs are
+    bit-identical (a scratch-layout slip would show as a small difference)."""
+    assert np.all(np.isfinite(out))
+    assert np.array_equal(ref, out), float(np.max(np.abs(out - ref)))
 
 
 def test_noalloc_decode_matches_regular_entry_point_on_two_calls():
     first = si.attention_inputs(1, 32768, 32, 8, 128, 128, 1)
-    ref1, out1 = _both(first, heads=32, headDim=128, kvHeads=8, posOffset=32767)
+    _same(*_both(first, heads=32, headDim=128, kvHeads=8, posOffset=32767))
     second = si.attention_inputs(1, 3000, 16, 2, 64, 64, 2, bias="hts")
-    ref2, out2 = _both(second, heads=16, headDim=64, kvHeads=2, posOffset=2500, window=700, softcap=30.0)
-    for ref, out in ((ref1, out1), (ref2, out2)):
-        assert np.all(np.isfinite(out))
-        assert float(np.max(np.abs(out - ref))) <= TOL
+    _same(*_both(second, heads=16, headDim=64, kvHeads=2, posOffset=2500, window=700, softcap=30.0))
+
+
+def test_noalloc_after_a_larger_call_and_with_one_query_head_per_kv_head():
+    """A call with many splits leaves partials all over the array; a later
+    call with fewer splits and other heads must not read them.  Heads ==
+    kvHeads (group size 1) pads every KV head to two virtual heads."""
+    big = si.attention_inputs(1, 32768, 16, 16, 128, 128, 3)
+    _same(*_both(big, heads=16, headDim=128, kvHeads=16, posOffset=32767, decode_splits=64))
+    small = si.attention_inputs(1, 700, 8, 8, 32, 32, 4)
+    _same(*_both(small, heads=8, headDim=32, kvHeads=8, posOffset=650))
+    _same(*_both(big, heads=16, headDim=128, kvHeads=16, posOffset=20000, decode_splits=7))
 
 
 def test_noalloc_refuses_a_shape_beyond_its_scratch():
