@@ -1,4 +1,5 @@
-"""CPU oracle for the f32 ``attention``, ``cache_write`` and ``rope`` ops.
+"""CPU oracle for the f32 ``attention``, ``cache_write`` and ``rope`` ops, and
+for absorbed latent attention (``mla_attention``).
 
 TEST INFRASTRUCTURE ONLY: the tests, ``__graft_entry__.smoke()`` and the
 benchmark's CPU-baseline leg are the only callers.  The product path (the
@@ -19,6 +20,13 @@ defaults as the op catalog states them (vtmu.mpakt.dev/api/ops, op
 * ALiBi: ``alibiSlopes`` wins over ``alibiMax``, which wins over ``alibi``;
 * ``sinks`` (the IR page's attention sinks, not a param of the op page):
   with a window, keys before ``sinks`` stay visible; 0 or absent = none.
+
+``mla_attention`` (the IR schema page's ``$defs.op_mla_attention``) takes
+q [T, heads*(qk_nope + qk_rope)], the latent cache state [S, kv_rank +
+qk_rope], k_b [heads*qk_nope, kv_rank] and v_b [heads*v_head_dim, kv_rank]
+(the page's parameter names); ``scale`` defaults to 1/sqrt(qk_nope +
+qk_rope), the query/key width per head, as op "attention"'s scale defaults
+to 1/sqrt(headDim); causal, window and sinks as for ``attention``.
 
 ``Oracle(path)`` wraps one compiled build; the module-level functions use the
 default build of ``attention_oracle.c``.  The tests also compile copies with a
@@ -64,6 +72,23 @@ class _Desc(ctypes.Structure):
     ]
 
 
+class _MlaDesc(ctypes.Structure):
+    _fields_ = [
+        ("T", ctypes.c_int64),
+        ("S", ctypes.c_int64),
+        ("heads", ctypes.c_int),
+        ("kv_rank", ctypes.c_int),
+        ("qk_nope", ctypes.c_int),
+        ("qk_rope", ctypes.c_int),
+        ("v_head_dim", ctypes.c_int),
+        ("causal", ctypes.c_int),
+        ("pos_offset", ctypes.c_int64),
+        ("scale", ctypes.c_double),
+        ("window", ctypes.c_int64),
+        ("sinks", ctypes.c_int64),
+    ]
+
+
 def compile_source(src: str, out: str) -> str:
     """gcc -O2 -fopenmp a C file of the oracle into a shared library."""
     tmp = out + f".tmp{os.getpid()}"
@@ -105,6 +130,9 @@ class Oracle:
         lib.oracle_cache_write.argtypes = [p, ctypes.c_int64, ctypes.c_int64,
                                            p, ctypes.c_int64, ctypes.c_int64]
         lib.oracle_num_threads.restype = ctypes.c_int
+        lib.oracle_mla_attention.argtypes = [ctypes.POINTER(_MlaDesc), p, p, p, p, p]
+        lib.oracle_mla_attention_rows.argtypes = [ctypes.POINTER(_MlaDesc), p, p, p, p, p, p,
+                                                  ctypes.c_int64, p]
         lib.oracle_rope_inv_freq.argtypes = [ctypes.c_int, ctypes.c_double, p]
         lib.oracle_rope.argtypes = [p, ctypes.c_int64, ctypes.c_int, ctypes.c_int,
                                     ctypes.c_int, ctypes.c_int, ctypes.c_int64,
@@ -271,6 +299,62 @@ class Oracle:
             raise ValueError("oracle_rope failed")
         return out
 
+    def _mla_prepare(self, q, state, k_b, v_b, heads, kv_rank, qk_nope, qk_rope,
+                     v_head_dim, scale, causal, posOffset, window, sinks):
+        q, state, k_b, v_b = _f32(q), _f32(state), _f32(k_b), _f32(v_b)
+        H, R, N, P, Dv = int(heads), int(kv_rank), int(qk_nope), int(qk_rope), int(v_head_dim)
+        if q.ndim != 2 or q.shape[1] != H * (N + P):
+            raise ValueError("q must be [T, heads*(qk_nope + qk_rope)]")
+        if state.ndim != 2 or state.shape[1] != R + P:
+            raise ValueError("state must be [S, kv_rank + qk_rope]")
+        if k_b.shape != (H * N, R):
+            raise ValueError("k_b must be [heads*qk_nope, kv_rank]")
+        if v_b.shape != (H * Dv, R):
+            raise ValueError("v_b must be [heads*v_head_dim, kv_rank]")
+        d = _MlaDesc()
+        d.T, d.S = q.shape[0], state.shape[0]
+        d.heads, d.kv_rank, d.qk_nope, d.qk_rope, d.v_head_dim = H, R, N, P, Dv
+        d.causal = 1 if causal else 0
+        d.pos_offset = int(posOffset)
+        d.scale = (1.0 / math.sqrt(N + P)) if scale is None else float(scale)
+        d.window = 0 if window is None else int(window)
+        d.sinks = 0 if sinks is None else int(sinks)
+        if d.window < 0 or d.sinks < 0:
+            raise ValueError("window and sinks must be >= 0")
+        return d, (q, state, k_b, v_b)
+
+    def mla_attention(self, q, state, k_b, v_b, *, heads, kv_rank, qk_nope, qk_rope,
+                      v_head_dim, scale=None, causal=True, posOffset=0, window=None,
+                      sinks=None):
+        """Absorbed latent attention by its un-absorbed definition: returns
+        out [T, heads*v_head_dim] as float64."""
+        d, keep = self._mla_prepare(q, state, k_b, v_b, heads, kv_rank, qk_nope, qk_rope,
+                                    v_head_dim, scale, causal, posOffset, window, sinks)
+        q, state, k_b, v_b = keep
+        out = np.zeros((d.T, d.heads * d.v_head_dim), dtype=np.float64)
+        rc = self.lib.oracle_mla_attention(ctypes.byref(d), _ptr(q), _ptr(state), _ptr(k_b),
+                                           _ptr(v_b), _ptr(out))
+        if rc:
+            raise ValueError(f"oracle_mla_attention failed ({rc})")
+        return out
+
+    def mla_attention_rows(self, q, state, k_b, v_b, *, rows, heads, kv_rank, qk_nope,
+                           qk_rope, v_head_dim, scale=None, causal=True, posOffset=0,
+                           window=None, sinks=None):
+        """Selected (t, h) rows only: returns [len(rows), v_head_dim] float64."""
+        d, keep = self._mla_prepare(q, state, k_b, v_b, heads, kv_rank, qk_nope, qk_rope,
+                                    v_head_dim, scale, causal, posOffset, window, sinks)
+        q, state, k_b, v_b = keep
+        rows = list(rows)
+        ts = np.ascontiguousarray([int(t) for t, _ in rows], dtype=np.int64)
+        hs = np.ascontiguousarray([int(h) for _, h in rows], dtype=np.int32)
+        out = np.zeros((len(rows), d.v_head_dim), dtype=np.float64)
+        rc = self.lib.oracle_mla_attention_rows(ctypes.byref(d), _ptr(q), _ptr(state), _ptr(k_b),
+                                                _ptr(v_b), _ptr(ts), _ptr(hs), len(rows), _ptr(out))
+        if rc:
+            raise ValueError(f"oracle_mla_attention_rows failed ({rc})")
+        return out
+
 
 def default() -> Oracle:
     global _default
@@ -305,3 +389,11 @@ def rope(x, **params):
 
 def rope_inv_freq(rotaryDim, base=None):
     return default().rope_inv_freq(rotaryDim, base)
+
+
+def mla_attention(q, state, k_b, v_b, **params):
+    return default().mla_attention(q, state, k_b, v_b, **params)
+
+
+def mla_attention_rows(q, state, k_b, v_b, **params):
+    return default().mla_attention_rows(q, state, k_b, v_b, **params)

@@ -1,7 +1,9 @@
 /*
  * attention_oracle.c -- plain, slow CPU oracle for the f32 `attention`,
  * `cache_write` and `rope` ops of the volunteer-inference op catalog
- * (vtmu.mpakt.dev/api/ops, ops "attention", "cache_write" and "rope").
+ * (vtmu.mpakt.dev/api/ops, ops "attention", "cache_write" and "rope"), and
+ * for the absorbed latent attention of the IR schema page
+ * ($defs.op_mla_attention), at the end of this file.
  *
  * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may link, load or
  * call this file: only the tests, the package smoke check and the benchmark's
@@ -289,6 +291,183 @@ int oracle_rope(const float* x, int64_t T, int heads, int head_dim, int rotary_d
         }
     }
     return 0;
+}
+
+/*
+ * Absorbed latent attention ("mla_attention" of the IR schema page,
+ * $defs.op_mla_attention: heads, kv_rank, qk_nope, qk_rope, v_head_dim, the
+ * up-projections k_b and v_b, scale, causal, window, sinks).  The oracle
+ * computes its plain, un-absorbed definition (DeepSeek-V2's multi-head latent
+ * attention, which the parameter names follow):
+ *
+ *   state [S, kv_rank + qk_rope]: row s = [c_s (kv_rank) | r_s (qk_rope)],
+ *       the latent KV cache: the compressed latent and the shared rotary key;
+ *   k_b [heads*qk_nope, kv_rank], v_b [heads*v_head_dim, kv_rank]: the
+ *       up-projections as stored ([out, in]);
+ *   q [T, heads*(qk_nope + qk_rope)]: per head the no-rope part, then the
+ *       rotary part;
+ *   key of head h at s:   [ sum_j k_b[h*qk_nope + i, j] c_s[j]  (i < qk_nope) | r_s ]
+ *   value of head h at s: [ sum_j v_b[h*v_head_dim + e, j] c_s[j] (e < v_head_dim) ]
+ *   out[t, h*v_head_dim + e] = the attention of q's head-h row over those keys
+ *       and values: x_s = scale * q . key, visible keys as for op attention
+ *       (causal, window, sinks), max-subtracted softmax, zeros when nothing is
+ *       visible.
+ *
+ * Every head's keys and values are expanded in double first (the definition),
+ * then each requested row attends to them.  The absorbed form that a GPU
+ * kernel uses (queries through k_b into the latent space, one shared latent
+ * head, the output through v_b) is the same sum in another order.
+ */
+typedef struct {
+    int64_t T, S;
+    int heads, kv_rank, qk_nope, qk_rope, v_head_dim;
+    int causal;
+    int64_t pos_offset;
+    double scale;   /* resolved by the caller */
+    int64_t window; /* 0 = off */
+    int64_t sinks;  /* 0 = none */
+} oracle_mla_desc;
+
+static int mla_desc_ok(const oracle_mla_desc* a)
+{
+    if (!a || a->T < 0 || a->S < 0 || a->heads <= 0 || a->kv_rank <= 0 || a->qk_nope < 0 ||
+        a->qk_rope < 0 || a->qk_nope + a->qk_rope <= 0 || a->v_head_dim <= 0)
+        return 0;
+    if (a->window < 0 || a->sinks < 0) return 0;
+    return 1;
+}
+
+/* Keys and values of head h for every s: kh [S, qk_nope + qk_rope],
+ * vh [S, v_head_dim], in double. */
+static void mla_expand_head(const oracle_mla_desc* a, const float* state, const float* k_b,
+                            const float* v_b, int h, double* kh, double* vh)
+{
+    const int R = a->kv_rank, N = a->qk_nope, P = a->qk_rope, Dv = a->v_head_dim;
+    const int64_t W = (int64_t)R + P;
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < a->S; ++s) {
+        const float* c = state + s * W;
+        double* krow = kh + s * (int64_t)(N + P);
+        double* vrow = vh + s * (int64_t)Dv;
+        for (int i = 0; i < N; ++i) {
+            const float* w = k_b + ((int64_t)h * N + i) * R;
+            double acc = 0.0;
+            for (int j = 0; j < R; ++j) acc += (double)w[j] * (double)c[j];
+            krow[i] = acc;
+        }
+        for (int i = 0; i < P; ++i) krow[N + i] = (double)c[R + i];
+        for (int e = 0; e < Dv; ++e) {
+            const float* w = v_b + ((int64_t)h * Dv + e) * R;
+            double acc = 0.0;
+            for (int j = 0; j < R; ++j) acc += (double)w[j] * (double)c[j];
+            vrow[e] = acc;
+        }
+    }
+}
+
+/* Row t of head h against the expanded keys and values. */
+static void mla_attend_row(const oracle_mla_desc* a, const float* q, const double* kh,
+                           const double* vh, int64_t t, int h, double* x, char* vis, double* o)
+{
+    const int Dq = a->qk_nope + a->qk_rope, Dv = a->v_head_dim;
+    const int64_t pos = a->pos_offset + t;
+    const float* qrow = q + (t * (int64_t)a->heads + h) * Dq;
+    double m = -INFINITY;
+    for (int64_t s = 0; s < a->S; ++s) {
+        vis[s] = (char)key_visible(a->causal, a->window, a->sinks, pos, s);
+        if (!vis[s]) continue;
+        const double* krow = kh + s * (int64_t)Dq;
+        double dot = 0.0;
+        for (int d = 0; d < Dq; ++d) dot += (double)qrow[d] * krow[d];
+        x[s] = a->scale * dot;
+        if (x[s] > m) m = x[s];
+    }
+    for (int e = 0; e < Dv; ++e) o[e] = 0.0;
+    if (m == -INFINITY) return;
+    double l = 0.0;
+    for (int64_t s = 0; s < a->S; ++s) {
+        if (!vis[s]) continue;
+        const double wgt = exp(x[s] - m);
+        l += wgt;
+        const double* vrow = vh + s * (int64_t)Dv;
+        for (int e = 0; e < Dv; ++e) o[e] += wgt * vrow[e];
+    }
+    for (int e = 0; e < Dv; ++e) o[e] /= l;
+}
+
+/* Selected rows: for i < n, row (ts[i], hs[i]) -> out[i * v_head_dim ...].
+ * Returns 0 on success. */
+int oracle_mla_attention_rows(const oracle_mla_desc* a, const float* q, const float* state,
+                              const float* k_b, const float* v_b, const int64_t* ts,
+                              const int32_t* hs, int64_t n, double* out)
+{
+    if (!mla_desc_ok(a)) return 1;
+    for (int64_t i = 0; i < n; ++i)
+        if (ts[i] < 0 || ts[i] >= a->T || hs[i] < 0 || hs[i] >= a->heads) return 1;
+    const int Dq = a->qk_nope + a->qk_rope, Dv = a->v_head_dim;
+    const size_t S1 = (size_t)(a->S > 0 ? a->S : 1);
+    double* kh = (double*)malloc(sizeof(double) * S1 * (size_t)Dq);
+    double* vh = (double*)malloc(sizeof(double) * S1 * (size_t)Dv);
+    if (!kh || !vh) {
+        free(kh);
+        free(vh);
+        return 2;
+    }
+    int bad = 0;
+    for (int h = 0; h < a->heads && !bad; ++h) {
+        int any = 0;
+        for (int64_t i = 0; i < n && !any; ++i) any = hs[i] == h;
+        if (!any) continue;
+        mla_expand_head(a, state, k_b, v_b, h, kh, vh);
+#pragma omp parallel
+        {
+            double* x = (double*)malloc(sizeof(double) * S1);
+            char* vis = (char*)malloc(S1);
+            if (!x || !vis) {
+#pragma omp atomic write
+                bad = 1;
+            } else {
+#pragma omp for schedule(dynamic, 1)
+                for (int64_t i = 0; i < n; ++i)
+                    if (hs[i] == h) mla_attend_row(a, q, kh, vh, ts[i], h, x, vis, out + i * (int64_t)Dv);
+            }
+            free(x);
+            free(vis);
+        }
+    }
+    free(kh);
+    free(vh);
+    return bad ? 2 : 0;
+}
+
+/* Full output: out [T, heads * v_head_dim] doubles.  Returns 0 on success. */
+int oracle_mla_attention(const oracle_mla_desc* a, const float* q, const float* state,
+                         const float* k_b, const float* v_b, double* out)
+{
+    if (!mla_desc_ok(a)) return 1;
+    const int64_t n = a->T * a->heads;
+    int64_t* ts = (int64_t*)malloc(sizeof(int64_t) * (size_t)(n > 0 ? n : 1));
+    int32_t* hs = (int32_t*)malloc(sizeof(int32_t) * (size_t)(n > 0 ? n : 1));
+    double* tmp = (double*)malloc(sizeof(double) * (size_t)(n > 0 ? n : 1) * (size_t)a->v_head_dim);
+    if (!ts || !hs || !tmp) {
+        free(ts);
+        free(hs);
+        free(tmp);
+        return 2;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        ts[i] = i / a->heads;
+        hs[i] = (int32_t)(i % a->heads);
+    }
+    int rc = oracle_mla_attention_rows(a, q, state, k_b, v_b, ts, hs, n, tmp);
+    if (rc == 0)
+        for (int64_t i = 0; i < n; ++i)
+            memcpy(out + (ts[i] * a->heads + hs[i]) * (int64_t)a->v_head_dim,
+                   tmp + i * (int64_t)a->v_head_dim, sizeof(double) * (size_t)a->v_head_dim);
+    free(ts);
+    free(hs);
+    free(tmp);
+    return rc;
 }
 
 int oracle_num_threads(void)

@@ -2,7 +2,8 @@
 
 Each ``pin_*`` takes an ``oracle.Oracle`` and raises ``AssertionError`` when the
 oracle disagrees with something the op catalog (vtmu.mpakt.dev/api/ops, ops
-"attention", "softcap", "softmax", "cache_write", "rope") or plain mathematics fixes:
+"attention", "softcap", "softmax", "cache_write", "rope"), the IR schema page
+($defs.op_mla_attention, absorbed latent attention) or plain mathematics fixes:
 hand-worked examples, closed forms, limits, invariants, a library routine
 (PyTorch's float64 ``scaled_dot_product_attention``) on the cases it can
 express, and exact rational brute force.  ``test_oracle_pins.py`` runs them on
@@ -19,7 +20,7 @@ from fractions import Fraction
 import numpy as np
 
 GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
-_SYMBOLS = {"L3": math.log(3.0), "L2": math.log(2.0)}
+_SYMBOLS = {"L3": math.log(3.0), "L2": math.log(2.0), "L3m1": math.log(3.0) - 1.0}
 
 
 def _sym(x):
@@ -449,6 +450,162 @@ def pin_rope_linear_scaling_and_inv_freq(orc):
     assert np.allclose(plain[0], lin[0], rtol=0, atol=1e-12)  # row 0: 18 / 3 = 6
     inv = [10000.0 ** (-2.0 * j / 16) for j in range(8)]
     assert np.allclose(orc.rope(x, headDim=16, offset=6, invFreq=inv), plain, rtol=0, atol=1e-12)
+
+
+# ------------------------------------------------------- absorbed latent attention
+def _mla_inputs(g, T, S, H, R, N, P, Dv):
+    q = g.standard_normal((T, H * (N + P))).astype(np.float32)
+    state = g.standard_normal((S, R + P)).astype(np.float32)
+    k_b = (g.standard_normal((H * N, R)) / math.sqrt(R)).astype(np.float32)
+    v_b = (g.standard_normal((H * Dv, R)) / math.sqrt(R)).astype(np.float32)
+    return q, state, k_b, v_b
+
+
+def pin_mla_hand_examples(orc):
+    with open(os.path.join(GOLDEN, "mla_hand_examples.json")) as f:
+        cases = json.load(f)["cases"]
+    for c in cases:
+        out = orc.mla_attention(*(np.asarray(_sym(c[n]), np.float32) for n in ("q", "state", "k_b", "v_b")),
+                                **c["params"])
+        err = np.max(np.abs(out - np.asarray(c["expected"], np.float64)))
+        assert err <= c["tol"], f"{c['name']}: err {err} > {c['tol']} ({out})"
+
+
+def _mla_absorbed(q, state, k_b, v_b, *, heads, kv_rank, qk_nope, qk_rope, v_head_dim, scale,
+                  causal, posOffset, window, sinks):
+    """The absorbed order of the same sums, in float64: queries through k_b
+    into the latent space, one score against [latent | rotary key] shared by
+    every head, the softmax-weighted latent, then v_b."""
+    H, R, N, P, Dv = heads, kv_rank, qk_nope, qk_rope, v_head_dim
+    T, S = q.shape[0], state.shape[0]
+    q64 = q.astype(np.float64).reshape(T, H, N + P)
+    c = state[:, :R].astype(np.float64)
+    r = state[:, R:].astype(np.float64)
+    kb = k_b.astype(np.float64).reshape(H, N, R)
+    vb = v_b.astype(np.float64).reshape(H, Dv, R)
+    q_lat = np.einsum("thn,hnr->thr", q64[:, :, :N], kb)
+    x = scale * (np.einsum("thr,sr->ths", q_lat, c) + np.einsum("thp,sp->ths", q64[:, :, N:], r))
+    vis = np.array([[visible(causal, window or 0, posOffset + t, s, sinks or 0) for s in range(S)]
+                    for t in range(T)])
+    x = np.where(vis[:, None, :], x, -np.inf)
+    out = np.zeros((T, H, Dv))
+    for t in range(T):
+        if not vis[t].any():
+            continue
+        w = np.exp(x[t] - x[t].max(axis=1, keepdims=True))
+        o_lat = (w @ c) / w.sum(axis=1, keepdims=True)
+        out[t] = np.einsum("hr,her->he", o_lat, vb)
+    return out.reshape(T, H * Dv)
+
+
+MLA_CASES = [
+    dict(T=5, S=9, H=3, R=7, N=4, P=2, Dv=5, causal=True, posOffset=4),
+    dict(T=3, S=12, H=2, R=6, N=3, P=4, Dv=2, causal=False, posOffset=0, scale=0.4),
+    dict(T=4, S=16, H=4, R=8, N=2, P=2, Dv=3, causal=True, posOffset=12, window=3, sinks=2),
+    dict(T=2, S=10, H=1, R=5, N=5, P=1, Dv=6, causal=False, posOffset=5, window=2),
+    dict(T=6, S=6, H=2, R=4, N=3, P=3, Dv=4, causal=True, posOffset=0, window=2, sinks=3),
+]
+
+
+def _mla_params(c):
+    return dict(heads=c["H"], kv_rank=c["R"], qk_nope=c["N"], qk_rope=c["P"], v_head_dim=c["Dv"],
+                causal=c["causal"], posOffset=c["posOffset"], window=c.get("window"), sinks=c.get("sinks"))
+
+
+def pin_mla_absorbed_equals_unabsorbed(orc):
+    """The oracle expands keys and values per head; the absorbed order (the
+    GPU's) of the same sums must give the same rows in float64."""
+    g = _rng(41)
+    for c in MLA_CASES:
+        q, state, k_b, v_b = _mla_inputs(g, c["T"], c["S"], c["H"], c["R"], c["N"], c["P"], c["Dv"])
+        params = _mla_params(c)
+        out = orc.mla_attention(q, state, k_b, v_b, scale=c.get("scale"), **params)
+        scale = c.get("scale") or 1.0 / math.sqrt(c["N"] + c["P"])
+        want = _mla_absorbed(q, state, k_b, v_b, scale=scale, **params)
+        err = np.max(np.abs(out - want))
+        assert err < 1e-10, (c, err)
+
+
+def pin_mla_torch_sdpa(orc):
+    """Keys and values expanded with torch (float64), then PyTorch's
+    scaled_dot_product_attention with the visibility mask."""
+    import torch
+    g = _rng(43)
+    for c in MLA_CASES:
+        T, S, H, R, N, P, Dv = (c[k] for k in ("T", "S", "H", "R", "N", "P", "Dv"))
+        q, state, k_b, v_b = _mla_inputs(g, T, S, H, R, N, P, Dv)
+        st = torch.from_numpy(state.astype(np.float64))
+        lat, rope = st[:, :R], st[:, R:]
+        kn = torch.einsum("sr,hnr->hsn", lat, torch.from_numpy(k_b.astype(np.float64)).reshape(H, N, R))
+        keys = torch.cat([kn, rope[None].expand(H, S, P)], dim=2)
+        vals = torch.einsum("sr,her->hse", lat, torch.from_numpy(v_b.astype(np.float64)).reshape(H, Dv, R))
+        tq = torch.from_numpy(q.astype(np.float64)).reshape(T, H, N + P).transpose(0, 1)
+        mask = torch.zeros((T, S), dtype=torch.float64)
+        for t in range(T):
+            for s in range(S):
+                if not visible(c["causal"], c.get("window") or 0, c["posOffset"] + t, s, c.get("sinks") or 0):
+                    mask[t, s] = -math.inf
+        scale = c.get("scale") or 1.0 / math.sqrt(N + P)
+        o = torch.nn.functional.scaled_dot_product_attention(tq[None], keys[None], vals[None],
+                                                             attn_mask=mask[None, None], scale=scale)
+        want = o[0].transpose(0, 1).reshape(T, H * Dv).numpy()
+        out = orc.mla_attention(q, state, k_b, v_b, scale=c.get("scale"), **_mla_params(c))
+        err = np.max(np.abs(out - want))
+        assert err < 1e-10, (c, err)
+
+
+def pin_mla_identity_up_projections_are_mqa(orc):
+    """With k_b and v_b the identity for every head (qk_nope = v_head_dim =
+    kv_rank), each head attends to [latent | rotary key] with the latent as
+    value: op attention with one KV head (kvHeads 1), which the attention
+    pins fix."""
+    g = _rng(47)
+    for T, S, H, R, P, causal, pos, window in ((4, 9, 3, 5, 2, True, 5, None), (3, 7, 2, 4, 3, False, 0, 3)):
+        q = g.standard_normal((T, H * (R + P))).astype(np.float32)
+        state = g.standard_normal((S, R + P)).astype(np.float32)
+        eye = np.tile(np.eye(R, dtype=np.float32), (H, 1))
+        out = orc.mla_attention(q, state, eye, eye, heads=H, kv_rank=R, qk_nope=R, qk_rope=P, v_head_dim=R,
+                                causal=causal, posOffset=pos, window=window)
+        want = orc.attention(q, state, np.ascontiguousarray(state[:, :R]), heads=H, headDim=R + P, kvHeads=1,
+                             vHeadDim=R, causal=causal, posOffset=pos, window=window)
+        err = np.max(np.abs(out - want))
+        assert err < 1e-12, err
+
+
+def pin_mla_latent_rotation_invariance(orc):
+    """An orthogonal change of the latent basis (c -> c Q, k_b -> k_b Q,
+    v_b -> v_b Q) leaves every key and value, and so the output, unchanged;
+    permuting the heads (query blocks with their k_b and v_b blocks) permutes
+    the output blocks."""
+    g = _rng(53)
+    T, S, H, R, N, P, Dv = 3, 10, 3, 6, 4, 2, 5
+    q, state, k_b, v_b = _mla_inputs(g, T, S, H, R, N, P, Dv)
+    params = dict(heads=H, kv_rank=R, qk_nope=N, qk_rope=P, v_head_dim=Dv, causal=True, posOffset=7)
+    base = orc.mla_attention(q, state, k_b, v_b, **params)
+    Q, _ = np.linalg.qr(g.standard_normal((R, R)))
+    st2 = state.astype(np.float64).copy()
+    st2[:, :R] = st2[:, :R] @ Q
+    rot = orc.mla_attention(q, st2, k_b.astype(np.float64) @ Q, v_b.astype(np.float64) @ Q, **params)
+    assert np.max(np.abs(rot - base)) < 1e-5  # the rotated inputs are rounded to f32
+    perm = [2, 0, 1]
+    qp = q.reshape(T, H, N + P)[:, perm].reshape(T, -1)
+    kbp = k_b.reshape(H, N, R)[perm].reshape(H * N, R)
+    vbp = v_b.reshape(H, Dv, R)[perm].reshape(H * Dv, R)
+    outp = orc.mla_attention(qp, state, kbp, vbp, **params)
+    assert np.array_equal(outp.reshape(T, H, Dv), base.reshape(T, H, Dv)[:, perm])
+
+
+def pin_mla_decode_is_last_prefill_row(orc):
+    g = _rng(59)
+    T, H, R, N, P, Dv = 6, 2, 5, 3, 2, 4
+    q, state, k_b, v_b = _mla_inputs(g, T, T, H, R, N, P, Dv)
+    params = dict(heads=H, kv_rank=R, qk_nope=N, qk_rope=P, v_head_dim=Dv)
+    full = orc.mla_attention(q, state, k_b, v_b, causal=True, posOffset=0, **params)
+    last = orc.mla_attention(q[-1:], state, k_b, v_b, causal=True, posOffset=T - 1, **params)
+    assert np.array_equal(last[0], full[-1])
+    rows = orc.mla_attention_rows(q, state, k_b, v_b, rows=[(T - 1, 1), (2, 0)], causal=True, posOffset=0,
+                                  **params)
+    assert np.array_equal(rows[0], full[-1, Dv:]) and np.array_equal(rows[1], full[2, :Dv])
 
 
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -74,6 +74,24 @@ MUTANTS = [
      "const double position = (double)(offset + t) / pos_divisor;", "const double position = (double)t / pos_divisor;"),
     ("rope linear scaling ignored",
      "const double position = (double)(offset + t) / pos_divisor;", "const double position = (double)(offset + t);"),
+    # absorbed latent attention (IR schema page, $defs.op_mla_attention)
+    ("mla: rotary key dropped from the keys (qk_rope)",
+     "for (int i = 0; i < P; ++i) krow[N + i] = (double)c[R + i];",
+     "for (int i = 0; i < P; ++i) krow[N + i] = 0.0;"),
+    ("mla: rotary key read from the start of the latent row",
+     "for (int i = 0; i < P; ++i) krow[N + i] = (double)c[R + i];",
+     "for (int i = 0; i < P; ++i) krow[N + i] = (double)c[i];"),
+    ("mla: every head uses head 0's k_b block",
+     "const float* w = k_b + ((int64_t)h * N + i) * R;", "const float* w = k_b + ((int64_t)0 * N + i) * R;"),
+    ("mla: v_b read as [v_head_dim, heads] rows",
+     "const float* w = v_b + ((int64_t)h * Dv + e) * R;", "const float* w = v_b + ((int64_t)e * a->heads + h) * R;"),
+    ("mla: query heads strided by qk_nope (q is [T, heads*(qk_nope+qk_rope)])",
+     "const float* qrow = q + (t * (int64_t)a->heads + h) * Dq;",
+     "const float* qrow = q + (t * (int64_t)a->heads + h) * a->qk_nope;"),
+    ("mla: scale dropped",
+     "x[s] = a->scale * dot;", "x[s] = dot;"),
+    ("mla: posOffset ignored",
+     "const int64_t pos = a->pos_offset + t;", "const int64_t pos = t;"),
 ]
 
 
