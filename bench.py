@@ -2,13 +2,14 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vtmu|reference]
                     [--workload NAME] [--kernel auto|tc|ffma] [--no-cpu-baseline]
-                    [--no-prefill] [--cpu-budget SEC] [--prefill-cpu-budget SEC]
+                    [--no-prefill] [--no-mla] [--cpu-budget SEC] [--prefill-cpu-budget SEC]
 
 Workloads (seeded_inputs.WORKLOADS): gqa_decode (default), gqa_decode_rope
 (the same step with the rotary embedding fused in), gqa_spec_decode (4 query
 rows), gqa_decode_sinks (a window with attention sinks), gqa_prefill,
 swa_softcap_prefill, swa_sinks_prefill, latent_bias_prefill, alibi_prefill,
-tiny_prefill.  `--kernel ffma` forces the FFMA prefill (for a decode workload:
+tiny_prefill, mla_decode and mla_decode_v3 (absorbed latent attention, 16 and
+128 heads).  `--kernel ffma` forces the FFMA prefill (for a decode workload:
 the step as cache_writes + the FFMA prefill), `--kernel tc` the tensor cores.
 
 Default workload: the GQA decode step (Llama-3-8B shape): cache_write of one
@@ -28,7 +29,8 @@ alibi_prefill) with its step and kernel time, TFLOP/s, its tensor-pipe
 roofline against two ceilings (the measured bf16 rate scaled to 3xTF32, and
 the measured kind::tf32 rate per SM at the sampled SM clock), end-to-end
 TFLOP/s from host buffers and a bounded oracle sample; `--no-prefill` leaves
-them out.  `--impl reference` times the CPU oracle on the host cores instead,
+them out.  It also carries `mla`: the latent-attention decode step (mla_decode,
+DeepSeek-V2-Lite's shape) with its GB/s and both rooflines (`--no-mla`).  `--impl reference` times the CPU oracle on the host cores instead,
 on a bounded sample of the same workload.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
@@ -118,6 +120,28 @@ def prefill_flops(w):
     D = w["headDim"]
     Dv = w.get("vHeadDim") or D
     return visible_pairs(w) * w["heads"] * (2 * D + 2 * Dv)
+
+
+def mla_work(w):
+    """Algorithmic bytes and FLOPs of one latent-attention decode step: the
+    visible cache rows once (576 floats each), k_b and v_b once, q and out,
+    the new cache rows read and written; FLOPs of the absorbed form (query
+    absorption, 2 x 576 + 2 x 512 per visible (row, head, key), the output
+    projection)."""
+    H, R, N, P, Dv, off = w["heads"], w["kv_rank"], w["qk_nope"], w["qk_rope"], w["v_head_dim"], w["offset"]
+    T = w.get("rows", 1)
+    S = off + T
+    pos = np.arange(T, dtype=np.int64) + w["params"].get("posOffset", 0)
+    seen = np.zeros(S, dtype=bool)
+    for p in pos:
+        s = np.arange(S)
+        vis = s <= p if w["params"].get("causal", True) else np.ones(S, dtype=bool)
+        seen |= vis
+    Wd = R + P
+    nbytes = (int(seen.sum()) * Wd + H * N * R + H * Dv * R + T * H * (N + P) + T * H * Dv + 2 * T * Wd) * 4
+    pairs = int(visible_counts(pos, S, w["params"]).sum())
+    flops = 2 * T * H * N * R + pairs * H * (2 * Wd + 2 * R) + 2 * T * H * Dv * R
+    return nbytes, flops
 
 
 def load_peaks():
@@ -281,8 +305,9 @@ def workload_config(name, world):
     the replica count and how L2 is kept out of the timing (the same for both
     arms)."""
     w = si.WORKLOADS[name]
-    l2 = ("inputs > L2: two 256 MiB K/V cache sets alternate between steps" if w["kind"] == "decode"
-          else "L2 flushed between timed steps (256 MiB write, outside the timed events)")
+    l2 = {"decode": "inputs > L2: two 256 MiB K/V cache sets alternate between steps",
+          "mla_decode": "inputs > L2: four 72 MiB latent caches alternate between steps"}.get(
+        w["kind"], "L2 flushed between timed steps (256 MiB write, outside the timed events)")
     return {"workload": name, **{k: w[k] for k in w if k not in ("params", "kind")}, **w["params"],
             "parallelism": f"replicas x{world}", "l2": l2}
 
@@ -303,11 +328,20 @@ def oracle_decode_step(x, w):
     return oracle.attention(q, x["kc"], x["vc"], heads=H, headDim=D, kvHeads=Hk, **w["params"])
 
 
+def oracle_mla_step(x, w):
+    import oracle
+    off = w["offset"]
+    oracle.cache_write(x["state"], x["state_new"], off)
+    return oracle.mla_attention(x["q"], x["state"][:off + w.get("rows", 1)], x["k_b"], x["v_b"], heads=w["heads"],
+                                kv_rank=w["kv_rank"], qk_nope=w["qk_nope"], qk_rope=w["qk_rope"],
+                                v_head_dim=w["v_head_dim"], **w["params"])
+
+
 class OracleSampler:
     """Bounded samples of a workload computed by the oracle as it stands, on
-    all host cores.  decode: one whole decode step per sample; prefill: 16
-    query rows x all heads per sample (rows drawn at random), counted by their
-    visible pairs."""
+    all host cores.  decode and latent-attention decode: one whole decode
+    step per sample; prefill: 16 query rows x all heads per sample (rows
+    drawn at random), counted by their visible pairs."""
 
     ROWS = 16
 
@@ -327,6 +361,9 @@ class OracleSampler:
         if w["kind"] == "decode":
             oracle_decode_step(x, w)
             return decode_bytes(w)[1] / 1e9, time.perf_counter() - t0
+        if w["kind"] == "mla_decode":
+            oracle_mla_step(x, w)
+            return mla_work(w)[0] / 1e9, time.perf_counter() - t0
         H = w["heads"]
         D = w["headDim"]
         Dv = w.get("vHeadDim") or D
@@ -344,6 +381,9 @@ class OracleSampler:
     def describe(self, n):
         if self.w["kind"] == "decode":
             return f"{n} whole decode steps (cache_write x2 + attention over {self.w['offset'] + 1} keys)"
+        if self.w["kind"] == "mla_decode":
+            return (f"{n} whole latent decode steps (cache_write + {self.w['heads']} heads over "
+                    f"{self.w['offset'] + 1} latent rows)")
         return f"{n} samples of {self.ROWS} random query rows x all {self.w['heads']} heads"
 
 
@@ -642,6 +682,92 @@ def measure_decode(ctx, name):
             "launches_per_step": 3 if args.kernel == "ffma" else 1, "_window": window}
 
 
+def measure_mla(ctx, name):
+    """A latent-attention decode step (vtmu_mla_decode_step: the new latent
+    row written, queries absorbed, split-KV attention over the latent cache,
+    merge and output projection), W + K steps over four cache copies that
+    alternate (302 MB > L2, so every step reads its cache from HBM), then the
+    same step end to end from pinned host buffers."""
+    torch, vtmu, dev, stream, st, args = ctx.torch, ctx.vtmu, ctx.dev, ctx.stream, ctx.st, ctx.args
+    w = si.WORKLOADS[name]
+    x = si.workload_inputs(name)
+    H, N, Dv, off = w["heads"], w["qk_nope"], w["v_head_dim"], w["offset"]
+    T = w.get("rows", 1)
+    nbytes, flops = mla_work(w)
+    with torch.cuda.stream(stream):
+        states = [torch.from_numpy(x["state"]).to(dev) for _ in range(4)]
+        q = torch.from_numpy(x["q"]).to(dev)
+        k_b = torch.from_numpy(x["k_b"]).to(dev)
+        v_b = torch.from_numpy(x["v_b"]).to(dev)
+        sn = torch.from_numpy(x["state_new"]).to(dev)
+        out = torch.empty((T, H * Dv), dtype=torch.float32, device=dev)
+    p = vtmu.make_mla_params(T, off + T, heads=H, qk_nope=N, v_head_dim=Dv, kv_rank=w["kv_rank"],
+                             qk_rope=w["qk_rope"], **w["params"])
+    ws_bytes = vtmu.vtmu_mla_workspace_size(p)
+    ws = torch.zeros(ws_bytes, dtype=torch.uint8, device=dev)
+    max_rows = w["max_rows"]
+
+    def step(i, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        vtmu.vtmu_mla_decode_step(states[i % 4], max_rows, sn, T, off, q, k_b, v_b, out, p, ws, ws_bytes, st)
+        if ev is not None:
+            ev[1].record(stream)
+
+    step_ms, kern_ms, window = timed_loop(ctx, step, args.steps, args.warmup)
+    qh = torch.from_numpy(x["q"]).pin_memory()
+    snh = torch.from_numpy(x["state_new"]).pin_memory()
+    outh = torch.empty((T, H * Dv), dtype=torch.float32).pin_memory()
+
+    def e2e_step(i):
+        with torch.cuda.stream(stream):
+            q.copy_(qh, non_blocking=True)
+            sn.copy_(snh, non_blocking=True)
+        step(i)
+        with torch.cuda.stream(stream):
+            outh.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    e2e_step(0)
+    n_e2e = max(3, min(args.steps, 200))
+    barrier(ctx.world)
+    t0 = time.perf_counter()
+    for i in range(n_e2e):
+        e2e_step(i)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
+    e2e = {"value": round(nbytes / 1e9 * ctx.world / e2e_s, 3), "unit": "GB/s",
+           "h2d_bytes_per_step": (qh.numel() + snh.numel()) * 4, "d2h_bytes_per_step": outh.numel() * 4,
+           "steps": n_e2e}
+    del states, q, k_b, v_b, sn, out, ws
+    torch.cuda.empty_cache()
+    return {"workload": name, "x": x, "w": w, "step_bytes": nbytes, "flops": flops, "step_ms": step_ms,
+            "kernel_ms": kern_ms, "e2e": e2e, "_window": window}
+
+
+def mla_roofline(ctx, d, clocks):
+    """Both rooflines of the latent-attention step (its three launches timed
+    together): algorithmic bytes against the HBM copy peak and algorithmic
+    FLOPs against the FP32 FMA peak; `bound` is the one whose ideal time is
+    longer."""
+    peaks = ctx.peaks
+    t = d["kernel_ms"] / 1e3
+    sm = clocks.get("sm_mhz") or float(peaks.get("sm_max_mhz", 2070.0))
+    hbm = float(peaks["hbm_gbs"])
+    fp32 = SMS * FP32_LANES_PER_SM * 2 * sm * 1e6 / 1e12
+    gbs = d["step_bytes"] / t / 1e9
+    tfs = d["flops"] / t / 1e12
+    t_hbm = d["step_bytes"] / (hbm * 1e9)
+    t_alu = d["flops"] / (fp32 * 1e12)
+    hbm_line = {"achieved": round(gbs, 3), "peak": round(hbm, 1), "unit": "GB/s", "frac": round(gbs / hbm, 4),
+                "peak_source": ctx.peak_kind}
+    alu_line = {"achieved": round(tfs, 3), "peak": round(fp32, 1), "unit": "TFLOP/s", "frac": round(tfs / fp32, 4),
+                "peak_source": f"derived: {SMS} SMs x {FP32_LANES_PER_SM} FP32 lanes x 2 x {sm:.0f} MHz (sampled)"}
+    main, other = (alu_line, hbm_line) if t_alu > t_hbm else (hbm_line, alu_line)
+    return {"bound": "alu" if t_alu > t_hbm else "hbm", "kernel": "mla", **main,
+            "traffic": profile_traffic("mla__" + d["workload"]), "kernel_ms": round(d["kernel_ms"], 5),
+            "other_bound": other, "algorithmic_bytes": d["step_bytes"], "algorithmic_flop": d["flops"]}
+
+
 def run_vtmu(args, rank, world, local):
     import torch
     import f32_gqa_attention_gb300 as vtmu
@@ -658,6 +784,25 @@ def run_vtmu(args, rank, world, local):
     name = args.workload
     w = si.WORKLOADS[name]
 
+    if w["kind"] == "mla_decode":
+        d = measure_mla(ctx, name)
+        sampler.stop()
+        clocks = sampler.summary(*d["_window"])
+        cpu = None
+        if rank == 0 and not args.no_cpu_baseline:
+            val, sample, cores = time_oracle(name, w, budget_s=args.cpu_budget, x=d["x"])
+            cpu = {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+        line = {
+            "metric": METRIC, "value": round(d["step_bytes"] / 1e9 * world / (d["step_ms"] / 1e3), 3),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(d["step_ms"], 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": DATA, "config": workload_config(name, world),
+            "impl": "vtmu", "roofline": mla_roofline(ctx, d, clocks), "cpu_baseline": cpu, "e2e": d["e2e"],
+            "gpu_launches": 3 * args.steps, "clocks": clocks,
+        }
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+        return
     if w["kind"] == "decode":
         d = measure_decode(ctx, name)
         block = []
@@ -666,6 +811,7 @@ def run_vtmu(args, rank, world, local):
                 block.append(measure_prefill(ctx, pname, args.steps, args.warmup,
                                              cpu_budget=0.0 if args.no_cpu_baseline else args.prefill_cpu_budget,
                                              e2e_steps=3))
+        mla = None if args.no_mla else measure_mla(ctx, "mla_decode")
         sampler.stop()
         clocks = sampler.summary(*d["_window"])
         achieved = d["step_bytes"] / (d["kernel_ms"] / 1e3) / 1e9
@@ -688,6 +834,19 @@ def run_vtmu(args, rank, world, local):
         }
         if block:
             line["prefill"] = [finish_prefill(ctx, r) for r in block]
+        if mla is not None:
+            mclk = sampler.summary(*mla["_window"])
+            mcpu = None
+            if rank == 0 and not args.no_cpu_baseline:
+                val, sample, cores = time_oracle("mla_decode", mla["w"], budget_s=args.prefill_cpu_budget,
+                                                 min_samples=1, x=mla["x"])
+                mcpu = {"value": round(val, 5), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+            line["mla"] = {"workload": "mla_decode", "config": workload_config("mla_decode", world),
+                           "value": round(mla["step_bytes"] / 1e9 * world / (mla["step_ms"] / 1e3), 3),
+                           "unit": "GB/s", "ms_per_step": round(mla["step_ms"], 5),
+                           "kernel_ms": round(mla["kernel_ms"], 5), "steps": args.steps, "warmup": args.warmup,
+                           "roofline": mla_roofline(ctx, mla, mclk), "e2e": mla["e2e"], "cpu_baseline": mcpu,
+                           "gpu_launches": 3 * args.steps, "clocks": mclk}
     else:
         r = measure_prefill(ctx, name, args.steps, args.warmup, kernel_arg=args.kernel,
                             cpu_budget=0.0 if args.no_cpu_baseline else args.cpu_budget)
@@ -710,7 +869,7 @@ def run_reference(args, rank, world):
         return
     name = args.workload
     w = si.WORKLOADS[name]
-    unit = "GB/s" if w["kind"] == "decode" else "TFLOP/s"
+    unit = "GB/s" if w["kind"] in ("decode", "mla_decode") else "TFLOP/s"
     smp = OracleSampler(name, w)
     for _ in range(args.warmup):
         smp.sample()
@@ -743,6 +902,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode workloads: leave out the four prefill workloads that follow the decode line")
+    ap.add_argument("--no-mla", action="store_true",
+                    help="decode workloads: leave out the latent-attention decode step that follows the decode line")
     ap.add_argument("--prefill-cpu-budget", type=float, default=3.0,
                     help="seconds of oracle timing per prefill workload after a decode line")
     ap.add_argument("--kernel", choices=["auto", "tc", "ffma"], default="auto",

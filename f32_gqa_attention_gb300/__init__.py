@@ -34,7 +34,8 @@ VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREF
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
             "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",
             "vtmu_device_error", "vtmu_decode_step", "vtmu_decode_step_host_workspace_size",
-            "vtmu_decode_step_host", "vtmu_rope_params_init", "vtmu_rope", "vtmu_decode_step_rope")
+            "vtmu_decode_step_host", "vtmu_rope_params_init", "vtmu_rope", "vtmu_decode_step_rope",
+            "vtmu_mla_params_init", "vtmu_mla_workspace_size", "vtmu_mla_attention", "vtmu_mla_decode_step")
 NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 
@@ -86,6 +87,25 @@ class vtmu_rope_params(ctypes.Structure):
     ]
 
 
+class vtmu_mla_params(ctypes.Structure):
+    """Mirror of ``vtmu_mla_params`` (include/vtmu_attention.h)."""
+    _fields_ = [
+        ("T", ctypes.c_int64),
+        ("S", ctypes.c_int64),
+        ("heads", ctypes.c_int32),
+        ("kv_rank", ctypes.c_int32),
+        ("qk_nope", ctypes.c_int32),
+        ("qk_rope", ctypes.c_int32),
+        ("v_head_dim", ctypes.c_int32),
+        ("causal", ctypes.c_int32),
+        ("has_scale", ctypes.c_int32),
+        ("scale", ctypes.c_float),
+        ("pos_offset", ctypes.c_int64),
+        ("window", ctypes.c_int64),
+        ("sinks", ctypes.c_int64),
+    ]
+
+
 _lib = None
 _lib_lock = threading.Lock()
 
@@ -134,6 +154,16 @@ def load_library():
         lib.vtmu_decode_step_host.argtypes = [vp, vp, ctypes.c_int64, vp, vp, ctypes.c_int64, ctypes.c_int64,
                                               vp, vp, vp, P, vp, ctypes.c_size_t, vp]
         lib.vtmu_decode_step_host.restype = ctypes.c_int
+        M = ctypes.POINTER(vtmu_mla_params)
+        lib.vtmu_mla_params_init.argtypes = [M]
+        lib.vtmu_mla_params_init.restype = None
+        lib.vtmu_mla_workspace_size.argtypes = [M, ctypes.POINTER(ctypes.c_size_t)]
+        lib.vtmu_mla_workspace_size.restype = ctypes.c_int
+        lib.vtmu_mla_attention.argtypes = [vp, vp, vp, vp, vp, M, vp, ctypes.c_size_t, vp]
+        lib.vtmu_mla_attention.restype = ctypes.c_int
+        lib.vtmu_mla_decode_step.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp,
+                                             M, vp, ctypes.c_size_t, vp]
+        lib.vtmu_mla_decode_step.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -243,6 +273,33 @@ def vtmu_attention_decode_noalloc(q, k, v, bias, out, p: vtmu_attention_params, 
     capture); calls that overlap on the GPU race on the shared scratch."""
     _check(load_library().vtmu_attention_decode_noalloc(_addr(q), _addr(k), _addr(v), _addr(bias), _addr(out),
                                                         ctypes.byref(p), stream or None))
+
+
+def vtmu_mla_params_init() -> vtmu_mla_params:
+    p = vtmu_mla_params()
+    load_library().vtmu_mla_params_init(ctypes.byref(p))
+    return p
+
+
+def vtmu_mla_workspace_size(p: vtmu_mla_params) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().vtmu_mla_workspace_size(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
+def vtmu_mla_attention(q, state, k_b, v_b, out, p: vtmu_mla_params, workspace, workspace_bytes: int,
+                       stream: int = 0) -> None:
+    _check(load_library().vtmu_mla_attention(_addr(q), _addr(state), _addr(k_b), _addr(v_b), _addr(out),
+                                             ctypes.byref(p), _addr(workspace), int(workspace_bytes),
+                                             stream or None))
+
+
+def vtmu_mla_decode_step(state, max_rows: int, state_new, new_rows: int, offset: int, q, k_b, v_b, out,
+                         p: vtmu_mla_params, workspace, workspace_bytes: int, stream: int = 0) -> None:
+    _check(load_library().vtmu_mla_decode_step(_addr(state), int(max_rows), _addr(state_new), int(new_rows),
+                                               int(offset), _addr(q), _addr(k_b), _addr(v_b), _addr(out),
+                                               ctypes.byref(p), _addr(workspace), int(workspace_bytes),
+                                               stream or None))
 
 
 def vtmu_device_error() -> int:
@@ -444,3 +501,62 @@ def cache_write(cache, values, offset: int, stream=None):
     st = stream if stream is not None else torch.cuda.current_stream(cache.device).cuda_stream
     vtmu_cache_write(cache, cache.shape[0], cache.shape[1], values, values.shape[0], offset, st)
     return cache
+
+
+def make_mla_params(T, S, *, heads, kv_rank=512, qk_nope, qk_rope=64, v_head_dim, scale=None, causal=True,
+                    posOffset=0, window=None, sinks=None):
+    """An mla params struct from the IR page's parameter names (mla_attention)."""
+    p = vtmu_mla_params_init()
+    p.T, p.S = int(T), int(S)
+    p.heads, p.kv_rank, p.qk_nope, p.qk_rope, p.v_head_dim = (int(heads), int(kv_rank), int(qk_nope), int(qk_rope),
+                                                              int(v_head_dim))
+    p.causal = 1 if causal else 0
+    if scale is not None:
+        p.has_scale, p.scale = 1, float(scale)
+    p.pos_offset = int(posOffset)
+    p.window = 0 if window is None else int(window)
+    p.sinks = 0 if sinks is None else int(sinks)
+    return p
+
+
+def mla_attention(q, state, k_b, v_b, *, heads, qk_nope, v_head_dim, out=None, workspace=None, stream=None,
+                  S=None, **params):
+    """mla_attention on CUDA tensors: q [T, heads*(qk_nope+qk_rope)], state
+    [rows, kv_rank+qk_rope] (its first S rows are read; all by default),
+    k_b [heads*qk_nope, kv_rank], v_b [heads*v_head_dim, kv_rank]; returns
+    out [T, heads*v_head_dim] (float32)."""
+    import torch
+    T = q.shape[0]
+    p = make_mla_params(T, state.shape[0] if S is None else S, heads=heads, qk_nope=qk_nope,
+                        v_head_dim=v_head_dim, **params)
+    for name, t in (("q", q), ("state", state), ("k_b", k_b), ("v_b", v_b)):
+        if not t.is_cuda or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous float32 CUDA tensor")
+    if out is None:
+        out = torch.empty((T, heads * v_head_dim), dtype=torch.float32, device=q.device)
+    nbytes = vtmu_mla_workspace_size(p)
+    ws = workspace if workspace is not None else _default_workspace(q.device)
+    buf, cap = ws.get(nbytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    vtmu_mla_attention(q, state, k_b, v_b, out, p, buf, cap, st)
+    return out
+
+
+def mla_decode_step(state, state_new, offset: int, q, k_b, v_b, *, heads, qk_nope, v_head_dim, out=None,
+                    workspace=None, stream=None, **params):
+    """A latent-attention decode step on CUDA tensors: cache_write of
+    state_new into state at row ``offset``, then mla_attention over the
+    first offset + new rows of the cache (posOffset defaulting to the last
+    new row).  Returns out."""
+    import torch
+    T, R = q.shape[0], state_new.shape[0]
+    params.setdefault("posOffset", offset + R - T)
+    p = make_mla_params(T, offset + R, heads=heads, qk_nope=qk_nope, v_head_dim=v_head_dim, **params)
+    if out is None:
+        out = torch.empty((T, heads * v_head_dim), dtype=torch.float32, device=q.device)
+    nbytes = vtmu_mla_workspace_size(p)
+    ws = workspace if workspace is not None else _default_workspace(q.device)
+    buf, cap = ws.get(nbytes)
+    st = stream if stream is not None else torch.cuda.current_stream(q.device).cuda_stream
+    vtmu_mla_decode_step(state, state.shape[0], state_new, R, offset, q, k_b, v_b, out, p, buf, cap, st)
+    return out

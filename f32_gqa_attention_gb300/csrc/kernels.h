@@ -78,4 +78,40 @@ cudaError_t launch_rope(const float* x, float* out, int64_t T, int H, int D, int
 cudaError_t launch_cache_write(float* cache, int64_t width, const float* values, int64_t rows,
                                int64_t offset, cudaStream_t stream);
 
+// ---- absorbed latent attention (mla_attention), decode form ------------------------
+// The latent cache row is [latent (kMlaKvRank) | rotary key (kMlaRope)].
+constexpr int kMlaKvRank = 512;
+constexpr int kMlaRope = 64;
+struct MlaDesc {
+    const float* q;      // [T, H * (N + kMlaRope)]
+    const float* state;  // [S, kMlaKvRank + kMlaRope] (first S rows read)
+    const float* k_b;    // [H * N, kMlaKvRank]
+    const float* v_b;    // [H * Dv, kMlaKvRank]
+    float* out;          // [T, H * Dv]
+    int64_t T, S;
+    int32_t H, N, Dv;
+    int32_t causal;
+    int64_t pos_offset, window, sinks;
+    float qscale;        // scale * log2 e, folded into the absorbed queries
+};
+// The new cache rows of a decode step (state_new == nullptr: none), written
+// by the first launch: state[offset + r, :] = state_new[r, :].
+struct MlaCacheWrite {
+    float* state;
+    const float* state_new;
+    int64_t rows, offset;
+};
+struct MlaPlan {
+    int32_t hq = 2;           // head quads per CTA (4 * hq virtual heads)
+    int32_t groups = 1;       // CTAs per split (virtual heads / (4 * hq))
+    int32_t splits = 1;
+    int32_t sink_splits = 0;
+    int64_t lo = 0, hi = 0, sink_end = 0, per = 32;
+    size_t qabs_off = 0, m_off = 0, l_off = 0, o_off = 0, workspace_bytes = 0;
+};
+void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan);
+cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, const MlaCacheWrite& cw,
+                       cudaStream_t stream);
+unsigned int mla_take_device_error();
+
 }  // namespace vtmu

@@ -2,11 +2,10 @@
 //
 // Op "attention" (vtmu.mpakt.dev/api/ops), f32 in and out.  Both
 // contractions run on kind::tf32 UMMAs with error compensation: every f32
-// operand x is split into hi = x with the low 13 mantissa bits cleared
-// (exactly a tf32 value) and lo = x - hi (exact in f32), and each product
-// A.B is issued as A_hi.B_hi + A_hi.B_lo + A_lo.B_hi into one f32
-// accumulator.  The dropped A_lo.B_lo term and the tf32 rounding of lo are
-// both of order 2^-21 relative, so the result matches an f32 FMA kernel.
+// operand x is split into hi = x rounded to the nearest tf32 value and
+// lo = x - hi, itself rounded to tf32 (|x - hi - lo| <= 2^-22 |x|), and
+// each product A.B is issued as A_hi.B_hi + A_hi.B_lo + A_lo.B_hi into f32
+// accumulators.  The dropped A_lo.B_lo term is below 2^-22 relative.
 // Single-pass TF32 is never used.
 //
 // Work split:
@@ -28,7 +27,8 @@
 //    the 64 K_hi rows followed by the 64 K_lo rows, i.e. a 128-row B operand,
 //    so Q_hi.[K_hi; K_lo]^T lands as [S_hihi | S_hilo] in 128 TMEM columns at
 //    the full N = 128 tensor rate; the third product Q_lo.K_hi (N = 64)
-//    accumulates into the first half and the softmax adds the two halves;
+//    accumulates into the second half, with the other small product, and
+//    the softmax adds the two halves;
 //  * TMEM columns: Q_hi | O | S | P.  At headDim <= 128 S and P are separate
 //    128-column buffers: the score MMAs of tile j+1 start as soon as the
 //    softmax has read S_j and run while it works on tile j; P_j (hi | lo)
@@ -112,6 +112,12 @@ struct TcCfg {
     static constexpr int NCOL = kBN * 4 / SMW;  // keys per softmax thread and tile
     static constexpr int THREADS = PMODE == 0 ? 32 * (2 + SMW) : 224;
     static constexpr bool SPLIT = PMODE != 0;  // S and P apart
+    // With P over S the softmax warps fold O into registers every tile: each
+    // tile's P.V starts a fresh TMEM accumulator and is added to the running
+    // total in f32 round-to-nearest.  The tensor pipe's accumulation rounds
+    // toward zero, so a total built in TMEM over thousands of keys shrinks by
+    // ~1e-5 relative; per tile the shrink stays ~1e-7 and does not add up.
+    static constexpr bool FOLD = PMODE == 0;
     static constexpr int SCOLS = 2 * kBN;
     static constexpr int QLO_FLOATS = kBM * D;                 // Q_lo: KB x [128 x 32]
     static constexpr int PLO_FLOATS = PMODE == 1 ? kBM * kBN : 0;  // P_lo: 2 x [128 x 32]
@@ -498,7 +504,10 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
                                QSUB_D = kBM * 32 * 4 / 16,
                                VCH_D = C::VCHUNK_FLOATS * 4 / 16, VLO_D = DVC * 32 * 4 / 16, KSTEP_D = 32 / 16,
                                PLO_CHUNK_D = kBM * 32 * 4 / 16;
-            // S: [Q_hi K_hi^T + Q_lo K_hi^T | Q_hi K_lo^T].
+            // S: [Q_hi K_hi^T | Q_hi K_lo^T + Q_lo K_hi^T]: the two small
+            // correction products share the second half, so the large first
+            // half takes one product per k-step (the tensor pipe truncates each
+            // accumulation, with an error relative to the accumulator).
             auto issue_s = [&](int j) -> bool {
                 const uint32_t d = tmem + C::S;
                 const int it0 = s_first(j);
@@ -521,7 +530,7 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
                                     mma_tf32_ts(d, a_hi, bk, id_s2, 0u);
                                 else
                                     mma_tf32_ts_acc(d, a_hi + k * 8, bk, id_s2);
-                                mma_tf32_ss_acc(d, a_lo + k * KSTEP_D, bk, id_s);
+                                mma_tf32_ss_acc(d + kBN, a_lo + k * KSTEP_D, bk, id_s);
                             }
                         }
                     }
@@ -539,7 +548,7 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
                 for (int k = 0; k < 4; ++k) {
                     const uint32_t col = c * 32 + k * 8;
                     if (c == 0 && k == 0)
-                        mma_tf32_ts(o, p_hi + col, v_hi + k * KSTEP_D, id_o, j > 0 ? 1u : 0u);
+                        mma_tf32_ts(o, p_hi + col, v_hi + k * KSTEP_D, id_o, (C::FOLD || j == 0) ? 0u : 1u);
                     else
                         mma_tf32_ts_acc(o, p_hi + col, v_hi + k * KSTEP_D, id_o);
                     mma_tf32_ts_acc(o, p_hi + col, v_lo + k * KSTEP_D, id_o);
@@ -641,7 +650,7 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
                     const float vv[4] = {v4.x, v4.y, v4.z, v4.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        hi[4 * c + e] = tf32_hi(vv[e]);
+                        hi[4 * c + e] = tf32_trunc(vv[e]);
                         lo[4 * c + e] = vv[e] - hi[4 * c + e];
                     }
                 }
@@ -702,6 +711,11 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
         if (bstage && n_tiles > 0) issue_bias(0);
         const int feat = (a.softcap_on ? 1 : 0) | (a.alibi_on ? 2 : 0) | (a.bias_kind ? 4 : 0);
         float m_ref = -INFINITY, l = 0.f;
+        // FOLD: this thread's O columns, summed over the tiles folded so far
+        // (in units of the current reference max).
+        float otot[C::FOLD ? OCOLS : 1];
+#pragma unroll
+        for (int i = 0; i < (C::FOLD ? OCOLS : 1); ++i) otot[i] = 0.f;
         bool ok = true;
         for (int j = 0; j < n_tiles; ++j) {
             bool got = __all_sync(FULL, mbar_wait(&s_full, j & 1));
@@ -824,7 +838,7 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
             const uint64_t m1 = f2_pack(-1.f, -1.f);
 #pragma unroll
             for (int i = 0; i < NCOL; i += 2) {  // P_hi replaces P in registers; P_lo = P - P_hi (exact)
-                const float h0 = tf32_hi(x[i]), h1 = tf32_hi(x[i + 1]);
+                const float h0 = tf32_trunc(x[i]), h1 = tf32_trunc(x[i + 1]);
                 f2_unpack(f2_fma(f2_pack(h0, h1), m1, f2_pack(x[i], x[i + 1])), plo[i], plo[i + 1]);
                 x[i] = h0;
                 x[i + 1] = h1;
@@ -855,7 +869,22 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
 #pragma unroll
                 for (int c = 0; c < NCOL; c += 32) tmem_st32(trow + C::P + kBN + c0 + c, plo + c);
             }
-            if (j > 0 && __any_sync(FULL, alpha != 1.f)) {
+            if constexpr (C::FOLD) {
+                // O holds P.V_{j-1} alone (S_j has landed, so it is done, and
+                // P.V_j overwrites it only after this warp's p_full arrival):
+                // add it to the total, then bring the total to this tile's max.
+                if (j >= 1) {
+#pragma unroll
+                    for (int c = 0; c < OCOLS; c += 32) {
+                        float o[32];
+                        tmem_ld32(trow + C::O + oc0 + c, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) otot[c + i] = (otot[c + i] + o[i]) * alpha;
+                    }
+                }
+            }
+            if (!C::FOLD && j > 0 && __any_sync(FULL, alpha != 1.f)) {
 #pragma unroll 1
                 for (int c = oc0; c < oc0 + OCOLS; c += 32) {
                     float o[32];
@@ -894,9 +923,17 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
         tc_fence_after();
         const float inv = (ok && l > 0.f) ? 1.f / l : 0.f;
         float* orow = a.out + t * (int64_t)a.H * DV + (int64_t)h * DV + dv0;
-#pragma unroll 1
-        for (int c = oc0; c < oc0 + OCOLS; c += 32) {
-            float o[32];
+        // Row r's output: O / l (with FOLD: the folded total plus the last
+        // tile's P.V, in an unrolled loop so that the total stays in registers).
+        auto store_row = [&](int c, float (&o)[32]) {
+            if (row_ok) {
+#pragma unroll
+                for (int i = 0; i < 32; i += 4)
+                    *reinterpret_cast<float4*>(orow + c + i) =
+                        make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            }
+        };
+        auto load_o = [&](int c, float (&o)[32]) {
             if (n_tiles > 0) {
                 tmem_ld32(trow + C::O + c, o);
                 tmem_wait_ld();
@@ -904,11 +941,22 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 32; ++i) o[i] = 0.f;
             }
-            if (row_ok) {
+        };
+        if constexpr (C::FOLD) {
 #pragma unroll
-                for (int i = 0; i < 32; i += 4)
-                    *reinterpret_cast<float4*>(orow + c + i) =
-                        make_float4(o[i] * inv, o[i + 1] * inv, o[i + 2] * inv, o[i + 3] * inv);
+            for (int cc = 0; cc < OCOLS; cc += 32) {
+                float o[32];
+                load_o(oc0 + cc, o);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) o[i] += otot[cc + i];
+                store_row(oc0 + cc, o);
+            }
+        } else {
+#pragma unroll 1
+            for (int c = oc0; c < oc0 + OCOLS; c += 32) {
+                float o[32];
+                load_o(c, o);
+                store_row(c, o);
             }
         }
     }
@@ -936,17 +984,17 @@ __global__ void split_k_kernel(const float* __restrict__ k, float* __restrict__ 
         float4* lo4 = reinterpret_cast<float4*>(klo);
         for (int64_t i = i0; i < n / 4; i += stride) {
             const float4 x = __ldg(k4 + i);
-            const float4 h = make_float4(tf32_hi(x.x), tf32_hi(x.y), tf32_hi(x.z), tf32_hi(x.w));
+            const float4 h = make_float4(tf32_rna(x.x), tf32_rna(x.y), tf32_rna(x.z), tf32_rna(x.w));
             hi4[i] = h;
-            lo4[i] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+            lo4[i] = make_float4(tf32_rna(x.x - h.x), tf32_rna(x.y - h.y), tf32_rna(x.z - h.z), tf32_rna(x.w - h.w));
         }
         return;
     }
     for (int64_t i = i0; i < n; i += stride) {
         const float x = __ldg(k + i);
-        const float hi = tf32_hi(x);
+        const float hi = tf32_rna(x);
         khi[i] = hi;
-        klo[i] = x - hi;
+        klo[i] = tf32_rna(x - hi);
     }
 }
 
@@ -974,9 +1022,9 @@ __global__ void split_vt_kernel(const float* __restrict__ v, float* __restrict__
         const int64_t s = s0 + threadIdx.x;
         if (c < cols && s < s_pad) {
             const float x = tile[threadIdx.x][r];
-            const float hi = tf32_hi(x);
+            const float hi = tf32_rna(x);
             vthi[(int64_t)c * s_pad + s] = hi;
-            vtlo[(int64_t)c * s_pad + s] = x - hi;
+            vtlo[(int64_t)c * s_pad + s] = tf32_rna(x - hi);
         }
     }
 }

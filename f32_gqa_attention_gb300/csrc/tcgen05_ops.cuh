@@ -139,8 +139,34 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// tf32 split of x: hi keeps the sign, exponent and top 10 mantissa bits
-// (exactly representable in tf32), lo = x - hi (exact in f32).
-__device__ __forceinline__ float tf32_hi(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
+// tf32 split of an f32 x into hi + lo, both tf32 values: hi is x rounded to
+// the nearest tf32 value (sign, exponent and 10 mantissa bits), lo = x - hi
+// (exact in f32, at most 2^-11 |x|) rounded to the nearest tf32 value, so
+// |x - hi - lo| <= 2^-22 |x|.  The MMA reads a 32-bit operand as tf32 by
+// ignoring its low 13 bits (truncation), which would leave up to 2^-20 |x|;
+// rounding before the MMA sees the value gives the 4x tighter split.
+
+// Nearest tf32 value, ties away from zero (the PTX conversion; NaN and
+// infinities pass through).  For the memory-bound pre-pass.
+__device__ __forceinline__ float tf32_rna(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return __uint_as_float(r & 0xFFFFE000u);
+}
+
+// The same rounding by integer arithmetic on the bit pattern (adding half a
+// tf32 ulp to the magnitude bits; a carry into the exponent is the correct
+// round-up), two integer operations; NaN and infinities pass through.
+__device__ __forceinline__ float tf32_round(float x) {
+    const uint32_t b = __float_as_uint(x);
+    const uint32_t r = (b & 0x7F800000u) == 0x7F800000u ? b : b + 0x1000u;
+    return __uint_as_float(r & 0xFFFFE000u);
+}
+
+// x with its low 13 mantissa bits cleared (a tf32 value, |x| - |hi| below
+// 2^-10 |x|), one operation: for the softmax probabilities, whose lo = x - hi
+// is then exact and non-negative (the MMA's truncation of lo leaves at most
+// 2^-20 P, a shrink of the weights far below the score error).
+__device__ __forceinline__ float tf32_trunc(float x) { return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u); }
 
 }  // namespace vtmu

@@ -289,6 +289,49 @@ HostStaging host_staging(const Resolved& r, int64_t new_rows) {
     return h;
 }
 
+// Checks of mla_attention's parameters that need no pointer; fills the
+// kernels' description (pointers excepted).
+vtmu_status resolve_mla(const vtmu_mla_params* p, vtmu::MlaDesc* m) {
+    if (!p) return fail(VTMU_ERR_INVALID, "mla params is NULL");
+    std::memset(m, 0, sizeof(*m));
+    if (p->T < 0 || p->S < 0)
+        return fail(VTMU_ERR_INVALID, "mla: T and S must be >= 0 (got %lld, %lld)", (long long)p->T, (long long)p->S);
+    if (p->heads <= 0) return fail(VTMU_ERR_INVALID, "mla: heads must be > 0 (got %d)", p->heads);
+    if (p->kv_rank <= 0 || p->qk_rope < 0 || p->qk_nope < 0 || p->v_head_dim <= 0 || p->qk_nope + p->qk_rope <= 0)
+        return fail(VTMU_ERR_INVALID, "mla: kv_rank, v_head_dim must be > 0 and qk_nope, qk_rope >= 0");
+    if (p->kv_rank != vtmu::kMlaKvRank || p->qk_rope != vtmu::kMlaRope)
+        return fail(VTMU_ERR_UNSUPPORTED, "mla: this build serves kv_rank %d with qk_rope %d (got %d, %d)",
+                    vtmu::kMlaKvRank, vtmu::kMlaRope, p->kv_rank, p->qk_rope);
+    if (p->qk_nope > 512) return fail(VTMU_ERR_UNSUPPORTED, "mla: qk_nope %d above 512", p->qk_nope);
+    if (p->v_head_dim > 4096) return fail(VTMU_ERR_UNSUPPORTED, "mla: v_head_dim %d above 4096", p->v_head_dim);
+    if (p->pos_offset < 0) return fail(VTMU_ERR_RANGE, "mla: posOffset must be >= 0 (got %lld)", (long long)p->pos_offset);
+    if (p->window < 0 || p->sinks < 0) return fail(VTMU_ERR_INVALID, "mla: window and sinks must be >= 0");
+    if (p->has_scale && !std::isfinite(p->scale)) return fail(VTMU_ERR_INVALID, "mla: scale must be finite");
+    if (p->S >= ((int64_t)1 << 31)) return fail(VTMU_ERR_UNSUPPORTED, "mla: S above 2^31 - 1");
+    if (p->T * (int64_t)p->heads > 65536)
+        return fail(VTMU_ERR_UNSUPPORTED, "mla: T * heads %lld above 65536 (this is the decode form)",
+                    (long long)(p->T * (int64_t)p->heads));
+    m->T = p->T;
+    m->S = p->S;
+    m->H = p->heads;
+    m->N = p->qk_nope;
+    m->Dv = p->v_head_dim;
+    m->causal = p->causal ? 1 : 0;
+    m->pos_offset = p->pos_offset;
+    m->window = p->window;
+    m->sinks = p->window > 0 ? p->sinks : 0;  // without a window no key is dropped
+    const double scale = p->has_scale ? (double)p->scale : 1.0 / std::sqrt((double)(p->qk_nope + p->qk_rope));
+    m->qscale = (float)(scale * 1.4426950408889634);
+    return VTMU_OK;
+}
+
+size_t mla_workspace(const vtmu::MlaDesc& m) {
+    // Upper bound over devices: the most splits the plan can choose.
+    vtmu::MlaPlan plan;
+    vtmu::mla_plan(m, 1 << 20, &plan);
+    return plan.workspace_bytes;
+}
+
 }  // namespace
 
 namespace vtmu {
@@ -635,6 +678,106 @@ vtmu_status vtmu_cache_write(float* cache, int64_t max_rows, int64_t width, cons
     return ok();
 }
 
+void vtmu_mla_params_init(vtmu_mla_params* p) {
+    if (!p) return;
+    std::memset(p, 0, sizeof(*p));
+    p->causal = 1;
+    p->kv_rank = vtmu::kMlaKvRank;
+    p->qk_rope = vtmu::kMlaRope;
+}
+
+vtmu_status vtmu_mla_workspace_size(const vtmu_mla_params* p, size_t* bytes) {
+    if (!bytes) return fail(VTMU_ERR_INVALID, "bytes is NULL");
+    vtmu::MlaDesc m;
+    vtmu_status st = resolve_mla(p, &m);
+    if (st != VTMU_OK) return st;
+    *bytes = mla_workspace(m);
+    return ok();
+}
+
+// mla_attention after resolve_mla(), with the decode step's cache write.
+static vtmu_status run_mla(vtmu::MlaDesc& m, const float* q, const float* state, const float* k_b,
+                           const float* v_b, float* out, void* workspace, size_t workspace_bytes,
+                           const vtmu::MlaCacheWrite& cw, cudaStream_t stream) {
+    if (m.T > 0) {
+        if (!q || !k_b || !v_b || !out || (m.S > 0 && !state))
+            return fail(VTMU_ERR_INVALID, "mla: q, state, k_b, v_b or out is NULL");
+        if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_b) | reinterpret_cast<uintptr_t>(out)) & 3u)
+            return fail(VTMU_ERR_INVALID, "mla: q, k_b and out must be 4-byte aligned");
+        if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(v_b)) & 15u)
+            return fail(VTMU_ERR_INVALID, "mla: state and v_b must be 16-byte aligned");
+        const size_t W = (size_t)vtmu::kMlaKvRank + vtmu::kMlaRope;
+        const size_t out_b = (size_t)m.T * m.H * m.Dv * 4;
+        if (overlaps(out, out_b, q, (size_t)m.T * m.H * (m.N + vtmu::kMlaRope) * 4) ||
+            overlaps(out, out_b, state, (size_t)m.S * W * 4) ||
+            overlaps(out, out_b, k_b, (size_t)m.H * m.N * vtmu::kMlaKvRank * 4) ||
+            overlaps(out, out_b, v_b, (size_t)m.H * m.Dv * vtmu::kMlaKvRank * 4))
+            return fail(VTMU_ERR_INVALID, "mla: out overlaps an input");
+    }
+    vtmu::MlaPlan plan;
+    vtmu::mla_plan(m, device_sm_count(), &plan);
+    if (!workspace || workspace_bytes < plan.workspace_bytes)
+        return fail(VTMU_ERR_WORKSPACE, "mla needs a workspace of %zu bytes (got %zu)", mla_workspace(m),
+                    workspace ? workspace_bytes : (size_t)0);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+    m.q = q;
+    m.state = state;
+    m.k_b = k_b;
+    m.v_b = v_b;
+    m.out = out;
+    cudaError_t e = vtmu::launch_mla(m, plan, workspace, cw, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla launch");
+    return ok();
+}
+
+vtmu_status vtmu_mla_attention(const float* q, const float* state, const float* k_b, const float* v_b, float* out,
+                               const vtmu_mla_params* p, void* workspace, size_t workspace_bytes,
+                               cudaStream_t stream) {
+    vtmu::MlaDesc m;
+    vtmu_status st = resolve_mla(p, &m);
+    if (st != VTMU_OK) return st;
+    if (m.T == 0) return ok();
+    const vtmu::MlaCacheWrite none{nullptr, nullptr, 0, 0};
+    return run_mla(m, q, state, k_b, v_b, out, workspace, workspace_bytes, none, stream);
+}
+
+vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const float* state_new, int64_t new_rows,
+                                 int64_t offset, const float* q, const float* k_b, const float* v_b, float* out,
+                                 const vtmu_mla_params* p, void* workspace, size_t workspace_bytes,
+                                 cudaStream_t stream) {
+    vtmu::MlaDesc m;
+    vtmu_status st = resolve_mla(p, &m);
+    if (st != VTMU_OK) return st;
+    if (max_rows < 0 || new_rows < 0)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step: negative size (max_rows %lld, new_rows %lld)",
+                    (long long)max_rows, (long long)new_rows);
+    if (offset < 0 || offset > max_rows || new_rows > max_rows - offset)
+        return fail(VTMU_ERR_RANGE, "mla_decode_step: offset %lld + rows %lld exceeds maxRows %lld",
+                    (long long)offset, (long long)new_rows, (long long)max_rows);
+    if (m.S > max_rows)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step: S %lld exceeds the cache's %lld rows", (long long)m.S,
+                    (long long)max_rows);
+    const size_t W = (size_t)vtmu::kMlaKvRank + vtmu::kMlaRope;
+    vtmu::MlaCacheWrite cw{nullptr, nullptr, 0, 0};
+    if (new_rows > 0) {
+        if (!state || !state_new) return fail(VTMU_ERR_INVALID, "mla_decode_step: state or state_new is NULL");
+        if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(state_new)) & 15u)
+            return fail(VTMU_ERR_INVALID, "mla_decode_step: state and state_new must be 16-byte aligned");
+        if (overlaps(state, (size_t)max_rows * W * 4, state_new, (size_t)new_rows * W * 4))
+            return fail(VTMU_ERR_INVALID, "mla_decode_step: state_new overlaps the cache");
+        if (out && overlaps(out, (size_t)m.T * m.H * m.Dv * 4, state, (size_t)max_rows * W * 4))
+            return fail(VTMU_ERR_INVALID, "mla_decode_step: out overlaps the cache");
+        cw = vtmu::MlaCacheWrite{state, state_new, new_rows, offset};
+    }
+    if (m.T == 0) {  // the cache write alone
+        if (new_rows == 0) return ok();
+        cudaError_t e = vtmu::launch_cache_write(state, (int64_t)W, state_new, new_rows, offset, stream);
+        return e == cudaSuccess ? ok() : cuda_fail(e, "cache_write launch");
+    }
+    return run_mla(m, q, state, k_b, v_b, out, workspace, workspace_bytes, cw, stream);
+}
+
 const char* vtmu_features(void) {
     return "attention.alibi attention.bias attention.scale attention.softcap attention.window rope.interleaved "
            "rope.rotaryDim";
@@ -647,7 +790,7 @@ vtmu_status vtmu_device_error(unsigned int* flags) {
     *flags = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device_error: synchronize");
-    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error();
+    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error() | vtmu::mla_take_device_error();
     return ok();
 }
 

@@ -346,6 +346,88 @@ VTMU_API vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64
                                            void* workspace, size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Absorbed latent attention: mla_attention of the IR schema page
+ * (graph_ir_schema.h, $defs.op_mla_attention: heads, kv_rank, qk_nope,
+ * qk_rope, v_head_dim, the up-projections k_b and v_b, scale, causal,
+ * window, sinks), read as DeepSeek-V2's multi-head latent attention.
+ *   state [max_rows, kv_rank + qk_rope]: latent KV cache; row s is
+ *       [c_s (kv_rank) | r_s (qk_rope)], the compressed latent and the
+ *       rotary key shared by every head (the first S rows are read)
+ *   q     [T, heads*(qk_nope + qk_rope)]: per head the no-rope part, then
+ *       the rotary part (already turned)
+ *   k_b   [heads*qk_nope, kv_rank], v_b [heads*v_head_dim, kv_rank]: the
+ *       up-projections as a checkpoint stores them ([out, in])
+ *   out   [T, heads*v_head_dim]
+ * Head h's key at s is [k_b_h c_s | r_s] and its value v_b_h c_s (k_b_h,
+ * v_b_h: head h's rows); query row t at position pos_offset + t scores
+ * x = scale * q . key over the visible keys (causal, window and sinks as for
+ * op "attention"), and the output is the max-subtracted softmax of the scores
+ * applied to the values (zeros when no key is visible).  The kernels compute
+ * it in the absorbed order: every head's query is taken through k_b_h into
+ * the latent space, so all heads read the same 576-wide cache rows once, and
+ * the weighted latent is taken through v_b_h at the end.
+ * This build serves kv_rank 512 with qk_rope 64 (DeepSeek-V2 and -V3),
+ * qk_nope 0..512, v_head_dim 1..4096 and T * heads <= 65536 (the decode
+ * form: it reads the cache once per 32 query rows x heads); other widths are
+ * refused with VTMU_ERR_UNSUPPORTED.
+ */
+typedef struct vtmu_mla_params {
+    int64_t T;            /* query rows (0 is a no-op) */
+    int64_t S;            /* cache rows the attention reads */
+    int32_t heads;        /* > 0 */
+    int32_t kv_rank;      /* latent width (params_init: 512) */
+    int32_t qk_nope;      /* no-rope query/key width per head */
+    int32_t qk_rope;      /* rotary width, shared by the heads (params_init: 64) */
+    int32_t v_head_dim;   /* value width per head, > 0 */
+    int32_t causal;       /* default 1 */
+    int32_t has_scale;    /* 0: scale = 1/sqrt(qk_nope + qk_rope) */
+    float scale;          /* used when has_scale != 0; must be finite */
+    int64_t pos_offset;   /* absolute position of query row 0, >= 0 */
+    int64_t window;       /* 0 = off; as for op "attention" */
+    int64_t sinks;        /* with a window: keys s < sinks stay visible */
+} vtmu_mla_params;
+
+/* Writes the defaults: causal = 1, kv_rank 512, qk_rope 64, the rest 0. */
+VTMU_API void vtmu_mla_params_init(vtmu_mla_params* p);
+
+/* Scratch bytes vtmu_mla_attention / vtmu_mla_decode_step need for `p` (the
+ * absorbed queries and the split partials), an upper bound over devices.
+ * Errors: those of vtmu_mla_attention's parameter checks. */
+VTMU_API vtmu_status vtmu_mla_workspace_size(const vtmu_mla_params* p, size_t* bytes);
+
+/*
+ * mla_attention (IR schema page, $defs.op_mla_attention).  q, k_b, out:
+ * DEVICE, 4-byte aligned; state, v_b: DEVICE, 16-byte aligned; out must not
+ * overlap an input.  workspace: DEVICE, at least vtmu_mla_workspace_size()
+ * bytes, 256-byte aligned, no initial contents needed; calls that share a
+ * workspace must not overlap on the GPU.  Three launches on `stream`.
+ * Errors: VTMU_ERR_INVALID (null or misaligned pointer, negative sizes or
+ * window/sinks, scale not finite, out overlapping an input), VTMU_ERR_RANGE
+ * (pos_offset < 0), VTMU_ERR_UNSUPPORTED (kv_rank/qk_rope other than 512/64,
+ * qk_nope above 512, v_head_dim above 4096, T * heads above 65536, S at or
+ * above 2^31), VTMU_ERR_WORKSPACE, VTMU_ERR_CUDA.
+ */
+VTMU_API vtmu_status vtmu_mla_attention(const float* q, const float* state, const float* k_b,
+                                        const float* v_b, float* out, const vtmu_mla_params* p,
+                                        void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * A decode step of a latent-attention model: op "cache_write" of state_new
+ * [new_rows, kv_rank + qk_rope] into state at row `offset`, then
+ * vtmu_mla_attention over the updated cache (its first p->S rows).  The
+ * rows are written by the first of the three launches, before any read.
+ * state [max_rows, kv_rank + qk_rope] and state_new: DEVICE, 16-byte
+ * aligned, not overlapping.  Errors: those of vtmu_mla_attention, plus
+ * VTMU_ERR_RANGE (offset < 0 or offset + new_rows > max_rows) and
+ * VTMU_ERR_INVALID (p->S > max_rows, NULL or overlapping buffers).
+ */
+VTMU_API vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const float* state_new,
+                                          int64_t new_rows, int64_t offset, const float* q,
+                                          const float* k_b, const float* v_b, float* out,
+                                          const vtmu_mla_params* p, void* workspace,
+                                          size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Kernel-side failures.  Every wait inside a kernel (TMA stage arrival,
  * stage release) gives up after one second instead of hanging the GPU; the
  * kernel then sets a bit in a device flag, abandons its output and returns.
@@ -355,7 +437,8 @@ VTMU_API vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64
  * producer gave up on a free stage, 4 = the producer gave up draining its
  * copies; tensor-core prefill bits: 0x100 stage load, 0x200 free stage,
  * 0x400 drain, 0x800 query load, 0x1000 score tile, 0x2000 probabilities,
- * 0x4000 P.V product.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
+ * 0x4000 P.V product; latent attention bits: 0x10000 stage load, 0x20000
+ * free stage, 0x40000 drain.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
  */
 VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
 

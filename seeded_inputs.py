@@ -14,7 +14,8 @@ same float32 arrays on every machine (up to last-ulp differences of the host's
 log/cos/sin, which the f32 cast almost always hides).
 
 Draw order inside one workload: q, k, v, then the bias values, then the bias
-mask uniforms, then the new K/V rows of a decode step.
+mask uniforms, then the new K/V rows of a decode step (latent attention: q,
+the latent cache, k_b, v_b, the new cache rows).
 """
 from __future__ import annotations
 
@@ -107,6 +108,25 @@ def decode_inputs(max_rows, heads, kvHeads, headDim, vHeadDim, seed, *, sigma=1.
     }
 
 
+def mla_inputs(rows, T, heads, kv_rank, qk_nope, qk_rope, v_head_dim, seed, *, new_rows=0):
+    """Absorbed latent attention: q [T, heads*(qk_nope+qk_rope)] and the
+    latent cache state [rows, kv_rank+qk_rope] of N(0, 1) values; the
+    up-projections k_b [heads*qk_nope, kv_rank] and v_b [heads*v_head_dim,
+    kv_rank] of N(0, 1/kv_rank) values (so keys and values have unit
+    variance); and state_new [new_rows, kv_rank+qk_rope] of N(0, 1) values.
+    Draw order: q, state, k_b, v_b, state_new."""
+    st = Stream(seed)
+    W = kv_rank + qk_rope
+    sw = 1.0 / math.sqrt(kv_rank)
+    return {
+        "q": st.normal_f32(T * heads * (qk_nope + qk_rope)).reshape(T, heads * (qk_nope + qk_rope)),
+        "state": st.normal_f32(rows * W).reshape(rows, W),
+        "k_b": st.normal_f32(heads * qk_nope * kv_rank, sw).reshape(heads * qk_nope, kv_rank),
+        "v_b": st.normal_f32(heads * v_head_dim * kv_rank, sw).reshape(heads * v_head_dim, kv_rank),
+        "state_new": st.normal_f32(new_rows * W).reshape(new_rows, W),
+    }
+
+
 # The workloads: shapes, op parameters (named as the op catalog names them),
 # seeds and input scale.  Parameters left out take the op's defaults.
 WORKLOADS = {
@@ -144,12 +164,25 @@ WORKLOADS = {
     "alibi_prefill": dict(
         kind="prefill", T=2048, S=2048, heads=32, kvHeads=32, headDim=128,
         seed=5, params=dict(causal=True, alibi=True)),
+    # Absorbed latent attention (the IR page's mla_attention), decode steps:
+    # cache_write of one latent row at 32767, then one query row over 32768
+    # cache rows.  DeepSeek-V2-Lite's shape (16 heads) and DeepSeek-V3's (128).
+    "mla_decode": dict(
+        kind="mla_decode", max_rows=32768, offset=32767, heads=16, kv_rank=512, qk_nope=128,
+        qk_rope=64, v_head_dim=128, seed=7, params=dict(causal=True, posOffset=32767)),
+    "mla_decode_v3": dict(
+        kind="mla_decode", max_rows=32768, offset=32767, heads=128, kv_rank=512, qk_nope=128,
+        qk_rope=64, v_head_dim=128, seed=8, params=dict(causal=True, posOffset=32767)),
 }
 
 
 def workload_inputs(name):
     """Inputs of a catalogue workload (see WORKLOADS)."""
     w = WORKLOADS[name]
+    if w["kind"] == "mla_decode":
+        R = w.get("rows", 1)
+        return mla_inputs(w["max_rows"], R, w["heads"], w["kv_rank"], w["qk_nope"], w["qk_rope"],
+                          w["v_head_dim"], w["seed"], new_rows=R)
     vhd = w.get("vHeadDim", w["headDim"])
     if w["kind"] == "decode":
         return decode_inputs(w["max_rows"], w["heads"], w["kvHeads"],

@@ -42,12 +42,14 @@ __global__ void tile_kernel(const float* __restrict__ y, float* __restrict__ out
 
 }  // namespace
 
+#define PROBE_API __attribute__((visibility("default")))
+
 extern "C" {
 
-int softcap_probe_values_per_warp() { return 32 * kPer; }
+PROBE_API int softcap_probe_values_per_warp() { return 32 * kPer; }
 
 // y, out_lib, out_ref: DEVICE [n] floats.
-int softcap_probe_scalar(const float* y, float* out_lib, float* out_ref, int n, cudaStream_t stream) {
+PROBE_API int softcap_probe_scalar(const float* y, float* out_lib, float* out_ref, int n, cudaStream_t stream) {
     if (n <= 0) return 0;
     scalar_kernel<<<(n + 255) / 256, 256, 0, stream>>>(y, out_lib, out_ref, n);
     return (int)cudaGetLastError();
@@ -55,7 +57,7 @@ int softcap_probe_scalar(const float* y, float* out_lib, float* out_ref, int n, 
 
 // y, out: DEVICE [n] floats, series: DEVICE [n / (32 * kPer)] ints; n must be
 // a multiple of 32 * kPer.
-int softcap_probe_tile(const float* y, float* out, int* series, float qk_mul, float cap, int n,
+PROBE_API int softcap_probe_tile(const float* y, float* out, int* series, float qk_mul, float cap, int n,
                        cudaStream_t stream) {
     if (n <= 0 || n % (32 * kPer) != 0) return (int)cudaErrorInvalidValue;
     const int nthreads = n / kPer;

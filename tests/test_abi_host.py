@@ -331,3 +331,54 @@ def test_noalloc_scratch_limit_in_virtual_heads(lib):
     cap = vtmu.NOALLOC_SCRATCH_BYTES
     assert need(62, 31) <= cap < need(64, 32)
     assert need(31, 31) <= cap < need(32, 32)
+
+
+# ---- absorbed latent attention ------------------------------------------------
+def test_mla_params_init_writes_defaults(lib):
+    p = vtmu.vtmu_mla_params_init()
+    assert p.causal == 1 and p.kv_rank == 512 and p.qk_rope == 64 and p.has_scale == 0 and p.window == 0
+
+
+@pytest.mark.parametrize("kw,status,word", [
+    (dict(kv_rank=256), vtmu.VTMU_ERR_UNSUPPORTED, "kv_rank"),
+    (dict(qk_rope=32), vtmu.VTMU_ERR_UNSUPPORTED, "qk_rope"),
+    (dict(qk_nope=600), vtmu.VTMU_ERR_UNSUPPORTED, "qk_nope"),
+    (dict(v_head_dim=0), vtmu.VTMU_ERR_INVALID, "v_head_dim"),
+    (dict(heads=0), vtmu.VTMU_ERR_INVALID, "heads"),
+    (dict(posOffset=-1), vtmu.VTMU_ERR_RANGE, "posOffset"),
+    (dict(window=-2), vtmu.VTMU_ERR_INVALID, "window"),
+    (dict(scale=float("inf")), vtmu.VTMU_ERR_INVALID, "scale"),
+    (dict(T=4097, heads=16), vtmu.VTMU_ERR_UNSUPPORTED, "T * heads"),
+])
+def test_mla_invalid_params_are_refused(lib, kw, status, word):
+    base = dict(T=1, S=128, heads=4, qk_nope=64, v_head_dim=64)
+    base.update(kw)
+    T, S = base.pop("T"), base.pop("S")
+    e = _err(lambda: vtmu.vtmu_mla_workspace_size(vtmu.make_mla_params(T, S, **base)))
+    assert e.status == status and word in str(e), str(e)
+
+
+def test_mla_workspace_holds_queries_and_partials(lib):
+    """The workspace holds the header, the absorbed queries (T * heads rows of
+    576 floats) and at least one split's partials per virtual head."""
+    p = vtmu.make_mla_params(1, 32768, heads=16, qk_nope=128, v_head_dim=128, posOffset=32767)
+    n = vtmu.vtmu_mla_workspace_size(p)
+    assert n >= 64 * 1024 + 16 * 576 * 4 + 16 * (512 + 2) * 4
+    assert n < 64 * 1024 * 1024
+
+
+@host_only
+def test_mla_pointer_checks(lib):
+    p = vtmu.make_mla_params(1, 128, heads=4, qk_nope=64, v_head_dim=64, posOffset=127)
+    n = vtmu.vtmu_mla_workspace_size(p)
+    e = _err(lambda: vtmu.vtmu_mla_attention(FAKE, None, FAKE * 5, FAKE * 7, FAKE * 9, p, FAKE * 11, n, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "NULL" in str(e)
+    e = _err(lambda: vtmu.vtmu_mla_attention(FAKE, FAKE * 3 + 4, FAKE * 5, FAKE * 7, FAKE * 9, p, FAKE * 11, n, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "16-byte" in str(e)
+    e = _err(lambda: vtmu.vtmu_mla_attention(FAKE, FAKE * 3, FAKE * 5, FAKE * 7, FAKE * 3, p, FAKE * 11, n, 0))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "overlaps" in str(e)
+    e = _err(lambda: vtmu.vtmu_mla_attention(FAKE, FAKE * 3, FAKE * 5, FAKE * 7, FAKE * 9, p, FAKE * 11, n - 256, 0))
+    assert e.status == vtmu.VTMU_ERR_WORKSPACE
+    e = _err(lambda: vtmu.vtmu_mla_decode_step(FAKE * 3, 128, FAKE * 13, 1, 128, FAKE, FAKE * 5, FAKE * 7,
+                                               FAKE * 9, p, FAKE * 11, n, 0))
+    assert e.status == vtmu.VTMU_ERR_RANGE
