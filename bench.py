@@ -745,7 +745,7 @@ def measure_mla(ctx, name):
 
 
 def mla_roofline(ctx, d, clocks):
-    """Both rooflines of the latent-attention step (its three launches timed
+    """Both rooflines of the latent-attention step (its four launches timed
     together): algorithmic bytes against the HBM copy peak and algorithmic
     FLOPs against the FP32 FMA peak; `bound` is the one whose ideal time is
     longer."""
@@ -798,7 +798,7 @@ def run_vtmu(args, rank, world, local):
             "ms_per_step": round(d["step_ms"], 5), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32", "data": DATA, "config": workload_config(name, world),
             "impl": "vtmu", "roofline": mla_roofline(ctx, d, clocks), "cpu_baseline": cpu, "e2e": d["e2e"],
-            "gpu_launches": 3 * args.steps, "clocks": clocks,
+            "gpu_launches": 4 * args.steps, "clocks": clocks,
         }
         if rank == 0:
             print(json.dumps(line), flush=True)
@@ -846,7 +846,7 @@ def run_vtmu(args, rank, world, local):
                            "unit": "GB/s", "ms_per_step": round(mla["step_ms"], 5),
                            "kernel_ms": round(mla["kernel_ms"], 5), "steps": args.steps, "warmup": args.warmup,
                            "roofline": mla_roofline(ctx, mla, mclk), "e2e": mla["e2e"], "cpu_baseline": mcpu,
-                           "gpu_launches": 3 * args.steps, "clocks": mclk}
+                           "gpu_launches": 4 * args.steps, "clocks": mclk}
     else:
         r = measure_prefill(ctx, name, args.steps, args.warmup, kernel_arg=args.kernel,
                             cpu_budget=0.0 if args.no_cpu_baseline else args.cpu_budget)

@@ -107,7 +107,7 @@ struct MlaPlan {
     int32_t splits = 1;
     int32_t sink_splits = 0;
     int64_t lo = 0, hi = 0, sink_end = 0, per = 32;
-    size_t qabs_off = 0, m_off = 0, l_off = 0, o_off = 0, workspace_bytes = 0;
+    size_t qabs_off = 0, m_off = 0, l_off = 0, o_off = 0, olat_off = 0, workspace_bytes = 0;
 };
 void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan);
 cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, const MlaCacheWrite& cw,

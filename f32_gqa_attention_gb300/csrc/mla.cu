@@ -8,7 +8,7 @@
 // query against the SAME 576-wide latent row:
 //     score(t, h, s) = scale * ( (k_b_h^T q_nope) . c_s + q_rope . r_s )
 //     out(t, h)      = v_b_h ( sum_s p(t, h, s) c_s / sum_s p(t, h, s) )
-// so the cache is read once for all heads.  Three launches:
+// so the cache is read once for all heads.  Four launches:
 //  1. mla_absorb_kernel: q_abs[t, h] = [k_b_h^T q_nope | q_rope] * scale *
 //     log2 e (scores come out in base 2), and the new cache rows of a decode
 //     step (op cache_write) -- the next launch reads them;
@@ -27,8 +27,9 @@
 //     The same 16 latent dims serve as key and as value.  Warps holding
 //     other key slices of the same heads merge in shared memory; the CTA
 //     writes (m, l, o) per virtual head and split;
-//  3. mla_merge_project_kernel: per virtual head the log-sum-exp merge of the
-//     splits, then the output projection through v_b_h.
+//  3. mla_merge_kernel: per virtual head the log-sum-exp merge of the splits
+//     into the weighted latent; mla_project_kernel: its projection through
+//     v_b_h.
 // Every mbarrier wait is bounded (tma_sync.cuh); a wait that gives up sets a
 // bit of g_mla_device_error and the kernel unwinds.
 #include <cstring>
@@ -61,7 +62,6 @@ constexpr int kConsumerWarps = 8;
 constexpr int kLatThreads = 32 * kConsumerWarps;  // lane 0 of warp 0 also issues the copies
 constexpr size_t kLatSmem = (size_t)kStages * kStageBytes + 1024;
 constexpr float kRescaleLog2 = 8.f;
-constexpr int kAbsorbRows = 16;              // query rows per absorb block
 constexpr int kMaxMlaSplits = 256;
 
 enum MlaError : unsigned int {
@@ -73,20 +73,23 @@ enum MlaError : unsigned int {
 static_assert(kW % kBoxCols == 0 && kR == 512 && kP == 64, "latent row layout");
 
 // ---- 1. absorb the queries, write the new cache rows ------------------------
-// grid (heads, kR / 64, ceil(T / 16)), 256 threads: 64 latent columns x 4
-// slices of the qk_nope sum.
+// grid (heads, kR / 128, ceil(T / 4)), 256 threads.  Lane l of warp w owns
+// latent columns 128 jb + 4 l .. + 3 and the k_b rows i = w, w + 8, ... of
+// head h: one 16-byte load per row, all issued before the sums (the read of
+// k_b is latency-bound otherwise); the eight warps' sums meet in shared memory.
+constexpr int kAbsorbRows = 4;  // query rows per block
 __global__ void __launch_bounds__(256) mla_absorb_kernel(const float* __restrict__ q,
                                                          const float* __restrict__ k_b,
                                                          float* __restrict__ qabs, int64_t T, int H, int N,
                                                          float qscale, MlaCacheWrite cw) {
     extern __shared__ float sh[];
-    float* qn = sh;                         // [kAbsorbRows][N]
-    float* red = sh + kAbsorbRows * N;      // [4][kAbsorbRows][64]
+    float* qn = sh;                          // [kAbsorbRows][N]
+    float* red = sh + kAbsorbRows * N;       // [8][kAbsorbRows][128]
     const int h = blockIdx.x, jb = blockIdx.y;
     const int64_t t0 = (int64_t)blockIdx.z * kAbsorbRows;
     const int rows = (int)((T - t0) < kAbsorbRows ? (T - t0) : kAbsorbRows);
     const int Dq = N + kP;
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     // The decode step's new cache rows (op cache_write), by one block.
     if (cw.state_new != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
         const int64_t n4 = cw.rows * kW / 4;
@@ -99,25 +102,33 @@ __global__ void __launch_bounds__(256) mla_absorb_kernel(const float* __restrict
         qn[idx] = t < rows ? __ldg(q + (t0 + t) * H * Dq + (int64_t)h * Dq + i) : 0.f;
     }
     __syncthreads();
-    const int jl = tid & 63, slice = tid >> 6;
-    const int j = jb * 64 + jl;
-    float acc[kAbsorbRows];
+    float acc[kAbsorbRows][4];
 #pragma unroll
-    for (int t = 0; t < kAbsorbRows; ++t) acc[t] = 0.f;
-    const float* kb = k_b + (int64_t)h * N * kR + j;
-    for (int i = slice; i < N; i += 4) {
-        const float w = __ldg(kb + (int64_t)i * kR);
+    for (int t = 0; t < kAbsorbRows; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+    const float* kb = k_b + (int64_t)h * N * kR + jb * 128 + 4 * lane;
+#pragma unroll 16
+    for (int i = warp; i < N; i += 8) {
+        const float4 w = __ldg(reinterpret_cast<const float4*>(kb + (int64_t)i * kR));
 #pragma unroll
-        for (int t = 0; t < kAbsorbRows; ++t) acc[t] = fmaf(qn[t * N + i], w, acc[t]);
+        for (int t = 0; t < kAbsorbRows; ++t) {
+            const float qv = qn[t * N + i];
+            acc[t][0] = fmaf(qv, w.x, acc[t][0]);
+            acc[t][1] = fmaf(qv, w.y, acc[t][1]);
+            acc[t][2] = fmaf(qv, w.z, acc[t][2]);
+            acc[t][3] = fmaf(qv, w.w, acc[t][3]);
+        }
     }
 #pragma unroll
-    for (int t = 0; t < kAbsorbRows; ++t) red[(slice * kAbsorbRows + t) * 64 + jl] = acc[t];
+    for (int t = 0; t < kAbsorbRows; ++t)
+        *reinterpret_cast<float4*>(red + (warp * kAbsorbRows + t) * 128 + 4 * lane) =
+            make_float4(acc[t][0], acc[t][1], acc[t][2], acc[t][3]);
     __syncthreads();
-    for (int idx = tid; idx < rows * 64; idx += blockDim.x) {
-        const int t = idx / 64, c = idx % 64;
-        const float s = red[(0 * kAbsorbRows + t) * 64 + c] + red[(1 * kAbsorbRows + t) * 64 + c] +
-                        red[(2 * kAbsorbRows + t) * 64 + c] + red[(3 * kAbsorbRows + t) * 64 + c];
-        qabs[((t0 + t) * H + h) * kW + jb * 64 + c] = s * qscale;
+    for (int idx = tid; idx < rows * 128; idx += blockDim.x) {
+        const int t = idx / 128, c = idx % 128;
+        float sum = 0.f;
+#pragma unroll
+        for (int w8 = 0; w8 < 8; ++w8) sum += red[(w8 * kAbsorbRows + t) * 128 + c];
+        qabs[((t0 + t) * H + h) * kW + jb * 128 + c] = sum * qscale;
     }
     if (jb == 0) {  // the rotary part passes through, scaled
         for (int idx = tid; idx < rows * kP; idx += blockDim.x) {
@@ -141,12 +152,19 @@ struct LatArgs {
 };
 
 // 16 partial sums per lane -> lanes l and l ^ 16 hold the warp-wide sum of
-// entry l % 16: a butterfly reduce-scatter over lane bits 3..0 (each step
-// keeps the half of the entries whose bit matches the lane's), then one add
-// across the two half-warps.
+// entry l % 16 (entry 4 k + h: key k, head h of a 4-key batch).  Slot 4 k + h
+// of lane l holds the partial of key k ^ ((l >> 2) & 3), head h: with the
+// keys permuted by the lane's bits 3..2, the first two butterfly steps need
+// no selects (a lane keeps its low slots, whose entries match the partner's
+// high slots); the two head steps keep/send by the lane's bit; a last add
+// joins the half-warps.
 __device__ __forceinline__ float reduce_scatter16(float (&v)[16], int lane) {
 #pragma unroll
-    for (int w = 8; w >= 1; w >>= 1) {
+    for (int w = 8; w >= 4; w >>= 1)
+#pragma unroll
+        for (int i = 0; i < w; ++i) v[i] += __shfl_xor_sync(FULL, v[i + w], w);
+#pragma unroll
+    for (int w = 2; w >= 1; w >>= 1) {
         const bool up = (lane & w) != 0;
 #pragma unroll
         for (int i = 0; i < w; ++i) {
@@ -242,14 +260,15 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         }
     }
     float o[4][16];
-    float m_ref[4], l_sum[4];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-        m_ref[h] = -INFINITY;
-        l_sum[h] = 0.f;
+    for (int h = 0; h < 4; ++h)
 #pragma unroll
         for (int d = 0; d < 16; ++d) o[h][d] = 0.f;
-    }
+    // The lane's head (lane % 4): its reference max (base 2, lazily raised)
+    // and its running sum, the same in every lane of that head.
+    float m_my = -INFINITY, l_my = 0.f;
+    __shared__ __align__(16) float pbuf[kConsumerWarps][16];  // a batch's probabilities, per warp
+    const int kx = (lane >> 2) & 3;  // key permutation of the score slots
     bool ok = true;
     for (int it = 0; it < nst; ++it) {
         const int slot = it % kStages;
@@ -270,24 +289,28 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             float part[16];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
+                const int kk = k ^ kx;  // this lane's key for slot group k
                 float kv[18];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 x = *reinterpret_cast<const float4*>(lp + k * kBoxCols + 2 * j * kBoxFloats);
+                    const float4 x = *reinterpret_cast<const float4*>(lp + kk * kBoxCols + 2 * j * kBoxFloats);
                     kv[4 * j] = x.x;
                     kv[4 * j + 1] = x.y;
                     kv[4 * j + 2] = x.z;
                     kv[4 * j + 3] = x.w;
                 }
-                const float2 r = *reinterpret_cast<const float2*>(rp + k * kBoxCols);
+                const float2 r = *reinterpret_cast<const float2*>(rp + kk * kBoxCols);
                 kv[16] = r.x;
                 kv[17] = r.y;
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    float s = 0.f;
+                for (int h = 0; h < 4; ++h) {  // two chains per dot product
+                    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-                    for (int d = 0; d < 18; ++d) s = fmaf(q[h][d], kv[d], s);
-                    part[4 * k + h] = s;
+                    for (int d = 0; d < 9; ++d) {
+                        s0 = fmaf(q[h][d], kv[d], s0);
+                        s1 = fmaf(q[h][d + 9], kv[d + 9], s1);
+                    }
+                    part[4 * k + h] = s0 + s1;
                 }
             }
             // Lanes l and l ^ 16: the score of key kb + (l % 16) / 4 for head
@@ -296,42 +319,45 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             const int64_t s_key = stage_key0 + kb + ((lane & 15) >> 2);
             const bool vis = my_v < args.V && s_key < k1 && key_visible<true>(args.a, my_pos, s_key);
             if (!vis) x = -INFINITY;
-            float mt = x;  // the batch's max per head (both half-warps agree)
+            float mt = x;  // the batch's max for the lane's head (both half-warps agree)
             mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 4));
             mt = fmaxf(mt, __shfl_xor_sync(FULL, mt, 8));
-            float alpha[4];
-            bool rescale = false;
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const float mh = __shfl_sync(FULL, mt, h);
-                alpha[h] = 1.f;
-                if (mh > m_ref[h] + kRescaleLog2) {  // lazy: keep the reference unless beaten by > 2^8
-                    alpha[h] = fast_exp2(m_ref[h] - mh);  // 0 while nothing was visible
-                    m_ref[h] = mh;
-                    rescale = true;
-                }
-            }
-            if (rescale) {
+            // Lazy rescale: only when some head's max beats its reference by > 2^8.
+            const bool raise = mt > m_my + kRescaleLog2;
+            if (__any_sync(FULL, raise)) {
+                // 0 when nothing was visible before; 1 for the heads not raised
+                // (also those that have seen nothing: -inf - -inf is no number).
+                const float a_my = raise ? fast_exp2(m_my - mt) : 1.f;
+                if (raise) m_my = mt;
+                l_my *= a_my;
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
-                    l_sum[h] *= alpha[h];
+                    const float ah = __shfl_sync(FULL, a_my, h);
 #pragma unroll
-                    for (int d = 0; d < 16; ++d) o[h][d] *= alpha[h];
+                    for (int d = 0; d < 16; ++d) o[h][d] *= ah;
                 }
             }
-            const float m_my = my_h == 0 ? m_ref[0] : my_h == 1 ? m_ref[1] : my_h == 2 ? m_ref[2] : m_ref[3];
             const float pv = fast_exp2(x - (m_my == -INFINITY ? 0.f : m_my));
-            float ps = pv;  // the batch's sum per head, within a half-warp
+            float ps = pv;  // the batch's sum for the lane's head, within a half-warp
             ps += __shfl_xor_sync(FULL, ps, 4);
             ps += __shfl_xor_sync(FULL, ps, 8);
-#pragma unroll
-            for (int h = 0; h < 4; ++h) l_sum[h] += __shfl_sync(FULL, ps, h);
+            l_my += ps;
             // O += P c: the latent dims of each key serve as its value.  The
-            // batch's 16 probabilities first go to every lane (in the score
-            // registers, dead by now), then one 16-byte load of a key's block
+            // batch's 16 probabilities go through shared memory to every lane
+            // (four broadcast loads), then one 16-byte load of a key's block
             // feeds 16 FMAs.
+            if (lane < 16) pbuf[warp][lane] = pv;
+            __syncwarp();
+            float pk[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) part[i] = __shfl_sync(FULL, pv, i);
+            for (int i = 0; i < 4; ++i) {
+                const float4 p4 = *reinterpret_cast<const float4*>(&pbuf[warp][4 * i]);
+                pk[4 * i] = p4.x;
+                pk[4 * i + 1] = p4.y;
+                pk[4 * i + 2] = p4.z;
+                pk[4 * i + 3] = p4.w;
+            }
+            __syncwarp();
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
 #pragma unroll
@@ -339,11 +365,11 @@ __global__ void __launch_bounds__(kLatThreads, 1)
                     const float4 c = *reinterpret_cast<const float4*>(lp + k * kBoxCols + 2 * j * kBoxFloats);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        const float pk = part[4 * k + h];
-                        o[h][4 * j] = fmaf(pk, c.x, o[h][4 * j]);
-                        o[h][4 * j + 1] = fmaf(pk, c.y, o[h][4 * j + 1]);
-                        o[h][4 * j + 2] = fmaf(pk, c.z, o[h][4 * j + 2]);
-                        o[h][4 * j + 3] = fmaf(pk, c.w, o[h][4 * j + 3]);
+                        const float p = pk[4 * k + h];
+                        o[h][4 * j] = fmaf(p, c.x, o[h][4 * j]);
+                        o[h][4 * j + 1] = fmaf(p, c.y, o[h][4 * j + 1]);
+                        o[h][4 * j + 2] = fmaf(p, c.z, o[h][4 * j + 2]);
+                        o[h][4 * j + 3] = fmaf(p, c.w, o[h][4 * j + 3]);
                     }
                 }
             }
@@ -368,6 +394,13 @@ __global__ void __launch_bounds__(kLatThreads, 1)
         for (int it = last - kStages < 0 ? 0 : last - kStages; it < last; ++it)
             if (!mbar_wait(&full[it % kStages], (uint32_t)((it / kStages) & 1)))
                 raise_device_error(&g_mla_device_error, kErrMlaDrain);
+    }
+    // Every head's reference max and sum, in every lane.
+    float m_ref[4], l_sum[4];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        m_ref[h] = __shfl_sync(FULL, m_my, h);
+        l_sum[h] = __shfl_sync(FULL, l_my, h);
     }
 
     // ---- merge the key slices of each head, write the split's partials ----
@@ -441,19 +474,20 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     }
 }
 
-// ---- 3. merge the splits, project through v_b --------------------------------
-// grid (V, ceil(Dv / 32)), 256 threads.
-__global__ void __launch_bounds__(256) mla_merge_project_kernel(const float* __restrict__ part_m,
-                                                                const float* __restrict__ part_l,
-                                                                const float* __restrict__ part_o,
-                                                                const float* __restrict__ v_b, float* __restrict__ out,
-                                                                int splits, int H, int Dv) {
+// ---- 3. merge the splits, then project through v_b ----------------------------
+// Merge: grid (V, kR / 32), 256 threads.  Warp w takes splits w, w + 8, ...
+// of its 32 latent dims (lane = dim), eight loads in flight per lane; the
+// log-sum-exp weights come from one pass over the split maxima.  olat[v] =
+// sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i (zeros when nothing was
+// visible).
+__global__ void __launch_bounds__(256) mla_merge_kernel(const float* __restrict__ part_m,
+                                                        const float* __restrict__ part_l,
+                                                        const float* __restrict__ part_o, float* __restrict__ olat,
+                                                        int splits) {
     __shared__ float wsp[kMaxMlaSplits];
-    __shared__ __align__(16) float olat[kR];
+    __shared__ float red[8][32];
     __shared__ float inv_l;
-    const int v = blockIdx.x;
-    const int64_t t = v / H;
-    const int h = v % H;
+    const int v = blockIdx.x, d = blockIdx.y * 32 + (threadIdx.x & 31);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (warp == 0) {
         float M = -INFINITY;
@@ -469,33 +503,54 @@ __global__ void __launch_bounds__(256) mla_merge_project_kernel(const float* __r
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(FULL, L, off);
-        if (lane == 0) inv_l = L > 0.f ? 1.f / L : 0.f;  // nothing visible: zeros
+        if (lane == 0) inv_l = L > 0.f ? 1.f / L : 0.f;
     }
     __syncthreads();
-    for (int d = tid; d < kR; d += blockDim.x) {
-        float acc = 0.f;
-        const float* po = part_o + (int64_t)v * splits * kR + d;
-        for (int i = 0; i < splits; ++i) acc = fmaf(__ldcg(po + (int64_t)i * kR), wsp[i], acc);
-        olat[d] = acc * inv_l;
-    }
+    const float* po = part_o + (int64_t)v * splits * kR + d;
+    float acc = 0.f;
+#pragma unroll 8
+    for (int i = warp; i < splits; i += 8) acc = fmaf(__ldcg(po + (int64_t)i * kR), wsp[i], acc);
+    red[warp][lane] = acc;
     __syncthreads();
-    // Warp w: outputs e0 + 4 w .. + 3, each a 512-long dot product with v_b's row.
+    if (warp == 0) {
+        float sum = 0.f;
+#pragma unroll
+        for (int w = 0; w < 8; ++w) sum += red[w][lane];
+        olat[(int64_t)v * kR + d] = sum * inv_l;
+    }
+}
+
+// Project: grid (V, ceil(Dv / 32)), 256 threads; warp w computes outputs
+// e0 + 4 w .. + 3, each the dot product of v_b's row with olat[v] (512 long).
+__global__ void __launch_bounds__(256) mla_project_kernel(const float* __restrict__ olat,
+                                                          const float* __restrict__ v_b, float* __restrict__ out,
+                                                          int H, int Dv) {
+    const int v = blockIdx.x;
+    const int64_t t = v / H;
+    const int h = v % H;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float4 c[kR / 128];
+#pragma unroll
+    for (int j = 0; j < kR / 128; ++j) c[j] = __ldcg(reinterpret_cast<const float4*>(olat + (int64_t)v * kR + 128 * j + 4 * lane));
     const int e0 = blockIdx.y * 32 + warp * 4;
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
         const int e = e0 + u;
-        if (e >= Dv) break;
-        const float* row = v_b + ((int64_t)h * Dv + e) * kR;
-        float acc = 0.f;
+        if (e < Dv) {
+            const float* row = v_b + ((int64_t)h * Dv + e) * kR;
 #pragma unroll
-        for (int j = 0; j < kR / 128; ++j) {
-            const float4 w = __ldg(reinterpret_cast<const float4*>(row + 128 * j + 4 * lane));
-            const float4 c = *reinterpret_cast<const float4*>(olat + 128 * j + 4 * lane);
-            acc = fmaf(w.x, c.x, fmaf(w.y, c.y, fmaf(w.z, c.z, fmaf(w.w, c.w, acc))));
+            for (int j = 0; j < kR / 128; ++j) {
+                const float4 w = __ldg(reinterpret_cast<const float4*>(row + 128 * j + 4 * lane));
+                acc[u] = fmaf(w.x, c[j].x, fmaf(w.y, c[j].y, fmaf(w.z, c[j].z, fmaf(w.w, c[j].w, acc[u]))));
+            }
         }
+    }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(FULL, acc, off);
-        if (lane == 0) out[(t * H + h) * Dv + e] = acc;
+    for (int u = 0; u < 4; ++u) {
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[u] += __shfl_xor_sync(FULL, acc[u], off);
+        if (lane == 0 && e0 + u < Dv) out[(t * H + h) * Dv + e0 + u] = acc[u];
     }
 }
 
@@ -592,7 +647,8 @@ void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan) {
     plan->m_off = plan->qabs_off + up256((size_t)V * kW * 4);
     plan->l_off = plan->m_off + up256((size_t)V * n * 4);
     plan->o_off = plan->l_off + up256((size_t)V * n * 4);
-    plan->workspace_bytes = plan->o_off + up256((size_t)V * n * kR * 4);
+    plan->olat_off = plan->o_off + up256((size_t)V * n * kR * 4);
+    plan->workspace_bytes = plan->olat_off + up256((size_t)V * kR * 4);
 }
 
 cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, const MlaCacheWrite& cw,
@@ -601,12 +657,12 @@ cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, c
     float* qabs = reinterpret_cast<float*>(w + plan.qabs_off);
     if (m.T == 0) return cudaSuccess;
     const int64_t tblocks = (m.T + kAbsorbRows - 1) / kAbsorbRows;
-    const size_t absorb_smem = (size_t)(kAbsorbRows * m.N + 4 * kAbsorbRows * 64) * sizeof(float);
+    const size_t absorb_smem = (size_t)(kAbsorbRows * m.N + 8 * kAbsorbRows * 128) * sizeof(float);
     if (absorb_smem > 48 * 1024) {
         cudaError_t e = set_smem_once(reinterpret_cast<const void*>(mla_absorb_kernel), (int)absorb_smem);
         if (e != cudaSuccess) return e;
     }
-    mla_absorb_kernel<<<dim3(m.H, kR / 64, (unsigned)tblocks), 256, absorb_smem, stream>>>(
+    mla_absorb_kernel<<<dim3(m.H, kR / 128, (unsigned)tblocks), 256, absorb_smem, stream>>>(
         m.q, m.k_b, qabs, m.T, m.H, m.N, m.qscale, cw);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
@@ -641,8 +697,13 @@ cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, c
         default: e = launch_latent<8>(tm, args, plan.groups, stream); break;
     }
     if (e != cudaSuccess) return e;
-    mla_merge_project_kernel<<<dim3((unsigned)args.V, (unsigned)((m.Dv + 31) / 32)), 256, 0, stream>>>(
-        args.part_m, args.part_l, args.part_o, m.v_b, m.out, plan.splits, m.H, m.Dv);
+    float* olat = reinterpret_cast<float*>(w + plan.olat_off);
+    mla_merge_kernel<<<dim3((unsigned)args.V, kR / 32), 256, 0, stream>>>(args.part_m, args.part_l, args.part_o,
+                                                                         olat, plan.splits);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    mla_project_kernel<<<dim3((unsigned)args.V, (unsigned)((m.Dv + 31) / 32)), 256, 0, stream>>>(olat, m.v_b, m.out,
+                                                                                                 m.H, m.Dv);
     return cudaGetLastError();
 }
 

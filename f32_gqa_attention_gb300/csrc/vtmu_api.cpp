@@ -700,12 +700,13 @@ static vtmu_status run_mla(vtmu::MlaDesc& m, const float* q, const float* state,
                            const float* v_b, float* out, void* workspace, size_t workspace_bytes,
                            const vtmu::MlaCacheWrite& cw, cudaStream_t stream) {
     if (m.T > 0) {
-        if (!q || !k_b || !v_b || !out || (m.S > 0 && !state))
+        if (!q || (m.N > 0 && !k_b) || !v_b || !out || (m.S > 0 && !state))
             return fail(VTMU_ERR_INVALID, "mla: q, state, k_b, v_b or out is NULL");
-        if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k_b) | reinterpret_cast<uintptr_t>(out)) & 3u)
-            return fail(VTMU_ERR_INVALID, "mla: q, k_b and out must be 4-byte aligned");
-        if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(v_b)) & 15u)
-            return fail(VTMU_ERR_INVALID, "mla: state and v_b must be 16-byte aligned");
+        if ((reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(out)) & 3u)
+            return fail(VTMU_ERR_INVALID, "mla: q and out must be 4-byte aligned");
+        if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(k_b) | reinterpret_cast<uintptr_t>(v_b)) &
+            15u)
+            return fail(VTMU_ERR_INVALID, "mla: state, k_b and v_b must be 16-byte aligned");
         const size_t W = (size_t)vtmu::kMlaKvRank + vtmu::kMlaRope;
         const size_t out_b = (size_t)m.T * m.H * m.Dv * 4;
         if (overlaps(out, out_b, q, (size_t)m.T * m.H * (m.N + vtmu::kMlaRope) * 4) ||

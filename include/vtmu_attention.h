@@ -355,7 +355,8 @@ VTMU_API vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64
  *       rotary key shared by every head (the first S rows are read)
  *   q     [T, heads*(qk_nope + qk_rope)]: per head the no-rope part, then
  *       the rotary part (already turned)
- *   k_b   [heads*qk_nope, kv_rank], v_b [heads*v_head_dim, kv_rank]: the
+ *   k_b   [heads*qk_nope, kv_rank] (may be NULL when qk_nope is 0), v_b
+ *       [heads*v_head_dim, kv_rank]: the
  *       up-projections as a checkpoint stores them ([out, in])
  *   out   [T, heads*v_head_dim]
  * Head h's key at s is [k_b_h c_s | r_s] and its value v_b_h c_s (k_b_h,
@@ -396,11 +397,11 @@ VTMU_API void vtmu_mla_params_init(vtmu_mla_params* p);
 VTMU_API vtmu_status vtmu_mla_workspace_size(const vtmu_mla_params* p, size_t* bytes);
 
 /*
- * mla_attention (IR schema page, $defs.op_mla_attention).  q, k_b, out:
- * DEVICE, 4-byte aligned; state, v_b: DEVICE, 16-byte aligned; out must not
+ * mla_attention (IR schema page, $defs.op_mla_attention).  q, out: DEVICE,
+ * 4-byte aligned; state, k_b, v_b: DEVICE, 16-byte aligned; out must not
  * overlap an input.  workspace: DEVICE, at least vtmu_mla_workspace_size()
  * bytes, 256-byte aligned, no initial contents needed; calls that share a
- * workspace must not overlap on the GPU.  Three launches on `stream`.
+ * workspace must not overlap on the GPU.  Four launches on `stream`.
  * Errors: VTMU_ERR_INVALID (null or misaligned pointer, negative sizes or
  * window/sinks, scale not finite, out overlapping an input), VTMU_ERR_RANGE
  * (pos_offset < 0), VTMU_ERR_UNSUPPORTED (kv_rank/qk_rope other than 512/64,
@@ -415,7 +416,7 @@ VTMU_API vtmu_status vtmu_mla_attention(const float* q, const float* state, cons
  * A decode step of a latent-attention model: op "cache_write" of state_new
  * [new_rows, kv_rank + qk_rope] into state at row `offset`, then
  * vtmu_mla_attention over the updated cache (its first p->S rows).  The
- * rows are written by the first of the three launches, before any read.
+ * rows are written by the first of the four launches, before any read.
  * state [max_rows, kv_rank + qk_rope] and state_new: DEVICE, 16-byte
  * aligned, not overlapping.  Errors: those of vtmu_mla_attention, plus
  * VTMU_ERR_RANGE (offset < 0 or offset + new_rows > max_rows) and
