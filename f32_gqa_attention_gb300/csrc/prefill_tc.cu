@@ -296,7 +296,7 @@ __device__ __forceinline__ void run_epilogue_staged(int feat, const AttnDesc& a,
 // common path carries none of their bookkeeping).
 template <int D, int DV, bool SINKS>
 __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
-    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const int bias_staged,
+    prefill_tc_kernel(const AttnDesc a, const AlibiTable alibi, const int bias_staged, const int hgroup,
                       const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_bias,
                       const __grid_constant__ CUtensorMap tm_khi,
                       const __grid_constant__ CUtensorMap tm_klo, const __grid_constant__ CUtensorMap tm_vhi,
@@ -318,17 +318,27 @@ __global__ void __launch_bounds__(TcCfg<D, DV>::THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_qt = (int)((a.T + kBM - 1) / kBM);
     // CTAs start in linear block order (V half innermost).  When the query
-    // tiles' work differs (causal or windowed), the query tile is outermost,
-    // latest (heaviest) first, so the longest CTAs of every head start first
-    // and short ones fill the tail; when every tile sees the same keys, heads
-    // are outermost so that the CTAs running together share one head's K/V
-    // in L2.
+    // tiles' work differs (causal or windowed), the heads come in groups of
+    // `hgroup` whose K/V hi/lo fit in L2 together; within a group the query
+    // tile is outermost, latest (heaviest) first, so the longest CTAs start
+    // first and short ones fill the tail, and the CTAs running together share
+    // the group's K/V in L2.  When every tile sees the same keys, heads are
+    // outermost so that the CTAs running together share one head's K/V.
     const int nz = (int)gridDim.z;
     const int64_t lin = blockIdx.x + (int64_t)gridDim.x * (blockIdx.y + (int64_t)gridDim.y * blockIdx.z);
     const int zz = (int)(lin % nz);
     const bool uniform = !a.causal && a.window <= 0;
-    const int h = (int)(uniform ? lin / ((int64_t)nz * n_qt) : (lin / nz) % a.H), kh = h / a.G;
-    const int qt = n_qt - 1 - (int)(uniform ? (lin / nz) % n_qt : lin / ((int64_t)nz * a.H));
+    int h, qt;
+    if (uniform) {
+        h = (int)(lin / ((int64_t)nz * n_qt));
+        qt = n_qt - 1 - (int)((lin / nz) % n_qt);
+    } else {
+        const int64_t r = lin / nz, per_group = (int64_t)n_qt * hgroup;
+        const int64_t grp = r / per_group, rem = r % per_group;
+        h = (int)(grp * hgroup + rem % hgroup);
+        qt = n_qt - 1 - (int)(rem / hgroup);
+    }
+    const int kh = h / a.G;
     const int dv0 = zz * DVC;  // this CTA's V columns [dv0, dv0 + DVC)
     const int64_t t0 = (int64_t)qt * kBM;
     const int64_t t_last = (t0 + kBM < a.T ? t0 + kBM : a.T) - 1;
@@ -1097,8 +1107,17 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     auto kern = prefill_tc_kernel<D, DV, SINKS>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), (int)C::SMEM);
     if (e != cudaSuccess) return e;
+    // Query heads per launch-order group: whole KV groups (a divisor of
+    // kvHeads) whose K and V^T hi/lo over the keys of a few concurrent query
+    // tiles stay under ~80 MB of the 126 MB L2.
+    const int64_t keys = a.window > 0 ? (a.window + 5 * kBM < a.S ? a.window + 5 * kBM : a.S) : a.S;
+    const double per_kv = (double)keys * (D + DV) * 2 * sizeof(float);
+    int gk = a.Hk;
+    while (gk > 1 && (a.Hk % gk != 0 || per_kv * gk > 80e6)) --gk;
+    const int hgroup = gk * a.G;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
-    kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi, bias_staged, m_q, m_bias, m_khi, m_klo, m_vhi, m_vlo);
+    kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi, bias_staged, hgroup, m_q, m_bias, m_khi, m_klo, m_vhi,
+                                                m_vlo);
     return cudaGetLastError();
 }
 
