@@ -103,8 +103,11 @@ class vtmu_mla_params(ctypes.Structure):
         ("pos_offset", ctypes.c_int64),
         ("window", ctypes.c_int64),
         ("sinks", ctypes.c_int64),
+        ("kernel", ctypes.c_int32),
     ]
 
+
+MLA_KERNEL_AUTO, MLA_KERNEL_CUDA_CORES, MLA_KERNEL_TENSOR_CORES = 0, 1, 2
 
 _lib = None
 _lib_lock = threading.Lock()
@@ -504,7 +507,7 @@ def cache_write(cache, values, offset: int, stream=None):
 
 
 def make_mla_params(T, S, *, heads, kv_rank=512, qk_nope, qk_rope=64, v_head_dim, scale=None, causal=True,
-                    posOffset=0, window=None, sinks=None):
+                    posOffset=0, window=None, sinks=None, kernel=0):
     """An mla params struct from the IR page's parameter names (mla_attention)."""
     p = vtmu_mla_params_init()
     p.T, p.S = int(T), int(S)
@@ -516,6 +519,7 @@ def make_mla_params(T, S, *, heads, kv_rank=512, qk_nope, qk_rope=64, v_head_dim
     p.pos_offset = int(posOffset)
     p.window = 0 if window is None else int(window)
     p.sinks = 0 if sinks is None else int(sinks)
+    p.kernel = int(kernel)
     return p
 
 

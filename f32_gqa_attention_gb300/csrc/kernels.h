@@ -93,6 +93,7 @@ struct MlaDesc {
     int32_t causal;
     int64_t pos_offset, window, sinks;
     float qscale;        // scale * log2 e, folded into the absorbed queries
+    int32_t use_tc;      // scores on the tensor cores (mla_tc.cu); 0: CUDA cores only
 };
 // The new cache rows of a decode step (state_new == nullptr: none), written
 // by the first launch: state[offset + r, :] = state_new[r, :].
@@ -102,13 +103,26 @@ struct MlaCacheWrite {
     int64_t rows, offset;
 };
 struct MlaPlan {
+    int32_t num_sms = 152;
     int32_t hq = 2;           // head quads per CTA (4 * hq virtual heads)
     int32_t groups = 1;       // CTAs per split (virtual heads / (4 * hq))
     int32_t splits = 1;
     int32_t sink_splits = 0;
     int64_t lo = 0, hi = 0, sink_end = 0, per = 32;
-    size_t qabs_off = 0, m_off = 0, l_off = 0, o_off = 0, olat_off = 0, workspace_bytes = 0;
+    size_t qabs_off = 0, qlo_off = 0, m_off = 0, l_off = 0, o_off = 0, olat_off = 0, workspace_bytes = 0;
 };
+// The tensor-core attention's split of the same key ranges into 128-row tiles.
+constexpr int kMlaTcMaxSplits = 256;
+struct MlaTcPlan {
+    int32_t groups = 1;       // CTAs per split (16 virtual heads each)
+    int32_t splits = 1;
+    int32_t sink_splits = 0;
+    int32_t n_sink_tiles = 0, n_tiles = 0;
+};
+void mla_tc_plan(const MlaDesc& m, const MlaPlan& base, int num_sms, MlaTcPlan* tp);
+cudaError_t launch_mla_latent_tc(const MlaDesc& m, const MlaPlan& base, const MlaTcPlan& tp, const float* qhi,
+                                 const float* qlo, float* part_m, float* part_l, float* part_o, cudaStream_t stream);
+unsigned int mla_tc_take_device_error();
 void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan);
 cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, const MlaCacheWrite& cw,
                        cudaStream_t stream);

@@ -72,16 +72,28 @@ enum MlaError : unsigned int {
 
 static_assert(kW % kBoxCols == 0 && kR == 512 && kP == 64, "latent row layout");
 
+__device__ __forceinline__ void store_q(float* qabs, float* qlo, int64_t i, float x) {
+    if (qlo == nullptr) {
+        qabs[i] = x;
+    } else {
+        const float hi = __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+        qabs[i] = hi;
+        qlo[i] = x - hi;
+    }
+}
+
 // ---- 1. absorb the queries, write the new cache rows ------------------------
 // grid (heads, kR / 128, ceil(T / 4)), 256 threads.  Lane l of warp w owns
 // latent columns 128 jb + 4 l .. + 3 and the k_b rows i = w, w + 8, ... of
 // head h: one 16-byte load per row, all issued before the sums (the read of
 // k_b is latency-bound otherwise); the eight warps' sums meet in shared memory.
 constexpr int kAbsorbRows = 4;  // query rows per block
+// With `qlo`, the result is written split for the tensor cores: qabs = its
+// value with the low 13 mantissa bits cleared (a tf32 value), qlo = the rest.
 __global__ void __launch_bounds__(256) mla_absorb_kernel(const float* __restrict__ q,
                                                          const float* __restrict__ k_b,
-                                                         float* __restrict__ qabs, int64_t T, int H, int N,
-                                                         float qscale, MlaCacheWrite cw) {
+                                                         float* __restrict__ qabs, float* __restrict__ qlo,
+                                                         int64_t T, int H, int N, float qscale, MlaCacheWrite cw) {
     extern __shared__ float sh[];
     float* qn = sh;                          // [kAbsorbRows][N]
     float* red = sh + kAbsorbRows * N;       // [8][kAbsorbRows][128]
@@ -128,12 +140,13 @@ __global__ void __launch_bounds__(256) mla_absorb_kernel(const float* __restrict
         float sum = 0.f;
 #pragma unroll
         for (int w8 = 0; w8 < 8; ++w8) sum += red[(w8 * kAbsorbRows + t) * 128 + c];
-        qabs[((t0 + t) * H + h) * kW + jb * 128 + c] = sum * qscale;
+        store_q(qabs, qlo, ((t0 + t) * H + h) * kW + jb * 128 + c, sum * qscale);
     }
     if (jb == 0) {  // the rotary part passes through, scaled
         for (int idx = tid; idx < rows * kP; idx += blockDim.x) {
             const int t = idx / kP, r = idx % kP;
-            qabs[((t0 + t) * H + h) * kW + kR + r] = __ldg(q + (t0 + t) * H * Dq + (int64_t)h * Dq + N + r) * qscale;
+            store_q(qabs, qlo, ((t0 + t) * H + h) * kW + kR + r,
+                    __ldg(q + (t0 + t) * H * Dq + (int64_t)h * Dq + N + r) * qscale);
         }
     }
 }
@@ -596,6 +609,8 @@ size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 }  // namespace
 
+void mla_layout(MlaPlan* plan, int64_t V, int n);
+
 void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan) {
     const int64_t V = m.T * m.H;
     plan->hq = V <= 8 ? 2 : (V <= 16 ? 4 : 8);
@@ -642,20 +657,34 @@ void mla_plan(const MlaDesc& m, int num_sms, MlaPlan* plan) {
     plan->per = per;
     plan->sink_splits = (int)n_sink;
     plan->splits = (int)n;
-    // Workspace: the decode counters' header, q_abs, then m, l and o partials.
+    plan->num_sms = num_sms;
+    mla_layout(plan, V, (int)n);
+}
+
+// Workspace: the decode counters' header, q_abs (and its tf32 remainder),
+// then the m, l and o partials of n splits, then the merged latents.
+void mla_layout(MlaPlan* plan, int64_t V, int n) {
     plan->qabs_off = kWorkspaceHeader;
-    plan->m_off = plan->qabs_off + up256((size_t)V * kW * 4);
+    plan->qlo_off = plan->qabs_off + up256((size_t)V * kW * 4);
+    plan->m_off = plan->qlo_off + up256((size_t)V * kW * 4);
     plan->l_off = plan->m_off + up256((size_t)V * n * 4);
     plan->o_off = plan->l_off + up256((size_t)V * n * 4);
     plan->olat_off = plan->o_off + up256((size_t)V * n * kR * 4);
     plan->workspace_bytes = plan->olat_off + up256((size_t)V * kR * 4);
 }
 
-cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, const MlaCacheWrite& cw,
+cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& base, void* workspace, const MlaCacheWrite& cw,
                        cudaStream_t stream) {
+    if (m.T == 0) return cudaSuccess;
+    MlaPlan plan = base;
+    MlaTcPlan tp;
+    if (m.use_tc) {
+        mla_tc_plan(m, base, base.num_sms, &tp);
+        mla_layout(&plan, m.T * m.H, tp.splits);
+    }
     char* w = static_cast<char*>(workspace);
     float* qabs = reinterpret_cast<float*>(w + plan.qabs_off);
-    if (m.T == 0) return cudaSuccess;
+    float* qlo = m.use_tc ? reinterpret_cast<float*>(w + plan.qlo_off) : nullptr;
     const int64_t tblocks = (m.T + kAbsorbRows - 1) / kAbsorbRows;
     const size_t absorb_smem = (size_t)(kAbsorbRows * m.N + 8 * kAbsorbRows * 128) * sizeof(float);
     if (absorb_smem > 48 * 1024) {
@@ -663,47 +692,55 @@ cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& plan, void* workspace, c
         if (e != cudaSuccess) return e;
     }
     mla_absorb_kernel<<<dim3(m.H, kR / 128, (unsigned)tblocks), 256, absorb_smem, stream>>>(
-        m.q, m.k_b, qabs, m.T, m.H, m.N, m.qscale, cw);
+        m.q, m.k_b, qabs, qlo, m.T, m.H, m.N, m.qscale, cw);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (m.S == 0)  // no cache row: every output row is zero
         return cudaMemsetAsync(m.out, 0, (size_t)m.T * m.H * m.Dv * sizeof(float), stream);
-    CUtensorMap tm;
-    std::memset(&tm, 0, sizeof(tm));
-    if (!encode_state(&tm, m.state, m.S)) return cudaErrorInvalidValue;
-    LatArgs args;
-    std::memset(&args, 0, sizeof(args));
-    args.a.S = m.S;
-    args.a.T = m.T;
-    args.a.H = m.H;
-    args.a.causal = m.causal;
-    args.a.pos_offset = m.pos_offset;
-    args.a.window = m.window;
-    args.a.sinks = m.window > 0 ? m.sinks : 0;
-    args.qabs = qabs;
-    args.part_m = reinterpret_cast<float*>(w + plan.m_off);
-    args.part_l = reinterpret_cast<float*>(w + plan.l_off);
-    args.part_o = reinterpret_cast<float*>(w + plan.o_off);
-    args.V = (int32_t)(m.T * m.H);
-    args.splits = plan.splits;
-    args.sink_splits = plan.sink_splits;
-    args.sink_end = plan.sink_end;
-    args.lo = plan.lo;
-    args.hi = plan.hi;
-    args.per = plan.per;
-    switch (plan.hq) {
-        case 2: e = launch_latent<2>(tm, args, plan.groups, stream); break;
-        case 4: e = launch_latent<4>(tm, args, plan.groups, stream); break;
-        default: e = launch_latent<8>(tm, args, plan.groups, stream); break;
+    float* part_m = reinterpret_cast<float*>(w + plan.m_off);
+    float* part_l = reinterpret_cast<float*>(w + plan.l_off);
+    float* part_o = reinterpret_cast<float*>(w + plan.o_off);
+    int splits = plan.splits;
+    if (m.use_tc) {
+        e = launch_mla_latent_tc(m, plan, tp, qabs, qlo, part_m, part_l, part_o, stream);
+        splits = tp.splits;
+    } else {
+        CUtensorMap tm;
+        std::memset(&tm, 0, sizeof(tm));
+        if (!encode_state(&tm, m.state, m.S)) return cudaErrorInvalidValue;
+        LatArgs args;
+        std::memset(&args, 0, sizeof(args));
+        args.a.S = m.S;
+        args.a.T = m.T;
+        args.a.H = m.H;
+        args.a.causal = m.causal;
+        args.a.pos_offset = m.pos_offset;
+        args.a.window = m.window;
+        args.a.sinks = m.window > 0 ? m.sinks : 0;
+        args.qabs = qabs;
+        args.part_m = part_m;
+        args.part_l = part_l;
+        args.part_o = part_o;
+        args.V = (int32_t)(m.T * m.H);
+        args.splits = plan.splits;
+        args.sink_splits = plan.sink_splits;
+        args.sink_end = plan.sink_end;
+        args.lo = plan.lo;
+        args.hi = plan.hi;
+        args.per = plan.per;
+        switch (plan.hq) {
+            case 2: e = launch_latent<2>(tm, args, plan.groups, stream); break;
+            case 4: e = launch_latent<4>(tm, args, plan.groups, stream); break;
+            default: e = launch_latent<8>(tm, args, plan.groups, stream); break;
+        }
     }
     if (e != cudaSuccess) return e;
+    const unsigned V = (unsigned)(m.T * m.H);
     float* olat = reinterpret_cast<float*>(w + plan.olat_off);
-    mla_merge_kernel<<<dim3((unsigned)args.V, kR / 32), 256, 0, stream>>>(args.part_m, args.part_l, args.part_o,
-                                                                         olat, plan.splits);
+    mla_merge_kernel<<<dim3(V, kR / 32), 256, 0, stream>>>(part_m, part_l, part_o, olat, splits);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    mla_project_kernel<<<dim3((unsigned)args.V, (unsigned)((m.Dv + 31) / 32)), 256, 0, stream>>>(olat, m.v_b, m.out,
-                                                                                                 m.H, m.Dv);
+    mla_project_kernel<<<dim3(V, (unsigned)((m.Dv + 31) / 32)), 256, 0, stream>>>(olat, m.v_b, m.out, m.H, m.Dv);
     return cudaGetLastError();
 }
 

@@ -322,6 +322,8 @@ vtmu_status resolve_mla(const vtmu_mla_params* p, vtmu::MlaDesc* m) {
     m->sinks = p->window > 0 ? p->sinks : 0;  // without a window no key is dropped
     const double scale = p->has_scale ? (double)p->scale : 1.0 / std::sqrt((double)(p->qk_nope + p->qk_rope));
     m->qscale = (float)(scale * 1.4426950408889634);
+    if (p->kernel < 0 || p->kernel > 2) return fail(VTMU_ERR_INVALID, "mla: kernel %d is not 0, 1 or 2", p->kernel);
+    m->use_tc = p->kernel == 2 ? 1 : 0;
     return VTMU_OK;
 }
 
@@ -717,8 +719,9 @@ static vtmu_status run_mla(vtmu::MlaDesc& m, const float* q, const float* state,
     }
     vtmu::MlaPlan plan;
     vtmu::mla_plan(m, device_sm_count(), &plan);
-    if (!workspace || workspace_bytes < plan.workspace_bytes)
-        return fail(VTMU_ERR_WORKSPACE, "mla needs a workspace of %zu bytes (got %zu)", mla_workspace(m),
+    const size_t need = mla_workspace(m);
+    if (!workspace || workspace_bytes < need)
+        return fail(VTMU_ERR_WORKSPACE, "mla needs a workspace of %zu bytes (got %zu)", need,
                     workspace ? workspace_bytes : (size_t)0);
     if (reinterpret_cast<uintptr_t>(workspace) & 255u)
         return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
@@ -791,7 +794,8 @@ vtmu_status vtmu_device_error(unsigned int* flags) {
     *flags = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device_error: synchronize");
-    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error() | vtmu::mla_take_device_error();
+    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error() | vtmu::mla_take_device_error() |
+             vtmu::mla_tc_take_device_error();
     return ok();
 }
 

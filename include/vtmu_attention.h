@@ -386,6 +386,10 @@ typedef struct vtmu_mla_params {
     int64_t pos_offset;   /* absolute position of query row 0, >= 0 */
     int64_t window;       /* 0 = off; as for op "attention" */
     int64_t sinks;        /* with a window: keys s < sinks stay visible */
+    int32_t kernel;       /* 0 (auto): the CUDA-core kernel, the faster of the
+                             two on the decode shapes measured; 1: the CUDA-core
+                             kernel; 2: scores on the tensor cores (3xTF32),
+                             values on the CUDA cores */
 } vtmu_mla_params;
 
 /* Writes the defaults: causal = 1, kv_rank 512, qk_rope 64, the rest 0. */
@@ -439,7 +443,9 @@ VTMU_API vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const 
  * copies; tensor-core prefill bits: 0x100 stage load, 0x200 free stage,
  * 0x400 drain, 0x800 query load, 0x1000 score tile, 0x2000 probabilities,
  * 0x4000 P.V product; latent attention bits: 0x10000 stage load, 0x20000
- * free stage, 0x40000 drain.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
+ * free stage, 0x40000 drain (CUDA-core kernel), 0x100000 ring item,
+ * 0x200000 free slot, 0x400000 split item, 0x800000 score tile, 0x1000000
+ * free score buffer, 0x2000000 drain (tensor-core kernel).  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
  */
 VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
 

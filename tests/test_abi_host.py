@@ -349,6 +349,8 @@ def test_mla_params_init_writes_defaults(lib):
     (dict(window=-2), vtmu.VTMU_ERR_INVALID, "window"),
     (dict(scale=float("inf")), vtmu.VTMU_ERR_INVALID, "scale"),
     (dict(T=4097, heads=16), vtmu.VTMU_ERR_UNSUPPORTED, "T * heads"),
+    (dict(kernel=3), vtmu.VTMU_ERR_INVALID, "kernel"),
+    (dict(kernel=-1), vtmu.VTMU_ERR_INVALID, "kernel"),
 ])
 def test_mla_invalid_params_are_refused(lib, kw, status, word):
     base = dict(T=1, S=128, heads=4, qk_nope=64, v_head_dim=64)

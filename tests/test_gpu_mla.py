@@ -52,12 +52,16 @@ CASES = [
 ]
 
 
+KERNELS = [vtmu.MLA_KERNEL_TENSOR_CORES, vtmu.MLA_KERNEL_CUDA_CORES]
+
+
+@pytest.mark.parametrize("kernel", KERNELS, ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("case", range(len(CASES)))
-def test_mla_attention_cases(case):
+def test_mla_attention_cases(case, kernel):
     T, S, H, N, Dv, params = CASES[case]
     x = si.mla_inputs(S, T, H, R, N, P, Dv, 100 + case)
     kw = dict(heads=H, qk_nope=N, v_head_dim=Dv, **params)
-    out = vtmu.mla_attention(_dev(x["q"]), _dev(x["state"]), _dev(x["k_b"]), _dev(x["v_b"]), **kw)
+    out = vtmu.mla_attention(_dev(x["q"]), _dev(x["state"]), _dev(x["k_b"]), _dev(x["v_b"]), kernel=kernel, **kw)
     torch.cuda.synchronize()
     ref = oracle.mla_attention(x["q"], x["state"], x["k_b"], x["v_b"], kv_rank=R, qk_rope=P, **kw)
     _check(out.cpu().numpy(), ref, f"case {case}")
@@ -75,8 +79,9 @@ def test_mla_no_visible_key_gives_zeros():
     assert np.array_equal(out.cpu().numpy(), np.zeros((T, H * Dv), np.float32))
 
 
+@pytest.mark.parametrize("kernel", KERNELS, ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("name", ["mla_decode", "mla_decode_v3"])
-def test_mla_decode_step_workload(name):
+def test_mla_decode_step_workload(name, kernel):
     """The full-size decode step (cache_write of the new latent row, then one
     query row over 32768 cache rows), as the benchmark runs it; the oracle
     recomputes every head (16) or 12 of them (128 heads), and the cache must
@@ -86,7 +91,7 @@ def test_mla_decode_step_workload(name):
     H, N, Dv, off = w["heads"], w["qk_nope"], w["v_head_dim"], w["offset"]
     state = _dev(x["state"])
     out = vtmu.mla_decode_step(state, _dev(x["state_new"]), off, _dev(x["q"]), _dev(x["k_b"]), _dev(x["v_b"]),
-                               heads=H, qk_nope=N, v_head_dim=Dv, **w["params"])
+                               heads=H, qk_nope=N, v_head_dim=Dv, kernel=kernel, **w["params"])
     torch.cuda.synchronize()
     oracle.cache_write(x["state"], x["state_new"], off)
     st = state.cpu().numpy()
