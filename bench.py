@@ -567,6 +567,20 @@ def finish_prefill(ctx, res):
             "gpu_launches": res["gpu_launches"], "clocks": clocks}
 
 
+def decode_launches(w, args):
+    """Kernels one decode step launches: the fused decode kernel (1), the
+    tensor-core decode of several query rows (query split with the cache
+    write, attention, split merge: 3) or, forced, cache writes plus the FFMA
+    prefill (3)."""
+    if args.kernel == "ffma":
+        return 3
+    R, G = w.get("rows", 1), w["heads"] // w["kvHeads"]
+    p = w["params"]
+    tc = (R >= 2 and R * G <= 16 and w["headDim"] == 128 and not p.get("softcap") and not p.get("alibi")
+          and not w.get("rope"))
+    return 3 if tc else 1
+
+
 def measure_decode(ctx, name):
     """The decode step of a decode workload: W + K fused steps alternating two
     cache sets (each step's K/V come from HBM), the same step as separate
@@ -676,10 +690,11 @@ def measure_decode(ctx, name):
            "d2h_bytes_per_step": d2h, "steps": n_e2e}
     del sessions, q, kn, vn, out, ws
     torch.cuda.empty_cache()
-    kernel_tag = "prefill_ffma" if args.kernel == "ffma" else "decode"
+    kernel_tag = ("prefill_ffma" if args.kernel == "ffma" else
+                  "decode_tc" if decode_launches(w, args) == 3 else "decode")
     return {"workload": name, "x": x, "w": w, "step_bytes": step_bytes, "step_ms": step_ms, "kernel_ms": kern_ms,
             "unfused_ms": unfused_ms, "e2e": e2e, "kernel_tag": kernel_tag,
-            "launches_per_step": 3 if args.kernel == "ffma" else 1, "_window": window}
+            "launches_per_step": decode_launches(w, args), "_window": window}
 
 
 def measure_mla(ctx, name):

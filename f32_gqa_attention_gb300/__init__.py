@@ -30,6 +30,7 @@ VTMU_ERR_CUDA = 5
 VTMU_ALIBI_NONE, VTMU_ALIBI_BLOOM, VTMU_ALIBI_MPT, VTMU_ALIBI_SLOPES = 0, 1, 2, 3
 VTMU_BIAS_NONE, VTMU_BIAS_TS, VTMU_BIAS_HTS = 0, 1, 2
 VTMU_KERNEL_AUTO, VTMU_KERNEL_DECODE, VTMU_KERNEL_PREFILL_FFMA, VTMU_KERNEL_PREFILL_TF32X3 = 0, 1, 2, 3
+VTMU_KERNEL_DECODE_TF32X3 = 4
 
 EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu_attention",
             "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",

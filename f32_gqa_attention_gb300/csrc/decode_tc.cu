@@ -1,0 +1,797 @@
+// decode_tc.cu -- split-KV decode of a few query rows (a speculative or
+// chunked step: T rows at positions posOffset .. posOffset + T - 1 against a
+// KV cache, headDim 128) with both contractions on the tcgen05 tensor cores
+// in 3xTF32.
+//
+// Op "attention" (vtmu.mpakt.dev/api/ops) with GQA: query head h reads KV
+// head h / G.  For one KV head the T rows x G heads form up to 16 virtual
+// heads v = t G + g, and all of them meet the same K and V rows.  The roles
+// of the MMAs are swapped with respect to a prefill: the 16 virtual heads are
+// the N side of both products,
+//     S^T[key, v] = sum_d K[key, d] q[v, d] scale log2 e     (M = 128 keys)
+//     O^T[d, v]   = sum_key V^T[d, key] P^T[key, v]          (M = 128 dims)
+// each as hi.hi + hi.lo + lo.hi (3xTF32), so one M = 128, N = 16 MMA does
+// 2048 (key, head) or (dim, head) pairs.  K and Q are K-major in shared
+// memory as the score MMA reads them; the values' contraction index (the
+// cache row) is not contiguous in the cache, so V goes to TMEM transposed
+// (dims as lanes, rows as columns) through registers and serves as the TMEM
+// operand A, with P^T (heads x rows, rows contiguous) from shared memory.
+// Each K and V byte of the visible range is read from HBM once for all T
+// rows.
+//
+// Three launches:
+//  1. decode_tc_prep: the step's new cache rows written (when the call is a
+//     decode step), and the scaled query split into Q_hi (tf32, rounded to
+//     nearest) and Q_lo = q - Q_hi, laid out [kv head][hi|lo][16][128] with
+//     zero rows for virtual heads past T G;
+//  2. decode_tc_kernel, grid (kv heads, splits); one CTA streams a run of
+//     128-row tiles of its KV head's range (the attention sinks' tiles
+//     first, as splits of their own).  Warps:
+//       0      lane 0: the query tiles once, then the score ring (K blocks of
+//              [128 rows x 32 dims] by TMA, 128-byte swizzle);
+//       1      lane 0 issues the score MMAs into S buffer (tile & 1); warp 1
+//              owns TMEM (S 2 x 16 columns, O 2 x 16, V^T hi and lo 128
+//              each);
+//       2      lane 0: the value ring (V blocks of [128 rows x 32 dims]);
+//       3      lane 0 issues the P.V MMAs of a tile into O buffer (tile & 1)
+//              once its P^T and V^T are in place;
+//       4 .. 7 split each K block in place into K_hi (low 13 mantissa bits
+//              cleared) and K_lo = K - K_hi beside it;
+//       8 .. 15 two softmax groups: warps 8 .. 11 take the even tiles of
+//              the run, 12 .. 15 the odd ones, so two tiles are in flight;
+//              each group has its own S buffer, P^T buffer and O buffer and
+//              its own running (m, l, o).  Thread = a row of the tile, all 16
+//              heads: read S^T from TMEM, mask, reduce max and sum over the
+//              rows (a reduce-scatter over the warp, then the group's four
+//              warps through shared memory), online softmax in base 2 with
+//              a lazy reference max (rescale only when a max grows by more
+//              than 2^8), P^T hi and lo to shared memory; then warp q of
+//              the group moves the tile's V block q (dims 32 q ..) into TMEM
+//              lanes 32 q .. as V^T hi and lo (once the previous tile's P.V
+//              MMAs are done with V^T), and the group folds its previous
+//              tile's O into registers, o = o alpha + O (a fresh accumulator
+//              per tile, so no sum runs long inside the tensor pipe);
+//     and writes (m, l, o) per virtual head and group of its split;
+//  3. decode_tc_merge: per (KV head, virtual head) the log-sum-exp merge of
+//     the (split, group) partials, m* = max m_i, l* = sum l_i 2^(m_i - m*),
+//     o* = sum o_i 2^(m_i - m*) / l*, written to the output row (zeros when
+//     no key is visible).
+// Every ring item is waited for and released by every role that reads it,
+// so no role is ever two phases behind a slot (an mbarrier wait only checks
+// a phase's parity); a value block always lands in the slots of the one
+// warp that reads it.  Every wait is bounded; a wait that gives up sets a
+// bit of g_decode_tc_device_error and the kernel unwinds.
+#include <cstring>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "attn_common.cuh"
+#include "kernels.h"
+#include "launch_cache.h"
+#include "tcgen05_ops.cuh"
+#include "tma_sync.cuh"
+
+namespace vtmu {
+
+__device__ unsigned int g_decode_tc_device_error;
+
+namespace {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int kNV = kDecodeTcHeads;   // virtual heads per KV head (MMA N)
+constexpr int kD = 128;               // head dim (the P.V MMA's M)
+constexpr int kKT = 128;              // cache rows per tile (the score MMA's M)
+constexpr int kC = kD / 32;           // 32-dim blocks per tile
+constexpr int kNK = 3;                // score ring slots
+constexpr int kNVR = 4;               // value ring slots
+constexpr uint32_t kBlockBytes = kKT * 32 * 4;  // one [128 rows x 32 dims] block, 16 KB
+constexpr uint32_t kKSlot = 2 * kBlockBytes;    // K (hi after the split) | K_lo
+constexpr uint32_t kQChunk = kNV * 32 * 4;      // [16 heads x 32 dims or rows], 2 KB
+constexpr uint32_t kQBytes = 2u * kC * kQChunk;   // Q_hi chunks, then Q_lo chunks
+constexpr uint32_t kPTBytes = 2u * (kKT / 32) * kQChunk;  // per group: P^T hi blocks, then lo blocks
+constexpr int kThreads = 16 * 32;
+constexpr size_t kSmem = 1024 + (size_t)kNK * kKSlot + (size_t)kNVR * kBlockBytes + kQBytes + 2 * kPTBytes;
+constexpr float kRescaleLog2 = 8.f;
+// TMEM columns: S (2 buffers x 16), O (2 buffers x 16), V^T hi and lo (128 each).
+constexpr uint32_t kColS = 0, kColO = 32, kColVhi = 128, kColVlo = 256, kTmemCols = 512;
+constexpr uint32_t kKReleases = 4 + 1;  // splitter warps, the score issuer's commit
+static_assert(kSmem + 2048 <= 232448, "shared memory budget");
+static_assert(kC == 4 && kNVR == kC, "slot q holds value block q of every tile (one arrival per tile)");
+
+enum : unsigned int {
+    kErrDtFull = 1u << 26,    // a consumer gave up on an arriving ring item or the query tiles
+    kErrDtEmpty = 1u << 27,   // a producer gave up on a free slot
+    kErrDtSplit = 1u << 28,   // an issuer gave up on a split item
+    kErrDtS = 1u << 29,       // a softmax warp gave up on a score tile
+    kErrDtFree = 1u << 30,    // an issuer gave up on a free score buffer
+    kErrDtDrain = 1u << 31,   // a producer gave up draining its copies
+    kErrDtPV = kErrDtS,       // a P.V or fold wait gave up (reported with the score-tile bit)
+    kErrDtV = kErrDtFull,     // a value block or free V^T wait gave up
+};
+
+struct DtArgs {
+    AttnDesc a;        // S, T, H, G, causal, pos_offset, window, sinks (visibility)
+    float* part_m;     // [Hk][16][splits]
+    float* part_l;
+    float* part_o;     // [Hk][16][splits][D]
+    int32_t nv;        // virtual heads in use: T * G
+    int32_t sink_lim;  // with a window: rows below this are attention sinks (0: none)
+    int32_t splits;
+    int32_t sink_splits;
+    int32_t n_sink_tiles, n_tiles;  // tiles of the sink range and of the main range
+    int64_t lo;        // first row of the main range (the sink range starts at 0)
+    int64_t sink_end, hi;
+};
+
+// Tiles [t0, t1) of this split in the concatenated (sink, main) tile list.
+__device__ __forceinline__ void split_tiles(const DtArgs& g, int split, int& t0, int& t1) {
+    if (split < g.sink_splits) {
+        t0 = (int)((int64_t)g.n_sink_tiles * split / g.sink_splits);
+        t1 = (int)((int64_t)g.n_sink_tiles * (split + 1) / g.sink_splits);
+    } else {
+        const int ms = g.splits - g.sink_splits, i = split - g.sink_splits;
+        t0 = g.n_sink_tiles + (int)((int64_t)g.n_tiles * i / ms);
+        t1 = g.n_sink_tiles + (int)((int64_t)g.n_tiles * (i + 1) / ms);
+    }
+}
+// First cache row of tile `t` of the concatenated list, and its range end.
+__device__ __forceinline__ void tile_rows(const DtArgs& g, int t, int64_t& r0, int64_t& rend) {
+    if (t < g.n_sink_tiles) {
+        r0 = (int64_t)t * kKT;
+        rend = g.sink_end;
+    } else {
+        r0 = g.lo + (int64_t)(t - g.n_sink_tiles) * kKT;
+        rend = g.hi;
+    }
+}
+
+// Barrier over one softmax group's four warps (named barrier ID, 128
+// threads); returns the AND of `v` over them.
+template <int ID>
+__device__ __forceinline__ bool group_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, %2, 128, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(ID)
+        : "memory");
+    return r != 0;
+}
+
+// ---- 1: new cache rows, query split ----------------------------------------
+// Blocks [0, Hk): the query tiles of KV head blockIdx.x.  Blocks after them:
+// the cache write, float4 per thread (K rows, then V rows).
+template <int D>
+__global__ void __launch_bounds__(256) decode_tc_prep(AttnDesc a, float* qhl, DecodeCacheWrite cw, int64_t cw_vec) {
+    if ((int)blockIdx.x < a.Hk) {
+        const int hk = blockIdx.x;
+        const int nv = (int)a.T * a.G;
+        for (int i = threadIdx.x; i < kNV * D; i += blockDim.x) {
+            const int v = i / D, d = i % D;
+            float x = 0.f;
+            if (v < nv) {
+                const int t = v / a.G, h = hk * a.G + v % a.G;
+                x = a.q[((int64_t)t * a.H + h) * D + d] * a.qk_mul;
+            }
+            const float hi = tf32_rna(x);
+            qhl[((size_t)(hk * 2 + 0) * kNV + v) * D + d] = hi;
+            qhl[((size_t)(hk * 2 + 1) * kNV + v) * D + d] = x - hi;
+        }
+        return;
+    }
+    const int64_t i = (int64_t)(blockIdx.x - a.Hk) * blockDim.x + threadIdx.x;  // float4 index
+    const int64_t width = (int64_t)a.Hk * D / 4;                                   // float4 per row
+    if (i < cw_vec) {
+        const int64_t r = i / width, c = i % width;
+        reinterpret_cast<float4*>(cw.kc)[(cw.lo + r) * width + c] = reinterpret_cast<const float4*>(cw.k_new)[i];
+    } else if (i < 2 * cw_vec) {
+        const int64_t j = i - cw_vec, r = j / width, c = j % width;
+        reinterpret_cast<float4*>(cw.vc)[(cw.lo + r) * width + c] = reinterpret_cast<const float4*>(cw.v_new)[j];
+    }
+}
+
+// ---- 2: the split-KV attention ----------------------------------------------
+__global__ void __launch_bounds__(kThreads, 1)
+    decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                     const __grid_constant__ CUtensorMap tm_q, const DtArgs g) {
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                           ~uintptr_t(1023));
+    unsigned char* kring = base;                              // kNK slots
+    unsigned char* vring = kring + kNK * kKSlot;              // kNVR slots
+    unsigned char* qsm = vring + kNVR * kBlockBytes;          // Q_hi chunks, Q_lo chunks
+    unsigned char* pt = qsm + kQBytes;                        // per group: P^T hi blocks, then lo blocks
+    __shared__ __align__(8) uint64_t kfull[kNK], kempty[kNK], split_done[kNK], vfull[kNVR], vempty[kNVR],
+        s_full[2], s_free[2], q_full, p_full[2], p_free[2], vt_full, vt_free, o_full[2], o_free[2];
+    __shared__ uint32_t tmem_base_s;
+    __shared__ __align__(16) float red_max[2][4][kNV], red_sum[2][4][kNV];  // [group][warp][head]
+    __shared__ __align__(16) float alpha_s[2][2][kNV];  // [group][its tile parity][head]
+    __shared__ __align__(16) int32_t vis_lo[kNV], vis_hi[kNV], vis_shi[kNV];  // per virtual head
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hk = blockIdx.x, split = blockIdx.y;
+    const int col0 = hk * kD;  // the KV head's first column in the caches
+    int t0, t1;
+    split_tiles(g, split, t0, t1);
+    const int ntile = t1 - t0;
+    const int nk = ntile * kC;  // items of each ring
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNK; ++i) {
+            mbar_init(&kfull[i], 1);
+            mbar_init(&kempty[i], kKReleases);
+            mbar_init(&split_done[i], 4);
+        }
+        for (int i = 0; i < kNVR; ++i) {
+            mbar_init(&vfull[i], 1);
+            mbar_init(&vempty[i], 1);
+        }
+        for (int b = 0; b < 2; ++b) {  // per softmax group (its tiles use buffer b)
+            mbar_init(&s_full[b], 1);
+            mbar_init(&s_free[b], 4);
+            mbar_init(&p_full[b], 4);
+            mbar_init(&p_free[b], 1);
+            mbar_init(&o_full[b], 1);
+            mbar_init(&o_free[b], 4);
+        }
+        mbar_init(&q_full, 1);
+        mbar_init(&vt_full, 4);
+        mbar_init(&vt_free, 1);
+        fence_barrier_init();
+        // Visible keys of virtual head v (query row v / G): the window's
+        // range [lo, hi] and the sinks below vis_shi + 1 (int32: S < 2^31).
+        const AttnDesc& a = g.a;
+        for (int v = 0; v < kNV; ++v) {
+            int64_t lo = a.S, hi = -1, shi = -1;
+            if (v < g.nv) {
+                const int64_t pos = a.pos_offset + v / a.G;
+                hi = a.causal ? pos : (a.window > 0 ? pos + a.window : a.S - 1);
+                lo = a.window > 0 ? (a.causal ? pos - a.window + 1 : pos - a.window) : 0;
+                shi = a.causal ? pos : a.S - 1;
+                if (hi > a.S - 1) hi = a.S - 1;
+                if (shi > a.S - 1) shi = a.S - 1;
+                if (lo < 0) lo = 0;
+                if (lo > a.S) lo = a.S;
+                if (hi < -1) hi = -1;
+                if (shi < -1) shi = -1;
+            }
+            vis_lo[v] = (int32_t)lo;
+            vis_hi[v] = (int32_t)hi;
+            vis_shi[v] = (int32_t)shi;
+        }
+    }
+    if (warp == 1) tmem_alloc(&tmem_base_s, kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = tmem_base_s;
+
+    if (warp == 0 || warp == 2) {
+        // ---- producers: warp 0 the query tiles and the score ring, warp 2 the value ring ----
+        if (lane == 0) {
+            const bool scores = warp == 0;
+            const CUtensorMap* map = scores ? &tm_k : &tm_v;
+            const int ns = scores ? kNK : kNVR;
+            const uint32_t slot_bytes = scores ? kKSlot : kBlockBytes;
+            unsigned char* ring = scores ? kring : vring;
+            uint64_t* fullb = scores ? kfull : vfull;
+            uint64_t* emptyb = scores ? kempty : vempty;
+            prefetch_tensormap(map);
+            if (scores) {
+                prefetch_tensormap(&tm_v);
+                prefetch_tensormap(&tm_q);
+                mbar_arrive_expect_tx(&q_full, kQBytes);
+#pragma unroll 1
+                for (int c = 0; c < 2 * kC; ++c)  // hi chunks (rows 0..15), then lo chunks (rows 16..31)
+                    tma_load_2d(qsm + c * kQChunk, &tm_q, 32 * (c % kC), hk * 2 * kNV + (c / kC) * kNV, &q_full);
+            }
+            int it = 0;
+            for (; it < nk; ++it) {
+                const int s = it % ns;
+                const int tl = it / kC, c = it % kC;
+                if (it >= ns && !mbar_wait(&emptyb[s], (uint32_t)((it / ns - 1) & 1))) {
+                    raise_device_error(&g_decode_tc_device_error, kErrDtEmpty);
+                    break;
+                }
+                int64_t r0, rend;
+                tile_rows(g, t0 + tl, r0, rend);
+                mbar_arrive_expect_tx(&fullb[s], kBlockBytes);
+                tma_load_2d(ring + (size_t)s * slot_bytes, map, col0 + 32 * c, (int)r0, &fullb[s]);
+            }
+            // No copy may be in flight when the CTA exits.
+            for (int j = it - ns < 0 ? 0 : it - ns; j < it; ++j)
+                if (!mbar_wait(&fullb[j % ns], (uint32_t)((j / ns) & 1)))
+                    raise_device_error(&g_decode_tc_device_error, kErrDtDrain);
+            if (scores && nk == 0 && !mbar_wait(&q_full, 0))  // the query copy, when no MMA waited for it
+                raise_device_error(&g_decode_tc_device_error, kErrDtDrain);
+        }
+    } else if (warp == 1) {
+        // ---- score MMAs: S^T = K_hi.Q_hi + K_hi.Q_lo + K_lo.Q_hi into buffer tl & 1 ----
+        if (lane == 0 && nk > 0) {
+            constexpr uint32_t idesc = idesc_tf32(kKT, kNV);
+            bool ok = mbar_wait(&q_full, 0);
+            if (!ok) raise_device_error(&g_decode_tc_device_error, kErrDtFull);
+            uint32_t sd_phase = 0;  // one parity bit per slot
+            for (int it = 0; ok && it < nk; ++it) {
+                const int s = it % kNK;
+                const int tl = it / kC, c = it % kC;
+                const int b = tl & 1;
+                if (c == 0 && tl >= 2 && !mbar_wait(&s_free[b], (uint32_t)(((tl - 2) >> 1) & 1))) {
+                    raise_device_error(&g_decode_tc_device_error, kErrDtFree);
+                    break;
+                }
+                if (!mbar_wait(&split_done[s], (sd_phase >> s) & 1u)) {
+                    raise_device_error(&g_decode_tc_device_error, kErrDtSplit);
+                    break;
+                }
+                sd_phase ^= 1u << s;
+                tc_fence_after();
+                unsigned char* slot = kring + (size_t)s * kKSlot;
+                const uint64_t khi = smem_desc_sw128(slot), klo = smem_desc_sw128(slot + kBlockBytes);
+                const uint64_t qhi = smem_desc_sw128(qsm + c * kQChunk);
+                const uint64_t qlo = smem_desc_sw128(qsm + (kC + c) * kQChunk);
+                const uint32_t d = tmem + kColS + b * kNV;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    mma_tf32_ss(d, khi + 2 * k, qhi + 2 * k, idesc, (c > 0 || k > 0) ? 1u : 0u);
+                    mma_tf32_ss_acc(d, khi + 2 * k, qlo + 2 * k, idesc);
+                    mma_tf32_ss_acc(d, klo + 2 * k, qhi + 2 * k, idesc);
+                }
+                mma_commit(&kempty[s]);
+                if (c == kC - 1) mma_commit(&s_full[b]);
+            }
+        }
+    } else if (warp == 3) {
+        // ---- P.V MMAs: O^T[dims, heads] = V^T_hi.P^T_hi + V^T_hi.P^T_lo + V^T_lo.P^T_hi ----
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_tf32(kD, kNV);
+            for (int tl = 0; tl < ntile; ++tl) {
+                const int b = tl & 1;
+                if (!mbar_wait(&p_full[b], (uint32_t)((tl >> 1) & 1)) || !mbar_wait(&vt_full, (uint32_t)(tl & 1))) {
+                    raise_device_error(&g_decode_tc_device_error, kErrDtPV);
+                    break;
+                }
+                if (tl >= 2 && !mbar_wait(&o_free[b], (uint32_t)(((tl - 2) >> 1) & 1))) {
+                    raise_device_error(&g_decode_tc_device_error, kErrDtPV);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d = tmem + kColO + b * kNV;
+#pragma unroll
+                for (int j = 0; j < kKT / 8; ++j) {  // 8 rows of the tile per MMA
+                    const uint32_t vhi = tmem + kColVhi + 8 * j, vlo = tmem + kColVlo + 8 * j;
+                    unsigned char* ptb = pt + b * kPTBytes;
+                    const uint64_t phi = smem_desc_sw128(ptb + (j >> 2) * kQChunk) + 2 * (j & 3);
+                    const uint64_t plo = smem_desc_sw128(ptb + (kKT / 32 + (j >> 2)) * kQChunk) + 2 * (j & 3);
+                    mma_tf32_ts(d, vhi, phi, idesc, j > 0 ? 1u : 0u);
+                    mma_tf32_ts_acc(d, vhi, plo, idesc);
+                    mma_tf32_ts_acc(d, vlo, phi, idesc);
+                }
+                mma_commit(&p_free[b]);
+                mma_commit(&vt_free);
+                mma_commit(&o_full[b]);
+            }
+        }
+    } else if (warp <= 7) {
+        // ---- splitters: K block -> K_hi in place, K_lo beside it ----
+        const int st = threadIdx.x - 4 * 32;  // 0 .. 127
+        uint32_t f_phase = 0;
+        for (int it = 0; it < nk; ++it) {
+            const int s = it % kNK;
+            const bool got = __all_sync(FULL, mbar_wait(&kfull[s], (f_phase >> s) & 1u));
+            f_phase ^= 1u << s;
+            if (!got) {
+                raise_device_error(&g_decode_tc_device_error, kErrDtFull);
+                break;
+            }
+            float4* hi = reinterpret_cast<float4*>(kring + (size_t)s * kKSlot);
+            float4* lo = reinterpret_cast<float4*>(kring + (size_t)s * kKSlot + kBlockBytes);
+#pragma unroll
+            for (int i = 0; i < (int)(kBlockBytes / 16) / 128; ++i) {
+                const int j = st + 128 * i;
+                const float4 x = hi[j];
+                const float4 h = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
+                hi[j] = h;
+                lo[j] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+            }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic writes -> MMA
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&split_done[s]);
+                mbar_arrive(&kempty[s]);  // the MMAs hold the slot until their own commits
+            }
+        }
+    } else {
+        // ---- softmax groups: warps 8 .. 11 take the even tiles, 12 .. 15 the
+        // odd ones; thread = a row of the tile, all 16 heads ----
+        const int grp = (warp - 8) >> 2;
+        const int quarter = warp & 3;           // TMEM lanes 32 quarter .. + 31
+        const int key_l = 32 * quarter + lane;  // this thread's row of a tile
+        const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+        float o[kNV];  // O^T of dim 32 quarter + lane, every head
+        float m_ref[kNV];
+#pragma unroll
+        for (int h = 0; h < kNV; ++h) {
+            o[h] = 0.f;
+            m_ref[h] = -INFINITY;
+        }
+        float l_run = 0.f;  // head `lane` (lane < 16) of the group's first warp
+        bool ok = true;
+        // V^T of tile vl, once the previous tile's P.V MMAs are done with
+        // V^T.  Row kk, dim lane of a V block sits at byte kk * 128 +
+        // ((lane / 4) ^ (kk % 8)) * 16 + (lane % 4) * 4 (128-byte swizzle).
+        // Slot q holds block q of every tile, and the two groups take turns:
+        // the wait for the previous tile's P.V comes first, because it also
+        // means the other group has taken block q of tile vl - 1 out of the
+        // slot, so the slot's barrier is at most one phase behind tile vl and
+        // its parity names that tile alone.
+        auto move_v = [&](int vl) -> bool {
+            const int vs = (vl * kC + quarter) % kNVR;  // one block per slot and tile
+            const bool vok = (vl == 0 || __all_sync(FULL, mbar_wait(&vt_free, (uint32_t)((vl - 1) & 1)))) &&
+                             __all_sync(FULL, mbar_wait(&vfull[vs], (uint32_t)(vl & 1)));
+            if (!vok) {
+                raise_device_error(&g_decode_tc_device_error, kErrDtV);
+                return false;
+            }
+            tc_fence_after();
+            const unsigned char* vblk = vring + (size_t)vs * kBlockBytes;
+            const int lane_off = (lane & 3) * 4, lane_chunk = lane >> 2;
+#pragma unroll 1
+            for (int ch = 0; ch < kKT / 16; ++ch) {
+                float vh[16], vlo[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) {
+                    const int kk = 16 * ch + r;
+                    const float xv =
+                        *reinterpret_cast<const float*>(vblk + kk * 128 + ((lane_chunk ^ (kk & 7)) << 4) + lane_off);
+                    vh[r] = tf32_trunc(xv);
+                    vlo[r] = xv - vh[r];
+                }
+                tmem_st16(tmem + lanes + kColVhi + 16 * ch, vh);
+                tmem_st16(tmem + lanes + kColVlo + 16 * ch, vlo);
+            }
+            tmem_wait_st();
+            tc_fence_before();
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // read before TMA refills the slot
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&vempty[vs]);
+                mbar_arrive(&vt_full);
+            }
+            return true;
+        };
+        // o = o * alpha + O for the group's tile number fj (its P.V done).
+        auto fold = [&](int fj) -> bool {
+            if (!__all_sync(FULL, mbar_wait(&o_full[grp], (uint32_t)(fj & 1)))) {
+                raise_device_error(&g_decode_tc_device_error, kErrDtPV);
+                return false;
+            }
+            tc_fence_after();
+            float acc[kNV];
+            tmem_ld16(tmem + lanes + kColO + grp * kNV, acc);
+            tmem_wait_ld();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&o_free[grp]);
+            const float4* al = reinterpret_cast<const float4*>(alpha_s[grp][fj & 1]);
+#pragma unroll
+            for (int h4 = 0; h4 < kNV / 4; ++h4) {
+                const float4 a4 = al[h4];
+                o[4 * h4 + 0] = fmaf(o[4 * h4 + 0], a4.x, acc[4 * h4 + 0]);
+                o[4 * h4 + 1] = fmaf(o[4 * h4 + 1], a4.y, acc[4 * h4 + 1]);
+                o[4 * h4 + 2] = fmaf(o[4 * h4 + 2], a4.z, acc[4 * h4 + 2]);
+                o[4 * h4 + 3] = fmaf(o[4 * h4 + 3], a4.w, acc[4 * h4 + 3]);
+            }
+            return true;
+        };
+        // Reduce-scatter of 16 values over the warp's 32 rows: lane ends with
+        // the reduction for head lane / 2 (five shuffle steps, 16 shuffles).
+        auto reduce16 = [&](const float (&v)[kNV], bool is_max) -> float {
+            auto op = [&](float a, float b) { return is_max ? fmaxf(a, b) : a + b; };
+            float a8[8], a4[4], a2[2];
+            const bool b4 = lane & 16, b3 = lane & 8, b2 = lane & 4, b1 = lane & 2;
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                a8[i] = op(b4 ? v[i + 8] : v[i], __shfl_xor_sync(FULL, b4 ? v[i] : v[i + 8], 16));
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                a4[i] = op(b3 ? a8[i + 4] : a8[i], __shfl_xor_sync(FULL, b3 ? a8[i] : a8[i + 4], 8));
+#pragma unroll
+            for (int i = 0; i < 2; ++i)
+                a2[i] = op(b2 ? a4[i + 2] : a4[i], __shfl_xor_sync(FULL, b2 ? a4[i] : a4[i + 2], 4));
+            float r = op(b1 ? a2[1] : a2[0], __shfl_xor_sync(FULL, b1 ? a2[0] : a2[1], 2));
+            return op(r, __shfl_xor_sync(FULL, r, 1));
+        };
+        auto group_sync = [&](bool v) -> bool {  // named barrier 1 or 2 of the group
+            return grp == 0 ? group_sync_and<1>(v) : group_sync_and<2>(v);
+        };
+        int j = 0;  // the group's tile count
+        for (int tl = grp; tl < ntile; tl += 2, ++j) {
+            // A wait that gives up marks the warp; every warp of the group still
+            // reaches the barriers below, which AND the marks, so the group
+            // leaves together (no warp waits alone).
+            float x[kNV];
+#pragma unroll
+            for (int h = 0; h < kNV; ++h) x[h] = -INFINITY;
+            if (ok && !__all_sync(FULL, mbar_wait(&s_full[grp], (uint32_t)(j & 1)))) {
+                raise_device_error(&g_decode_tc_device_error, kErrDtS);
+                ok = false;
+            }
+            if (ok) {
+                tc_fence_after();
+                tmem_ld16(tmem + lanes + kColS + grp * kNV, x);
+                tmem_wait_ld();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[grp]);  // the next score MMAs may overwrite buffer grp
+            }
+            int64_t r0, rend;
+            tile_rows(g, t0 + tl, r0, rend);
+            const int key = (int)(r0 + key_l);
+            const int kend = (int)rend;
+#pragma unroll
+            for (int h4 = 0; h4 < kNV / 4; ++h4) {
+                const int4 lo4 = reinterpret_cast<const int4*>(vis_lo)[h4];
+                const int4 hi4 = reinterpret_cast<const int4*>(vis_hi)[h4];
+                const int4 sh4 = reinterpret_cast<const int4*>(vis_shi)[h4];
+                const int lo[4] = {lo4.x, lo4.y, lo4.z, lo4.w}, hi[4] = {hi4.x, hi4.y, hi4.z, hi4.w},
+                          sh[4] = {sh4.x, sh4.y, sh4.z, sh4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const bool vis = key < kend && ((key >= lo[u] && key <= hi[u]) ||
+                                                    (key < g.sink_lim && key <= sh[u]));
+                    if (!vis) x[4 * h4 + u] = -INFINITY;
+                }
+            }
+            // Tile max per head: the warp's 32 rows, then the group's 4 warps.
+            const float wmax = reduce16(x, true);
+            if (!(lane & 1)) red_max[grp][quarter][lane >> 1] = wmax;
+            ok = group_sync(ok);
+            if (!ok) break;
+            float alpha[kNV];
+#pragma unroll
+            for (int h4 = 0; h4 < kNV / 4; ++h4) {
+                float4 m4 = reinterpret_cast<const float4*>(red_max[grp][0])[h4];
+#pragma unroll
+                for (int q2 = 1; q2 < 4; ++q2) {
+                    const float4 n4 = reinterpret_cast<const float4*>(red_max[grp][q2])[h4];
+                    m4 = make_float4(fmaxf(m4.x, n4.x), fmaxf(m4.y, n4.y), fmaxf(m4.z, n4.z), fmaxf(m4.w, n4.w));
+                }
+                const float mt[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int h = 4 * h4 + u;
+                    alpha[h] = 1.f;
+                    if (mt[u] > m_ref[h] + kRescaleLog2) {  // lazy: keep the reference unless beaten by > 2^8
+                        alpha[h] = fast_exp2(m_ref[h] - mt[u]);  // 0 while nothing was visible
+                        m_ref[h] = mt[u];
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < kNV; ++h) x[h] = fast_exp2(x[h] - (m_ref[h] == -INFINITY ? 0.f : m_ref[h]));
+            // P^T[head][row] into the group's K-major blocks (block = row / 32,
+            // head h's row of a block is 128 bytes, 128-byte swizzle), hi and lo.
+            if (j > 0 && !__all_sync(FULL, mbar_wait(&p_free[grp], (uint32_t)((j - 1) & 1)))) {
+                raise_device_error(&g_decode_tc_device_error, kErrDtPV);
+                ok = false;
+            }
+            if (ok) {
+                unsigned char* blk_hi = pt + grp * kPTBytes + quarter * kQChunk;
+                unsigned char* blk_lo = blk_hi + (kKT / 32) * kQChunk;
+#pragma unroll
+                for (int h = 0; h < kNV; ++h) {
+                    const uint32_t off = h * 128 + (((lane >> 2) ^ (h & 7)) << 4) + (lane & 3) * 4;
+                    const float ph = tf32_rna(x[h]);
+                    *reinterpret_cast<float*>(blk_hi + off) = ph;
+                    *reinterpret_cast<float*>(blk_lo + off) = x[h] - ph;
+                }
+                asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic writes -> MMA
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&p_full[grp]);
+            }
+            const float wsum = reduce16(x, false);
+            if (!(lane & 1)) red_sum[grp][quarter][lane >> 1] = wsum;
+            if (quarter == 0 && lane == 0) {
+                float4* as = reinterpret_cast<float4*>(alpha_s[grp][j & 1]);
+#pragma unroll
+                for (int h4 = 0; h4 < kNV / 4; ++h4)
+                    as[h4] = make_float4(alpha[4 * h4], alpha[4 * h4 + 1], alpha[4 * h4 + 2], alpha[4 * h4 + 3]);
+            }
+            ok = group_sync(ok);
+            if (!ok) break;
+            if (quarter == 0 && lane < kNV)
+                l_run = fmaf(l_run, alpha_s[grp][j & 1][lane],
+                             red_sum[grp][0][lane] + red_sum[grp][1][lane] + red_sum[grp][2][lane] +
+                                 red_sum[grp][3][lane]);
+            // A failed wait leaves the warp's mark for the next barrier.
+            if (!move_v(tl)) ok = false;
+            if (ok && j > 0 && !fold(j - 1)) ok = false;
+        }
+        if (ok && j > 0 && !fold(j - 1)) ok = false;
+        ok = group_sync(ok);
+        if (ok) {
+            const int sub = 2 * split + grp;  // the group's partial sums count as a split of their own
+            const int nsub = 2 * g.splits;
+            if (quarter == 0 && lane < kNV) {
+                float mm = m_ref[0];
+#pragma unroll
+                for (int h = 1; h < kNV; ++h)
+                    if (lane == h) mm = m_ref[h];
+                const int64_t idx = ((int64_t)hk * kNV + lane) * nsub + sub;
+                g.part_m[idx] = j > 0 ? mm : -INFINITY;
+                g.part_l[idx] = j > 0 ? l_run : 0.f;
+            }
+#pragma unroll
+            for (int h = 0; h < kNV; ++h)
+                g.part_o[(((int64_t)hk * kNV + h) * nsub + sub) * kD + 32 * quarter + lane] = o[h];
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+// ---- 3: merge of the splits --------------------------------------------------
+// Block (hk, v): one virtual head, D threads (one dim each).
+template <int D>
+__global__ void __launch_bounds__(D) decode_tc_merge(AttnDesc a, const float* part_m, const float* part_l,
+                                                     const float* part_o, int splits) {
+    const int hk = blockIdx.x, v = blockIdx.y, d = threadIdx.x;
+    if (v >= (int)a.T * a.G) return;
+    const int64_t row = (int64_t)hk * kNV + v;
+    const float* pm = part_m + row * splits;
+    const float* pl = part_l + row * splits;
+    float m = -INFINITY;
+    for (int i = 0; i < splits; ++i) m = fmaxf(m, pm[i]);
+    float l = 0.f, acc = 0.f;
+    if (m != -INFINITY) {
+        for (int i = 0; i < splits; ++i) {
+            const float w = fast_exp2(pm[i] - m);  // 0 for a split that saw nothing
+            l = fmaf(pl[i], w, l);
+            acc = fmaf(part_o[(row * splits + i) * D + d], w, acc);
+        }
+    }
+    const int t = v / a.G, h = hk * a.G + v % a.G;
+    a.out[((int64_t)t * a.H + h) * D + d] = l > 0.f ? acc / l : 0.f;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 dt_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    });
+    return fn;
+}
+
+// Row-major [rows, cols] f32, boxes of 32 columns x box_rows rows, 128-byte swizzle.
+bool encode_blocks(CUtensorMap* map, const float* p, int64_t rows, int64_t cols, int box_rows) {
+    return cached_tensor_map(map, p, rows, cols, 32, box_rows, 3, [&](CUtensorMap* m) {
+        auto fn = dt_encoder();
+        if (!fn) return false;
+        const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)cols * sizeof(float)};
+        const cuuint32_t box[2] = {32u, (cuuint32_t)box_rows};
+        const cuuint32_t estr[2] = {1, 1};
+        return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(p), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    });
+}
+
+size_t up256(size_t b) { return (b + 255) / 256 * 256; }
+
+cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
+                     const DecodeCacheWrite* cw) {
+    unsigned char* ws = static_cast<unsigned char*>(workspace) + kWorkspaceHeader;
+    float* qhl = reinterpret_cast<float*>(ws);
+    const size_t rows = (size_t)a.Hk * kNV * 2 * tp.splits;  // two softmax groups per split
+    float* part_m = reinterpret_cast<float*>(ws + up256((size_t)a.Hk * 2 * kNV * kD * 4));
+    float* part_l = part_m + up256(rows * 4) / 4;
+    float* part_o = part_l + up256(rows * 4) / 4;
+
+    DecodeCacheWrite w{};
+    int64_t cw_vec = 0;
+    if (cw && cw->hi > cw->lo) {
+        w = *cw;
+        cw_vec = (cw->hi - cw->lo) * (int64_t)a.Hk * kD / 4;
+    }
+    const int prep_blocks = a.Hk + (int)((2 * cw_vec + 255) / 256);
+    decode_tc_prep<kD><<<prep_blocks, 256, 0, stream>>>(a, qhl, w, cw_vec);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+
+    CUtensorMap tm_k, tm_v, tm_q;
+    if (!encode_blocks(&tm_k, a.k, a.S, (int64_t)a.Hk * kD, kKT) ||
+        !encode_blocks(&tm_v, a.v, a.S, (int64_t)a.Hk * kD, kKT) ||
+        !encode_blocks(&tm_q, qhl, (int64_t)a.Hk * 2 * kNV, kD, kNV))
+        return cudaErrorInvalidValue;
+    DtArgs g;
+    std::memset(&g, 0, sizeof(g));
+    g.a = a;
+    g.part_m = part_m;
+    g.part_l = part_l;
+    g.part_o = part_o;
+    g.nv = (int32_t)(a.T * a.G);
+    g.sink_lim = a.window > 0 ? (int32_t)(a.sinks < a.S ? a.sinks : a.S) : 0;
+    g.splits = tp.splits;
+    g.sink_splits = tp.sink_splits;
+    g.n_sink_tiles = tp.n_sink_tiles;
+    g.n_tiles = tp.n_tiles;
+    g.lo = tp.lo;
+    g.sink_end = tp.sink_end;
+    g.hi = tp.hi;
+    e = set_smem_once(reinterpret_cast<const void*>(decode_tc_kernel), (int)kSmem);
+    if (e != cudaSuccess) return e;
+    decode_tc_kernel<<<dim3(a.Hk, tp.splits), kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, g);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    decode_tc_merge<kD><<<dim3(a.Hk, kNV), kD, 0, stream>>>(a, part_m, part_l, part_o, 2 * tp.splits);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool decode_tc_supported(const AttnDesc& a) {
+    return a.T >= 1 && a.T * a.G <= kNV && a.D == kD && a.Dv == kD && !a.softcap_on &&
+           !a.alibi_on && a.bias_kind == 0 && a.S < ((int64_t)1 << 31) && a.Hk <= 65535;
+}
+
+void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcPlan* tp) {
+    DecodePlan base;
+    decode_plan(a, 0, 1, &base);  // the visible range and the sink range
+    tp->lo = base.s_lo;
+    tp->hi = base.s_end;
+    tp->sink_end = base.sink_end;
+    tp->n_sink_tiles = (int)((base.sink_end + kKT - 1) / kKT);
+    tp->n_tiles = (int)((base.s_end - base.s_lo + kKT - 1) / kKT);
+    const int total = tp->n_sink_tiles + tp->n_tiles;
+    int splits = forced_splits > 0 ? forced_splits : num_sms / (a.Hk > 0 ? a.Hk : 1);
+    if (splits < 1) splits = 1;
+    if (splits > kDecodeTcMaxSplits) splits = kDecodeTcMaxSplits;
+    if (splits > total) splits = total > 0 ? total : 1;
+    // Each range takes whole splits, in proportion to its tiles.
+    int ss = 0;
+    if (tp->n_sink_tiles > 0) {
+        ss = (int)((int64_t)splits * tp->n_sink_tiles / total);
+        if (ss < 1) ss = 1;
+        if (splits - ss < 1 && tp->n_tiles > 0) splits = ss + 1;
+    }
+    if (tp->n_tiles == 0) splits = ss;
+    if (splits < 1) splits = 1;
+    tp->sink_splits = ss;
+    tp->splits = splits;
+    const size_t rows = (size_t)a.Hk * kNV * 2 * splits;
+    tp->workspace_bytes = kWorkspaceHeader + up256((size_t)a.Hk * 2 * kNV * a.D * 4) + 2 * up256(rows * 4) +
+                          up256(rows * (size_t)a.D * 4);
+}
+
+cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
+                             const DecodeCacheWrite* cw) {
+    return launch_d(a, tp, workspace, stream, cw);
+}
+
+unsigned int decode_tc_take_device_error() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_decode_tc_device_error, sizeof(v)) != cudaSuccess) return 0;
+    if (v) {
+        const unsigned int zero = 0;
+        cudaMemcpyToSymbol(g_decode_tc_device_error, &zero, sizeof(zero));
+    }
+    return v;
+}
+
+}  // namespace vtmu

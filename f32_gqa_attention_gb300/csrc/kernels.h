@@ -57,6 +57,29 @@ cudaError_t launch_decode(const AttnDesc& a, const AlibiTable& alibi, const Deco
 // Reads and clears the decode kernel's device error flag (synchronous).
 unsigned int decode_take_device_error();
 
+// ---- decode of a few query rows, scores on the tensor cores ------------------
+// Up to 16 virtual heads (query rows x group heads) per KV head.
+constexpr int kDecodeTcHeads = 16;
+constexpr int kDecodeTcMaxSplits = 256;
+struct DecodeTcPlan {
+    int64_t lo = 0, hi = 0;  // the visible range [lo, hi)
+    int64_t sink_end = 0;    // attention sinks: rows [0, sink_end) as a range of their own
+    int32_t n_sink_tiles = 0, n_tiles = 0;  // 128-row tiles of the two ranges
+    int32_t splits = 1, sink_splits = 0;    // per KV head
+    size_t workspace_bytes = 0;
+};
+// True when the kernel covers the call: T * group size <= 16, headDim ==
+// vHeadDim == 128, no softcap, ALiBi or bias.  16-byte aligned q, k, v, out
+// are checked at launch.
+bool decode_tc_supported(const AttnDesc& a);
+// `forced_splits` > 0 overrides the split count (at most one split per tile).
+void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcPlan* tp);
+// Launches the query split (with the cache write `cw`, whose pointers must be
+// 16-byte aligned, when given), the attention and the split merge.
+cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
+                             const DecodeCacheWrite* cw);
+unsigned int decode_tc_take_device_error();
+
 // ---- tiled prefill on FP32 FMA ----------------------------------------------
 bool prefill_ffma_supported(const AttnDesc& a);
 cudaError_t launch_prefill_ffma(const AttnDesc& a, const AlibiTable& alibi, cudaStream_t stream);

@@ -97,6 +97,19 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // Shared-memory matrix descriptor of a K-major tile stored with the 128-byte
 // swizzle (rows of 32 f32 = 128 B, 8-row atoms of 1024 B, the layout a TMA
 // load with CU_TENSOR_MAP_SWIZZLE_128B and a 32-float box produces).  The
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::
+            "r"(taddr),
+        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+        "r"(__float_as_uint(v[15]))
+        : "memory");
+}
+
 // tile must start on a 1024-byte boundary; a K offset of k elements inside
 // the 128-byte row is added to the start address (k * 4 bytes).
 __device__ __forceinline__ uint64_t smem_desc_sw128(const void* tile) {

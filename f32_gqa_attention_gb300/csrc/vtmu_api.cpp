@@ -135,7 +135,7 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
     if (p->alibi != VTMU_ALIBI_NONE && p->heads > vtmu::kMaxAlibiHeads)
         return fail(VTMU_ERR_UNSUPPORTED, "attention.alibi with heads %d > %d is not supported", p->heads,
                     vtmu::kMaxAlibiHeads);
-    if (p->kernel < VTMU_KERNEL_AUTO || p->kernel > VTMU_KERNEL_PREFILL_TF32X3)
+    if (p->kernel < VTMU_KERNEL_AUTO || p->kernel > VTMU_KERNEL_DECODE_TF32X3)
         return fail(VTMU_ERR_INVALID, "kernel %d is not a vtmu_kernel", p->kernel);
     if (p->decode_splits < 0) return fail(VTMU_ERR_INVALID, "decode_splits must be >= 0");
     if (p->heads > 65535 || Hk > 65535) return fail(VTMU_ERR_UNSUPPORTED, "more than 65535 heads");
@@ -166,7 +166,9 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
 
     int kernel = p->kernel;
     if (kernel == VTMU_KERNEL_AUTO) {
-        if (a.T <= kDecodeAutoRows && vtmu::decode_supported(a))
+        if (a.T >= 2 && vtmu::decode_tc_supported(a))
+            kernel = VTMU_KERNEL_DECODE_TF32X3;
+        else if (a.T <= kDecodeAutoRows && vtmu::decode_supported(a))
             kernel = VTMU_KERNEL_DECODE;
         else if (a.T >= kTcMinRows && vtmu::prefill_tc_supported(a))
             kernel = VTMU_KERNEL_PREFILL_TF32X3;
@@ -181,6 +183,12 @@ vtmu_status resolve(const vtmu_attention_params* p, Resolved* r) {
                         "kernel DECODE covers headDim == vHeadDim in {32,64,128} and group size "
                         "heads/kvHeads in {1,2,4,8} (got headDim %d, vHeadDim %d, group %d)",
                         a.D, a.Dv, a.G);
+    } else if (kernel == VTMU_KERNEL_DECODE_TF32X3) {
+        if (a.T < 1 || !vtmu::decode_tc_supported(a))
+            return fail(VTMU_ERR_UNSUPPORTED,
+                        "kernel DECODE_TF32X3 covers 1 <= T * group size <= 16, headDim == vHeadDim == 128, "
+                        "no softcap, ALiBi or bias (got T %lld, group %d, headDim %d, vHeadDim %d)",
+                        (long long)a.T, a.G, a.D, a.Dv);
     } else if (kernel == VTMU_KERNEL_PREFILL_TF32X3) {
         if (!vtmu::prefill_tc_supported(a))
             return fail(VTMU_ERR_UNSUPPORTED,
@@ -217,8 +225,15 @@ size_t decode_workspace(const vtmu::AttnDesc& a) {
     return plan.workspace_bytes;
 }
 
+size_t decode_tc_workspace(const vtmu::AttnDesc& a) {
+    vtmu::DecodeTcPlan plan;
+    vtmu::decode_tc_plan(a, 0, 1 << 20, &plan);  // upper bound: the most splits
+    return plan.workspace_bytes;
+}
+
 size_t attention_workspace(const Resolved& r) {
-    return r.kernel == VTMU_KERNEL_DECODE         ? decode_workspace(r.a)
+    return r.kernel == VTMU_KERNEL_DECODE_TF32X3  ? decode_tc_workspace(r.a)
+           : r.kernel == VTMU_KERNEL_DECODE         ? decode_workspace(r.a)
            : r.kernel == VTMU_KERNEL_PREFILL_TF32X3 ? vtmu::prefill_tc_workspace(r.a)
                                                     : 0;
 }
@@ -442,6 +457,42 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
     vtmu::AlibiTable alibi;
     fill_alibi(p, &alibi);
 
+    if (r.kernel == VTMU_KERNEL_DECODE_TF32X3) {
+        const uintptr_t m16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
+                              reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
+        if (m16 & 15u) {
+            if (p->kernel == VTMU_KERNEL_DECODE_TF32X3)
+                return fail(VTMU_ERR_UNSUPPORTED, "kernel DECODE_TF32X3 needs 16-byte aligned q, k, v, out");
+            r.kernel = vtmu::decode_supported(a) && a.T <= kDecodeAutoRows ? VTMU_KERNEL_DECODE
+                                                                            : VTMU_KERNEL_PREFILL_FFMA;
+        }
+    }
+    if (r.kernel == VTMU_KERNEL_DECODE_TF32X3) {
+        const size_t need = decode_tc_workspace(a);
+        if (!workspace || workspace_bytes < need)
+            return fail(VTMU_ERR_WORKSPACE, "tensor-core decode needs a workspace of %zu bytes (got %zu)", need,
+                        workspace ? workspace_bytes : (size_t)0);
+        if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+            return fail(VTMU_ERR_WORKSPACE, "workspace must be 256-byte aligned");
+        // The new rows go in with the query split when every pointer allows
+        // float4 copies, else by the cache_write kernel first.
+        const vtmu::DecodeCacheWrite* fused = nullptr;
+        if (cw) {
+            const uintptr_t c16 = reinterpret_cast<uintptr_t>(cw->kc) | reinterpret_cast<uintptr_t>(cw->vc) |
+                                  reinterpret_cast<uintptr_t>(cw->k_new) | reinterpret_cast<uintptr_t>(cw->v_new);
+            if (c16 & 15u) {
+                e = write_caches();
+                if (e != cudaSuccess) return cuda_fail(e, "cache_write launch");
+            } else {
+                fused = cw;
+            }
+        }
+        vtmu::DecodeTcPlan plan;
+        vtmu::decode_tc_plan(a, p->decode_splits, device_sm_count(), &plan);
+        e = vtmu::launch_decode_tc(a, plan, workspace, stream, fused);
+        if (e != cudaSuccess) return cuda_fail(e, "tensor-core decode launch");
+        return ok();
+    }
     if (r.kernel == VTMU_KERNEL_DECODE) {
         const uintptr_t m16 = reinterpret_cast<uintptr_t>(q) | reinterpret_cast<uintptr_t>(k) |
                               reinterpret_cast<uintptr_t>(v) | reinterpret_cast<uintptr_t>(out);
@@ -794,7 +845,8 @@ vtmu_status vtmu_device_error(unsigned int* flags) {
     *flags = 0;
     cudaError_t e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return cuda_fail(e, "device_error: synchronize");
-    *flags = vtmu::decode_take_device_error() | vtmu::tc_take_device_error() | vtmu::mla_take_device_error() |
+    *flags = vtmu::decode_take_device_error() | vtmu::decode_tc_take_device_error() | vtmu::tc_take_device_error() |
+             vtmu::mla_take_device_error() |
              vtmu::mla_tc_take_device_error();
     return ok();
 }

@@ -82,7 +82,10 @@ typedef enum vtmu_bias_kind {
     VTMU_BIAS_HTS = 2  /* bias [heads, T, S] */
 } vtmu_bias_kind;
 
-/* Kernel choice.  AUTO takes the split-KV decode kernel for 1 <= T <= 8
+/* Kernel choice.  AUTO takes the tensor-core decode kernel for T >= 2 when
+ * it covers the call (T * group size <= 16, headDim == vHeadDim == 128,
+ * no softcap, ALiBi or bias; 16-byte aligned q, k, v, out), else the split-KV
+ * decode kernel for 1 <= T <= 8
  * (when its shape table covers headDim/vHeadDim/group size), the tcgen05 3xTF32
  * prefill for T >= 64 when it covers the shape (headDim == vHeadDim in
  * {32, 64, 96, 128, 256}, or headDim 192 with vHeadDim 128; 16-byte aligned q
@@ -92,7 +95,10 @@ typedef enum vtmu_kernel {
     VTMU_KERNEL_AUTO = 0,
     VTMU_KERNEL_DECODE = 1,        /* 1 <= T <= 16: T query rows against a cache */
     VTMU_KERNEL_PREFILL_FFMA = 2,  /* tiled online-softmax kernel on FP32 FMA */
-    VTMU_KERNEL_PREFILL_TF32X3 = 3 /* tcgen05 3xTF32 tensor-core prefill */
+    VTMU_KERNEL_PREFILL_TF32X3 = 3, /* tcgen05 3xTF32 tensor-core prefill */
+    VTMU_KERNEL_DECODE_TF32X3 = 4   /* T query rows against a cache, T * group
+                                       size <= 16, headDim 128: scores and
+                                       P.V on the tensor cores (3xTF32) */
 } vtmu_kernel;
 
 /*
@@ -120,7 +126,7 @@ typedef struct vtmu_attention_params {
     const float* alibi_slopes; /* HOST [heads], for VTMU_ALIBI_SLOPES */
     int32_t bias_kind;    /* vtmu_bias_kind; bias pointer must agree */
     int32_t kernel;       /* vtmu_kernel */
-    int32_t decode_splits; /* decode kernel: KV splits per KV head, 0 = auto */
+    int32_t decode_splits; /* decode kernels: KV splits per KV head, 0 = auto */
     int64_t sinks;        /* attention sinks (the IR page's op_attention.sinks, not a
                              param of the op page): with a window, keys s < sinks
                              stay visible (causality still applies); 0 = none */
@@ -445,7 +451,10 @@ VTMU_API vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const 
  * 0x4000 P.V product; latent attention bits: 0x10000 stage load, 0x20000
  * free stage, 0x40000 drain (CUDA-core kernel), 0x100000 ring item,
  * 0x200000 free slot, 0x400000 split item, 0x800000 score tile, 0x1000000
- * free score buffer, 0x2000000 drain (tensor-core kernel).  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
+ * free score buffer, 0x2000000 drain (tensor-core kernel); tensor-core
+ * decode bits: 0x4000000 ring item or query tiles, 0x8000000 free slot,
+ * 0x10000000 split item, 0x20000000 score tile, 0x40000000 free score
+ * buffer, 0x80000000 drain.  Errors: VTMU_ERR_INVALID (NULL flags), VTMU_ERR_CUDA.
  */
 VTMU_API vtmu_status vtmu_device_error(unsigned int* flags);
 

@@ -118,6 +118,29 @@ def test_decode_shape_outside_its_table_is_refused(lib):
 
 
 @host_only
+@pytest.mark.parametrize("kw", [
+    dict(T=4, heads=32, kvHeads=4, headDim=128),             # group 8 x 4 rows: 32 virtual heads
+    dict(T=2, heads=4, kvHeads=2, headDim=96),               # headDim other than 128
+    dict(T=2, heads=4, kvHeads=2, headDim=64),
+    dict(T=2, heads=4, kvHeads=2, headDim=128, softcap=30.0),
+    dict(T=2, heads=4, kvHeads=2, headDim=128, alibi=True),
+    dict(T=2, heads=4, kvHeads=2, headDim=128, vHeadDim=64),
+])
+def test_tensor_core_decode_outside_its_shapes_is_refused(lib, kw):
+    kw = dict(kw)
+    p = vtmu.make_params(kw.pop("T"), 300, kernel=vtmu.VTMU_KERNEL_DECODE_TF32X3, **kw)
+    e = _err(lambda: vtmu.vtmu_attention_workspace_size(p))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "DECODE_TF32X3" in str(e)
+
+
+@host_only
+def test_unknown_kernel_is_refused(lib):
+    p = vtmu.make_params(2, 300, heads=4, headDim=64, kernel=vtmu.VTMU_KERNEL_DECODE_TF32X3 + 1)
+    e = _err(lambda: vtmu.vtmu_attention_workspace_size(p))
+    assert e.status == vtmu.VTMU_ERR_INVALID and "vtmu_kernel" in str(e)
+
+
+@host_only
 def test_null_and_aliasing_pointers_are_refused(lib):
     p = vtmu.make_params(4, 4, heads=2, headDim=8)
     assert _err(lambda: vtmu.vtmu_attention(None, FAKE, FAKE, None, FAKE * 2, p, None, 0, 0)).status == \
