@@ -568,17 +568,17 @@ def finish_prefill(ctx, res):
 
 
 def decode_launches(w, args):
-    """Kernels one decode step launches: the fused decode kernel (1), the
-    tensor-core decode of several query rows (query split with the cache
-    write, attention, split merge: 3) or, forced, cache writes plus the FFMA
-    prefill (3)."""
+    """(path, kernels launched per step) of a decode step: the CUDA-core
+    decode kernel or the tensor-core decode of several query rows (each one
+    launch with the cache write and the split merge inside), or, forced,
+    cache writes plus the FFMA prefill (3)."""
     if args.kernel == "ffma":
-        return 3
+        return ("prefill", 3)
     R, G = w.get("rows", 1), w["heads"] // w["kvHeads"]
     p = w["params"]
     tc = (R >= 2 and R * G <= 16 and w["headDim"] == 128 and not p.get("softcap") and not p.get("alibi")
           and not w.get("rope"))
-    return 3 if tc else 1
+    return ("tc", 1) if tc else ("ffma", 1)
 
 
 def measure_decode(ctx, name):
@@ -691,10 +691,10 @@ def measure_decode(ctx, name):
     del sessions, q, kn, vn, out, ws
     torch.cuda.empty_cache()
     kernel_tag = ("prefill_ffma" if args.kernel == "ffma" else
-                  "decode_tc" if decode_launches(w, args) == 3 else "decode")
+                  "decode_tc" if decode_launches(w, args)[0] == "tc" else "decode")
     return {"workload": name, "x": x, "w": w, "step_bytes": step_bytes, "step_ms": step_ms, "kernel_ms": kern_ms,
             "unfused_ms": unfused_ms, "e2e": e2e, "kernel_tag": kernel_tag,
-            "launches_per_step": decode_launches(w, args), "_window": window}
+            "launches_per_step": decode_launches(w, args)[1], "_window": window}
 
 
 def measure_mla(ctx, name):

@@ -19,25 +19,27 @@
 // Each K and V byte of the visible range is read from HBM once for all T
 // rows.
 //
-// Three launches:
-//  1. decode_tc_prep: the step's new cache rows written (when the call is a
-//     decode step), and the scaled query split into Q_hi (tf32, rounded to
-//     nearest) and Q_lo = q - Q_hi, laid out [kv head][hi|lo][16][128] with
-//     zero rows for virtual heads past T G;
-//  2. decode_tc_kernel, grid (kv heads, splits); one CTA streams a run of
+// One launch, decode_tc_kernel, grid (kv heads, splits):
+//  1. one CTA streams a run of
 //     128-row tiles of its KV head's range (the attention sinks' tiles
-//     first, as splits of their own).  Warps:
-//       0      lane 0: the query tiles once, then the score ring (K blocks of
-//              [128 rows x 32 dims] by TMA, 128-byte swizzle);
+//     first, as splits of their own).  In a decode step, the CTA whose
+//     tile shows a new cache row writes that row (its KV head's columns)
+//     before its first TMA read; rows no tile shows go to split 0.  Warps:
+//       0      the new K rows, then lane 0 streams the score ring (K blocks
+//              of [128 rows x 32 dims] by TMA, 128-byte swizzle);
 //       1      lane 0 issues the score MMAs into S buffer (tile & 1); warp 1
 //              owns TMEM (S 2 x 16 columns, O 2 x 16, V^T hi and lo 128
 //              each);
-//       2      lane 0: the value ring (V blocks of [128 rows x 32 dims]);
+//       2      the new V rows, then lane 0 streams the value ring (V blocks
+//              of [128 rows x 32 dims]);
 //       3      lane 0 issues the P.V MMAs of a tile into O buffer (tile & 1)
 //              once its P^T and V^T are in place;
 //       4 .. 7 split each K block in place into K_hi (low 13 mantissa bits
 //              cleared) and K_lo = K - K_hi beside it;
-//       8 .. 15 two softmax groups: warps 8 .. 11 take the even tiles of
+//       8 .. 15 first the query tiles: q scaled by scale log2 e, split into
+//              Q_hi (tf32, rounded to nearest) and Q_lo = q - Q_hi in the
+//              K-major blocks the score MMA reads (zero rows past T G); then
+//              two softmax groups: warps 8 .. 11 take the even tiles of
 //              the run, 12 .. 15 the odd ones, so two tiles are in flight;
 //              each group has its own S buffer, P^T buffer and O buffer and
 //              its own running (m, l, o).  Thread = a row of the tile, all 16
@@ -45,15 +47,18 @@
 //              rows (a reduce-scatter over the warp, then the group's four
 //              warps through shared memory), online softmax in base 2 with
 //              a lazy reference max (rescale only when a max grows by more
-//              than 2^8), P^T hi and lo to shared memory; then warp q of
-//              the group moves the tile's V block q (dims 32 q ..) into TMEM
-//              lanes 32 q .. as V^T hi and lo (once the previous tile's P.V
-//              MMAs are done with V^T), and the group folds its previous
-//              tile's O into registers, o = o alpha + O (a fresh accumulator
-//              per tile, so no sum runs long inside the tensor pipe);
-//     and writes (m, l, o) per virtual head and group of its split;
-//  3. decode_tc_merge: per (KV head, virtual head) the log-sum-exp merge of
-//     the (split, group) partials, m* = max m_i, l* = sum l_i 2^(m_i - m*),
+//              than 2^8), P^T hi and lo to shared memory; then the group
+//              folds its previous tile's O into registers, o = o alpha + O
+//              (a fresh accumulator per tile, so no sum runs long inside the
+//              tensor pipe), and warp q of the group moves the next tile's V
+//              block q (dims 32 q ..) into TMEM lanes 32 q .. as V^T hi and
+//              lo once this tile's P.V MMAs are done with V^T (group 1 moves
+//              the first tile's at the start);
+//     then the two groups' (m, l, o) are combined (rescaled to the larger
+//     reference) and written as the split's partial;
+//  2. the last CTA of a KV head to finish (an arrival counter in the
+//     workspace header, no waiting) merges, per virtual head, the splits'
+//     partials by the log-sum-exp rule, m* = max m_i, l* = sum l_i 2^(m_i - m*),
 //     o* = sum o_i 2^(m_i - m*) / l*, written to the output row (zeros when
 //     no key is visible).
 // Every ring item is waited for and released by every role that reads it,
@@ -113,11 +118,13 @@ enum : unsigned int {
 
 struct DtArgs {
     AttnDesc a;        // S, T, H, G, causal, pos_offset, window, sinks (visibility)
-    float* part_m;     // [Hk][16][splits]
+    float* part_m;     // [Hk][16][splits] (both softmax groups combined)
     float* part_l;
     float* part_o;     // [Hk][16][splits][D]
+    unsigned int* counters;  // [Hk] arrival counters (workspace header), zero between calls
     int32_t nv;        // virtual heads in use: T * G
     int32_t sink_lim;  // with a window: rows below this are attention sinks (0: none)
+    DecodeCacheWrite cw;  // the step's new rows (cw.hi == cw.lo: none); 16-byte aligned
     int32_t splits;
     int32_t sink_splits;
     int32_t n_sink_tiles, n_tiles;  // tiles of the sink range and of the main range
@@ -147,6 +154,18 @@ __device__ __forceinline__ void tile_rows(const DtArgs& g, int t, int64_t& r0, i
     }
 }
 
+// Barrier over the eight softmax warps (named barrier 3, 256 threads);
+// returns the AND of `v` over them.
+__device__ __forceinline__ bool softmax_sync_and(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred p, 3, 256, q;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)v)
+        : "memory");
+    return r != 0;
+}
+
 // Barrier over one softmax group's four warps (named barrier ID, 128
 // threads); returns the AND of `v` over them.
 template <int ID>
@@ -160,42 +179,119 @@ __device__ __forceinline__ bool group_sync_and(bool v) {
     return r != 0;
 }
 
-// ---- 1: new cache rows, query split ----------------------------------------
-// Blocks [0, Hk): the query tiles of KV head blockIdx.x.  Blocks after them:
-// the cache write, float4 per thread (K rows, then V rows).
-template <int D>
-__global__ void __launch_bounds__(256) decode_tc_prep(AttnDesc a, float* qhl, DecodeCacheWrite cw, int64_t cw_vec) {
-    if ((int)blockIdx.x < a.Hk) {
-        const int hk = blockIdx.x;
-        const int nv = (int)a.T * a.G;
-        for (int i = threadIdx.x; i < kNV * D; i += blockDim.x) {
-            const int v = i / D, d = i % D;
-            float x = 0.f;
-            if (v < nv) {
-                const int t = v / a.G, h = hk * a.G + v % a.G;
-                x = a.q[((int64_t)t * a.H + h) * D + d] * a.qk_mul;
-            }
-            const float hi = tf32_rna(x);
-            qhl[((size_t)(hk * 2 + 0) * kNV + v) * D + d] = hi;
-            qhl[((size_t)(hk * 2 + 1) * kNV + v) * D + d] = x - hi;
+// True when new cache row r belongs to this CTA: a row of one of its tiles'
+// visible ranges, or, for a row that no tile shows, split 0.
+__device__ __forceinline__ bool owns_row(const DtArgs& g, int split, int t0, int t1, int64_t r) {
+    int64_t ti = -1;
+    if (r < g.sink_end)
+        ti = r / kKT;
+    else if (r >= g.lo && r < g.hi)
+        ti = g.n_sink_tiles + (r - g.lo) / kKT;
+    return ti >= 0 ? (ti >= t0 && ti < t1) : split == 0;
+}
+
+// The new cache rows this CTA owns, its KV head's columns (128 floats = 32
+// float4 per row, one per lane), into `cache` before any TMA read of them:
+// each lane's generic writes are fenced against the async proxy.
+__device__ __forceinline__ void write_new_rows(const DtArgs& g, int split, int t0, int t1, int hk, int lane,
+                                               float* cache, const float* rows) {
+    const int64_t width4 = (int64_t)g.a.Hk * (kD / 4);
+    for (int64_t r = g.cw.lo; r < g.cw.hi; ++r)
+        if (owns_row(g, split, t0, t1, r))
+            reinterpret_cast<float4*>(cache)[r * width4 + hk * (kD / 4) + lane] =
+                reinterpret_cast<const float4*>(rows)[(r - g.cw.lo) * width4 + hk * (kD / 4) + lane];
+    asm volatile("fence.proxy.async.global;\n" ::: "memory");
+    __syncwarp();
+}
+
+// The last CTA of a KV head to arrive merges the splits' partials:
+// m* = max m_i, weights 2^(m_i - m*) (kept in shared memory, in the score
+// ring, idle by now), l* = sum l_i 2^(m_i - m*); warp v serves virtual head
+// v; then output (v, d) = sum_i w_i o_i[d] / l*.
+__device__ __noinline__ void merge_splits(const DtArgs& g, unsigned char* smem_raw, float* sinv, int* s_is_last) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, hk = blockIdx.x;
+    if (threadIdx.x == 0) {
+        unsigned ticket;
+        asm volatile("atom.add.acq_rel.gpu.u32 %0, [%1], 1;" : "=r"(ticket) : "l"(&g.counters[hk]) : "memory");
+        *s_is_last = ticket == (unsigned)(g.splits - 1);
+    }
+    __syncthreads();
+    if (!*s_is_last) return;
+    const int nsub = g.splits;
+    float* sw = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // Thread t: virtual head t / 32, dims 4 (t % 32) .. + 3.  Its first 16
+    // partial outputs are loaded before the weights are worked out, so the
+    // two round trips to L2 overlap.
+    static_assert(kNV * kD / 4 == kThreads, "one output quad per thread");
+    constexpr int kCh = 16;
+    const int v = threadIdx.x / (kD / 4), d4 = threadIdx.x % (kD / 4);
+    const float4* po = reinterpret_cast<const float4*>(g.part_o) + ((int64_t)hk * kNV + v) * nsub * (kD / 4) + d4;
+    float4 ov[kCh];
+    auto load_chunk = [&](int i0) {
+#pragma unroll
+        for (int c = 0; c < kCh; ++c)
+            ov[c] = (v < g.nv && i0 + c < nsub) ? __ldcg(po + (int64_t)(i0 + c) * (kD / 4))
+                                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    load_chunk(0);
+    // Warp w, virtual head w: m* = max m_i, weights 2^(m_i - m*) into shared
+    // memory (the score ring, idle by now), l* = sum l_i 2^(m_i - m*).
+    if (warp < g.nv) {
+        const int64_t row = (int64_t)hk * kNV + warp;
+        constexpr int kPer = kDecodeTcMaxSplits / 32;
+        float mv[kPer], lv[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = lane + 32 * k;
+            mv[k] = i < nsub ? __ldcg(g.part_m + row * nsub + i) : -INFINITY;
+            lv[k] = i < nsub ? __ldcg(g.part_l + row * nsub + i) : 0.f;
         }
-        return;
+        float m = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) m = fmaxf(m, mv[k]);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(FULL, m, off));
+        float l = 0.f;
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = lane + 32 * k;
+            const float w = m == -INFINITY ? 0.f : fast_exp2(mv[k] - m);  // 0 for a split that saw nothing
+            if (i < nsub) sw[warp * nsub + i] = w;
+            l = fmaf(lv[k], w, l);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) l += __shfl_xor_sync(FULL, l, off);
+        if (lane == 0) sinv[warp] = l > 0.f ? 1.f / l : 0.f;
     }
-    const int64_t i = (int64_t)(blockIdx.x - a.Hk) * blockDim.x + threadIdx.x;  // float4 index
-    const int64_t width = (int64_t)a.Hk * D / 4;                                   // float4 per row
-    if (i < cw_vec) {
-        const int64_t r = i / width, c = i % width;
-        reinterpret_cast<float4*>(cw.kc)[(cw.lo + r) * width + c] = reinterpret_cast<const float4*>(cw.k_new)[i];
-    } else if (i < 2 * cw_vec) {
-        const int64_t j = i - cw_vec, r = j / width, c = j % width;
-        reinterpret_cast<float4*>(cw.vc)[(cw.lo + r) * width + c] = reinterpret_cast<const float4*>(cw.v_new)[j];
+    __syncthreads();
+    if (v < g.nv) {
+        const float* wv = sw + v * nsub;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i0 = 0;;) {
+#pragma unroll
+            for (int c = 0; c < kCh; ++c) {
+                const float w = i0 + c < nsub ? wv[i0 + c] : 0.f;
+                acc.x = fmaf(w, ov[c].x, acc.x);
+                acc.y = fmaf(w, ov[c].y, acc.y);
+                acc.z = fmaf(w, ov[c].z, acc.z);
+                acc.w = fmaf(w, ov[c].w, acc.w);
+            }
+            i0 += kCh;
+            if (i0 >= nsub) break;
+            load_chunk(i0);
+        }
+        const float si = sinv[v];
+        const int t = v / g.a.G, h = hk * g.a.G + v % g.a.G;
+        reinterpret_cast<float4*>(g.a.out + ((int64_t)t * g.a.H + h) * kD)[d4] =
+            make_float4(acc.x * si, acc.y * si, acc.z * si, acc.w * si);
     }
+    if (threadIdx.x == 0) g.counters[hk] = 0u;  // ready for the next call
 }
 
 // ---- 2: the split-KV attention ----------------------------------------------
 __global__ void __launch_bounds__(kThreads, 1)
     decode_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                     const __grid_constant__ CUtensorMap tm_q, const DtArgs g) {
+                     const DtArgs g) {
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                            ~uintptr_t(1023));
@@ -209,6 +305,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     __shared__ __align__(16) float red_max[2][4][kNV], red_sum[2][4][kNV];  // [group][warp][head]
     __shared__ __align__(16) float alpha_s[2][2][kNV];  // [group][its tile parity][head]
     __shared__ __align__(16) int32_t vis_lo[kNV], vis_hi[kNV], vis_shi[kNV];  // per virtual head
+    __shared__ float sinv[kNV];  // merge: 1 / l* per virtual head
+    __shared__ int s_is_last;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int hk = blockIdx.x, split = blockIdx.y;
@@ -236,31 +334,32 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&o_full[b], 1);
             mbar_init(&o_free[b], 4);
         }
-        mbar_init(&q_full, 1);
+        mbar_init(&q_full, 8);  // the softmax warps, once the query tiles are in place
         mbar_init(&vt_full, 4);
         mbar_init(&vt_free, 1);
         fence_barrier_init();
+    }
+    if (threadIdx.x < kNV) {
         // Visible keys of virtual head v (query row v / G): the window's
-        // range [lo, hi] and the sinks below vis_shi + 1 (int32: S < 2^31).
+        // range [lo, hi] and the sinks up to vis_shi (int32: S < 2^31).
         const AttnDesc& a = g.a;
-        for (int v = 0; v < kNV; ++v) {
-            int64_t lo = a.S, hi = -1, shi = -1;
-            if (v < g.nv) {
-                const int64_t pos = a.pos_offset + v / a.G;
-                hi = a.causal ? pos : (a.window > 0 ? pos + a.window : a.S - 1);
-                lo = a.window > 0 ? (a.causal ? pos - a.window + 1 : pos - a.window) : 0;
-                shi = a.causal ? pos : a.S - 1;
-                if (hi > a.S - 1) hi = a.S - 1;
-                if (shi > a.S - 1) shi = a.S - 1;
-                if (lo < 0) lo = 0;
-                if (lo > a.S) lo = a.S;
-                if (hi < -1) hi = -1;
-                if (shi < -1) shi = -1;
-            }
-            vis_lo[v] = (int32_t)lo;
-            vis_hi[v] = (int32_t)hi;
-            vis_shi[v] = (int32_t)shi;
+        const int v = threadIdx.x;
+        int64_t lo = a.S, hi = -1, shi = -1;
+        if (v < g.nv) {
+            const int64_t pos = a.pos_offset + v / a.G;
+            hi = a.causal ? pos : (a.window > 0 ? pos + a.window : a.S - 1);
+            lo = a.window > 0 ? (a.causal ? pos - a.window + 1 : pos - a.window) : 0;
+            shi = a.causal ? pos : a.S - 1;
+            if (hi > a.S - 1) hi = a.S - 1;
+            if (shi > a.S - 1) shi = a.S - 1;
+            if (lo < 0) lo = 0;
+            if (lo > a.S) lo = a.S;
+            if (hi < -1) hi = -1;
+            if (shi < -1) shi = -1;
         }
+        vis_lo[v] = (int32_t)lo;
+        vis_hi[v] = (int32_t)hi;
+        vis_shi[v] = (int32_t)shi;
     }
     if (warp == 1) tmem_alloc(&tmem_base_s, kTmemCols);
     tc_fence_before();
@@ -269,7 +368,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = tmem_base_s;
 
     if (warp == 0 || warp == 2) {
-        // ---- producers: warp 0 the query tiles and the score ring, warp 2 the value ring ----
+        // ---- producers: warp 0 the score ring, warp 2 the value ring; first
+        // the step's new K (warp 0) or V (warp 2) rows this CTA reads ----
+        if (g.cw.hi > g.cw.lo)
+            write_new_rows(g, split, t0, t1, hk, lane, warp == 0 ? g.cw.kc : g.cw.vc,
+                           warp == 0 ? g.cw.k_new : g.cw.v_new);
         if (lane == 0) {
             const bool scores = warp == 0;
             const CUtensorMap* map = scores ? &tm_k : &tm_v;
@@ -279,14 +382,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t* fullb = scores ? kfull : vfull;
             uint64_t* emptyb = scores ? kempty : vempty;
             prefetch_tensormap(map);
-            if (scores) {
-                prefetch_tensormap(&tm_v);
-                prefetch_tensormap(&tm_q);
-                mbar_arrive_expect_tx(&q_full, kQBytes);
-#pragma unroll 1
-                for (int c = 0; c < 2 * kC; ++c)  // hi chunks (rows 0..15), then lo chunks (rows 16..31)
-                    tma_load_2d(qsm + c * kQChunk, &tm_q, 32 * (c % kC), hk * 2 * kNV + (c / kC) * kNV, &q_full);
-            }
             int it = 0;
             for (; it < nk; ++it) {
                 const int s = it % ns;
@@ -304,8 +399,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = it - ns < 0 ? 0 : it - ns; j < it; ++j)
                 if (!mbar_wait(&fullb[j % ns], (uint32_t)((j / ns) & 1)))
                     raise_device_error(&g_decode_tc_device_error, kErrDtDrain);
-            if (scores && nk == 0 && !mbar_wait(&q_full, 0))  // the query copy, when no MMA waited for it
-                raise_device_error(&g_decode_tc_device_error, kErrDtDrain);
         }
     } else if (warp == 1) {
         // ---- score MMAs: S^T = K_hi.Q_hi + K_hi.Q_lo + K_lo.Q_hi into buffer tl & 1 ----
@@ -410,6 +503,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;           // TMEM lanes 32 quarter .. + 31
         const int key_l = 32 * quarter + lane;  // this thread's row of a tile
         const uint32_t lanes = (uint32_t)(32 * quarter) << 16;
+        // The query tiles: q of virtual head v (row v / G, head hk G + v % G)
+        // scaled by scale log2 e, split into Q_hi (tf32, rounded to nearest)
+        // and Q_lo = q - Q_hi, in the K-major blocks the score MMA reads
+        // (block = dim / 32, head v's row of a block is 128 bytes, 128-byte
+        // swizzle); zero rows past T G.
+        {
+            const int u = threadIdx.x - 8 * 32;  // 0 .. 255
+            constexpr int kPer = kNV * kD / 256;
+            float qv[kPer];  // every load in flight before the first shared store
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int idx = u + 256 * k, v = idx / kD, dd = idx % kD;
+                qv[k] = v < g.nv ? __ldg(g.a.q + ((int64_t)(v / g.a.G) * g.a.H + hk * g.a.G + v % g.a.G) * kD + dd)
+                                 : 0.f;
+            }
+#pragma unroll
+            for (int k = 0; k < kPer; ++k) {
+                const int idx = u + 256 * k, v = idx / kD, dd = idx % kD;
+                const float xq = qv[k] * g.a.qk_mul;
+                const float qh = tf32_rna(xq);
+                const int e = dd & 31;
+                const uint32_t off = v * 128 + (((e >> 2) ^ (v & 7)) << 4) + (e & 3) * 4;
+                *reinterpret_cast<float*>(qsm + (dd >> 5) * kQChunk + off) = qh;
+                *reinterpret_cast<float*>(qsm + (kC + (dd >> 5)) * kQChunk + off) = xq - qh;
+            }
+            asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic writes -> MMA
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&q_full);
+        }
         float o[kNV];  // O^T of dim 32 quarter + lane, every head
         float m_ref[kNV];
 #pragma unroll
@@ -422,11 +544,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V^T of tile vl, once the previous tile's P.V MMAs are done with
         // V^T.  Row kk, dim lane of a V block sits at byte kk * 128 +
         // ((lane / 4) ^ (kk % 8)) * 16 + (lane % 4) * 4 (128-byte swizzle).
-        // Slot q holds block q of every tile, and the two groups take turns:
-        // the wait for the previous tile's P.V comes first, because it also
-        // means the other group has taken block q of tile vl - 1 out of the
-        // slot, so the slot's barrier is at most one phase behind tile vl and
-        // its parity names that tile alone.
+        // Slot q holds block q of every tile, and the groups take turns (the
+        // group of tile t moves tile t + 1): the wait for the previous tile's
+        // P.V comes first, because it also means the other group has taken
+        // block q of tile vl - 1 out of the slot, so the slot's barrier is at
+        // most one phase behind tile vl and its parity names that tile alone.
         auto move_v = [&](int vl) -> bool {
             const int vs = (vl * kC + quarter) % kNVR;  // one block per slot and tile
             const bool vok = (vl == 0 || __all_sync(FULL, mbar_wait(&vt_free, (uint32_t)((vl - 1) & 1)))) &&
@@ -508,6 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             return grp == 0 ? group_sync_and<1>(v) : group_sync_and<2>(v);
         };
         int j = 0;  // the group's tile count
+        // Group 1 moves the first tile's V while group 0 takes its scores.
+        if (grp == 1 && ntile > 0 && !move_v(0)) ok = false;
         for (int tl = grp; tl < ntile; tl += 2, ++j) {
             // A wait that gives up marks the warp; every warp of the group still
             // reaches the barriers below, which AND the marks, so the group
@@ -607,26 +731,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                              red_sum[grp][0][lane] + red_sum[grp][1][lane] + red_sum[grp][2][lane] +
                                  red_sum[grp][3][lane]);
             // A failed wait leaves the warp's mark for the next barrier.
-            if (!move_v(tl)) ok = false;
             if (ok && j > 0 && !fold(j - 1)) ok = false;
+            // The next tile's V: its P.V follows this tile's, which is issued
+            // by now (this group's P^T and the other group's V^T are in).
+            if (ok && tl + 1 < ntile && !move_v(tl + 1)) ok = false;
         }
         if (ok && j > 0 && !fold(j - 1)) ok = false;
-        ok = group_sync(ok);
-        if (ok) {
-            const int sub = 2 * split + grp;  // the group's partial sums count as a split of their own
-            const int nsub = 2 * g.splits;
+        // The two groups' partial sums into one: group 1 leaves (m, l, o) in
+        // the idle value ring, group 0 rescales both to the larger reference
+        // and writes the CTA's partial.  (Every V block has been moved and
+        // every P.V product is done once the groups have folded their last
+        // tiles.)
+        float* xm = reinterpret_cast<float*>(vring);  // [16] m, [16] l, then [16][128] o
+        if (grp == 1) {
             if (quarter == 0 && lane < kNV) {
                 float mm = m_ref[0];
 #pragma unroll
                 for (int h = 1; h < kNV; ++h)
                     if (lane == h) mm = m_ref[h];
-                const int64_t idx = ((int64_t)hk * kNV + lane) * nsub + sub;
-                g.part_m[idx] = j > 0 ? mm : -INFINITY;
-                g.part_l[idx] = j > 0 ? l_run : 0.f;
+                xm[lane] = j > 0 ? mm : -INFINITY;
+                xm[kNV + lane] = j > 0 ? l_run : 0.f;
             }
 #pragma unroll
-            for (int h = 0; h < kNV; ++h)
-                g.part_o[(((int64_t)hk * kNV + h) * nsub + sub) * kD + 32 * quarter + lane] = o[h];
+            for (int h = 0; h < kNV; ++h) xm[2 * kNV + h * kD + 32 * quarter + lane] = o[h];
+        }
+        ok = softmax_sync_and(ok);
+        if (grp == 0 && ok) {
+            const int64_t rows = (int64_t)hk * kNV;
+#pragma unroll
+            for (int h = 0; h < kNV; ++h) {
+                const float m0 = j > 0 ? m_ref[h] : -INFINITY, m1 = xm[h];
+                const float mx = fmaxf(m0, m1);
+                const float a0 = mx == -INFINITY ? 0.f : fast_exp2(m0 - mx);  // 0 for a group that saw nothing
+                const float a1 = mx == -INFINITY ? 0.f : fast_exp2(m1 - mx);
+                g.part_o[((rows + h) * g.splits + split) * kD + 32 * quarter + lane] =
+                    o[h] * a0 + xm[2 * kNV + h * kD + 32 * quarter + lane] * a1;
+                if (quarter == 0 && lane == h) {
+                    g.part_m[(rows + h) * g.splits + split] = mx;
+                    g.part_l[(rows + h) * g.splits + split] = l_run * a0 + xm[kNV + h] * a1;
+                }
+            }
         }
     }
 
@@ -637,31 +781,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, kTmemCols);
     }
+
+    // ---- the last CTA of this KV head merges the splits' partials ----
+    // (Indices are taken afresh here so that nothing stays live across the
+    // roles above.)  The barrier above orders every thread's partial stores
+    // before thread 0's ticket, an acquire-release atomic at gpu scope: it
+    // publishes this CTA's partials and, for the last CTA, acquires the
+    // others'.
+    merge_splits(g, smem_raw, sinv, &s_is_last);
 }
 
-// ---- 3: merge of the splits --------------------------------------------------
-// Block (hk, v): one virtual head, D threads (one dim each).
-template <int D>
-__global__ void __launch_bounds__(D) decode_tc_merge(AttnDesc a, const float* part_m, const float* part_l,
-                                                     const float* part_o, int splits) {
-    const int hk = blockIdx.x, v = blockIdx.y, d = threadIdx.x;
-    if (v >= (int)a.T * a.G) return;
-    const int64_t row = (int64_t)hk * kNV + v;
-    const float* pm = part_m + row * splits;
-    const float* pl = part_l + row * splits;
-    float m = -INFINITY;
-    for (int i = 0; i < splits; ++i) m = fmaxf(m, pm[i]);
-    float l = 0.f, acc = 0.f;
-    if (m != -INFINITY) {
-        for (int i = 0; i < splits; ++i) {
-            const float w = fast_exp2(pm[i] - m);  // 0 for a split that saw nothing
-            l = fmaf(pl[i], w, l);
-            acc = fmaf(part_o[(row * splits + i) * D + d], w, acc);
-        }
-    }
-    const int t = v / a.G, h = hk * a.G + v % a.G;
-    a.out[((int64_t)t * a.H + h) * D + d] = l > 0.f ? acc / l : 0.f;
-}
 
 PFN_cuTensorMapEncodeTiled_v12000 dt_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -697,27 +826,14 @@ size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
                      const DecodeCacheWrite* cw) {
     unsigned char* ws = static_cast<unsigned char*>(workspace) + kWorkspaceHeader;
-    float* qhl = reinterpret_cast<float*>(ws);
-    const size_t rows = (size_t)a.Hk * kNV * 2 * tp.splits;  // two softmax groups per split
-    float* part_m = reinterpret_cast<float*>(ws + up256((size_t)a.Hk * 2 * kNV * kD * 4));
+    const size_t rows = (size_t)a.Hk * kNV * tp.splits;
+    float* part_m = reinterpret_cast<float*>(ws);
     float* part_l = part_m + up256(rows * 4) / 4;
     float* part_o = part_l + up256(rows * 4) / 4;
 
-    DecodeCacheWrite w{};
-    int64_t cw_vec = 0;
-    if (cw && cw->hi > cw->lo) {
-        w = *cw;
-        cw_vec = (cw->hi - cw->lo) * (int64_t)a.Hk * kD / 4;
-    }
-    const int prep_blocks = a.Hk + (int)((2 * cw_vec + 255) / 256);
-    decode_tc_prep<kD><<<prep_blocks, 256, 0, stream>>>(a, qhl, w, cw_vec);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-
-    CUtensorMap tm_k, tm_v, tm_q;
+    CUtensorMap tm_k, tm_v;
     if (!encode_blocks(&tm_k, a.k, a.S, (int64_t)a.Hk * kD, kKT) ||
-        !encode_blocks(&tm_v, a.v, a.S, (int64_t)a.Hk * kD, kKT) ||
-        !encode_blocks(&tm_q, qhl, (int64_t)a.Hk * 2 * kNV, kD, kNV))
+        !encode_blocks(&tm_v, a.v, a.S, (int64_t)a.Hk * kD, kKT))
         return cudaErrorInvalidValue;
     DtArgs g;
     std::memset(&g, 0, sizeof(g));
@@ -725,8 +841,10 @@ cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace,
     g.part_m = part_m;
     g.part_l = part_l;
     g.part_o = part_o;
+    g.counters = static_cast<unsigned int*>(workspace);  // the workspace header
     g.nv = (int32_t)(a.T * a.G);
     g.sink_lim = a.window > 0 ? (int32_t)(a.sinks < a.S ? a.sinks : a.S) : 0;
+    if (cw && cw->hi > cw->lo) g.cw = *cw;
     g.splits = tp.splits;
     g.sink_splits = tp.sink_splits;
     g.n_sink_tiles = tp.n_sink_tiles;
@@ -734,12 +852,9 @@ cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace,
     g.lo = tp.lo;
     g.sink_end = tp.sink_end;
     g.hi = tp.hi;
-    e = set_smem_once(reinterpret_cast<const void*>(decode_tc_kernel), (int)kSmem);
+    cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_tc_kernel), (int)kSmem);
     if (e != cudaSuccess) return e;
-    decode_tc_kernel<<<dim3(a.Hk, tp.splits), kThreads, kSmem, stream>>>(tm_k, tm_v, tm_q, g);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    decode_tc_merge<kD><<<dim3(a.Hk, kNV), kD, 0, stream>>>(a, part_m, part_l, part_o, 2 * tp.splits);
+    decode_tc_kernel<<<dim3(a.Hk, tp.splits), kThreads, kSmem, stream>>>(tm_k, tm_v, g);
     return cudaGetLastError();
 }
 
@@ -774,9 +889,8 @@ void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcP
     if (splits < 1) splits = 1;
     tp->sink_splits = ss;
     tp->splits = splits;
-    const size_t rows = (size_t)a.Hk * kNV * 2 * splits;
-    tp->workspace_bytes = kWorkspaceHeader + up256((size_t)a.Hk * 2 * kNV * a.D * 4) + 2 * up256(rows * 4) +
-                          up256(rows * (size_t)a.D * 4);
+    const size_t rows = (size_t)a.Hk * kNV * splits;
+    tp->workspace_bytes = kWorkspaceHeader + 2 * up256(rows * 4) + up256(rows * (size_t)a.D * 4);
 }
 
 cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,

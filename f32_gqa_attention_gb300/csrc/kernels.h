@@ -74,8 +74,8 @@ struct DecodeTcPlan {
 bool decode_tc_supported(const AttnDesc& a);
 // `forced_splits` > 0 overrides the split count (at most one split per tile).
 void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcPlan* tp);
-// Launches the query split (with the cache write `cw`, whose pointers must be
-// 16-byte aligned, when given), the attention and the split merge.
+// Launches the attention (which also writes the new rows of `cw` when given;
+// its pointers must be 16-byte aligned) and the split merge.
 cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
                              const DecodeCacheWrite* cw);
 unsigned int decode_tc_take_device_error();
