@@ -28,14 +28,15 @@
 //       0      the new K rows, then lane 0 streams the score ring (K blocks
 //              of [128 rows x 32 dims] by TMA, 128-byte swizzle);
 //       1      lane 0 issues the score MMAs into S buffer (tile & 1); warp 1
-//              owns TMEM (S 2 x 16 columns, O 2 x 16, V^T hi and lo 128
-//              each);
+//              owns TMEM (S 2 x 16 columns, O 2 x 16, K_lo 6 x 32, V^T hi
+//              and lo 128 each);
 //       2      the new V rows, then lane 0 streams the value ring (V blocks
 //              of [128 rows x 32 dims]);
 //       3      lane 0 issues the P.V MMAs of a tile into O buffer (tile & 1)
 //              once its P^T and V^T are in place;
 //       4 .. 7 split each K block in place into K_hi (low 13 mantissa bits
-//              cleared) and K_lo = K - K_hi beside it;
+//              cleared) and K_lo = K - K_hi, which goes to TMEM (thread =
+//              row = lane) as the operand A of the K_lo.Q_hi product;
 //       8 .. 15 first the query tiles: q scaled by scale log2 e, split into
 //              Q_hi (tf32, rounded to nearest) and Q_lo = q - Q_hi in the
 //              K-major blocks the score MMA reads (zero rows past T G); then
@@ -89,21 +90,23 @@ constexpr int kNV = kDecodeTcHeads;   // virtual heads per KV head (MMA N)
 constexpr int kD = 128;               // head dim (the P.V MMA's M)
 constexpr int kKT = 128;              // cache rows per tile (the score MMA's M)
 constexpr int kC = kD / 32;           // 32-dim blocks per tile
-constexpr int kNK = 3;                // score ring slots
-constexpr int kNVR = 4;               // value ring slots
+constexpr int kNK = 6;                // score ring slots (1.5 tiles)
+constexpr int kNVR = 4;               // value ring slots (one tile; eight, with three K slots, measured slower)
 constexpr uint32_t kBlockBytes = kKT * 32 * 4;  // one [128 rows x 32 dims] block, 16 KB
-constexpr uint32_t kKSlot = 2 * kBlockBytes;    // K (hi after the split) | K_lo
+constexpr uint32_t kKSlot = kBlockBytes;        // a K block (K_hi after the split; K_lo goes to TMEM)
 constexpr uint32_t kQChunk = kNV * 32 * 4;      // [16 heads x 32 dims or rows], 2 KB
 constexpr uint32_t kQBytes = 2u * kC * kQChunk;   // Q_hi chunks, then Q_lo chunks
 constexpr uint32_t kPTBytes = 2u * (kKT / 32) * kQChunk;  // per group: P^T hi blocks, then lo blocks
 constexpr int kThreads = 16 * 32;
 constexpr size_t kSmem = 1024 + (size_t)kNK * kKSlot + (size_t)kNVR * kBlockBytes + kQBytes + 2 * kPTBytes;
 constexpr float kRescaleLog2 = 8.f;
-// TMEM columns: S (2 buffers x 16), O (2 buffers x 16), V^T hi and lo (128 each).
-constexpr uint32_t kColS = 0, kColO = 32, kColVhi = 128, kColVlo = 256, kTmemCols = 512;
+// TMEM columns: S (2 buffers x 16), O (2 buffers x 16), K_lo (one 32-column block per score ring
+// slot), V^T hi and lo (128 each).
+constexpr uint32_t kColS = 0, kColO = 32, kColKlo = 64, kColVhi = 256, kColVlo = 384, kTmemCols = 512;
+static_assert(kColKlo + 32 * kNK <= kColVhi && kColVlo + 128 <= kTmemCols, "TMEM budget");
 constexpr uint32_t kKReleases = 4 + 1;  // splitter warps, the score issuer's commit
 static_assert(kSmem + 2048 <= 232448, "shared memory budget");
-static_assert(kC == 4 && kNVR == kC, "slot q holds value block q of every tile (one arrival per tile)");
+static_assert(kC == 4 && kNVR % kC == 0, "slot (t % 2) * 4 + q holds value block q of tile t");
 
 enum : unsigned int {
     kErrDtFull = 1u << 26,    // a consumer gave up on an arriving ring item or the query tiles
@@ -300,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char* qsm = vring + kNVR * kBlockBytes;          // Q_hi chunks, Q_lo chunks
     unsigned char* pt = qsm + kQBytes;                        // per group: P^T hi blocks, then lo blocks
     __shared__ __align__(8) uint64_t kfull[kNK], kempty[kNK], split_done[kNK], vfull[kNVR], vempty[kNVR],
-        s_full[2], s_free[2], q_full, p_full[2], p_free[2], vt_full, vt_free, o_full[2], o_free[2];
+        s_full[2], s_free[2], q_full, p_full[2], p_free[2], vt_full, vt_free[2], o_full[2], o_free[2];
     __shared__ uint32_t tmem_base_s;
     __shared__ __align__(16) float red_max[2][4][kNV], red_sum[2][4][kNV];  // [group][warp][head]
     __shared__ __align__(16) float alpha_s[2][2][kNV];  // [group][its tile parity][head]
@@ -333,10 +336,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&p_free[b], 1);
             mbar_init(&o_full[b], 1);
             mbar_init(&o_free[b], 4);
+            mbar_init(&vt_free[b], 1);  // P.V of the tiles with parity b is done with V^T
         }
         mbar_init(&q_full, 8);  // the softmax warps, once the query tiles are in place
         mbar_init(&vt_full, 4);
-        mbar_init(&vt_free, 1);
         fence_barrier_init();
     }
     if (threadIdx.x < kNV) {
@@ -422,7 +425,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sd_phase ^= 1u << s;
                 tc_fence_after();
                 unsigned char* slot = kring + (size_t)s * kKSlot;
-                const uint64_t khi = smem_desc_sw128(slot), klo = smem_desc_sw128(slot + kBlockBytes);
+                const uint64_t khi = smem_desc_sw128(slot);
+                const uint32_t klo = tmem + kColKlo + 32 * s;  // K_lo of the slot: TMEM operand A
                 const uint64_t qhi = smem_desc_sw128(qsm + c * kQChunk);
                 const uint64_t qlo = smem_desc_sw128(qsm + (kC + c) * kQChunk);
                 const uint32_t d = tmem + kColS + b * kNV;
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int k = 0; k < 4; ++k) {
                     mma_tf32_ss(d, khi + 2 * k, qhi + 2 * k, idesc, (c > 0 || k > 0) ? 1u : 0u);
                     mma_tf32_ss_acc(d, khi + 2 * k, qlo + 2 * k, idesc);
-                    mma_tf32_ss_acc(d, klo + 2 * k, qhi + 2 * k, idesc);
+                    mma_tf32_ts_acc(d, klo + 8 * k, qhi + 2 * k, idesc);
                 }
                 mma_commit(&kempty[s]);
                 if (c == kC - 1) mma_commit(&s_full[b]);
@@ -463,13 +467,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_tf32_ts_acc(d, vlo, phi, idesc);
                 }
                 mma_commit(&p_free[b]);
-                mma_commit(&vt_free);
+                mma_commit(&vt_free[b]);
                 mma_commit(&o_full[b]);
             }
         }
     } else if (warp <= 7) {
-        // ---- splitters: K block -> K_hi in place, K_lo beside it ----
-        const int st = threadIdx.x - 4 * 32;  // 0 .. 127
+        // ---- splitters: K block -> K_hi in place, K_lo into the slot's TMEM
+        // block.  Warp 4 + q takes rows 32 q .. 32 q + 31 of the block (TMEM
+        // lanes 32 q ..), a thread one row: chunk c (dims 4 c .. 4 c + 3) of
+        // row r sits at byte r * 128 + (c ^ (r % 8)) * 16 (128-byte swizzle).
+        const int r = 32 * (warp & 3) + lane;
+        const uint32_t rlanes = (uint32_t)(32 * (warp & 3)) << 16;
         uint32_t f_phase = 0;
         for (int it = 0; it < nk; ++it) {
             const int s = it % kNK;
@@ -479,16 +487,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 raise_device_error(&g_decode_tc_device_error, kErrDtFull);
                 break;
             }
-            float4* hi = reinterpret_cast<float4*>(kring + (size_t)s * kKSlot);
-            float4* lo = reinterpret_cast<float4*>(kring + (size_t)s * kKSlot + kBlockBytes);
+            float4* row = reinterpret_cast<float4*>(kring + (size_t)s * kKSlot + r * 128);
+            float lo[32];
 #pragma unroll
-            for (int i = 0; i < (int)(kBlockBytes / 16) / 128; ++i) {
-                const int j = st + 128 * i;
-                const float4 x = hi[j];
+            for (int c = 0; c < 8; ++c) {
+                const int pc = c ^ (r & 7);
+                const float4 x = row[pc];
                 const float4 h = make_float4(tf32_trunc(x.x), tf32_trunc(x.y), tf32_trunc(x.z), tf32_trunc(x.w));
-                hi[j] = h;
-                lo[j] = make_float4(x.x - h.x, x.y - h.y, x.z - h.z, x.w - h.w);
+                row[pc] = h;
+                lo[4 * c + 0] = x.x - h.x;
+                lo[4 * c + 1] = x.y - h.y;
+                lo[4 * c + 2] = x.z - h.z;
+                lo[4 * c + 3] = x.w - h.w;
             }
+            tmem_st32(tmem + rlanes + kColKlo + 32 * s, lo);
+            tmem_wait_st();
+            tc_fence_before();
             asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // generic writes -> MMA
             __syncwarp();
             if (lane == 0) {
@@ -544,15 +558,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         // V^T of tile vl, once the previous tile's P.V MMAs are done with
         // V^T.  Row kk, dim lane of a V block sits at byte kk * 128 +
         // ((lane / 4) ^ (kk % 8)) * 16 + (lane % 4) * 4 (128-byte swizzle).
-        // Slot q holds block q of every tile, and the groups take turns (the
-        // group of tile t moves tile t + 1): the wait for the previous tile's
-        // P.V comes first, because it also means the other group has taken
-        // block q of tile vl - 1 out of the slot, so the slot's barrier is at
-        // most one phase behind tile vl and its parity names that tile alone.
+        // Slot (t % 2) * 4 + q holds block q of tile t, and the groups take
+        // turns (the group of tile t moves tile t + 1).  An mbarrier wait only
+        // checks a phase's parity, so each wait below is for a phase at most
+        // one ahead of what this group already knows has completed: the P.V
+        // of tile vl - 1 is waited on the barrier of its tile parity (this
+        // group's own tile vl - 3, the previous phase there, was waited when
+        // it wrote P), and it comes first because it also means block q of
+        // tile vl - 2 has been taken out of the slot.
         auto move_v = [&](int vl) -> bool {
-            const int vs = (vl * kC + quarter) % kNVR;  // one block per slot and tile
-            const bool vok = (vl == 0 || __all_sync(FULL, mbar_wait(&vt_free, (uint32_t)((vl - 1) & 1)))) &&
-                             __all_sync(FULL, mbar_wait(&vfull[vs], (uint32_t)(vl & 1)));
+            const int vi = vl * kC + quarter, vs = vi % kNVR;  // the ring item and its slot
+            const bool vok = (vl == 0 || __all_sync(FULL, mbar_wait(&vt_free[(vl - 1) & 1], (uint32_t)(((vl - 1) >> 1) & 1)))) &&
+                             __all_sync(FULL, mbar_wait(&vfull[vs], (uint32_t)((vi / kNVR) & 1)));
             if (!vok) {
                 raise_device_error(&g_decode_tc_device_error, kErrDtV);
                 return false;
