@@ -2,7 +2,8 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl vtmu|reference]
                     [--workload NAME] [--kernel auto|tc|ffma] [--no-cpu-baseline]
-                    [--no-prefill] [--no-mla] [--cpu-budget SEC] [--prefill-cpu-budget SEC]
+                    [--no-prefill] [--no-mla] [--no-rows] [--cpu-budget SEC]
+                    [--prefill-cpu-budget SEC]
 
 Workloads (seeded_inputs.WORKLOADS): gqa_decode (default), gqa_decode_rope
 (the same step with the rotary embedding fused in), gqa_spec_decode (4 query
@@ -30,8 +31,11 @@ roofline against two ceilings (the measured bf16 rate scaled to 3xTF32, and
 the measured kind::tf32 rate per SM at the sampled SM clock), end-to-end
 TFLOP/s from host buffers and a bounded oracle sample; `--no-prefill` leaves
 them out.  It also carries `mla`: the latent-attention decode step (mla_decode,
-DeepSeek-V2-Lite's shape) with its GB/s and both rooflines (`--no-mla`).  `--impl reference` times the CPU oracle on the host cores instead,
-on a bounded sample of the same workload.
+DeepSeek-V2-Lite's shape) with its GB/s and both rooflines (`--no-mla`), and
+(default workload only) `decode_rows`: the 4-row speculative step
+(gqa_spec_decode, the tensor-core decode) with its GB/s and HBM roofline
+(`--no-rows`).  `--impl reference` times the CPU oracle on the host cores
+instead, on a bounded sample of the same workload.
 
 N > 1 (torchrun): every rank runs an independent replica on its own GPU (the
 op has no exchange step); ranks meet at a barrier around the timed region
@@ -827,6 +831,9 @@ def run_vtmu(args, rank, world, local):
                                              cpu_budget=0.0 if args.no_cpu_baseline else args.prefill_cpu_budget,
                                              e2e_steps=3))
         mla = None if args.no_mla else measure_mla(ctx, "mla_decode")
+        # The few-query-row step (the scope table's second next row) beside
+        # the one-row step it extends.
+        rows = measure_decode(ctx, "gqa_spec_decode") if name == "gqa_decode" and not args.no_rows else None
         sampler.stop()
         clocks = sampler.summary(*d["_window"])
         achieved = d["step_bytes"] / (d["kernel_ms"] / 1e3) / 1e9
@@ -849,6 +856,26 @@ def run_vtmu(args, rank, world, local):
         }
         if block:
             line["prefill"] = [finish_prefill(ctx, r) for r in block]
+        if rows is not None:
+            rclk = sampler.summary(*rows["_window"])
+            rw = si.WORKLOADS["gqa_spec_decode"]
+            r_ach = rows["step_bytes"] / (rows["kernel_ms"] / 1e3) / 1e9
+            rcpu = None
+            if rank == 0 and not args.no_cpu_baseline:
+                val, sample, cores = time_oracle("gqa_spec_decode", rw, budget_s=args.prefill_cpu_budget, x=rows["x"])
+                rcpu = {"value": round(val, 4), "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample}
+            line["decode_rows"] = {
+                "workload": "gqa_spec_decode", "config": workload_config("gqa_spec_decode", world),
+                "value": round(rows["step_bytes"] / 1e9 * world / (rows["step_ms"] / 1e3), 3), "unit": "GB/s",
+                "ms_per_step": round(rows["step_ms"], 5), "kernel_ms": round(rows["kernel_ms"], 5),
+                "steps": args.steps, "warmup": args.warmup,
+                "roofline": {"bound": "hbm", "kernel": rows["kernel_tag"], "achieved": round(r_ach, 3),
+                             "peak": round(peak, 1), "peak_source": peak_kind, "unit": "GB/s",
+                             "frac": round(r_ach / peak, 4),
+                             "traffic": profile_traffic(rows["kernel_tag"] + "__gqa_spec_decode"),
+                             "kernel_ms": round(rows["kernel_ms"], 5)},
+                "e2e": rows["e2e"], "cpu_baseline": rcpu,
+                "gpu_launches": rows["launches_per_step"] * args.steps, "clocks": rclk}
         if mla is not None:
             mclk = sampler.summary(*mla["_window"])
             mcpu = None
@@ -917,6 +944,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill", action="store_true",
                     help="decode workloads: leave out the four prefill workloads that follow the decode line")
+    ap.add_argument("--no-rows", action="store_true",
+                    help="default decode line: leave out the 4-row speculative step (decode_rows)")
     ap.add_argument("--no-mla", action="store_true",
                     help="decode workloads: leave out the latent-attention decode step that follows the decode line")
     ap.add_argument("--prefill-cpu-budget", type=float, default=3.0,
