@@ -879,7 +879,8 @@ cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace,
 
 bool decode_tc_supported(const AttnDesc& a) {
     return a.T >= 1 && a.T * a.G <= kNV && a.D == kD && a.Dv == kD && !a.softcap_on &&
-           !a.alibi_on && a.bias_kind == 0 && a.S < ((int64_t)1 << 31) && a.Hk <= 65535;
+           !a.alibi_on && a.bias_kind == 0 && a.S < ((int64_t)1 << 31) &&
+           a.Hk <= kMaxDecodeKvHeads;  // one arrival counter per KV head in the workspace header
 }
 
 void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcPlan* tp) {

@@ -125,6 +125,7 @@ def test_decode_shape_outside_its_table_is_refused(lib):
     dict(T=2, heads=4, kvHeads=2, headDim=128, softcap=30.0),
     dict(T=2, heads=4, kvHeads=2, headDim=128, alibi=True),
     dict(T=2, heads=4, kvHeads=2, headDim=128, vHeadDim=64),
+    dict(T=2, heads=16385, kvHeads=16385, headDim=128),     # more KV heads than arrival counters
 ])
 def test_tensor_core_decode_outside_its_shapes_is_refused(lib, kw):
     kw = dict(kw)

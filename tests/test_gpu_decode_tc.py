@@ -161,3 +161,27 @@ def test_decode_tc_refuses_what_it_does_not_cover():
         gpu_attention(x["q"], x["k"], x["v"], heads=4, headDim=128, kvHeads=2, posOffset=298, softcap=30.0,
                       kernel=DECODE_TC)
     assert e.value.status == vtmu.VTMU_ERR_UNSUPPORTED
+
+
+def test_decode_kernels_share_a_workspace():
+    """The CUDA-core decode and the tensor-core decode keep their arrival
+    counters in the same workspace header, each leaving them at zero: calls of
+    both kinds and of different shapes in a row on one workspace all stay
+    correct."""
+    ws = vtmu.Workspace()
+    cases = [
+        (4, 3000, 32, 8, DECODE_TC),
+        (1, 3000, 32, 8, vtmu.VTMU_KERNEL_DECODE),
+        (2, 1500, 16, 4, DECODE_TC),
+        (3, 2000, 8, 8, vtmu.VTMU_KERNEL_DECODE),
+        (4, 3000, 32, 8, DECODE_TC),
+    ]
+    # One buffer for all of them (a workspace that grows is a new, zeroed one).
+    ws.get(max(vtmu.vtmu_attention_workspace_size(
+        vtmu.make_params(T, S, heads=H, headDim=128, kvHeads=Hk, posOffset=S - T, kernel=kern))
+        for T, S, H, Hk, kern in cases))
+    first = ws.buf
+    for i, (T, S, H, Hk, kern) in enumerate(cases):
+        x = si.attention_inputs(T, S, H, Hk, 128, 128, 3300 + i)
+        check(x, dict(heads=H, headDim=128, kvHeads=Hk, posOffset=S - T, kernel=kern, workspace=ws))
+    assert ws.buf is first
