@@ -561,11 +561,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Slot (t % 2) * 4 + q holds block q of tile t, and the groups take
         // turns (the group of tile t moves tile t + 1).  An mbarrier wait only
         // checks a phase's parity, so each wait below is for a phase at most
-        // one ahead of what this group already knows has completed: the P.V
-        // of tile vl - 1 is waited on the barrier of its tile parity (this
-        // group's own tile vl - 3, the previous phase there, was waited when
-        // it wrote P), and it comes first because it also means block q of
-        // tile vl - 2 has been taken out of the slot.
+        // one ahead of one this group has already seen complete: the P.V of
+        // tile vl - 1 is waited on the barrier of that tile's parity, which
+        // only this group (the group of tile vl - 1) waits on, one tile after
+        // the other; and that wait comes first because it also means block q
+        // of tile vl - 2 has been taken out of the slot (the P.V of tile
+        // vl - 1 started only after tile vl - 1's V was moved, which came
+        // after tile vl - 2's).
         auto move_v = [&](int vl) -> bool {
             const int vi = vl * kC + quarter, vs = vi % kNVR;  // the ring item and its slot
             const bool vok = (vl == 0 || __all_sync(FULL, mbar_wait(&vt_free[(vl - 1) & 1], (uint32_t)(((vl - 1) >> 1) & 1)))) &&
