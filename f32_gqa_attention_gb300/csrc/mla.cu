@@ -41,6 +41,7 @@
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "launch_cache.h"
+#include "pdl.cuh"
 #include "tma_sync.cuh"
 
 namespace vtmu {
@@ -82,6 +83,7 @@ __device__ __forceinline__ void store_q(float* qabs, float* qlo, int64_t i, floa
     }
 }
 
+
 // ---- 1. absorb the queries, write the new cache rows ------------------------
 // grid (heads, kR / 128, ceil(T / 4)), 256 threads.  Lane l of warp w owns
 // latent columns 128 jb + 4 l .. + 3 and the k_b rows i = w, w + 8, ... of
@@ -102,6 +104,7 @@ __global__ void __launch_bounds__(256) mla_absorb_kernel(const float* __restrict
     const int rows = (int)((T - t0) < kAbsorbRows ? (T - t0) : kAbsorbRows);
     const int Dq = N + kP;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_launch_dependents();  // the attention kernel may start its own prologue
     // The decode step's new cache rows (op cache_write), by one block.
     if (cw.state_new != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
         const int64_t n4 = cw.rows * kW / 4;
@@ -162,7 +165,9 @@ struct LatArgs {
     int32_t splits;
     int32_t sink_splits;
     int64_t sink_end, lo, hi, per;
+    int64_t new_lo, new_hi;  // cache rows the absorb launch writes (new_lo == new_hi: none)
 };
+
 
 // 16 partial sums per lane -> lanes l and l ^ 16 hold the warp-wide sum of
 // entry l % 16 (entry 4 k + h: key k, head h of a 4-key batch).  Slot 4 k + h
@@ -239,10 +244,15 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     };
     const bool producer = threadIdx.x == 0;
     int issued = 0;  // stages issued (producer thread)
+    pdl_launch_dependents();
     if (producer) {
         prefetch_tensormap(&tm_state);
+        // Rows the absorb launch writes must be in memory before a TMA read
+        // of them; other splits stream the cache at once.
+        if (args.new_hi > args.new_lo && k0 < args.new_hi && args.new_lo < k0 + (int64_t)nst * kNK) pdl_wait();
         for (; issued < nst && issued < kStages; ++issued) issue(issued);
     }
+    pdl_wait();  // the absorbed queries
 
     // ---- consumers ----
     const int hq = warp % HQ, ks = warp / HQ;
@@ -500,6 +510,8 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const float* __restrict_
     __shared__ float wsp[kMaxMlaSplits];
     __shared__ float red[8][32];
     __shared__ float inv_l;
+    pdl_launch_dependents();
+    pdl_wait();  // the attention kernel's partials
     const int v = blockIdx.x, d = blockIdx.y * 32 + (threadIdx.x & 31);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     if (warp == 0) {
@@ -538,6 +550,7 @@ __global__ void __launch_bounds__(256) mla_merge_kernel(const float* __restrict_
 __global__ void __launch_bounds__(256) mla_project_kernel(const float* __restrict__ olat,
                                                           const float* __restrict__ v_b, float* __restrict__ out,
                                                           int H, int Dv) {
+    pdl_wait();  // the merged latent
     const int v = blockIdx.x;
     const int64_t t = v / H;
     const int h = v % H;
@@ -601,8 +614,7 @@ cudaError_t launch_latent(const CUtensorMap& tm, const LatArgs& args, int groups
     auto kern = mla_latent_kernel<HQ>;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(kern), (int)kLatSmem);
     if (e != cudaSuccess) return e;
-    kern<<<dim3(groups, args.splits), kLatThreads, kLatSmem, stream>>>(tm, args);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(groups, args.splits), dim3(kLatThreads), kLatSmem, stream, tm, args);
 }
 
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
@@ -728,6 +740,8 @@ cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& base, void* workspace, c
         args.lo = plan.lo;
         args.hi = plan.hi;
         args.per = plan.per;
+        args.new_lo = cw.state_new != nullptr ? cw.offset : 0;
+        args.new_hi = cw.state_new != nullptr ? cw.offset + cw.rows : 0;
         switch (plan.hq) {
             case 2: e = launch_latent<2>(tm, args, plan.groups, stream); break;
             case 4: e = launch_latent<4>(tm, args, plan.groups, stream); break;
@@ -737,11 +751,11 @@ cudaError_t launch_mla(const MlaDesc& m, const MlaPlan& base, void* workspace, c
     if (e != cudaSuccess) return e;
     const unsigned V = (unsigned)(m.T * m.H);
     float* olat = reinterpret_cast<float*>(w + plan.olat_off);
-    mla_merge_kernel<<<dim3(V, kR / 32), 256, 0, stream>>>(part_m, part_l, part_o, olat, splits);
-    e = cudaGetLastError();
+    e = launch_pdl(mla_merge_kernel, dim3(V, kR / 32), dim3(256), 0, stream, (const float*)part_m,
+                   (const float*)part_l, (const float*)part_o, olat, splits);
     if (e != cudaSuccess) return e;
-    mla_project_kernel<<<dim3(V, (unsigned)((m.Dv + 31) / 32)), 256, 0, stream>>>(olat, m.v_b, m.out, m.H, m.Dv);
-    return cudaGetLastError();
+    return launch_pdl(mla_project_kernel, dim3(V, (unsigned)((m.Dv + 31) / 32)), dim3(256), 0, stream,
+                      (const float*)olat, m.v_b, m.out, m.H, m.Dv);
 }
 
 unsigned int mla_take_device_error() {
