@@ -1109,11 +1109,13 @@ cudaError_t launch_cfg(const AttnDesc& a, const AlibiTable& alibi, float* khi, f
     if (e != cudaSuccess) return e;
     // Query heads per launch-order group: whole KV groups (a divisor of
     // kvHeads) whose K and V^T hi/lo over the keys of a few concurrent query
-    // tiles stay under ~80 MB of the 126 MB L2.
+    // tiles stay under ~40 MB of the 126 MB L2 (80 MB let the headDim-256
+    // windowed prefill read its K/V from DRAM ~1.8 times; 20 MB slowed the
+    // ALiBi prefill by splitting its heads too finely).
     const int64_t keys = a.window > 0 ? (a.window + 5 * kBM < a.S ? a.window + 5 * kBM : a.S) : a.S;
     const double per_kv = (double)keys * (D + DV) * 2 * sizeof(float);
     int gk = a.Hk;
-    while (gk > 1 && (a.Hk % gk != 0 || per_kv * gk > 80e6)) --gk;
+    while (gk > 1 && (a.Hk % gk != 0 || per_kv * gk > 40e6)) --gk;
     const int hgroup = gk * a.G;
     dim3 grid((unsigned)((a.T + kBM - 1) / kBM), (unsigned)a.H, (unsigned)(DV / C::DVC));
     kern<<<grid, C::THREADS, C::SMEM, stream>>>(a, alibi, bias_staged, hgroup, m_q, m_bias, m_khi, m_klo, m_vhi,
