@@ -76,6 +76,7 @@
 #include "attn_common.cuh"
 #include "kernels.h"
 #include "launch_cache.h"
+#include "rope.cuh"
 #include "tcgen05_ops.cuh"
 #include "tma_sync.cuh"
 
@@ -106,6 +107,7 @@ constexpr uint32_t kColS = 0, kColO = 32, kColKlo = 64, kColVhi = 256, kColVlo =
 static_assert(kColKlo + 32 * kNK <= kColVhi && kColVlo + 128 <= kTmemCols, "TMEM budget");
 constexpr uint32_t kKReleases = 4 + 1;  // splitter warps, the score issuer's commit
 static_assert(kSmem + 2048 <= 232448, "shared memory budget");
+static_assert(kNV * kRopeMaxPairs * (int)sizeof(float2) <= kPTBytes, "the query's rotary table fits a P^T buffer");
 static_assert(kC == 4 && kNVR % kC == 0, "slot (t % 2) * 4 + q holds value block q of tile t");
 
 enum : unsigned int {
@@ -133,6 +135,7 @@ struct DtArgs {
     int32_t n_sink_tiles, n_tiles;  // tiles of the sink range and of the main range
     int64_t lo;        // first row of the main range (the sink range starts at 0)
     int64_t sink_end, hi;
+    RopeDev rope;      // rotary embedding of q and the new keys (rope.half == 0: none)
 };
 
 // Tiles [t0, t1) of this split in the concatenated (sink, main) tile list.
@@ -195,14 +198,31 @@ __device__ __forceinline__ bool owns_row(const DtArgs& g, int split, int t0, int
 
 // The new cache rows this CTA owns, its KV head's columns (128 floats = 32
 // float4 per row, one per lane), into `cache` before any TMA read of them:
-// each lane's generic writes are fenced against the async proxy.
+// each lane's generic writes are fenced against the async proxy.  With
+// `turn` (the keys under a rotary embedding) channel d < rotary_dim of row r
+// is turned at position r with its pair partner, as op "rope" turns it.
 __device__ __forceinline__ void write_new_rows(const DtArgs& g, int split, int t0, int t1, int hk, int lane,
-                                               float* cache, const float* rows) {
+                                               float* cache, const float* rows, bool turn) {
     const int64_t width4 = (int64_t)g.a.Hk * (kD / 4);
-    for (int64_t r = g.cw.lo; r < g.cw.hi; ++r)
-        if (owns_row(g, split, t0, t1, r))
-            reinterpret_cast<float4*>(cache)[r * width4 + hk * (kD / 4) + lane] =
-                reinterpret_cast<const float4*>(rows)[(r - g.cw.lo) * width4 + hk * (kD / 4) + lane];
+    for (int64_t r = g.cw.lo; r < g.cw.hi; ++r) {
+        if (!owns_row(g, split, t0, t1, r)) continue;
+        const int64_t src4 = (r - g.cw.lo) * width4 + hk * (kD / 4);
+        float4 x = reinterpret_cast<const float4*>(rows)[src4 + lane];
+        if (turn) {
+            float* e = reinterpret_cast<float*>(&x);
+            const float* src = rows + src4 * 4;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int d = 4 * lane + c;
+                if (d >= 2 * g.rope.half) continue;
+                int j, partner;
+                bool first;
+                rope_pair_of(g.rope, d, j, partner, first);
+                e[c] = rope_channel(e[c], __ldg(src + partner), first, rope_cos_sin(g.rope, r, j));
+            }
+        }
+        reinterpret_cast<float4*>(cache)[r * width4 + hk * (kD / 4) + lane] = x;
+    }
     asm volatile("fence.proxy.async.global;\n" ::: "memory");
     __syncwarp();
 }
@@ -375,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the step's new K (warp 0) or V (warp 2) rows this CTA reads ----
         if (g.cw.hi > g.cw.lo)
             write_new_rows(g, split, t0, t1, hk, lane, warp == 0 ? g.cw.kc : g.cw.vc,
-                           warp == 0 ? g.cw.k_new : g.cw.v_new);
+                           warp == 0 ? g.cw.k_new : g.cw.v_new, warp == 0 && g.rope.half > 0);
         if (lane == 0) {
             const bool scores = warp == 0;
             const CUtensorMap* map = scores ? &tm_k : &tm_v;
@@ -521,16 +541,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // scaled by scale log2 e, split into Q_hi (tf32, rounded to nearest)
         // and Q_lo = q - Q_hi, in the K-major blocks the score MMA reads
         // (block = dim / 32, head v's row of a block is 128 bytes, 128-byte
-        // swizzle); zero rows past T G.
+        // swizzle); zero rows past T G.  Under a rotary embedding q is
+        // turned first (row t at position posOffset + t, as op "rope" turns
+        // it), with the T x rotary_dim/2 (cos, sin) pairs worked out once into
+        // group 0's P^T buffer, idle until the first score tile (which needs
+        // every softmax warp's query tiles).
         {
             const int u = threadIdx.x - 8 * 32;  // 0 .. 255
             constexpr int kPer = kNV * kD / 256;
-            float qv[kPer];  // every load in flight before the first shared store
+            const int half = g.rope.half;
+            float qv[kPer], qp[kPer];  // every load in flight before the first shared store
 #pragma unroll
             for (int k = 0; k < kPer; ++k) {
                 const int idx = u + 256 * k, v = idx / kD, dd = idx % kD;
-                qv[k] = v < g.nv ? __ldg(g.a.q + ((int64_t)(v / g.a.G) * g.a.H + hk * g.a.G + v % g.a.G) * kD + dd)
-                                 : 0.f;
+                const float* qrow = g.a.q + ((int64_t)(v / g.a.G) * g.a.H + hk * g.a.G + v % g.a.G) * kD;
+                qv[k] = v < g.nv ? __ldg(qrow + dd) : 0.f;
+                qp[k] = 0.f;
+                if (half > 0 && v < g.nv && dd < 2 * half) {
+                    int j, partner;
+                    bool first;
+                    rope_pair_of(g.rope, dd, j, partner, first);
+                    qp[k] = __ldg(qrow + partner);
+                }
+            }
+            if (half > 0) {
+                float2* cs = reinterpret_cast<float2*>(pt);  // [t][j]; T half <= 16 x 128 pairs = kPTBytes
+                const int rows_t = g.nv / g.a.G;
+                for (int i = u; i < rows_t * half; i += 256)
+                    cs[i] = rope_cos_sin(g.rope, g.a.pos_offset + i / half, i % half);
+                softmax_sync_and(true);
+#pragma unroll
+                for (int k = 0; k < kPer; ++k) {
+                    const int idx = u + 256 * k, v = idx / kD, dd = idx % kD;
+                    if (v < g.nv && dd < 2 * half) {
+                        int j, partner;
+                        bool first;
+                        rope_pair_of(g.rope, dd, j, partner, first);
+                        qv[k] = rope_channel(qv[k], qp[k], first, cs[(v / g.a.G) * half + j]);
+                    }
+                }
             }
 #pragma unroll
             for (int k = 0; k < kPer; ++k) {
@@ -843,7 +892,7 @@ bool encode_blocks(CUtensorMap* map, const float* p, int64_t rows, int64_t cols,
 size_t up256(size_t b) { return (b + 255) / 256 * 256; }
 
 cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
-                     const DecodeCacheWrite* cw) {
+                     const DecodeCacheWrite* cw, const RopeDev* rope) {
     unsigned char* ws = static_cast<unsigned char*>(workspace) + kWorkspaceHeader;
     const size_t rows = (size_t)a.Hk * kNV * tp.splits;
     float* part_m = reinterpret_cast<float*>(ws);
@@ -871,6 +920,7 @@ cudaError_t launch_d(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace,
     g.lo = tp.lo;
     g.sink_end = tp.sink_end;
     g.hi = tp.hi;
+    if (rope) g.rope = *rope;
     cudaError_t e = set_smem_once(reinterpret_cast<const void*>(decode_tc_kernel), (int)kSmem);
     if (e != cudaSuccess) return e;
     decode_tc_kernel<<<dim3(a.Hk, tp.splits), kThreads, kSmem, stream>>>(tm_k, tm_v, g);
@@ -914,8 +964,8 @@ void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcP
 }
 
 cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
-                             const DecodeCacheWrite* cw) {
-    return launch_d(a, tp, workspace, stream, cw);
+                             const DecodeCacheWrite* cw, const RopeDev* rope) {
+    return launch_d(a, tp, workspace, stream, cw, rope);
 }
 
 unsigned int decode_tc_take_device_error() {

@@ -75,9 +75,11 @@ bool decode_tc_supported(const AttnDesc& a);
 // `forced_splits` > 0 overrides the split count (at most one split per tile).
 void decode_tc_plan(const AttnDesc& a, int forced_splits, int num_sms, DecodeTcPlan* tp);
 // Launches the attention (which also writes the new rows of `cw` when given;
-// its pointers must be 16-byte aligned) and the split merge.
+// its pointers must be 16-byte aligned) and the split merge.  `rope` (or
+// NULL) turns q and the new keys inside the launch; the caches receive
+// turned keys.
 cudaError_t launch_decode_tc(const AttnDesc& a, const DecodeTcPlan& tp, void* workspace, cudaStream_t stream,
-                             const DecodeCacheWrite* cw);
+                             const DecodeCacheWrite* cw, const RopeDev* rope);
 unsigned int decode_tc_take_device_error();
 
 // ---- tiled prefill on FP32 FMA ----------------------------------------------

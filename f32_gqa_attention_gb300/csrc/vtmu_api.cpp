@@ -481,6 +481,10 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
             const uintptr_t c16 = reinterpret_cast<uintptr_t>(cw->kc) | reinterpret_cast<uintptr_t>(cw->vc) |
                                   reinterpret_cast<uintptr_t>(cw->k_new) | reinterpret_cast<uintptr_t>(cw->v_new);
             if (c16 & 15u) {
+                if (rope)
+                    return fail(VTMU_ERR_UNSUPPORTED,
+                                "decode_step_rope: the tensor-core decode turns new keys only from 16-byte aligned "
+                                "caches and new rows; compose vtmu_rope and vtmu_decode_step otherwise");
                 e = write_caches();
                 if (e != cudaSuccess) return cuda_fail(e, "cache_write launch");
             } else {
@@ -489,7 +493,7 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
         }
         vtmu::DecodeTcPlan plan;
         vtmu::decode_tc_plan(a, p->decode_splits, device_sm_count(), &plan);
-        e = vtmu::launch_decode_tc(a, plan, workspace, stream, fused);
+        e = vtmu::launch_decode_tc(a, plan, workspace, stream, fused, rope);
         if (e != cudaSuccess) return cuda_fail(e, "tensor-core decode launch");
         return ok();
     }
@@ -502,10 +506,12 @@ vtmu_status run_attention(Resolved& r, const float* q, const float* k, const flo
             r.kernel = VTMU_KERNEL_PREFILL_FFMA;
         }
     }
-    if (rope && r.kernel != VTMU_KERNEL_DECODE)
+    if (rope && (r.kernel != VTMU_KERNEL_DECODE || a.T != 1))
         return fail(VTMU_ERR_UNSUPPORTED,
-                    "decode_step_rope: the fused step needs T == 1, a decode-kernel shape and 16-byte aligned "
-                    "q, caches, out; compose vtmu_rope and vtmu_decode_step otherwise");
+                    "decode_step_rope: the fused step needs a shape of the tensor-core decode, or T == 1 and a "
+                    "decode-kernel shape, with 16-byte aligned q, caches, out (T = %lld); compose vtmu_rope and "
+                    "vtmu_decode_step otherwise",
+                    (long long)a.T);
     if (r.kernel == VTMU_KERNEL_DECODE) {
         const size_t need = decode_workspace(a);
         if (!workspace || workspace_bytes < need)
@@ -568,9 +574,10 @@ static vtmu_status decode_step_impl(float* k_cache, float* v_cache, int64_t max_
     vtmu_status st = resolve(p, &r);
     if (st != VTMU_OK) return st;
     const vtmu::AttnDesc& a = r.a;
-    if (rope && a.T != 1)
-        return fail(VTMU_ERR_UNSUPPORTED, "decode_step_rope: the fused step takes one query row (T = %lld)",
-                    (long long)a.T);
+    if (rope && a.T < 1)
+        return fail(VTMU_ERR_UNSUPPORTED,
+                    "decode_step_rope: no query row (T = 0); turn the new keys with vtmu_rope and write them "
+                    "with vtmu_decode_step");
     if (max_rows < 0 || new_rows < 0)
         return fail(VTMU_ERR_INVALID, "decode_step: negative size (max_rows %lld, new_rows %lld)",
                     (long long)max_rows, (long long)new_rows);

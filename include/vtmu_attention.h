@@ -334,15 +334,18 @@ VTMU_API vtmu_status vtmu_rope(const float* x, float* out, int64_t T, int32_t he
 
 /*
  * A decode step with the rotary embedding fused in: what op "rope" on q
- * (position p->pos_offset) and on k_new (row i at position offset + i),
- * then vtmu_decode_step with the turned q and k_new compute -- the caches
- * receive turned keys, q is left as given -- in ONE launch of the decode
- * kernel (vtmu.mpakt.dev/api/ops: a whole decode step is meant to stay on
- * the worker).  Arguments as for vtmu_decode_step, plus `rope` with
+ * (row t at position p->pos_offset + t) and on k_new (row i at position
+ * offset + i), then vtmu_decode_step with the turned q and k_new compute --
+ * the caches receive turned keys, q is left as given -- in ONE launch of a
+ * decode kernel (vtmu.mpakt.dev/api/ops: a whole decode step is meant to stay
+ * on the worker).  Arguments as for vtmu_decode_step, plus `rope` with
  * rope->head_dim == p->head_dim.  Only the fused form is offered: the call
- * needs T == 1 and a shape the decode kernel covers (same table and 16-byte
- * alignment as VTMU_KERNEL_DECODE); anything else is refused with
- * VTMU_ERR_UNSUPPORTED -- compose vtmu_rope and vtmu_decode_step there.
+ * needs either a shape the tensor-core decode covers (VTMU_KERNEL_DECODE_TF32X3
+ * chosen or picked by AUTO: T x group <= 16, headDim 128, with 16-byte
+ * aligned q, caches, k_new, v_new and out), or T == 1 and a shape the CUDA-core
+ * decode covers (same table and 16-byte alignment as VTMU_KERNEL_DECODE);
+ * anything else, T == 0 included, is refused with VTMU_ERR_UNSUPPORTED --
+ * compose vtmu_rope and vtmu_decode_step there.
  * Errors: those of vtmu_decode_step and vtmu_rope, VTMU_ERR_UNSUPPORTED.
  */
 VTMU_API vtmu_status vtmu_decode_step_rope(float* k_cache, float* v_cache, int64_t max_rows,

@@ -296,8 +296,15 @@ def test_decode_step_rope_refusals(lib):
     e = call(p=vtmu.make_params(1, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095,
                                 kernel=vtmu.VTMU_KERNEL_PREFILL_FFMA))
     assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "compose" in str(e)
-    e = call(p=vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094))
+    # 5 rows x group 4 = 20 virtual heads: past the tensor-core decode, and
+    # the CUDA-core decode turns one row only
+    e = call(p=vtmu.make_params(5, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4091))
     assert e.status == vtmu.VTMU_ERR_UNSUPPORTED
+    e = call(p=vtmu.make_params(2, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4094,
+                                kernel=vtmu.VTMU_KERNEL_DECODE))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "compose" in str(e)
+    e = call(p=vtmu.make_params(0, 4096, heads=32, headDim=128, kvHeads=8, posOffset=4095))
+    assert e.status == vtmu.VTMU_ERR_UNSUPPORTED and "T = 0" in str(e)
     assert call(r=vtmu.make_rope_params(headDim=128, rotaryDim=130)).status == vtmu.VTMU_ERR_INVALID
 
 

@@ -48,16 +48,16 @@ def test_rope_matches_oracle(case):
     assert np.array_equal(xd.cpu().numpy(), x), "input changed"
 
 
-def _rope_step_case(S, H, Hk, D, new_rows, offset, seed, rope, **params):
+def _rope_step_case(S, H, Hk, D, new_rows, offset, seed, rope, T=1, **params):
     g = si.Stream(seed)
     x = {
-        "q": g.normal_f32(H * D).reshape(1, H * D),
+        "q": g.normal_f32(T * H * D).reshape(T, H * D),
         "kc": g.normal_f32(S * Hk * D).reshape(S, Hk * D),
         "vc": g.normal_f32(S * Hk * D).reshape(S, Hk * D),
         "kn": g.normal_f32(new_rows * Hk * D).reshape(new_rows, Hk * D),
         "vn": g.normal_f32(new_rows * Hk * D).reshape(new_rows, Hk * D),
     }
-    pos = params.pop("posOffset", offset + new_rows - 1)
+    pos = params.pop("posOffset", offset + new_rows - T)
     # fused
     Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
     q = to_dev(x["q"])
@@ -108,9 +108,54 @@ def test_decode_step_rope_cases(case):
                     case.pop("offset"), 621, case.pop("rope"), **case)
 
 
+def test_spec_decode_step_rope_workload():
+    """The 4-row speculative step (the tensor-core decode) with Llama-3-style
+    rotary embedding fused in: four new rows at 32764 .. 32767 of the
+    [32768, 1024] caches, theta 500000."""
+    _rope_step_case(32768, 32, 8, 128, 4, 32764, 622, dict(base=500000.0), T=4)
+
+
+@pytest.mark.parametrize("case", [
+    dict(T=2, S=2500, H=16, Hk=2, new_rows=2, offset=2498, rope=dict(interleaved=True), window=500),
+    dict(T=3, S=3000, H=12, Hk=3, new_rows=1, offset=2999, rope=dict(rotaryDim=64), posOffset=2997,
+         window=700, sinks=40),
+    dict(T=16, S=1800, H=4, Hk=4, new_rows=16, offset=1700, rope=dict(scaling={"rope_type": "linear", "factor": 4.0}),
+         decode_splits=5),
+    dict(T=4, S=900, H=8, Hk=2, new_rows=6, offset=600, rope=dict(attentionFactor=1.2, base=1e6), posOffset=896,
+         scale=0.1),
+    dict(T=8, S=4000, H=16, Hk=8, new_rows=0, offset=4000, rope=dict(rotaryDim=128, interleaved=True),
+         posOffset=3992),
+])
+def test_decode_step_rope_multi_row(case):
+    """Several query rows on the tensor-core decode: q row t turned at
+    posOffset + t, the new keys at their cache rows (some of them outside
+    the visible range, turned and written all the same)."""
+    case = dict(case)
+    _rope_step_case(case.pop("S"), case.pop("H"), case.pop("Hk"), 128, case.pop("new_rows"), case.pop("offset"),
+                    623, case.pop("rope"), T=case.pop("T"), kernel=vtmu.VTMU_KERNEL_DECODE_TF32X3, **case)
+
+
+def test_decode_step_rope_refuses_unaligned_rows_on_tensor_cores():
+    """The tensor-core decode turns new keys only in its own fused write
+    (float4 rows): 4- but not 16-byte aligned new rows are refused before any
+    launch."""
+    T, S, H, Hk, D = 2, 300, 8, 2, 128
+    Kc = torch.zeros((S, Hk * D), device="cuda")
+    Vc = torch.zeros((S, Hk * D), device="cuda")
+    buf = torch.ones(T * Hk * D + 1, device="cuda")
+    kn = buf[1:].view(T, Hk * D)
+    with pytest.raises(vtmu.VtmuError) as e:
+        vtmu.decode_step_rope(Kc, Vc, kn, kn.clone(), 100, torch.ones((T, H * D), device="cuda"), heads=H,
+                              headDim=D, kvHeads=Hk, rope={})
+    assert e.value.status == vtmu.VTMU_ERR_UNSUPPORTED and "compose" in str(e.value)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(Kc).item() == 0 and torch.count_nonzero(Vc).item() == 0
+
+
 def test_decode_step_rope_refuses_unfused_shapes():
-    """Only the fused form is offered: T > 1, or a shape outside the decode
-    kernel, is refused before any launch (the caches stay as they were)."""
+    """Only the fused form is offered: several rows outside the tensor-core
+    decode's shapes, or a single row outside the decode kernel's, are refused
+    before any launch (the caches stay as they were)."""
     Kc = torch.zeros((64, 2 * 96), device="cuda")
     Vc = torch.zeros((64, 2 * 96), device="cuda")
     kn = torch.ones((1, 2 * 96), device="cuda")
