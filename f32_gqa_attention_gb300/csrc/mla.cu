@@ -20,7 +20,9 @@
 //     every thread below what the consumers hold); warp w takes 4 heads
 //     and a slice of each stage's keys.  Lane l holds 18 of the 576 dims of
 //     every key (dims 128j + 4l .. +3 of the latent and 2l, 2l+1 of the
-//     rotary key) and of its heads' queries; per 4 keys it forms 16 partial
+//     rotary key) and of its heads' queries, as packed pairs of neighbouring
+//     dims (Blackwell's f32x2 FMA: two products per instruction, here and in
+//     P.c); per 4 keys it forms 16 partial
 //     dot products, a butterfly reduce-scatter leaves the score of (key
 //     (l%16)/4, head l%4) in lane l, then an online softmax in base 2 (rescale only
 //     when a max grows by more than 2^8) and P.c into 4 x 16 accumulators.
@@ -42,6 +44,7 @@
 #include "kernels.h"
 #include "launch_cache.h"
 #include "pdl.cuh"
+#include "softcap.cuh"
 #include "tma_sync.cuh"
 
 namespace vtmu {
@@ -260,7 +263,10 @@ __global__ void __launch_bounds__(kLatThreads, 1)
     const int my_h = lane & 3;
     const int my_v = vh0 + my_h;
     const int64_t my_pos = args.a.pos_offset + (my_v < args.V ? my_v / args.a.H : 0);
-    float q[4][18];
+    // The lane's 18 dims of each of its heads' queries as packed pairs of
+    // neighbouring dims (f32x2 registers): latent dims 128 j + 4 lane + (0, 1)
+    // and (2, 3), then the rotary pair.
+    uint64_t q2[4][9];
 #pragma unroll
     for (int h = 0; h < 4; ++h) {
         const int v = vh0 + h;
@@ -268,29 +274,26 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             const float* qr = args.qabs + (int64_t)v * kW;
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const float4 x = __ldg(reinterpret_cast<const float4*>(qr + 128 * j + 4 * lane));
-                q[h][4 * j] = x.x;
-                q[h][4 * j + 1] = x.y;
-                q[h][4 * j + 2] = x.z;
-                q[h][4 * j + 3] = x.w;
+                const ulonglong2 x = __ldg(reinterpret_cast<const ulonglong2*>(qr + 128 * j + 4 * lane));
+                q2[h][2 * j] = x.x;
+                q2[h][2 * j + 1] = x.y;
             }
-            const float2 r = __ldg(reinterpret_cast<const float2*>(qr + kR + 2 * lane));
-            q[h][16] = r.x;
-            q[h][17] = r.y;
+            q2[h][8] = __ldg(reinterpret_cast<const unsigned long long*>(qr + kR + 2 * lane));
         } else {
 #pragma unroll
-            for (int d = 0; d < 18; ++d) q[h][d] = 0.f;
+            for (int i = 0; i < 9; ++i) q2[h][i] = 0ull;
         }
     }
-    float o[4][16];
+    // O's latent dims 128 j + 4 lane + (0, 1) and (2, 3) of each head, packed.
+    uint64_t o2[4][8];
 #pragma unroll
     for (int h = 0; h < 4; ++h)
 #pragma unroll
-        for (int d = 0; d < 16; ++d) o[h][d] = 0.f;
+        for (int i = 0; i < 8; ++i) o2[h][i] = 0ull;
     // The lane's head (lane % 4): its reference max (base 2, lazily raised)
     // and its running sum, the same in every lane of that head.
     float m_my = -INFINITY, l_my = 0.f;
-    __shared__ __align__(16) float pbuf[kConsumerWarps][16];  // a batch's probabilities, per warp
+    __shared__ __align__(16) float2 pbuf[kConsumerWarps][16];  // a batch's probabilities (p, p), per warp
     const int kx = (lane >> 2) & 3;  // key permutation of the score slots
     bool ok = true;
     for (int it = 0; it < nst; ++it) {
@@ -313,27 +316,22 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int kk = k ^ kx;  // this lane's key for slot group k
-                float kv[18];
+                uint64_t kv[9];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 x = *reinterpret_cast<const float4*>(lp + kk * kBoxCols + 2 * j * kBoxFloats);
-                    kv[4 * j] = x.x;
-                    kv[4 * j + 1] = x.y;
-                    kv[4 * j + 2] = x.z;
-                    kv[4 * j + 3] = x.w;
+                    const ulonglong2 x = *reinterpret_cast<const ulonglong2*>(lp + kk * kBoxCols + 2 * j * kBoxFloats);
+                    kv[2 * j] = x.x;
+                    kv[2 * j + 1] = x.y;
                 }
-                const float2 r = *reinterpret_cast<const float2*>(rp + kk * kBoxCols);
-                kv[16] = r.x;
-                kv[17] = r.y;
+                kv[8] = *reinterpret_cast<const unsigned long long*>(rp + kk * kBoxCols);
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {  // two chains per dot product
-                    float s0 = 0.f, s1 = 0.f;
+                for (int h = 0; h < 4; ++h) {  // even and odd dims in the two halves of a pair
+                    uint64_t s2 = f2_mul(q2[h][0], kv[0]);
 #pragma unroll
-                    for (int d = 0; d < 9; ++d) {
-                        s0 = fmaf(q[h][d], kv[d], s0);
-                        s1 = fmaf(q[h][d + 9], kv[d + 9], s1);
-                    }
-                    part[4 * k + h] = s0 + s1;
+                    for (int i = 1; i < 9; ++i) s2 = f2_fma(q2[h][i], kv[i], s2);
+                    float se, so;
+                    f2_unpack(s2, se, so);
+                    part[4 * k + h] = se + so;
                 }
             }
             // Lanes l and l ^ 16: the score of key kb + (l % 16) / 4 for head
@@ -356,8 +354,9 @@ __global__ void __launch_bounds__(kLatThreads, 1)
 #pragma unroll
                 for (int h = 0; h < 4; ++h) {
                     const float ah = __shfl_sync(FULL, a_my, h);
+                    const uint64_t ah2 = f2_pack(ah, ah);
 #pragma unroll
-                    for (int d = 0; d < 16; ++d) o[h][d] *= ah;
+                    for (int i = 0; i < 8; ++i) o2[h][i] = f2_mul(o2[h][i], ah2);
                 }
             }
             const float pv = fast_exp2(x - (m_my == -INFINITY ? 0.f : m_my));
@@ -367,32 +366,27 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             l_my += ps;
             // O += P c: the latent dims of each key serve as its value.  The
             // batch's 16 probabilities go through shared memory to every lane
-            // (four broadcast loads), then one 16-byte load of a key's block
-            // feeds 16 FMAs.
-            if (lane < 16) pbuf[warp][lane] = pv;
+            // as (p, p) pairs (eight broadcast loads), then one 16-byte load
+            // of a key's block feeds 8 packed FMAs (16 products).
+            if (lane < 16) pbuf[warp][lane] = make_float2(pv, pv);
             __syncwarp();
-            float pk[16];
+            uint64_t pk2[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 p4 = *reinterpret_cast<const float4*>(&pbuf[warp][4 * i]);
-                pk[4 * i] = p4.x;
-                pk[4 * i + 1] = p4.y;
-                pk[4 * i + 2] = p4.z;
-                pk[4 * i + 3] = p4.w;
+            for (int i = 0; i < 8; ++i) {
+                const ulonglong2 p2 = *reinterpret_cast<const ulonglong2*>(&pbuf[warp][2 * i]);
+                pk2[2 * i] = p2.x;
+                pk2[2 * i + 1] = p2.y;
             }
             __syncwarp();
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
-                    const float4 c = *reinterpret_cast<const float4*>(lp + k * kBoxCols + 2 * j * kBoxFloats);
+                    const ulonglong2 c = *reinterpret_cast<const ulonglong2*>(lp + k * kBoxCols + 2 * j * kBoxFloats);
 #pragma unroll
                     for (int h = 0; h < 4; ++h) {
-                        const float p = pk[4 * k + h];
-                        o[h][4 * j] = fmaf(p, c.x, o[h][4 * j]);
-                        o[h][4 * j + 1] = fmaf(p, c.y, o[h][4 * j + 1]);
-                        o[h][4 * j + 2] = fmaf(p, c.z, o[h][4 * j + 2]);
-                        o[h][4 * j + 3] = fmaf(p, c.w, o[h][4 * j + 3]);
+                        o2[h][2 * j] = f2_fma(pk2[4 * k + h], c.x, o2[h][2 * j]);
+                        o2[h][2 * j + 1] = f2_fma(pk2[4 * k + h], c.y, o2[h][2 * j + 1]);
                     }
                 }
             }
@@ -418,6 +412,11 @@ __global__ void __launch_bounds__(kLatThreads, 1)
             if (!mbar_wait(&full[it % kStages], (uint32_t)((it / kStages) & 1)))
                 raise_device_error(&g_mla_device_error, kErrMlaDrain);
     }
+    float o[4][16];
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) f2_unpack(o2[h][i], o[h][2 * i], o[h][2 * i + 1]);
     // Every head's reference max and sum, in every lane.
     float m_ref[4], l_sum[4];
 #pragma unroll
