@@ -436,7 +436,9 @@ def test_decode_step_unfused_paths():
 @pytest.mark.parametrize("case", [
     dict(S=32768, H=32, Hk=8, D=128, T=1, new_rows=1, offset=32767, pinned=True),   # the decode workload
     dict(S=3000, H=8, Hk=4, D=64, T=1, new_rows=3, offset=2990, pinned=False, bias=True),
-    dict(S=700, H=4, Hk=2, D=128, T=6, new_rows=6, offset=600, pinned=True),       # unfused (T = 6)
+    dict(S=700, H=4, Hk=2, D=128, T=6, new_rows=6, offset=600, pinned=True),       # tensor-core decode (12 virtual heads)
+    dict(S=32768, H=32, Hk=8, D=128, T=4, new_rows=4, offset=32764, pinned=True),  # the 4-row speculative workload
+    dict(S=900, H=16, Hk=2, D=64, T=3, new_rows=3, offset=800, pinned=False),     # CUDA-core decode, 24 virtual heads
 ])
 def test_decode_step_host_buffers(case):
     """vtmu_decode_step_host: the step's inputs and output in host memory

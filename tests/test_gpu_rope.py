@@ -125,11 +125,12 @@ def test_spec_decode_step_rope_workload():
          scale=0.1),
     dict(T=8, S=4000, H=16, Hk=8, new_rows=0, offset=4000, rope=dict(rotaryDim=128, interleaved=True),
          posOffset=3992),
+    dict(T=1, S=2100, H=16, Hk=1, new_rows=1, offset=2099, rope=dict(base=500000.0)),  # one row, group 16
 ])
 def test_decode_step_rope_multi_row(case):
-    """Several query rows on the tensor-core decode: q row t turned at
-    posOffset + t, the new keys at their cache rows (some of them outside
-    the visible range, turned and written all the same)."""
+    """Query rows on the tensor-core decode (forced, so one row too): q row t
+    turned at posOffset + t, the new keys at their cache rows (some of them
+    outside the visible range, turned and written all the same)."""
     case = dict(case)
     _rope_step_case(case.pop("S"), case.pop("H"), case.pop("Hk"), 128, case.pop("new_rows"), case.pop("offset"),
                     623, case.pop("rope"), T=case.pop("T"), kernel=vtmu.VTMU_KERNEL_DECODE_TF32X3, **case)
