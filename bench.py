@@ -671,8 +671,10 @@ def measure_decode(ctx, name):
                 outh.copy_(out, non_blocking=True)
             stream.synchronize()
     else:
-        # The host-buffer decode step of the C ABI: it copies q and the new
-        # rows in, runs the fused step, copies the output row back and waits.
+        # The host-buffer decode step of the C ABI on pinned buffers: the
+        # fused step's kernel reads q and the new rows from them and writes
+        # the output row back over the host link (no staging copies), then
+        # the call waits for it.
         hws_bytes = vtmu.vtmu_decode_step_host_workspace_size(p, R)
         hws = torch.zeros(hws_bytes, dtype=torch.uint8, device=dev)
 

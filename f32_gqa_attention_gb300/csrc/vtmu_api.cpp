@@ -697,6 +697,42 @@ vtmu_status vtmu_decode_step_host(float* k_cache, float* v_cache, int64_t max_ro
         return fail(VTMU_ERR_INVALID, "decode_step_host: S %lld exceeds the cache's %lld rows", (long long)a.S,
                     (long long)max_rows);
     char* w = static_cast<char*>(workspace);
+    // Page-locked buffers the device addresses directly (its pointer for
+    // them), or nullptr.  On a decode kernel, which reads q and the new rows
+    // with plain loads and writes the output row with plain stores, such
+    // buffers are used in place: the kernel pulls q and the new rows over
+    // the host link and pushes the output row back, with no staging copies.
+    // Only when all of them qualify and they and the caches are 16-byte
+    // aligned (so that the decode kernel runs and none of its fallbacks) and
+    // no bias is given; otherwise every buffer goes through the workspace.
+    auto mapped = [](const void* hp) -> void* {
+        if (!hp) return nullptr;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, hp) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+    };
+    const bool decode_kernel = r.kernel == VTMU_KERNEL_DECODE || r.kernel == VTMU_KERNEL_DECODE_TF32X3;
+    if (decode_kernel && !bias_host && h.q_b && h.out_b) {
+        void* q_d = mapped(q_host);
+        void* out_d = mapped(out_host);
+        void* kn_d = h.k_new_b ? mapped(k_new_host) : nullptr;
+        void* vn_d = h.v_new_b ? mapped(v_new_host) : nullptr;
+        const uintptr_t m16 = reinterpret_cast<uintptr_t>(q_d) | reinterpret_cast<uintptr_t>(out_d) |
+                              reinterpret_cast<uintptr_t>(kn_d) | reinterpret_cast<uintptr_t>(vn_d) |
+                              reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
+        if (q_d && out_d && (!h.k_new_b || (kn_d && vn_d)) && (m16 & 15u) == 0) {
+            st = vtmu_decode_step(k_cache, v_cache, max_rows, static_cast<const float*>(kn_d),
+                                  static_cast<const float*>(vn_d), new_rows, offset, static_cast<const float*>(q_d),
+                                  nullptr, static_cast<float*>(out_d), p, workspace, h.q, stream);
+            if (st != VTMU_OK) return st;
+            const cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "decode_step_host: stream synchronisation");
+            return ok();
+        }
+    }
     auto stage = [&](size_t off, const float* src, size_t n) -> cudaError_t {
         return n ? cudaMemcpyAsync(w + off, src, n, cudaMemcpyHostToDevice, stream) : cudaSuccess;
     };

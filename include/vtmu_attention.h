@@ -215,7 +215,13 @@ VTMU_API vtmu_status vtmu_decode_step_host_workspace_size(const vtmu_attention_p
  * v_new_host and bias_host into the staging areas of `workspace`, runs
  * vtmu_decode_step on those copies, copies out back to out_host and WAITS for
  * the stream: unlike every other entry point it returns only when out_host
- * holds the result (or an error occurred).
+ * holds the result (or an error occurred).  When the step runs on a decode
+ * kernel (VTMU_KERNEL_DECODE or VTMU_KERNEL_DECODE_TF32X3), no bias is given,
+ * and q_host, k_new_host, v_new_host and out_host are page-locked buffers the
+ * device can address (cudaHostAlloc / cudaMallocHost / cudaHostRegister,
+ * e.g. a pinned PyTorch tensor) that are, like the caches, 16-byte aligned,
+ * the kernel reads q and the new rows and writes the output row in place over
+ * the host link, with no staging copy (same result, bit for bit).
  *   k_cache, v_cache, max_rows, new_rows, offset, p: as for vtmu_decode_step
  *     (the caches are DEVICE memory, updated in place).
  *   q_host [T, heads*headDim], k_new_host / v_new_host [new_rows, kvHeads*
