@@ -36,7 +36,8 @@ EXPORTED = ("vtmu_attention_params_init", "vtmu_attention_workspace_size", "vtmu
             "vtmu_cache_write", "vtmu_features", "vtmu_last_error", "vtmu_attention_decode_noalloc",
             "vtmu_device_error", "vtmu_decode_step", "vtmu_decode_step_host_workspace_size",
             "vtmu_decode_step_host", "vtmu_rope_params_init", "vtmu_rope", "vtmu_decode_step_rope",
-            "vtmu_mla_params_init", "vtmu_mla_workspace_size", "vtmu_mla_attention", "vtmu_mla_decode_step")
+            "vtmu_mla_params_init", "vtmu_mla_workspace_size", "vtmu_mla_attention", "vtmu_mla_decode_step",
+            "vtmu_mla_decode_step_host_workspace_size", "vtmu_mla_decode_step_host")
 NOALLOC_SCRATCH_BYTES = 8 << 20  # VTMU_NOALLOC_SCRATCH_BYTES
 
 
@@ -168,6 +169,11 @@ def load_library():
         lib.vtmu_mla_decode_step.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int64, vp, vp, vp, vp,
                                              M, vp, ctypes.c_size_t, vp]
         lib.vtmu_mla_decode_step.restype = ctypes.c_int
+        lib.vtmu_mla_decode_step_host_workspace_size.argtypes = [M, ctypes.c_int64, ctypes.POINTER(ctypes.c_size_t)]
+        lib.vtmu_mla_decode_step_host_workspace_size.restype = ctypes.c_int
+        lib.vtmu_mla_decode_step_host.argtypes = [vp, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int64, vp, vp,
+                                                  vp, vp, M, vp, ctypes.c_size_t, vp]
+        lib.vtmu_mla_decode_step_host.restype = ctypes.c_int
         _lib = lib
         return lib
 
@@ -304,6 +310,23 @@ def vtmu_mla_decode_step(state, max_rows: int, state_new, new_rows: int, offset:
                                                int(offset), _addr(q), _addr(k_b), _addr(v_b), _addr(out),
                                                ctypes.byref(p), _addr(workspace), int(workspace_bytes),
                                                stream or None))
+
+
+def vtmu_mla_decode_step_host_workspace_size(p: vtmu_mla_params, new_rows: int) -> int:
+    n = ctypes.c_size_t(0)
+    _check(load_library().vtmu_mla_decode_step_host_workspace_size(ctypes.byref(p), int(new_rows), ctypes.byref(n)))
+    return int(n.value)
+
+
+def vtmu_mla_decode_step_host(state, max_rows: int, state_new_host, new_rows: int, offset: int, q_host, k_b, v_b,
+                              out_host, p: vtmu_mla_params, workspace, workspace_bytes: int, stream: int = 0) -> None:
+    """vtmu_mla_decode_step with q / new latent rows / out in host memory
+    (numpy arrays or CPU tensors, f32, contiguous; pinned buffers are used in
+    place).  Returns once out_host holds the result."""
+    _check(load_library().vtmu_mla_decode_step_host(_addr(state), int(max_rows), _haddr(state_new_host),
+                                                    int(new_rows), int(offset), _haddr(q_host), _addr(k_b),
+                                                    _addr(v_b), _haddr(out_host), ctypes.byref(p), _addr(workspace),
+                                                    int(workspace_bytes), stream or None))
 
 
 def vtmu_device_error() -> int:

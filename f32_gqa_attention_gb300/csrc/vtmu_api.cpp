@@ -876,6 +876,109 @@ vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const float* st
     return run_mla(m, q, state, k_b, v_b, out, workspace, workspace_bytes, cw, stream);
 }
 
+// Staging areas of vtmu_mla_decode_step_host after the latent attention's
+// own workspace: q, the new cache rows, the output.
+struct MlaHostStaging {
+    size_t q, q_b, sn, sn_b, out, out_b, total;
+};
+static MlaHostStaging mla_host_staging(const vtmu::MlaDesc& m, int64_t new_rows) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    MlaHostStaging h;
+    h.q_b = (size_t)m.T * m.H * (m.N + vtmu::kMlaRope) * 4;
+    h.sn_b = (size_t)new_rows * (vtmu::kMlaKvRank + vtmu::kMlaRope) * 4;
+    h.out_b = (size_t)m.T * m.H * m.Dv * 4;
+    h.q = up(mla_workspace(m));
+    h.sn = h.q + up(h.q_b);
+    h.out = h.sn + up(h.sn_b);
+    h.total = h.out + up(h.out_b);
+    return h;
+}
+
+vtmu_status vtmu_mla_decode_step_host_workspace_size(const vtmu_mla_params* p, int64_t new_rows, size_t* bytes) {
+    if (!bytes) return fail(VTMU_ERR_INVALID, "bytes is NULL");
+    if (new_rows < 0) return fail(VTMU_ERR_INVALID, "mla_decode_step_host: negative new_rows %lld", (long long)new_rows);
+    vtmu::MlaDesc m;
+    vtmu_status st = resolve_mla(p, &m);
+    if (st != VTMU_OK) return st;
+    *bytes = mla_host_staging(m, new_rows).total;
+    return ok();
+}
+
+vtmu_status vtmu_mla_decode_step_host(float* state, int64_t max_rows, const float* state_new_host, int64_t new_rows,
+                                      int64_t offset, const float* q_host, const float* k_b, const float* v_b,
+                                      float* out_host, const vtmu_mla_params* p, void* workspace,
+                                      size_t workspace_bytes, cudaStream_t stream) {
+    vtmu::MlaDesc m;
+    vtmu_status st = resolve_mla(p, &m);
+    if (st != VTMU_OK) return st;
+    if (new_rows < 0) return fail(VTMU_ERR_INVALID, "mla_decode_step_host: negative new_rows %lld", (long long)new_rows);
+    const MlaHostStaging h = mla_host_staging(m, new_rows);
+    if (!workspace || workspace_bytes < h.total)
+        return fail(VTMU_ERR_WORKSPACE, "mla_decode_step_host: workspace of %zu bytes, %zu needed",
+                    workspace ? workspace_bytes : (size_t)0, h.total);
+    if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: workspace must be 256-byte aligned");
+    if ((h.q_b && !q_host) || (h.out_b && !out_host) || (h.sn_b && !state_new_host))
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: a host buffer is NULL");
+    // The checks of vtmu_mla_decode_step on the device buffers, before any copy.
+    if (max_rows < 0) return fail(VTMU_ERR_INVALID, "mla_decode_step_host: negative max_rows %lld", (long long)max_rows);
+    if (offset < 0 || offset > max_rows || new_rows > max_rows - offset)
+        return fail(VTMU_ERR_RANGE, "mla_decode_step_host: offset %lld + rows %lld exceeds maxRows %lld",
+                    (long long)offset, (long long)new_rows, (long long)max_rows);
+    if (m.S > max_rows)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: S %lld exceeds the cache's %lld rows", (long long)m.S,
+                    (long long)max_rows);
+    if ((new_rows > 0 || (m.T > 0 && m.S > 0)) && !state)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: state is NULL");
+    if (m.T > 0 && ((m.N > 0 && !k_b) || !v_b))
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: k_b or v_b is NULL");
+    if ((reinterpret_cast<uintptr_t>(state) | reinterpret_cast<uintptr_t>(k_b) | reinterpret_cast<uintptr_t>(v_b)) & 15u)
+        return fail(VTMU_ERR_INVALID, "mla_decode_step_host: state, k_b and v_b must be 16-byte aligned");
+    char* w = static_cast<char*>(workspace);
+    const size_t ws_attn = h.q;  // the latent attention's own part of the workspace
+    // Page-locked, device-addressable buffers are used in place, as in
+    // vtmu_decode_step_host: the absorb launch reads q and the new rows and
+    // the projection writes the output row with plain loads and stores.
+    auto mapped = [](const void* hp) -> void* {
+        if (!hp) return nullptr;
+        cudaPointerAttributes at;
+        if (cudaPointerGetAttributes(&at, hp) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return nullptr;
+        }
+        return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+    };
+    if (h.q_b && h.out_b) {
+        void* q_d = mapped(q_host);
+        void* out_d = mapped(out_host);
+        void* sn_d = h.sn_b ? mapped(state_new_host) : nullptr;
+        if (q_d && out_d && (!h.sn_b || (sn_d && (reinterpret_cast<uintptr_t>(sn_d) & 15u) == 0))) {
+            st = vtmu_mla_decode_step(state, max_rows, static_cast<const float*>(sn_d), new_rows, offset,
+                                      static_cast<const float*>(q_d), k_b, v_b, static_cast<float*>(out_d), p,
+                                      workspace, ws_attn, stream);
+            if (st != VTMU_OK) return st;
+            const cudaError_t e = cudaStreamSynchronize(stream);
+            if (e != cudaSuccess) return cuda_fail(e, "mla_decode_step_host: stream synchronisation");
+            return ok();
+        }
+    }
+    cudaError_t e = cudaSuccess;
+    if (h.q_b) e = cudaMemcpyAsync(w + h.q, q_host, h.q_b, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && h.sn_b) e = cudaMemcpyAsync(w + h.sn, state_new_host, h.sn_b, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode_step_host: host to device copy");
+    st = vtmu_mla_decode_step(state, max_rows, h.sn_b ? reinterpret_cast<const float*>(w + h.sn) : nullptr,
+                              new_rows, offset, h.q_b ? reinterpret_cast<const float*>(w + h.q) : nullptr, k_b, v_b,
+                              h.out_b ? reinterpret_cast<float*>(w + h.out) : nullptr, p, workspace, ws_attn, stream);
+    if (st != VTMU_OK) return st;
+    if (h.out_b) {
+        e = cudaMemcpyAsync(out_host, w + h.out, h.out_b, cudaMemcpyDeviceToHost, stream);
+        if (e != cudaSuccess) return cuda_fail(e, "mla_decode_step_host: device to host copy");
+    }
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return cuda_fail(e, "mla_decode_step_host: stream synchronisation");
+    return ok();
+}
+
 const char* vtmu_features(void) {
     return "attention.alibi attention.bias attention.scale attention.softcap attention.window rope.interleaved "
            "rope.rotaryDim";

@@ -448,6 +448,36 @@ VTMU_API vtmu_status vtmu_mla_decode_step(float* state, int64_t max_rows, const 
                                           size_t workspace_bytes, cudaStream_t stream);
 
 /*
+ * Workspace bytes of vtmu_mla_decode_step_host for these params and new_rows:
+ * the latent attention's workspace followed by staging areas for q, the new
+ * cache rows and the output.  Errors: those of the parameter checks,
+ * VTMU_ERR_INVALID (new_rows < 0, bytes NULL).
+ */
+VTMU_API vtmu_status vtmu_mla_decode_step_host_workspace_size(const vtmu_mla_params* p, int64_t new_rows,
+                                                              size_t* bytes);
+
+/*
+ * vtmu_mla_decode_step with q, the new latent rows and the output in HOST
+ * memory (as vtmu_decode_step_host is to vtmu_decode_step): q_host [T,
+ * heads*(qk_nope + qk_rope)], state_new_host [new_rows, kv_rank + qk_rope],
+ * out_host [T, heads*v_head_dim], row-major f32; state, k_b, v_b: DEVICE as
+ * for vtmu_mla_decode_step.  Page-locked buffers the device can address
+ * (state_new_host also 16-byte aligned) are read and written in place by the
+ * launches (the absorb launch reads q and copies the new rows, the projection
+ * writes the output row); other buffers are copied through the staging areas
+ * of `workspace` (DEVICE, at least vtmu_mla_decode_step_host_workspace_size
+ * bytes, 256-byte aligned).  The call WAITS for `stream` and returns when
+ * out_host holds the result.  Every check runs before any copy.  Errors:
+ * those of vtmu_mla_decode_step, VTMU_ERR_WORKSPACE, VTMU_ERR_INVALID (a host
+ * buffer NULL where data is needed), VTMU_ERR_CUDA (a copy or the wait).
+ */
+VTMU_API vtmu_status vtmu_mla_decode_step_host(float* state, int64_t max_rows, const float* state_new_host,
+                                               int64_t new_rows, int64_t offset, const float* q_host,
+                                               const float* k_b, const float* v_b, float* out_host,
+                                               const vtmu_mla_params* p, void* workspace,
+                                               size_t workspace_bytes, cudaStream_t stream);
+
+/*
  * Kernel-side failures.  Every wait inside a kernel (TMA stage arrival,
  * stage release) gives up after one second instead of hanging the GPU; the
  * kernel then sets a bit in a device flag, abandons its output and returns.

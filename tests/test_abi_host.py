@@ -415,3 +415,38 @@ def test_mla_pointer_checks(lib):
     e = _err(lambda: vtmu.vtmu_mla_decode_step(FAKE * 3, 128, FAKE * 13, 1, 128, FAKE, FAKE * 5, FAKE * 7,
                                                FAKE * 9, p, FAKE * 11, n, 0))
     assert e.status == vtmu.VTMU_ERR_RANGE
+
+
+def test_host_mla_decode_step_workspace_adds_the_staging_areas(lib):
+    """vtmu_mla_decode_step_host's workspace: the latent attention's
+    workspace, then q, the new latent rows and out, each on a 256-byte
+    boundary."""
+    p = vtmu.make_mla_params(2, 4096, heads=16, qk_nope=128, v_head_dim=128, posOffset=4094)
+    base = vtmu.vtmu_mla_workspace_size(p)
+    up = lambda n: (n + 255) // 256 * 256
+    want = up(base) + up(2 * 16 * (128 + 64) * 4) + up(3 * 576 * 4) + up(2 * 16 * 128 * 4)
+    assert vtmu.vtmu_mla_decode_step_host_workspace_size(p, 3) == want
+    assert _err(lambda: vtmu.vtmu_mla_decode_step_host_workspace_size(p, -1)).status == vtmu.VTMU_ERR_INVALID
+
+
+@host_only
+def test_host_mla_decode_step_checks_before_any_copy(lib):
+    import numpy as np
+
+    p = vtmu.make_mla_params(1, 4096, heads=16, qk_nope=128, v_head_dim=128, posOffset=4095)
+    need = vtmu.vtmu_mla_decode_step_host_workspace_size(p, 1)
+    q = np.zeros((1, 16 * 192), np.float32)
+    sn = np.zeros((1, 576), np.float32)
+    out = np.zeros((1, 16 * 128), np.float32)
+    call = lambda **o: _err(lambda: vtmu.vtmu_mla_decode_step_host(
+        o.get("state", FAKE * 3), o.get("rows", 4096), o.get("sn", sn), 1, o.get("off", 4095), o.get("q", q),
+        o.get("kb", FAKE * 5), FAKE * 7, out, p, o.get("ws", FAKE * 9), o.get("wsb", need), 0))
+    assert call(wsb=need - 1).status == vtmu.VTMU_ERR_WORKSPACE
+    assert "256-byte" in str(call(ws=FAKE * 9 + 16))
+    assert call(q=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(sn=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(off=4096).status == vtmu.VTMU_ERR_RANGE
+    assert call(rows=4000, off=3000).status == vtmu.VTMU_ERR_INVALID  # S > max_rows
+    assert call(state=None).status == vtmu.VTMU_ERR_INVALID
+    assert call(kb=None).status == vtmu.VTMU_ERR_INVALID
+    assert "16-byte" in str(call(state=FAKE * 3 + 4))

@@ -132,3 +132,37 @@ def test_mla_refuses_widths_it_does_not_serve():
     with pytest.raises(vtmu.VtmuError) as e:
         vtmu.vtmu_mla_workspace_size(p)
     assert e.value.status == vtmu.VTMU_ERR_UNSUPPORTED and "kv_rank" in str(e.value)
+
+
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+@pytest.mark.parametrize("T,kernel", [(1, vtmu.MLA_KERNEL_AUTO), (2, vtmu.MLA_KERNEL_TENSOR_CORES)])
+def test_mla_decode_step_host_buffers(pinned, T, kernel):
+    """vtmu_mla_decode_step_host: q, the new latent row and the output in host
+    memory (pinned buffers are used in place, pageable ones staged).  The
+    output is bit-identical to the device-buffer step on the same data, the
+    cache row bit-exact."""
+    S0, H, N, Dv = 1500, 16, 128, 128
+    x = si.mla_inputs(S0 + 1, T, H, R, N, P, Dv, 40 + T, new_rows=1)
+    off = S0
+    p = vtmu.make_mla_params(T, S0 + 1, heads=H, qk_nope=N, v_head_dim=Dv, posOffset=S0 + 1 - T, kernel=kernel)
+    host = (lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) if pinned else np.ascontiguousarray
+    state = _dev(x["state"])
+    out_h = host(np.zeros((T, H * Dv), np.float32))
+    nb = vtmu.vtmu_mla_decode_step_host_workspace_size(p, 1)
+    ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
+    vtmu.vtmu_mla_decode_step_host(state, S0 + 1, host(x["state_new"][:1]), 1, off, host(x["q"]), _dev(x["k_b"]),
+                                   _dev(x["v_b"]), out_h, p, ws, nb, torch.cuda.current_stream().cuda_stream)
+    got = np.asarray(out_h).copy()
+    state2 = _dev(x["state"])
+    ref_dev = vtmu.mla_decode_step(state2, _dev(x["state_new"][:1]), off, _dev(x["q"]), _dev(x["k_b"]),
+                                   _dev(x["v_b"]), heads=H, qk_nope=N, v_head_dim=Dv, posOffset=S0 + 1 - T,
+                                   kernel=kernel)
+    torch.cuda.synchronize()
+    assert got.tobytes() == ref_dev.cpu().numpy().tobytes(), "host-buffer step differs from the device step"
+    st = state.cpu().numpy()
+    assert np.array_equal(st[off:off + 1], x["state_new"][:1]) and np.array_equal(st[:off], x["state"][:off])
+    oracle.cache_write(x["state"], x["state_new"][:1], off)
+    ref = oracle.mla_attention(x["q"], x["state"], x["k_b"], x["v_b"], heads=H, kv_rank=R, qk_nope=N, qk_rope=P,
+                               v_head_dim=Dv, posOffset=S0 + 1 - T)
+    _check(got, ref, "host buffers")
+    assert vtmu.vtmu_device_error() == 0
