@@ -284,6 +284,18 @@ struct HostStaging {
     size_t q_b, k_new_b, v_new_b, bias_b, out_b;
 };
 
+// The device's address of a page-locked host buffer (cudaHostAlloc,
+// cudaMallocHost, cudaHostRegister), or nullptr for any other pointer.
+void* device_view_of_host(const void* hp) {
+    if (!hp) return nullptr;
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, hp) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
 HostStaging host_staging(const Resolved& r, int64_t new_rows) {
     const vtmu::AttnDesc& a = r.a;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
@@ -697,29 +709,20 @@ vtmu_status vtmu_decode_step_host(float* k_cache, float* v_cache, int64_t max_ro
         return fail(VTMU_ERR_INVALID, "decode_step_host: S %lld exceeds the cache's %lld rows", (long long)a.S,
                     (long long)max_rows);
     char* w = static_cast<char*>(workspace);
-    // Page-locked buffers the device addresses directly (its pointer for
-    // them), or nullptr.  On a decode kernel, which reads q and the new rows
-    // with plain loads and writes the output row with plain stores, such
-    // buffers are used in place: the kernel pulls q and the new rows over
-    // the host link and pushes the output row back, with no staging copies.
+    // On a decode kernel, which reads q and the new rows with plain loads
+    // and writes the output row with plain stores, page-locked buffers the
+    // device can address are used in place: the kernel pulls q and the new
+    // rows over the host link and pushes the output row back, with no
+    // staging copies.
     // Only when all of them qualify and they and the caches are 16-byte
     // aligned (so that the decode kernel runs and none of its fallbacks) and
     // no bias is given; otherwise every buffer goes through the workspace.
-    auto mapped = [](const void* hp) -> void* {
-        if (!hp) return nullptr;
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, hp) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
-    };
     const bool decode_kernel = r.kernel == VTMU_KERNEL_DECODE || r.kernel == VTMU_KERNEL_DECODE_TF32X3;
     if (decode_kernel && !bias_host && h.q_b && h.out_b) {
-        void* q_d = mapped(q_host);
-        void* out_d = mapped(out_host);
-        void* kn_d = h.k_new_b ? mapped(k_new_host) : nullptr;
-        void* vn_d = h.v_new_b ? mapped(v_new_host) : nullptr;
+        void* q_d = device_view_of_host(q_host);
+        void* out_d = device_view_of_host(out_host);
+        void* kn_d = h.k_new_b ? device_view_of_host(k_new_host) : nullptr;
+        void* vn_d = h.v_new_b ? device_view_of_host(v_new_host) : nullptr;
         const uintptr_t m16 = reinterpret_cast<uintptr_t>(q_d) | reinterpret_cast<uintptr_t>(out_d) |
                               reinterpret_cast<uintptr_t>(kn_d) | reinterpret_cast<uintptr_t>(vn_d) |
                               reinterpret_cast<uintptr_t>(k_cache) | reinterpret_cast<uintptr_t>(v_cache);
@@ -939,19 +942,10 @@ vtmu_status vtmu_mla_decode_step_host(float* state, int64_t max_rows, const floa
     // Page-locked, device-addressable buffers are used in place, as in
     // vtmu_decode_step_host: the absorb launch reads q and the new rows and
     // the projection writes the output row with plain loads and stores.
-    auto mapped = [](const void* hp) -> void* {
-        if (!hp) return nullptr;
-        cudaPointerAttributes at;
-        if (cudaPointerGetAttributes(&at, hp) != cudaSuccess) {
-            (void)cudaGetLastError();
-            return nullptr;
-        }
-        return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
-    };
     if (h.q_b && h.out_b) {
-        void* q_d = mapped(q_host);
-        void* out_d = mapped(out_host);
-        void* sn_d = h.sn_b ? mapped(state_new_host) : nullptr;
+        void* q_d = device_view_of_host(q_host);
+        void* out_d = device_view_of_host(out_host);
+        void* sn_d = h.sn_b ? device_view_of_host(state_new_host) : nullptr;
         if (q_d && out_d && (!h.sn_b || (sn_d && (reinterpret_cast<uintptr_t>(sn_d) & 15u) == 0))) {
             st = vtmu_mla_decode_step(state, max_rows, static_cast<const float*>(sn_d), new_rows, offset,
                                       static_cast<const float*>(q_d), k_b, v_b, static_cast<float*>(out_d), p,

@@ -29,11 +29,11 @@
  * Conventions shared by every entry point
  *  - Tensor pointers are DEVICE pointers (cudaMalloc / PyTorch allocations)
  *    owned by the caller; the library never allocates or frees, and never
- *    synchronises except in vtmu_decode_step_host (host buffers), which
- *    waits for its stream.  Work is enqueued on `stream` and the call
- *    returns at once.  Results are visible once the stream reaches that
- *    point.
- *  - Host pointers are marked HOST and are read during the call only.
+ *    synchronises except in vtmu_decode_step_host and
+ *    vtmu_mla_decode_step_host (host buffers), which wait for their stream.
+ *    Work is enqueued on `stream` and the call returns at once.  Results are
+ *    visible once the stream reaches that point.
+ *  - Host pointers are marked HOST and are used during the call only.
  *  - Every check runs on the host before any launch.  A failed check
  *    launches nothing and returns a status; vtmu_last_error() then names the
  *    offending parameter or feature (the catalog, likewise, names the missing
