@@ -942,11 +942,15 @@ vtmu_status vtmu_mla_decode_step_host(float* state, int64_t max_rows, const floa
     // Page-locked, device-addressable buffers are used in place, as in
     // vtmu_decode_step_host: the absorb launch reads q and the new rows and
     // the projection writes the output row with plain loads and stores.
+    // Buffers the launches could not take as they are (q or out not 4-byte
+    // aligned, new rows not 16-byte aligned) go through the workspace.
     if (h.q_b && h.out_b) {
         void* q_d = device_view_of_host(q_host);
         void* out_d = device_view_of_host(out_host);
         void* sn_d = h.sn_b ? device_view_of_host(state_new_host) : nullptr;
-        if (q_d && out_d && (!h.sn_b || (sn_d && (reinterpret_cast<uintptr_t>(sn_d) & 15u) == 0))) {
+        const bool aligned = ((reinterpret_cast<uintptr_t>(q_d) | reinterpret_cast<uintptr_t>(out_d)) & 3u) == 0 &&
+                             (reinterpret_cast<uintptr_t>(sn_d) & 15u) == 0;
+        if (q_d && out_d && (!h.sn_b || sn_d) && aligned) {
             st = vtmu_mla_decode_step(state, max_rows, static_cast<const float*>(sn_d), new_rows, offset,
                                       static_cast<const float*>(q_d), k_b, v_b, static_cast<float*>(out_d), p,
                                       workspace, ws_attn, stream);

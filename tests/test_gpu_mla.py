@@ -134,18 +134,27 @@ def test_mla_refuses_widths_it_does_not_serve():
     assert e.value.status == vtmu.VTMU_ERR_UNSUPPORTED and "kv_rank" in str(e.value)
 
 
-@pytest.mark.parametrize("pinned", [True, False], ids=["pinned", "pageable"])
+def _pinned_shifted(a):
+    """A pinned copy of `a` that starts 4 bytes past a 16-byte boundary."""
+    buf = torch.empty(a.size + 1, dtype=torch.float32).pin_memory()
+    view = buf[1:].view(a.shape)
+    view.copy_(torch.from_numpy(np.ascontiguousarray(a)))
+    return view
+
+
+@pytest.mark.parametrize("pinned", ["pinned", "pageable", "pinned_shifted"])
 @pytest.mark.parametrize("T,kernel", [(1, vtmu.MLA_KERNEL_AUTO), (2, vtmu.MLA_KERNEL_TENSOR_CORES)])
 def test_mla_decode_step_host_buffers(pinned, T, kernel):
     """vtmu_mla_decode_step_host: q, the new latent row and the output in host
-    memory (pinned buffers are used in place, pageable ones staged).  The
-    output is bit-identical to the device-buffer step on the same data, the
-    cache row bit-exact."""
+    memory (pinned buffers are used in place, pageable ones and pinned ones
+    off the 16-byte grid staged).  The output is bit-identical to the
+    device-buffer step on the same data, the cache row bit-exact."""
     S0, H, N, Dv = 1500, 16, 128, 128
     x = si.mla_inputs(S0 + 1, T, H, R, N, P, Dv, 40 + T, new_rows=1)
     off = S0
     p = vtmu.make_mla_params(T, S0 + 1, heads=H, qk_nope=N, v_head_dim=Dv, posOffset=S0 + 1 - T, kernel=kernel)
-    host = (lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()) if pinned else np.ascontiguousarray
+    host = {"pinned": lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory(),
+            "pageable": np.ascontiguousarray, "pinned_shifted": _pinned_shifted}[pinned]
     state = _dev(x["state"])
     out_h = host(np.zeros((T, H * Dv), np.float32))
     nb = vtmu.vtmu_mla_decode_step_host_workspace_size(p, 1)

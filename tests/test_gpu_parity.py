@@ -439,6 +439,7 @@ def test_decode_step_unfused_paths():
     dict(S=700, H=4, Hk=2, D=128, T=6, new_rows=6, offset=600, pinned=True),       # tensor-core decode (12 virtual heads)
     dict(S=32768, H=32, Hk=8, D=128, T=4, new_rows=4, offset=32764, pinned=True),  # the 4-row speculative workload
     dict(S=900, H=16, Hk=2, D=64, T=3, new_rows=3, offset=800, pinned=False),     # CUDA-core decode, 24 virtual heads
+    dict(S=3000, H=32, Hk=8, D=128, T=1, new_rows=1, offset=2999, pinned="shifted"),  # pinned, off the 16-byte grid
 ])
 def test_decode_step_host_buffers(case):
     """vtmu_decode_step_host: the step's inputs and output in host memory
@@ -454,7 +455,13 @@ def test_decode_step_host_buffers(case):
     pos = off + n - T
     p = vtmu.make_params(T, S, heads=H, headDim=D, kvHeads=Hk, posOffset=pos,
                          bias_kind=vtmu.VTMU_BIAS_TS if bias is not None else vtmu.VTMU_BIAS_NONE)
-    host = lambda a: torch.from_numpy(a).pin_memory() if case["pinned"] else a
+    def host(a):
+        if case["pinned"] == "shifted":  # staged: the kernels take 16-byte aligned rows only
+            buf = torch.empty(a.size + 1, dtype=torch.float32).pin_memory()
+            view = buf[1:].view(a.shape)
+            view.copy_(torch.from_numpy(a))
+            return view
+        return torch.from_numpy(a).pin_memory() if case["pinned"] else a
     nb = vtmu.vtmu_decode_step_host_workspace_size(p, n)
     ws = torch.zeros(nb, dtype=torch.uint8, device="cuda")
     Kc, Vc = to_dev(x["kc"]), to_dev(x["vc"])
