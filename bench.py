@@ -521,7 +521,8 @@ def measure_prefill(ctx, name, steps, warmup, kernel_arg="auto", cpu_budget=0.0,
     e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
     h2d = (qh.numel() + kh.numel() + vh.numel() + (bh.numel() if bh is not None else 0)) * 4
     e2e = {"value": round(flops / 1e12 * ctx.world / e2e_s, 3), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": outh.numel() * 4, "steps": n_e2e}
+           "d2h_bytes_per_step": outh.numel() * 4, "steps": n_e2e,
+           "transfer": "cudaMemcpyAsync from pinned buffers in, attention, copy out, host sync"}
     del q, k, v, b, out, flush, ws, qh, kh, vh, bh, outh
     torch.cuda.empty_cache()
 
@@ -693,7 +694,10 @@ def measure_decode(ctx, name):
         e2e_step(i)
     e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
     e2e = {"value": round(step_bytes / 1e9 * ctx.world / e2e_s, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "steps": n_e2e}
+           "d2h_bytes_per_step": d2h, "steps": n_e2e,
+           "transfer": ("cudaMemcpyAsync from pinned buffers around the fused step, host sync" if rope is not None else
+                        "vtmu_decode_step_host on pinned buffers: the kernel reads q and the new rows and writes "
+                        "the output row over the host link, then the call waits")}
     del sessions, q, kn, vn, out, ws
     torch.cuda.empty_cache()
     kernel_tag = ("prefill_ffma" if args.kernel == "ffma" else
@@ -759,7 +763,9 @@ def measure_mla(ctx, name):
     e2e_s = max_over_ranks((time.perf_counter() - t0) / n_e2e, ctx.world)
     e2e = {"value": round(nbytes / 1e9 * ctx.world / e2e_s, 3), "unit": "GB/s",
            "h2d_bytes_per_step": (qh.numel() + snh.numel()) * 4, "d2h_bytes_per_step": outh.numel() * 4,
-           "steps": n_e2e}
+           "steps": n_e2e,
+           "transfer": "vtmu_mla_decode_step_host on pinned buffers: the absorb launch reads q and the new row, "
+                       "the projection writes the output row over the host link, then the call waits"}
     del hws
     del states, q, k_b, v_b, sn, out, ws
     torch.cuda.empty_cache()
