@@ -696,6 +696,8 @@ def measure_decode(ctx, name):
     e2e = {"value": round(step_bytes / 1e9 * ctx.world / e2e_s, 3), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "steps": n_e2e,
            "transfer": ("cudaMemcpyAsync from pinned buffers around the fused step, host sync" if rope is not None else
+                        "vtmu_decode_step_host on pinned buffers, staged through the workspace (the prefill "
+                        "kernels take device buffers), then the call waits" if args.kernel == "ffma" else
                         "vtmu_decode_step_host on pinned buffers: the kernel reads q and the new rows and writes "
                         "the output row over the host link, then the call waits")}
     del sessions, q, kn, vn, out, ws
